@@ -1,0 +1,210 @@
+"""fp64 CPU oracle for paged-KV GQA verify attention -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+and reference arm may import this package.  The product path (the package
+``speculative_decoding_verify_gqa_gb300``) never imports it, and this package
+never imports the product: the two share nothing but the seeded input
+generators in ``synthetic``.
+
+The arithmetic lives in ``verify_attn_oracle.c`` (plain C, double precision,
+the definition written out: gather the pages, build the dense mask, softmax,
+LSE).  This module compiles it with gcc on first use and wraps it with ctypes.
+``brute.py`` holds an independent pure-Python scalar version for tiny inputs.
+
+Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
+what the source pages and the mathematics fix (triu mask == causal, chain tree
+== causal, GQA == MHA on expanded K/V, split + LSE merge == unsplit, L = 1 ==
+single-query decode, tree row == decode over its root path, closed forms,
+hand-worked golden cases, fp8/bf16 decode tables, brute force).  No function
+is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "verify_attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle (gcc, no fast-math: IEEE double semantics)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + ".tmp%d" % os.getpid()
+    subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-std=c11",
+                           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_decode_bf16.restype = dbl
+        lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
+        lib.oracle_decode_e4m3.restype = dbl
+        lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
+        lib.oracle_kv_len.restype = i64
+        lib.oracle_kv_len.argtypes = [P, P, i32, i32]
+        lib.oracle_dense_attention.restype = None
+        lib.oracle_dense_attention.argtypes = [i32, i32, i32, P, i64, P, P, i64, P, dbl, P, P, P]
+        lib.oracle_verify_attn.restype = i32
+        lib.oracle_verify_attn.argtypes = [P, P, P, i32, P, P, P, P, P, P, i32, i32, i32, i32,
+                                           i32, i32, dbl, dbl, dbl, P, i64, P, P, i32]
+        lib.oracle_attn_range.restype = i32
+        lib.oracle_attn_range.argtypes = [P, P, P, i32, P, P, P, P, P, P, i32, i32, i32, i32,
+                                          i32, i32, dbl, dbl, dbl, i32, i64, i32, i64, i64,
+                                          P, P]
+        lib.oracle_merge_partials.restype = None
+        lib.oracle_merge_partials.argtypes = [i32, i32, i32, P, P, P, P]
+        lib.oracle_paged_kv_append.restype = i32
+        lib.oracle_paged_kv_append.argtypes = [P, P, i32, P, P, P, P, i32, i32, i32, i32, i32,
+                                               P, P]
+        _lib = lib
+        return lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def decode_bf16(bits) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(bits, dtype=np.uint16).reshape(-1)
+    return np.array([lib.oracle_decode_bf16(int(x)) for x in flat]).reshape(np.shape(bits))
+
+
+def decode_e4m3(bits) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(bits, dtype=np.uint8).reshape(-1)
+    return np.array([lib.oracle_decode_e4m3(int(x)) for x in flat]).reshape(np.shape(bits))
+
+
+def dense_attention(Q, K, V, M, scale):
+    """softmax(scale * Q K^T + M) V and its natural-log LSE, row by row, in fp64.
+    Q [n, d], K/V [m, d], M [n, m] additive."""
+    lib = _load()
+    Q = _c(Q, np.float64); K = _c(K, np.float64); V = _c(V, np.float64); M = _c(M, np.float64)
+    n, d = Q.shape
+    m = K.shape[0]
+    out = np.zeros((n, d)); lse = np.zeros(n)
+    s = np.zeros(max(m, 1))
+    lib.oracle_dense_attention(n, m, d, _p(Q), d, _p(K), _p(V), d, _p(M), float(scale),
+                               _p(out), _p(lse), _p(s))
+    return out, lse
+
+
+def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_len, qo_indptr,
+                mask, mask_indptr, h_q, h_kv, d, page_size, num_pages, sm_scale, k_scale=1.0,
+                v_scale=1.0, rows=None, nthreads=None):
+    """Verify attention of a batch.  ``rows``: optional flat row ids
+    token * h_q + head; returns (out [n, d] fp64, lse [n] fp64)."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint8 if kv_fp8 else np.uint16)
+    vc = _c(v_cache, np.uint8 if kv_fp8 else np.uint16)
+    kv_indptr = _c(kv_indptr, np.int32); kv_indices = _c(kv_indices, np.int32)
+    last_page_len = _c(last_page_len, np.int32); qo_indptr = _c(qo_indptr, np.int32)
+    mask = _c(mask, np.uint8); mask_indptr = _c(mask_indptr, np.int32)
+    batch = len(qo_indptr) - 1
+    total_qo = int(qo_indptr[-1])
+    sel = _c(rows, np.int32)
+    n = total_qo * h_q if sel is None else len(sel)
+    out = np.zeros((max(n, 1), d)); lse = np.zeros(max(n, 1))
+    rc = lib.oracle_verify_attn(_p(q), _p(kc), _p(vc), int(bool(kv_fp8)), _p(kv_indptr),
+                                _p(kv_indices), _p(last_page_len), _p(qo_indptr), _p(mask),
+                                _p(mask_indptr), batch, h_q, h_kv, d, page_size, num_pages,
+                                float(sm_scale), float(k_scale), float(v_scale), _p(sel),
+                                int(n), _p(out), _p(lse),
+                                int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_verify_attn rejected its inputs (status %d)" % rc)
+    return out[:n], lse[:n]
+
+
+def attn_range(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_len, qo_indptr,
+               mask, mask_indptr, h_q, h_kv, d, page_size, num_pages, sm_scale, k_scale,
+               v_scale, b, t, qh, lo, hi):
+    """One row's attention restricted to key positions [lo, hi) of its request."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint8 if kv_fp8 else np.uint16)
+    vc = _c(v_cache, np.uint8 if kv_fp8 else np.uint16)
+    args = [_c(a, np.int32) for a in (kv_indptr, kv_indices, last_page_len, qo_indptr)]
+    mask = _c(mask, np.uint8); mask_indptr = _c(mask_indptr, np.int32)
+    out = np.zeros(d); lse = np.zeros(1)
+    rc = lib.oracle_attn_range(_p(q), _p(kc), _p(vc), int(bool(kv_fp8)), *[_p(a) for a in args],
+                               _p(mask), _p(mask_indptr), len(args[3]) - 1, h_q, h_kv, d,
+                               page_size, num_pages, float(sm_scale), float(k_scale),
+                               float(v_scale), b, t, qh, lo, hi, _p(out), _p(lse))
+    if rc != 0:
+        raise ValueError("oracle_attn_range rejected its inputs (status %d)" % rc)
+    return out, float(lse[0])
+
+
+def merge_partials(outs, lses):
+    """outs [S, n, d], lses [S, n] -> (out [n, d], lse [n])."""
+    lib = _load()
+    outs = _c(outs, np.float64); lses = _c(lses, np.float64)
+    S, n, d = outs.shape
+    out = np.zeros((n, d)); lse = np.zeros(n)
+    lib.oracle_merge_partials(S, n, d, _p(outs), _p(lses), _p(out), _p(lse))
+    return out, lse
+
+
+def paged_kv_append(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_page_len,
+                    page_size, num_pages, k_cache, v_cache):
+    """Host scatter (in place on k_cache / v_cache, numpy [pages, h_kv, P, d])."""
+    lib = _load()
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    k_new = np.ascontiguousarray(k_new); v_new = np.ascontiguousarray(v_new)
+    h_kv, d = k_cache.shape[1], k_cache.shape[3]
+    idx = [_c(a, np.int32) for a in (append_indptr, kv_indptr, kv_indices, last_page_len)]
+    rc = lib.oracle_paged_kv_append(_p(k_new), _p(v_new), k_cache.itemsize, *[_p(a) for a in idx],
+                                    len(idx[0]) - 1, h_kv, d, page_size, num_pages,
+                                    _p(k_cache), _p(v_cache))
+    if rc != 0:
+        raise ValueError("oracle_paged_kv_append rejected its inputs (status %d)" % rc)
+
+
+# ---- convenience over synthetic.Workload (inputs only; no arithmetic here) ----
+
+def build_cache(wl):
+    """The workload's page pool, written by the oracle's own host scatter:
+    sentinel-filled (NaN bytes), then every token of every request appended."""
+    import synthetic
+    kc = synthetic.sentinel_pool(wl)
+    vc = synthetic.sentinel_pool(wl)
+    paged_kv_append(wl.k_tok, wl.v_tok, wl.tok_append_indptr(), wl.kv_indptr, wl.kv_indices,
+                    wl.last_page_len, wl.page_size, wl.num_pages, kc, vc)
+    return kc, vc
+
+
+def verify_attn_workload(wl, rows=None, nthreads=None, caches=None):
+    kc, vc = caches if caches is not None else build_cache(wl)
+    return verify_attn(wl.q, kc, vc, wl.kv_dtype == "fp8_e4m3", wl.kv_indptr, wl.kv_indices,
+                       wl.last_page_len, wl.qo_indptr, wl.mask, wl.mask_indptr, wl.h_q, wl.h_kv,
+                       wl.d, wl.page_size, wl.num_pages, wl.sm_scale, wl.k_scale, wl.v_scale,
+                       rows=rows, nthreads=nthreads)

@@ -1,0 +1,74 @@
+"""Pure-Python scalar brute force of verify attention for tiny inputs --
+TEST INFRASTRUCTURE (a second, independent statement of the definition that
+pins the C oracle; it shares no code with it).
+
+For each request b, token t and query head qh it walks key positions j of the
+request one by one, finds each key through the page table (page
+``kv_indices[kv_indptr[b] + j // page_size]``, slot ``j % page_size``),
+decides visibility from the rule (prefix always visible; draft column u
+visible iff mask bit (t, u) is set, or u <= t without a mask), and evaluates
+``lse = log(sum exp(s_j))`` and ``out = sum exp(s_j - lse) v_j`` with
+``math.fsum``.  Decoding uses torch's own dtype casts (a library routine),
+not the oracle's decoder.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+
+def _decode(bits: np.ndarray, kv_fp8: bool) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(bits))
+    if kv_fp8:
+        return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return t.view(torch.int16).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_len, qo_indptr,
+                mask, mask_indptr, h_q, h_kv, d, page_size, sm_scale, k_scale=1.0, v_scale=1.0):
+    qd = _decode(q, False)
+    kd = _decode(k_cache, kv_fp8)
+    vd = _decode(v_cache, kv_fp8)
+    G = h_q // h_kv
+    total = int(qo_indptr[-1])
+    out = np.zeros((total * h_q, d))
+    lse = np.zeros(total * h_q)
+    for b in range(len(qo_indptr) - 1):
+        npg = int(kv_indptr[b + 1] - kv_indptr[b])
+        kv_len = 0 if npg == 0 else (npg - 1) * page_size + int(last_page_len[b])
+        L = int(qo_indptr[b + 1] - qo_indptr[b])
+        prefix = kv_len - L
+        for t in range(L):
+            tok = int(qo_indptr[b]) + t
+            for qh in range(h_q):
+                h = qh // G
+                logits, values = [], []
+                for j in range(kv_len):
+                    if j >= prefix:
+                        u = j - prefix
+                        if mask is None:
+                            vis = u <= t
+                        else:
+                            bit = int(mask_indptr[b]) + t * L + u
+                            vis = (int(mask[bit // 8]) >> (bit % 8)) & 1 == 1
+                        if not vis:
+                            continue
+                    page = int(kv_indices[int(kv_indptr[b]) + j // page_size])
+                    slot = j % page_size
+                    dot = math.fsum(float(qd[tok, qh, e]) * float(kd[page, h, slot, e]) * k_scale
+                                    for e in range(d))
+                    logits.append(sm_scale * dot)
+                    values.append([float(vd[page, h, slot, e]) * v_scale for e in range(d)])
+                row = tok * h_q + qh
+                if not logits:
+                    lse[row] = -math.inf
+                    continue
+                mx = max(logits)
+                l = mx + math.log(math.fsum(math.exp(s - mx) for s in logits))
+                lse[row] = l
+                w = [math.exp(s - l) for s in logits]
+                for e in range(d):
+                    out[row, e] = math.fsum(w[j] * values[j][e] for j in range(len(w)))
+    return out, lse
