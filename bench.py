@@ -1,0 +1,580 @@
+"""Benchmark of paged-KV GQA verify attention on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-configs] [--no-e2e]
+
+One step is one pass of the hot path over one batch: the paged append of
+the batch's draft K/V into the cache, then verify attention (split kernel +
+LSE merge).  The plan (host) is built once before the timed region and
+reused, as a serving step shares it across layers; the end-to-end number
+re-plans every step.  Inputs are synthetic (seeded, shaped like the
+workload) and resident in HBM when the timed region starts.  L2 (129 MB) is
+defeated by rotating over copies of the KV pool totalling >= 4x L2.
+
+Prints ONE JSON line.  The default workload is the Llama-3-8B-shaped tree
+verify (batch 1, 32 q / 8 kv heads, d 128, 4096-token prefix, 17-node tree).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+HEADLINE = "llama3_8b_tree_verify"
+METRIC = "verify-attn tokens/s and achieved HBM GB/s (% of GB300 peak) per config"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GRAPH_STEPS = 128
+
+
+# ---------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {k: float(pk[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(wl):
+    """Algorithmic bytes and FLOPs of one verify-attention call.
+    Bytes: K and V of every (request, KV head, kv token) read once, Q read
+    once, out and LSE written once, page-table, qo_indptr and mask bytes.
+    FLOPs: 4 * d per visible (query row, key) pair per query head."""
+    es = wl.kv_elem_bytes
+    kv = int(wl.kv_lens.sum()) * wl.h_kv * wl.d * es * 2
+    q = wl.total_qo * wl.h_q * wl.d * 2
+    out = q
+    lse = wl.total_qo * wl.h_q * 4
+    idx = 4 * (2 * (wl.batch + 1) + wl.batch + len(wl.kv_indices))
+    mask = 0
+    if wl.mask is not None:
+        mask = int(math.ceil(int(wl.mask_indptr[-1]) / 8)) + 4 * (wl.batch + 1)
+    visible = 0
+    for b in range(wl.batch):
+        L = int(wl.qo_lens[b])
+        pre = int(wl.prefix_lens[b])
+        if wl.mask_dense is not None:
+            draft = int(wl.mask_dense[b].sum())
+        else:
+            draft = L * (L + 1) // 2
+        visible += L * pre + draft
+    flops = 4 * wl.d * visible * wl.h_q
+    return dict(kv_bytes=kv, read_bytes=kv + q + idx + mask, total_bytes=kv + q + out + lse + idx + mask,
+                flops=flops, tokens=wl.total_qo)
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("k_partial_mma.cu", "va_device.cuh", "va_kernels.h"):
+        with open(os.path.join(ROOT, "speculative_decoding_verify_gqa_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the split kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic_per_launch.md")
+    sha = kernel_source_sha()
+    try:
+        for line in open(path):
+            parts = line.strip().strip("|").split("|")
+            parts = [p.strip() for p in parts]
+            if len(parts) >= 4 and parts[0] == workload and parts[2] == sha:
+                return float(parts[1])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            n += 1
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def make_event(torch):
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return torch.cuda.Event(enable_timing=True)
+
+
+# ---------------------------------------------------------------- our arm
+
+class Bench:
+    def __init__(self, name, device, seed=0):
+        import torch
+        import speculative_decoding_verify_gqa_gb300 as va
+        self.torch, self.va = torch, va
+        self.name = name
+        self.dev = device
+        wl = synthetic.make_workload(name, seed=seed)
+        self.wl = wl
+        fp8 = wl.kv_dtype == synthetic.FP8
+        self.kvd = torch.float8_e4m3fn if fp8 else torch.bfloat16
+        raw = np.uint8 if fp8 else np.int16
+
+        def dt(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+        def dkv(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(raw)).to(device).view(self.kvd)
+
+        self.q = dt(wl.q.view(np.int16)).view(torch.bfloat16)
+        kn, vn = wl.new_tokens()
+        self.k_new, self.v_new = dkv(kn), dkv(vn)
+        self.kv_indptr, self.kv_indices = dt(wl.kv_indptr), dt(wl.kv_indices)
+        self.last_page_len, self.qo_indptr = dt(wl.last_page_len), dt(wl.qo_indptr)
+        self.mask = None if wl.mask is None else dt(wl.mask)
+        self.mask_indptr = None if wl.mask_indptr is None else dt(wl.mask_indptr)
+        shape = (wl.num_pages, wl.h_kv, wl.page_size, wl.d)
+        k0 = torch.full(shape, 0xFF, dtype=torch.uint8, device=device).view(self.kvd)
+        v0 = torch.full(shape, 0xFF, dtype=torch.uint8, device=device).view(self.kvd)
+        if not fp8:
+            k0 = torch.full(shape, -1, dtype=torch.int16, device=device).view(self.kvd)
+            v0 = torch.full(shape, -1, dtype=torch.int16, device=device).view(self.kvd)
+        k_tok, v_tok = dkv(wl.k_tok), dkv(wl.v_tok)
+        va.paged_kv_append(k_tok, v_tok, dt(wl.tok_indptr.astype(np.int32)), self.kv_indptr,
+                           self.kv_indices, self.last_page_len, k0, v0)
+        del k_tok, v_tok
+        pool_bytes = 2 * k0.numel() * k0.element_size()
+        self.n_copies = int(min(64, max(2, math.ceil(4 * L2_BYTES / pool_bytes))))
+        self.pool_bytes = pool_bytes
+        self.pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(self.n_copies - 1)]
+        self.plan = va.verify_attn_plan(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
+                                        wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                        kv_dtype=wl.kv_dtype, device=device)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
+        self.launches_per_step = 1 + self.plan.launches()
+        torch.cuda.synchronize()
+
+    # one step on pool copy i; ev: optional 4 events around append / partial / merge
+    def step(self, i, ev=None):
+        va, wl = self.va, self.wl
+        kc, vc = self.pools[i % self.n_copies]
+        if ev:
+            ev[0].record()
+        va.paged_kv_append(self.k_new, self.v_new, self.qo_indptr, self.kv_indptr,
+                           self.kv_indices, self.last_page_len, kc, vc)
+        if ev:
+            ev[1].record()
+        va.verify_attn_partial(self.q, kc, vc, self.kv_indptr, self.kv_indices,
+                               self.last_page_len, self.qo_indptr, self.mask, self.mask_indptr,
+                               self.plan, sm_scale=wl.sm_scale, k_scale=wl.k_scale,
+                               v_scale=wl.v_scale, out=self.out, lse=self.lse)
+        if ev:
+            ev[2].record()
+        va.verify_attn_merge(self.qo_indptr, self.plan, self.out, self.lse)
+        if ev:
+            ev[3].record()
+
+    def capture(self, n, start=0, events=None):
+        torch = self.torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(2):
+                self.step(start + i)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                self.step(start + i, events[i] if events else None)
+        return g
+
+    def run_steps(self, k, graphs):
+        """Exactly k steps via graph replays (graphs: full GRAPH_STEPS graph,
+        remainder graph)."""
+        full, rem = graphs
+        for _ in range(k // GRAPH_STEPS):
+            full.replay()
+        if k % GRAPH_STEPS:
+            rem.replay()
+
+    def time_steps(self, k, warmup, sampler=None, barrier=None):
+        torch = self.torch
+        graphs = (self.capture(GRAPH_STEPS), self.capture(k % GRAPH_STEPS) if k % GRAPH_STEPS else None)
+        self.run_steps(warmup, (graphs[0], self.capture(warmup % GRAPH_STEPS)
+                                if warmup % GRAPH_STEPS else None))
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        if sampler:
+            sampler.start()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        self.run_steps(k, graphs)
+        e1.record()
+        torch.cuda.synchronize()
+        clocks = sampler.stop() if sampler else None
+        if barrier:
+            barrier()
+        return e0.elapsed_time(e1) / k, clocks
+
+    def kernel_times(self, n=64):
+        """Per-kernel average durations (ms) from CUDA events recorded around
+        each launch inside a captured graph of n steps."""
+        torch = self.torch
+        ev = [[make_event(torch) for _ in range(4)] for _ in range(n)]
+        g = self.capture(n, events=ev)
+        g.replay()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        app = [e[0].elapsed_time(e[1]) for e in ev]
+        part = [e[1].elapsed_time(e[2]) for e in ev]
+        mrg = [e[2].elapsed_time(e[3]) for e in ev]
+        return dict(append_ms=statistics.mean(app), partial_ms=statistics.mean(part),
+                    merge_ms=statistics.mean(mrg), partial_median_ms=statistics.median(part))
+
+    def e2e(self, steps):
+        """End to end through the public API: pinned host inputs copied in,
+        plan on the host, append, attention, out / LSE copied back, every step."""
+        torch, va, wl = self.torch, self.va, self.wl
+
+        def pin(t):
+            return t.cpu().pin_memory()
+
+        h = dict(q=pin(self.q), k_new=pin(self.k_new.view(torch.uint8)),
+                 v_new=pin(self.v_new.view(torch.uint8)), kv_indptr=pin(self.kv_indptr),
+                 kv_indices=pin(self.kv_indices), last_page_len=pin(self.last_page_len),
+                 qo_indptr=pin(self.qo_indptr))
+        if self.mask is not None:
+            h["mask"], h["mask_indptr"] = pin(self.mask), pin(self.mask_indptr)
+        d = {k: torch.empty_like(v, device=self.dev) for k, v in h.items()}
+        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        lse_h = torch.empty(self.lse.shape, dtype=self.lse.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in h.values())
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+        np_tables = {k: h[k].numpy() for k in ("kv_indptr", "qo_indptr", "last_page_len")}
+        np_mask_indptr = h["mask_indptr"].numpy() if "mask_indptr" in h else None
+        ws = self.plan.workspace
+
+        def one(i):
+            for k in h:
+                d[k].copy_(h[k], non_blocking=True)
+            plan = va.verify_attn_plan(np_tables["kv_indptr"], np_tables["qo_indptr"],
+                                       np_tables["last_page_len"], np_mask_indptr, wl.h_q,
+                                       wl.h_kv, wl.d, wl.page_size, kv_dtype=wl.kv_dtype,
+                                       workspace=ws, device=self.dev)
+            kc, vc = self.pools[i % self.n_copies]
+            va.paged_kv_append(d["k_new"].view(self.kvd), d["v_new"].view(self.kvd),
+                               d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                               d["last_page_len"], kc, vc)
+            va.verify_attn_run(d["q"], kc, vc, d["kv_indptr"], d["kv_indices"],
+                               d["last_page_len"], d["qo_indptr"], d.get("mask"),
+                               d.get("mask_indptr"), plan, sm_scale=wl.sm_scale,
+                               k_scale=wl.k_scale, v_scale=wl.v_scale, out=self.out, lse=self.lse)
+            out_h.copy_(self.out, non_blocking=True)
+            lse_h.copy_(self.lse, non_blocking=True)
+            torch.cuda.synchronize()
+
+        for i in range(5):
+            one(i)
+        t0 = time.perf_counter()
+        for i in range(steps):
+            one(i)
+        dt_s = (time.perf_counter() - t0) / steps
+        return dict(value=wl.total_qo / dt_s, unit="tokens/s", h2d_bytes_per_step=int(h2d),
+                    d2h_bytes_per_step=int(d2h), ms_per_step=dt_s * 1e3)
+
+    def plan_us(self, n=50):
+        va, wl = self.va, self.wl
+        t0 = time.perf_counter()
+        for _ in range(n):
+            va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, wl.mask_indptr,
+                                     wl.h_q, wl.h_kv, wl.d, wl.page_size, kv_dtype=wl.kv_dtype,
+                                     num_sms=self.plan.header()["num_sms"])
+        return (time.perf_counter() - t0) / n * 1e6
+
+
+def roofline_for(wl, kt, peaks, peak_kind):
+    alg = algorithmic(wl)
+    t = kt["partial_ms"] * 1e-3
+    hbm = alg["read_bytes"] / t / 1e9
+    tfl = alg["flops"] / t / 1e12
+    rows_per_kv_head = int((wl.group * wl.qo_lens).max())
+    tensor_bound = alg["flops"] / alg["read_bytes"] > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        rf = {"bound": "tensor", "achieved": round(tfl, 2), "peak": peaks["bf16_tflops"],
+              "unit": "TFLOP/s", "frac": round(tfl / peaks["bf16_tflops"], 4)}
+    else:
+        rf = {"bound": "hbm", "achieved": round(hbm, 1), "peak": peaks["hbm_gbs"],
+              "unit": "GB/s", "frac": round(hbm / peaks["hbm_gbs"], 4)}
+    rf.update({"kernel": "verify_partial_mma_kernel",
+               "peak_source": "MEASURED_PEAKS.json (of %s)" % peak_kind,
+               "algorithmic_bytes_per_launch": alg["read_bytes"],
+               "algorithmic_flops_per_launch": alg["flops"],
+               "kernel_ms": round(kt["partial_ms"], 5),
+               "hbm_gbs": round(hbm, 1), "tflops": round(tfl, 2),
+               "rows_per_kv_head_max": rows_per_kv_head})
+    return rf
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def reduce_max(x, world):
+    """Max over ranks of a float (the slowest rank's time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier_fn(world):
+    if world == 1:
+        return None
+    import torch.distributed as dist
+    return dist.barrier
+
+
+def cpu_baseline(wl, seconds=10.0, nthreads=None):
+    """The oracle as it stands, on the host cores, on the workload's full call
+    (every row), repeated for about `seconds`."""
+    import oracle
+    nthreads = nthreads or oracle.default_threads()
+    caches = oracle.build_cache(wl)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.verify_attn_workload(wl, caches=caches, nthreads=nthreads)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (n >= 1 and el * (n + 1) / n > 3 * seconds):
+            break
+    per = el / n
+    return {"value": wl.total_qo / per, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": "%d full calls of the workload (%d tokens x %d heads each), %.2f s per call"
+                      % (n, wl.total_qo, wl.h_q, per)}
+
+
+def workload_config(wl, bench=None):
+    cfg = {"workload": wl.name, "batch": wl.batch, "num_qo_heads": wl.h_q,
+           "num_kv_heads": wl.h_kv, "head_dim": wl.d, "page_size": wl.page_size,
+           "kv_dtype": wl.kv_dtype, "mask": wl.mask_kind,
+           "prefix_tokens": int(wl.prefix_lens.sum()), "draft_tokens": wl.total_qo,
+           "kv_tokens": int(wl.kv_lens.sum())}
+    if bench is not None:
+        cfg["l2"] = ("inputs rotate over %d KV-pool copies of %.1f MB (%.0f MB total vs 129 MB L2)"
+                     % (bench.n_copies, bench.pool_bytes / 1e6,
+                        bench.n_copies * bench.pool_bytes / 1e6))
+        cfg["timing"] = "CUDA-graph replays of %d-step graphs, CUDA events on the launch stream" % GRAPH_STEPS
+    return cfg
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = load_peaks()
+    bench = Bench(args.workload, dev, seed=0)
+    wl = bench.wl
+    sampler = ClockSampler(local)
+    ms, clocks = bench.time_steps(args.steps, args.warmup, sampler=sampler,
+                                  barrier=barrier_fn(world))
+    ms_max = reduce_max(ms, world)
+    kt = bench.kernel_times()
+    rf = roofline_for(wl, kt, peaks, peak_kind)
+    rf["traffic"] = profiled_traffic(wl.name)
+    alg = algorithmic(wl)
+    value = world * wl.total_qo / (ms_max * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 q/out, %s kv, fp32 accumulate" % wl.kv_dtype, "data": "synthetic",
+        "config": workload_config(wl, bench),
+        "gpu_launches": args.steps * bench.launches_per_step,
+        "roofline": rf, "clocks": clocks,
+        "us_per_call": round((kt["partial_ms"] + kt["merge_ms"]) * 1e3, 3),
+        "kernel_us": {k: round(v * 1e3, 3) for k, v in kt.items()},
+        "attention_hbm_gbs": round(alg["total_bytes"] / ((kt["partial_ms"] + kt["merge_ms"]) * 1e-3) / 1e9, 1),
+        "plan_host_us": round(bench.plan_us(), 2),
+    }
+    if not args.no_e2e:
+        line["e2e"] = bench.e2e(args.e2e_steps)
+        line["e2e"]["value"] = round(world * line["e2e"]["value"], 1)
+    del bench
+    torch.cuda.empty_cache()
+    if not args.no_configs and world == 1:
+        others = {}
+        for name in synthetic.WORKLOAD_ORDER:
+            if name == args.workload:
+                continue
+            b = Bench(name, dev, seed=0)
+            steps = 256 if name != "tiny_verify" else 1024
+            ms_o, _ = b.time_steps(steps, 16)
+            kto = b.kernel_times(32)
+            rfo = roofline_for(b.wl, kto, peaks, peak_kind)
+            rfo["traffic"] = profiled_traffic(name)
+            others[name] = {"tokens_per_s": round(b.wl.total_qo / (ms_o * 1e-3), 1),
+                            "ms_per_step": round(ms_o, 6),
+                            "us_per_call": round((kto["partial_ms"] + kto["merge_ms"]) * 1e3, 3),
+                            "kernel_us": {k: round(v * 1e3, 3) for k, v in kto.items()},
+                            "roofline": rfo, "config": workload_config(b.wl, b)}
+            del b
+            torch.cuda.empty_cache()
+        line["configs"] = others
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle (fp64 C on the host cores) as the reference implementation:
+    rank 0 alone; each step is one bounded sample (a seeded subset of the
+    workload's rows, or the whole call when it fits) of the same workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    wl = synthetic.make_workload(args.workload)
+    nthreads = oracle.default_threads()
+    caches = oracle.build_cache(wl)
+    total_rows = wl.total_qo * wl.h_q
+    t0 = time.perf_counter()
+    oracle.verify_attn_workload(wl, caches=caches, nthreads=nthreads)
+    t_full = time.perf_counter() - t0
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    frac = min(1.0, budget / max(t_full, 1e-9))
+    n_rows = max(wl.h_q, int(total_rows * frac))
+    rows = None if n_rows >= total_rows else synthetic.sample_rows(wl, n_rows)
+    if rows is not None:
+        n_rows = len(rows)
+    for _ in range(args.warmup):
+        oracle.verify_attn_workload(wl, rows=rows, caches=caches, nthreads=nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify_attn_workload(wl, rows=rows, caches=caches, nthreads=nthreads)
+    per = (time.perf_counter() - t0) / args.steps
+    tokens = n_rows / wl.h_q
+    value = tokens / per
+    sample = ("%s per step: %d of %d (token, head) rows (%.1f tokens' worth), fp64, %d threads"
+              % ("whole call" if rows is None else "seeded row sample", n_rows, total_rows,
+                 tokens, nthreads))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl),
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": nthreads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=synthetic.WORKLOAD_ORDER)
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' summary")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

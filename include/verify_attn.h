@@ -1,0 +1,248 @@
+/*
+ * verify_attn.h -- C ABI of the GB300 (sm_103a) paged-KV GQA/MQA verify
+ * attention library (libverify_attn.so).
+ *
+ * One step of speculative-decoding verification: each request b holds L_b
+ * query tokens (a draft chain under a causal mask, or a draft tree under a
+ * bit-packed ancestor mask; L_b = 1 is plain decode, and a request with no
+ * cached prefix and a causal mask is ordinary varlen causal prefill).  They
+ * attend to the request's cached keys / values -- the prefix plus the drafts
+ * themselves, appended first -- reached through a paged KV cache, and the
+ * library returns out = softmax(Q K^T * sm_scale * k_scale + M) V * v_scale
+ * and the natural-log LSE of every (token, query head) row.
+ *
+ * Sources (by page and section):
+ *  - flashmap 0.1.0, flashmap/sglang/verify_attention.py: the split-KV verify
+ *    design (one program per request, KV head, row block and split holding
+ *    all G query heads of the KV head; an LSE merge of the splits; k_scale on
+ *    the logits and v_scale on the values; a host plan that reads only
+ *    shapes so that the run is graph-capturable).
+ *  - FlashInfer PR #286 "Separate Q and KV dtypes for decode": the paged
+ *    table (indptr, indices, last_page_len, page_size), the plan / run split
+ *    (begin_forward caches auxiliary data for many forward calls), the
+ *    validation in BeginForward (int32 index arrays, num_qo_heads divisible
+ *    by num_kv_heads), a caller-owned workspace, status-code errors, and a
+ *    query dtype separate from the (possibly fp8) KV dtype.
+ *  - FlashInfer issue #152 "How to implement a tree attention": custom tree
+ *    masks; a triu -inf mask is the causal mask.
+ *  - vLLM PR #1679 "cached multi-query attention towards speculative
+ *    decoding": write every draft's K/V into the cache, then attend.
+ *  - vLLM PR #2401 "Support MQA/GQA in prefill stage": GQA as MHA over K/V
+ *    shared by G query heads (query head qh uses KV head qh / G).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Status: every function returns VA_OK (0) or a negative VA_ERR_* code; no
+ *  function throws, aborts or exits.  verify_attn_status_string() names a code.
+ *
+ *  Ownership: the caller owns every buffer, host and device, including the
+ *  device workspace and the host plan buffer.  Nothing is allocated on the
+ *  device by any entry point, and verify_attn_run / paged_kv_append read no
+ *  device memory on the host, so both may be captured into a CUDA graph.
+ *
+ *  Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *  default stream).  Device work is enqueued asynchronously on it.
+ *
+ *  Layouts (all contiguous, row-major):
+ *   q, out         [total_qo, num_qo_heads, head_dim]   bf16
+ *   lse            [total_qo, num_qo_heads]             fp32, natural log
+ *   k_cache/v_cache[num_pages, num_kv_heads, page_size, head_dim]  ("HND")
+ *                  bf16 or fp8-e4m3 (the KV dtype)
+ *   k_new / v_new  [total_new, num_kv_heads, head_dim]  KV dtype
+ *   kv_indptr      [batch+1] int32: request b's pages are
+ *                  kv_indices[kv_indptr[b] .. kv_indptr[b+1])
+ *   kv_indices     [kv_indptr[batch]] int32 page ids in [0, num_pages)
+ *   last_page_len  [batch] int32 in [1, page_size] (any value when the
+ *                  request has no page); kv_len_b = (pages_b - 1) *
+ *                  page_size + last_page_len_b, or 0 with no page
+ *   qo_indptr      [batch+1] int32: request b's query tokens are rows
+ *                  qo_indptr[b] .. qo_indptr[b+1] of q / out; L_b >= 0
+ *   mask           bit-packed uint8, LSB first (element e is bit e & 7 of
+ *                  byte e >> 3); request b's L_b x L_b row-major block starts
+ *                  at BIT offset mask_indptr[b]; bit (t, u) = 1 means draft
+ *                  token t may attend to draft token u.  NULL = causal
+ *                  (u <= t).  Prefix keys are always visible.
+ *   mask_indptr    [batch+1] int32 bit offsets, mask_indptr[b+1] -
+ *                  mask_indptr[b] = L_b * L_b.
+ *  The drafts are the LAST L_b positions of each request's kv range, so the
+ *  prefix length is kv_len_b - L_b (kv_len_b >= L_b is required).
+ *
+ *  Supported: head_dim 64 or 128; page_size a power of two in [1, 256];
+ *  num_qo_heads a multiple of num_kv_heads (any group G = num_qo_heads /
+ *  num_kv_heads; a request's G * L_b rows are cut into row blocks); q / out
+ *  bf16; KV bf16 or fp8-e4m3 (OCP "fn": no infinities).  Device pointers
+ *  must be 16-byte aligned.
+ *  Unsupported requests (other head dims, page sizes, dtypes; logit caps,
+ *  sinks, sliding windows, RoPE) return VA_ERR_UNSUPPORTED -- there is no
+ *  fallback path.
+ */
+#ifndef VERIFY_ATTN_H
+#define VERIFY_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VA_OK 0
+#define VA_ERR_INVALID_ARGUMENT (-1)   /* null pointer, bad size, inconsistent tables */
+#define VA_ERR_UNSUPPORTED (-2)        /* a valid request this library does not serve */
+#define VA_ERR_WORKSPACE_TOO_SMALL (-3)
+#define VA_ERR_PLAN_MISMATCH (-4)      /* plan built for other shapes / dtypes */
+#define VA_ERR_CUDA (-5)               /* a CUDA runtime call failed */
+#define VA_ERR_DEVICE_CHECK (-6)       /* a kernel's bounds check fired (see device_status) */
+#define VA_ERR_PLAN_BUFFER_TOO_SMALL (-7)
+
+/* Element types. */
+#define VA_DTYPE_BF16 0
+#define VA_DTYPE_FP8_E4M3 1
+
+/* Device-side check bits reported by verify_attn_device_status(). */
+#define VA_DEV_BAD_PAGE 1        /* a page id outside [0, num_pages): read as zeros / skipped */
+#define VA_DEV_BAD_TABLE 2       /* device tables disagree with the plan: item skipped */
+#define VA_DEV_BAD_APPEND 4      /* append position outside the request's pages: skipped */
+#define VA_DEV_TIMEOUT 8         /* a bounded wait gave up */
+
+/* Optional planner knobs (pass NULL for the defaults). */
+typedef struct {
+    int max_splits;      /* upper bound on kv splits per (request, KV head, row block);
+                            0 = planner's choice, 1 = never split */
+    int min_chunk;       /* smallest kv chunk (keys) a split may hold; 0 = default */
+    int target_ctas;     /* CTAs the plan aims to fill; 0 = derived from the SM count */
+    int kernel;          /* force a kernel variant (VA_KERNEL_*); 0 = automatic */
+    int reserved[4];     /* must be zero */
+} va_plan_options_t;
+
+#define VA_KERNEL_AUTO 0
+#define VA_KERNEL_MMA_64 1      /* warp-level tensor cores, 64-row blocks, 4 warps */
+#define VA_KERNEL_MMA_128 2     /* warp-level tensor cores, 128-row blocks, 8 warps */
+
+/* Name of a status code (static string). */
+const char* verify_attn_status_string(int status);
+
+/* Number of SMs of the current CUDA device (or an error). */
+int verify_attn_num_sms(int* num_sms);
+
+/*
+ * Upper bounds, for a batch with at most `batch` requests and `total_qo`
+ * query tokens, of the host plan buffer and the device workspace any
+ * verify_attn_plan() call can need (e.g. to size buffers once before
+ * graph capture).  num_sms <= 0 queries the current device.
+ */
+int verify_attn_plan_bounds(int batch, int64_t total_qo, int num_qo_heads, int num_kv_heads,
+                            int head_dim, int num_sms, size_t* plan_bytes,
+                            size_t* workspace_bytes);
+
+/*
+ * Host half of the plan (flashmap's split planner and FlashInfer's
+ * begin_forward): from HOST copies of the index arrays, cut the work into
+ * items (request b, KV head h, row block, kv chunk [lo, hi)) that fill the
+ * GPU, and record it in the caller's host buffer `plan_h` (plan_bytes long).
+ * Performs no CUDA call.  mask_indptr_h may be NULL when has_mask = 0.
+ * num_sms <= 0 queries the current device (that query is the one CUDA call).
+ * On success *workspace_bytes receives the device workspace this plan needs.
+ * Errors: VA_ERR_INVALID_ARGUMENT (inconsistent tables, null pointers),
+ * VA_ERR_UNSUPPORTED, VA_ERR_PLAN_BUFFER_TOO_SMALL (*workspace_bytes then
+ * holds the plan bytes needed).
+ */
+int verify_attn_plan_host(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h,
+                          const int32_t* last_page_len_h, const int32_t* mask_indptr_h,
+                          int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                          int page_size, int q_dtype, int kv_dtype, int has_mask, int num_sms,
+                          const va_plan_options_t* options, void* plan_h, size_t plan_bytes,
+                          size_t* workspace_bytes);
+
+/*
+ * verify_attn_plan_host() followed by an asynchronous upload of the plan's
+ * work list into the device workspace on `stream`.  The workspace must hold
+ * at least the bytes verify_attn_plan_host reports (else
+ * VA_ERR_WORKSPACE_TOO_SMALL).  It also clears the workspace's device status
+ * word.  If plan_h is pinned host memory it must not change until the
+ * upload has run on `stream`.  Pointers into the workspace stay valid until
+ * the next plan into the same workspace.
+ */
+int verify_attn_plan(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h,
+                     const int32_t* last_page_len_h, const int32_t* mask_indptr_h, int batch,
+                     int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                     int q_dtype, int kv_dtype, int has_mask, int num_sms,
+                     const va_plan_options_t* options, void* plan_h, size_t plan_bytes,
+                     void* workspace_d, size_t workspace_bytes, void* stream);
+
+/*
+ * Verify attention (flashmap's partial kernel followed by its LSE merge).
+ * All array arguments are DEVICE pointers with the layouts above; the index
+ * arrays must hold the same values the plan was built from (a kernel that
+ * finds otherwise skips the item and raises VA_DEV_BAD_TABLE).  mask /
+ * mask_indptr are NULL iff the plan was made with has_mask = 0.
+ * sm_scale <= 0 selects head_dim^-1/2.  k_scale / v_scale multiply the
+ * stored keys / values (1 for bf16 caches); both must be finite and > 0.
+ * lse may be NULL.  num_pages bounds every page id (a page id outside the
+ * pool is read as zeros and raises VA_DEV_BAD_PAGE).  plan_h is the host plan
+ * buffer; it is read on the host during the call only.
+ * Errors: VA_ERR_INVALID_ARGUMENT, VA_ERR_PLAN_MISMATCH,
+ * VA_ERR_WORKSPACE_TOO_SMALL, VA_ERR_CUDA (launch failure).
+ */
+int verify_attn_run(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* kv_indptr, const int32_t* kv_indices,
+                    const int32_t* last_page_len, const int32_t* qo_indptr, const uint8_t* mask,
+                    const int32_t* mask_indptr, int num_qo_heads, int num_kv_heads, int head_dim,
+                    int page_size, float sm_scale, float k_scale, float v_scale, void* out,
+                    float* lse, int num_pages, const void* plan_h, void* workspace_d,
+                    size_t workspace_bytes, void* stream);
+
+/*
+ * The two halves of verify_attn_run, for callers that time or schedule them
+ * apart: the split attention kernel (it writes the final out / lse of every
+ * unsplit item and the fp32 partials of split items into the workspace), and
+ * the LSE merge of those partials (a no-op when the plan has no split).
+ * verify_attn_merge must follow verify_attn_partial of the same plan on the
+ * same stream, with the same out / lse.
+ */
+int verify_attn_partial(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* kv_indptr, const int32_t* kv_indices,
+                        const int32_t* last_page_len, const int32_t* qo_indptr,
+                        const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads,
+                        int num_kv_heads, int head_dim, int page_size, float sm_scale,
+                        float k_scale, float v_scale, void* out, float* lse, int num_pages,
+                        const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                        void* stream);
+int verify_attn_merge(const int32_t* qo_indptr, int num_qo_heads, int num_kv_heads, int head_dim,
+                      void* out, float* lse, const void* plan_h, void* workspace_d,
+                      size_t workspace_bytes, void* stream);
+
+/* Number of kernel launches verify_attn_run makes for this plan (1 or 2; 0
+ * when the batch has no query token). */
+int verify_attn_plan_launches(const void* plan_h, int* launches);
+
+/*
+ * Read and clear the workspace's device status word (an OR of VA_DEV_* bits
+ * raised by kernels since the last plan / read).  Synchronises `stream`.
+ * Returns VA_ERR_DEVICE_CHECK when any bit was set, else VA_OK.
+ */
+int verify_attn_device_status(void* workspace_d, int* bits, void* stream);
+
+/*
+ * Paged append (vLLM PR #1679: cache every draft's K/V before attention):
+ * for request b and new token i < n_b = append_indptr[b+1] - append_indptr[b]
+ * (host-known total_new = append_indptr[batch]), position pos = kv_len_b -
+ * n_b + i; copy k_new[append_indptr[b] + i, h, :] bit for bit to
+ * k_cache[kv_indices[kv_indptr[b] + pos / page_size], h, pos % page_size, :],
+ * and likewise v.  The page table must already cover the new tokens
+ * (kv_len_b counts them).  k_new / v_new are in the cache dtype (a pure
+ * copy).  Device pointers; status_d (nullable, device int) receives
+ * VA_DEV_BAD_APPEND / VA_DEV_BAD_PAGE bits (OR-ed) for skipped tokens.
+ * Errors: VA_ERR_INVALID_ARGUMENT, VA_ERR_UNSUPPORTED, VA_ERR_CUDA.
+ */
+int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_indptr,
+                    const int32_t* kv_indptr, const int32_t* kv_indices,
+                    const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
+                    int num_kv_heads, int head_dim, int page_size, int num_pages, int kv_dtype,
+                    int64_t total_new, int* status_d, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_ATTN_H */

@@ -1,0 +1,351 @@
+"""Python binding of libverify_attn.so: GQA/MQA verify attention over a paged
+KV cache, hand-written CUDA for sm_103a (GB300).
+
+The functions mirror the C ABI (include/verify_attn.h) and only marshal
+arguments: torch tensors supply device memory and the current CUDA stream;
+every step of the computation runs in the library's kernels.  There is no
+CPU or PyTorch fallback: if the shared library is missing, importing the
+binding's functions raises.
+
+Typical step::
+
+    plan = verify_attn_plan(kv_indptr_h, qo_indptr_h, last_page_len_h,
+                            mask_indptr_h, num_qo_heads, num_kv_heads,
+                            head_dim, page_size, kv_dtype="bf16")
+    paged_kv_append(k_new, v_new, qo_indptr, kv_indptr, kv_indices,
+                    last_page_len, k_cache, v_cache)
+    verify_attn_run(q, k_cache, v_cache, kv_indptr, kv_indices,
+                    last_page_len, qo_indptr, mask, mask_indptr, plan,
+                    out=out, lse=lse)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+__all__ = [
+    "VerifyAttnError", "Plan", "lib", "verify_attn_plan", "verify_attn_run",
+    "verify_attn_partial", "verify_attn_merge", "paged_kv_append",
+    "verify_attn_device_status", "verify_attn_plan_bounds", "verify_attn_plan_host",
+    "status_string", "num_sms", "KV_BF16", "KV_FP8_E4M3", "library_path",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "libverify_attn.so")
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+_DTYPES = {"bf16": KV_BF16, "bfloat16": KV_BF16, "fp8_e4m3": KV_FP8_E4M3,
+           "float8_e4m3fn": KV_FP8_E4M3, torch.bfloat16: KV_BF16,
+           torch.float8_e4m3fn: KV_FP8_E4M3}
+
+VA_OK = 0
+VA_ERR_DEVICE_CHECK = -6
+VA_ERR_PLAN_BUFFER_TOO_SMALL = -7
+
+_lib = None
+
+
+class VerifyAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (fn, status_string(status), status))
+
+
+class PlanOptions(ctypes.Structure):
+    _fields_ = [("max_splits", ctypes.c_int), ("min_chunk", ctypes.c_int),
+                ("target_ctas", ctypes.c_int), ("kernel", ctypes.c_int),
+                ("reserved", ctypes.c_int * 4)]
+
+
+def lib():
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise ImportError(
+            "libverify_attn.so is not built (expected at %s); run "
+            "`python -c 'import __graft_entry__ as g; g.build()'`" % library_path)
+    L = ctypes.CDLL(library_path)
+    P, i32, i64, sz, f32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                            ctypes.c_float)
+    Psz = ctypes.POINTER(ctypes.c_size_t)
+    Pi = ctypes.POINTER(ctypes.c_int)
+    sigs = {
+        "verify_attn_status_string": (ctypes.c_char_p, [i32]),
+        "verify_attn_num_sms": (i32, [Pi]),
+        "verify_attn_plan_bounds": (i32, [i32, i64, i32, i32, i32, i32, Psz, Psz]),
+        "verify_attn_plan_host": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                        P, P, sz, Psz]),
+        "verify_attn_plan": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, P, P,
+                                   sz, P, sz, P]),
+        "verify_attn_run": (i32, [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, f32, f32, f32,
+                                  P, P, i32, P, P, sz, P]),
+        "verify_attn_partial": (i32, [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, f32, f32,
+                                      f32, P, P, i32, P, P, sz, P]),
+        "verify_attn_merge": (i32, [P, i32, i32, i32, P, P, P, P, sz, P]),
+        "verify_attn_plan_launches": (i32, [P, Pi]),
+        "verify_attn_device_status": (i32, [P, Pi, P]),
+        "paged_kv_append": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, P,
+                                  P]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().verify_attn_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != VA_OK:
+        raise VerifyAttnError(fn, status)
+
+
+def num_sms() -> int:
+    n = ctypes.c_int(0)
+    _check("verify_attn_num_sms", lib().verify_attn_num_sms(ctypes.byref(n)))
+    return n.value
+
+
+def _kv_code(kv_dtype) -> int:
+    if isinstance(kv_dtype, int):
+        return kv_dtype
+    return _DTYPES[kv_dtype]
+
+
+def _host_i32(a) -> Optional[np.ndarray]:
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _hp(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dp(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0):
+    o = PlanOptions()
+    o.max_splits, o.min_chunk, o.target_ctas, o.kernel = (int(max_splits), int(min_chunk),
+                                                          int(target_ctas), int(kernel))
+    return o
+
+
+@dataclass
+class Plan:
+    """A plan: the host buffer (numpy) and the device workspace (torch) it was
+    uploaded to, plus the shapes it was built for."""
+    host: np.ndarray
+    workspace: Optional[torch.Tensor]
+    workspace_bytes: int
+    batch: int
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    kv_dtype: int
+    has_mask: bool
+    total_qo: int
+
+    def header(self) -> dict:
+        h = self.host[:184].view(np.uint8)
+        ints = np.frombuffer(h[:72].tobytes(), dtype=np.int32)
+        i64 = np.frombuffer(h[72:96].tobytes(), dtype=np.int64)
+        return dict(group=int(ints[10]), kernel=int(ints[11]), block_rows=int(ints[12]),
+                    tile_keys=int(ints[13]), n_items=int(ints[14]), n_merge=int(ints[15]),
+                    n_units=int(ints[16]), num_sms=int(ints[17]), total_qo=int(i64[0]),
+                    part_rows=int(i64[1]), chunk=int(i64[2]))
+
+    def launches(self) -> int:
+        n = ctypes.c_int(0)
+        _check("verify_attn_plan_launches",
+               lib().verify_attn_plan_launches(_hp(self.host), ctypes.byref(n)))
+        return n.value
+
+    def items(self) -> np.ndarray:
+        """The work list as an [n_items, 8] int32 array (b, h, row0, nrows,
+        kv_lo, kv_hi, part_row, pad)."""
+        hd = self.header()
+        raw = self.host[184:184 + 32 * hd["n_items"]].tobytes()
+        return np.frombuffer(raw, dtype=np.int32).reshape(-1, 8)
+
+    def merges(self) -> np.ndarray:
+        hd = self.header()
+        off = 184 + 32 * hd["n_items"]
+        raw = self.host[off:off + 32 * hd["n_merge"]].tobytes()
+        return np.frombuffer(raw, dtype=np.int32).reshape(-1, 8)
+
+
+def verify_attn_plan_bounds(batch, total_qo, num_qo_heads, num_kv_heads, head_dim, num_sms=0):
+    pb, wb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("verify_attn_plan_bounds",
+           lib().verify_attn_plan_bounds(int(batch), int(total_qo), int(num_qo_heads),
+                                         int(num_kv_heads), int(head_dim), int(num_sms),
+                                         ctypes.byref(pb), ctypes.byref(wb)))
+    return pb.value, wb.value
+
+
+def verify_attn_plan_host(kv_indptr_h, qo_indptr_h, last_page_len_h, mask_indptr_h,
+                          num_qo_heads, num_kv_heads, head_dim, page_size, kv_dtype="bf16",
+                          has_mask=None, num_sms=0, **options) -> Plan:
+    """Host-only plan (no CUDA call when num_sms > 0)."""
+    kvp, qop, lpl, mip = (_host_i32(kv_indptr_h), _host_i32(qo_indptr_h),
+                          _host_i32(last_page_len_h), _host_i32(mask_indptr_h))
+    batch = len(qop) - 1
+    if has_mask is None:
+        has_mask = mip is not None
+    total_qo = int(qop[-1]) if batch >= 0 else 0
+    if num_sms <= 0:
+        num_sms = globals()["num_sms"]()
+    pb, _ = verify_attn_plan_bounds(batch, total_qo, num_qo_heads, num_kv_heads, head_dim,
+                                    num_sms)
+    host = np.zeros(pb, dtype=np.uint8)
+    need = ctypes.c_size_t(0)
+    opt = _options(**options)
+    rc = lib().verify_attn_plan_host(_hp(kvp), _hp(qop), _hp(lpl), _hp(mip), batch,
+                                     int(num_qo_heads), int(num_kv_heads), int(head_dim),
+                                     int(page_size), 0, _kv_code(kv_dtype), int(bool(has_mask)),
+                                     int(num_sms), ctypes.byref(opt), _hp(host), host.nbytes,
+                                     ctypes.byref(need))
+    _check("verify_attn_plan_host", rc)
+    return Plan(host, None, need.value, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                _kv_code(kv_dtype), bool(has_mask), total_qo)
+
+
+def verify_attn_plan(kv_indptr_h, qo_indptr_h, last_page_len_h, mask_indptr_h, num_qo_heads,
+                     num_kv_heads, head_dim, page_size, kv_dtype="bf16", has_mask=None,
+                     workspace: Optional[torch.Tensor] = None, device=None, stream=None,
+                     num_sms=0, **options) -> Plan:
+    """Plan a batch from HOST index arrays and upload the work list to a
+    device workspace (allocated here with torch if not given)."""
+    plan = verify_attn_plan_host(kv_indptr_h, qo_indptr_h, last_page_len_h, mask_indptr_h,
+                                 num_qo_heads, num_kv_heads, head_dim, page_size, kv_dtype,
+                                 has_mask, num_sms, **options)
+    if workspace is None or workspace.numel() < plan.workspace_bytes:
+        workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8,
+                                device=device or "cuda")
+    kvp, qop, lpl, mip = (_host_i32(kv_indptr_h), _host_i32(qo_indptr_h),
+                          _host_i32(last_page_len_h), _host_i32(mask_indptr_h))
+    opt = _options(**options)
+    host = np.zeros_like(plan.host)
+    rc = lib().verify_attn_plan(_hp(kvp), _hp(qop), _hp(lpl), _hp(mip), plan.batch,
+                                int(num_qo_heads), int(num_kv_heads), int(head_dim),
+                                int(page_size), 0, plan.kv_dtype, int(plan.has_mask),
+                                int(num_sms), ctypes.byref(opt), _hp(host), host.nbytes,
+                                _dp(workspace), workspace.numel(), _stream(stream))
+    _check("verify_attn_plan", rc)
+    plan.host = host
+    plan.workspace = workspace
+    return plan
+
+
+def _run_args(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
+              mask_indptr, plan: Plan, sm_scale, k_scale, v_scale, out, lse, num_pages):
+    if q.dtype != torch.bfloat16:
+        raise ValueError("q must be bfloat16")
+    if out.dtype != torch.bfloat16:
+        raise ValueError("out must be bfloat16")
+    if lse is not None and lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    if num_pages is None:
+        num_pages = k_cache.shape[0]
+    return (_dp(q), _dp(k_cache), _dp(v_cache), _dp(kv_indptr), _dp(kv_indices),
+            _dp(last_page_len), _dp(qo_indptr), _dp(mask), _dp(mask_indptr),
+            plan.num_qo_heads, plan.num_kv_heads, plan.head_dim, plan.page_size,
+            float(sm_scale), float(k_scale), float(v_scale), _dp(out), _dp(lse),
+            int(num_pages), _hp(plan.host), _dp(plan.workspace), plan.workspace.numel())
+
+
+def _alloc_out(q, plan, out, lse, want_lse):
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    return out, lse
+
+
+def verify_attn_run(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr,
+                    mask, mask_indptr, plan: Plan, sm_scale=0.0, k_scale=1.0, v_scale=1.0,
+                    out=None, lse=None, want_lse=True, num_pages=None, stream=None):
+    """out = softmax(q k^T * sm_scale * k_scale + mask) v * v_scale, and its LSE."""
+    out, lse = _alloc_out(q, plan, out, lse, want_lse)
+    args = _run_args(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
+                     mask_indptr, plan, sm_scale, k_scale, v_scale, out, lse, num_pages)
+    _check("verify_attn_run", lib().verify_attn_run(*args, _stream(stream)))
+    return out, lse
+
+
+def verify_attn_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr,
+                        mask, mask_indptr, plan: Plan, sm_scale=0.0, k_scale=1.0, v_scale=1.0,
+                        out=None, lse=None, want_lse=True, num_pages=None, stream=None):
+    out, lse = _alloc_out(q, plan, out, lse, want_lse)
+    args = _run_args(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
+                     mask_indptr, plan, sm_scale, k_scale, v_scale, out, lse, num_pages)
+    _check("verify_attn_partial", lib().verify_attn_partial(*args, _stream(stream)))
+    return out, lse
+
+
+def verify_attn_merge(qo_indptr, plan: Plan, out, lse=None, stream=None):
+    _check("verify_attn_merge",
+           lib().verify_attn_merge(_dp(qo_indptr), plan.num_qo_heads, plan.num_kv_heads,
+                                   plan.head_dim, _dp(out), _dp(lse), _hp(plan.host),
+                                   _dp(plan.workspace), plan.workspace.numel(), _stream(stream)))
+    return out, lse
+
+
+def verify_attn_device_status(plan: Plan, stream=None) -> int:
+    """OR of VA_DEV_* bits raised by kernels since the plan (synchronises)."""
+    bits = ctypes.c_int(0)
+    rc = lib().verify_attn_device_status(_dp(plan.workspace), ctypes.byref(bits), _stream(stream))
+    if rc not in (VA_OK, VA_ERR_DEVICE_CHECK):
+        _check("verify_attn_device_status", rc)
+    return bits.value
+
+
+def paged_kv_append(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_page_len, k_cache,
+                    v_cache, total_new=None, num_pages=None, status=None, stream=None):
+    """Copy new tokens' K/V into their pages (bit-exact).  total_new defaults
+    to k_new.shape[0]."""
+    if k_cache.dtype != k_new.dtype or v_cache.dtype != v_new.dtype:
+        raise ValueError("k_new / v_new must be in the cache dtype")
+    kv_dtype = KV_FP8_E4M3 if k_cache.element_size() == 1 else KV_BF16
+    batch = append_indptr.shape[0] - 1
+    if total_new is None:
+        total_new = k_new.shape[0]
+    if num_pages is None:
+        num_pages = k_cache.shape[0]
+    h_kv, page_size, head_dim = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
+    rc = lib().paged_kv_append(_dp(k_new), _dp(v_new), _dp(append_indptr), _dp(kv_indptr),
+                               _dp(kv_indices), _dp(last_page_len), _dp(k_cache), _dp(v_cache),
+                               int(batch), int(h_kv), int(head_dim), int(page_size),
+                               int(num_pages), kv_dtype, int(total_new), _dp(status),
+                               _stream(stream))
+    _check("paged_kv_append", rc)

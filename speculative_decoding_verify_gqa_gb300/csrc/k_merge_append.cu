@@ -1,0 +1,134 @@
+// LSE merge of split partials, and the paged K/V append.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "../../include/verify_attn.h"
+#include "va_device.cuh"
+#include "va_kernels.h"
+
+namespace va {
+namespace {
+
+// Merge ("flashmap 0.1.0 -- flashmap/sglang/verify_attention.py", merge
+// kernel): for each row, m = max_s lse_s, w_s = e^(lse_s - m), out =
+// sum_s w_s out_s / sum_s w_s, lse = m + ln sum_s w_s; splits with lse = -inf
+// carry no mass, and a row with no mass at all gets out = 0, lse = -inf.
+// One warp per row; each lane owns D / 32 consecutive output elements.
+template <int D>
+__global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) {
+  constexpr int V = D / 32;
+  const MergeItem it = p.items[blockIdx.x];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.y * 4 + warp;
+  if (r >= it.nrows) return;
+  const float* lse_base = p.part_lse + it.part_row0 + r;
+  float m = -INFINITY;
+  for (int s = 0; s < it.nsplit; ++s) m = fmaxf(m, lse_base[(size_t)s * it.nrows]);
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  float den = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < it.nsplit; ++s) {
+      const float ls = lse_base[(size_t)s * it.nrows];
+      if (ls == -INFINITY) continue;
+      const float w = ex2((ls - m) * kLog2e);
+      den += w;
+      const float* src = p.part_out + ((size_t)it.part_row0 + (size_t)s * it.nrows + r) * D + lane * V;
+      if constexpr (V == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * x.x; acc[1] += w * x.y;
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  const int rr = it.row0 + r;
+  const int t = rr / p.group, g = rr - t * p.group;
+  const size_t orow = (size_t)(p.qo_indptr[it.b] + t) * p.h_q + (size_t)it.h * p.group + g;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + orow * D + lane * V;
+  if constexpr (V == 4) {
+    uint2 v;
+    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = v;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+  if (p.lse && lane == 0) p.lse[orow] = den > 0.f ? m + logf(den) : -INFINITY;
+}
+
+// Paged append (vLLM PR #1679: every draft's K/V is cached before attention;
+// FlashInfer PR #286's page table).  One thread per 16-byte chunk of one
+// (token, KV head) row, for K and V: a bit-exact copy to slot pos % P of page
+// kv_indices[kv_indptr[b] + pos / P], pos = kv_len_b - n_b + i.
+__global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams p) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long per_tok = (long long)p.h_kv * p.row_chunks;
+  if (idx >= p.total_new * per_tok) return;
+  const int i = (int)(idx / per_tok);
+  const int rem = (int)(idx - (long long)i * per_tok);
+  const int h = rem / p.row_chunks, ch = rem - h * p.row_chunks;
+  // request of token i: the last b with append_indptr[b] <= i
+  int lo = 0, hi = p.batch;  // invariant: append_indptr[lo] <= i < append_indptr[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.append_indptr + mid) <= i) lo = mid; else hi = mid;
+  }
+  const int b = lo;
+  const int a0 = __ldg(p.append_indptr + b);
+  const int n = __ldg(p.append_indptr + b + 1) - a0;
+  const int pg0 = __ldg(p.kv_indptr + b);
+  const int npg = __ldg(p.kv_indptr + b + 1) - pg0;
+  const int lpl = npg > 0 ? __ldg(p.last_page_len + b) : 0;
+  const long long kv_len = npg > 0 ? (long long)(npg - 1) * p.page_size + lpl : 0;
+  const long long pos = kv_len - n + (i - a0);
+  if (i < a0 || i - a0 >= n || pos < 0 || (npg > 0 && (lpl < 1 || lpl > p.page_size)) ||
+      (pos >> p.log2_page) >= npg) {
+    if (p.status) atomicOr(p.status, VA_DEV_BAD_APPEND);
+    return;
+  }
+  const int page = __ldg(p.kv_indices + pg0 + (int)(pos >> p.log2_page));
+  if ((unsigned)page >= (unsigned)p.num_pages) {
+    if (p.status) atomicOr(p.status, VA_DEV_BAD_PAGE);
+    return;
+  }
+  const size_t row_bytes = (size_t)p.row_chunks * 16;
+  const size_t dst = (((size_t)page * p.h_kv + h) * p.page_size + (size_t)(pos & (p.page_size - 1))) *
+                         row_bytes + (size_t)ch * 16;
+  const size_t src = ((size_t)i * p.h_kv + h) * row_bytes + (size_t)ch * 16;
+  const uint4 kv = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.k_new) + src);
+  const uint4 vv = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.v_new) + src);
+  *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_cache) + dst) = kv;
+  *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_cache) + dst) = vv;
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams& p, int head_dim, int n_merge, int block_rows,
+                         cudaStream_t stream) {
+  if (n_merge <= 0) return cudaSuccess;
+  dim3 grid(n_merge, (block_rows + 3) / 4);
+  void* args[] = {const_cast<MergeParams*>(&p)};
+  if (head_dim == 128)
+    return cudaLaunchKernel(reinterpret_cast<const void*>(verify_merge_kernel<128>), grid,
+                            dim3(128), args, 0, stream);
+  if (head_dim == 64)
+    return cudaLaunchKernel(reinterpret_cast<const void*>(verify_merge_kernel<64>), grid,
+                            dim3(128), args, 0, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
+  const long long threads = p.total_new * (long long)p.h_kv * p.row_chunks;
+  if (threads <= 0) return cudaSuccess;
+  const long long blocks = (threads + 255) / 256;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  void* args[] = {const_cast<AppendParams*>(&p)};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(paged_kv_append_kernel),
+                          dim3((unsigned)blocks), dim3(256), args, 0, stream);
+}
+
+}  // namespace va

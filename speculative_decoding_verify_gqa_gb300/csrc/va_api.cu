@@ -1,0 +1,311 @@
+// C ABI of libverify_attn.so: argument checks, plan upload and kernel
+// launches.  See include/verify_attn.h for the contract of every entry point.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <string.h>
+
+#include "../../include/verify_attn.h"
+#include "va_internal.h"
+#include "va_kernels.h"
+
+namespace va {
+int check_common(int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int q_dtype,
+                 int kv_dtype);
+int plan_bounds(int batch, int64_t total_qo, int num_qo_heads, int num_kv_heads, int head_dim,
+                int num_sms, size_t* plan_bytes, size_t* workspace_bytes);
+int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t* last_page_len,
+              const int32_t* mask_indptr, int batch, int num_qo_heads, int num_kv_heads,
+              int head_dim, int page_size, int q_dtype, int kv_dtype, int has_mask, int num_sms,
+              const va_plan_options_t* opts, void* plan_h, size_t plan_bytes,
+              size_t* workspace_bytes);
+}  // namespace va
+
+using namespace va;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int log2_int(int x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+int query_sms(int* n) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return VA_ERR_CUDA;
+  return *n > 0 ? VA_OK : VA_ERR_CUDA;
+}
+
+const PlanHeader* plan_header(const void* plan_h) {
+  if (!plan_h) return nullptr;
+  const PlanHeader* hd = static_cast<const PlanHeader*>(plan_h);
+  if (hd->magic != kPlanMagic || hd->version != kPlanVersion) return nullptr;
+  return hd;
+}
+
+// Shared checks of verify_attn_run / _partial: the plan matches the call.
+int check_run(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
+              const int32_t* kv_indices, const int32_t* last_page_len, const int32_t* qo_indptr,
+              const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads, int num_kv_heads,
+              int head_dim, int page_size, float* sm_scale, float k_scale, float v_scale,
+              const void* out, const float* lse, int num_pages, const void* plan_h,
+              const void* workspace_d, size_t workspace_bytes, const PlanHeader** hd_out) {
+  const PlanHeader* hd = plan_header(plan_h);
+  if (!hd) return VA_ERR_INVALID_ARGUMENT;
+  if (hd->h_q != num_qo_heads || hd->h_kv != num_kv_heads || hd->head_dim != head_dim ||
+      hd->page_size != page_size || hd->has_mask != (mask != nullptr ? 1 : 0))
+    return VA_ERR_PLAN_MISMATCH;
+  if ((mask != nullptr) != (mask_indptr != nullptr)) return VA_ERR_INVALID_ARGUMENT;
+  if (!workspace_d || workspace_bytes < hd->ws_bytes) return VA_ERR_WORKSPACE_TOO_SMALL;
+  if (!(isfinite(k_scale) && k_scale > 0.f && isfinite(v_scale) && v_scale > 0.f))
+    return VA_ERR_INVALID_ARGUMENT;
+  if (!isfinite(*sm_scale)) return VA_ERR_INVALID_ARGUMENT;
+  if (*sm_scale <= 0.f) *sm_scale = 1.0f / sqrtf((float)head_dim);
+  *hd_out = hd;
+  if (hd->n_items == 0) return VA_OK;
+  if (!q || !k_cache || !v_cache || !kv_indptr || !kv_indices || !last_page_len || !qo_indptr ||
+      !out || num_pages <= 0)
+    return VA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(workspace_d))
+    return VA_ERR_INVALID_ARGUMENT;
+  (void)lse;
+  return VA_OK;
+}
+
+PartialParams make_partial(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* kv_indptr, const int32_t* kv_indices,
+                           const int32_t* last_page_len, const int32_t* qo_indptr,
+                           const uint8_t* mask, const int32_t* mask_indptr, float sm_scale,
+                           float k_scale, float v_scale, void* out, float* lse, int num_pages,
+                           const PlanHeader* hd, void* workspace_d) {
+  char* ws = static_cast<char*>(workspace_d);
+  PartialParams p;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.kv_indptr = kv_indptr;
+  p.kv_indices = kv_indices;
+  p.last_page_len = last_page_len;
+  p.qo_indptr = qo_indptr;
+  p.mask = mask;
+  p.mask_indptr = mask_indptr;
+  p.out = out;
+  p.lse = lse;
+  p.items = reinterpret_cast<const WorkItem*>(ws + hd->off_items);
+  p.part_out = reinterpret_cast<float*>(ws + hd->off_part_out);
+  p.part_lse = reinterpret_cast<float*>(ws + hd->off_part_lse);
+  p.status = reinterpret_cast<int*>(ws + hd->off_status);
+  p.h_q = hd->h_q;
+  p.h_kv = hd->h_kv;
+  p.group = hd->group;
+  p.page_size = hd->page_size;
+  p.log2_page = log2_int(hd->page_size);
+  p.num_pages = num_pages;
+  p.scale_nat = sm_scale * k_scale;
+  p.scale_log2 = sm_scale * k_scale * 1.4426950408889634f;
+  p.v_scale = v_scale;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* verify_attn_status_string(int status) {
+  switch (status) {
+    case VA_OK: return "ok";
+    case VA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case VA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case VA_ERR_WORKSPACE_TOO_SMALL: return "device workspace too small";
+    case VA_ERR_PLAN_MISMATCH: return "plan does not match the call";
+    case VA_ERR_CUDA: return "CUDA runtime error";
+    case VA_ERR_DEVICE_CHECK: return "a device-side check failed";
+    case VA_ERR_PLAN_BUFFER_TOO_SMALL: return "host plan buffer too small";
+    default: return "unknown status";
+  }
+}
+
+int verify_attn_num_sms(int* num_sms) {
+  if (!num_sms) return VA_ERR_INVALID_ARGUMENT;
+  return query_sms(num_sms);
+}
+
+int verify_attn_plan_bounds(int batch, int64_t total_qo, int num_qo_heads, int num_kv_heads,
+                            int head_dim, int num_sms, size_t* plan_bytes,
+                            size_t* workspace_bytes) {
+  if (num_sms <= 0) {
+    int rc = query_sms(&num_sms);
+    if (rc) return rc;
+  }
+  return plan_bounds(batch, total_qo, num_qo_heads, num_kv_heads, head_dim, num_sms, plan_bytes,
+                     workspace_bytes);
+}
+
+int verify_attn_plan_host(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h,
+                          const int32_t* last_page_len_h, const int32_t* mask_indptr_h,
+                          int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                          int page_size, int q_dtype, int kv_dtype, int has_mask, int num_sms,
+                          const va_plan_options_t* options, void* plan_h, size_t plan_bytes,
+                          size_t* workspace_bytes) {
+  if (num_sms <= 0) {
+    int rc = query_sms(&num_sms);
+    if (rc) return rc;
+  }
+  return plan_host(kv_indptr_h, qo_indptr_h, last_page_len_h, mask_indptr_h, batch,
+                   num_qo_heads, num_kv_heads, head_dim, page_size, q_dtype, kv_dtype, has_mask,
+                   num_sms, options, plan_h, plan_bytes, workspace_bytes);
+}
+
+int verify_attn_plan(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h,
+                     const int32_t* last_page_len_h, const int32_t* mask_indptr_h, int batch,
+                     int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                     int q_dtype, int kv_dtype, int has_mask, int num_sms,
+                     const va_plan_options_t* options, void* plan_h, size_t plan_bytes,
+                     void* workspace_d, size_t workspace_bytes, void* stream) {
+  size_t need = 0;
+  int rc = verify_attn_plan_host(kv_indptr_h, qo_indptr_h, last_page_len_h, mask_indptr_h, batch,
+                                 num_qo_heads, num_kv_heads, head_dim, page_size, q_dtype,
+                                 kv_dtype, has_mask, num_sms, options, plan_h, plan_bytes, &need);
+  if (rc) return rc;
+  if (!workspace_d || workspace_bytes < need) return VA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace_d)) return VA_ERR_INVALID_ARGUMENT;
+  const PlanHeader* hd = static_cast<const PlanHeader*>(plan_h);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace_d);
+  if (cudaMemsetAsync(ws + hd->off_status, 0, sizeof(int), s) != cudaSuccess) return VA_ERR_CUDA;
+  size_t list = (size_t)hd->n_items * sizeof(WorkItem) + (size_t)hd->n_merge * sizeof(MergeItem);
+  if (list > 0 &&
+      cudaMemcpyAsync(ws + hd->off_items, static_cast<const char*>(plan_h) + sizeof(PlanHeader),
+                      list, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return VA_ERR_CUDA;
+  return VA_OK;
+}
+
+int verify_attn_plan_launches(const void* plan_h, int* launches) {
+  const PlanHeader* hd = plan_header(plan_h);
+  if (!hd || !launches) return VA_ERR_INVALID_ARGUMENT;
+  *launches = (hd->n_items > 0 ? 1 : 0) + (hd->n_merge > 0 ? 1 : 0);
+  return VA_OK;
+}
+
+int verify_attn_partial(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* kv_indptr, const int32_t* kv_indices,
+                        const int32_t* last_page_len, const int32_t* qo_indptr,
+                        const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads,
+                        int num_kv_heads, int head_dim, int page_size, float sm_scale,
+                        float k_scale, float v_scale, void* out, float* lse, int num_pages,
+                        const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                        void* stream) {
+  const PlanHeader* hd = nullptr;
+  int rc = check_run(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
+                     mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size, &sm_scale,
+                     k_scale, v_scale, out, lse, num_pages, plan_h, workspace_d, workspace_bytes,
+                     &hd);
+  if (rc) return rc;
+  if (hd->n_items == 0) return VA_OK;
+  PartialParams p = make_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len,
+                                 qo_indptr, mask, mask_indptr, sm_scale, k_scale, v_scale, out,
+                                 lse, num_pages, hd, workspace_d);
+  cudaError_t e = launch_partial_mma(p, hd->kernel, hd->head_dim,
+                                     hd->kv_dtype == VA_DTYPE_FP8_E4M3, hd->n_items,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
+int verify_attn_merge(const int32_t* qo_indptr, int num_qo_heads, int num_kv_heads, int head_dim,
+                      void* out, float* lse, const void* plan_h, void* workspace_d,
+                      size_t workspace_bytes, void* stream) {
+  const PlanHeader* hd = plan_header(plan_h);
+  if (!hd) return VA_ERR_INVALID_ARGUMENT;
+  if (hd->h_q != num_qo_heads || hd->h_kv != num_kv_heads || hd->head_dim != head_dim)
+    return VA_ERR_PLAN_MISMATCH;
+  if (hd->n_merge == 0) return VA_OK;
+  if (!workspace_d || workspace_bytes < hd->ws_bytes) return VA_ERR_WORKSPACE_TOO_SMALL;
+  if (!qo_indptr || !out || !aligned16(out) || !aligned16(workspace_d))
+    return VA_ERR_INVALID_ARGUMENT;
+  char* ws = static_cast<char*>(workspace_d);
+  MergeParams m;
+  m.items = reinterpret_cast<const MergeItem*>(ws + hd->off_merge);
+  m.part_out = reinterpret_cast<const float*>(ws + hd->off_part_out);
+  m.part_lse = reinterpret_cast<const float*>(ws + hd->off_part_lse);
+  m.qo_indptr = qo_indptr;
+  m.out = out;
+  m.lse = lse;
+  m.h_q = hd->h_q;
+  m.group = hd->group;
+  cudaError_t e = launch_merge(m, hd->head_dim, hd->n_merge, hd->block_rows,
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
+int verify_attn_run(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* kv_indptr, const int32_t* kv_indices,
+                    const int32_t* last_page_len, const int32_t* qo_indptr, const uint8_t* mask,
+                    const int32_t* mask_indptr, int num_qo_heads, int num_kv_heads, int head_dim,
+                    int page_size, float sm_scale, float k_scale, float v_scale, void* out,
+                    float* lse, int num_pages, const void* plan_h, void* workspace_d,
+                    size_t workspace_bytes, void* stream) {
+  int rc = verify_attn_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len,
+                               qo_indptr, mask, mask_indptr, num_qo_heads, num_kv_heads, head_dim,
+                               page_size, sm_scale, k_scale, v_scale, out, lse, num_pages, plan_h,
+                               workspace_d, workspace_bytes, stream);
+  if (rc) return rc;
+  return verify_attn_merge(qo_indptr, num_qo_heads, num_kv_heads, head_dim, out, lse, plan_h,
+                           workspace_d, workspace_bytes, stream);
+}
+
+int verify_attn_device_status(void* workspace_d, int* bits, void* stream) {
+  if (!workspace_d || !bits) return VA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, workspace_d, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return VA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return VA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace_d, 0, sizeof(int), s) != cudaSuccess) return VA_ERR_CUDA;
+  *bits = v;
+  return v ? VA_ERR_DEVICE_CHECK : VA_OK;
+}
+
+int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_indptr,
+                    const int32_t* kv_indptr, const int32_t* kv_indices,
+                    const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
+                    int num_kv_heads, int head_dim, int page_size, int num_pages, int kv_dtype,
+                    int64_t total_new, int* status_d, void* stream) {
+  if (batch < 0 || total_new < 0 || num_kv_heads <= 0) return VA_ERR_INVALID_ARGUMENT;
+  int rc = check_common(num_kv_heads, num_kv_heads, head_dim, page_size, VA_DTYPE_BF16, kv_dtype);
+  if (rc) return rc;
+  if (total_new == 0) return VA_OK;
+  if (batch == 0) return VA_ERR_INVALID_ARGUMENT;
+  if (!k_new || !v_new || !append_indptr || !kv_indptr || !kv_indices || !last_page_len ||
+      !k_cache || !v_cache || num_pages <= 0)
+    return VA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return VA_ERR_INVALID_ARGUMENT;
+  if (total_new > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
+  AppendParams p;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.append_indptr = append_indptr;
+  p.kv_indptr = kv_indptr;
+  p.kv_indices = kv_indices;
+  p.last_page_len = last_page_len;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.status = status_d;
+  p.batch = batch;
+  p.h_kv = num_kv_heads;
+  p.page_size = page_size;
+  p.log2_page = log2_int(page_size);
+  p.num_pages = num_pages;
+  p.row_chunks = head_dim * (kv_dtype == VA_DTYPE_FP8_E4M3 ? 1 : 2) / 16;
+  p.total_new = total_new;
+  cudaError_t e = launch_append(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// Internal definitions shared by the host planner, the C ABI and the kernels
+// of libverify_attn.so: the plan's header and work-list records, and the
+// workspace layout.  Not part of the public ABI.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace va {
+
+constexpr uint32_t kPlanMagic = 0x31504156u;  // "VAP1"
+constexpr uint32_t kPlanVersion = 1;
+
+// Key tile of the partial kernels (keys per pipeline stage).  Split chunks are
+// cut on multiples of it, so every tile starts on a page boundary whenever
+// page_size <= kTileKeys, and lies inside one page otherwise.
+constexpr int kTileKeys = 64;
+
+// Kernel variants (values match VA_KERNEL_* in verify_attn.h).
+enum Kernel : int32_t {
+  kKernelMma64 = 1,   // warp-level mma.sync, 4 warps x 16 rows
+  kKernelMma128 = 2,  // warp-level mma.sync, 8 warps x 16 rows
+};
+
+inline int kernel_rows(int k) { return k == kKernelMma64 ? 64 : 128; }
+inline int kernel_threads(int k) { return k == kKernelMma64 ? 128 : 256; }
+inline int kernel_ctas_per_sm(int k) { return k == kKernelMma64 ? 2 : 1; }
+
+// One CTA's work: rows [row0, row0 + nrows) of request b's KV head h (row r is
+// query head h * G + r % G at draft token r / G: the G heads sharing the KV
+// head sit next to each other), against kv positions [kv_lo, kv_hi).
+// part_row < 0: the item covers the unit's whole kv range and writes the final
+// out / lse; otherwise it writes fp32 partials at rows part_row .. of the
+// workspace partial buffers.
+struct WorkItem {
+  int32_t b, h, row0, nrows;
+  int32_t kv_lo, kv_hi, part_row, pad;
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+
+// One split unit to merge: nsplit partials of nrows rows each, split s at
+// part rows part_row0 + s * nrows.
+struct MergeItem {
+  int32_t b, h, row0, nrows;
+  int32_t part_row0, nsplit, pad0, pad1;
+};
+static_assert(sizeof(MergeItem) == 32, "MergeItem layout");
+
+// Host plan buffer: PlanHeader, then n_items WorkItems, then n_merge
+// MergeItems.  The WorkItems and MergeItems are uploaded verbatim to the
+// device workspace at off_items.
+struct PlanHeader {
+  uint32_t magic, version;
+  int32_t batch, h_q, h_kv, head_dim, page_size, q_dtype, kv_dtype, has_mask;
+  int32_t group, kernel, block_rows, tile_keys;
+  int32_t n_items, n_merge, n_units, num_sms;
+  int64_t total_qo, part_rows, chunk;
+  uint64_t off_status, off_items, off_merge, off_part_lse, off_part_out, ws_bytes;
+  uint64_t plan_bytes;
+  uint64_t reserved[4];
+};
+static_assert(sizeof(PlanHeader) == 184, "PlanHeader layout (read by the Python binding)");
+
+constexpr size_t kWsAlign = 256;
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace va

@@ -1,0 +1,66 @@
+// Kernel parameter blocks and host-side launchers (internal to
+// libverify_attn.so).  Every pointer is a device pointer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "va_internal.h"
+
+namespace va {
+
+struct PartialParams {
+  const void* q;              // [total_qo, h_q, D] bf16
+  const void* k_cache;        // [num_pages, h_kv, P, D] bf16 / fp8
+  const void* v_cache;
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  const int32_t* last_page_len;
+  const int32_t* qo_indptr;
+  const uint8_t* mask;        // nullable: causal drafts
+  const int32_t* mask_indptr;
+  void* out;                  // [total_qo, h_q, D] bf16
+  float* lse;                 // nullable
+  const WorkItem* items;
+  float* part_out;            // [part_rows, D]
+  float* part_lse;            // [part_rows]
+  int* status;                // device status word
+  int h_q, h_kv, group, page_size, log2_page, num_pages;
+  float scale_log2;           // sm_scale * k_scale * log2(e)
+  float scale_nat;            // sm_scale * k_scale
+  float v_scale;
+};
+
+struct MergeParams {
+  const MergeItem* items;
+  const float* part_out;
+  const float* part_lse;
+  const int32_t* qo_indptr;
+  void* out;
+  float* lse;                 // nullable
+  int h_q, group;
+};
+
+struct AppendParams {
+  const void* k_new;
+  const void* v_new;
+  const int32_t* append_indptr;
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  const int32_t* last_page_len;
+  void* k_cache;
+  void* v_cache;
+  int* status;                // nullable
+  int batch, h_kv, page_size, log2_page, num_pages, row_chunks;  // row_chunks: 16-byte chunks per row
+  int64_t total_new;
+};
+
+// Launchers: return the launch's cudaError_t (cudaErrorInvalidValue for a
+// variant that is not compiled).
+cudaError_t launch_partial_mma(const PartialParams& p, int kernel, int head_dim, bool kv_fp8,
+                               int n_items, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, int head_dim, int n_merge, int block_rows,
+                         cudaStream_t stream);
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
+}  // namespace va

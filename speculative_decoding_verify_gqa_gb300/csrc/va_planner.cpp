@@ -1,0 +1,234 @@
+// Host planner for paged-KV GQA verify attention (no CUDA calls).
+//
+// Restates the work decomposition of "flashmap 0.1.0 -- flashmap/sglang/
+// verify_attention.py" (one program per request, KV head, row block and kv
+// split; row blocks of up to 128 rows; splits sized to fill the GPU's SMs for
+// a few waves, each holding at least a minimum chunk of keys) and the
+// plan-once / run-many split of FlashInfer PR #286 "Separate Q and KV dtypes
+// for decode" (begin_forward reads the index arrays on the host, sizes the
+// split from the SM count, and caches the result for many forward calls).
+//
+// Differences from the page's planner, for this GPU: the split count is
+// chosen per (request, KV head, row block) from its own kv length rather
+// than one power of two for the whole batch, so a batch of very different
+// prefix lengths is cut into chunks of near-equal size; the verify tokens are
+// not a separate split (they are appended into the pages first and fall in the
+// last chunk); and the work list is sorted longest-first so the hardware
+// block scheduler packs the SMs evenly.
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "../../include/verify_attn.h"
+#include "va_internal.h"
+
+namespace va {
+
+namespace {
+
+constexpr int kWaves = 2;         // work items per CTA slot the plan aims for
+constexpr int kMaxTargetPerSm = 4;
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Unit {
+  int32_t b, row0, nrows, kv_end;
+};
+
+}  // namespace
+
+int check_common(int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int q_dtype,
+                 int kv_dtype) {
+  if (num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0)
+    return VA_ERR_INVALID_ARGUMENT;
+  if (num_qo_heads % num_kv_heads != 0) return VA_ERR_INVALID_ARGUMENT;
+  if (head_dim != 64 && head_dim != 128) return VA_ERR_UNSUPPORTED;
+  if (!is_pow2(page_size) || page_size > 256) return VA_ERR_UNSUPPORTED;
+  if (q_dtype != VA_DTYPE_BF16) return VA_ERR_UNSUPPORTED;
+  if (kv_dtype != VA_DTYPE_BF16 && kv_dtype != VA_DTYPE_FP8_E4M3) return VA_ERR_UNSUPPORTED;
+  return VA_OK;
+}
+
+int plan_bounds(int batch, int64_t total_qo, int num_qo_heads, int num_kv_heads, int head_dim,
+                int num_sms, size_t* plan_bytes, size_t* workspace_bytes) {
+  if (!plan_bytes || !workspace_bytes || batch < 0 || total_qo < 0 || num_sms <= 0 ||
+      num_qo_heads <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads || head_dim <= 0)
+    return VA_ERR_INVALID_ARGUMENT;
+  // Units: a request's G * L_b rows in blocks of >= 64 rows, per KV head.
+  int64_t units = ceil_div((int64_t)num_qo_heads * total_qo, 64) + (int64_t)num_kv_heads * batch;
+  int64_t target = (int64_t)kMaxTargetPerSm * num_sms;
+  // sum_u ceil(kv_end_u / C) <= W / C + units <= target + units.
+  int64_t items = target + units;
+  // Split units hold kv_end > C keys, so their split counts total < 2 W / C.
+  int64_t part_rows = 128 * 2 * target;
+  size_t pb = sizeof(PlanHeader) + (size_t)(items + units) * 32;
+  size_t ws = kWsAlign + (size_t)(items + units) * 32;
+  ws = align_up(ws, kWsAlign) + (size_t)part_rows * 4;
+  ws = align_up(ws, kWsAlign) + (size_t)part_rows * head_dim * 4;
+  *plan_bytes = pb;
+  *workspace_bytes = align_up(ws, kWsAlign);
+  return VA_OK;
+}
+
+int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t* last_page_len,
+              const int32_t* mask_indptr, int batch, int num_qo_heads, int num_kv_heads,
+              int head_dim, int page_size, int q_dtype, int kv_dtype, int has_mask, int num_sms,
+              const va_plan_options_t* opts, void* plan_h, size_t plan_bytes,
+              size_t* workspace_bytes) {
+  if (!workspace_bytes || !plan_h || batch < 0 || num_sms <= 0) return VA_ERR_INVALID_ARGUMENT;
+  if (!kv_indptr || !qo_indptr || (batch > 0 && !last_page_len)) return VA_ERR_INVALID_ARGUMENT;
+  if (has_mask && !mask_indptr) return VA_ERR_INVALID_ARGUMENT;
+  int rc = check_common(num_qo_heads, num_kv_heads, head_dim, page_size, q_dtype, kv_dtype);
+  if (rc) return rc;
+  va_plan_options_t o;
+  std::memset(&o, 0, sizeof(o));
+  if (opts) o = *opts;
+  for (int r : o.reserved)
+    if (r) return VA_ERR_INVALID_ARGUMENT;
+  if (o.max_splits < 0 || o.min_chunk < 0 || o.target_ctas < 0) return VA_ERR_INVALID_ARGUMENT;
+  if (o.kernel != VA_KERNEL_AUTO && o.kernel != VA_KERNEL_MMA_64 && o.kernel != VA_KERNEL_MMA_128)
+    return VA_ERR_INVALID_ARGUMENT;
+
+  const int G = num_qo_heads / num_kv_heads;
+  if (qo_indptr[0] < 0 || kv_indptr[0] < 0) return VA_ERR_INVALID_ARGUMENT;
+  int64_t max_rows = 0;
+  std::vector<int64_t> prefix(batch), qlen(batch);
+  for (int b = 0; b < batch; ++b) {
+    int64_t np = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
+    int64_t L = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
+    if (np < 0 || L < 0) return VA_ERR_INVALID_ARGUMENT;
+    int64_t kv_len = 0;
+    if (np > 0) {
+      if (last_page_len[b] < 1 || last_page_len[b] > page_size) return VA_ERR_INVALID_ARGUMENT;
+      kv_len = (np - 1) * page_size + last_page_len[b];
+    }
+    if (kv_len > INT32_MAX) return VA_ERR_UNSUPPORTED;
+    if (kv_len < L) return VA_ERR_INVALID_ARGUMENT;
+    if (has_mask) {
+      if (mask_indptr[b] < 0 || (int64_t)mask_indptr[b + 1] - mask_indptr[b] != L * L)
+        return VA_ERR_INVALID_ARGUMENT;
+    }
+    if ((int64_t)G * L > INT32_MAX) return VA_ERR_UNSUPPORTED;
+    prefix[b] = kv_len - L;
+    qlen[b] = L;
+    max_rows = std::max(max_rows, (int64_t)G * L);
+  }
+
+  int kernel = o.kernel;
+  if (kernel == VA_KERNEL_AUTO) kernel = max_rows <= 64 ? kKernelMma64 : kKernelMma128;
+  const int BM = kernel_rows(kernel);
+  const int TK = kTileKeys;
+
+  // Units of work: row blocks of each request (times each KV head).  A row
+  // block's last visible key is that of its last token: prefix + t_max.
+  std::vector<Unit> units;
+  int64_t W = 0;
+  int max_unit_rows = 0;
+  for (int b = 0; b < batch; ++b) {
+    int64_t R = (int64_t)G * qlen[b];
+    for (int64_t row0 = 0; row0 < R; row0 += BM) {
+      int32_t nrows = (int32_t)std::min<int64_t>(BM, R - row0);
+      int64_t tmax = (row0 + nrows - 1) / G;
+      int32_t kv_end = (int32_t)(prefix[b] + tmax + 1);
+      units.push_back({b, (int32_t)row0, nrows, kv_end});
+      W += (int64_t)kv_end * num_kv_heads;
+      max_unit_rows = std::max(max_unit_rows, (int)nrows);
+    }
+  }
+
+  // Split size.  Each split adds an fp32 partial of nrows x D written and
+  // read back by the merge, i.e. 8 * nrows bytes per head-dim element against
+  // 2 * es * C bytes of K/V read: a chunk of at least 8 * nrows / es keys keeps
+  // that traffic at or below half of the K/V bytes.
+  const int64_t slots = (int64_t)num_sms * kernel_ctas_per_sm(kernel);
+  int64_t target = o.target_ctas > 0 ? std::min<int64_t>(o.target_ctas, kMaxTargetPerSm * num_sms)
+                                     : std::min<int64_t>(kWaves * slots, kMaxTargetPerSm * num_sms);
+  const int es = kv_dtype == VA_DTYPE_FP8_E4M3 ? 1 : 2;
+  int64_t min_chunk = o.min_chunk > 0 ? o.min_chunk
+                                      : std::max<int64_t>(2 * TK, 8 * (int64_t)max_unit_rows / es);
+  min_chunk = ceil_div(min_chunk, TK) * TK;
+  int64_t chunk = std::max<int64_t>(min_chunk, ceil_div(ceil_div(W, std::max<int64_t>(target, 1)), TK) * TK);
+
+  struct Tmp {
+    WorkItem it;
+    int64_t cost;
+    int64_t order;
+  };
+  std::vector<Tmp> items;
+  std::vector<MergeItem> merges;
+  int64_t part_rows = 0;
+  int64_t order = 0;
+  for (const Unit& u : units) {
+    int64_t n = ceil_div(u.kv_end, chunk);
+    if (o.max_splits > 0) n = std::min<int64_t>(n, o.max_splits);
+    n = std::max<int64_t>(n, 1);
+    int64_t cu = ceil_div(ceil_div(u.kv_end, n), TK) * TK;
+    n = ceil_div(u.kv_end, cu);
+    for (int h = 0; h < num_kv_heads; ++h) {
+      int64_t base = part_rows;
+      if (n > 1) {
+        merges.push_back({u.b, h, u.row0, u.nrows, (int32_t)base, (int32_t)n, 0, 0});
+        part_rows += n * u.nrows;
+      }
+      for (int64_t s = 0; s < n; ++s) {
+        int64_t lo = s * cu, hi = std::min<int64_t>(lo + cu, u.kv_end);
+        WorkItem w{u.b, h, u.row0, u.nrows, (int32_t)lo, (int32_t)hi,
+                   n > 1 ? (int32_t)(base + s * u.nrows) : -1, 0};
+        items.push_back({w, (hi - lo) * (int64_t)(u.nrows + 16), order++});
+      }
+    }
+  }
+  if (part_rows > INT32_MAX) return VA_ERR_UNSUPPORTED;
+  std::stable_sort(items.begin(), items.end(),
+                   [](const Tmp& a, const Tmp& b) { return a.cost > b.cost; });
+
+  size_t need = sizeof(PlanHeader) + items.size() * sizeof(WorkItem) +
+                merges.size() * sizeof(MergeItem);
+  if (plan_bytes < need) {
+    *workspace_bytes = need;
+    return VA_ERR_PLAN_BUFFER_TOO_SMALL;
+  }
+  PlanHeader hd;
+  std::memset(&hd, 0, sizeof(hd));
+  hd.magic = kPlanMagic;
+  hd.version = kPlanVersion;
+  hd.batch = batch;
+  hd.h_q = num_qo_heads;
+  hd.h_kv = num_kv_heads;
+  hd.head_dim = head_dim;
+  hd.page_size = page_size;
+  hd.q_dtype = q_dtype;
+  hd.kv_dtype = kv_dtype;
+  hd.has_mask = has_mask ? 1 : 0;
+  hd.group = G;
+  hd.kernel = kernel;
+  hd.block_rows = BM;
+  hd.tile_keys = TK;
+  hd.n_items = (int32_t)items.size();
+  hd.n_merge = (int32_t)merges.size();
+  hd.n_units = (int32_t)units.size();
+  hd.num_sms = num_sms;
+  hd.total_qo = batch > 0 ? qo_indptr[batch] : 0;
+  hd.part_rows = part_rows;
+  hd.chunk = chunk;
+  hd.off_status = 0;
+  hd.off_items = kWsAlign;
+  hd.off_merge = hd.off_items + items.size() * sizeof(WorkItem);
+  hd.off_part_lse = align_up(hd.off_merge + merges.size() * sizeof(MergeItem), kWsAlign);
+  hd.off_part_out = align_up(hd.off_part_lse + (size_t)part_rows * 4, kWsAlign);
+  hd.ws_bytes = align_up(hd.off_part_out + (size_t)part_rows * head_dim * 4, kWsAlign);
+  hd.plan_bytes = need;
+
+  char* dst = static_cast<char*>(plan_h);
+  std::memcpy(dst, &hd, sizeof(hd));
+  WorkItem* wi = reinterpret_cast<WorkItem*>(dst + sizeof(hd));
+  for (size_t i = 0; i < items.size(); ++i) wi[i] = items[i].it;
+  if (!merges.empty())
+    std::memcpy(wi + items.size(), merges.data(), merges.size() * sizeof(MergeItem));
+  *workspace_bytes = hd.ws_bytes;
+  return VA_OK;
+}
+
+}  // namespace va

@@ -191,7 +191,10 @@ def make_workload(name: str, seed: int = 0, **overrides) -> Workload:
 def make_custom(name="custom", seed=0, batch=2, h_q=4, h_kv=2, d=64, page_size=16,
                 kv_dtype=BF16, prefix=("fixed", [37, 70]), qo=("fixed", [5, 5]),
                 mask="causal", pool_pages=None, pool_factor=1.25, sm_scale=None,
-                shuffle_pages=True, value_std=1.0) -> Workload:
+                shuffle_pages=True, value_std=1.0, with_values=True) -> Workload:
+    """A workload from explicit parameters.  with_values=False draws only the
+    tables (lengths, trees, pages; q / k / v come last in the draw order, so the
+    tables are the same either way) and leaves q / k_tok / v_tok empty."""
     gen = torch.Generator().manual_seed(seed)
     prefix_lens = _draw_lengths(prefix, batch, gen)
     qo_lens = _draw_lengths(qo, batch, gen)
@@ -246,6 +249,8 @@ def make_custom(name="custom", seed=0, batch=2, h_q=4, h_kv=2, d=64, page_size=1
 
     total_qo = int(qo_indptr[-1])
     total_tok = int(tok_indptr[-1])
+    if not with_values:
+        total_qo = total_tok = 0
     qf = torch.randn((total_qo, h_q, d), generator=gen) * value_std
     q = _bf16_bits(qf)
     del qf

@@ -1,0 +1,250 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/verify_attn.h declares, and the host planner's work lists cover each
+request's rows and keys exactly once; argument validation returns the
+documented status codes without touching a device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synthetic
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "verify_attn.h")
+
+
+@pytest.fixture(scope="module")
+def va():
+    import __graft_entry__
+    from speculative_decoding_verify_gqa_gb300 import build as b
+    b.build()
+    import speculative_decoding_verify_gqa_gb300 as m
+    m.lib()
+    return m
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while", "for", "sizeof")))
+
+
+def test_header_declares_the_boundary_calls():
+    names = _declared_functions()
+    for must in ("verify_attn_plan", "verify_attn_run", "paged_kv_append",
+                 "verify_attn_plan_host", "verify_attn_partial", "verify_attn_merge",
+                 "verify_attn_device_status", "verify_attn_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(va):
+    lib = ctypes.CDLL(va.library_path)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(va):
+    assert va.status_string(0) == "ok"
+    for code in range(-7, 0):
+        assert va.status_string(code) != "unknown status"
+    assert va.status_string(-99) == "unknown status"
+
+
+# ------------------------------------------------------------------ planner
+
+def _tables(seed, batch, G, h_kv, page_size, max_prefix, max_L, masked):
+    rng = np.random.default_rng(seed)
+    prefix = rng.integers(0, max_prefix + 1, size=batch)
+    L = rng.integers(0, max_L + 1, size=batch)
+    kv_len = prefix + L
+    pages = (kv_len + page_size - 1) // page_size
+    kv_indptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    last = np.where(pages > 0, kv_len - (pages - 1) * page_size, 0).astype(np.int32)
+    qo_indptr = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    mask_indptr = np.concatenate([[0], np.cumsum(L * L)]).astype(np.int32) if masked else None
+    return dict(prefix=prefix, L=L, kv_len=kv_len, kv_indptr=kv_indptr, last=last,
+                qo_indptr=qo_indptr, mask_indptr=mask_indptr, h_q=G * h_kv, h_kv=h_kv,
+                G=G, page_size=page_size)
+
+
+def _check_cover(va, t, plan):
+    hd = plan.header()
+    items = plan.items()
+    merges = plan.merges()
+    assert hd["n_items"] == len(items) and hd["n_merge"] == len(merges)
+    BM = hd["block_rows"]
+    G = t["G"]
+    units = {}
+    for it in items:
+        b, h, row0, nrows, lo, hi, part_row, _ = (int(x) for x in it)
+        assert 0 <= b < len(t["L"]) and 0 <= h < t["h_kv"]
+        assert 0 < nrows <= BM and row0 % BM == 0
+        assert lo % 64 == 0 and lo < hi
+        units.setdefault((b, h, row0, nrows), []).append((lo, hi, part_row))
+    for b in range(len(t["L"])):
+        R = G * int(t["L"][b])
+        for h in range(t["h_kv"]):
+            rows = sorted((k[2], k[3]) for k in units if k[0] == b and k[1] == h)
+            pos = 0
+            for row0, nrows in rows:
+                assert row0 == pos
+                pos += nrows
+            assert pos == R
+    merge_by_unit = {(int(m[0]), int(m[1]), int(m[2]), int(m[3])): m for m in merges}
+    used = np.zeros(max(hd["part_rows"], 1), dtype=np.int32)
+    for (b, h, row0, nrows), chunks in units.items():
+        chunks.sort()
+        tmax = (row0 + nrows - 1) // G
+        kv_end = int(t["prefix"][b]) + tmax + 1
+        pos = 0
+        for lo, hi, _ in chunks:
+            assert lo == pos
+            pos = hi
+        assert pos == kv_end
+        if len(chunks) == 1:
+            assert chunks[0][2] == -1 and (b, h, row0, nrows) not in merge_by_unit
+        else:
+            m = merge_by_unit[(b, h, row0, nrows)]
+            assert int(m[5]) == len(chunks)
+            for s, (lo, hi, part_row) in enumerate(chunks):
+                assert part_row == int(m[4]) + s * nrows
+                used[part_row:part_row + nrows] += 1
+    assert used.max(initial=0) <= 1
+    assert used.sum() == hd["part_rows"]
+
+
+@pytest.mark.parametrize("case", [
+    dict(seed=1, batch=5, G=4, h_kv=2, page_size=16, max_prefix=300, max_L=17, masked=True),
+    dict(seed=2, batch=64, G=8, h_kv=8, page_size=16, max_prefix=8192, max_L=8, masked=False),
+    dict(seed=3, batch=3, G=8, h_kv=1, page_size=1, max_prefix=50, max_L=40, masked=False),
+    dict(seed=4, batch=7, G=1, h_kv=4, page_size=64, max_prefix=2000, max_L=200, masked=True),
+    dict(seed=5, batch=1, G=16, h_kv=1, page_size=256, max_prefix=0, max_L=300, masked=False),
+    dict(seed=6, batch=4, G=2, h_kv=3, page_size=8, max_prefix=5, max_L=0, masked=False),
+])
+@pytest.mark.parametrize("num_sms", [152, 7])
+def test_plan_covers_rows_and_keys_exactly_once(va, case, num_sms):
+    t = _tables(**case)
+    for opts in (dict(), dict(max_splits=1), dict(max_splits=3, min_chunk=64),
+                 dict(target_ctas=10000)):
+        plan = va.verify_attn_plan_host(t["kv_indptr"], t["qo_indptr"], t["last"],
+                                        t["mask_indptr"], t["h_q"], t["h_kv"], 128,
+                                        t["page_size"], num_sms=num_sms, **opts)
+        _check_cover(va, t, plan)
+        if opts.get("max_splits") == 1:
+            assert plan.header()["n_merge"] == 0
+        pb, wb = va.verify_attn_plan_bounds(len(t["L"]), int(t["qo_indptr"][-1]), t["h_q"],
+                                            t["h_kv"], 128, num_sms)
+        assert plan.workspace_bytes <= wb
+        assert 184 + 32 * (plan.header()["n_items"] + plan.header()["n_merge"]) <= pb
+
+
+@pytest.mark.parametrize("name", synthetic.WORKLOAD_ORDER)
+def test_plans_of_the_named_workloads(va, name):
+    wl = synthetic.make_workload(name, with_values=False)
+    t = dict(prefix=wl.prefix_lens, L=wl.qo_lens, G=wl.group, h_kv=wl.h_kv)
+    plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
+                                    wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                    kv_dtype=wl.kv_dtype, num_sms=152)
+    _check_cover(va, t, plan)
+    hd = plan.header()
+    # kernel variant follows the rows per KV head (G * L)
+    assert hd["kernel"] == (1 if (wl.group * wl.qo_lens).max() <= 64 else 2)
+
+
+def test_plan_items_sorted_longest_first(va):
+    wl = synthetic.make_workload("codellama34b_chain_verify", with_values=False)
+    plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, None,
+                                    wl.h_q, wl.h_kv, wl.d, wl.page_size, num_sms=152)
+    it = plan.items()
+    cost = (it[:, 5] - it[:, 4]) * (it[:, 3] + 16)
+    assert np.all(np.diff(cost) <= 0)
+
+
+# ------------------------------------------------------------------ validation
+
+def _plan_rc(va, kv_indptr, qo_indptr, last, mask_indptr, h_q=4, h_kv=2, d=128, P=16,
+             kv_dtype=0, has_mask=None, plan_bytes=1 << 16, **opts):
+    lib = va.lib()
+    host = np.zeros(plan_bytes, np.uint8)
+    need = ctypes.c_size_t(0)
+    o = va._options(**opts)
+    arrs = [None if a is None else np.ascontiguousarray(a, np.int32)
+            for a in (kv_indptr, qo_indptr, last, mask_indptr)]
+    if has_mask is None:
+        has_mask = mask_indptr is not None
+    return lib.verify_attn_plan_host(*[va._hp(a) for a in arrs], len(arrs[1]) - 1, h_q, h_kv, d,
+                                     P, 0, kv_dtype, int(has_mask), 152, ctypes.byref(o),
+                                     va._hp(host), plan_bytes, ctypes.byref(need))
+
+
+def test_plan_validation_codes(va):
+    ok = ([0, 2], [0, 3], [5], None)
+    assert _plan_rc(va, *ok) == 0
+    assert _plan_rc(va, *ok, h_q=5, h_kv=2) == -1          # h_q % h_kv
+    assert _plan_rc(va, *ok, d=96) == -2                   # head_dim
+    assert _plan_rc(va, *ok, P=12) == -2                   # page size not a power of two
+    assert _plan_rc(va, *ok, P=512) == -2
+    assert _plan_rc(va, *ok, kv_dtype=7) == -2
+    assert _plan_rc(va, [0, 1], [0, 3], [2], None) == -1   # kv_len 2 < L 3
+    assert _plan_rc(va, [0, 2], [0, 3], [0], None) == -1   # last_page_len 0 with pages
+    assert _plan_rc(va, [0, 2], [0, 3], [17], None) == -1  # last_page_len > page size
+    assert _plan_rc(va, [0, 2], [0, 3], [5], [0, 8]) == -1  # mask block != L*L
+    assert _plan_rc(va, [0, 2], [0, 3], [5], [0, 9]) == 0
+    assert _plan_rc(va, [0, 2], [0, 3], [5], None, has_mask=1) == -1
+    assert _plan_rc(va, *ok, plan_bytes=64) == -7
+    assert _plan_rc(va, [0, 2, 1], [0, 3, 3], [5, 1], None) == -1  # decreasing indptr
+    assert _plan_rc(va, *ok, max_splits=-1) == -1
+    assert _plan_rc(va, *ok, kernel=9) == -1
+
+
+def test_empty_batches_plan_to_nothing(va):
+    plan = va.verify_attn_plan_host([0], [0], [], None, 4, 2, 64, 16, num_sms=152)
+    assert plan.header()["n_items"] == 0 and plan.launches() == 0
+    plan = va.verify_attn_plan_host([0, 3, 3], [0, 0, 0], [7, 0], None, 4, 2, 64, 16,
+                                    num_sms=152)
+    assert plan.header()["n_items"] == 0
+
+
+def test_run_rejects_mismatched_plan_without_touching_the_device(va):
+    lib = va.lib()
+    plan = va.verify_attn_plan_host([0, 2], [0, 3], [5], None, 4, 2, 128, 16, num_sms=152)
+    fake = ctypes.c_void_p(4096)  # never dereferenced: the checks fail first
+    args = [fake] * 9
+    args[7] = None  # mask
+    args[8] = None
+    rc = lib.verify_attn_run(*args, 8, 2, 128, 16, 0.0, 1.0, 1.0, fake, None, 10,
+                             va._hp(plan.host), fake, 1 << 30, None)
+    assert rc == -4  # num_qo_heads differs from the plan
+    rc = lib.verify_attn_run(*args, 4, 2, 128, 16, 0.0, 1.0, 1.0, fake, None, 10,
+                             None, fake, 1 << 30, None)
+    assert rc == -1  # no plan
+    rc = lib.verify_attn_run(*args, 4, 2, 128, 16, 0.0, 1.0, 1.0, fake, None, 10,
+                             va._hp(plan.host), fake, 16, None)
+    assert rc == -3  # workspace too small
+    rc = lib.verify_attn_run(*args, 4, 2, 128, 16, 0.0, float("nan"), 1.0, fake, None, 10,
+                             va._hp(plan.host), fake, 1 << 30, None)
+    assert rc == -1  # non-finite scale
+    rc = lib.verify_attn_run(*args, 4, 2, 128, 16, 0.0, 1.0, -2.0, fake, None, 10,
+                             va._hp(plan.host), fake, 1 << 30, None)
+    assert rc == -1  # negative scale
+    margs = list(args)
+    margs[7] = fake
+    rc = lib.verify_attn_run(*margs, 4, 2, 128, 16, 0.0, 1.0, 1.0, fake, None, 10,
+                             va._hp(plan.host), fake, 1 << 30, None)
+    assert rc == -4  # mask given to a maskless plan
+
+
+def test_append_validation_without_device(va):
+    lib = va.lib()
+    fake = ctypes.c_void_p(4096)
+    P = [fake] * 8
+    assert lib.paged_kv_append(*P, 1, 2, 96, 16, 10, 0, 5, None, None) == -2   # head_dim
+    assert lib.paged_kv_append(*P, 1, 2, 128, 16, 10, 3, 5, None, None) == -2  # dtype
+    assert lib.paged_kv_append(*P, 1, 2, 128, 16, 10, 0, 0, None, None) == 0   # nothing to do
+    assert lib.paged_kv_append(*P, 1, 2, 128, 16, 10, 0, -1, None, None) == -1
+    Q = list(P)
+    Q[0] = ctypes.c_void_p(4097)  # misaligned
+    assert lib.paged_kv_append(*Q, 1, 2, 128, 16, 10, 0, 5, None, None) == -1

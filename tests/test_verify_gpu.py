@@ -1,0 +1,294 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs.  Tolerances: max |out - oracle| <= 1e-2 and
+max |lse - oracle| <= 1e-3 (bf16 inputs, fp32 accumulation); the paged
+append is compared bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from gpu_util import DeviceWorkload, compare, host_out
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def va():
+    import __graft_entry__
+    __graft_entry__.build()
+    import speculative_decoding_verify_gqa_gb300 as m
+    return m
+
+
+# ------------------------------------------------------------------ append
+
+APPEND_CASES = [
+    dict(batch=3, h_q=4, h_kv=2, d=64, page_size=16, prefix=("fixed", [37, 0, 70]),
+         qo=("fixed", [5, 3, 1])),
+    dict(batch=2, h_q=8, h_kv=8, d=128, page_size=1, prefix=("fixed", [5, 9]),
+         qo=("fixed", [4, 2])),
+    dict(batch=2, h_q=4, h_kv=1, d=128, page_size=64, prefix=("fixed", [100, 1]),
+         qo=("fixed", [30, 64]), kv_dtype=synthetic.FP8),
+    dict(batch=4, h_q=2, h_kv=2, d=64, page_size=256, prefix=("fixed", [0, 255, 256, 3]),
+         qo=("fixed", [1, 1, 2, 0]), kv_dtype=synthetic.FP8),
+]
+
+
+@pytest.mark.parametrize("case", APPEND_CASES, ids=range(len(APPEND_CASES)))
+def test_append_is_bit_exact(va, case):
+    wl = synthetic.make_custom(seed=5, **case)
+    dw = DeviceWorkload(wl)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dw.append_drafts(status=status)
+    torch.cuda.synchronize()
+    kc, vc = oracle.build_cache(wl)
+    raw = np.uint8 if wl.kv_dtype == synthetic.FP8 else np.uint16
+    gk = dw.k_cache.view(torch.uint8).cpu().numpy().view(raw)
+    gv = dw.v_cache.view(torch.uint8).cpu().numpy().view(raw)
+    assert np.array_equal(gk.reshape(kc.shape), kc)
+    assert np.array_equal(gv.reshape(vc.shape), vc)
+    assert int(status.item()) == 0
+
+
+def test_append_flags_bad_page_and_writes_the_rest(va):
+    wl = synthetic.make_custom(batch=2, h_q=4, h_kv=2, d=64, page_size=16,
+                               prefix=("fixed", [20, 20]), qo=("fixed", [3, 3]), seed=9)
+    dw = DeviceWorkload(wl, append=False)
+    bad = wl.kv_indices.copy()
+    bad[wl.kv_indptr[1]] = wl.num_pages + 5      # request 1's first page id is out of range
+    dw.kv_indices = torch.from_numpy(bad).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dw.append_drafts(status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 1  # VA_DEV_BAD_PAGE: the tokens of request 1 that map there
+    # request 0's drafts landed
+    kc = dw.k_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+    kn, _ = wl.new_tokens()
+    pages = wl.kv_indices[:wl.kv_indptr[1]]
+    for i in range(3):
+        pos = 20 + i
+        assert np.array_equal(kc[pages[pos // 16], :, pos % 16], kn[i])
+
+
+# ------------------------------------------------------------------ verify, small
+
+SMALL = [
+    ("chain_d64", dict(batch=2, h_q=4, h_kv=2, d=64, prefix=("fixed", [37, 70]),
+                       qo=("fixed", [5, 5]), mask="causal")),
+    ("tree_d128", dict(batch=3, h_q=8, h_kv=2, d=128, prefix=("fixed", [100, 513, 7]),
+                       qo=("fixed", [17, 9, 4]), mask="tree")),
+    ("random_mask", dict(batch=2, h_q=4, h_kv=4, d=64, prefix=("fixed", [60, 200]),
+                         qo=("fixed", [12, 33]), mask="random")),
+    ("decode_L1", dict(batch=5, h_q=32, h_kv=8, d=128, prefix=("fixed", [1, 15, 16, 17, 900]),
+                       qo=("fixed", [1, 1, 1, 1, 1]), mask="causal")),
+    ("mqa_g16", dict(batch=2, h_q=16, h_kv=1, d=128, prefix=("fixed", [300, 64]),
+                     qo=("fixed", [3, 8]), mask="tree")),
+    ("prefill_no_prefix", dict(batch=3, h_q=8, h_kv=2, d=128, prefix=("fixed", [0, 0, 0]),
+                               qo=("fixed", [300, 17, 64]), mask="causal")),
+    ("fp8_tree", dict(batch=2, h_q=8, h_kv=2, d=128, prefix=("fixed", [700, 33]),
+                      qo=("fixed", [64, 20]), mask="tree", kv_dtype=synthetic.FP8)),
+    ("fp8_d64_chain", dict(batch=2, h_q=4, h_kv=2, d=64, prefix=("fixed", [99, 1000]),
+                           qo=("fixed", [3, 8]), mask="causal", kv_dtype=synthetic.FP8)),
+    ("page1", dict(batch=2, h_q=4, h_kv=2, d=128, page_size=1, prefix=("fixed", [50, 3]),
+                   qo=("fixed", [4, 6]), mask="tree")),
+    ("page4", dict(batch=2, h_q=4, h_kv=2, d=64, page_size=4, prefix=("fixed", [77, 0]),
+                   qo=("fixed", [9, 5]), mask="causal")),
+    ("page256", dict(batch=2, h_q=4, h_kv=2, d=128, page_size=256, prefix=("fixed", [600, 10]),
+                     qo=("fixed", [4, 6]), mask="tree")),
+    ("empty_request", dict(batch=3, h_q=4, h_kv=2, d=128, prefix=("fixed", [40, 30, 20]),
+                           qo=("fixed", [3, 0, 2]), mask="causal")),
+    ("fully_masked_rows", dict(batch=2, h_q=4, h_kv=2, d=64, prefix=("fixed", [0, 5]),
+                               qo=("fixed", [4, 3]), mask="none_visible")),
+    ("full_mask", dict(batch=1, h_q=4, h_kv=2, d=128, prefix=("fixed", [10]),
+                       qo=("fixed", [40]), mask="full")),
+    ("g3_many_rows", dict(batch=2, h_q=6, h_kv=2, d=128, prefix=("fixed", [129, 1]),
+                          qo=("fixed", [50, 45]), mask="tree")),
+]
+
+
+@pytest.mark.parametrize("name,case", SMALL, ids=[s[0] for s in SMALL])
+def test_small_cases_match_oracle(va, name, case):
+    wl = synthetic.make_custom(seed=11, **case)
+    dw = DeviceWorkload(wl)
+    out, lse, plan = dw.run()
+    torch.cuda.synchronize()
+    compare(wl, out, lse)
+    assert va.verify_attn_device_status(plan) == 0
+
+
+@pytest.mark.parametrize("opts", [dict(max_splits=1), dict(min_chunk=64, target_ctas=2000),
+                                  dict(kernel=1), dict(kernel=2), dict(max_splits=2)])
+def test_forced_plans_match_oracle(va, opts):
+    wl = synthetic.make_custom(batch=3, h_q=8, h_kv=2, d=128, prefix=("fixed", [1000, 3000, 50]),
+                               qo=("fixed", [6, 2, 7]), mask="tree", seed=13)
+    dw = DeviceWorkload(wl)
+    out, lse, plan = dw.run(**opts)
+    torch.cuda.synchronize()
+    if opts.get("max_splits") == 1:
+        assert plan.header()["n_merge"] == 0
+    if "target_ctas" in opts:
+        assert plan.header()["n_merge"] > 0
+    compare(wl, out, lse)
+
+
+def test_split_and_unsplit_agree(va):
+    wl = synthetic.make_workload("llama3_8b_tree_verify")
+    dw = DeviceWorkload(wl)
+    o1, l1, p1 = dw.run(max_splits=1)
+    o2, l2, p2 = dw.run()
+    torch.cuda.synchronize()
+    assert p1.header()["n_merge"] == 0 and p2.header()["n_merge"] > 0
+    assert float((o1.float() - o2.float()).abs().max()) <= 1e-2
+    assert float((l1 - l2).abs().max()) <= 1e-3
+    compare(wl, o1, l1)
+
+
+def test_page_placement_does_not_change_bits(va):
+    base = dict(batch=3, h_q=8, h_kv=2, d=128, prefix=("fixed", [300, 47, 1000]),
+                qo=("fixed", [5, 9, 2]), mask="tree", seed=17)
+    w1 = synthetic.make_custom(shuffle_pages=True, **base)
+    w2 = synthetic.make_custom(shuffle_pages=False, **base)
+    d1, d2 = DeviceWorkload(w1), DeviceWorkload(w2)
+    o1, l1, _ = d1.run()
+    o2, l2, _ = d2.run()
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+def test_chain_mask_equals_causal_on_gpu(va):
+    base = dict(batch=2, h_q=8, h_kv=2, d=128, prefix=("fixed", [200, 31]),
+                qo=("fixed", [8, 13]), seed=19)
+    wc = synthetic.make_custom(mask="chain", **base)
+    wn = synthetic.make_custom(mask="causal", **base)
+    oc, lc, _ = DeviceWorkload(wc).run()
+    on, ln, _ = DeviceWorkload(wn).run()
+    torch.cuda.synchronize()
+    assert torch.equal(oc.view(torch.int16), on.view(torch.int16))
+    assert torch.equal(lc, ln)
+
+
+def test_partial_then_merge_equals_run(va):
+    wl = synthetic.make_workload("llama3_8b_tree_verify")
+    dw = DeviceWorkload(wl)
+    out1, lse1, plan = dw.run()
+    out2 = torch.empty_like(out1)
+    lse2 = torch.empty_like(lse1)
+    va.verify_attn_partial(dw.q, dw.k_cache, dw.v_cache, dw.kv_indptr, dw.kv_indices,
+                           dw.last_page_len, dw.qo_indptr, dw.mask, dw.mask_indptr, plan,
+                           sm_scale=wl.sm_scale, out=out2, lse=lse2)
+    va.verify_attn_merge(dw.qo_indptr, plan, out2, lse2)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+
+
+def test_lse_may_be_omitted(va):
+    wl = synthetic.make_workload("tiny_verify")
+    dw = DeviceWorkload(wl)
+    out1, lse1, plan = dw.run()
+    out2, none = va.verify_attn_run(dw.q, dw.k_cache, dw.v_cache, dw.kv_indptr, dw.kv_indices,
+                                    dw.last_page_len, dw.qo_indptr, None, None, plan,
+                                    sm_scale=wl.sm_scale, want_lse=False)
+    torch.cuda.synchronize()
+    assert none is None
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_empty_batch_is_a_no_op(va):
+    wl = synthetic.make_custom(batch=2, h_q=4, h_kv=2, d=64, prefix=("fixed", [10, 20]),
+                               qo=("fixed", [0, 0]), mask="causal", seed=21)
+    dw = DeviceWorkload(wl)
+    out = torch.zeros(0, 4, 64, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(0, 4, dtype=torch.float32, device="cuda")
+    plan = dw.plan()
+    assert plan.launches() == 0
+    dw.run(plan=plan, out=out, lse=lse)
+    torch.cuda.synchronize()
+
+
+def test_bad_page_id_is_flagged_not_read(va):
+    wl = synthetic.make_custom(batch=2, h_q=4, h_kv=2, d=128, prefix=("fixed", [100, 100]),
+                               qo=("fixed", [3, 3]), mask="causal", seed=23)
+    dw = DeviceWorkload(wl)
+    bad = wl.kv_indices.copy()
+    bad[wl.kv_indptr[1] + 1] = 1 << 30          # request 1, second page
+    dw.kv_indices = torch.from_numpy(bad).cuda()
+    out, lse, plan = dw.run()
+    torch.cuda.synchronize()
+    assert va.verify_attn_device_status(plan) & 1
+    assert torch.isfinite(out.float()).all()
+    # request 0 is unaffected
+    rows = np.arange(3 * wl.h_q, dtype=np.int32)
+    o, l = host_out(out, lse, wl.d)
+    ro, rl = oracle.verify_attn_workload(wl, rows=rows)
+    assert np.abs(o[rows] - ro).max() <= 1e-2 and np.abs(l[rows] - rl).max() <= 1e-3
+
+
+def test_stale_plan_is_flagged(va):
+    wl = synthetic.make_custom(batch=2, h_q=4, h_kv=2, d=64, prefix=("fixed", [40, 40]),
+                               qo=("fixed", [3, 3]), mask="causal", seed=25)
+    dw = DeviceWorkload(wl)
+    plan = dw.plan()
+    short = wl.qo_indptr.copy()
+    short[2] = short[1] + 1                      # request 1 now has 1 token, the plan says 3
+    dw.qo_indptr = torch.from_numpy(short).cuda()
+    dw.run(plan=plan)
+    torch.cuda.synchronize()
+    assert va.verify_attn_device_status(plan) & 2
+
+
+def test_graph_capture_of_append_and_run(va):
+    wl = synthetic.make_workload("llama3_8b_tree_verify")
+    dw = DeviceWorkload(wl)
+    plan = dw.plan()
+    out = torch.empty_like(dw.q)
+    lse = torch.empty(dw.q.shape[:2], dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dw.append_drafts()
+        dw.run(plan=plan, out=out, lse=lse)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dw.append_drafts()
+        dw.run(plan=plan, out=out, lse=lse)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    compare(wl, out, lse, rows=synthetic.sample_rows(wl, 200))
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+@pytest.mark.parametrize("name", synthetic.WORKLOAD_ORDER)
+def test_named_workload_matches_oracle(va, name):
+    """Each named workload at full size, in the launch configuration the
+    benchmark times: every row for the tiny case, a seeded sample of rows
+    (with each request's first and last token) for the others, plus
+    properties of every row."""
+    wl = synthetic.make_workload(name)
+    dw = DeviceWorkload(wl)
+    out, lse, plan = dw.run()
+    torch.cuda.synchronize()
+    assert va.verify_attn_device_status(plan) == 0
+    of = out.float()
+    assert torch.isfinite(of).all() and torch.isfinite(lse).all()
+    fp8 = wl.kv_dtype == synthetic.FP8
+    v_vals = torch.from_numpy(wl.v_tok.view(np.uint8 if fp8 else np.int16)).view(
+        torch.float8_e4m3fn if fp8 else torch.bfloat16)
+    vmax = float(v_vals.float().abs().max()) * wl.v_scale
+    assert float(of.abs().max()) <= vmax * (1 + 2 ** -7)   # a convex combination of V rows
+    rows = None if name == "tiny_verify" else synthetic.sample_rows(wl, 256)
+    caches = None
+    if wl.kv_dtype == synthetic.FP8 or name != "tiny_verify":
+        raw = np.uint8 if wl.kv_dtype == synthetic.FP8 else np.uint16
+        caches = (dw.k_cache.view(torch.uint8).cpu().numpy().view(raw),
+                  dw.v_cache.view(torch.uint8).cpu().numpy().view(raw))
+        ok, ov = oracle.build_cache(wl)
+        # the device pool (written by the append kernel) is the oracle's pool, bit for bit
+        assert np.array_equal(caches[0], ok) and np.array_equal(caches[1], ov)
+        caches = (ok, ov)
+    compare(wl, out, lse, rows=rows, caches=caches)
