@@ -118,6 +118,8 @@ typedef struct {
 #define VA_KERNEL_AUTO 0
 #define VA_KERNEL_MMA_64 1      /* warp-level tensor cores, 64-row blocks, 4 warps */
 #define VA_KERNEL_MMA_128 2     /* warp-level tensor cores, 128-row blocks, 8 warps */
+#define VA_KERNEL_TC_128 3      /* tcgen05 tensor cores + TMA, 128-row blocks; needs head_dim
+                                   128, bf16 KV, page_size a multiple of 16, 128 % G == 0 */
 
 /* Name of a status code (static string). */
 const char* verify_attn_status_string(int status);

@@ -17,30 +17,53 @@ namespace {
 template <int D>
 __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) {
   constexpr int V = D / 32;
+  constexpr int CH = 8;  // splits whose loads are issued together
   const MergeItem it = p.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * 4 + warp;
+  grid_dependency_wait();  // the partials come from the preceding split kernel
   if (r >= it.nrows) return;
   const float* lse_base = p.part_lse + it.part_row0 + r;
+  // Every lane reads one split's LSE (32 at a time), then a warp max.
   float m = -INFINITY;
-  for (int s = 0; s < it.nsplit; ++s) m = fmaxf(m, lse_base[(size_t)s * it.nrows]);
+  for (int s0 = 0; s0 < it.nsplit; s0 += 32) {
+    const int s = s0 + lane;
+    if (s < it.nsplit) m = fmaxf(m, lse_base[(size_t)s * it.nrows]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
   float den = 0.f;
   if (m != -INFINITY) {
-    for (int s = 0; s < it.nsplit; ++s) {
-      const float ls = lse_base[(size_t)s * it.nrows];
-      if (ls == -INFINITY) continue;
-      const float w = ex2((ls - m) * kLog2e);
-      den += w;
-      const float* src = p.part_out + ((size_t)it.part_row0 + (size_t)s * it.nrows + r) * D + lane * V;
-      if constexpr (V == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * x.x; acc[1] += w * x.y;
+    for (int s0 = 0; s0 < it.nsplit; s0 += CH) {
+      float ls[CH];
+      float x[CH][V];
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int s = s0 + c;
+        ls[c] = -INFINITY;
+        if (s < it.nsplit) {
+          ls[c] = lse_base[(size_t)s * it.nrows];
+          const float* src =
+              p.part_out + ((size_t)it.part_row0 + (size_t)s * it.nrows + r) * D + lane * V;
+          if constexpr (V == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            x[c][0] = v.x; x[c][1] = v.y; x[c][2] = v.z; x[c][3] = v.w;
+          } else {
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            x[c][0] = v.x; x[c][1] = v.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        if (ls[c] == -INFINITY) continue;  // an empty split carries no mass
+        const float w = ex2((ls[c] - m) * kLog2e);
+        den += w;
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += w * x[c][i];
       }
     }
   }
@@ -113,11 +136,11 @@ cudaError_t launch_merge(const MergeParams& p, int head_dim, int n_merge, int bl
   dim3 grid(n_merge, (block_rows + 3) / 4);
   void* args[] = {const_cast<MergeParams*>(&p)};
   if (head_dim == 128)
-    return cudaLaunchKernel(reinterpret_cast<const void*>(verify_merge_kernel<128>), grid,
-                            dim3(128), args, 0, stream);
+    return launch_kernel(reinterpret_cast<const void*>(verify_merge_kernel<128>), grid,
+                         dim3(128), 0, stream, args, /*pdl=*/true);
   if (head_dim == 64)
-    return cudaLaunchKernel(reinterpret_cast<const void*>(verify_merge_kernel<64>), grid,
-                            dim3(128), args, 0, stream);
+    return launch_kernel(reinterpret_cast<const void*>(verify_merge_kernel<64>), grid,
+                         dim3(128), 0, stream, args, /*pdl=*/true);
   return cudaErrorInvalidValue;
 }
 

@@ -42,8 +42,10 @@ struct MmaCfg {
   static constexpr int TILE_BYTES = BN * KVROW;   // one K (or V) tile in cache format
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int CONV_BYTES = FP8 ? 2 * BN * QROW : 0;
-  static constexpr int SMEM = Q_BYTES + STAGES * STAGE_BYTES + CONV_BYTES;
+  static constexpr int RING_BYTES = STAGES * BN * 4;  // page id of every key of the tiles in flight
+  static constexpr int SMEM = Q_BYTES + STAGES * STAGE_BYTES + CONV_BYTES + RING_BYTES;
   static_assert(BN == 64, "tile loop assumes 64 keys");
+  static_assert(NT >= BN, "one thread per key fetches page ids");
 };
 
 template <int D, bool FP8, int NW, int STAGES>
@@ -54,7 +56,11 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
   uint8_t* sQ = smem;
   uint8_t* sStage = smem + C::Q_BYTES;
   uint8_t* sConv = sStage + STAGES * C::STAGE_BYTES;
+  int* sPage = reinterpret_cast<int*>(sConv + C::CONV_BYTES);  // [STAGES][BN]
 
+  // Inputs (pages appended by the previous kernel, q, tables) may come from
+  // the grid before this one in the stream.
+  grid_dependency_wait();
   const WorkItem it = p.items[blockIdx.x];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = it.b, h = it.h;
@@ -103,8 +109,15 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
   }
   cp_async_commit();
 
-  auto load_tile = [&](int tile, int stage) {
+  // Page id of one key of a tile (-1 past the chunk end).
+  auto page_of = [&](int tile, int r) -> int {
+    const int key = lo + tile * C::BN + r;
+    return (tile < n_tiles && key < hi) ? __ldg(p.kv_indices + pg0 + (key >> p.log2_page)) : -1;
+  };
+  // Issue the K and V rows of a tile from the page ids in its ring slot.
+  auto issue_tile = [&](int tile, int stage) {
     const int k0 = lo + tile * C::BN;
+    const int* pages = sPage + (tile % STAGES) * C::BN;
     uint8_t* sK = sStage + stage * C::STAGE_BYTES;
     uint8_t* sV = sK + C::TILE_BYTES;
 #pragma unroll 4
@@ -115,7 +128,7 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
       const uint8_t* vs = vbase;
       int bytes = 0;
       if (key < hi) {
-        const int page = __ldg(p.kv_indices + pg0 + (key >> p.log2_page));
+        const int page = pages[r];
         if ((unsigned)page < (unsigned)p.num_pages) {
           const size_t off = (size_t)page * page_stride + (size_t)(key & pmask) * C::KVROW + ch * 16;
           ks = kbase + off;
@@ -131,9 +144,12 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
     }
   };
 
+  // Page ids of the first STAGES tiles, then the first STAGES-1 tiles' rows.
+  for (int i = tid; i < STAGES * C::BN; i += C::NT) sPage[i] = page_of(i / C::BN, i % C::BN);
+  __syncthreads();
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < n_tiles) load_tile(s, s);
+    if (s < n_tiles) issue_tile(s, s);
     cp_async_commit();
   }
 
@@ -144,7 +160,9 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
   const int t_lo = (row0 + wrow + g4) / G;
   const int t_hi = (row0 + wrow + g4 + 8) / G;
   const int w_last = min(wrow + 15, nrows - 1);
-  const int warp_kv_end = prefix + (row0 + w_last) / G + 1;  // keys past it are masked for the warp
+  // keys past it are masked for every row of the warp (causal drafts only: a
+  // custom mask may open later drafts)
+  const int warp_kv_end = p.mask ? kv_len : prefix + (row0 + w_last) / G + 1;
   const int moff = p.mask ? p.mask_indptr[b] : 0;
   const float sl2 = p.scale_log2;
 
@@ -155,10 +173,13 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
 
   for (int tile = 0; tile < n_tiles; ++tile) {
+    // page ids of tile + STAGES, stored after this tile's compute (ring slot
+    // tile % STAGES, whose ids were last read when this tile was issued)
+    const int next_page = tid < C::BN ? page_of(tile + STAGES, tid) : -1;
     cp_async_wait<STAGES - 2>();
     __syncthreads();
     const int stage = tile % STAGES;
-    if (tile + STAGES - 1 < n_tiles) load_tile(tile + STAGES - 1, (tile + STAGES - 1) % STAGES);
+    if (tile + STAGES - 1 < n_tiles) issue_tile(tile + STAGES - 1, (tile + STAGES - 1) % STAGES);
     cp_async_commit();
 
     if (tile == 0 && warp_active) {
@@ -294,8 +315,10 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
         }
       }
     }
+    if (tid < C::BN) sPage[(tile % STAGES) * C::BN + tid] = next_page;
   }
   cp_async_wait<0>();
+  grid_dependents_launch();
   if (bad_page) atomicOr(p.status, VA_DEV_BAD_PAGE);
   if (!warp_active) return;
 
@@ -334,14 +357,16 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
 
 template <int D, bool FP8, int NW>
 cudaError_t launch_variant(const PartialParams& p, int n_items, cudaStream_t stream) {
-  constexpr int STAGES = 3;
+  // 8 warps: one CTA per SM, 4 tiles in flight; 4 warps: two CTAs per SM, 3 each.
+  constexpr int STAGES = NW == 8 ? 4 : 3;
   using C = MmaCfg<D, FP8, NW, STAGES>;
+  static_assert(C::SMEM <= (NW == 8 ? 227 * 1024 : 113 * 1024), "shared memory budget");
   auto kern = verify_partial_mma_kernel<D, FP8, NW, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PartialParams*>(&p)};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(n_items), dim3(C::NT), args,
-                          C::SMEM, stream);
+  return launch_kernel(reinterpret_cast<const void*>(kern), dim3(n_items), dim3(C::NT), C::SMEM,
+                       stream, args, /*pdl=*/true);
 }
 
 }  // namespace

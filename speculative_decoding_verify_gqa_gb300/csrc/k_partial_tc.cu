@@ -1,0 +1,376 @@
+// Split-KV verify attention on the 5th-generation tensor cores (tcgen05, TMEM
+// accumulators, TMA page gather) for blocks of 128 query rows.
+//
+// Same algorithm as the warp-level variant ("flashmap 0.1.0 --
+// flashmap/sglang/verify_attention.py", partial kernel: one CTA per request,
+// KV head, row block and kv chunk; online softmax; normalised output or fp32
+// partial + LSE), laid out for sm_103a:
+//  * warp 0, one thread: TMA producer.  Q arrives as one 3-D box per 64-column
+//    half (G heads x 128/G tokens: the block's token-major rows); each tile of
+//    128 keys arrives as 16-row page boxes of the 4-D cache [page, head, slot,
+//    dim] (page ids read from the page table; boxes past the chunk are pointed
+//    outside the pool so TMA zero-fills them), 128-byte swizzled, in a 2-stage
+//    ring of mbarrier-tracked stages.
+//  * warp 1, one thread: tcgen05.mma issuer.  S_j = Q K_j^T (M 128, N 128,
+//    K 128) into one of two TMEM S buffers while the softmax works on the
+//    other; O += P_{j-1} V_{j-1} (V read MN-major) into a TMEM O accumulator.
+//    tcgen05.commit signals S-ready, O-ready and stage-free mbarriers.
+//  * warps 4-7: one thread per query row (= TMEM lane).  Loads its S row,
+//    masks it, keeps a running max m and sum l in fp32, writes P = 2^(s c - m)
+//    as bf16 into shared memory for the next PV MMA.  The max used for P is
+//    only raised when a logit exceeds it by more than 2^8 (then O and l are
+//    rescaled in TMEM); the final O / l is exact either way.
+// All mbarrier waits are bounded; on expiry the CTA raises VA_DEV_TIMEOUT,
+// stops issuing work, frees its TMEM and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "../../include/verify_attn.h"
+#include "va_device.cuh"
+#include "va_kernels.h"
+#include "va_tc.cuh"
+
+namespace va {
+namespace {
+
+constexpr int TC_ROWS = 128;
+constexpr int TC_D = 128;
+constexpr int TC_KEYS = 128;
+constexpr int TC_STAGES = 2;
+constexpr int TC_THREADS = 256;
+constexpr int TC_Q_BYTES = TC_ROWS * TC_D * 2;             // [2 halves][128 rows][128 B]
+constexpr int TC_KT_BYTES = TC_KEYS * TC_D * 2;            // K (or V) tile, same layout
+constexpr int TC_STAGE_BYTES = 2 * TC_KT_BYTES;
+constexpr int TC_P_BYTES = TC_ROWS * TC_KEYS * 2;          // [2 key blocks][128 rows][128 B]
+constexpr int TC_OFF_Q = 0;
+constexpr int TC_OFF_KV = TC_OFF_Q + TC_Q_BYTES;
+constexpr int TC_OFF_P = TC_OFF_KV + TC_STAGES * TC_STAGE_BYTES;
+constexpr int TC_OFF_BAR = TC_OFF_P + TC_P_BYTES;
+constexpr int TC_SMEM = TC_OFF_BAR + 256 + 1024;           // barriers, slack for 1024-B alignment
+constexpr uint32_t TC_TMEM_COLS = 512;                     // S0 | S1 | O (128 columns each)
+constexpr uint32_t TC_COL_O = 2 * TC_KEYS;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// barrier slots
+enum { B_Q = 0, B_KV_FULL = 1, B_KV_EMPTY = 3, B_S_FULL = 5, B_S_FREE = 7, B_P_FULL = 9,
+       B_O_DONE = 10, B_COUNT = 11 };
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    verify_partial_tc_kernel(const PartialParams p, const __grid_constant__ TcMaps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + TC_OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TC_OFF_BAR + 8 * B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + TC_OFF_BAR + 8 * B_COUNT + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  grid_dependency_wait();
+  const WorkItem it = p.items[blockIdx.x];
+  const int b = it.b, h = it.h, G = p.group;
+  const int qo0 = p.qo_indptr[b];
+  const int L = p.qo_indptr[b + 1] - qo0;
+  const int pg0 = p.kv_indptr[b];
+  const int npg = p.kv_indptr[b + 1] - pg0;
+  const int lpl = npg > 0 ? p.last_page_len[b] : 1;
+  const long long kv_len_ll = npg > 0 ? (long long)(npg - 1) * p.page_size + lpl : 0;
+  const int kv_len = (int)kv_len_ll;
+  const int prefix = kv_len - L;
+  const bool ok = L >= 0 && npg >= 0 && lpl >= 1 && lpl <= p.page_size && prefix >= 0 &&
+                  it.row0 >= 0 && it.nrows > 0 && it.nrows <= TC_ROWS && it.row0 % TC_ROWS == 0 &&
+                  (long long)it.row0 + it.nrows <= (long long)G * L && it.kv_lo >= 0 &&
+                  it.kv_lo % 16 == 0 && it.kv_lo < it.kv_hi && it.kv_hi <= kv_len &&
+                  kv_len_ll <= 0x7fffffffLL;
+  if (!ok) {
+    if (tid == 0) atomicOr(p.status, VA_DEV_BAD_TABLE);
+    return;
+  }
+  const int nrows = it.nrows, row0 = it.row0, lo = it.kv_lo, hi = it.kv_hi;
+  const int n_tiles = (hi - lo + TC_KEYS - 1) / TC_KEYS;
+
+  if (tid == 0) {
+    mbar_init(bar(B_Q), 1);
+    for (int s = 0; s < TC_STAGES; ++s) {
+      mbar_init(bar(B_KV_FULL + s), 1);
+      mbar_init(bar(B_KV_EMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_S_FULL + s), 1);
+      mbar_init(bar(B_S_FREE + s), 4);
+    }
+    mbar_init(bar(B_P_FULL), 4);
+    mbar_init(bar(B_O_DONE), 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TC_TMEM_COLS);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      mbar_expect_tx(bar(B_Q), TC_Q_BYTES);
+      const int tok0 = qo0 + row0 / G;
+      for (int half = 0; half < 2; ++half)
+        tma_load_3d(sbase + TC_OFF_Q + half * (TC_Q_BYTES / 2), &maps.q, half * 64, h * G, tok0,
+                    bar(B_Q));
+      int bad = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % TC_STAGES;
+        if (j >= TC_STAGES && !mbar_wait(bar(B_KV_EMPTY + s), ((j / TC_STAGES) - 1) & 1, abort_flag))
+          break;
+        mbar_expect_tx(bar(B_KV_FULL + s), TC_STAGE_BYTES);
+        const uint32_t kdst = sbase + TC_OFF_KV + s * TC_STAGE_BYTES;
+        const uint32_t vdst = kdst + TC_KT_BYTES;
+        const int k0 = lo + j * TC_KEYS;
+        for (int g = 0; g < TC_KEYS / 16; ++g) {
+          const int key = k0 + 16 * g;
+          int page = p.num_pages;  // outside the pool: zero fill
+          int slot = 0;
+          if (key < hi) {
+            const int pid = __ldg(p.kv_indices + pg0 + (key >> p.log2_page));
+            if ((unsigned)pid < (unsigned)p.num_pages) {
+              page = pid;
+              slot = key & (p.page_size - 1);
+            } else {
+              bad = 1;
+            }
+          }
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t off = half * (TC_KEYS * 128) + g * 2048;
+            tma_load_4d(kdst + off, &maps.k, half * 64, slot, h, page, bar(B_KV_FULL + s));
+            tma_load_4d(vdst + off, &maps.v, half * 64, slot, h, page, bar(B_KV_FULL + s));
+          }
+        }
+      }
+      if (bad) atomicOr(p.status, VA_DEV_BAD_PAGE);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t id_s = idesc_bf16(TC_ROWS, TC_KEYS, false);
+      constexpr uint32_t id_o = idesc_bf16(TC_ROWS, TC_D, true);
+      const uint32_t qaddr = sbase + TC_OFF_Q, paddr = sbase + TC_OFF_P;
+      auto pv = [&](int j) {  // O (+)= P_j V_j
+        const uint32_t vaddr = sbase + TC_OFF_KV + (j % TC_STAGES) * TC_STAGE_BYTES + TC_KT_BYTES;
+        for (int kk = 0; kk < TC_KEYS / 16; ++kk) {
+          const uint64_t a = smem_desc_sw128(paddr + (kk >> 2) * (TC_ROWS * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(vaddr + kk * 16 * 128, TC_KEYS * 128, 1024);
+          umma_bf16(tmem + TC_COL_O, a, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(B_O_DONE));
+        umma_commit(bar(B_KV_EMPTY + j % TC_STAGES));
+      };
+      bool live = mbar_wait(bar(B_Q), 0, abort_flag);
+      int issued_pv = 0;
+      for (int j = 0; live && j < n_tiles; ++j) {
+        const int s = j % TC_STAGES, sb = j & 1;
+        if (!mbar_wait(bar(B_KV_FULL + s), (j / TC_STAGES) & 1, abort_flag)) break;
+        if (j >= 2 && !mbar_wait(bar(B_S_FREE + sb), ((j >> 1) - 1) & 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t kaddr = sbase + TC_OFF_KV + s * TC_STAGE_BYTES;
+        for (int kk = 0; kk < TC_D / 16; ++kk) {
+          const uint64_t a = smem_desc_sw128(qaddr + (kk >> 2) * (TC_ROWS * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(kaddr + (kk >> 2) * (TC_KEYS * 128) + (kk & 3) * 32, 16, 1024);
+          umma_bf16(tmem + sb * TC_KEYS, a, bd, id_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(B_S_FULL + sb));
+        if (j >= 1) {
+          if (!mbar_wait(bar(B_P_FULL), (j - 1) & 1, abort_flag)) break;
+          tc_fence_after();
+          pv(j - 1);
+          issued_pv = j;
+        }
+      }
+      if (!*abort_flag && issued_pv == n_tiles - 1) {
+        if (mbar_wait(bar(B_P_FULL), (n_tiles - 1) & 1, abort_flag)) {
+          tc_fence_after();
+          pv(n_tiles - 1);
+          // the last stage release lands before the CTA's shared memory goes away
+          const int j = n_tiles - 1;
+          mbar_wait(bar(B_KV_EMPTY + j % TC_STAGES), (j / TC_STAGES) & 1, abort_flag);
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax / epilogue: one thread per row ----------------
+    const int quad = warp - 4;
+    const int r = quad * 32 + lane;                 // row of the block = TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+    const bool row_ok = r < nrows;
+    const int t = (row0 + r) / G;                   // draft token of the row
+    const int moff = p.mask ? p.mask_indptr[b] : 0;
+    const float c = p.scale_log2;
+    float m_used = -INFINITY;                       // in units of s * c (log2 domain)
+    float l = 0.f;
+    float s[TC_KEYS];
+    uint32_t pk[TC_KEYS / 2];
+    bool live = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(bar(B_S_FULL + sb), (j >> 1) & 1, abort_flag)) { live = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < TC_KEYS / 32; ++q) {
+        uint32_t raw[32];
+        tmem_ld32(lane_addr + sb * TC_KEYS + q * 32, raw);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[q * 32 + e] = __uint_as_float(raw[e]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_S_FREE + sb));
+
+      const int k0 = lo + j * TC_KEYS;
+      if (k0 + TC_KEYS > prefix || k0 + TC_KEYS > hi) {
+#pragma unroll
+        for (int cc = 0; cc < TC_KEYS; ++cc) {
+          const int key = k0 + cc;
+          bool vis = key < hi;
+          if (vis && key >= prefix) {
+            const int u = key - prefix;
+            if (p.mask) {
+              const long long bit = (long long)moff + (long long)t * L + u;
+              vis = t < L && ((__ldg(p.mask + (bit >> 3)) >> (bit & 7)) & 1);
+            } else {
+              vis = u <= t;
+            }
+          }
+          if (!vis) s[cc] = -INFINITY;
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < TC_KEYS; ++cc) mx = fmaxf(mx, s[cc]);
+      mx *= c;  // c > 0
+      float m_new = m_used;
+      if (mx > m_used + 8.f) m_new = mx;   // also taken when m_used = -inf and mx is finite
+      const float alpha = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
+      const float base = m_new == -INFINITY ? 0.f : m_new;
+      float sum = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < TC_KEYS; cc += 2) {
+        const float p0 = ex2(fmaf(s[cc], c, -base));
+        const float p1 = ex2(fmaf(s[cc + 1], c, -base));
+        sum += p0 + p1;
+        pk[cc / 2] = pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + sum;
+      // P buffer and O are free once the previous PV has completed.
+      if (j >= 1) {
+        if (!mbar_wait(bar(B_O_DONE), (j - 1) & 1, abort_flag)) { live = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          for (int q = 0; q < TC_D / 32; ++q) {
+            uint32_t ov[32];
+            tmem_ld32(lane_addr + TC_COL_O + q * 32, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(lane_addr + TC_COL_O + q * 32, ov);
+          }
+          tmem_wait_st();
+        }
+      }
+      // Rows of V past the chunk end inside the last 16-key box may hold
+      // stale (even NaN) slots: zero them, since 0 * NaN would poison O.
+      const int tail = hi - k0;
+      if (tail < TC_KEYS && (tail & 15)) {
+        const int zlo = tail, zhi = (tail + 15) & ~15;
+        uint8_t* vt = smem + TC_OFF_KV + (j % TC_STAGES) * TC_STAGE_BYTES + TC_KT_BYTES;
+        for (int z = r; z < (zhi - zlo) * 16; z += TC_ROWS) {
+          const int row = zlo + z / 16, half = (z / 8) & 1, ch = z & 7;
+          *reinterpret_cast<uint4*>(vt + half * (TC_KEYS * 128) + row * 128 + (ch << 4)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      // P row -> shared memory, K-major 128-byte-swizzled [key block][row][128 B]
+      uint8_t* prow = smem + TC_OFF_P;
+#pragma unroll
+      for (int ch = 0; ch < TC_KEYS / 8; ++ch) {
+        const int kb = ch >> 3, c8 = ch & 7;
+        *reinterpret_cast<uint4*>(prow + kb * (TC_ROWS * 128) + r * 128 + ((c8 ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_P_FULL));
+      m_used = m_new;
+    }
+    // epilogue
+    if (live && mbar_wait(bar(B_O_DONE), (n_tiles - 1) & 1, abort_flag)) {
+      tc_fence_after();
+      const float lse = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      const float inv = l > 0.f ? p.v_scale / l : 0.f;
+      size_t orow = 0;
+      if (row_ok) {
+        const int g = (row0 + r) - t * G;
+        orow = (size_t)(qo0 + t) * p.h_q + (size_t)h * G + g;
+      }
+      for (int q = 0; q < TC_D / 32; ++q) {
+        uint32_t ov[32];
+        tmem_ld32(lane_addr + TC_COL_O + q * 32, ov);
+        tmem_wait_ld();
+        if (!row_ok) continue;
+        if (it.part_row < 0) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * TC_D + q * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv, __uint_as_float(ov[8 * e + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv, __uint_as_float(ov[8 * e + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv, __uint_as_float(ov[8 * e + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv, __uint_as_float(ov[8 * e + 7]) * inv);
+            dst[e] = w;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.part_out + ((size_t)it.part_row + r) * TC_D + q * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
+                                 __uint_as_float(ov[4 * e + 2]) * inv, __uint_as_float(ov[4 * e + 3]) * inv);
+        }
+      }
+      if (row_ok) {
+        if (it.part_row < 0) {
+          if (p.lse) p.lse[orow] = lse;
+        } else {
+          p.part_lse[(size_t)it.part_row + r] = lse;
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  grid_dependents_launch();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TC_TMEM_COLS);
+  }
+  if (tid == 0 && *abort_flag) atomicOr(p.status, VA_DEV_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, int n_items,
+                              cudaStream_t stream) {
+  if (n_items <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(verify_partial_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+  if (e != cudaSuccess) return e;
+  void* args[] = {const_cast<PartialParams*>(&p), const_cast<TcMaps*>(&maps)};
+  return launch_kernel(reinterpret_cast<const void*>(verify_partial_tc_kernel), dim3(n_items),
+                       dim3(TC_THREADS), TC_SMEM, stream, args, /*pdl=*/true);
+}
+
+int tc_smem_bytes() { return TC_SMEM; }
+
+}  // namespace va

@@ -1,5 +1,7 @@
 // C ABI of libverify_attn.so: argument checks, plan upload and kernel
 // launches.  See include/verify_attn.h for the contract of every entry point.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <string.h>
@@ -112,6 +114,50 @@ PartialParams make_partial(const void* q, const void* k_cache, const void* v_cac
   return p;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// TMA descriptors of the tensor-core variant (see TcMaps).
+int make_tc_maps(const void* q, int64_t total_qo, const void* k_cache, const void* v_cache,
+                 int num_pages, const PlanHeader* hd, TcMaps* m) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return VA_ERR_CUDA;
+  const int G = hd->group, D = hd->head_dim, P = hd->page_size;
+  if (total_qo <= 0 || num_pages <= 0) return VA_ERR_INVALID_ARGUMENT;
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hd->h_q, (cuuint64_t)total_qo};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)hd->h_q * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
+    if (enc(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return VA_ERR_CUDA;
+  }
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)P, (cuuint64_t)hd->h_kv, (cuuint64_t)num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)P * D * 2, (cuuint64_t)hd->h_kv * P * D * 2};
+  cuuint32_t box[4] = {64, 16, 1, 1};
+  const void* src[2] = {k_cache, v_cache};
+  CUtensorMap* dst[2] = {&m->k, &m->v};
+  for (int i = 0; i < 2; ++i)
+    if (enc(dst[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(src[i]), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return VA_ERR_CUDA;
+  return VA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -211,9 +257,16 @@ int verify_attn_partial(const void* q, const void* k_cache, const void* v_cache,
   PartialParams p = make_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len,
                                  qo_indptr, mask, mask_indptr, sm_scale, k_scale, v_scale, out,
                                  lse, num_pages, hd, workspace_d);
-  cudaError_t e = launch_partial_mma(p, hd->kernel, hd->head_dim,
-                                     hd->kv_dtype == VA_DTYPE_FP8_E4M3, hd->n_items,
-                                     static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (hd->kernel == kKernelTc128) {
+    TcMaps maps;
+    rc = make_tc_maps(q, hd->total_qo, k_cache, v_cache, num_pages, hd, &maps);
+    if (rc) return rc;
+    e = launch_partial_tc(p, maps, hd->n_items, static_cast<cudaStream_t>(stream));
+  } else {
+    e = launch_partial_mma(p, hd->kernel, hd->head_dim, hd->kv_dtype == VA_DTYPE_FP8_E4M3,
+                           hd->n_items, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
 }
 

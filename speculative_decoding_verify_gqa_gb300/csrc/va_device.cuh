@@ -48,6 +48,19 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Programmatic dependent launch: block until the grids this one depends on
+// have completed and their writes are visible (a no-op when the kernel was
+// launched without the programmatic-serialization attribute).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+// Allow the next kernel in the stream (if launched with programmatic
+// serialization) to be scheduled now; it still waits for our completion
+// before touching memory.
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // 2^x via the SFU instruction (denormal results flushed to zero; 2^-inf = 0).
 __device__ __forceinline__ float ex2(float x) {
   float y;

@@ -20,6 +20,7 @@ constexpr int kTileKeys = 64;
 enum Kernel : int32_t {
   kKernelMma64 = 1,   // warp-level mma.sync, 4 warps x 16 rows
   kKernelMma128 = 2,  // warp-level mma.sync, 8 warps x 16 rows
+  kKernelTc128 = 3,   // tcgen05 + TMA, 128 rows per CTA
 };
 
 inline int kernel_rows(int k) { return k == kKernelMma64 ? 64 : 128; }

@@ -2,6 +2,7 @@
 // libverify_attn.so).  Every pointer is a device pointer.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -55,10 +56,37 @@ struct AppendParams {
   int64_t total_new;
 };
 
+// Launch `func` with void** args; pdl = true lets the grid be scheduled
+// before the previous kernel in the stream finishes (programmatic dependent
+// launch); such kernels call grid_dependency_wait() before touching memory.
+inline cudaError_t launch_kernel(const void* func, dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, void** args, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, func, args);
+}
+
 // Launchers: return the launch's cudaError_t (cudaErrorInvalidValue for a
 // variant that is not compiled).
 cudaError_t launch_partial_mma(const PartialParams& p, int kernel, int head_dim, bool kv_fp8,
                                int n_items, cudaStream_t stream);
+
+// TMA descriptors of the tensor-core variant: q as [total_qo, h_q, 128] with
+// 64 x G x (128 / G) boxes, the caches as [num_pages, h_kv, P, 128] with
+// 64 x 16 x 1 x 1 boxes; bf16, 128-byte swizzle, zero fill out of bounds.
+struct TcMaps {
+  CUtensorMap q, k, v;
+};
+cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, int n_items,
+                              cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int head_dim, int n_merge, int block_rows,
                          cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);

@@ -17,6 +17,8 @@
 // block scheduler packs the SMs evenly.
 #include <algorithm>
 #include <cstring>
+#include <functional>
+#include <queue>
 #include <vector>
 
 #include "../../include/verify_attn.h"
@@ -26,7 +28,6 @@ namespace va {
 
 namespace {
 
-constexpr int kWaves = 2;         // work items per CTA slot the plan aims for
 constexpr int kMaxTargetPerSm = 4;
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -88,7 +89,8 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   for (int r : o.reserved)
     if (r) return VA_ERR_INVALID_ARGUMENT;
   if (o.max_splits < 0 || o.min_chunk < 0 || o.target_ctas < 0) return VA_ERR_INVALID_ARGUMENT;
-  if (o.kernel != VA_KERNEL_AUTO && o.kernel != VA_KERNEL_MMA_64 && o.kernel != VA_KERNEL_MMA_128)
+  if (o.kernel != VA_KERNEL_AUTO && o.kernel != VA_KERNEL_MMA_64 && o.kernel != VA_KERNEL_MMA_128 &&
+      o.kernel != VA_KERNEL_TC_128)
     return VA_ERR_INVALID_ARGUMENT;
 
   const int G = num_qo_heads / num_kv_heads;
@@ -116,13 +118,20 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     max_rows = std::max(max_rows, (int64_t)G * L);
   }
 
+  // The tensor-core variant serves head_dim 128, bf16 caches, page sizes that
+  // are multiples of its 16-row TMA boxes, and groups that tile its 128 rows.
+  const bool tc_ok = head_dim == 128 && kv_dtype == VA_DTYPE_BF16 && page_size % 16 == 0 &&
+                     128 % G == 0;
   int kernel = o.kernel;
+  if (kernel == VA_KERNEL_TC_128 && !tc_ok) return VA_ERR_UNSUPPORTED;
   if (kernel == VA_KERNEL_AUTO) kernel = max_rows <= 64 ? kKernelMma64 : kKernelMma128;
   const int BM = kernel_rows(kernel);
   const int TK = kTileKeys;
 
-  // Units of work: row blocks of each request (times each KV head).  A row
-  // block's last visible key is that of its last token: prefix + t_max.
+  // Units of work: row blocks of each request (times each KV head).  Without
+  // a mask a row block's last visible key is that of its last token, prefix +
+  // t_max; a custom mask may let a draft see later drafts, so its rows scan
+  // the request's whole kv range.
   std::vector<Unit> units;
   int64_t W = 0;
   int max_unit_rows = 0;
@@ -131,25 +140,75 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     for (int64_t row0 = 0; row0 < R; row0 += BM) {
       int32_t nrows = (int32_t)std::min<int64_t>(BM, R - row0);
       int64_t tmax = (row0 + nrows - 1) / G;
-      int32_t kv_end = (int32_t)(prefix[b] + tmax + 1);
+      int32_t kv_end = (int32_t)(has_mask ? prefix[b] + qlen[b] : prefix[b] + tmax + 1);
       units.push_back({b, (int32_t)row0, nrows, kv_end});
       W += (int64_t)kv_end * num_kv_heads;
       max_unit_rows = std::max(max_unit_rows, (int)nrows);
     }
   }
 
-  // Split size.  Each split adds an fp32 partial of nrows x D written and
-  // read back by the merge, i.e. 8 * nrows bytes per head-dim element against
-  // 2 * es * C bytes of K/V read: a chunk of at least 8 * nrows / es keys keeps
-  // that traffic at or below half of the K/V bytes.
+  // Split size.  A CTA's cost is modelled in bytes: its K/V rows (2 * D * es
+  // per key), a fixed prologue / pipeline-fill cost, and for a split item its
+  // fp32 partial (written, then read by the merge, mostly inside L2).  The
+  // hardware hands the longest-first list to the SMs as they free up, so for
+  // a few candidate wave counts the chunk size is derived from the total key
+  // count, the list is packed onto the CTA slots longest-first, and the
+  // candidate with the smallest estimated finish time wins.
   const int64_t slots = (int64_t)num_sms * kernel_ctas_per_sm(kernel);
-  int64_t target = o.target_ctas > 0 ? std::min<int64_t>(o.target_ctas, kMaxTargetPerSm * num_sms)
-                                     : std::min<int64_t>(kWaves * slots, kMaxTargetPerSm * num_sms);
   const int es = kv_dtype == VA_DTYPE_FP8_E4M3 ? 1 : 2;
-  int64_t min_chunk = o.min_chunk > 0 ? o.min_chunk
-                                      : std::max<int64_t>(2 * TK, 8 * (int64_t)max_unit_rows / es);
+  const int64_t key_bytes = 2LL * head_dim * es;
+  const int64_t fixed_bytes = 48 * 1024;
+  const int64_t partial_bytes_per_row = 4LL * head_dim;
+  int64_t min_chunk = o.min_chunk > 0 ? o.min_chunk : 2 * TK;
   min_chunk = ceil_div(min_chunk, TK) * TK;
-  int64_t chunk = std::max<int64_t>(min_chunk, ceil_div(ceil_div(W, std::max<int64_t>(target, 1)), TK) * TK);
+  auto chunk_for = [&](int64_t target) {
+    return std::max<int64_t>(min_chunk,
+                             ceil_div(ceil_div(W, std::max<int64_t>(target, 1)), TK) * TK);
+  };
+  auto split_of = [&](const Unit& u, int64_t chunk, int64_t* cu) {
+    int64_t n = ceil_div(u.kv_end, chunk);
+    if (o.max_splits > 0) n = std::min<int64_t>(n, o.max_splits);
+    n = std::max<int64_t>(n, 1);
+    *cu = ceil_div(ceil_div(u.kv_end, n), TK) * TK;
+    return ceil_div(u.kv_end, *cu);
+  };
+  int64_t chunk;
+  if (o.target_ctas > 0) {
+    chunk = chunk_for(std::min<int64_t>(o.target_ctas, kMaxTargetPerSm * num_sms));
+  } else {
+    chunk = chunk_for(slots);
+    double best = -1.0;
+    std::vector<int64_t> costs;
+    for (int waves : {1, 2, 3, 4}) {
+      const int64_t target = std::min<int64_t>(waves * slots, kMaxTargetPerSm * num_sms);
+      const int64_t c = chunk_for(target);
+      costs.clear();
+      for (const Unit& u : units) {
+        int64_t cu;
+        const int64_t n = split_of(u, c, &cu);
+        for (int64_t s = 0; s < n; ++s) {
+          const int64_t keys = std::min<int64_t>(cu, u.kv_end - s * cu);
+          const int64_t cost = fixed_bytes + keys * key_bytes +
+                               (n > 1 ? (int64_t)u.nrows * partial_bytes_per_row : 0);
+          for (int h = 0; h < num_kv_heads; ++h) costs.push_back(cost);
+        }
+      }
+      std::sort(costs.begin(), costs.end(), std::greater<int64_t>());
+      std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> load;
+      for (int64_t i = 0; i < slots; ++i) load.push(0);
+      int64_t finish = 0;
+      for (int64_t cst : costs) {
+        int64_t t = load.top() + cst;
+        load.pop();
+        load.push(t);
+        finish = std::max(finish, t);
+      }
+      if (best < 0 || (double)finish < best * 0.97) {
+        best = (double)finish;
+        chunk = c;
+      }
+    }
+  }
 
   struct Tmp {
     WorkItem it;
@@ -161,11 +220,8 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   int64_t part_rows = 0;
   int64_t order = 0;
   for (const Unit& u : units) {
-    int64_t n = ceil_div(u.kv_end, chunk);
-    if (o.max_splits > 0) n = std::min<int64_t>(n, o.max_splits);
-    n = std::max<int64_t>(n, 1);
-    int64_t cu = ceil_div(ceil_div(u.kv_end, n), TK) * TK;
-    n = ceil_div(u.kv_end, cu);
+    int64_t cu;
+    const int64_t n = split_of(u, chunk, &cu);
     for (int h = 0; h < num_kv_heads; ++h) {
       int64_t base = part_rows;
       if (n > 1) {

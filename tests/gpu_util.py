@@ -86,9 +86,19 @@ def host_out(out, lse, d):
     return o, l
 
 
-def compare(wl, out, lse, rows=None, caches=None, nthreads=None):
-    """Max errors of the device result (all rows, or the flat rows given)
-    against the oracle; asserts the tolerances and -inf agreement."""
+def bf16_half_spacing(x):
+    """Half the spacing of the bf16 grid at |x| (8 significant bits)."""
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    return np.where(ax > 0, np.exp2(e - 8), 0.0)
+
+
+def compare(wl, out, lse, rows=None, caches=None, nthreads=None, strict=False):
+    """Errors of the device result (all rows, or the flat rows given) against
+    the oracle.  Asserts -inf agreement, |lse - oracle| <= 1e-3 and
+    |out - oracle| <= 1e-2 + half the bf16 spacing at the oracle value (the
+    output is bf16: where |out| >= 4 that spacing alone exceeds 1e-2);
+    strict=True asserts the plain 1e-2 on every element."""
     o, l = host_out(out, lse, wl.d)
     ref_o, ref_l = oracle.verify_attn_workload(wl, rows=rows, caches=caches, nthreads=nthreads)
     if rows is not None:
@@ -97,8 +107,14 @@ def compare(wl, out, lse, rows=None, caches=None, nthreads=None):
     assert np.array_equal(np.isfinite(l), fin), "-inf LSE rows differ"
     assert np.all(l[~fin] == -np.inf)
     assert np.all(o[~fin] == 0.0)
-    err_o = float(np.abs(o - ref_o).max()) if o.size else 0.0
+    diff = np.abs(o - ref_o)
+    err_o = float(diff.max()) if o.size else 0.0
     err_l = float(np.abs(l[fin] - ref_l[fin]).max()) if fin.any() else 0.0
-    assert err_o <= OUT_TOL, "max |out - oracle| = %g" % err_o
+    if strict:
+        assert err_o <= OUT_TOL, "max |out - oracle| = %g" % err_o
+    else:
+        excess = diff - (OUT_TOL + bf16_half_spacing(ref_o))
+        assert o.size == 0 or excess.max() <= 0, \
+            "max |out - oracle| = %g exceeds 1e-2 + bf16 half-spacing" % err_o
     assert err_l <= LSE_TOL, "max |lse - oracle| = %g" % err_l
     return err_o, err_l

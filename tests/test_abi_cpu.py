@@ -65,7 +65,7 @@ def _tables(seed, batch, G, h_kv, page_size, max_prefix, max_L, masked):
     last = np.where(pages > 0, kv_len - (pages - 1) * page_size, 0).astype(np.int32)
     qo_indptr = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
     mask_indptr = np.concatenate([[0], np.cumsum(L * L)]).astype(np.int32) if masked else None
-    return dict(prefix=prefix, L=L, kv_len=kv_len, kv_indptr=kv_indptr, last=last,
+    return dict(masked=masked, prefix=prefix, L=L, kv_len=kv_len, kv_indptr=kv_indptr, last=last,
                 qo_indptr=qo_indptr, mask_indptr=mask_indptr, h_q=G * h_kv, h_kv=h_kv,
                 G=G, page_size=page_size)
 
@@ -98,7 +98,10 @@ def _check_cover(va, t, plan):
     for (b, h, row0, nrows), chunks in units.items():
         chunks.sort()
         tmax = (row0 + nrows - 1) // G
-        kv_end = int(t["prefix"][b]) + tmax + 1
+        if t.get("masked"):   # a custom mask may open later drafts: whole kv range
+            kv_end = int(t["prefix"][b]) + int(t["L"][b])
+        else:
+            kv_end = int(t["prefix"][b]) + tmax + 1
         pos = 0
         for lo, hi, _ in chunks:
             assert lo == pos
@@ -144,7 +147,7 @@ def test_plan_covers_rows_and_keys_exactly_once(va, case, num_sms):
 @pytest.mark.parametrize("name", synthetic.WORKLOAD_ORDER)
 def test_plans_of_the_named_workloads(va, name):
     wl = synthetic.make_workload(name, with_values=False)
-    t = dict(prefix=wl.prefix_lens, L=wl.qo_lens, G=wl.group, h_kv=wl.h_kv)
+    t = dict(masked=wl.mask is not None, prefix=wl.prefix_lens, L=wl.qo_lens, G=wl.group, h_kv=wl.h_kv)
     plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
                                     wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
                                     kv_dtype=wl.kv_dtype, num_sms=152)

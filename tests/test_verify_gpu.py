@@ -56,7 +56,7 @@ def test_append_flags_bad_page_and_writes_the_rest(va):
                                prefix=("fixed", [20, 20]), qo=("fixed", [3, 3]), seed=9)
     dw = DeviceWorkload(wl, append=False)
     bad = wl.kv_indices.copy()
-    bad[wl.kv_indptr[1]] = wl.num_pages + 5      # request 1's first page id is out of range
+    bad[wl.kv_indptr[1] + 1] = wl.num_pages + 5  # request 1's drafts (positions 20-22) live on its page 1
     dw.kv_indices = torch.from_numpy(bad).cuda()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     dw.append_drafts(status=status)
@@ -130,6 +130,60 @@ def test_forced_plans_match_oracle(va, opts):
     if "target_ctas" in opts:
         assert plan.header()["n_merge"] > 0
     compare(wl, out, lse)
+
+
+def test_custom_mask_may_open_later_drafts(va):
+    """A custom mask is not limited to earlier drafts: rows of the first row
+    block must still see every later draft the mask allows (3 row blocks)."""
+    wl = synthetic.make_custom(batch=2, h_q=16, h_kv=2, d=128, prefix=("fixed", [70, 3]),
+                               qo=("fixed", [40, 33]), mask="random", seed=27)
+    assert int((wl.group * wl.qo_lens).max()) > 256
+    dw = DeviceWorkload(wl)
+    for opts in (dict(), dict(kernel=1), dict(kernel=3)):
+        out, lse, plan = dw.run(**opts)
+        torch.cuda.synchronize()
+        compare(wl, out, lse)
+
+
+TC_CASES = [
+    ("tree_g4", dict(batch=2, h_q=32, h_kv=8, d=128, prefix=("fixed", [700, 64]),
+                     qo=("fixed", [17, 40]), mask="tree")),
+    ("prefill_g8", dict(batch=3, h_q=16, h_kv=2, d=128, prefix=("fixed", [0, 0, 0]),
+                        qo=("fixed", [300, 17, 129]), mask="causal")),
+    ("chain_prefix", dict(batch=2, h_q=8, h_kv=1, d=128, prefix=("fixed", [1000, 257]),
+                          qo=("fixed", [20, 16]), mask="causal")),
+    ("page32", dict(batch=2, h_q=8, h_kv=2, d=128, page_size=32, prefix=("fixed", [333, 31]),
+                    qo=("fixed", [40, 33]), mask="tree")),
+    ("page256", dict(batch=2, h_q=4, h_kv=2, d=128, page_size=256, prefix=("fixed", [600, 10]),
+                     qo=("fixed", [70, 6]), mask="tree")),
+    ("g1_mha", dict(batch=1, h_q=2, h_kv=2, d=128, prefix=("fixed", [190]),
+                    qo=("fixed", [150]), mask="causal")),
+    ("masked_rows", dict(batch=2, h_q=8, h_kv=2, d=128, prefix=("fixed", [0, 5]),
+                         qo=("fixed", [40, 37]), mask="none_visible")),
+]
+
+
+@pytest.mark.parametrize("name,case", TC_CASES, ids=[c[0] for c in TC_CASES])
+@pytest.mark.parametrize("splits", [1, 0])
+def test_tcgen05_kernel_matches_oracle(va, name, case, splits):
+    wl = synthetic.make_custom(seed=29, **case)
+    dw = DeviceWorkload(wl)
+    opts = dict(kernel=3, max_splits=splits)
+    if splits == 0:
+        opts["target_ctas"] = 600
+    out, lse, plan = dw.run(**opts)
+    torch.cuda.synchronize()
+    assert plan.header()["kernel"] == 3
+    assert va.verify_attn_device_status(plan) == 0
+    compare(wl, out, lse)
+
+
+def test_tcgen05_kernel_rejects_what_it_cannot_serve(va):
+    wl = synthetic.make_custom(batch=1, h_q=6, h_kv=2, d=128, prefix=("fixed", [10]),
+                               qo=("fixed", [3]), seed=31)
+    with pytest.raises(va.VerifyAttnError):
+        va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, None, 6, 2, 128,
+                                 16, kernel=3, num_sms=152)   # 128 % G != 0
 
 
 def test_split_and_unsplit_agree(va):
@@ -291,4 +345,4 @@ def test_named_workload_matches_oracle(va, name):
         # the device pool (written by the append kernel) is the oracle's pool, bit for bit
         assert np.array_equal(caches[0], ok) and np.array_equal(caches[1], ov)
         caches = (ok, ov)
-    compare(wl, out, lse, rows=rows, caches=caches)
+    compare(wl, out, lse, rows=rows, caches=caches, strict=True)
