@@ -165,12 +165,13 @@ def make_event(torch):
 # ---------------------------------------------------------------- our arm
 
 class Bench:
-    def __init__(self, name, device, seed=0):
+    def __init__(self, name, device, seed=0, plan_opts=None):
         import torch
         import speculative_decoding_verify_gqa_gb300 as va
         self.torch, self.va = torch, va
         self.name = name
         self.dev = device
+        self.plan_opts = dict(plan_opts or {})
         wl = synthetic.make_workload(name, seed=seed)
         self.wl = wl
         fp8 = wl.kv_dtype == synthetic.FP8
@@ -206,7 +207,7 @@ class Bench:
         self.pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(self.n_copies - 1)]
         self.plan = va.verify_attn_plan(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
                                         wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
-                                        kv_dtype=wl.kv_dtype, device=device)
+                                        kv_dtype=wl.kv_dtype, device=device, **self.plan_opts)
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
         self.launches_per_step = 1 + self.plan.launches()
@@ -322,7 +323,7 @@ class Bench:
             plan = va.verify_attn_plan(np_tables["kv_indptr"], np_tables["qo_indptr"],
                                        np_tables["last_page_len"], np_mask_indptr, wl.h_q,
                                        wl.h_kv, wl.d, wl.page_size, kv_dtype=wl.kv_dtype,
-                                       workspace=ws, device=self.dev)
+                                       workspace=ws, device=self.dev, **self.plan_opts)
             kc, vc = self.pools[i % self.n_copies]
             va.paged_kv_append(d["k_new"].view(self.kvd), d["v_new"].view(self.kvd),
                                d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
@@ -350,11 +351,15 @@ class Bench:
         for _ in range(n):
             va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, wl.mask_indptr,
                                      wl.h_q, wl.h_kv, wl.d, wl.page_size, kv_dtype=wl.kv_dtype,
-                                     num_sms=self.plan.header()["num_sms"])
+                                     num_sms=self.plan.header()["num_sms"], **self.plan_opts)
         return (time.perf_counter() - t0) / n * 1e6
 
 
-def roofline_for(wl, kt, peaks, peak_kind):
+KERNEL_NAMES = {1: "verify_partial_mma_kernel<4 warps>", 2: "verify_partial_mma_kernel<8 warps>",
+                3: "verify_partial_tc_kernel"}
+
+
+def roofline_for(wl, kt, peaks, peak_kind, kernel=0):
     alg = algorithmic(wl)
     t = kt["partial_ms"] * 1e-3
     hbm = alg["read_bytes"] / t / 1e9
@@ -367,7 +372,7 @@ def roofline_for(wl, kt, peaks, peak_kind):
     else:
         rf = {"bound": "hbm", "achieved": round(hbm, 1), "peak": peaks["hbm_gbs"],
               "unit": "GB/s", "frac": round(hbm / peaks["hbm_gbs"], 4)}
-    rf.update({"kernel": "verify_partial_mma_kernel",
+    rf.update({"kernel": KERNEL_NAMES.get(kernel, "verify_partial"),
                "peak_source": "MEASURED_PEAKS.json (of %s)" % peak_kind,
                "algorithmic_bytes_per_launch": alg["read_bytes"],
                "algorithmic_flops_per_launch": alg["flops"],
@@ -451,14 +456,16 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks, peak_kind = load_peaks()
-    bench = Bench(args.workload, dev, seed=0)
+    plan_opts = {k: v for k, v in (("kernel", args.kernel), ("target_ctas", args.target_ctas),
+                                   ("min_chunk", args.min_chunk)) if v}
+    bench = Bench(args.workload, dev, seed=0, plan_opts=plan_opts)
     wl = bench.wl
     sampler = ClockSampler(local)
     ms, clocks = bench.time_steps(args.steps, args.warmup, sampler=sampler,
                                   barrier=barrier_fn(world))
     ms_max = reduce_max(ms, world)
     kt = bench.kernel_times()
-    rf = roofline_for(wl, kt, peaks, peak_kind)
+    rf = roofline_for(wl, kt, peaks, peak_kind, bench.plan.header()["kernel"])
     rf["traffic"] = profiled_traffic(wl.name)
     alg = algorithmic(wl)
     value = world * wl.total_qo / (ms_max * 1e-3)
@@ -489,7 +496,7 @@ def run_ours(args):
             steps = 256 if name != "tiny_verify" else 1024
             ms_o, _ = b.time_steps(steps, 16)
             kto = b.kernel_times(32)
-            rfo = roofline_for(b.wl, kto, peaks, peak_kind)
+            rfo = roofline_for(b.wl, kto, peaks, peak_kind, b.plan.header()["kernel"])
             rfo["traffic"] = profiled_traffic(name)
             others[name] = {"tokens_per_s": round(b.wl.total_qo / (ms_o * 1e-3), 1),
                             "ms_per_step": round(ms_o, 6),
@@ -567,6 +574,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--kernel", type=int, default=0,
+                    help="force a split-kernel variant (1: mma 64 rows, 2: mma 128 rows, "
+                         "3: tcgen05); 0 = the planner's choice")
+    ap.add_argument("--target-ctas", type=int, default=0, help="planner option (0 = auto)")
+    ap.add_argument("--min-chunk", type=int, default=0, help="planner option (0 = auto)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -6,20 +6,26 @@
 // KV head, row block and kv chunk; online softmax; normalised output or fp32
 // partial + LSE), laid out for sm_103a:
 //  * warp 0, one thread: TMA producer.  Q arrives as one 3-D box per 64-column
-//    half (G heads x 128/G tokens: the block's token-major rows); each tile of
-//    128 keys arrives as 16-row page boxes of the 4-D cache [page, head, slot,
-//    dim] (page ids read from the page table; boxes past the chunk are pointed
-//    outside the pool so TMA zero-fills them), 128-byte swizzled, in a 2-stage
-//    ring of mbarrier-tracked stages.
-//  * warp 1, one thread: tcgen05.mma issuer.  S_j = Q K_j^T (M 128, N 128,
-//    K 128) into one of two TMEM S buffers while the softmax works on the
+//    half (G heads x 128/G tokens: the block's token-major rows); each key tile
+//    arrives as 16-row page boxes of the 4-D cache [page, head, slot, dim]
+//    (page ids read from the page table; boxes past the chunk point outside
+//    the pool, so TMA zero-fills them) into a ring of mbarrier-tracked stages.
+//  * warp 1, one thread: tcgen05.mma issuer.  S_j = Q K_j^T (M 128, N = tile
+//    keys, K 128) into one of two TMEM S buffers while the softmax works on the
 //    other; O += P_{j-1} V_{j-1} (V read MN-major) into a TMEM O accumulator.
-//    tcgen05.commit signals S-ready, O-ready and stage-free mbarriers.
+//    tcgen05.commit signals S-ready, O-ready and buffer-free mbarriers.
 //  * warps 4-7: one thread per query row (= TMEM lane).  Loads its S row,
 //    masks it, keeps a running max m and sum l in fp32, writes P = 2^(s c - m)
-//    as bf16 into shared memory for the next PV MMA.  The max used for P is
-//    only raised when a logit exceeds it by more than 2^8 (then O and l are
-//    rescaled in TMEM); the final O / l is exact either way.
+//    for the next PV MMA.  The max used for P is only raised when a logit
+//    exceeds it by more than 2^8 (then O and l are rescaled in TMEM); O / l is
+//    exact either way.
+//  * bf16 caches: 128-key tiles, bf16 MMAs, 128-byte-swizzled TMA boxes that
+//    are the MMA operands as they land.
+//  * fp8-e4m3 caches: 64-key tiles land unswizzled; warps 2-3 widen each tile
+//    to f16 (cvt.rn.f16x2.e4m3x2, exact) into a double-buffered swizzled
+//    operand, zeroing rows past the chunk; the MMAs run on f16 (Q converted
+//    once per CTA, P packed as f16); k_scale / v_scale stay in the softmax
+//    scale and the final normalisation.
 // All mbarrier waits are bounded; on expiry the CTA raises VA_DEV_TIMEOUT,
 // stops issuing work, frees its TMEM and exits.
 #include <cuda.h>
@@ -34,38 +40,53 @@
 namespace va {
 namespace {
 
-constexpr int TC_ROWS = 128;
-constexpr int TC_D = 128;
-constexpr int TC_KEYS = 128;
-constexpr int TC_STAGES = 2;
-constexpr int TC_THREADS = 256;
-constexpr int TC_Q_BYTES = TC_ROWS * TC_D * 2;             // [2 halves][128 rows][128 B]
-constexpr int TC_KT_BYTES = TC_KEYS * TC_D * 2;            // K (or V) tile, same layout
-constexpr int TC_STAGE_BYTES = 2 * TC_KT_BYTES;
-constexpr int TC_P_BYTES = TC_ROWS * TC_KEYS * 2;          // [2 key blocks][128 rows][128 B]
-constexpr int TC_OFF_Q = 0;
-constexpr int TC_OFF_KV = TC_OFF_Q + TC_Q_BYTES;
-constexpr int TC_OFF_P = TC_OFF_KV + TC_STAGES * TC_STAGE_BYTES;
-constexpr int TC_OFF_BAR = TC_OFF_P + TC_P_BYTES;
-constexpr int TC_SMEM = TC_OFF_BAR + 256 + 1024;           // barriers, slack for 1024-B alignment
-constexpr uint32_t TC_TMEM_COLS = 512;                     // S0 | S1 | O (128 columns each)
-constexpr uint32_t TC_COL_O = 2 * TC_KEYS;
+template <bool FP8>
+struct TcCfg {
+  static constexpr int ROWS = 128, D = 128, THREADS = 256;
+  static constexpr int KEYS = FP8 ? 64 : 128;            // keys per tile
+  static constexpr int STAGES = FP8 ? 3 : 2;             // TMA stages (raw fp8, or bf16 operands)
+  static constexpr int Q_BYTES = ROWS * D * 2;           // [2 halves][128 rows][128 B]
+  static constexpr int OP_BYTES = KEYS * D * 2;          // 16-bit K (or V) operand tile
+  static constexpr int RAW_BYTES = KEYS * D;             // fp8 K (or V) tile [keys][128 B]
+  static constexpr int STAGE_BYTES = FP8 ? 2 * RAW_BYTES : 2 * OP_BYTES;
+  static constexpr int CONV_BUFS = FP8 ? 2 : 0;          // widened K+V operand buffers
+  static constexpr int P_BYTES = ROWS * KEYS * 2;        // [key blocks][128 rows][128 B]
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + Q_BYTES;
+  static constexpr int OFF_CONV = OFF_KV + STAGES * STAGE_BYTES;
+  static constexpr int OFF_P = OFF_CONV + CONV_BUFS * 2 * OP_BYTES;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;       // barriers; slack for 1024-B alignment
+  static constexpr uint32_t TMEM_COLS = FP8 ? 256 : 512;  // S0 | S1 | O
+  static constexpr uint32_t COL_O = 2 * KEYS;
+  static constexpr int CONV_WARPS = 2;                    // warps 2-3 (fp8 only)
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
 constexpr float kLn2 = 0.6931471805599453f;
 
 // barrier slots
-enum { B_Q = 0, B_KV_FULL = 1, B_KV_EMPTY = 3, B_S_FULL = 5, B_S_FREE = 7, B_P_FULL = 9,
-       B_O_DONE = 10, B_COUNT = 11 };
+enum { B_Q = 0, B_Q_READY = 1, B_KV_FULL = 2, B_KV_EMPTY = 5, B_CONV_FULL = 8, B_CONV_FREE = 10,
+       B_S_FULL = 12, B_S_FREE = 14, B_P_FULL = 16, B_O_DONE = 17, B_COUNT = 18 };
 
-__global__ void __launch_bounds__(TC_THREADS, 1)
+// Instruction descriptor, kind::f16 with f16 A and B (fp32 accumulator).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(256, 1)
     verify_partial_tc_kernel(const PartialParams p, const __grid_constant__ TcMaps maps) {
+  using C = TcCfg<FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + TC_OFF_BAR;
+  const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TC_OFF_BAR + 8 * B_COUNT);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + TC_OFF_BAR + 8 * B_COUNT + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 8 * B_COUNT + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   grid_dependency_wait();
@@ -80,7 +101,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int kv_len = (int)kv_len_ll;
   const int prefix = kv_len - L;
   const bool ok = L >= 0 && npg >= 0 && lpl >= 1 && lpl <= p.page_size && prefix >= 0 &&
-                  it.row0 >= 0 && it.nrows > 0 && it.nrows <= TC_ROWS && it.row0 % TC_ROWS == 0 &&
+                  it.row0 >= 0 && it.nrows > 0 && it.nrows <= C::ROWS && it.row0 % C::ROWS == 0 &&
                   (long long)it.row0 + it.nrows <= (long long)G * L && it.kv_lo >= 0 &&
                   it.kv_lo % 16 == 0 && it.kv_lo < it.kv_hi && it.kv_hi <= kv_len &&
                   kv_len_ll <= 0x7fffffffLL;
@@ -89,15 +110,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     return;
   }
   const int nrows = it.nrows, row0 = it.row0, lo = it.kv_lo, hi = it.kv_hi;
-  const int n_tiles = (hi - lo + TC_KEYS - 1) / TC_KEYS;
+  const int n_tiles = (hi - lo + C::KEYS - 1) / C::KEYS;
 
   if (tid == 0) {
     mbar_init(bar(B_Q), 1);
-    for (int s = 0; s < TC_STAGES; ++s) {
+    mbar_init(bar(B_Q_READY), 4);
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(B_KV_FULL + s), 1);
-      mbar_init(bar(B_KV_EMPTY + s), 1);
+      mbar_init(bar(B_KV_EMPTY + s), FP8 ? C::CONV_WARPS : 1);
     }
     for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_CONV_FULL + s), C::CONV_WARPS);
+      mbar_init(bar(B_CONV_FREE + s), 1);
       mbar_init(bar(B_S_FULL + s), 1);
       mbar_init(bar(B_S_FREE + s), 4);
     }
@@ -106,7 +130,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TC_TMEM_COLS);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -114,21 +138,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      mbar_expect_tx(bar(B_Q), TC_Q_BYTES);
+      mbar_expect_tx(bar(B_Q), C::Q_BYTES);
       const int tok0 = qo0 + row0 / G;
       for (int half = 0; half < 2; ++half)
-        tma_load_3d(sbase + TC_OFF_Q + half * (TC_Q_BYTES / 2), &maps.q, half * 64, h * G, tok0,
+        tma_load_3d(sbase + C::OFF_Q + half * (C::Q_BYTES / 2), &maps.q, half * 64, h * G, tok0,
                     bar(B_Q));
       int bad = 0;
       for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % TC_STAGES;
-        if (j >= TC_STAGES && !mbar_wait(bar(B_KV_EMPTY + s), ((j / TC_STAGES) - 1) & 1, abort_flag))
+        const int s = j % C::STAGES;
+        if (j >= C::STAGES &&
+            !mbar_wait(bar(B_KV_EMPTY + s), ((j / C::STAGES) - 1) & 1, abort_flag))
           break;
-        mbar_expect_tx(bar(B_KV_FULL + s), TC_STAGE_BYTES);
-        const uint32_t kdst = sbase + TC_OFF_KV + s * TC_STAGE_BYTES;
-        const uint32_t vdst = kdst + TC_KT_BYTES;
-        const int k0 = lo + j * TC_KEYS;
-        for (int g = 0; g < TC_KEYS / 16; ++g) {
+        mbar_expect_tx(bar(B_KV_FULL + s), C::STAGE_BYTES);
+        const uint32_t kdst = sbase + C::OFF_KV + s * C::STAGE_BYTES;
+        const uint32_t vdst = kdst + C::STAGE_BYTES / 2;
+        const int k0 = lo + j * C::KEYS;
+        for (int g = 0; g < C::KEYS / 16; ++g) {
           const int key = k0 + 16 * g;
           int page = p.num_pages;  // outside the pool: zero fill
           int slot = 0;
@@ -141,10 +166,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               bad = 1;
             }
           }
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t off = half * (TC_KEYS * 128) + g * 2048;
-            tma_load_4d(kdst + off, &maps.k, half * 64, slot, h, page, bar(B_KV_FULL + s));
-            tma_load_4d(vdst + off, &maps.v, half * 64, slot, h, page, bar(B_KV_FULL + s));
+          if constexpr (FP8) {
+            tma_load_4d(kdst + g * 2048, &maps.k, 0, slot, h, page, bar(B_KV_FULL + s));
+            tma_load_4d(vdst + g * 2048, &maps.v, 0, slot, h, page, bar(B_KV_FULL + s));
+          } else {
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t off = half * (C::KEYS * 128) + g * 2048;
+              tma_load_4d(kdst + off, &maps.k, half * 64, slot, h, page, bar(B_KV_FULL + s));
+              tma_load_4d(vdst + off, &maps.v, half * 64, slot, h, page, bar(B_KV_FULL + s));
+            }
           }
         }
       }
@@ -153,31 +183,40 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t id_s = idesc_bf16(TC_ROWS, TC_KEYS, false);
-      constexpr uint32_t id_o = idesc_bf16(TC_ROWS, TC_D, true);
-      const uint32_t qaddr = sbase + TC_OFF_Q, paddr = sbase + TC_OFF_P;
+      constexpr uint32_t id_s = FP8 ? idesc_f16(C::ROWS, C::KEYS, false)
+                                    : idesc_bf16(C::ROWS, C::KEYS, false);
+      constexpr uint32_t id_o = FP8 ? idesc_f16(C::ROWS, C::D, true) : idesc_bf16(C::ROWS, C::D, true);
+      const uint32_t qaddr = sbase + C::OFF_Q, paddr = sbase + C::OFF_P;
+      auto kop = [&](int j) {  // K operand of tile j
+        return FP8 ? sbase + C::OFF_CONV + (j & 1) * 2 * C::OP_BYTES
+                   : sbase + C::OFF_KV + (j % C::STAGES) * C::STAGE_BYTES;
+      };
       auto pv = [&](int j) {  // O (+)= P_j V_j
-        const uint32_t vaddr = sbase + TC_OFF_KV + (j % TC_STAGES) * TC_STAGE_BYTES + TC_KT_BYTES;
-        for (int kk = 0; kk < TC_KEYS / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(paddr + (kk >> 2) * (TC_ROWS * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(vaddr + kk * 16 * 128, TC_KEYS * 128, 1024);
-          umma_bf16(tmem + TC_COL_O, a, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+        const uint32_t vaddr = kop(j) + C::OP_BYTES;
+        for (int kk = 0; kk < C::KEYS / 16; ++kk) {
+          const uint64_t a = smem_desc_sw128(paddr + (kk >> 2) * (C::ROWS * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(vaddr + kk * 16 * 128, C::KEYS * 128, 1024);
+          umma_bf16(tmem + C::COL_O, a, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(bar(B_O_DONE));
-        umma_commit(bar(B_KV_EMPTY + j % TC_STAGES));
+        umma_commit(FP8 ? bar(B_CONV_FREE + (j & 1)) : bar(B_KV_EMPTY + j % C::STAGES));
       };
-      bool live = mbar_wait(bar(B_Q), 0, abort_flag);
+      bool live = mbar_wait(bar(FP8 ? B_Q_READY : B_Q), 0, abort_flag);
       int issued_pv = 0;
       for (int j = 0; live && j < n_tiles; ++j) {
-        const int s = j % TC_STAGES, sb = j & 1;
-        if (!mbar_wait(bar(B_KV_FULL + s), (j / TC_STAGES) & 1, abort_flag)) break;
+        const int sb = j & 1;
+        if (FP8) {
+          if (!mbar_wait(bar(B_CONV_FULL + sb), (j >> 1) & 1, abort_flag)) break;
+        } else {
+          if (!mbar_wait(bar(B_KV_FULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag)) break;
+        }
         if (j >= 2 && !mbar_wait(bar(B_S_FREE + sb), ((j >> 1) - 1) & 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t kaddr = sbase + TC_OFF_KV + s * TC_STAGE_BYTES;
-        for (int kk = 0; kk < TC_D / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(qaddr + (kk >> 2) * (TC_ROWS * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(kaddr + (kk >> 2) * (TC_KEYS * 128) + (kk & 3) * 32, 16, 1024);
-          umma_bf16(tmem + sb * TC_KEYS, a, bd, id_s, kk > 0 ? 1u : 0u);
+        const uint32_t kaddr = kop(j);
+        for (int kk = 0; kk < C::D / 16; ++kk) {
+          const uint64_t a = smem_desc_sw128(qaddr + (kk >> 2) * (C::ROWS * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(kaddr + (kk >> 2) * (C::KEYS * 128) + (kk & 3) * 32, 16, 1024);
+          umma_bf16(tmem + sb * C::KEYS, a, bd, id_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar(B_S_FULL + sb));
         if (j >= 1) {
@@ -191,14 +230,58 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (mbar_wait(bar(B_P_FULL), (n_tiles - 1) & 1, abort_flag)) {
           tc_fence_after();
           pv(n_tiles - 1);
-          // the last stage release lands before the CTA's shared memory goes away
+          // the last buffer release lands before the CTA's shared memory goes away
           const int j = n_tiles - 1;
-          mbar_wait(bar(B_KV_EMPTY + j % TC_STAGES), (j / TC_STAGES) & 1, abort_flag);
+          if (FP8)
+            mbar_wait(bar(B_CONV_FREE + (j & 1)), (j >> 1) & 1, abort_flag);
+          else
+            mbar_wait(bar(B_KV_EMPTY + j % C::STAGES), (j / C::STAGES) & 1, abort_flag);
         }
       }
     }
-  } else if (warp >= 4) {
-    // ---------------- softmax / epilogue: one thread per row ----------------
+  } else if (warp < 4) {
+    if constexpr (FP8) {
+      // ---------------- fp8 -> f16 widening (warps 2-3) ----------------
+      const int ct = tid - 64;                      // 0 .. 63
+      constexpr int CH = C::KEYS * 8;               // 16-byte raw chunks per K (or V) tile
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % C::STAGES, cb = j & 1;
+        if (!mbar_wait(bar(B_KV_FULL + s), (j / C::STAGES) & 1, abort_flag)) break;
+        if (j >= 2 && !mbar_wait(bar(B_CONV_FREE + cb), ((j >> 1) - 1) & 1, abort_flag)) break;
+        const uint8_t* raw = smem + C::OFF_KV + s * C::STAGE_BYTES;
+        uint8_t* dst = smem + C::OFF_CONV + cb * 2 * C::OP_BYTES;
+        const int k0 = lo + j * C::KEYS;
+        for (int c = ct; c < 2 * CH; c += 64) {
+          const int which = c / CH, cc = c - which * CH;
+          const int r = cc >> 3, ch = cc & 7;       // key row, 16-element column group
+          uint4 a = make_uint4(0u, 0u, 0u, 0u), bq = a;
+          if (k0 + r < hi) {
+            const uint4 w = *reinterpret_cast<const uint4*>(raw + which * C::RAW_BYTES + r * 128 + ch * 16);
+            a.x = e4m3x2_to_f16x2((uint16_t)(w.x & 0xffff));
+            a.y = e4m3x2_to_f16x2((uint16_t)(w.x >> 16));
+            a.z = e4m3x2_to_f16x2((uint16_t)(w.y & 0xffff));
+            a.w = e4m3x2_to_f16x2((uint16_t)(w.y >> 16));
+            bq.x = e4m3x2_to_f16x2((uint16_t)(w.z & 0xffff));
+            bq.y = e4m3x2_to_f16x2((uint16_t)(w.z >> 16));
+            bq.z = e4m3x2_to_f16x2((uint16_t)(w.w & 0xffff));
+            bq.w = e4m3x2_to_f16x2((uint16_t)(w.w >> 16));
+          }
+          // 16 f16 = 2 chunks of the swizzled operand row (half = ch / 4)
+          uint8_t* row = dst + which * C::OP_BYTES + (ch >> 2) * (C::KEYS * 128) + r * 128;
+          const int c0 = (ch & 3) * 2;
+          *reinterpret_cast<uint4*>(row + (((c0) ^ (r & 7)) << 4)) = a;
+          *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = bq;
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(B_CONV_FULL + cb));
+          mbar_arrive(bar(B_KV_EMPTY + s));
+        }
+      }
+    }
+  } else {
+    // ---------------- softmax / epilogue: one thread per row (warps 4-7) ----------------
     const int quad = warp - 4;
     const int r = quad * 32 + lane;                 // row of the block = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
@@ -208,17 +291,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const float c = p.scale_log2;
     float m_used = -INFINITY;                       // in units of s * c (log2 domain)
     float l = 0.f;
-    float s[TC_KEYS];
-    uint32_t pk[TC_KEYS / 2];
+    float s[C::KEYS];
+    uint32_t pk[C::KEYS / 2];
     bool live = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    if (FP8) {
+      // Q to f16, in place (each thread its own row)
+      if (!mbar_wait(bar(B_Q), 0, abort_flag)) live = false;
+      if (live) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint4* q4 = reinterpret_cast<uint4*>(smem + C::OFF_Q + half * (C::Q_BYTES / 2) + r * 128);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            uint4 v = q4[ch];
+            v.x = bf16x2_to_f16x2(v.x);
+            v.y = bf16x2_to_f16x2(v.y);
+            v.z = bf16x2_to_f16x2(v.z);
+            v.w = bf16x2_to_f16x2(v.w);
+            q4[ch] = v;
+          }
+        }
+        fence_proxy_async();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_Q_READY));
+    }
+    for (int j = 0; live && j < n_tiles; ++j) {
       const int sb = j & 1;
       if (!mbar_wait(bar(B_S_FULL + sb), (j >> 1) & 1, abort_flag)) { live = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int q = 0; q < TC_KEYS / 32; ++q) {
+      for (int q = 0; q < C::KEYS / 32; ++q) {
         uint32_t raw[32];
-        tmem_ld32(lane_addr + sb * TC_KEYS + q * 32, raw);
+        tmem_ld32(lane_addr + sb * C::KEYS + q * 32, raw);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; ++e) s[q * 32 + e] = __uint_as_float(raw[e]);
@@ -227,10 +332,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_S_FREE + sb));
 
-      const int k0 = lo + j * TC_KEYS;
-      if (k0 + TC_KEYS > prefix || k0 + TC_KEYS > hi) {
+      const int k0 = lo + j * C::KEYS;
+      if (k0 + C::KEYS > prefix || k0 + C::KEYS > hi) {
 #pragma unroll
-        for (int cc = 0; cc < TC_KEYS; ++cc) {
+        for (int cc = 0; cc < C::KEYS; ++cc) {
           const int key = k0 + cc;
           bool vis = key < hi;
           if (vis && key >= prefix) {
@@ -247,7 +352,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int cc = 0; cc < TC_KEYS; ++cc) mx = fmaxf(mx, s[cc]);
+      for (int cc = 0; cc < C::KEYS; ++cc) mx = fmaxf(mx, s[cc]);
       mx *= c;  // c > 0
       float m_new = m_used;
       if (mx > m_used + 8.f) m_new = mx;   // also taken when m_used = -inf and mx is finite
@@ -255,11 +360,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const float base = m_new == -INFINITY ? 0.f : m_new;
       float sum = 0.f;
 #pragma unroll
-      for (int cc = 0; cc < TC_KEYS; cc += 2) {
+      for (int cc = 0; cc < C::KEYS; cc += 2) {
         const float p0 = ex2(fmaf(s[cc], c, -base));
         const float p1 = ex2(fmaf(s[cc + 1], c, -base));
         sum += p0 + p1;
-        pk[cc / 2] = pack_bf16x2(p0, p1);
+        pk[cc / 2] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
       }
       l = l * alpha + sum;
       // P buffer and O are free once the previous PV has completed.
@@ -267,35 +372,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (!mbar_wait(bar(B_O_DONE), (j - 1) & 1, abort_flag)) { live = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          for (int q = 0; q < TC_D / 32; ++q) {
+          for (int q = 0; q < C::D / 32; ++q) {
             uint32_t ov[32];
-            tmem_ld32(lane_addr + TC_COL_O + q * 32, ov);
+            tmem_ld32(lane_addr + C::COL_O + q * 32, ov);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(lane_addr + TC_COL_O + q * 32, ov);
+            tmem_st32(lane_addr + C::COL_O + q * 32, ov);
           }
           tmem_wait_st();
         }
       }
-      // Rows of V past the chunk end inside the last 16-key box may hold
-      // stale (even NaN) slots: zero them, since 0 * NaN would poison O.
-      const int tail = hi - k0;
-      if (tail < TC_KEYS && (tail & 15)) {
-        const int zlo = tail, zhi = (tail + 15) & ~15;
-        uint8_t* vt = smem + TC_OFF_KV + (j % TC_STAGES) * TC_STAGE_BYTES + TC_KT_BYTES;
-        for (int z = r; z < (zhi - zlo) * 16; z += TC_ROWS) {
-          const int row = zlo + z / 16, half = (z / 8) & 1, ch = z & 7;
-          *reinterpret_cast<uint4*>(vt + half * (TC_KEYS * 128) + row * 128 + (ch << 4)) =
-              make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (!FP8) {
+        // Rows of V past the chunk end inside the last 16-key box may hold
+        // stale (even NaN) slots: zero them, since 0 * NaN would poison O.
+        const int tail = hi - k0;
+        if (tail < C::KEYS && (tail & 15)) {
+          const int zlo = tail, zhi = (tail + 15) & ~15;
+          uint8_t* vt = smem + C::OFF_KV + (j % C::STAGES) * C::STAGE_BYTES + C::OP_BYTES;
+          for (int z = r; z < (zhi - zlo) * 16; z += C::ROWS) {
+            const int row = zlo + z / 16, half = (z / 8) & 1, ch = z & 7;
+            *reinterpret_cast<uint4*>(vt + half * (C::KEYS * 128) + row * 128 + (ch << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
         }
       }
       // P row -> shared memory, K-major 128-byte-swizzled [key block][row][128 B]
-      uint8_t* prow = smem + TC_OFF_P;
+      uint8_t* prow = smem + C::OFF_P;
 #pragma unroll
-      for (int ch = 0; ch < TC_KEYS / 8; ++ch) {
+      for (int ch = 0; ch < C::KEYS / 8; ++ch) {
         const int kb = ch >> 3, c8 = ch & 7;
-        *reinterpret_cast<uint4*>(prow + kb * (TC_ROWS * 128) + r * 128 + ((c8 ^ (r & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(prow + kb * (C::ROWS * 128) + r * 128 + ((c8 ^ (r & 7)) << 4)) =
             make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
       }
       fence_proxy_async();
@@ -314,13 +421,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int g = (row0 + r) - t * G;
         orow = (size_t)(qo0 + t) * p.h_q + (size_t)h * G + g;
       }
-      for (int q = 0; q < TC_D / 32; ++q) {
+      for (int q = 0; q < C::D / 32; ++q) {
         uint32_t ov[32];
-        tmem_ld32(lane_addr + TC_COL_O + q * 32, ov);
+        tmem_ld32(lane_addr + C::COL_O + q * 32, ov);
         tmem_wait_ld();
         if (!row_ok) continue;
         if (it.part_row < 0) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * TC_D + q * 32);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * C::D + q * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint4 w;
@@ -331,7 +438,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             dst[e] = w;
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(p.part_out + ((size_t)it.part_row + r) * TC_D + q * 32);
+          float4* dst = reinterpret_cast<float4*>(p.part_out + ((size_t)it.part_row + r) * C::D + q * 32);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
@@ -353,24 +460,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   grid_dependents_launch();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TC_TMEM_COLS);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
   if (tid == 0 && *abort_flag) atomicOr(p.status, VA_DEV_TIMEOUT);
 }
 
-}  // namespace
-
-cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, int n_items,
-                              cudaStream_t stream) {
-  if (n_items <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(verify_partial_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+template <bool FP8>
+cudaError_t launch_tc(const PartialParams& p, const TcMaps& maps, int n_items,
+                      cudaStream_t stream) {
+  auto kern = verify_partial_tc_kernel<FP8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TcCfg<FP8>::SMEM);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PartialParams*>(&p), const_cast<TcMaps*>(&maps)};
-  return launch_kernel(reinterpret_cast<const void*>(verify_partial_tc_kernel), dim3(n_items),
-                       dim3(TC_THREADS), TC_SMEM, stream, args, /*pdl=*/true);
+  return launch_kernel(reinterpret_cast<const void*>(kern), dim3(n_items),
+                       dim3(TcCfg<FP8>::THREADS), TcCfg<FP8>::SMEM, stream, args, /*pdl=*/true);
 }
 
-int tc_smem_bytes() { return TC_SMEM; }
+}  // namespace
+
+cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, bool kv_fp8,
+                              int n_items, cudaStream_t stream) {
+  if (n_items <= 0) return cudaSuccess;
+  return kv_fp8 ? launch_tc<true>(p, maps, n_items, stream)
+                : launch_tc<false>(p, maps, n_items, stream);
+}
 
 }  // namespace va

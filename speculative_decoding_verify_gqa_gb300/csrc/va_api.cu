@@ -145,14 +145,18 @@ int make_tc_maps(const void* q, int64_t total_qo, const void* k_cache, const voi
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return VA_ERR_CUDA;
   }
+  const bool fp8 = hd->kv_dtype == VA_DTYPE_FP8_E4M3;
+  const cuuint64_t es = fp8 ? 1 : 2;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)P, (cuuint64_t)hd->h_kv, (cuuint64_t)num_pages};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)P * D * 2, (cuuint64_t)hd->h_kv * P * D * 2};
-  cuuint32_t box[4] = {64, 16, 1, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)D * es, (cuuint64_t)P * D * es,
+                           (cuuint64_t)hd->h_kv * P * D * es};
+  cuuint32_t box[4] = {fp8 ? 128u : 64u, 16, 1, 1};
   const void* src[2] = {k_cache, v_cache};
   CUtensorMap* dst[2] = {&m->k, &m->v};
   for (int i = 0; i < 2; ++i)
-    if (enc(dst[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(src[i]), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (enc(dst[i], fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+            const_cast<void*>(src[i]), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return VA_ERR_CUDA;
   return VA_OK;
@@ -262,7 +266,8 @@ int verify_attn_partial(const void* q, const void* k_cache, const void* v_cache,
     TcMaps maps;
     rc = make_tc_maps(q, hd->total_qo, k_cache, v_cache, num_pages, hd, &maps);
     if (rc) return rc;
-    e = launch_partial_tc(p, maps, hd->n_items, static_cast<cudaStream_t>(stream));
+    e = launch_partial_tc(p, maps, hd->kv_dtype == VA_DTYPE_FP8_E4M3, hd->n_items,
+                          static_cast<cudaStream_t>(stream));
   } else {
     e = launch_partial_mma(p, hd->kernel, hd->head_dim, hd->kv_dtype == VA_DTYPE_FP8_E4M3,
                            hd->n_items, static_cast<cudaStream_t>(stream));

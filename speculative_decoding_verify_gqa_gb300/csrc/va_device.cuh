@@ -82,6 +82,25 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t codes) {
   return pack_bf16x2(f.x, f.y);
 }
 
+// Two fp8-e4m3 codes (low byte first) -> two f16 (exact), one instruction.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// bf16x2 -> f16x2 (exact for values inside f16's normal range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+  return pack_f16x2(lo, hi);
+}
+
 // Byte offset of 16-byte chunk `ch` of row `r` in a row-major shared tile of
 // `row_bytes` per row, XOR-swizzled so that 8 consecutive rows' same chunk
 // fall in 8 different bank groups (conflict-free ldmatrix).

@@ -79,14 +79,15 @@ inline cudaError_t launch_kernel(const void* func, dim3 grid, dim3 block, size_t
 cudaError_t launch_partial_mma(const PartialParams& p, int kernel, int head_dim, bool kv_fp8,
                                int n_items, cudaStream_t stream);
 
-// TMA descriptors of the tensor-core variant: q as [total_qo, h_q, 128] with
-// 64 x G x (128 / G) boxes, the caches as [num_pages, h_kv, P, 128] with
-// 64 x 16 x 1 x 1 boxes; bf16, 128-byte swizzle, zero fill out of bounds.
+// TMA descriptors of the tensor-core variant: q as [total_qo, h_q, 128] bf16
+// with 64 x G x (128 / G) boxes, 128-byte swizzle; the caches as
+// [num_pages, h_kv, P, 128] with 64 x 16 x 1 x 1 bf16 boxes (128-byte swizzle)
+// or 128 x 16 x 1 x 1 fp8 boxes (no swizzle); zero fill out of bounds.
 struct TcMaps {
   CUtensorMap q, k, v;
 };
-cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, int n_items,
-                              cudaStream_t stream);
+cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, bool kv_fp8,
+                              int n_items, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int head_dim, int n_merge, int block_rows,
                          cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);

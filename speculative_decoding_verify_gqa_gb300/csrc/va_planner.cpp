@@ -118,10 +118,9 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     max_rows = std::max(max_rows, (int64_t)G * L);
   }
 
-  // The tensor-core variant serves head_dim 128, bf16 caches, page sizes that
-  // are multiples of its 16-row TMA boxes, and groups that tile its 128 rows.
-  const bool tc_ok = head_dim == 128 && kv_dtype == VA_DTYPE_BF16 && page_size % 16 == 0 &&
-                     128 % G == 0;
+  // The tensor-core variant serves head_dim 128, page sizes that are multiples
+  // of its 16-row TMA boxes, and groups that tile its 128 rows.
+  const bool tc_ok = head_dim == 128 && page_size % 16 == 0 && 128 % G == 0;
   int kernel = o.kernel;
   if (kernel == VA_KERNEL_TC_128 && !tc_ok) return VA_ERR_UNSUPPORTED;
   if (kernel == VA_KERNEL_AUTO) kernel = max_rows <= 64 ? kKernelMma64 : kKernelMma128;

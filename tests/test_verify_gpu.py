@@ -160,6 +160,11 @@ TC_CASES = [
                     qo=("fixed", [150]), mask="causal")),
     ("masked_rows", dict(batch=2, h_q=8, h_kv=2, d=128, prefix=("fixed", [0, 5]),
                          qo=("fixed", [40, 37]), mask="none_visible")),
+    ("fp8_tree", dict(batch=2, h_q=32, h_kv=8, d=128, prefix=("fixed", [1000, 77]),
+                      qo=("fixed", [64, 20]), mask="tree", kv_dtype=synthetic.FP8)),
+    ("fp8_chain_page64", dict(batch=3, h_q=16, h_kv=2, d=128, page_size=64,
+                              prefix=("fixed", [500, 3, 129]), qo=("fixed", [9, 16, 1]),
+                              mask="causal", kv_dtype=synthetic.FP8)),
 ]
 
 
