@@ -94,6 +94,7 @@ extern "C" {
 #define VA_ERR_CUDA (-5)               /* a CUDA runtime call failed */
 #define VA_ERR_DEVICE_CHECK (-6)       /* a kernel's bounds check fired (see device_status) */
 #define VA_ERR_PLAN_BUFFER_TOO_SMALL (-7)
+#define VA_ERR_STATIC_SCRATCH_TOO_SMALL (-8) /* plan needs more than VA_STATIC_SCRATCH_BYTES */
 
 /* Element types. */
 #define VA_DTYPE_BF16 0
@@ -242,6 +243,49 @@ int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_
                     const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
                     int num_kv_heads, int head_dim, int page_size, int num_pages, int kv_dtype,
                     int64_t total_new, int* status_d, void* stream);
+
+/*
+ * verify_attn_run for callers that cannot allocate device memory.
+ *
+ * No page describes this entry point; it exists for callers that may not
+ * call cudaMalloc (or any allocating routine) at all -- e.g. code running
+ * inside a memory pool or graph-building framework that owns every device
+ * allocation, or a plugin host that forbids allocation on its hot path -- and
+ * so cannot hand verify_attn_run a workspace.  It computes exactly what
+ * verify_attn_run computes (same kernels, same plan), but its scratch (the
+ * work list, the fp32 split partials and the device status word) lives in one
+ * file-scope __device__ array of VA_STATIC_SCRATCH_BYTES inside this library.
+ *
+ *  - Allocates nothing: no cudaMalloc / cudaFree and no allocating library
+ *    call.  The caller still owns and passes every input and output; plan_h is
+ *    a plan from verify_attn_plan_host (the workspace arguments of
+ *    verify_attn_plan are not needed).
+ *  - Limit: a plan whose workspace exceeds VA_STATIC_SCRATCH_BYTES is refused
+ *    with VA_ERR_STATIC_SCRATCH_TOO_SMALL before anything is enqueued.
+ *  - Memory: every GPU that loads the library holds the array until the
+ *    process exits.
+ *  - Set-up: the first call on each device (with that device current) looks
+ *    up the array's device address with cudaGetSymbolAddress; make that first
+ *    call before any stream capture begins.
+ *  - Every call copies the plan's work list from plan_h into the array and
+ *    clears its status word on `stream` (so plan_h, if pinned, must stay
+ *    unchanged until the copy has run), then launches the kernels.  All calls
+ *    share the one array, which keeps the last call's contents: calls that can
+ *    overlap on the GPU (different streams, or devices sharing the array's
+ *    context) race and must be serialised by the caller.  Device-side check
+ *    bits are not reported by this entry point.
+ * Errors: as verify_attn_run, plus VA_ERR_STATIC_SCRATCH_TOO_SMALL, and
+ * VA_ERR_CUDA if the address look-up or an enqueue fails.
+ */
+#define VA_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+int verify_attn_run_static_scratch(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* kv_indptr, const int32_t* kv_indices,
+                                   const int32_t* last_page_len, const int32_t* qo_indptr,
+                                   const uint8_t* mask, const int32_t* mask_indptr,
+                                   int num_qo_heads, int num_kv_heads, int head_dim,
+                                   int page_size, float sm_scale, float k_scale, float v_scale,
+                                   void* out, float* lse, int num_pages, const void* plan_h,
+                                   void* stream);
 
 #ifdef __cplusplus
 }

@@ -94,6 +94,8 @@ def lib():
         "verify_attn_device_status": (i32, [P, Pi, P]),
         "paged_kv_append": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, P,
                                   P]),
+        "verify_attn_run_static_scratch": (i32, [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32,
+                                                 f32, f32, f32, P, P, i32, P, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -349,3 +351,28 @@ def paged_kv_append(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_pag
                                int(num_pages), kv_dtype, int(total_new), _dp(status),
                                _stream(stream))
     _check("paged_kv_append", rc)
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def verify_attn_run_static_scratch(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len,
+                                   qo_indptr, mask, mask_indptr, plan: Plan, sm_scale=0.0,
+                                   k_scale=1.0, v_scale=1.0, out=None, lse=None, want_lse=True,
+                                   num_pages=None, stream=None):
+    """verify_attn_run for callers that cannot allocate device memory: the
+    library's own static scratch array (STATIC_SCRATCH_BYTES) stands in for
+    the workspace, so `plan` may come from verify_attn_plan_host (no device
+    workspace).  The first call on a device looks up the array's address
+    (make it before any graph capture); calls that overlap on the GPU share
+    the array and race."""
+    out, lse = _alloc_out(q, plan, out, lse, want_lse)
+    if num_pages is None:
+        num_pages = k_cache.shape[0]
+    rc = lib().verify_attn_run_static_scratch(
+        _dp(q), _dp(k_cache), _dp(v_cache), _dp(kv_indptr), _dp(kv_indices), _dp(last_page_len),
+        _dp(qo_indptr), _dp(mask), _dp(mask_indptr), plan.num_qo_heads, plan.num_kv_heads,
+        plan.head_dim, plan.page_size, float(sm_scale), float(k_scale), float(v_scale), _dp(out),
+        _dp(lse), int(num_pages), _hp(plan.host), _stream(stream))
+    _check("verify_attn_run_static_scratch", rc)
+    return out, lse

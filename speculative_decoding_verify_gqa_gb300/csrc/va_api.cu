@@ -6,6 +6,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/verify_attn.h"
 #include "va_internal.h"
 #include "va_kernels.h"
@@ -176,6 +178,8 @@ const char* verify_attn_status_string(int status) {
     case VA_ERR_CUDA: return "CUDA runtime error";
     case VA_ERR_DEVICE_CHECK: return "a device-side check failed";
     case VA_ERR_PLAN_BUFFER_TOO_SMALL: return "host plan buffer too small";
+    case VA_ERR_STATIC_SCRATCH_TOO_SMALL:
+      return "plan needs more scratch than the library's static scratch array holds";
     default: return "unknown status";
   }
 }
@@ -315,6 +319,68 @@ int verify_attn_run(const void* q, const void* k_cache, const void* v_cache,
   if (rc) return rc;
   return verify_attn_merge(qo_indptr, num_qo_heads, num_kv_heads, head_dim, out, lse, plan_h,
                            workspace_d, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+// ---- scratch for callers that cannot allocate ---------------------------------
+// One file-scope device array serves every verify_attn_run_static_scratch call
+// (work list, split partials, status word).  In host code its name is only a
+// host-side stand-in for the symbol; its device address comes from
+// cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) unsigned char g_static_scratch[VA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+int static_scratch_address(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return VA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *ptr = g_scratch_ptr[dev];
+  return VA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int verify_attn_run_static_scratch(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* kv_indptr, const int32_t* kv_indices,
+                                   const int32_t* last_page_len, const int32_t* qo_indptr,
+                                   const uint8_t* mask, const int32_t* mask_indptr,
+                                   int num_qo_heads, int num_kv_heads, int head_dim,
+                                   int page_size, float sm_scale, float k_scale, float v_scale,
+                                   void* out, float* lse, int num_pages, const void* plan_h,
+                                   void* stream) {
+  const PlanHeader* hd = plan_header(plan_h);
+  if (!hd) return VA_ERR_INVALID_ARGUMENT;
+  if (hd->ws_bytes > VA_STATIC_SCRATCH_BYTES) return VA_ERR_STATIC_SCRATCH_TOO_SMALL;
+  void* scratch = nullptr;
+  int rc = static_scratch_address(&scratch);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(scratch);
+  // the status word starts at zero; the work list comes from this plan
+  if (cudaMemsetAsync(ws + hd->off_status, 0, sizeof(int), s) != cudaSuccess) return VA_ERR_CUDA;
+  const size_t list =
+      (size_t)hd->n_items * sizeof(WorkItem) + (size_t)hd->n_merge * sizeof(MergeItem);
+  if (list > 0 &&
+      cudaMemcpyAsync(ws + hd->off_items, static_cast<const char*>(plan_h) + sizeof(PlanHeader),
+                      list, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return VA_ERR_CUDA;
+  return verify_attn_run(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr,
+                         mask, mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size,
+                         sm_scale, k_scale, v_scale, out, lse, num_pages, plan_h, scratch,
+                         VA_STATIC_SCRATCH_BYTES, stream);
 }
 
 int verify_attn_device_status(void* workspace_d, int* bits, void* stream) {

@@ -1,0 +1,78 @@
+"""The allocation-free entry point, verify_attn_run_static_scratch, for
+callers that may not allocate device memory (their framework owns every
+allocation, or allocation is forbidden on their hot path).  It must give the
+same result as verify_attn_run, call after call, although its scratch is the
+library's one static array rather than a caller workspace.
+
+Collected last on purpose (file name), so a run that stops at the first
+failure has already run every other test.  Works alone in a fresh process
+and after the rest of the suite."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from gpu_util import DeviceWorkload, compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def va():
+    import __graft_entry__
+    __graft_entry__.build()
+    import speculative_decoding_verify_gqa_gb300 as m
+    return m
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_tree_verify", "tiny_verify"])
+def test_static_scratch_matches_run_twice_in_a_row(va, name):
+    wl = synthetic.make_workload(name)
+    dw = DeviceWorkload(wl)
+    ref_out, ref_lse, plan = dw.run()            # the existing entry point, caller workspace
+    torch.cuda.synchronize()
+    # a host-only plan: this caller never allocates a device workspace
+    hplan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
+                                     wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                     kv_dtype=wl.kv_dtype)
+    if name == "llama3_8b_tree_verify":
+        assert hplan.header()["n_merge"] > 0     # the split partials live in the static array
+    assert hplan.workspace_bytes <= va.STATIC_SCRATCH_BYTES
+    ref_o = ref_out.float().cpu().numpy()
+    ref_l = ref_lse.cpu().numpy()
+    for call in range(2):
+        out = torch.full_like(dw.q, float("nan"))
+        lse = torch.full(dw.q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+        # through the C ABI directly
+        L = va.lib()
+        rc = L.verify_attn_run_static_scratch(
+            va._dp(dw.q), va._dp(dw.k_cache), va._dp(dw.v_cache), va._dp(dw.kv_indptr),
+            va._dp(dw.kv_indices), va._dp(dw.last_page_len), va._dp(dw.qo_indptr),
+            va._dp(dw.mask), va._dp(dw.mask_indptr), wl.h_q, wl.h_kv, wl.d, wl.page_size,
+            ctypes.c_float(wl.sm_scale), ctypes.c_float(wl.k_scale), ctypes.c_float(wl.v_scale),
+            va._dp(out), va._dp(lse), wl.num_pages, va._hp(hplan.host),
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0, va.status_string(rc)
+        torch.cuda.synchronize()
+        o = out.float().cpu().numpy()
+        l = lse.cpu().numpy()
+        assert np.abs(o - ref_o).max() <= 1e-2
+        assert np.abs(l - ref_l).max() <= 1e-3
+        compare(wl, out, lse, rows=None if name == "tiny_verify" else synthetic.sample_rows(wl, 64))
+
+
+def test_static_scratch_refuses_plans_beyond_its_size(va):
+    # 64 requests x 64 query heads with a long prefix, forced into many splits
+    wl = synthetic.make_custom(batch=64, h_q=64, h_kv=8, d=128, prefix=("fixed", [8192] * 64),
+                               qo=("fixed", [16] * 64), mask="causal", with_values=False)
+    plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, None, 64, 8,
+                                    128, 16, min_chunk=64, target_ctas=600, max_splits=64)
+    assert plan.workspace_bytes > va.STATIC_SCRATCH_BYTES
+    fake = ctypes.c_void_p(256)
+    rc = va.lib().verify_attn_run_static_scratch(
+        fake, fake, fake, fake, fake, fake, fake, None, None, 64, 8, 128, 16,
+        ctypes.c_float(0.0), ctypes.c_float(1.0), ctypes.c_float(1.0), fake, None, 10,
+        va._hp(plan.host), None)
+    assert rc == -8
