@@ -17,7 +17,7 @@ namespace {
 template <int D>
 __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) {
   constexpr int V = D / 32;
-  constexpr int CH = 8;  // splits whose loads are issued together
+  constexpr int CH = 16;  // splits whose loads are issued together
   const MergeItem it = p.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * 4 + warp;

@@ -144,7 +144,21 @@ __global__ void __launch_bounds__(256, 1)
         tma_load_3d(sbase + C::OFF_Q + half * (C::Q_BYTES / 2), &maps.q, half * 64, h * G, tok0,
                     bar(B_Q));
       int bad = 0;
+      // Page ids of a tile's 16-key boxes (-1 past the chunk), loaded one tile
+      // ahead so their latency hides behind the previous tile's wait.
+      constexpr int NG = C::KEYS / 16;
+      int cur[NG], nxt[NG];
+      auto load_pages = [&](int j, int* pg) {
+        const int k0 = lo + j * C::KEYS;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const int key = k0 + 16 * g;
+          pg[g] = (j < n_tiles && key < hi) ? __ldg(p.kv_indices + pg0 + (key >> p.log2_page)) : -1;
+        }
+      };
+      load_pages(0, cur);
       for (int j = 0; j < n_tiles; ++j) {
+        load_pages(j + 1, nxt);
         const int s = j % C::STAGES;
         if (j >= C::STAGES &&
             !mbar_wait(bar(B_KV_EMPTY + s), ((j / C::STAGES) - 1) & 1, abort_flag))
@@ -153,12 +167,13 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t kdst = sbase + C::OFF_KV + s * C::STAGE_BYTES;
         const uint32_t vdst = kdst + C::STAGE_BYTES / 2;
         const int k0 = lo + j * C::KEYS;
-        for (int g = 0; g < C::KEYS / 16; ++g) {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
           const int key = k0 + 16 * g;
           int page = p.num_pages;  // outside the pool: zero fill
           int slot = 0;
           if (key < hi) {
-            const int pid = __ldg(p.kv_indices + pg0 + (key >> p.log2_page));
+            const int pid = cur[g];
             if ((unsigned)pid < (unsigned)p.num_pages) {
               page = pid;
               slot = key & (p.page_size - 1);
@@ -177,6 +192,8 @@ __global__ void __launch_bounds__(256, 1)
             }
           }
         }
+#pragma unroll
+        for (int g = 0; g < NG; ++g) cur[g] = nxt[g];
       }
       if (bad) atomicOr(p.status, VA_DEV_BAD_PAGE);
     }
@@ -320,13 +337,13 @@ __global__ void __launch_bounds__(256, 1)
       const int sb = j & 1;
       if (!mbar_wait(bar(B_S_FULL + sb), (j >> 1) & 1, abort_flag)) { live = false; break; }
       tc_fence_after();
+      {
+        uint32_t raw[C::KEYS];
 #pragma unroll
-      for (int q = 0; q < C::KEYS / 32; ++q) {
-        uint32_t raw[32];
-        tmem_ld32(lane_addr + sb * C::KEYS + q * 32, raw);
+        for (int q = 0; q < C::KEYS / 32; ++q) tmem_ld32(lane_addr + sb * C::KEYS + q * 32, raw + q * 32);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[q * 32 + e] = __uint_as_float(raw[e]);
+        for (int e = 0; e < C::KEYS; ++e) s[e] = __uint_as_float(raw[e]);
       }
       tc_fence_before();
       __syncwarp();

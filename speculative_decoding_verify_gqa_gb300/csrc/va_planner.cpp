@@ -164,27 +164,33 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     return std::max<int64_t>(min_chunk,
                              ceil_div(ceil_div(W, std::max<int64_t>(target, 1)), TK) * TK);
   };
-  auto split_of = [&](const Unit& u, int64_t chunk, int64_t* cu) {
+  // A unit is cut either into near-equal chunks (equal = true) or into full
+  // chunks of the target size plus a shorter remainder; the remainders let
+  // the longest-first packing fill SMs that equal cuts would leave idle.
+  auto split_of = [&](const Unit& u, int64_t chunk, bool equal, int64_t* cu) {
     int64_t n = ceil_div(u.kv_end, chunk);
     if (o.max_splits > 0) n = std::min<int64_t>(n, o.max_splits);
     n = std::max<int64_t>(n, 1);
-    *cu = ceil_div(ceil_div(u.kv_end, n), TK) * TK;
+    *cu = equal || n * chunk < u.kv_end ? ceil_div(ceil_div(u.kv_end, n), TK) * TK : chunk;
     return ceil_div(u.kv_end, *cu);
   };
   int64_t chunk;
+  bool equal = true;
   if (o.target_ctas > 0) {
     chunk = chunk_for(std::min<int64_t>(o.target_ctas, kMaxTargetPerSm * num_sms));
   } else {
     chunk = chunk_for(slots);
     double best = -1.0;
     std::vector<int64_t> costs;
-    for (int waves : {1, 2, 3, 4}) {
+    for (int cand = 0; cand < 8; ++cand) {
+      const int waves = 1 + (cand >> 1);
+      const bool eq = (cand & 1) == 0;
       const int64_t target = std::min<int64_t>(waves * slots, kMaxTargetPerSm * num_sms);
       const int64_t c = chunk_for(target);
       costs.clear();
       for (const Unit& u : units) {
         int64_t cu;
-        const int64_t n = split_of(u, c, &cu);
+        const int64_t n = split_of(u, c, eq, &cu);
         for (int64_t s = 0; s < n; ++s) {
           const int64_t keys = std::min<int64_t>(cu, u.kv_end - s * cu);
           const int64_t cost = fixed_bytes + keys * key_bytes +
@@ -205,6 +211,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
       if (best < 0 || (double)finish < best * 0.97) {
         best = (double)finish;
         chunk = c;
+        equal = eq;
       }
     }
   }
@@ -220,7 +227,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   int64_t order = 0;
   for (const Unit& u : units) {
     int64_t cu;
-    const int64_t n = split_of(u, chunk, &cu);
+    const int64_t n = split_of(u, chunk, equal, &cu);
     for (int h = 0; h < num_kv_heads; ++h) {
       int64_t base = part_rows;
       if (n > 1) {
@@ -236,8 +243,16 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     }
   }
   if (part_rows > INT32_MAX) return VA_ERR_UNSUPPORTED;
-  std::stable_sort(items.begin(), items.end(),
-                   [](const Tmp& a, const Tmp& b) { return a.cost > b.cost; });
+  // Longest first; among equals, row blocks that read the same (request, KV
+  // head, kv chunk) sit next to each other so they run together and the
+  // later ones find the chunk in L2.
+  std::stable_sort(items.begin(), items.end(), [](const Tmp& a, const Tmp& b) {
+    if (a.cost != b.cost) return a.cost > b.cost;
+    if (a.it.b != b.it.b) return a.it.b < b.it.b;
+    if (a.it.h != b.it.h) return a.it.h < b.it.h;
+    if (a.it.kv_lo != b.it.kv_lo) return a.it.kv_lo < b.it.kv_lo;
+    return a.it.row0 < b.it.row0;
+  });
 
   size_t need = sizeof(PlanHeader) + items.size() * sizeof(WorkItem) +
                 merges.size() * sizeof(MergeItem);
