@@ -238,7 +238,19 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
       }
       // Visibility: keys < prefix always; draft key prefix + u when the mask
       // bit (t, u) is set (or u <= t without a mask); nothing at or past hi.
-      if (k0 + C::BN > prefix || k0 + C::BN > hi) {
+      if (!p.mask && (k0 + C::BN > prefix || k0 + C::BN > hi)) {
+        // causal drafts: a row sees keys below min(hi, prefix + t + 1)
+        const int lim_lo = min(hi, prefix + t_lo + 1) - k0;
+        const int lim_hi = min(hi, prefix + t_hi + 1) - k0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int kc = j * 8 + 2 * tq + (e & 1);
+            if (kc >= (e < 2 ? lim_lo : lim_hi)) s[j][e] = -INFINITY;
+          }
+        }
+      } else if (k0 + C::BN > prefix || k0 + C::BN > hi) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
 #pragma unroll

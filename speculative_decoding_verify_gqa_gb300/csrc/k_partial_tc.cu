@@ -43,8 +43,9 @@ namespace {
 template <bool FP8>
 struct TcCfg {
   static constexpr int ROWS = 128, D = 128, THREADS = 256;
-  static constexpr int KEYS = FP8 ? 64 : 128;            // keys per tile
+  static constexpr int KEYS = 64;                        // keys per tile
   static constexpr int STAGES = FP8 ? 3 : 2;             // TMA stages (raw fp8, or bf16 operands)
+  static constexpr int CTAS_PER_SM = FP8 ? 1 : 2;        // bf16: two CTAs hide each other's waits
   static constexpr int Q_BYTES = ROWS * D * 2;           // [2 halves][128 rows][128 B]
   static constexpr int OP_BYTES = KEYS * D * 2;          // 16-bit K (or V) operand tile
   static constexpr int RAW_BYTES = KEYS * D;             // fp8 K (or V) tile [keys][128 B]
@@ -56,11 +57,13 @@ struct TcCfg {
   static constexpr int OFF_CONV = OFF_KV + STAGES * STAGE_BYTES;
   static constexpr int OFF_P = OFF_CONV + CONV_BUFS * 2 * OP_BYTES;
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;       // barriers; slack for 1024-B alignment
-  static constexpr uint32_t TMEM_COLS = FP8 ? 256 : 512;  // S0 | S1 | O
+  static constexpr int SMEM = OFF_BAR + 256;              // + barriers, TMEM address, abort flag
+  static constexpr uint32_t TMEM_COLS = 256;              // S0 | S1 | O (64 + 64 + 128 columns)
   static constexpr uint32_t COL_O = 2 * KEYS;
   static constexpr int CONV_WARPS = 2;                    // warps 2-3 (fp8 only)
-  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  // 228 KB per SM, 1 KB reserved per CTA
+  static_assert(CTAS_PER_SM * (SMEM + 1024) <= 228 * 1024, "shared memory budget");
+  static_assert(CTAS_PER_SM * TMEM_COLS <= 512, "tensor memory budget");
 };
 
 constexpr float kLn2 = 0.6931471805599453f;
@@ -76,13 +79,15 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) 
 }
 
 template <bool FP8>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
     verify_partial_tc_kernel(const PartialParams p, const __grid_constant__ TcMaps maps) {
   using C = TcCfg<FP8>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {  // the swizzled operand tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicOr(p.status, VA_DEV_BAD_TABLE);
+    return;
+  }
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * B_COUNT);
@@ -351,20 +356,44 @@ __global__ void __launch_bounds__(256, 1)
 
       const int k0 = lo + j * C::KEYS;
       if (k0 + C::KEYS > prefix || k0 + C::KEYS > hi) {
+        if (!p.mask) {
+          // causal drafts: this row sees keys below min(hi, prefix + t + 1)
+          const int lim = min(hi, prefix + t + 1) - k0;
 #pragma unroll
-        for (int cc = 0; cc < C::KEYS; ++cc) {
-          const int key = k0 + cc;
-          bool vis = key < hi;
-          if (vis && key >= prefix) {
-            const int u = key - prefix;
-            if (p.mask) {
-              const long long bit = (long long)moff + (long long)t * L + u;
-              vis = t < L && ((__ldg(p.mask + (bit >> 3)) >> (bit & 7)) & 1);
-            } else {
-              vis = u <= t;
+          for (int cc = 0; cc < C::KEYS; ++cc) s[cc] = cc < lim ? s[cc] : -INFINITY;
+        } else {
+          // per 32-key group: visibility bits (prefix 1, drafts from the
+          // row's mask bits, nothing at or past hi), then one select per key
+#pragma unroll
+          for (int q = 0; q < C::KEYS / 32; ++q) {
+            const int g0 = k0 + 32 * q;
+            uint32_t vis = 0;
+            if (g0 < hi) {
+              const int below_prefix = min(max(prefix - g0, 0), 32);
+              vis = below_prefix == 32 ? 0xffffffffu : ((1u << below_prefix) - 1u);
+              if (below_prefix < 32 && t < L) {
+                // draft columns u = g0 + i - prefix for i >= below_prefix
+                const int u0 = g0 + below_prefix - prefix;
+                const long long bit0 = (long long)moff + (long long)t * L + u0;
+                const int nbits = min(32 - below_prefix, L - u0);
+                if (nbits > 0) {
+                  uint64_t w = 0;
+                  const int nbytes = (int)((((bit0 & 7) + nbits) + 7) >> 3);
+                  for (int k = 0; k < nbytes; ++k)
+                    w |= (uint64_t)__ldg(p.mask + (bit0 >> 3) + k) << (8 * k);
+                  w >>= (bit0 & 7);
+                  const uint32_t dbits =
+                      (uint32_t)(w & (nbits >= 32 ? 0xffffffffull : ((1ull << nbits) - 1ull)));
+                  vis |= dbits << below_prefix;
+                }
+              }
+              const int in_range = min(hi - g0, 32);
+              if (in_range < 32) vis &= (1u << in_range) - 1u;
             }
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              s[32 * q + i] = ((vis >> i) & 1u) ? s[32 * q + i] : -INFINITY;
           }
-          if (!vis) s[cc] = -INFINITY;
         }
       }
       float mx = -INFINITY;

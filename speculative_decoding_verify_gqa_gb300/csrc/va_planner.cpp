@@ -123,7 +123,14 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   const bool tc_ok = head_dim == 128 && page_size % 16 == 0 && 128 % G == 0;
   int kernel = o.kernel;
   if (kernel == VA_KERNEL_TC_128 && !tc_ok) return VA_ERR_UNSUPPORTED;
-  if (kernel == VA_KERNEL_AUTO) kernel = max_rows <= 64 ? kKernelMma64 : kKernelMma128;
+  if (kernel == VA_KERNEL_AUTO) {
+    // Measured on GB300: the tcgen05 variant wins once row blocks are full
+    // (prefill-like, >= 128 rows per KV head) on bf16 caches; the warp-level
+    // variant keeps verify-sized blocks (its 64-row form fits two CTAs per SM)
+    // and fp8 caches (exact bf16 widening, no f16 range limit on Q).
+    if (tc_ok && kv_dtype == VA_DTYPE_BF16 && max_rows >= 128) kernel = kKernelTc128;
+    else kernel = max_rows <= 64 ? kKernelMma64 : kKernelMma128;
+  }
   const int BM = kernel_rows(kernel);
   const int TK = kTileKeys;
 
@@ -153,7 +160,10 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   // a few candidate wave counts the chunk size is derived from the total key
   // count, the list is packed onto the CTA slots longest-first, and the
   // candidate with the smallest estimated finish time wins.
-  const int64_t slots = (int64_t)num_sms * kernel_ctas_per_sm(kernel);
+  // the tensor-core variant fits two CTAs per SM with bf16 caches, one with fp8
+  const int64_t slots =
+      (int64_t)num_sms * (kernel == kKernelTc128 ? (kv_dtype == VA_DTYPE_BF16 ? 2 : 1)
+                                                : kernel_ctas_per_sm(kernel));
   const int es = kv_dtype == VA_DTYPE_FP8_E4M3 ? 1 : 2;
   const int64_t key_bytes = 2LL * head_dim * es;
   const int64_t fixed_bytes = 48 * 1024;

@@ -153,8 +153,12 @@ def test_plans_of_the_named_workloads(va, name):
                                     kv_dtype=wl.kv_dtype, num_sms=152)
     _check_cover(va, t, plan)
     hd = plan.header()
-    # kernel variant follows the rows per KV head (G * L)
-    assert hd["kernel"] == (1 if (wl.group * wl.qo_lens).max() <= 64 else 2)
+    # kernel variant follows the rows per KV head (G * L) and the cache dtype
+    rows = int((wl.group * wl.qo_lens).max())
+    if rows >= 128 and wl.kv_dtype == synthetic.BF16 and wl.d == 128 and 128 % wl.group == 0:
+        assert hd["kernel"] == 3
+    else:
+        assert hd["kernel"] == (1 if rows <= 64 else 2)
 
 
 def test_plan_items_sorted_longest_first(va):
