@@ -113,7 +113,12 @@ typedef struct {
     int min_chunk;       /* smallest kv chunk (keys) a split may hold; 0 = default */
     int target_ctas;     /* CTAs the plan aims to fill; 0 = derived from the SM count */
     int kernel;          /* force a kernel variant (VA_KERNEL_*); 0 = automatic */
-    int reserved[4];     /* must be zero */
+    int cluster;         /* 0 or -1 = off (the default: measured slower on GB300), 2..16 =
+                            largest cluster size: with the warp-level variant, when every
+                            (request, KV head, row block) has the same kv range, its splits
+                            run as one thread-block cluster and merge through distributed
+                            shared memory (no merge kernel, no partials in the workspace) */
+    int reserved[3];     /* must be zero */
 } va_plan_options_t;
 
 #define VA_KERNEL_AUTO 0

@@ -60,7 +60,7 @@ class VerifyAttnError(RuntimeError):
 class PlanOptions(ctypes.Structure):
     _fields_ = [("max_splits", ctypes.c_int), ("min_chunk", ctypes.c_int),
                 ("target_ctas", ctypes.c_int), ("kernel", ctypes.c_int),
-                ("reserved", ctypes.c_int * 4)]
+                ("cluster", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 def lib():
@@ -154,10 +154,11 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0):
+def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0, cluster=0):
     o = PlanOptions()
     o.max_splits, o.min_chunk, o.target_ctas, o.kernel = (int(max_splits), int(min_chunk),
                                                           int(target_ctas), int(kernel))
+    o.cluster = int(cluster)
     return o
 
 
@@ -184,7 +185,8 @@ class Plan:
         return dict(group=int(ints[10]), kernel=int(ints[11]), block_rows=int(ints[12]),
                     tile_keys=int(ints[13]), n_items=int(ints[14]), n_merge=int(ints[15]),
                     n_units=int(ints[16]), num_sms=int(ints[17]), total_qo=int(i64[0]),
-                    part_rows=int(i64[1]), chunk=int(i64[2]))
+                    part_rows=int(i64[1]), chunk=int(i64[2]),
+                    cluster=int(np.frombuffer(h[152:160].tobytes(), dtype=np.int64)[0]))
 
     def launches(self) -> int:
         n = ctypes.c_int(0)

@@ -113,6 +113,7 @@ PartialParams make_partial(const void* q, const void* k_cache, const void* v_cac
   p.scale_nat = sm_scale * k_scale;
   p.scale_log2 = sm_scale * k_scale * 1.4426950408889634f;
   p.v_scale = v_scale;
+  p.cluster = hd->kernel == kKernelTc128 ? 0 : (int)hd->cluster;
   return p;
 }
 

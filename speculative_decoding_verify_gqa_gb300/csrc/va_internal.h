@@ -58,7 +58,8 @@ struct PlanHeader {
   int64_t total_qo, part_rows, chunk;
   uint64_t off_status, off_items, off_merge, off_part_lse, off_part_out, ws_bytes;
   uint64_t plan_bytes;
-  uint64_t reserved[4];
+  int64_t cluster;  // > 1: splits of a unit form a thread-block cluster of this size
+  uint64_t reserved[3];
 };
 static_assert(sizeof(PlanHeader) == 184, "PlanHeader layout (read by the Python binding)");
 

@@ -30,6 +30,8 @@ struct PartialParams {
   float scale_log2;           // sm_scale * k_scale * log2(e)
   float scale_nat;            // sm_scale * k_scale
   float v_scale;
+  int cluster;                // > 1: the splits of a unit are the CTAs of one thread-block
+                              // cluster (rank = split index) and merge through shared memory
 };
 
 struct MergeParams {
@@ -60,17 +62,38 @@ struct AppendParams {
 // before the previous kernel in the stream finishes (programmatic dependent
 // launch); such kernels call grid_dependency_wait() before touching memory.
 inline cudaError_t launch_kernel(const void* func, dim3 grid, dim3 block, size_t smem,
-                                 cudaStream_t stream, void** args, bool pdl) {
+                                 cudaStream_t stream, void** args, bool pdl, int cluster = 1) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {  // grid.x is a multiple of the cluster size (the planner makes it so)
+    if (cluster > 8) {
+      cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = n;
+  if (cluster > 1) {  // refuse a cluster shape the GPU cannot co-schedule
+    int fit = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&fit, func, &cfg);
+    if (e != cudaSuccess) return e;
+    if (fit < 1) return cudaErrorLaunchOutOfResources;
+  }
   return cudaLaunchKernelExC(&cfg, func, args);
 }
 

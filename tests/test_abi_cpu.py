@@ -77,13 +77,20 @@ def _check_cover(va, t, plan):
     assert hd["n_items"] == len(items) and hd["n_merge"] == len(merges)
     BM = hd["block_rows"]
     G = t["G"]
+    cl = hd["cluster"]
     units = {}
-    for it in items:
+    for i, it in enumerate(items):
         b, h, row0, nrows, lo, hi, part_row, _ = (int(x) for x in it)
         assert 0 <= b < len(t["L"]) and 0 <= h < t["h_kv"]
         assert 0 < nrows <= BM and row0 % BM == 0
-        assert lo % 64 == 0 and lo < hi
+        assert lo % (16 if cl else 64) == 0 and lo < hi
+        if cl:   # a cluster's CTAs are contiguous, rank = split index
+            first = items[i - i % cl]
+            assert (first[0], first[1], first[2]) == (b, h, row0) and part_row == -1
+            assert lo == (i % cl) * hd["chunk"]
         units.setdefault((b, h, row0, nrows), []).append((lo, hi, part_row))
+    if cl:
+        assert 2 <= cl <= 16 and len(items) % cl == 0 and hd["n_merge"] == 0
     for b in range(len(t["L"])):
         R = G * int(t["L"][b])
         for h in range(t["h_kv"]):
@@ -107,8 +114,8 @@ def _check_cover(va, t, plan):
             assert lo == pos
             pos = hi
         assert pos == kv_end
-        if len(chunks) == 1:
-            assert chunks[0][2] == -1 and (b, h, row0, nrows) not in merge_by_unit
+        if len(chunks) == 1 or cl:
+            assert all(c[2] == -1 for c in chunks) and (b, h, row0, nrows) not in merge_by_unit
         else:
             m = merge_by_unit[(b, h, row0, nrows)]
             assert int(m[5]) == len(chunks)

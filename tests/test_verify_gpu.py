@@ -197,10 +197,59 @@ def test_split_and_unsplit_agree(va):
     o1, l1, p1 = dw.run(max_splits=1)
     o2, l2, p2 = dw.run()
     torch.cuda.synchronize()
-    assert p1.header()["n_merge"] == 0 and p2.header()["n_merge"] > 0
+    assert p1.header()["n_merge"] == 0 and p1.header()["cluster"] == 0
+    assert p2.header()["n_merge"] > 0 or p2.header()["cluster"] > 1
     assert float((o1.float() - o2.float()).abs().max()) <= 1e-2
     assert float((l1 - l2).abs().max()) <= 1e-3
     compare(wl, o1, l1)
+
+
+@pytest.mark.parametrize("case", [
+    dict(name="llama3_8b_tree_verify"),
+    dict(batch=2, h_q=16, h_kv=2, d=128, prefix=("fixed", [900, 900]), qo=("fixed", [6, 6]),
+         mask="random"),
+    dict(batch=1, h_q=8, h_kv=8, d=64, prefix=("fixed", [1000]), qo=("fixed", [3]),
+         mask="causal", kv_dtype=synthetic.FP8),
+], ids=["llama3", "random_mask_g8", "fp8_d64_mha"])
+@pytest.mark.parametrize("cap", [16, 4])
+def test_cluster_merge_matches_workspace_merge(va, case, cap):
+    """Splits merged inside a thread-block cluster (distributed shared memory)
+    equal the oracle and the two-kernel merge through the workspace."""
+    if "name" in case:
+        wl = synthetic.make_workload(case["name"])
+    else:
+        wl = synthetic.make_custom(seed=33, **case)
+    dw = DeviceWorkload(wl)
+    oc, lc, pc = dw.run(cluster=cap)
+    ow, lw, pw = dw.run(cluster=-1)
+    torch.cuda.synchronize()
+    assert pc.header()["cluster"] > 1 and pc.launches() == 1
+    assert pw.header()["cluster"] == 0
+    assert va.verify_attn_device_status(pc) == 0
+    compare(wl, oc, lc, rows=synthetic.sample_rows(wl, 300))
+    assert float((oc.float() - ow.float()).abs().max()) <= 1e-2
+    assert float((lc - lw).abs().max()) <= 1e-3
+
+
+def test_cluster_with_a_stale_plan_flags_and_finishes(va):
+    """A CTA whose tables disagree with the plan still joins its cluster's
+    barriers (no hang), writes nothing, and raises VA_DEV_BAD_TABLE."""
+    wl = synthetic.make_workload("llama3_8b_tree_verify")
+    dw = DeviceWorkload(wl)
+    plan = dw.plan(cluster=16)
+    assert plan.header()["cluster"] > 1
+    # one page fewer (kv_len 4112 instead of 4113): only the last split of each
+    # cluster, which ends at 4113, finds its range past the tables
+    kvp = wl.kv_indptr.copy()
+    kvp[1] -= 1
+    lpl = wl.last_page_len.copy()
+    lpl[0] = 16
+    dw.kv_indptr = torch.from_numpy(kvp).cuda()
+    dw.last_page_len = torch.from_numpy(lpl).cuda()
+    out, lse, _ = dw.run(plan=plan)
+    torch.cuda.synchronize()
+    assert va.verify_attn_device_status(plan) & 2
+    assert torch.isfinite(lse).all()
 
 
 def test_page_placement_does_not_change_bits(va):

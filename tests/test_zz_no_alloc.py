@@ -34,9 +34,11 @@ def test_static_scratch_matches_run_twice_in_a_row(va, name):
     ref_out, ref_lse, plan = dw.run()            # the existing entry point, caller workspace
     torch.cuda.synchronize()
     # a host-only plan: this caller never allocates a device workspace
+    # (workspace merge rather than the in-cluster merge, so that the split
+    # partials really live in the static array)
     hplan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
                                      wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
-                                     kv_dtype=wl.kv_dtype)
+                                     kv_dtype=wl.kv_dtype, cluster=-1)
     if name == "llama3_8b_tree_verify":
         assert hplan.header()["n_merge"] > 0     # the split partials live in the static array
     assert hplan.workspace_bytes <= va.STATIC_SCRATCH_BYTES
