@@ -125,7 +125,10 @@ typedef struct {
 #define VA_KERNEL_MMA_64 1      /* warp-level tensor cores, 64-row blocks, 4 warps */
 #define VA_KERNEL_MMA_128 2     /* warp-level tensor cores, 128-row blocks, 8 warps */
 #define VA_KERNEL_TC_128 3      /* tcgen05 tensor cores + TMA, 128-row blocks; needs head_dim
-                                   128, bf16 KV, page_size a multiple of 16, 128 % G == 0 */
+                                   128, page_size a multiple of 16, 128 % G == 0; with fp8 KV
+                                   the MMAs run on f16, so |q| must stay below 65504 */
+#define VA_KERNEL_TC_256 4      /* as VA_KERNEL_TC_128 with two 128-row Q tiles per CTA sharing
+                                   every K/V tile (256-row blocks, one CTA per SM) */
 
 /* Name of a status code (static string). */
 const char* verify_attn_status_string(int status);

@@ -40,37 +40,48 @@
 namespace va {
 namespace {
 
-template <bool FP8>
+// NQ = 1: one 128-row Q tile per CTA.  NQ = 2: two Q tiles (256 rows) share
+// every K/V tile, each with its own softmax warpgroup, TMEM S buffers and O
+// accumulator, so K/V bytes, TMA traffic and fp8 widening per row halve and
+// one warpgroup's softmax overlaps the other's MMAs.
+template <bool FP8, int NQ>
 struct TcCfg {
-  static constexpr int ROWS = 128, D = 128, THREADS = 256;
+  static constexpr int ROWS = 128, D = 128;              // rows per Q tile = TMEM lanes
+  static constexpr int BLOCK_ROWS = NQ * ROWS;
+  static constexpr int THREADS = 128 + 128 * NQ;         // 4 role warps + 4 softmax warps per Q tile
   static constexpr int KEYS = 64;                        // keys per tile
-  static constexpr int STAGES = FP8 ? 3 : 2;             // TMA stages (raw fp8, or bf16 operands)
-  static constexpr int CTAS_PER_SM = FP8 ? 1 : 2;        // bf16: two CTAs hide each other's waits
-  static constexpr int Q_BYTES = ROWS * D * 2;           // [2 halves][128 rows][128 B]
+  static constexpr int STAGES = NQ == 2 ? 4 : (FP8 ? 3 : 2);  // TMA stages (raw fp8, or bf16 operands)
+  static constexpr int CTAS_PER_SM = (NQ == 1 && !FP8) ? 2 : 1;  // two small CTAs hide each other's waits
+  static constexpr int QT_BYTES = ROWS * D * 2;          // one Q tile: [2 halves][128 rows][128 B]
+  static constexpr int Q_BYTES = NQ * QT_BYTES;
   static constexpr int OP_BYTES = KEYS * D * 2;          // 16-bit K (or V) operand tile
   static constexpr int RAW_BYTES = KEYS * D;             // fp8 K (or V) tile [keys][128 B]
   static constexpr int STAGE_BYTES = FP8 ? 2 * RAW_BYTES : 2 * OP_BYTES;
   static constexpr int CONV_BUFS = FP8 ? 2 : 0;          // widened K+V operand buffers
-  static constexpr int P_BYTES = ROWS * KEYS * 2;        // [key blocks][128 rows][128 B]
+  static constexpr int PT_BYTES = ROWS * KEYS * 2;       // one P tile: [key blocks][128 rows][128 B]
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + Q_BYTES;
   static constexpr int OFF_CONV = OFF_KV + STAGES * STAGE_BYTES;
   static constexpr int OFF_P = OFF_CONV + CONV_BUFS * 2 * OP_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_BAR = OFF_P + NQ * PT_BYTES;
   static constexpr int SMEM = OFF_BAR + 256;              // + barriers, TMEM address, abort flag
-  static constexpr uint32_t TMEM_COLS = 256;              // S0 | S1 | O (64 + 64 + 128 columns)
+  static constexpr uint32_t QT_COLS = 256;               // per Q tile: S0 | S1 | O (64 + 64 + 128)
+  static constexpr uint32_t TMEM_COLS = NQ * QT_COLS;
   static constexpr uint32_t COL_O = 2 * KEYS;
   static constexpr int CONV_WARPS = 2;                    // warps 2-3 (fp8 only)
-  // 228 KB per SM, 1 KB reserved per CTA
+  // 228 KB per SM, 1 KB reserved per CTA; at most 227 KB for one CTA
   static_assert(CTAS_PER_SM * (SMEM + 1024) <= 228 * 1024, "shared memory budget");
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
   static_assert(CTAS_PER_SM * TMEM_COLS <= 512, "tensor memory budget");
+  static_assert(STAGES <= 4, "barrier slots");
 };
 
 constexpr float kLn2 = 0.6931471805599453f;
 
-// barrier slots
-enum { B_Q = 0, B_Q_READY = 1, B_KV_FULL = 2, B_KV_EMPTY = 5, B_CONV_FULL = 8, B_CONV_FREE = 10,
-       B_S_FULL = 12, B_S_FREE = 14, B_P_FULL = 16, B_O_DONE = 17, B_COUNT = 18 };
+// barrier slots (per-Q-tile barriers at base + qt, or base + 2 qt + buffer)
+enum { B_Q = 0, B_Q_READY = 1, B_KV_FULL = 2, B_KV_EMPTY = 6, B_CONV_FULL = 10, B_CONV_FREE = 12,
+       B_S_FULL = 14, B_S_FREE = 18, B_P_FULL = 22, B_O_DONE = 24, B_COUNT = 26 };
+static_assert(8 * B_COUNT + 16 <= 256, "barrier area");
 
 // Instruction descriptor, kind::f16 with f16 A and B (fp32 accumulator).
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
@@ -78,10 +89,10 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) 
          ((uint32_t)(M >> 4) << 24);
 }
 
-template <bool FP8>
-__global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
+template <bool FP8, int NQ>
+__global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, TcCfg<FP8, NQ>::CTAS_PER_SM)
     verify_partial_tc_kernel(const PartialParams p, const __grid_constant__ TcMaps maps) {
-  using C = TcCfg<FP8>;
+  using C = TcCfg<FP8, NQ>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the swizzled operand tiles need 1024-byte alignment
@@ -106,7 +117,8 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
   const int kv_len = (int)kv_len_ll;
   const int prefix = kv_len - L;
   const bool ok = L >= 0 && npg >= 0 && lpl >= 1 && lpl <= p.page_size && prefix >= 0 &&
-                  it.row0 >= 0 && it.nrows > 0 && it.nrows <= C::ROWS && it.row0 % C::ROWS == 0 &&
+                  it.row0 >= 0 && it.nrows > 0 && it.nrows <= C::BLOCK_ROWS &&
+                  it.row0 % C::BLOCK_ROWS == 0 &&
                   (long long)it.row0 + it.nrows <= (long long)G * L && it.kv_lo >= 0 &&
                   it.kv_lo % 16 == 0 && it.kv_lo < it.kv_hi && it.kv_hi <= kv_len &&
                   kv_len_ll <= 0x7fffffffLL;
@@ -116,10 +128,11 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
   }
   const int nrows = it.nrows, row0 = it.row0, lo = it.kv_lo, hi = it.kv_hi;
   const int n_tiles = (hi - lo + C::KEYS - 1) / C::KEYS;
+  const int nq = (nrows + C::ROWS - 1) / C::ROWS;  // live Q tiles (1 .. NQ)
 
   if (tid == 0) {
     mbar_init(bar(B_Q), 1);
-    mbar_init(bar(B_Q_READY), 4);
+    mbar_init(bar(B_Q_READY), 4 * nq);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(B_KV_FULL + s), 1);
       mbar_init(bar(B_KV_EMPTY + s), FP8 ? C::CONV_WARPS : 1);
@@ -127,11 +140,15 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_CONV_FULL + s), C::CONV_WARPS);
       mbar_init(bar(B_CONV_FREE + s), 1);
-      mbar_init(bar(B_S_FULL + s), 1);
-      mbar_init(bar(B_S_FREE + s), 4);
     }
-    mbar_init(bar(B_P_FULL), 4);
-    mbar_init(bar(B_O_DONE), 1);
+    for (int qt = 0; qt < NQ; ++qt) {
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(bar(B_S_FULL + 2 * qt + s), 1);
+        mbar_init(bar(B_S_FREE + 2 * qt + s), 4);
+      }
+      mbar_init(bar(B_P_FULL + qt), 4);
+      mbar_init(bar(B_O_DONE + qt), 1);
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -143,11 +160,12 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      mbar_expect_tx(bar(B_Q), C::Q_BYTES);
+      mbar_expect_tx(bar(B_Q), nq * C::QT_BYTES);
       const int tok0 = qo0 + row0 / G;
-      for (int half = 0; half < 2; ++half)
-        tma_load_3d(sbase + C::OFF_Q + half * (C::Q_BYTES / 2), &maps.q, half * 64, h * G, tok0,
-                    bar(B_Q));
+      for (int qt = 0; qt < nq; ++qt)
+        for (int half = 0; half < 2; ++half)
+          tma_load_3d(sbase + C::OFF_Q + qt * C::QT_BYTES + half * (C::QT_BYTES / 2), &maps.q,
+                      half * 64, h * G, tok0 + qt * (C::ROWS / G), bar(B_Q));
       int bad = 0;
       // Page ids of a tile's 16-key boxes (-1 past the chunk), loaded one tile
       // ahead so their latency hides behind the previous tile's wait.
@@ -208,20 +226,32 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
       constexpr uint32_t id_s = FP8 ? idesc_f16(C::ROWS, C::KEYS, false)
                                     : idesc_bf16(C::ROWS, C::KEYS, false);
       constexpr uint32_t id_o = FP8 ? idesc_f16(C::ROWS, C::D, true) : idesc_bf16(C::ROWS, C::D, true);
-      const uint32_t qaddr = sbase + C::OFF_Q, paddr = sbase + C::OFF_P;
       auto kop = [&](int j) {  // K operand of tile j
         return FP8 ? sbase + C::OFF_CONV + (j & 1) * 2 * C::OP_BYTES
                    : sbase + C::OFF_KV + (j % C::STAGES) * C::STAGE_BYTES;
       };
-      auto pv = [&](int j) {  // O (+)= P_j V_j
+      auto free_bar = [&](int j) {  // released once tile j's last MMA is done
+        return FP8 ? bar(B_CONV_FREE + (j & 1)) : bar(B_KV_EMPTY + j % C::STAGES);
+      };
+      auto pv = [&](int qt, int j) {  // O_qt (+)= P_qt V_j
         const uint32_t vaddr = kop(j) + C::OP_BYTES;
+        const uint32_t paddr = sbase + C::OFF_P + qt * C::PT_BYTES;
         for (int kk = 0; kk < C::KEYS / 16; ++kk) {
           const uint64_t a = smem_desc_sw128(paddr + (kk >> 2) * (C::ROWS * 128) + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = smem_desc_sw128(vaddr + kk * 16 * 128, C::KEYS * 128, 1024);
-          umma_bf16(tmem + C::COL_O, a, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16(tmem + qt * C::QT_COLS + C::COL_O, a, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(bar(B_O_DONE));
-        umma_commit(FP8 ? bar(B_CONV_FREE + (j & 1)) : bar(B_KV_EMPTY + j % C::STAGES));
+        umma_commit(bar(B_O_DONE + qt));
+      };
+      // all live Q tiles' P_{j} -> PV, then release tile j's operands
+      auto pv_all = [&](int j) {
+        for (int qt = 0; qt < nq; ++qt) {
+          if (!mbar_wait(bar(B_P_FULL + qt), j & 1, abort_flag)) return false;
+          tc_fence_after();
+          pv(qt, j);
+        }
+        umma_commit(free_bar(j));
+        return true;
       };
       bool live = mbar_wait(bar(FP8 ? B_Q_READY : B_Q), 0, abort_flag);
       int issued_pv = 0;
@@ -232,28 +262,31 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
         } else {
           if (!mbar_wait(bar(B_KV_FULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag)) break;
         }
-        if (j >= 2 && !mbar_wait(bar(B_S_FREE + sb), ((j >> 1) - 1) & 1, abort_flag)) break;
-        tc_fence_after();
         const uint32_t kaddr = kop(j);
-        for (int kk = 0; kk < C::D / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(qaddr + (kk >> 2) * (C::ROWS * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(kaddr + (kk >> 2) * (C::KEYS * 128) + (kk & 3) * 32, 16, 1024);
-          umma_bf16(tmem + sb * C::KEYS, a, bd, id_s, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(bar(B_S_FULL + sb));
-        if (j >= 1) {
-          if (!mbar_wait(bar(B_P_FULL), (j - 1) & 1, abort_flag)) break;
+        for (int qt = 0; qt < nq; ++qt) {
+          if (j >= 2 && !mbar_wait(bar(B_S_FREE + 2 * qt + sb), ((j >> 1) - 1) & 1, abort_flag)) {
+            live = false;
+            break;
+          }
           tc_fence_after();
-          pv(j - 1);
+          const uint32_t qaddr = sbase + C::OFF_Q + qt * C::QT_BYTES;
+          for (int kk = 0; kk < C::D / 16; ++kk) {
+            const uint64_t a = smem_desc_sw128(qaddr + (kk >> 2) * (C::ROWS * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(kaddr + (kk >> 2) * (C::KEYS * 128) + (kk & 3) * 32, 16, 1024);
+            umma_bf16(tmem + qt * C::QT_COLS + sb * C::KEYS, a, bd, id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(B_S_FULL + 2 * qt + sb));
+        }
+        if (!live) break;
+        if (j >= 1) {
+          if (!pv_all(j - 1)) break;
           issued_pv = j;
         }
       }
       if (!*abort_flag && issued_pv == n_tiles - 1) {
-        if (mbar_wait(bar(B_P_FULL), (n_tiles - 1) & 1, abort_flag)) {
-          tc_fence_after();
-          pv(n_tiles - 1);
-          // the last buffer release lands before the CTA's shared memory goes away
-          const int j = n_tiles - 1;
+        const int j = n_tiles - 1;
+        // the last buffer release lands before the CTA's shared memory goes away
+        if (pv_all(j)) {
           if (FP8)
             mbar_wait(bar(B_CONV_FREE + (j & 1)), (j >> 1) & 1, abort_flag);
           else
@@ -273,6 +306,7 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
         const uint8_t* raw = smem + C::OFF_KV + s * C::STAGE_BYTES;
         uint8_t* dst = smem + C::OFF_CONV + cb * 2 * C::OP_BYTES;
         const int k0 = lo + j * C::KEYS;
+#pragma unroll 4
         for (int c = ct; c < 2 * CH; c += 64) {
           const int which = c / CH, cc = c - which * CH;
           const int r = cc >> 3, ch = cc & 7;       // key row, 16-element column group
@@ -302,15 +336,20 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
         }
       }
     }
-  } else {
-    // ---------------- softmax / epilogue: one thread per row (warps 4-7) ----------------
-    const int quad = warp - 4;
-    const int r = quad * 32 + lane;                 // row of the block = TMEM lane
-    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-    const bool row_ok = r < nrows;
-    const int t = (row0 + r) / G;                   // draft token of the row
+  } else if ((warp - 4) / 4 < nq) {
+    // ---------------- softmax / epilogue: one thread per row, 4 warps per Q tile ----------------
+    const int qt = (warp - 4) >> 2;                 // Q tile of this warpgroup
+    const int quad = warp & 3;                      // TMEM lane quarter this warp may access
+    const int r = quad * 32 + lane;                 // row of the Q tile = TMEM lane
+    const int br = qt * C::ROWS + r;                // row of the block
+    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16) + qt * C::QT_COLS;
+    const bool row_ok = br < nrows;
+    const int t = (row0 + br) / G;                  // draft token of the row
     const int moff = p.mask ? p.mask_indptr[b] : 0;
     const float c = p.scale_log2;
+    const uint32_t b_s_full = bar(B_S_FULL + 2 * qt), b_s_free = bar(B_S_FREE + 2 * qt);
+    const uint32_t b_p_full = bar(B_P_FULL + qt), b_o_done = bar(B_O_DONE + qt);
+    uint8_t* const ptile = smem + C::OFF_P + qt * C::PT_BYTES;
     float m_used = -INFINITY;                       // in units of s * c (log2 domain)
     float l = 0.f;
     float s[C::KEYS];
@@ -322,7 +361,8 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
       if (live) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          uint4* q4 = reinterpret_cast<uint4*>(smem + C::OFF_Q + half * (C::Q_BYTES / 2) + r * 128);
+          uint4* q4 = reinterpret_cast<uint4*>(smem + C::OFF_Q + qt * C::QT_BYTES +
+                                               half * (C::QT_BYTES / 2) + r * 128);
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             uint4 v = q4[ch];
@@ -340,7 +380,7 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
     }
     for (int j = 0; live && j < n_tiles; ++j) {
       const int sb = j & 1;
-      if (!mbar_wait(bar(B_S_FULL + sb), (j >> 1) & 1, abort_flag)) { live = false; break; }
+      if (!mbar_wait(b_s_full + 8 * sb, (j >> 1) & 1, abort_flag)) { live = false; break; }
       tc_fence_after();
       {
         uint32_t raw[C::KEYS];
@@ -352,7 +392,7 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_S_FREE + sb));
+      if (lane == 0) mbar_arrive(b_s_free + 8 * sb);
 
       const int k0 = lo + j * C::KEYS;
       if (k0 + C::KEYS > prefix || k0 + C::KEYS > hi) {
@@ -415,7 +455,7 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
       l = l * alpha + sum;
       // P buffer and O are free once the previous PV has completed.
       if (j >= 1) {
-        if (!mbar_wait(bar(B_O_DONE), (j - 1) & 1, abort_flag)) { live = false; break; }
+        if (!mbar_wait(b_o_done, (j - 1) & 1, abort_flag)) { live = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           for (int q = 0; q < C::D / 32; ++q) {
@@ -432,8 +472,9 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
       if constexpr (!FP8) {
         // Rows of V past the chunk end inside the last 16-key box may hold
         // stale (even NaN) slots: zero them, since 0 * NaN would poison O.
+        // Q tile 0's warps do it; the MMAs of every Q tile's PV wait for them.
         const int tail = hi - k0;
-        if (tail < C::KEYS && (tail & 15)) {
+        if (qt == 0 && tail < C::KEYS && (tail & 15)) {
           const int zlo = tail, zhi = (tail + 15) & ~15;
           uint8_t* vt = smem + C::OFF_KV + (j % C::STAGES) * C::STAGE_BYTES + C::OP_BYTES;
           for (int z = r; z < (zhi - zlo) * 16; z += C::ROWS) {
@@ -444,27 +485,26 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
         }
       }
       // P row -> shared memory, K-major 128-byte-swizzled [key block][row][128 B]
-      uint8_t* prow = smem + C::OFF_P;
 #pragma unroll
       for (int ch = 0; ch < C::KEYS / 8; ++ch) {
         const int kb = ch >> 3, c8 = ch & 7;
-        *reinterpret_cast<uint4*>(prow + kb * (C::ROWS * 128) + r * 128 + ((c8 ^ (r & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(ptile + kb * (C::ROWS * 128) + r * 128 + ((c8 ^ (r & 7)) << 4)) =
             make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
       }
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P_FULL));
+      if (lane == 0) mbar_arrive(b_p_full);
       m_used = m_new;
     }
     // epilogue
-    if (live && mbar_wait(bar(B_O_DONE), (n_tiles - 1) & 1, abort_flag)) {
+    if (live && mbar_wait(b_o_done, (n_tiles - 1) & 1, abort_flag)) {
       tc_fence_after();
       const float lse = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
       const float inv = l > 0.f ? p.v_scale / l : 0.f;
       size_t orow = 0;
       if (row_ok) {
-        const int g = (row0 + r) - t * G;
+        const int g = (row0 + br) - t * G;
         orow = (size_t)(qo0 + t) * p.h_q + (size_t)h * G + g;
       }
       for (int q = 0; q < C::D / 32; ++q) {
@@ -484,7 +524,7 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
             dst[e] = w;
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(p.part_out + ((size_t)it.part_row + r) * C::D + q * 32);
+          float4* dst = reinterpret_cast<float4*>(p.part_out + ((size_t)it.part_row + br) * C::D + q * 32);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
@@ -495,7 +535,7 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
         if (it.part_row < 0) {
           if (p.lse) p.lse[orow] = lse;
         } else {
-          p.part_lse[(size_t)it.part_row + r] = lse;
+          p.part_lse[(size_t)it.part_row + br] = lse;
         }
       }
     }
@@ -511,25 +551,28 @@ __global__ void __launch_bounds__(256, TcCfg<FP8>::CTAS_PER_SM)
   if (tid == 0 && *abort_flag) atomicOr(p.status, VA_DEV_TIMEOUT);
 }
 
-template <bool FP8>
+template <bool FP8, int NQ>
 cudaError_t launch_tc(const PartialParams& p, const TcMaps& maps, int n_items,
                       cudaStream_t stream) {
-  auto kern = verify_partial_tc_kernel<FP8>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       TcCfg<FP8>::SMEM);
+  using C = TcCfg<FP8, NQ>;
+  auto kern = verify_partial_tc_kernel<FP8, NQ>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PartialParams*>(&p), const_cast<TcMaps*>(&maps)};
-  return launch_kernel(reinterpret_cast<const void*>(kern), dim3(n_items),
-                       dim3(TcCfg<FP8>::THREADS), TcCfg<FP8>::SMEM, stream, args, /*pdl=*/true);
+  return launch_kernel(reinterpret_cast<const void*>(kern), dim3(n_items), dim3(C::THREADS),
+                       C::SMEM, stream, args, /*pdl=*/true);
 }
 
 }  // namespace
 
 cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, bool kv_fp8,
-                              int n_items, cudaStream_t stream) {
+                              int block_rows, int n_items, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
-  return kv_fp8 ? launch_tc<true>(p, maps, n_items, stream)
-                : launch_tc<false>(p, maps, n_items, stream);
+  if (block_rows == 256)
+    return kv_fp8 ? launch_tc<true, 2>(p, maps, n_items, stream)
+                  : launch_tc<false, 2>(p, maps, n_items, stream);
+  return kv_fp8 ? launch_tc<true, 1>(p, maps, n_items, stream)
+                : launch_tc<false, 1>(p, maps, n_items, stream);
 }
 
 }  // namespace va

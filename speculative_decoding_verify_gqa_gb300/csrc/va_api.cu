@@ -48,6 +48,9 @@ const PlanHeader* plan_header(const void* plan_h) {
   if (!plan_h) return nullptr;
   const PlanHeader* hd = static_cast<const PlanHeader*>(plan_h);
   if (hd->magic != kPlanMagic || hd->version != kPlanVersion) return nullptr;
+  if (hd->kernel < kKernelMma64 || hd->kernel > kKernelTc256 ||
+      hd->block_rows != kernel_rows(hd->kernel))
+    return nullptr;
   return hd;
 }
 
@@ -113,7 +116,7 @@ PartialParams make_partial(const void* q, const void* k_cache, const void* v_cac
   p.scale_nat = sm_scale * k_scale;
   p.scale_log2 = sm_scale * k_scale * 1.4426950408889634f;
   p.v_scale = v_scale;
-  p.cluster = hd->kernel == kKernelTc128 ? 0 : (int)hd->cluster;
+  p.cluster = kernel_is_tc(hd->kernel) ? 0 : (int)hd->cluster;
   return p;
 }
 
@@ -267,11 +270,11 @@ int verify_attn_partial(const void* q, const void* k_cache, const void* v_cache,
                                  qo_indptr, mask, mask_indptr, sm_scale, k_scale, v_scale, out,
                                  lse, num_pages, hd, workspace_d);
   cudaError_t e;
-  if (hd->kernel == kKernelTc128) {
+  if (kernel_is_tc(hd->kernel)) {
     TcMaps maps;
     rc = make_tc_maps(q, hd->total_qo, k_cache, v_cache, num_pages, hd, &maps);
     if (rc) return rc;
-    e = launch_partial_tc(p, maps, hd->kv_dtype == VA_DTYPE_FP8_E4M3, hd->n_items,
+    e = launch_partial_tc(p, maps, hd->kv_dtype == VA_DTYPE_FP8_E4M3, hd->block_rows, hd->n_items,
                           static_cast<cudaStream_t>(stream));
   } else {
     e = launch_partial_mma(p, hd->kernel, hd->head_dim, hd->kv_dtype == VA_DTYPE_FP8_E4M3,

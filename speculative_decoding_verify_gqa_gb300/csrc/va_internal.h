@@ -21,9 +21,11 @@ enum Kernel : int32_t {
   kKernelMma64 = 1,   // warp-level mma.sync, 4 warps x 16 rows
   kKernelMma128 = 2,  // warp-level mma.sync, 8 warps x 16 rows
   kKernelTc128 = 3,   // tcgen05 + TMA, 128 rows per CTA
+  kKernelTc256 = 4,   // tcgen05 + TMA, two 128-row Q tiles per CTA
 };
 
-inline int kernel_rows(int k) { return k == kKernelMma64 ? 64 : 128; }
+inline int kernel_rows(int k) { return k == kKernelMma64 ? 64 : k == kKernelTc256 ? 256 : 128; }
+inline bool kernel_is_tc(int k) { return k == kKernelTc128 || k == kKernelTc256; }
 inline int kernel_threads(int k) { return k == kKernelMma64 ? 128 : 256; }
 inline int kernel_ctas_per_sm(int k) { return k == kKernelMma64 ? 2 : 1; }
 

@@ -110,7 +110,7 @@ struct TcMaps {
   CUtensorMap q, k, v;
 };
 cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, bool kv_fp8,
-                              int n_items, cudaStream_t stream);
+                              int block_rows, int n_items, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int head_dim, int n_merge, int block_rows,
                          cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);

@@ -92,7 +92,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
       o.cluster == 1 || o.cluster > 16)
     return VA_ERR_INVALID_ARGUMENT;
   if (o.kernel != VA_KERNEL_AUTO && o.kernel != VA_KERNEL_MMA_64 && o.kernel != VA_KERNEL_MMA_128 &&
-      o.kernel != VA_KERNEL_TC_128)
+      o.kernel != VA_KERNEL_TC_128 && o.kernel != VA_KERNEL_TC_256)
     return VA_ERR_INVALID_ARGUMENT;
 
   const int G = num_qo_heads / num_kv_heads;
@@ -124,7 +124,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   // of its 16-row TMA boxes, and groups that tile its 128 rows.
   const bool tc_ok = head_dim == 128 && page_size % 16 == 0 && 128 % G == 0;
   int kernel = o.kernel;
-  if (kernel == VA_KERNEL_TC_128 && !tc_ok) return VA_ERR_UNSUPPORTED;
+  if ((kernel == VA_KERNEL_TC_128 || kernel == VA_KERNEL_TC_256) && !tc_ok) return VA_ERR_UNSUPPORTED;
   if (kernel == VA_KERNEL_AUTO) {
     // Measured on GB300: the tcgen05 variant wins once row blocks are full
     // (prefill-like, >= 128 rows per KV head) on bf16 caches; the warp-level
@@ -162,7 +162,8 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   // a few candidate wave counts the chunk size is derived from the total key
   // count, the list is packed onto the CTA slots longest-first, and the
   // candidate with the smallest estimated finish time wins.
-  // the tensor-core variant fits two CTAs per SM with bf16 caches, one with fp8
+  // the 128-row tensor-core variant fits two CTAs per SM with bf16 caches, one
+  // with fp8; the 256-row one fills an SM's tensor memory alone
   const int64_t slots =
       (int64_t)num_sms * (kernel == kKernelTc128 ? (kv_dtype == VA_DTYPE_BF16 ? 2 : 1)
                                                 : kernel_ctas_per_sm(kernel));

@@ -168,6 +168,22 @@ def test_plans_of_the_named_workloads(va, name):
         assert hd["kernel"] == (1 if rows <= 64 else 2)
 
 
+@pytest.mark.parametrize("name", ["gqa_varlen_prefill", "wide_tree_fp8_verify",
+                                  "llama3_8b_tree_verify"])
+@pytest.mark.parametrize("kernel", [3, 4])
+def test_tcgen05_plans_cover_every_row_once(va, name, kernel):
+    """The tcgen05 variants' plans (128- and 256-row blocks) cover each
+    (request, KV head, row) with chunks that tile its kv range."""
+    wl = synthetic.make_workload(name, with_values=False)
+    t = dict(masked=wl.mask is not None, prefix=wl.prefix_lens, L=wl.qo_lens, G=wl.group, h_kv=wl.h_kv)
+    plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
+                                    wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                    kv_dtype=wl.kv_dtype, num_sms=152, kernel=kernel)
+    hd = plan.header()
+    assert hd["kernel"] == kernel and hd["block_rows"] == (128 if kernel == 3 else 256)
+    _check_cover(va, t, plan)
+
+
 def test_plan_items_sorted_longest_first(va):
     wl = synthetic.make_workload("codellama34b_chain_verify", with_values=False)
     plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, None,
@@ -212,6 +228,9 @@ def test_plan_validation_codes(va):
     assert _plan_rc(va, [0, 2, 1], [0, 3, 3], [5, 1], None) == -1  # decreasing indptr
     assert _plan_rc(va, *ok, max_splits=-1) == -1
     assert _plan_rc(va, *ok, kernel=9) == -1
+    assert _plan_rc(va, *ok, kernel=4) == 0
+    assert _plan_rc(va, *ok, kernel=4, d=64) == -2         # tcgen05 variants: head_dim 128 only
+    assert _plan_rc(va, *ok, kernel=3, P=8) == -2          # page boxes of 16 rows
 
 
 def test_empty_batches_plan_to_nothing(va):

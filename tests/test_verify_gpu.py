@@ -139,7 +139,7 @@ def test_custom_mask_may_open_later_drafts(va):
                                qo=("fixed", [40, 33]), mask="random", seed=27)
     assert int((wl.group * wl.qo_lens).max()) > 256
     dw = DeviceWorkload(wl)
-    for opts in (dict(), dict(kernel=1), dict(kernel=3)):
+    for opts in (dict(), dict(kernel=1), dict(kernel=3), dict(kernel=4)):
         out, lse, plan = dw.run(**opts)
         torch.cuda.synchronize()
         compare(wl, out, lse)
@@ -170,15 +170,16 @@ TC_CASES = [
 
 @pytest.mark.parametrize("name,case", TC_CASES, ids=[c[0] for c in TC_CASES])
 @pytest.mark.parametrize("splits", [1, 0])
-def test_tcgen05_kernel_matches_oracle(va, name, case, splits):
+@pytest.mark.parametrize("kernel", [3, 4], ids=["tc128", "tc256"])
+def test_tcgen05_kernel_matches_oracle(va, name, case, splits, kernel):
     wl = synthetic.make_custom(seed=29, **case)
     dw = DeviceWorkload(wl)
-    opts = dict(kernel=3, max_splits=splits)
+    opts = dict(kernel=kernel, max_splits=splits)
     if splits == 0:
         opts["target_ctas"] = 600
     out, lse, plan = dw.run(**opts)
     torch.cuda.synchronize()
-    assert plan.header()["kernel"] == 3
+    assert plan.header()["kernel"] == kernel
     assert va.verify_attn_device_status(plan) == 0
     compare(wl, out, lse)
 
@@ -186,9 +187,10 @@ def test_tcgen05_kernel_matches_oracle(va, name, case, splits):
 def test_tcgen05_kernel_rejects_what_it_cannot_serve(va):
     wl = synthetic.make_custom(batch=1, h_q=6, h_kv=2, d=128, prefix=("fixed", [10]),
                                qo=("fixed", [3]), seed=31)
-    with pytest.raises(va.VerifyAttnError):
-        va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, None, 6, 2, 128,
-                                 16, kernel=3, num_sms=152)   # 128 % G != 0
+    for kernel in (3, 4):
+        with pytest.raises(va.VerifyAttnError):
+            va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, None, 6, 2,
+                                     128, 16, kernel=kernel, num_sms=152)   # 128 % G != 0
 
 
 def test_split_and_unsplit_agree(va):
