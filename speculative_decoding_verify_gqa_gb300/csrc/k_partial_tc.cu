@@ -1,31 +1,37 @@
 // Split-KV verify attention on the 5th-generation tensor cores (tcgen05, TMEM
-// accumulators, TMA page gather) for blocks of 128 query rows.
+// accumulators, TMA page gather) for blocks of one or two 128-row Q tiles.
 //
 // Same algorithm as the warp-level variant ("flashmap 0.1.0 --
 // flashmap/sglang/verify_attention.py", partial kernel: one CTA per request,
 // KV head, row block and kv chunk; online softmax; normalised output or fp32
 // partial + LSE), laid out for sm_103a:
 //  * warp 0, one thread: TMA producer.  Q arrives as one 3-D box per 64-column
-//    half (G heads x 128/G tokens: the block's token-major rows); each key tile
-//    arrives as 16-row page boxes of the 4-D cache [page, head, slot, dim]
-//    (page ids read from the page table; boxes past the chunk point outside
-//    the pool, so TMA zero-fills them) into a ring of mbarrier-tracked stages.
-//  * warp 1, one thread: tcgen05.mma issuer.  S_j = Q K_j^T (M 128, N = tile
-//    keys, K 128) into one of two TMEM S buffers while the softmax works on the
-//    other; O += P_{j-1} V_{j-1} (V read MN-major) into a TMEM O accumulator.
-//    tcgen05.commit signals S-ready, O-ready and buffer-free mbarriers.
-//  * warps 4-7: one thread per query row (= TMEM lane).  Loads its S row,
-//    masks it, keeps a running max m and sum l in fp32, writes P = 2^(s c - m)
-//    for the next PV MMA.  The max used for P is only raised when a logit
-//    exceeds it by more than 2^8 (then O and l are rescaled in TMEM); O / l is
-//    exact either way.
-//  * bf16 caches: 128-key tiles, bf16 MMAs, 128-byte-swizzled TMA boxes that
-//    are the MMA operands as they land.
-//  * fp8-e4m3 caches: 64-key tiles land unswizzled; warps 2-3 widen each tile
-//    to f16 (cvt.rn.f16x2.e4m3x2, exact) into a double-buffered swizzled
-//    operand, zeroing rows past the chunk; the MMAs run on f16 (Q converted
-//    once per CTA, P packed as f16); k_scale / v_scale stay in the softmax
-//    scale and the final normalisation.
+//    half and Q tile (G heads x 128/G tokens: the tile's token-major rows);
+//    key tiles of 128 keys arrive as 16-row page boxes of the 4-D cache
+//    [page, head, slot, dim] (page ids read one tile ahead; boxes past the
+//    chunk point outside the pool, so TMA zero-fills them) into one ring of
+//    mbarrier-tracked slots holding K_0, V_0, K_1, V_1, ...
+//  * warp 1, one thread: tcgen05.mma issuer.  Per Q tile and key tile j it
+//    issues O += P_{j-1} V_{j-1} (P read from tensor memory, V MN-major from
+//    shared memory), then S_j = Q K_j^T (M 128, N 128, K 128) into the same
+//    TMEM columns, so P and S share them; the two Q tiles alternate, and one
+//    tile's softmax runs while the tensor core works on the other's MMAs.
+//    tcgen05.commit signals S-ready, O-done and slot-free mbarriers.
+//  * softmax warps, four per Q tile: one thread per query row (= TMEM lane).
+//    Loads its S row, masks it, keeps a running max m and sum l in fp32, and
+//    writes P = 2^(s c - m) back into tensor memory over S.  The max used for
+//    P is only raised when a logit exceeds it by more than 2^8 (then O and l
+//    are rescaled; O is idle at that point); O / l is exact either way.
+//  * bf16 caches: the TMA boxes land in the MMA's 128-byte-swizzled operand
+//    layout; rows of V past the chunk end are zeroed before the PV MMA reads
+//    them (stale slots may hold NaN).
+//  * fp8-e4m3 caches: raw tiles land unswizzled; four converter warps widen
+//    them into swizzled f16 operand buffers with integer ops -- an e4m3 code
+//    with its exponent and mantissa bits moved into f16 position is the same
+//    value times 2^-8, subnormals included -- and zero rows past the chunk;
+//    the 2^8 goes back in the softmax scale and the final normalisation, next
+//    to k_scale / v_scale.  The MMAs run on f16 (Q converted once per CTA,
+//    P packed as f16).
 // All mbarrier waits are bounded; on expiry the CTA raises VA_DEV_TIMEOUT,
 // stops issuing work, frees its TMEM and exits.
 #include <cuda.h>
@@ -40,48 +46,41 @@
 namespace va {
 namespace {
 
-// NQ = 1: one 128-row Q tile per CTA.  NQ = 2: two Q tiles (256 rows) share
-// every K/V tile, each with its own softmax warpgroup, TMEM S buffers and O
-// accumulator, so K/V bytes, TMA traffic and fp8 widening per row halve and
-// one warpgroup's softmax overlaps the other's MMAs.
 template <bool FP8, int NQ>
 struct TcCfg {
   static constexpr int ROWS = 128, D = 128;              // rows per Q tile = TMEM lanes
+  static constexpr int KEYS = 128;                       // keys per tile (MMA N of S, K of PV)
   static constexpr int BLOCK_ROWS = NQ * ROWS;
-  static constexpr int THREADS = 128 + 128 * NQ;         // 4 role warps + 4 softmax warps per Q tile
-  static constexpr int KEYS = 64;                        // keys per tile
-  static constexpr int STAGES = NQ == 2 ? 4 : (FP8 ? 3 : 2);  // TMA stages (raw fp8, or bf16 operands)
-  static constexpr int CTAS_PER_SM = (NQ == 1 && !FP8) ? 2 : 1;  // two small CTAs hide each other's waits
+  static constexpr int CONV_WARP0 = 4 + 4 * NQ;          // after producer, MMA, 2 spare, softmax
+  static constexpr int CONV_WARPS = FP8 ? 4 : 0;         // one per SM sub-partition
+  static constexpr int THREADS = 32 * (CONV_WARP0 + CONV_WARPS);
   static constexpr int QT_BYTES = ROWS * D * 2;          // one Q tile: [2 halves][128 rows][128 B]
   static constexpr int Q_BYTES = NQ * QT_BYTES;
   static constexpr int OP_BYTES = KEYS * D * 2;          // 16-bit K (or V) operand tile
   static constexpr int RAW_BYTES = KEYS * D;             // fp8 K (or V) tile [keys][128 B]
-  static constexpr int STAGE_BYTES = FP8 ? 2 * RAW_BYTES : 2 * OP_BYTES;
-  static constexpr int CONV_BUFS = FP8 ? 2 : 0;          // widened K+V operand buffers
-  static constexpr int PT_BYTES = ROWS * KEYS * 2;       // one P tile: [key blocks][128 rows][128 B]
+  static constexpr int SLOT_BYTES = FP8 ? RAW_BYTES : OP_BYTES;
+  static constexpr int CONV_BYTES = FP8 ? 3 * OP_BYTES : 0;  // widened K (two) and V (one)
+  static constexpr int RING_AVAIL = 227 * 1024 - 256 - Q_BYTES - CONV_BYTES;
+  static constexpr int NSLOT = RING_AVAIL / SLOT_BYTES > 8 ? 8 : RING_AVAIL / SLOT_BYTES;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + Q_BYTES;
-  static constexpr int OFF_CONV = OFF_KV + STAGES * STAGE_BYTES;
-  static constexpr int OFF_P = OFF_CONV + CONV_BUFS * 2 * OP_BYTES;
-  static constexpr int OFF_BAR = OFF_P + NQ * PT_BYTES;
+  static constexpr int OFF_CONV = OFF_Q + Q_BYTES;
+  static constexpr int OFF_RING = OFF_CONV + CONV_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + NSLOT * SLOT_BYTES;
   static constexpr int SMEM = OFF_BAR + 256;              // + barriers, TMEM address, abort flag
-  static constexpr uint32_t QT_COLS = 256;               // per Q tile: S0 | S1 | O (64 + 64 + 128)
+  static constexpr uint32_t QT_COLS = 256;               // per Q tile: S / P (128) | O (128)
+  static constexpr uint32_t COL_O = 128;
   static constexpr uint32_t TMEM_COLS = NQ * QT_COLS;
-  static constexpr uint32_t COL_O = 2 * KEYS;
-  static constexpr int CONV_WARPS = 2;                    // warps 2-3 (fp8 only)
-  // 228 KB per SM, 1 KB reserved per CTA; at most 227 KB for one CTA
-  static_assert(CTAS_PER_SM * (SMEM + 1024) <= 228 * 1024, "shared memory budget");
+  static_assert(NSLOT >= 3, "ring depth");
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
-  static_assert(CTAS_PER_SM * TMEM_COLS <= 512, "tensor memory budget");
-  static_assert(STAGES <= 4, "barrier slots");
+  static_assert(TMEM_COLS <= 512, "tensor memory budget");
 };
 
 constexpr float kLn2 = 0.6931471805599453f;
 
-// barrier slots (per-Q-tile barriers at base + qt, or base + 2 qt + buffer)
-enum { B_Q = 0, B_Q_READY = 1, B_KV_FULL = 2, B_KV_EMPTY = 6, B_CONV_FULL = 10, B_CONV_FREE = 12,
-       B_S_FULL = 14, B_S_FREE = 18, B_P_FULL = 22, B_O_DONE = 24, B_COUNT = 26 };
-static_assert(8 * B_COUNT + 16 <= 256, "barrier area");
+// barrier slots (per-Q-tile barriers at base + qt)
+enum { B_Q = 0, B_Q_READY = 1, B_FULL = 2, B_EMPTY = 10, B_CK_FULL = 18, B_CK_FREE = 20,
+       B_CV_FULL = 22, B_CV_FREE = 23, B_S_FULL = 24, B_P_FULL = 26, B_O_DONE = 28, B_COUNT = 30 };
+static_assert(8 * B_COUNT + 8 <= 256, "barrier area");
 
 // Instruction descriptor, kind::f16 with f16 A and B (fp32 accumulator).
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
@@ -89,8 +88,30 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) 
          ((uint32_t)(M >> 4) << 24);
 }
 
+// Two e4m3 codes (bits 0-7 and 16-23 of x, the rest zero) -> two f16 equal to
+// the codes' values times 2^-8: sign to bit 15, exponent and mantissa shifted
+// up by 7 (an e4m3 subnormal lands on the f16 subnormal of the same scaled
+// value, since both formats keep 3 resp. 10 mantissa bits under a fixed
+// exponent offset).  The NaN code 0x7f / 0xff maps to a finite value.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint32_t x) {
+  return (x + (x & 0x00800080u)) << 7;
+}
+
+// TMEM column (relative to the Q tile's S / P columns) of P's keys
+// 16 kk .. 16 kk + 15, packed two per column: the P of logits 32 q .. 32 q + 31
+// sits in the first half of their own S columns, 32 q .. 32 q + 15, so the
+// softmax may write it as soon as it has read that chunk of S.
+__host__ __device__ constexpr uint32_t p_col(int kk) { return 32u * (kk >> 1) + 8u * (kk & 1); }
+
+// max(a, b, c) in one instruction (three-input form of sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+
 template <bool FP8, int NQ>
-__global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, TcCfg<FP8, NQ>::CTAS_PER_SM)
+__global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     verify_partial_tc_kernel(const PartialParams p, const __grid_constant__ TcMaps maps) {
   using C = TcCfg<FP8, NQ>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -102,7 +123,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, TcCfg<FP8, NQ>::CTAS_
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * B_COUNT);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 8 * B_COUNT + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 8 * B_COUNT + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   grid_dependency_wait();
@@ -133,19 +154,18 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, TcCfg<FP8, NQ>::CTAS_
   if (tid == 0) {
     mbar_init(bar(B_Q), 1);
     mbar_init(bar(B_Q_READY), 4 * nq);
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar(B_KV_FULL + s), 1);
-      mbar_init(bar(B_KV_EMPTY + s), FP8 ? C::CONV_WARPS : 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_EMPTY + s), FP8 ? C::CONV_WARPS : 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_CONV_FULL + s), C::CONV_WARPS);
-      mbar_init(bar(B_CONV_FREE + s), 1);
+      mbar_init(bar(B_CK_FULL + s), C::CONV_WARPS > 0 ? C::CONV_WARPS : 1);
+      mbar_init(bar(B_CK_FREE + s), 1);
     }
+    mbar_init(bar(B_CV_FULL), C::CONV_WARPS > 0 ? C::CONV_WARPS : 1);
+    mbar_init(bar(B_CV_FREE), 1);
     for (int qt = 0; qt < NQ; ++qt) {
-      for (int s = 0; s < 2; ++s) {
-        mbar_init(bar(B_S_FULL + 2 * qt + s), 1);
-        mbar_init(bar(B_S_FREE + 2 * qt + s), 4);
-      }
+      mbar_init(bar(B_S_FULL + qt), 1);
       mbar_init(bar(B_P_FULL + qt), 4);
       mbar_init(bar(B_O_DONE + qt), 1);
     }
@@ -157,6 +177,8 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, TcCfg<FP8, NQ>::CTAS_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Operand u = 2 j (K_j) or 2 j + 1 (V_j) sits in ring slot u % NSLOT, on its
+  // (u / NSLOT)-th use of that slot.
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
@@ -180,38 +202,38 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, TcCfg<FP8, NQ>::CTAS_
         }
       };
       load_pages(0, cur);
-      for (int j = 0; j < n_tiles; ++j) {
+      bool live = true;
+      for (int j = 0; live && j < n_tiles; ++j) {
         load_pages(j + 1, nxt);
-        const int s = j % C::STAGES;
-        if (j >= C::STAGES &&
-            !mbar_wait(bar(B_KV_EMPTY + s), ((j / C::STAGES) - 1) & 1, abort_flag))
-          break;
-        mbar_expect_tx(bar(B_KV_FULL + s), C::STAGE_BYTES);
-        const uint32_t kdst = sbase + C::OFF_KV + s * C::STAGE_BYTES;
-        const uint32_t vdst = kdst + C::STAGE_BYTES / 2;
         const int k0 = lo + j * C::KEYS;
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          const int key = k0 + 16 * g;
-          int page = p.num_pages;  // outside the pool: zero fill
-          int slot = 0;
-          if (key < hi) {
-            const int pid = cur[g];
-            if ((unsigned)pid < (unsigned)p.num_pages) {
-              page = pid;
-              slot = key & (p.page_size - 1);
-            } else {
-              bad = 1;
-            }
+        for (int v = 0; v < 2; ++v) {
+          const int u = 2 * j + v, s = u % C::NSLOT, n = u / C::NSLOT;
+          if (n >= 1 && !mbar_wait(bar(B_EMPTY + s), (n - 1) & 1, abort_flag)) {
+            live = false;
+            break;
           }
-          if constexpr (FP8) {
-            tma_load_4d(kdst + g * 2048, &maps.k, 0, slot, h, page, bar(B_KV_FULL + s));
-            tma_load_4d(vdst + g * 2048, &maps.v, 0, slot, h, page, bar(B_KV_FULL + s));
-          } else {
-            for (int half = 0; half < 2; ++half) {
-              const uint32_t off = half * (C::KEYS * 128) + g * 2048;
-              tma_load_4d(kdst + off, &maps.k, half * 64, slot, h, page, bar(B_KV_FULL + s));
-              tma_load_4d(vdst + off, &maps.v, half * 64, slot, h, page, bar(B_KV_FULL + s));
+          mbar_expect_tx(bar(B_FULL + s), C::SLOT_BYTES);
+          const uint32_t dst = sbase + C::OFF_RING + s * C::SLOT_BYTES;
+          const void* map = v ? static_cast<const void*>(&maps.v) : static_cast<const void*>(&maps.k);
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const int key = k0 + 16 * g;
+            int page = p.num_pages;  // outside the pool: zero fill
+            int slot = 0;
+            if (key < hi) {
+              const int pid = cur[g];
+              if ((unsigned)pid < (unsigned)p.num_pages) {
+                page = pid;
+                slot = key & (p.page_size - 1);
+              } else {
+                bad = 1;
+              }
+            }
+            if constexpr (FP8) {
+              tma_load_4d(dst + g * 2048, map, 0, slot, h, page, bar(B_FULL + s));
+            } else {
+              tma_load_4d(dst + g * 2048, map, 0, slot, h, page, bar(B_FULL + s));
+              tma_load_4d(dst + C::KEYS * 128 + g * 2048, map, 64, slot, h, page, bar(B_FULL + s));
             }
           }
         }
@@ -226,104 +248,125 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, TcCfg<FP8, NQ>::CTAS_
       constexpr uint32_t id_s = FP8 ? idesc_f16(C::ROWS, C::KEYS, false)
                                     : idesc_bf16(C::ROWS, C::KEYS, false);
       constexpr uint32_t id_o = FP8 ? idesc_f16(C::ROWS, C::D, true) : idesc_bf16(C::ROWS, C::D, true);
-      auto kop = [&](int j) {  // K operand of tile j
-        return FP8 ? sbase + C::OFF_CONV + (j & 1) * 2 * C::OP_BYTES
-                   : sbase + C::OFF_KV + (j % C::STAGES) * C::STAGE_BYTES;
+      auto k_addr = [&](int j) {
+        return FP8 ? sbase + C::OFF_CONV + (j & 1) * C::OP_BYTES
+                   : sbase + C::OFF_RING + ((2 * j) % C::NSLOT) * C::SLOT_BYTES;
       };
-      auto free_bar = [&](int j) {  // released once tile j's last MMA is done
-        return FP8 ? bar(B_CONV_FREE + (j & 1)) : bar(B_KV_EMPTY + j % C::STAGES);
+      auto v_addr = [&](int j) {
+        return FP8 ? sbase + C::OFF_CONV + 2 * C::OP_BYTES
+                   : sbase + C::OFF_RING + ((2 * j + 1) % C::NSLOT) * C::SLOT_BYTES;
       };
-      auto pv = [&](int qt, int j) {  // O_qt (+)= P_qt V_j
-        const uint32_t vaddr = kop(j) + C::OP_BYTES;
-        const uint32_t paddr = sbase + C::OFF_P + qt * C::PT_BYTES;
-        for (int kk = 0; kk < C::KEYS / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(paddr + (kk >> 2) * (C::ROWS * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(vaddr + kk * 16 * 128, C::KEYS * 128, 1024);
-          umma_bf16(tmem + qt * C::QT_COLS + C::COL_O, a, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(B_O_DONE + qt));
+      auto wait_k = [&](int j) {
+        if (FP8) return mbar_wait(bar(B_CK_FULL + (j & 1)), (j >> 1) & 1, abort_flag);
+        const int u = 2 * j;
+        return mbar_wait(bar(B_FULL + u % C::NSLOT), (u / C::NSLOT) & 1, abort_flag);
       };
-      // all live Q tiles' P_{j} -> PV, then release tile j's operands
-      auto pv_all = [&](int j) {
-        for (int qt = 0; qt < nq; ++qt) {
-          if (!mbar_wait(bar(B_P_FULL + qt), j & 1, abort_flag)) return false;
-          tc_fence_after();
-          pv(qt, j);
-        }
-        umma_commit(free_bar(j));
-        return true;
+      auto wait_v = [&](int j) {
+        if (FP8) return mbar_wait(bar(B_CV_FULL), j & 1, abort_flag);
+        const int u = 2 * j + 1;
+        return mbar_wait(bar(B_FULL + u % C::NSLOT), (u / C::NSLOT) & 1, abort_flag);
       };
+      auto k_free_bar = [&](int j) {
+        return FP8 ? bar(B_CK_FREE + (j & 1)) : bar(B_EMPTY + (2 * j) % C::NSLOT);
+      };
+      auto v_free_bar = [&](int j) {
+        return FP8 ? bar(B_CV_FREE) : bar(B_EMPTY + (2 * j + 1) % C::NSLOT);
+      };
+      // The issue loop is this thread's critical path: descriptors are built
+      // once per operand and advanced by adding byte offsets >> 4 to their
+      // start-address field (every operand lies below 256 KB: no carry).
+      const uint64_t dq0 = smem_desc_sw128(sbase + C::OFF_Q, 16, 1024);
       bool live = mbar_wait(bar(FP8 ? B_Q_READY : B_Q), 0, abort_flag);
-      int issued_pv = 0;
-      for (int j = 0; live && j < n_tiles; ++j) {
-        const int sb = j & 1;
-        if (FP8) {
-          if (!mbar_wait(bar(B_CONV_FULL + sb), (j >> 1) & 1, abort_flag)) break;
-        } else {
-          if (!mbar_wait(bar(B_KV_FULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag)) break;
-        }
-        const uint32_t kaddr = kop(j);
-        for (int qt = 0; qt < nq; ++qt) {
-          if (j >= 2 && !mbar_wait(bar(B_S_FREE + 2 * qt + sb), ((j >> 1) - 1) & 1, abort_flag)) {
-            live = false;
-            break;
+      for (int j = 0; live && j <= n_tiles; ++j) {
+        // step j: PV of tile j - 1 and S of tile j, Q tile by Q tile
+        if (j < n_tiles && !wait_k(j)) break;
+        if (j >= 1 && !wait_v(j - 1)) break;
+        const uint64_t dk = j < n_tiles ? smem_desc_sw128(k_addr(j), 16, 1024) : 0;
+        const uint64_t dv = j >= 1 ? smem_desc_sw128(v_addr(j - 1), C::KEYS * 128, 1024) : 0;
+#pragma unroll
+        for (int qt = 0; qt < NQ; ++qt) {
+          if (qt >= nq) break;
+          const uint32_t ts = tmem + qt * C::QT_COLS;  // S_qt / P_qt columns
+          if (j >= 1) {
+            if (!mbar_wait(bar(B_P_FULL + qt), (j - 1) & 1, abort_flag)) {
+              live = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < C::KEYS / 16; ++kk)
+              umma_ts(ts + C::COL_O, ts + p_col(kk), dv + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                      (j > 1 || kk > 0) ? 1u : 0u);
+            if (j == n_tiles) umma_commit(bar(B_O_DONE + qt));
           }
-          tc_fence_after();
-          const uint32_t qaddr = sbase + C::OFF_Q + qt * C::QT_BYTES;
-          for (int kk = 0; kk < C::D / 16; ++kk) {
-            const uint64_t a = smem_desc_sw128(qaddr + (kk >> 2) * (C::ROWS * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(kaddr + (kk >> 2) * (C::KEYS * 128) + (kk & 3) * 32, 16, 1024);
-            umma_bf16(tmem + qt * C::QT_COLS + sb * C::KEYS, a, bd, id_s, kk > 0 ? 1u : 0u);
+          if (j < n_tiles) {
+            const uint64_t dq = dq0 + (uint64_t)(qt * (C::QT_BYTES >> 4));
+#pragma unroll
+            for (int kk = 0; kk < C::D / 16; ++kk)
+              umma_bf16(ts, dq + (uint64_t)((((kk >> 2) * (C::ROWS * 128)) + (kk & 3) * 32) >> 4),
+                        dk + (uint64_t)((((kk >> 2) * (C::KEYS * 128)) + (kk & 3) * 32) >> 4), id_s,
+                        kk > 0 ? 1u : 0u);
+            umma_commit(bar(B_S_FULL + qt));
           }
-          umma_commit(bar(B_S_FULL + 2 * qt + sb));
         }
         if (!live) break;
-        if (j >= 1) {
-          if (!pv_all(j - 1)) break;
-          issued_pv = j;
-        }
+        if (j >= 1) umma_commit(v_free_bar(j - 1));
+        if (j < n_tiles) umma_commit(k_free_bar(j));
       }
-      if (!*abort_flag && issued_pv == n_tiles - 1) {
+      // the last slot releases land before the CTA's shared memory goes away
+      if (live && !*abort_flag && n_tiles >= 1) {
         const int j = n_tiles - 1;
-        // the last buffer release lands before the CTA's shared memory goes away
-        if (pv_all(j)) {
-          if (FP8)
-            mbar_wait(bar(B_CONV_FREE + (j & 1)), (j >> 1) & 1, abort_flag);
-          else
-            mbar_wait(bar(B_KV_EMPTY + j % C::STAGES), (j / C::STAGES) & 1, abort_flag);
+        if (FP8) {
+          mbar_wait(bar(B_CV_FREE), j & 1, abort_flag);
+          mbar_wait(bar(B_CK_FREE + (j & 1)), (j >> 1) & 1, abort_flag);
+        } else {
+          const int uk = 2 * j, uv = 2 * j + 1;
+          mbar_wait(bar(B_EMPTY + uv % C::NSLOT), (uv / C::NSLOT) & 1, abort_flag);
+          mbar_wait(bar(B_EMPTY + uk % C::NSLOT), (uk / C::NSLOT) & 1, abort_flag);
         }
       }
     }
-  } else if (warp < 4) {
-    if constexpr (FP8) {
-      // ---------------- fp8 -> f16 widening (warps 2-3) ----------------
-      const int ct = tid - 64;                      // 0 .. 63
-      constexpr int CH = C::KEYS * 8;               // 16-byte raw chunks per K (or V) tile
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % C::STAGES, cb = j & 1;
-        if (!mbar_wait(bar(B_KV_FULL + s), (j / C::STAGES) & 1, abort_flag)) break;
-        if (j >= 2 && !mbar_wait(bar(B_CONV_FREE + cb), ((j >> 1) - 1) & 1, abort_flag)) break;
-        const uint8_t* raw = smem + C::OFF_KV + s * C::STAGE_BYTES;
-        uint8_t* dst = smem + C::OFF_CONV + cb * 2 * C::OP_BYTES;
+  } else if (FP8 && warp >= C::CONV_WARP0) {
+    // ---------------- fp8 -> scaled f16 widening ----------------
+    // Step i widens K_i, then V_{i-1}: K runs a tile ahead, since S_i needs
+    // only K_i while V's single buffer frees up one PV later.
+    const int ct = tid - 32 * C::CONV_WARP0;            // 0 .. 127
+    constexpr int NCT = 32 * C::CONV_WARPS;
+    for (int i = 0; i <= n_tiles; ++i) {
+      bool go = true;
+      for (int v = 0; v < 2; ++v) {
+        const int j = i - v;                            // tile of this operand
+        if (j < 0 || j >= n_tiles) continue;
+        const int u = 2 * j + v, s = u % C::NSLOT, n = u / C::NSLOT;
+        if (!mbar_wait(bar(B_FULL + s), n & 1, abort_flag)) { go = false; break; }
+        if (v == 0 && j >= 2 && !mbar_wait(bar(B_CK_FREE + (j & 1)), ((j >> 1) - 1) & 1, abort_flag)) {
+          go = false;
+          break;
+        }
+        if (v == 1 && j >= 1 && !mbar_wait(bar(B_CV_FREE), (j - 1) & 1, abort_flag)) {
+          go = false;
+          break;
+        }
         const int k0 = lo + j * C::KEYS;
+        const uint8_t* raw = smem + C::OFF_RING + s * C::SLOT_BYTES;
+        uint8_t* dst = smem + C::OFF_CONV + (v ? 2 : (j & 1)) * C::OP_BYTES;
 #pragma unroll 4
-        for (int c = ct; c < 2 * CH; c += 64) {
-          const int which = c / CH, cc = c - which * CH;
-          const int r = cc >> 3, ch = cc & 7;       // key row, 16-element column group
+        for (int c = ct; c < C::KEYS * 8; c += NCT) {
+          const int r = c >> 3, ch = c & 7;         // key row, 16-code group
           uint4 a = make_uint4(0u, 0u, 0u, 0u), bq = a;
           if (k0 + r < hi) {
-            const uint4 w = *reinterpret_cast<const uint4*>(raw + which * C::RAW_BYTES + r * 128 + ch * 16);
-            a.x = e4m3x2_to_f16x2((uint16_t)(w.x & 0xffff));
-            a.y = e4m3x2_to_f16x2((uint16_t)(w.x >> 16));
-            a.z = e4m3x2_to_f16x2((uint16_t)(w.y & 0xffff));
-            a.w = e4m3x2_to_f16x2((uint16_t)(w.y >> 16));
-            bq.x = e4m3x2_to_f16x2((uint16_t)(w.z & 0xffff));
-            bq.y = e4m3x2_to_f16x2((uint16_t)(w.z >> 16));
-            bq.z = e4m3x2_to_f16x2((uint16_t)(w.w & 0xffff));
-            bq.w = e4m3x2_to_f16x2((uint16_t)(w.w >> 16));
+            const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + ch * 16);
+            a.x = e4m3x2_scaled_f16x2(__byte_perm(w.x, 0u, 0x4140));
+            a.y = e4m3x2_scaled_f16x2(__byte_perm(w.x, 0u, 0x4342));
+            a.z = e4m3x2_scaled_f16x2(__byte_perm(w.y, 0u, 0x4140));
+            a.w = e4m3x2_scaled_f16x2(__byte_perm(w.y, 0u, 0x4342));
+            bq.x = e4m3x2_scaled_f16x2(__byte_perm(w.z, 0u, 0x4140));
+            bq.y = e4m3x2_scaled_f16x2(__byte_perm(w.z, 0u, 0x4342));
+            bq.z = e4m3x2_scaled_f16x2(__byte_perm(w.w, 0u, 0x4140));
+            bq.w = e4m3x2_scaled_f16x2(__byte_perm(w.w, 0u, 0x4342));
           }
           // 16 f16 = 2 chunks of the swizzled operand row (half = ch / 4)
-          uint8_t* row = dst + which * C::OP_BYTES + (ch >> 2) * (C::KEYS * 128) + r * 128;
+          uint8_t* row = dst + (ch >> 2) * (C::KEYS * 128) + r * 128;
           const int c0 = (ch & 3) * 2;
           *reinterpret_cast<uint4*>(row + (((c0) ^ (r & 7)) << 4)) = a;
           *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = bq;
@@ -331,12 +374,13 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, TcCfg<FP8, NQ>::CTAS_
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar(B_CONV_FULL + cb));
-          mbar_arrive(bar(B_KV_EMPTY + s));
+          mbar_arrive(bar(v ? B_CV_FULL : B_CK_FULL + (j & 1)));
+          mbar_arrive(bar(B_EMPTY + s));
         }
       }
+      if (!go) break;
     }
-  } else if ((warp - 4) / 4 < nq) {
+  } else if (warp >= 4 && warp < 4 + 4 * NQ && (warp - 4) / 4 < nq) {
     // ---------------- softmax / epilogue: one thread per row, 4 warps per Q tile ----------------
     const int qt = (warp - 4) >> 2;                 // Q tile of this warpgroup
     const int quad = warp & 3;                      // TMEM lane quarter this warp may access
@@ -346,18 +390,15 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, TcCfg<FP8, NQ>::CTAS_
     const bool row_ok = br < nrows;
     const int t = (row0 + br) / G;                  // draft token of the row
     const int moff = p.mask ? p.mask_indptr[b] : 0;
-    const float c = p.scale_log2;
-    const uint32_t b_s_full = bar(B_S_FULL + 2 * qt), b_s_free = bar(B_S_FREE + 2 * qt);
-    const uint32_t b_p_full = bar(B_P_FULL + qt), b_o_done = bar(B_O_DONE + qt);
-    uint8_t* const ptile = smem + C::OFF_P + qt * C::PT_BYTES;
+    // fp8 operands hold the codes' values times 2^-8 (see e4m3x2_scaled_f16x2)
+    const float c = FP8 ? p.scale_log2 * 256.f : p.scale_log2;
+    const uint32_t b_s_full = bar(B_S_FULL + qt), b_p_full = bar(B_P_FULL + qt);
     float m_used = -INFINITY;                       // in units of s * c (log2 domain)
     float l = 0.f;
-    float s[C::KEYS];
-    uint32_t pk[C::KEYS / 2];
     bool live = true;
     if (FP8) {
       // Q to f16, in place (each thread its own row)
-      if (!mbar_wait(bar(B_Q), 0, abort_flag)) live = false;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, abort_flag))) live = false;
       if (live) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -379,85 +420,95 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, TcCfg<FP8, NQ>::CTAS_
       if (lane == 0) mbar_arrive(bar(B_Q_READY));
     }
     for (int j = 0; live && j < n_tiles; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(b_s_full + 8 * sb, (j >> 1) & 1, abort_flag)) { live = false; break; }
-      tc_fence_after();
-      {
-        uint32_t raw[C::KEYS];
-#pragma unroll
-        for (int q = 0; q < C::KEYS / 32; ++q) tmem_ld32(lane_addr + sb * C::KEYS + q * 32, raw + q * 32);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < C::KEYS; ++e) s[e] = __uint_as_float(raw[e]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_s_free + 8 * sb);
-
       const int k0 = lo + j * C::KEYS;
-      if (k0 + C::KEYS > prefix || k0 + C::KEYS > hi) {
-        if (!p.mask) {
-          // causal drafts: this row sees keys below min(hi, prefix + t + 1)
-          const int lim = min(hi, prefix + t + 1) - k0;
-#pragma unroll
-          for (int cc = 0; cc < C::KEYS; ++cc) s[cc] = cc < lim ? s[cc] : -INFINITY;
-        } else {
-          // per 32-key group: visibility bits (prefix 1, drafts from the
-          // row's mask bits, nothing at or past hi), then one select per key
-#pragma unroll
-          for (int q = 0; q < C::KEYS / 32; ++q) {
-            const int g0 = k0 + 32 * q;
-            uint32_t vis = 0;
-            if (g0 < hi) {
-              const int below_prefix = min(max(prefix - g0, 0), 32);
-              vis = below_prefix == 32 ? 0xffffffffu : ((1u << below_prefix) - 1u);
-              if (below_prefix < 32 && t < L) {
-                // draft columns u = g0 + i - prefix for i >= below_prefix
-                const int u0 = g0 + below_prefix - prefix;
-                const long long bit0 = (long long)moff + (long long)t * L + u0;
-                const int nbits = min(32 - below_prefix, L - u0);
-                if (nbits > 0) {
-                  uint64_t w = 0;
-                  const int nbytes = (int)((((bit0 & 7) + nbits) + 7) >> 3);
-                  for (int k = 0; k < nbytes; ++k)
-                    w |= (uint64_t)__ldg(p.mask + (bit0 >> 3) + k) << (8 * k);
-                  w >>= (bit0 & 7);
-                  const uint32_t dbits =
-                      (uint32_t)(w & (nbits >= 32 ? 0xffffffffull : ((1ull << nbits) - 1ull)));
-                  vis |= dbits << below_prefix;
-                }
-              }
-              const int in_range = min(hi - g0, 32);
-              if (in_range < 32) vis &= (1u << in_range) - 1u;
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              s[32 * q + i] = ((vis >> i) & 1u) ? s[32 * q + i] : -INFINITY;
+      if constexpr (!FP8) {
+        // Rows of V_j past the chunk end inside the last 16-key box may hold
+        // stale (even NaN) slots: zero them, since 0 * NaN would poison O.
+        // Q tile 0's warps do it before their P_j is posted; PV_j of every Q
+        // tile is issued after that.
+        const int tail = hi - k0;
+        if (qt == 0 && tail < C::KEYS && (tail & 15)) {
+          const int u = 2 * j + 1, s = u % C::NSLOT;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_FULL + s), (u / C::NSLOT) & 1, abort_flag))) {
+            live = false;
+            break;
           }
+          const int zlo = tail, zhi = (tail + 15) & ~15;
+          uint8_t* vt = smem + C::OFF_RING + s * C::SLOT_BYTES;
+          for (int z = r; z < (zhi - zlo) * 16; z += C::ROWS) {
+            const int row = zlo + z / 16, half = (z / 8) & 1, ch = z & 7;
+            *reinterpret_cast<uint4*>(vt + half * (C::KEYS * 128) + row * 128 + (ch << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async();
         }
       }
-      float mx = -INFINITY;
+      if (!__all_sync(0xffffffffu, mbar_wait(b_s_full, j & 1, abort_flag))) { live = false; break; }
+      tc_fence_after();
+
+      // Visibility of the tile's keys for this row.  Causal drafts: keys below
+      // lim = min(hi, prefix + t + 1) - k0.  Custom mask: one word per 32 keys
+      // (prefix 1, drafts from the row's mask bits, nothing at or past hi).
+      // A tile every row of the warp sees whole skips the per-key selects.
+      const int lim = min(hi, prefix + t + 1) - k0;
+      uint32_t vis[C::KEYS / 32];
+      bool full;
+      if (!p.mask) {
+        full = __all_sync(0xffffffffu, lim >= C::KEYS);
+      } else if (k0 + C::KEYS <= prefix && k0 + C::KEYS <= hi) {
+        full = true;
+      } else {
+        uint32_t all = 0xffffffffu;
 #pragma unroll
-      for (int cc = 0; cc < C::KEYS; ++cc) mx = fmaxf(mx, s[cc]);
-      mx *= c;  // c > 0
-      float m_new = m_used;
-      if (mx > m_used + 8.f) m_new = mx;   // also taken when m_used = -inf and mx is finite
-      const float alpha = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
-      const float base = m_new == -INFINITY ? 0.f : m_new;
-      float sum = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < C::KEYS; cc += 2) {
-        const float p0 = ex2(fmaf(s[cc], c, -base));
-        const float p1 = ex2(fmaf(s[cc + 1], c, -base));
-        sum += p0 + p1;
-        pk[cc / 2] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+        for (int q = 0; q < C::KEYS / 32; ++q) {
+          const int g0 = k0 + 32 * q;
+          uint32_t w32 = 0;
+          if (g0 < hi) {
+            const int below_prefix = min(max(prefix - g0, 0), 32);
+            w32 = below_prefix == 32 ? 0xffffffffu : ((1u << below_prefix) - 1u);
+            if (below_prefix < 32 && t < L) {
+              // draft columns u = g0 + i - prefix for i >= below_prefix
+              const int u0 = g0 + below_prefix - prefix;
+              const long long bit0 = (long long)moff + (long long)t * L + u0;
+              const int nbits = min(32 - below_prefix, L - u0);
+              if (nbits > 0) {
+                uint64_t w = 0;
+                const int nbytes = (int)((((bit0 & 7) + nbits) + 7) >> 3);
+                for (int k = 0; k < nbytes; ++k)
+                  w |= (uint64_t)__ldg(p.mask + (bit0 >> 3) + k) << (8 * k);
+                w >>= (bit0 & 7);
+                const uint32_t dbits =
+                    (uint32_t)(w & (nbits >= 32 ? 0xffffffffull : ((1ull << nbits) - 1ull)));
+                w32 |= dbits << below_prefix;
+              }
+            }
+            const int in_range = min(hi - g0, 32);
+            if (in_range < 32) w32 &= (1u << in_range) - 1u;
+          }
+          vis[q] = w32;
+          all &= w32;
+        }
+        full = __all_sync(0xffffffffu, all == 0xffffffffu);
       }
-      l = l * alpha + sum;
-      // P buffer and O are free once the previous PV has completed.
-      if (j >= 1) {
-        if (!mbar_wait(b_o_done, (j - 1) & 1, abort_flag)) { live = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      // Keys 32 q .. 32 q + 31 of the tile this row may see, one bit each.
+      auto vis_word = [&](int q) -> uint32_t {
+        if (!p.mask) {
+          const int n = lim - 32 * q;
+          return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+        }
+        return q == 0 ? vis[0] : q == 1 ? vis[1] : q == 2 ? vis[2] : vis[3];
+      };
+      // the row's new reference max from this tile's max (log2 units); O is
+      // idle here (PV_{j-1} of this Q tile completed before S_j did), so a
+      // raised max rescales it at once
+      float alpha = 1.f, base = 0.f;
+      auto new_max = [&](float mx) {
+        mx *= c;  // c > 0
+        float m_new = m_used;
+        if (mx > m_used + 8.f) m_new = mx;   // also taken when m_used = -inf and mx is finite
+        alpha = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
+        base = m_new == -INFINITY ? 0.f : m_new;
+        if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
           for (int q = 0; q < C::D / 32; ++q) {
             uint32_t ov[32];
             tmem_ld32(lane_addr + C::COL_O + q * 32, ov);
@@ -466,42 +517,87 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, TcCfg<FP8, NQ>::CTAS_
             for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
             tmem_st32(lane_addr + C::COL_O + q * 32, ov);
           }
-          tmem_wait_st();
         }
-      }
-      if constexpr (!FP8) {
-        // Rows of V past the chunk end inside the last 16-key box may hold
-        // stale (even NaN) slots: zero them, since 0 * NaN would poison O.
-        // Q tile 0's warps do it; the MMAs of every Q tile's PV wait for them.
-        const int tail = hi - k0;
-        if (qt == 0 && tail < C::KEYS && (tail & 15)) {
-          const int zlo = tail, zhi = (tail + 15) & ~15;
-          uint8_t* vt = smem + C::OFF_KV + (j % C::STAGES) * C::STAGE_BYTES + C::OP_BYTES;
-          for (int z = r; z < (zhi - zlo) * 16; z += C::ROWS) {
-            const int row = zlo + z / 16, half = (z / 8) & 1, ch = z & 7;
-            *reinterpret_cast<uint4*>(vt + half * (C::KEYS * 128) + row * 128 + (ch << 4)) =
-                make_uint4(0u, 0u, 0u, 0u);
+        m_used = m_new;
+      };
+      // P of 32 logits (with visibility word vw) into columns 32 q .. 32 q + 15
+      float sums[4] = {0.f, 0.f, 0.f, 0.f};
+      auto exp_chunk = [&](const uint32_t (&raw)[32], int q, uint32_t vw, bool masked) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float s0 = __uint_as_float(raw[2 * i]), s1 = __uint_as_float(raw[2 * i + 1]);
+          if (masked) {
+            s0 = ((vw >> (2 * i)) & 1u) ? s0 : -INFINITY;
+            s1 = ((vw >> (2 * i + 1)) & 1u) ? s1 : -INFINITY;
+          }
+          const float p0 = ex2(fmaf(s0, c, -base));
+          const float p1 = ex2(fmaf(s1, c, -base));
+          sums[i & 3] += p0 + p1;
+          pk[i] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+        }
+        tmem_st16(lane_addr + 32 * q, pk);
+      };
+      if (full) {
+        // Every key visible: S read twice as two halves of 64 columns.  The
+        // second half is still in registers after the max, so it is
+        // exponentiated first and the first half read once more.
+        uint32_t ra[32], rb[32];
+        float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          tmem_ld32(lane_addr + 64 * h2, ra);
+          tmem_ld32(lane_addr + 64 * h2 + 32, rb);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+            mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
           }
         }
-      }
-      // P row -> shared memory, K-major 128-byte-swizzled [key block][row][128 B]
+        new_max(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])));
+        exp_chunk(ra, 2, 0xffffffffu, false);
+        exp_chunk(rb, 3, 0xffffffffu, false);
+        tmem_ld32(lane_addr, ra);
+        tmem_ld32(lane_addr + 32, rb);
+        tmem_wait_ld();
+        exp_chunk(ra, 0, 0xffffffffu, false);
+        exp_chunk(rb, 1, 0xffffffffu, false);
+      } else {
+        // Some keys hidden: 32 columns at a time in rolled loops (small code).
+        float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+        for (int q = 0; q < C::KEYS / 32; ++q) {
+          uint32_t raw[32];
+          tmem_ld32(lane_addr + q * 32, raw);
+          tmem_wait_ld();
+          const uint32_t vw = vis_word(q);
 #pragma unroll
-      for (int ch = 0; ch < C::KEYS / 8; ++ch) {
-        const int kb = ch >> 3, c8 = ch & 7;
-        *reinterpret_cast<uint4*>(ptile + kb * (C::ROWS * 128) + r * 128 + ((c8 ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          for (int i = 0; i < 16; ++i)
+            mxs[i & 3] = fmax3(mxs[i & 3], ((vw >> (2 * i)) & 1u) ? __uint_as_float(raw[2 * i]) : -INFINITY,
+                               ((vw >> (2 * i + 1)) & 1u) ? __uint_as_float(raw[2 * i + 1]) : -INFINITY);
+        }
+        new_max(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])));
+#pragma unroll 1
+        for (int q = 0; q < C::KEYS / 32; ++q) {
+          uint32_t raw[32];
+          tmem_ld32(lane_addr + q * 32, raw);
+          tmem_wait_ld();
+          exp_chunk(raw, q, vis_word(q), true);
+        }
       }
-      fence_proxy_async();
+      const float sum = (sums[0] + sums[1]) + (sums[2] + sums[3]);
+      l = l * alpha + sum;
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_p_full);
-      m_used = m_new;
     }
     // epilogue
-    if (live && mbar_wait(b_o_done, (n_tiles - 1) & 1, abort_flag)) {
+    if (live && __all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE + qt), 0, abort_flag))) {
       tc_fence_after();
       const float lse = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
-      const float inv = l > 0.f ? p.v_scale / l : 0.f;
+      const float inv = l > 0.f ? (FP8 ? p.v_scale * 256.f : p.v_scale) / l : 0.f;
       size_t orow = 0;
       if (row_ok) {
         const int g = (row0 + br) - t * G;

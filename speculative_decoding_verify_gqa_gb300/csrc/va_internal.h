@@ -15,6 +15,8 @@ constexpr uint32_t kPlanVersion = 1;
 // cut on multiples of it, so every tile starts on a page boundary whenever
 // page_size <= kTileKeys, and lies inside one page otherwise.
 constexpr int kTileKeys = 64;
+// Key tile of the tcgen05 variants (the MMA's N for S = Q K^T).
+constexpr int kTcTileKeys = 128;
 
 // Kernel variants (values match VA_KERNEL_* in verify_attn.h).
 enum Kernel : int32_t {

@@ -134,7 +134,8 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     else kernel = max_rows <= 64 ? kKernelMma64 : kKernelMma128;
   }
   const int BM = kernel_rows(kernel);
-  const int TK = kTileKeys;
+  // chunks are cut on the key tile of the chosen variant
+  const int TK = kernel_is_tc(kernel) ? kTcTileKeys : kTileKeys;
 
   // Units of work: row blocks of each request (times each KV head).  Without
   // a mask a row block's last visible key is that of its last token, prefix +

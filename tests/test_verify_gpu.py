@@ -402,3 +402,4 @@ def test_named_workload_matches_oracle(va, name):
         assert np.array_equal(caches[0], ok) and np.array_equal(caches[1], ov)
         caches = (ok, ov)
     compare(wl, out, lse, rows=rows, caches=caches, strict=True)
+
