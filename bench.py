@@ -81,19 +81,22 @@ def algorithmic(wl):
                 flops=flops, tokens=wl.total_qo)
 
 
-def kernel_source_sha():
+def kernel_source_sha(kernel=0):
+    """sha256 prefix of the sources of the split-kernel variant (1, 2: warp
+    level; 3, 4: tcgen05)."""
     h = hashlib.sha256()
-    for f in ("k_partial_mma.cu", "va_device.cuh", "va_kernels.h"):
+    files = ("k_partial_tc.cu", "va_tc.cuh") if kernel in (3, 4) else ("k_partial_mma.cu",)
+    for f in files + ("va_device.cuh", "va_kernels.h"):
         with open(os.path.join(ROOT, "speculative_decoding_verify_gqa_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, kernel=0):
     """DRAM bytes per launch of the split kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic_per_launch.md")
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(kernel)
     try:
         for line in open(path):
             parts = line.strip().strip("|").split("|")
@@ -356,7 +359,7 @@ class Bench:
 
 
 KERNEL_NAMES = {1: "verify_partial_mma_kernel<4 warps>", 2: "verify_partial_mma_kernel<8 warps>",
-                3: "verify_partial_tc_kernel"}
+                3: "verify_partial_tc_kernel<one Q tile>", 4: "verify_partial_tc_kernel<two Q tiles>"}
 
 
 def roofline_for(wl, kt, peaks, peak_kind, kernel=0):
@@ -466,7 +469,7 @@ def run_ours(args):
     ms_max = reduce_max(ms, world)
     kt = bench.kernel_times()
     rf = roofline_for(wl, kt, peaks, peak_kind, bench.plan.header()["kernel"])
-    rf["traffic"] = profiled_traffic(wl.name)
+    rf["traffic"] = profiled_traffic(wl.name, bench.plan.header()["kernel"])
     alg = algorithmic(wl)
     value = world * wl.total_qo / (ms_max * 1e-3)
     line = {
@@ -478,7 +481,7 @@ def run_ours(args):
         "gpu_launches": args.steps * bench.launches_per_step,
         "roofline": rf, "clocks": clocks,
         "us_per_call": round((kt["partial_ms"] + kt["merge_ms"]) * 1e3, 3),
-        "kernel_us": {k: round(v * 1e3, 3) for k, v in kt.items()},
+        "kernel_us": {k.replace("_ms", ""): round(v * 1e3, 3) for k, v in kt.items()},
         "attention_hbm_gbs": round(alg["total_bytes"] / ((kt["partial_ms"] + kt["merge_ms"]) * 1e-3) / 1e9, 1),
         "plan_host_us": round(bench.plan_us(), 2),
     }
@@ -497,11 +500,11 @@ def run_ours(args):
             ms_o, _ = b.time_steps(steps, 16)
             kto = b.kernel_times(32)
             rfo = roofline_for(b.wl, kto, peaks, peak_kind, b.plan.header()["kernel"])
-            rfo["traffic"] = profiled_traffic(name)
+            rfo["traffic"] = profiled_traffic(name, b.plan.header()["kernel"])
             others[name] = {"tokens_per_s": round(b.wl.total_qo / (ms_o * 1e-3), 1),
                             "ms_per_step": round(ms_o, 6),
                             "us_per_call": round((kto["partial_ms"] + kto["merge_ms"]) * 1e3, 3),
-                            "kernel_us": {k: round(v * 1e3, 3) for k, v in kto.items()},
+                            "kernel_us": {k.replace("_ms", ""): round(v * 1e3, 3) for k, v in kto.items()},
                             "roofline": rfo, "config": workload_config(b.wl, b)}
             del b
             torch.cuda.empty_cache()

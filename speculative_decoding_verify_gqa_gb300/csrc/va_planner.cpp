@@ -126,11 +126,11 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   int kernel = o.kernel;
   if ((kernel == VA_KERNEL_TC_128 || kernel == VA_KERNEL_TC_256) && !tc_ok) return VA_ERR_UNSUPPORTED;
   if (kernel == VA_KERNEL_AUTO) {
-    // Measured on GB300: the tcgen05 variant wins once row blocks are full
-    // (prefill-like, >= 128 rows per KV head) on bf16 caches; the warp-level
-    // variant keeps verify-sized blocks (its 64-row form fits two CTAs per SM)
-    // and fp8 caches (exact bf16 widening, no f16 range limit on Q).
-    if (tc_ok && kv_dtype == VA_DTYPE_BF16 && max_rows >= 128) kernel = kKernelTc128;
+    // Measured on GB300: the tcgen05 variant with two Q tiles per CTA wins
+    // once a KV head has >= 128 rows (prefill-like and wide trees, bf16 or fp8
+    // caches); the warp-level variant keeps verify-sized blocks, where the
+    // tcgen05 CTA's fixed pipeline fill would dominate.
+    if (tc_ok && max_rows >= 128) kernel = kKernelTc256;
     else kernel = max_rows <= 64 ? kKernelMma64 : kKernelMma128;
   }
   const int BM = kernel_rows(kernel);
@@ -170,7 +170,10 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
                                                 : kernel_ctas_per_sm(kernel));
   const int es = kv_dtype == VA_DTYPE_FP8_E4M3 ? 1 : 2;
   const int64_t key_bytes = 2LL * head_dim * es;
-  const int64_t fixed_bytes = 48 * 1024;
+  // fixed cost of a CTA (prologue, pipeline fill and drain, epilogue) in
+  // K/V-byte equivalents: measured about two to three key tiles' worth for the
+  // tcgen05 variants, under one tile for the warp-level ones
+  const int64_t fixed_bytes = kernel_is_tc(kernel) ? 152 * 1024 : 48 * 1024;
   const int64_t partial_bytes_per_row = 4LL * head_dim;
   int64_t min_chunk = o.min_chunk > 0 ? o.min_chunk : 2 * TK;
   min_chunk = ceil_div(min_chunk, TK) * TK;

@@ -162,8 +162,8 @@ def test_plans_of_the_named_workloads(va, name):
     hd = plan.header()
     # kernel variant follows the rows per KV head (G * L) and the cache dtype
     rows = int((wl.group * wl.qo_lens).max())
-    if rows >= 128 and wl.kv_dtype == synthetic.BF16 and wl.d == 128 and 128 % wl.group == 0:
-        assert hd["kernel"] == 3
+    if rows >= 128 and wl.d == 128 and 128 % wl.group == 0 and wl.page_size % 16 == 0:
+        assert hd["kernel"] == 4
     else:
         assert hd["kernel"] == (1 if rows <= 64 else 2)
 
