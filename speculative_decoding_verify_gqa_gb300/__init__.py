@@ -186,7 +186,8 @@ class Plan:
                     tile_keys=int(ints[13]), n_items=int(ints[14]), n_merge=int(ints[15]),
                     n_units=int(ints[16]), num_sms=int(ints[17]), total_qo=int(i64[0]),
                     part_rows=int(i64[1]), chunk=int(i64[2]),
-                    cluster=int(np.frombuffer(h[152:160].tobytes(), dtype=np.int64)[0]))
+                    cluster=int(np.frombuffer(h[152:160].tobytes(), dtype=np.int64)[0]),
+                    n_ctas=int(np.frombuffer(h[160:168].tobytes(), dtype=np.int64)[0]))
 
     def launches(self) -> int:
         n = ctypes.c_int(0)
@@ -196,7 +197,7 @@ class Plan:
 
     def items(self) -> np.ndarray:
         """The work list as an [n_items, 8] int32 array (b, h, row0, nrows,
-        kv_lo, kv_hi, part_row, pad)."""
+        kv_lo, kv_hi, part_row, next)."""
         hd = self.header()
         raw = self.host[184:184 + 32 * hd["n_items"]].tobytes()
         return np.frombuffer(raw, dtype=np.int32).reshape(-1, 8)

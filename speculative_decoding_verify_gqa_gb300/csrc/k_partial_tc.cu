@@ -1,5 +1,6 @@
 // Split-KV verify attention on the 5th-generation tensor cores (tcgen05, TMEM
-// accumulators, TMA page gather) for blocks of one or two 128-row Q tiles.
+// accumulators, TMA page gather) for blocks of one or two 128-row Q tiles,
+// one persistent CTA per SM.
 //
 // Same algorithm as the warp-level variant ("flashmap 0.1.0 --
 // flashmap/sglang/verify_attention.py", partial kernel: one CTA per request,
@@ -60,13 +61,13 @@ struct TcCfg {
   static constexpr int RAW_BYTES = KEYS * D;             // fp8 K (or V) tile [keys][128 B]
   static constexpr int SLOT_BYTES = FP8 ? RAW_BYTES : OP_BYTES;
   static constexpr int CONV_BYTES = FP8 ? 3 * OP_BYTES : 0;  // widened K (two) and V (one)
-  static constexpr int RING_AVAIL = 227 * 1024 - 256 - Q_BYTES - CONV_BYTES;
+  static constexpr int RING_AVAIL = 227 * 1024 - 512 - Q_BYTES - CONV_BYTES;
   static constexpr int NSLOT = RING_AVAIL / SLOT_BYTES > 8 ? 8 : RING_AVAIL / SLOT_BYTES;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_CONV = OFF_Q + Q_BYTES;
   static constexpr int OFF_RING = OFF_CONV + CONV_BYTES;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * SLOT_BYTES;
-  static constexpr int SMEM = OFF_BAR + 256;              // + barriers, TMEM address, abort flag
+  static constexpr int SMEM = OFF_BAR + 512;              // + barriers, TMEM address, abort flag
   static constexpr uint32_t QT_COLS = 256;               // per Q tile: S / P (128) | O (128)
   static constexpr uint32_t COL_O = 128;
   static constexpr uint32_t TMEM_COLS = NQ * QT_COLS;
@@ -78,9 +79,10 @@ struct TcCfg {
 constexpr float kLn2 = 0.6931471805599453f;
 
 // barrier slots (per-Q-tile barriers at base + qt)
-enum { B_Q = 0, B_Q_READY = 1, B_FULL = 2, B_EMPTY = 10, B_CK_FULL = 18, B_CK_FREE = 20,
-       B_CV_FULL = 22, B_CV_FREE = 23, B_S_FULL = 24, B_P_FULL = 26, B_O_DONE = 28, B_COUNT = 30 };
-static_assert(8 * B_COUNT + 8 <= 256, "barrier area");
+enum { B_Q = 0, B_Q_READY = 1, B_Q_FREE = 2, B_FULL = 3, B_EMPTY = 11, B_CK_FULL = 19,
+       B_CK_FREE = 21, B_CV_FULL = 23, B_CV_FREE = 24, B_S_FULL = 25, B_P_FULL = 27, B_O_DONE = 29,
+       B_O_FREE = 31, B_COUNT = 33 };
+static_assert(8 * B_COUNT + 8 <= 512, "barrier area");
 
 // Instruction descriptor, kind::f16 with f16 A and B (fp32 accumulator).
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
@@ -110,6 +112,45 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return m;
 }
 
+// One work item's geometry, as every role of the CTA decodes it.
+struct ItemGeo {
+  int b, h, row0, nrows, lo, hi, part_row, qo0, L, pg0, prefix, n_tiles, nq;
+  bool ok;
+};
+
+template <int BLOCK_ROWS, int ROWS, int KEYS>
+__device__ __forceinline__ ItemGeo decode_item(const PartialParams& p, int i) {
+  const WorkItem it = p.items[i];
+  ItemGeo g;
+  g.b = it.b;
+  g.h = it.h;
+  g.row0 = it.row0;
+  g.nrows = it.nrows;
+  g.lo = it.kv_lo;
+  g.hi = it.kv_hi;
+  g.part_row = it.part_row;
+  g.qo0 = p.qo_indptr[g.b];
+  g.L = p.qo_indptr[g.b + 1] - g.qo0;
+  g.pg0 = p.kv_indptr[g.b];
+  const int npg = p.kv_indptr[g.b + 1] - g.pg0;
+  const int lpl = npg > 0 ? p.last_page_len[g.b] : 1;
+  const long long kv_len = npg > 0 ? (long long)(npg - 1) * p.page_size + lpl : 0;
+  g.prefix = (int)kv_len - g.L;
+  g.ok = g.L >= 0 && npg >= 0 && lpl >= 1 && lpl <= p.page_size && kv_len <= 0x7fffffffLL &&
+         g.prefix >= 0 && g.row0 >= 0 && g.nrows > 0 && g.nrows <= BLOCK_ROWS &&
+         g.row0 % BLOCK_ROWS == 0 && (long long)g.row0 + g.nrows <= (long long)p.group * g.L &&
+         g.lo >= 0 && g.lo % 16 == 0 && g.lo < g.hi && g.hi <= kv_len;
+  g.n_tiles = g.ok ? (g.hi - g.lo + KEYS - 1) / KEYS : 0;
+  g.nq = (g.nrows + ROWS - 1) / ROWS;  // live Q tiles (1 .. NQ)
+  return g;
+}
+
+// Persistent: one CTA per SM walks its chain of work items (dealt by the
+// planner longest-first onto the least-loaded CTA), and every role streams
+// from one item into the next.  The producer loads item k + 1's Q as soon as
+// item k's last S MMA has read Q, and its keys into the same slot ring; the
+// MMA issuer starts item k + 1's S MMAs while the softmax warps still write
+// item k's output, and its first PV once that output has left O.
 template <bool FP8, int NQ>
 __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     verify_partial_tc_kernel(const PartialParams p, const __grid_constant__ TcMaps maps) {
@@ -126,34 +167,24 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 8 * B_COUNT + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  grid_dependency_wait();
-  const WorkItem it = p.items[blockIdx.x];
-  const int b = it.b, h = it.h, G = p.group;
-  const int qo0 = p.qo_indptr[b];
-  const int L = p.qo_indptr[b + 1] - qo0;
-  const int pg0 = p.kv_indptr[b];
-  const int npg = p.kv_indptr[b + 1] - pg0;
-  const int lpl = npg > 0 ? p.last_page_len[b] : 1;
-  const long long kv_len_ll = npg > 0 ? (long long)(npg - 1) * p.page_size + lpl : 0;
-  const int kv_len = (int)kv_len_ll;
-  const int prefix = kv_len - L;
-  const bool ok = L >= 0 && npg >= 0 && lpl >= 1 && lpl <= p.page_size && prefix >= 0 &&
-                  it.row0 >= 0 && it.nrows > 0 && it.nrows <= C::BLOCK_ROWS &&
-                  it.row0 % C::BLOCK_ROWS == 0 &&
-                  (long long)it.row0 + it.nrows <= (long long)G * L && it.kv_lo >= 0 &&
-                  it.kv_lo % 16 == 0 && it.kv_lo < it.kv_hi && it.kv_hi <= kv_len &&
-                  kv_len_ll <= 0x7fffffffLL;
-  if (!ok) {
-    if (tid == 0) atomicOr(p.status, VA_DEV_BAD_TABLE);
-    return;
-  }
-  const int nrows = it.nrows, row0 = it.row0, lo = it.kv_lo, hi = it.kv_hi;
-  const int n_tiles = (hi - lo + C::KEYS - 1) / C::KEYS;
-  const int nq = (nrows + C::ROWS - 1) / C::ROWS;  // live Q tiles (1 .. NQ)
+  const int G = p.group;
+  // This CTA's items: chain blockIdx.x (then blockIdx.x + gridDim.x, ... if
+  // the grid is smaller than the plan's chain count), linked through next; a
+  // malformed link ends its chain.
+  auto first_item = [&](int slot) -> int { return slot < p.n_ctas && slot < p.n_items ? slot : -1; };
+  auto next_item = [&](int i, int& slot, int& steps) -> int {
+    int n = p.items[i].next;
+    if (++steps > p.n_items || n >= p.n_items) n = -1;
+    if (n >= 0) return n;
+    slot += (int)gridDim.x;
+    return first_item(slot);
+  };
+  auto decode = [&](int i) { return decode_item<C::BLOCK_ROWS, C::ROWS, C::KEYS>(p, i); };
 
   if (tid == 0) {
     mbar_init(bar(B_Q), 1);
-    mbar_init(bar(B_Q_READY), 4 * nq);
+    mbar_init(bar(B_Q_READY), 4 * NQ);
+    mbar_init(bar(B_Q_FREE), 1);
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(bar(B_FULL + s), 1);
       mbar_init(bar(B_EMPTY + s), FP8 ? C::CONV_WARPS : 1);
@@ -168,6 +199,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       mbar_init(bar(B_S_FULL + qt), 1);
       mbar_init(bar(B_P_FULL + qt), 4);
       mbar_init(bar(B_O_DONE + qt), 1);
+      mbar_init(bar(B_O_FREE + qt), 4);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -176,71 +208,87 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Inputs (pages appended by the previous kernel, q, tables) may come from
+  // the grid before this one in the stream.
+  grid_dependency_wait();
 
-  // Operand u = 2 j (K_j) or 2 j + 1 (V_j) sits in ring slot u % NSLOT, on its
-  // (u / NSLOT)-th use of that slot.
+  // Operand u = 2 j (K_j) or 2 j + 1 (V_j) of the CTA's running tile count j
+  // sits in ring slot u % NSLOT, on its (u / NSLOT)-th use of that slot.
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      mbar_expect_tx(bar(B_Q), nq * C::QT_BYTES);
-      const int tok0 = qo0 + row0 / G;
-      for (int qt = 0; qt < nq; ++qt)
-        for (int half = 0; half < 2; ++half)
-          tma_load_3d(sbase + C::OFF_Q + qt * C::QT_BYTES + half * (C::QT_BYTES / 2), &maps.q,
-                      half * 64, h * G, tok0 + qt * (C::ROWS / G), bar(B_Q));
-      int bad = 0;
-      // Page ids of a tile's 16-key boxes (-1 past the chunk), loaded one tile
-      // ahead so their latency hides behind the previous tile's wait.
-      constexpr int NG = C::KEYS / 16;
-      int cur[NG], nxt[NG];
-      auto load_pages = [&](int j, int* pg) {
-        const int k0 = lo + j * C::KEYS;
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          const int key = k0 + 16 * g;
-          pg[g] = (j < n_tiles && key < hi) ? __ldg(p.kv_indices + pg0 + (key >> p.log2_page)) : -1;
-        }
-      };
-      load_pages(0, cur);
+      int bad = 0, bad_item = 0, nit = 0;
+      int u = 0;
       bool live = true;
-      for (int j = 0; live && j < n_tiles; ++j) {
-        load_pages(j + 1, nxt);
-        const int k0 = lo + j * C::KEYS;
-        for (int v = 0; v < 2; ++v) {
-          const int u = 2 * j + v, s = u % C::NSLOT, n = u / C::NSLOT;
-          if (n >= 1 && !mbar_wait(bar(B_EMPTY + s), (n - 1) & 1, abort_flag)) {
-            live = false;
-            break;
-          }
-          mbar_expect_tx(bar(B_FULL + s), C::SLOT_BYTES);
-          const uint32_t dst = sbase + C::OFF_RING + s * C::SLOT_BYTES;
-          const void* map = v ? static_cast<const void*>(&maps.v) : static_cast<const void*>(&maps.k);
+      constexpr int NG = C::KEYS / 16;
+      int slot = blockIdx.x, steps = 0;
+      for (int i = first_item(slot); live && i >= 0; i = next_item(i, slot, steps)) {
+        const ItemGeo g = decode(i);
+        if (!g.ok) {
+          bad_item = 1;
+          continue;
+        }
+        // Q of this item once the previous item's S MMAs are done with Q
+        if (nit >= 1 && !mbar_wait(bar(B_Q_FREE), (nit - 1) & 1, abort_flag)) break;
+        mbar_expect_tx(bar(B_Q), g.nq * C::QT_BYTES);
+        const int tok0 = g.qo0 + g.row0 / G;
+        for (int qt = 0; qt < g.nq; ++qt)
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(sbase + C::OFF_Q + qt * C::QT_BYTES + half * (C::QT_BYTES / 2), &maps.q,
+                        half * 64, g.h * G, tok0 + qt * (C::ROWS / G), bar(B_Q));
+        // Page ids of a tile's 16-key boxes (-1 past the chunk), loaded one
+        // tile ahead so their latency hides behind the previous tile's wait.
+        int cur[NG], nxt[NG];
+        auto load_pages = [&](int j, int* pg) {
+          const int k0 = g.lo + j * C::KEYS;
 #pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            const int key = k0 + 16 * g;
-            int page = p.num_pages;  // outside the pool: zero fill
-            int slot = 0;
-            if (key < hi) {
-              const int pid = cur[g];
-              if ((unsigned)pid < (unsigned)p.num_pages) {
-                page = pid;
-                slot = key & (p.page_size - 1);
+          for (int q = 0; q < NG; ++q) {
+            const int key = k0 + 16 * q;
+            pg[q] = (j < g.n_tiles && key < g.hi) ? __ldg(p.kv_indices + g.pg0 + (key >> p.log2_page)) : -1;
+          }
+        };
+        load_pages(0, cur);
+        for (int j = 0; live && j < g.n_tiles; ++j) {
+          load_pages(j + 1, nxt);
+          const int k0 = g.lo + j * C::KEYS;
+          for (int v = 0; v < 2; ++v, ++u) {
+            const int s = u % C::NSLOT, n = u / C::NSLOT;
+            if (n >= 1 && !mbar_wait(bar(B_EMPTY + s), (n - 1) & 1, abort_flag)) {
+              live = false;
+              break;
+            }
+            mbar_expect_tx(bar(B_FULL + s), C::SLOT_BYTES);
+            const uint32_t dst = sbase + C::OFF_RING + s * C::SLOT_BYTES;
+            const void* map = v ? static_cast<const void*>(&maps.v) : static_cast<const void*>(&maps.k);
+#pragma unroll
+            for (int q = 0; q < NG; ++q) {
+              const int key = k0 + 16 * q;
+              int page = p.num_pages;  // outside the pool: zero fill
+              int slot = 0;
+              if (key < g.hi) {
+                const int pid = cur[q];
+                if ((unsigned)pid < (unsigned)p.num_pages) {
+                  page = pid;
+                  slot = key & (p.page_size - 1);
+                } else {
+                  bad = 1;
+                }
+              }
+              if constexpr (FP8) {
+                tma_load_4d(dst + q * 2048, map, 0, slot, g.h, page, bar(B_FULL + s));
               } else {
-                bad = 1;
+                tma_load_4d(dst + q * 2048, map, 0, slot, g.h, page, bar(B_FULL + s));
+                tma_load_4d(dst + C::KEYS * 128 + q * 2048, map, 64, slot, g.h, page, bar(B_FULL + s));
               }
             }
-            if constexpr (FP8) {
-              tma_load_4d(dst + g * 2048, map, 0, slot, h, page, bar(B_FULL + s));
-            } else {
-              tma_load_4d(dst + g * 2048, map, 0, slot, h, page, bar(B_FULL + s));
-              tma_load_4d(dst + C::KEYS * 128 + g * 2048, map, 64, slot, h, page, bar(B_FULL + s));
-            }
           }
-        }
 #pragma unroll
-        for (int g = 0; g < NG; ++g) cur[g] = nxt[g];
+          for (int q = 0; q < NG; ++q) cur[q] = nxt[q];
+        }
+        ++nit;
       }
       if (bad) atomicOr(p.status, VA_DEV_BAD_PAGE);
+      if (bad_item) atomicOr(p.status, VA_DEV_BAD_TABLE);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -248,79 +296,107 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       constexpr uint32_t id_s = FP8 ? idesc_f16(C::ROWS, C::KEYS, false)
                                     : idesc_bf16(C::ROWS, C::KEYS, false);
       constexpr uint32_t id_o = FP8 ? idesc_f16(C::ROWS, C::D, true) : idesc_bf16(C::ROWS, C::D, true);
+      // running counts: ring operands (u0), tiles (t0), items (nit); per Q tile
+      // the S tiles issued (ns) and items completed (no)
+      int u0 = 0, t0 = 0, nit = 0;
+      int ns[NQ], no[NQ];
+#pragma unroll
+      for (int qt = 0; qt < NQ; ++qt) ns[qt] = no[qt] = 0;
       auto k_addr = [&](int j) {
-        return FP8 ? sbase + C::OFF_CONV + (j & 1) * C::OP_BYTES
-                   : sbase + C::OFF_RING + ((2 * j) % C::NSLOT) * C::SLOT_BYTES;
+        return FP8 ? sbase + C::OFF_CONV + ((t0 + j) & 1) * C::OP_BYTES
+                   : sbase + C::OFF_RING + ((u0 + 2 * j) % C::NSLOT) * C::SLOT_BYTES;
       };
       auto v_addr = [&](int j) {
         return FP8 ? sbase + C::OFF_CONV + 2 * C::OP_BYTES
-                   : sbase + C::OFF_RING + ((2 * j + 1) % C::NSLOT) * C::SLOT_BYTES;
+                   : sbase + C::OFF_RING + ((u0 + 2 * j + 1) % C::NSLOT) * C::SLOT_BYTES;
       };
       auto wait_k = [&](int j) {
-        if (FP8) return mbar_wait(bar(B_CK_FULL + (j & 1)), (j >> 1) & 1, abort_flag);
-        const int u = 2 * j;
+        if (FP8) return mbar_wait(bar(B_CK_FULL + ((t0 + j) & 1)), ((t0 + j) >> 1) & 1, abort_flag);
+        const int u = u0 + 2 * j;
         return mbar_wait(bar(B_FULL + u % C::NSLOT), (u / C::NSLOT) & 1, abort_flag);
       };
       auto wait_v = [&](int j) {
-        if (FP8) return mbar_wait(bar(B_CV_FULL), j & 1, abort_flag);
-        const int u = 2 * j + 1;
+        if (FP8) return mbar_wait(bar(B_CV_FULL), (t0 + j) & 1, abort_flag);
+        const int u = u0 + 2 * j + 1;
         return mbar_wait(bar(B_FULL + u % C::NSLOT), (u / C::NSLOT) & 1, abort_flag);
       };
       auto k_free_bar = [&](int j) {
-        return FP8 ? bar(B_CK_FREE + (j & 1)) : bar(B_EMPTY + (2 * j) % C::NSLOT);
+        return FP8 ? bar(B_CK_FREE + ((t0 + j) & 1)) : bar(B_EMPTY + (u0 + 2 * j) % C::NSLOT);
       };
       auto v_free_bar = [&](int j) {
-        return FP8 ? bar(B_CV_FREE) : bar(B_EMPTY + (2 * j + 1) % C::NSLOT);
+        return FP8 ? bar(B_CV_FREE) : bar(B_EMPTY + (u0 + 2 * j + 1) % C::NSLOT);
       };
       // The issue loop is this thread's critical path: descriptors are built
       // once per operand and advanced by adding byte offsets >> 4 to their
       // start-address field (every operand lies below 256 KB: no carry).
       const uint64_t dq0 = smem_desc_sw128(sbase + C::OFF_Q, 16, 1024);
-      bool live = mbar_wait(bar(FP8 ? B_Q_READY : B_Q), 0, abort_flag);
-      for (int j = 0; live && j <= n_tiles; ++j) {
-        // step j: PV of tile j - 1 and S of tile j, Q tile by Q tile
-        if (j < n_tiles && !wait_k(j)) break;
-        if (j >= 1 && !wait_v(j - 1)) break;
-        const uint64_t dk = j < n_tiles ? smem_desc_sw128(k_addr(j), 16, 1024) : 0;
-        const uint64_t dv = j >= 1 ? smem_desc_sw128(v_addr(j - 1), C::KEYS * 128, 1024) : 0;
+      bool live = true;
+      int slot = blockIdx.x, steps = 0;
+      for (int i = first_item(slot); live && i >= 0; i = next_item(i, slot, steps)) {
+        const ItemGeo g = decode(i);
+        if (!g.ok) continue;
+        if (!mbar_wait(bar(FP8 ? B_Q_READY : B_Q), nit & 1, abort_flag)) break;
+        for (int j = 0; live && j <= g.n_tiles; ++j) {
+          // step j: PV of tile j - 1 and S of tile j, Q tile by Q tile
+          if (j < g.n_tiles && !wait_k(j)) { live = false; break; }
+          if (j >= 1 && !wait_v(j - 1)) { live = false; break; }
+          const uint64_t dk = j < g.n_tiles ? smem_desc_sw128(k_addr(j), 16, 1024) : 0;
+          const uint64_t dv = j >= 1 ? smem_desc_sw128(v_addr(j - 1), C::KEYS * 128, 1024) : 0;
 #pragma unroll
-        for (int qt = 0; qt < NQ; ++qt) {
-          if (qt >= nq) break;
-          const uint32_t ts = tmem + qt * C::QT_COLS;  // S_qt / P_qt columns
-          if (j >= 1) {
-            if (!mbar_wait(bar(B_P_FULL + qt), (j - 1) & 1, abort_flag)) {
-              live = false;
-              break;
+          for (int qt = 0; qt < NQ; ++qt) {
+            if (qt >= g.nq) break;
+            const uint32_t ts = tmem + qt * C::QT_COLS;  // S_qt / P_qt columns
+            if (j >= 1) {
+              // the first PV of an item overwrites O: the previous item's
+              // epilogue must have read it out
+              if (j == 1 && no[qt] >= 1 &&
+                  !mbar_wait(bar(B_O_FREE + qt), (no[qt] - 1) & 1, abort_flag)) {
+                live = false;
+                break;
+              }
+              if (!mbar_wait(bar(B_P_FULL + qt), (ns[qt] - 1) & 1, abort_flag)) {
+                live = false;
+                break;
+              }
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < C::KEYS / 16; ++kk)
+                umma_ts(ts + C::COL_O, ts + p_col(kk), dv + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                        (j > 1 || kk > 0) ? 1u : 0u);
+              if (j == g.n_tiles) umma_commit(bar(B_O_DONE + qt));
             }
-            tc_fence_after();
+            if (j < g.n_tiles) {
+              const uint64_t dq = dq0 + (uint64_t)(qt * (C::QT_BYTES >> 4));
 #pragma unroll
-            for (int kk = 0; kk < C::KEYS / 16; ++kk)
-              umma_ts(ts + C::COL_O, ts + p_col(kk), dv + (uint64_t)((kk * 16 * 128) >> 4), id_o,
-                      (j > 1 || kk > 0) ? 1u : 0u);
-            if (j == n_tiles) umma_commit(bar(B_O_DONE + qt));
+              for (int kk = 0; kk < C::D / 16; ++kk)
+                umma_bf16(ts, dq + (uint64_t)((((kk >> 2) * (C::ROWS * 128)) + (kk & 3) * 32) >> 4),
+                          dk + (uint64_t)((((kk >> 2) * (C::KEYS * 128)) + (kk & 3) * 32) >> 4), id_s,
+                          kk > 0 ? 1u : 0u);
+              umma_commit(bar(B_S_FULL + qt));
+              ++ns[qt];
+            }
           }
-          if (j < n_tiles) {
-            const uint64_t dq = dq0 + (uint64_t)(qt * (C::QT_BYTES >> 4));
-#pragma unroll
-            for (int kk = 0; kk < C::D / 16; ++kk)
-              umma_bf16(ts, dq + (uint64_t)((((kk >> 2) * (C::ROWS * 128)) + (kk & 3) * 32) >> 4),
-                        dk + (uint64_t)((((kk >> 2) * (C::KEYS * 128)) + (kk & 3) * 32) >> 4), id_s,
-                        kk > 0 ? 1u : 0u);
-            umma_commit(bar(B_S_FULL + qt));
-          }
+          if (!live) break;
+          if (j == g.n_tiles - 1) umma_commit(bar(B_Q_FREE));  // Q read by this item's last S
+          if (j >= 1) umma_commit(v_free_bar(j - 1));
+          if (j < g.n_tiles) umma_commit(k_free_bar(j));
         }
         if (!live) break;
-        if (j >= 1) umma_commit(v_free_bar(j - 1));
-        if (j < n_tiles) umma_commit(k_free_bar(j));
+#pragma unroll
+        for (int qt = 0; qt < NQ; ++qt)
+          if (qt < g.nq) ++no[qt];
+        u0 += 2 * g.n_tiles;
+        t0 += g.n_tiles;
+        ++nit;
       }
       // the last slot releases land before the CTA's shared memory goes away
-      if (live && !*abort_flag && n_tiles >= 1) {
-        const int j = n_tiles - 1;
+      if (live && !*abort_flag && t0 >= 1) {
+        const int jt = t0 - 1;  // the CTA's last tile (running count)
         if (FP8) {
-          mbar_wait(bar(B_CV_FREE), j & 1, abort_flag);
-          mbar_wait(bar(B_CK_FREE + (j & 1)), (j >> 1) & 1, abort_flag);
+          mbar_wait(bar(B_CV_FREE), jt & 1, abort_flag);
+          mbar_wait(bar(B_CK_FREE + (jt & 1)), (jt >> 1) & 1, abort_flag);
         } else {
-          const int uk = 2 * j, uv = 2 * j + 1;
+          const int uk = 2 * jt, uv = 2 * jt + 1;
           mbar_wait(bar(B_EMPTY + uv % C::NSLOT), (uv / C::NSLOT) & 1, abort_flag);
           mbar_wait(bar(B_EMPTY + uk % C::NSLOT), (uk / C::NSLOT) & 1, abort_flag);
         }
@@ -328,287 +404,291 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     }
   } else if (FP8 && warp >= C::CONV_WARP0) {
     // ---------------- fp8 -> scaled f16 widening ----------------
-    // Step i widens K_i, then V_{i-1}: K runs a tile ahead, since S_i needs
-    // only K_i while V's single buffer frees up one PV later.
+    // Step i of an item widens K_i, then V_{i-1}: K runs a tile ahead, since
+    // S_i needs only K_i while V's single buffer frees up one PV later.
     const int ct = tid - 32 * C::CONV_WARP0;            // 0 .. 127
     constexpr int NCT = 32 * C::CONV_WARPS;
-    for (int i = 0; i <= n_tiles; ++i) {
-      bool go = true;
-      for (int v = 0; v < 2; ++v) {
-        const int j = i - v;                            // tile of this operand
-        if (j < 0 || j >= n_tiles) continue;
-        const int u = 2 * j + v, s = u % C::NSLOT, n = u / C::NSLOT;
-        if (!mbar_wait(bar(B_FULL + s), n & 1, abort_flag)) { go = false; break; }
-        if (v == 0 && j >= 2 && !mbar_wait(bar(B_CK_FREE + (j & 1)), ((j >> 1) - 1) & 1, abort_flag)) {
-          go = false;
-          break;
-        }
-        if (v == 1 && j >= 1 && !mbar_wait(bar(B_CV_FREE), (j - 1) & 1, abort_flag)) {
-          go = false;
-          break;
-        }
-        const int k0 = lo + j * C::KEYS;
-        const uint8_t* raw = smem + C::OFF_RING + s * C::SLOT_BYTES;
-        uint8_t* dst = smem + C::OFF_CONV + (v ? 2 : (j & 1)) * C::OP_BYTES;
-#pragma unroll 4
-        for (int c = ct; c < C::KEYS * 8; c += NCT) {
-          const int r = c >> 3, ch = c & 7;         // key row, 16-code group
-          uint4 a = make_uint4(0u, 0u, 0u, 0u), bq = a;
-          if (k0 + r < hi) {
-            const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + ch * 16);
-            a.x = e4m3x2_scaled_f16x2(__byte_perm(w.x, 0u, 0x4140));
-            a.y = e4m3x2_scaled_f16x2(__byte_perm(w.x, 0u, 0x4342));
-            a.z = e4m3x2_scaled_f16x2(__byte_perm(w.y, 0u, 0x4140));
-            a.w = e4m3x2_scaled_f16x2(__byte_perm(w.y, 0u, 0x4342));
-            bq.x = e4m3x2_scaled_f16x2(__byte_perm(w.z, 0u, 0x4140));
-            bq.y = e4m3x2_scaled_f16x2(__byte_perm(w.z, 0u, 0x4342));
-            bq.z = e4m3x2_scaled_f16x2(__byte_perm(w.w, 0u, 0x4140));
-            bq.w = e4m3x2_scaled_f16x2(__byte_perm(w.w, 0u, 0x4342));
+    int u0 = 0, t0 = 0;
+    bool go = true;
+    int slot = blockIdx.x, steps = 0;
+    for (int it_i = first_item(slot); go && it_i >= 0; it_i = next_item(it_i, slot, steps)) {
+      const ItemGeo g = decode(it_i);
+      if (!g.ok) continue;
+      for (int i = 0; go && i <= g.n_tiles; ++i) {
+        for (int v = 0; v < 2; ++v) {
+          const int j = i - v;                            // tile of this operand
+          if (j < 0 || j >= g.n_tiles) continue;
+          const int u = u0 + 2 * j + v, s = u % C::NSLOT, n = u / C::NSLOT;
+          const int tj = t0 + j;                          // running tile count
+          if (!mbar_wait(bar(B_FULL + s), n & 1, abort_flag)) { go = false; break; }
+          if (v == 0 && tj >= 2 && !mbar_wait(bar(B_CK_FREE + (tj & 1)), ((tj >> 1) - 1) & 1, abort_flag)) {
+            go = false;
+            break;
           }
-          // 16 f16 = 2 chunks of the swizzled operand row (half = ch / 4)
-          uint8_t* row = dst + (ch >> 2) * (C::KEYS * 128) + r * 128;
-          const int c0 = (ch & 3) * 2;
-          *reinterpret_cast<uint4*>(row + (((c0) ^ (r & 7)) << 4)) = a;
-          *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = bq;
-        }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(v ? B_CV_FULL : B_CK_FULL + (j & 1)));
-          mbar_arrive(bar(B_EMPTY + s));
+          if (v == 1 && tj >= 1 && !mbar_wait(bar(B_CV_FREE), (tj - 1) & 1, abort_flag)) {
+            go = false;
+            break;
+          }
+          const int k0 = g.lo + j * C::KEYS;
+          const uint8_t* raw = smem + C::OFF_RING + s * C::SLOT_BYTES;
+          uint8_t* dst = smem + C::OFF_CONV + (v ? 2 : (tj & 1)) * C::OP_BYTES;
+#pragma unroll 4
+          for (int c = ct; c < C::KEYS * 8; c += NCT) {
+            const int r = c >> 3, ch = c & 7;         // key row, 16-code group
+            uint4 a = make_uint4(0u, 0u, 0u, 0u), bq = a;
+            if (k0 + r < g.hi) {
+              const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + ch * 16);
+              a.x = e4m3x2_scaled_f16x2(__byte_perm(w.x, 0u, 0x4140));
+              a.y = e4m3x2_scaled_f16x2(__byte_perm(w.x, 0u, 0x4342));
+              a.z = e4m3x2_scaled_f16x2(__byte_perm(w.y, 0u, 0x4140));
+              a.w = e4m3x2_scaled_f16x2(__byte_perm(w.y, 0u, 0x4342));
+              bq.x = e4m3x2_scaled_f16x2(__byte_perm(w.z, 0u, 0x4140));
+              bq.y = e4m3x2_scaled_f16x2(__byte_perm(w.z, 0u, 0x4342));
+              bq.z = e4m3x2_scaled_f16x2(__byte_perm(w.w, 0u, 0x4140));
+              bq.w = e4m3x2_scaled_f16x2(__byte_perm(w.w, 0u, 0x4342));
+            }
+            // 16 f16 = 2 chunks of the swizzled operand row (half = ch / 4)
+            uint8_t* row = dst + (ch >> 2) * (C::KEYS * 128) + r * 128;
+            const int c0 = (ch & 3) * 2;
+            *reinterpret_cast<uint4*>(row + (((c0) ^ (r & 7)) << 4)) = a;
+            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = bq;
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bar(v ? B_CV_FULL : B_CK_FULL + (tj & 1)));
+            mbar_arrive(bar(B_EMPTY + s));
+          }
         }
       }
-      if (!go) break;
+      u0 += 2 * g.n_tiles;
+      t0 += g.n_tiles;
     }
-  } else if (warp >= 4 && warp < 4 + 4 * NQ && (warp - 4) / 4 < nq) {
+  } else if (warp >= 4 && warp < 4 + 4 * NQ) {
     // ---------------- softmax / epilogue: one thread per row, 4 warps per Q tile ----------------
     const int qt = (warp - 4) >> 2;                 // Q tile of this warpgroup
     const int quad = warp & 3;                      // TMEM lane quarter this warp may access
     const int r = quad * 32 + lane;                 // row of the Q tile = TMEM lane
-    const int br = qt * C::ROWS + r;                // row of the block
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16) + qt * C::QT_COLS;
-    const bool row_ok = br < nrows;
-    const int t = (row0 + br) / G;                  // draft token of the row
-    const int moff = p.mask ? p.mask_indptr[b] : 0;
     // fp8 operands hold the codes' values times 2^-8 (see e4m3x2_scaled_f16x2)
     const float c = FP8 ? p.scale_log2 * 256.f : p.scale_log2;
     const uint32_t b_s_full = bar(B_S_FULL + qt), b_p_full = bar(B_P_FULL + qt);
-    float m_used = -INFINITY;                       // in units of s * c (log2 domain)
-    float l = 0.f;
+    int ns = 0, no = 0, nit = 0, u0 = 0;            // S tiles seen, items done, items, ring base
     bool live = true;
-    if (FP8) {
-      // Q to f16, in place (each thread its own row)
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, abort_flag))) live = false;
-      if (live) {
+    int slot = blockIdx.x, steps = 0;
+    for (int it_i = first_item(slot); live && it_i >= 0; it_i = next_item(it_i, slot, steps)) {
+      const ItemGeo g = decode(it_i);
+      if (!g.ok) continue;
+      const bool mine = qt < g.nq;
+      if (FP8) {
+        // Q to f16, in place (each thread its own row); a Q tile the item
+        // does not use still counts its arrival
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q), nit & 1, abort_flag))) { live = false; break; }
+        if (mine) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint4* q4 = reinterpret_cast<uint4*>(smem + C::OFF_Q + qt * C::QT_BYTES +
-                                               half * (C::QT_BYTES / 2) + r * 128);
+          for (int half = 0; half < 2; ++half) {
+            uint4* q4 = reinterpret_cast<uint4*>(smem + C::OFF_Q + qt * C::QT_BYTES +
+                                                 half * (C::QT_BYTES / 2) + r * 128);
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            uint4 v = q4[ch];
-            v.x = bf16x2_to_f16x2(v.x);
-            v.y = bf16x2_to_f16x2(v.y);
-            v.z = bf16x2_to_f16x2(v.z);
-            v.w = bf16x2_to_f16x2(v.w);
-            q4[ch] = v;
-          }
-        }
-        fence_proxy_async();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_Q_READY));
-    }
-    for (int j = 0; live && j < n_tiles; ++j) {
-      const int k0 = lo + j * C::KEYS;
-      if constexpr (!FP8) {
-        // Rows of V_j past the chunk end inside the last 16-key box may hold
-        // stale (even NaN) slots: zero them, since 0 * NaN would poison O.
-        // Q tile 0's warps do it before their P_j is posted; PV_j of every Q
-        // tile is issued after that.
-        const int tail = hi - k0;
-        if (qt == 0 && tail < C::KEYS && (tail & 15)) {
-          const int u = 2 * j + 1, s = u % C::NSLOT;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_FULL + s), (u / C::NSLOT) & 1, abort_flag))) {
-            live = false;
-            break;
-          }
-          const int zlo = tail, zhi = (tail + 15) & ~15;
-          uint8_t* vt = smem + C::OFF_RING + s * C::SLOT_BYTES;
-          for (int z = r; z < (zhi - zlo) * 16; z += C::ROWS) {
-            const int row = zlo + z / 16, half = (z / 8) & 1, ch = z & 7;
-            *reinterpret_cast<uint4*>(vt + half * (C::KEYS * 128) + row * 128 + (ch << 4)) =
-                make_uint4(0u, 0u, 0u, 0u);
+            for (int ch = 0; ch < 8; ++ch) {
+              uint4 v = q4[ch];
+              v.x = bf16x2_to_f16x2(v.x);
+              v.y = bf16x2_to_f16x2(v.y);
+              v.z = bf16x2_to_f16x2(v.z);
+              v.w = bf16x2_to_f16x2(v.w);
+              q4[ch] = v;
+            }
           }
           fence_proxy_async();
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_Q_READY));
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(b_s_full, j & 1, abort_flag))) { live = false; break; }
-      tc_fence_after();
-
-      // Visibility of the tile's keys for this row.  Causal drafts: keys below
-      // lim = min(hi, prefix + t + 1) - k0.  Custom mask: one word per 32 keys
-      // (prefix 1, drafts from the row's mask bits, nothing at or past hi).
-      // A tile every row of the warp sees whole skips the per-key selects.
-      const int lim = min(hi, prefix + t + 1) - k0;
-      uint32_t vis[C::KEYS / 32];
-      bool full;
-      if (!p.mask) {
-        full = __all_sync(0xffffffffu, lim >= C::KEYS);
-      } else if (k0 + C::KEYS <= prefix && k0 + C::KEYS <= hi) {
-        full = true;
-      } else {
-        uint32_t all = 0xffffffffu;
-#pragma unroll
-        for (int q = 0; q < C::KEYS / 32; ++q) {
-          const int g0 = k0 + 32 * q;
-          uint32_t w32 = 0;
-          if (g0 < hi) {
-            const int below_prefix = min(max(prefix - g0, 0), 32);
-            w32 = below_prefix == 32 ? 0xffffffffu : ((1u << below_prefix) - 1u);
-            if (below_prefix < 32 && t < L) {
-              // draft columns u = g0 + i - prefix for i >= below_prefix
-              const int u0 = g0 + below_prefix - prefix;
-              const long long bit0 = (long long)moff + (long long)t * L + u0;
-              const int nbits = min(32 - below_prefix, L - u0);
-              if (nbits > 0) {
-                uint64_t w = 0;
-                const int nbytes = (int)((((bit0 & 7) + nbits) + 7) >> 3);
-                for (int k = 0; k < nbytes; ++k)
-                  w |= (uint64_t)__ldg(p.mask + (bit0 >> 3) + k) << (8 * k);
-                w >>= (bit0 & 7);
-                const uint32_t dbits =
-                    (uint32_t)(w & (nbits >= 32 ? 0xffffffffull : ((1ull << nbits) - 1ull)));
-                w32 |= dbits << below_prefix;
-              }
+      ++nit;
+      if (!mine) {
+        u0 += 2 * g.n_tiles;
+        continue;
+      }
+      const int br = qt * C::ROWS + r;              // row of the block
+      const bool row_ok = br < g.nrows;
+      const int t = (g.row0 + br) / G;              // draft token of the row
+      const int moff = p.mask ? p.mask_indptr[g.b] : 0;
+      const int L = g.L, prefix = g.prefix, hi = g.hi;
+      float m_used = -INFINITY;                     // in units of s * c (log2 domain)
+      float l = 0.f;
+      for (int j = 0; live && j < g.n_tiles; ++j) {
+        const int k0 = g.lo + j * C::KEYS;
+        if constexpr (!FP8) {
+          // Rows of V_j past the chunk end inside the last 16-key box may hold
+          // stale (even NaN) slots: zero them, since 0 * NaN would poison O.
+          // Q tile 0's warps do it before their P_j is posted; PV_j of every Q
+          // tile is issued after that.
+          const int tail = hi - k0;
+          if (qt == 0 && tail < C::KEYS && (tail & 15)) {
+            const int u = u0 + 2 * j + 1, s = u % C::NSLOT;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(B_FULL + s), (u / C::NSLOT) & 1, abort_flag))) {
+              live = false;
+              break;
             }
-            const int in_range = min(hi - g0, 32);
-            if (in_range < 32) w32 &= (1u << in_range) - 1u;
+            const int zlo = tail, zhi = (tail + 15) & ~15;
+            uint8_t* vt = smem + C::OFF_RING + s * C::SLOT_BYTES;
+            for (int z = r; z < (zhi - zlo) * 16; z += C::ROWS) {
+              const int row = zlo + z / 16, half = (z / 8) & 1, ch = z & 7;
+              *reinterpret_cast<uint4*>(vt + half * (C::KEYS * 128) + row * 128 + (ch << 4)) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async();
           }
-          vis[q] = w32;
-          all &= w32;
         }
-        full = __all_sync(0xffffffffu, all == 0xffffffffu);
-      }
-      // Keys 32 q .. 32 q + 31 of the tile this row may see, one bit each.
-      auto vis_word = [&](int q) -> uint32_t {
+        if (!__all_sync(0xffffffffu, mbar_wait(b_s_full, ns & 1, abort_flag))) { live = false; break; }
+        ++ns;
+        tc_fence_after();
+        // Visibility of the tile's keys for this row.  Causal drafts: keys below
+        // lim = min(hi, prefix + t + 1) - k0.  Custom mask: one word per 32 keys
+        // (prefix 1, drafts from the row's mask bits, nothing at or past hi).
+        // A tile every row of the warp sees whole skips the per-key selects.
+        const int lim = min(hi, prefix + t + 1) - k0;
+        uint32_t vis[C::KEYS / 32];
+        bool full;
         if (!p.mask) {
-          const int n = lim - 32 * q;
-          return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
-        }
-        return q == 0 ? vis[0] : q == 1 ? vis[1] : q == 2 ? vis[2] : vis[3];
-      };
-      // the row's new reference max from this tile's max (log2 units); O is
-      // idle here (PV_{j-1} of this Q tile completed before S_j did), so a
-      // raised max rescales it at once
-      float alpha = 1.f, base = 0.f;
-      auto new_max = [&](float mx) {
-        mx *= c;  // c > 0
-        float m_new = m_used;
-        if (mx > m_used + 8.f) m_new = mx;   // also taken when m_used = -inf and mx is finite
-        alpha = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
-        base = m_new == -INFINITY ? 0.f : m_new;
-        if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          for (int q = 0; q < C::D / 32; ++q) {
-            uint32_t ov[32];
-            tmem_ld32(lane_addr + C::COL_O + q * 32, ov);
-            tmem_wait_ld();
+          full = __all_sync(0xffffffffu, lim >= C::KEYS);
+        } else if (k0 + C::KEYS <= prefix && k0 + C::KEYS <= hi) {
+          full = true;
+        } else {
+          uint32_t all = 0xffffffffu;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(lane_addr + C::COL_O + q * 32, ov);
+          for (int q = 0; q < C::KEYS / 32; ++q) {
+            const int g0 = k0 + 32 * q;
+            uint32_t w32 = 0;
+            if (g0 < hi) {
+              const int below_prefix = min(max(prefix - g0, 0), 32);
+              w32 = below_prefix == 32 ? 0xffffffffu : ((1u << below_prefix) - 1u);
+              if (below_prefix < 32 && t < L) {
+                // draft columns d = g0 + i - prefix for i >= below_prefix
+                const int d0 = g0 + below_prefix - prefix;
+                const long long bit0 = (long long)moff + (long long)t * L + d0;
+                const int nbits = min(32 - below_prefix, L - d0);
+                if (nbits > 0) {
+                  uint64_t w = 0;
+                  const int nbytes = (int)((((bit0 & 7) + nbits) + 7) >> 3);
+                  for (int k = 0; k < nbytes; ++k)
+                    w |= (uint64_t)__ldg(p.mask + (bit0 >> 3) + k) << (8 * k);
+                  w >>= (bit0 & 7);
+                  const uint32_t dbits =
+                      (uint32_t)(w & (nbits >= 32 ? 0xffffffffull : ((1ull << nbits) - 1ull)));
+                  w32 |= dbits << below_prefix;
+                }
+              }
+              const int in_range = min(hi - g0, 32);
+              if (in_range < 32) w32 &= (1u << in_range) - 1u;
+            }
+            vis[q] = w32;
+            all &= w32;
           }
+          full = __all_sync(0xffffffffu, all == 0xffffffffu);
         }
-        m_used = m_new;
-      };
-      // P of 32 logits (with visibility word vw) into columns 32 q .. 32 q + 15
-      float sums[4] = {0.f, 0.f, 0.f, 0.f};
-      auto exp_chunk = [&](const uint32_t (&raw)[32], int q, uint32_t vw, bool masked) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float s0 = __uint_as_float(raw[2 * i]), s1 = __uint_as_float(raw[2 * i + 1]);
-          if (masked) {
-            s0 = ((vw >> (2 * i)) & 1u) ? s0 : -INFINITY;
-            s1 = ((vw >> (2 * i + 1)) & 1u) ? s1 : -INFINITY;
+        // Keys 32 q .. 32 q + 31 of the tile this row may see, one bit each.
+        auto vis_word = [&](int q) -> uint32_t {
+          if (!p.mask) {
+            const int n = lim - 32 * q;
+            return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
           }
-          const float p0 = ex2(fmaf(s0, c, -base));
-          const float p1 = ex2(fmaf(s1, c, -base));
-          sums[i & 3] += p0 + p1;
-          pk[i] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
-        }
-        tmem_st16(lane_addr + 32 * q, pk);
-      };
-      if (full) {
-        // Every key visible: S read twice as two halves of 64 columns.  The
-        // second half is still in registers after the max, so it is
-        // exponentiated first and the first half read once more.
-        uint32_t ra[32], rb[32];
-        float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          return q == 0 ? vis[0] : q == 1 ? vis[1] : q == 2 ? vis[2] : vis[3];
+        };
+        // the row's new reference max from this tile's max (log2 units); O is
+        // idle here (PV_{j-1} of this Q tile completed before S_j did), so a
+        // raised max rescales it at once
+        float alpha = 1.f, base = 0.f;
+        auto new_max = [&](float mx) {
+          mx *= c;  // c > 0
+          float m_new = m_used;
+          if (mx > m_used + 8.f) m_new = mx;   // also taken when m_used = -inf and mx is finite
+          alpha = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
+          base = m_new == -INFINITY ? 0.f : m_new;
+          if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            for (int q = 0; q < C::D / 32; ++q) {
+              uint32_t ov[32];
+              tmem_ld32(lane_addr + C::COL_O + q * 32, ov);
+              tmem_wait_ld();
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          tmem_ld32(lane_addr + 64 * h2, ra);
-          tmem_ld32(lane_addr + 64 * h2 + 32, rb);
-          tmem_wait_ld();
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              tmem_st32(lane_addr + C::COL_O + q * 32, ov);
+            }
+          }
+          m_used = m_new;
+        };
+        // P of 32 logits (with visibility word vw) into columns 32 q .. 32 q + 15
+        float sums[4] = {0.f, 0.f, 0.f, 0.f};
+        auto exp_chunk = [&](const uint32_t (&raw)[32], int q, uint32_t vw, bool masked) {
+          uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
-            mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+            float s0 = __uint_as_float(raw[2 * i]), s1 = __uint_as_float(raw[2 * i + 1]);
+            if (masked) {
+              s0 = ((vw >> (2 * i)) & 1u) ? s0 : -INFINITY;
+              s1 = ((vw >> (2 * i + 1)) & 1u) ? s1 : -INFINITY;
+            }
+            const float p0 = ex2(fmaf(s0, c, -base));
+            const float p1 = ex2(fmaf(s1, c, -base));
+            sums[i & 3] += p0 + p1;
+            pk[i] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+          }
+          tmem_st16(lane_addr + 32 * q, pk);
+        };
+        // Both passes walk the row 32 logits at a time in rolled loops: a
+        // small loop body keeps every warp's code in the instruction cache.
+        {
+          float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+          for (int q = 0; q < C::KEYS / 32; ++q) {
+            uint32_t raw[32];
+            tmem_ld32(lane_addr + q * 32, raw);
+            tmem_wait_ld();
+            if (full) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
+            } else {
+              const uint32_t vw = vis_word(q);
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                mxs[i & 3] = fmax3(mxs[i & 3], ((vw >> (2 * i)) & 1u) ? __uint_as_float(raw[2 * i]) : -INFINITY,
+                                   ((vw >> (2 * i + 1)) & 1u) ? __uint_as_float(raw[2 * i + 1]) : -INFINITY);
+            }
+          }
+          new_max(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])));
+#pragma unroll 1
+          for (int q = 0; q < C::KEYS / 32; ++q) {
+            uint32_t raw[32];
+            tmem_ld32(lane_addr + q * 32, raw);
+            tmem_wait_ld();
+            exp_chunk(raw, q, full ? 0xffffffffu : vis_word(q), !full);
           }
         }
-        new_max(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])));
-        exp_chunk(ra, 2, 0xffffffffu, false);
-        exp_chunk(rb, 3, 0xffffffffu, false);
-        tmem_ld32(lane_addr, ra);
-        tmem_ld32(lane_addr + 32, rb);
-        tmem_wait_ld();
-        exp_chunk(ra, 0, 0xffffffffu, false);
-        exp_chunk(rb, 1, 0xffffffffu, false);
-      } else {
-        // Some keys hidden: 32 columns at a time in rolled loops (small code).
-        float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-        for (int q = 0; q < C::KEYS / 32; ++q) {
-          uint32_t raw[32];
-          tmem_ld32(lane_addr + q * 32, raw);
-          tmem_wait_ld();
-          const uint32_t vw = vis_word(q);
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            mxs[i & 3] = fmax3(mxs[i & 3], ((vw >> (2 * i)) & 1u) ? __uint_as_float(raw[2 * i]) : -INFINITY,
-                               ((vw >> (2 * i + 1)) & 1u) ? __uint_as_float(raw[2 * i + 1]) : -INFINITY);
-        }
-        new_max(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])));
-#pragma unroll 1
-        for (int q = 0; q < C::KEYS / 32; ++q) {
-          uint32_t raw[32];
-          tmem_ld32(lane_addr + q * 32, raw);
-          tmem_wait_ld();
-          exp_chunk(raw, q, vis_word(q), true);
-        }
+        const float sum = (sums[0] + sums[1]) + (sums[2] + sums[3]);
+        l = l * alpha + sum;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_p_full);
       }
-      const float sum = (sums[0] + sums[1]) + (sums[2] + sums[3]);
-      l = l * alpha + sum;
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_p_full);
-    }
-    // epilogue
-    if (live && __all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE + qt), 0, abort_flag))) {
+      if (!live) break;
+      // epilogue
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE + qt), no & 1, abort_flag))) { live = false; break; }
       tc_fence_after();
       const float lse = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
       const float inv = l > 0.f ? (FP8 ? p.v_scale * 256.f : p.v_scale) / l : 0.f;
       size_t orow = 0;
       if (row_ok) {
-        const int g = (row0 + br) - t * G;
-        orow = (size_t)(qo0 + t) * p.h_q + (size_t)h * G + g;
+        const int gg = (g.row0 + br) - t * G;
+        orow = (size_t)(g.qo0 + t) * p.h_q + (size_t)g.h * G + gg;
       }
       for (int q = 0; q < C::D / 32; ++q) {
         uint32_t ov[32];
         tmem_ld32(lane_addr + C::COL_O + q * 32, ov);
         tmem_wait_ld();
         if (!row_ok) continue;
-        if (it.part_row < 0) {
+        if (g.part_row < 0) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * C::D + q * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -620,7 +700,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
             dst[e] = w;
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(p.part_out + ((size_t)it.part_row + br) * C::D + q * 32);
+          float4* dst = reinterpret_cast<float4*>(p.part_out + ((size_t)g.part_row + br) * C::D + q * 32);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
@@ -628,12 +708,18 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         }
       }
       if (row_ok) {
-        if (it.part_row < 0) {
+        if (g.part_row < 0) {
           if (p.lse) p.lse[orow] = lse;
         } else {
-          p.part_lse[(size_t)it.part_row + br] = lse;
+          p.part_lse[(size_t)g.part_row + br] = lse;
         }
       }
+      // O has been read: the next item's first PV may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_O_FREE + qt));
+      ++no;
+      u0 += 2 * g.n_tiles;
     }
     tc_fence_before();
   }
@@ -655,7 +741,10 @@ cudaError_t launch_tc(const PartialParams& p, const TcMaps& maps, int n_items,
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PartialParams*>(&p), const_cast<TcMaps*>(&maps)};
-  return launch_kernel(reinterpret_cast<const void*>(kern), dim3(n_items), dim3(C::THREADS),
+  // persistent: one CTA per item chain of the plan (one per SM)
+  (void)n_items;
+  if (p.n_ctas <= 0) return cudaSuccess;
+  return launch_kernel(reinterpret_cast<const void*>(kern), dim3(p.n_ctas), dim3(C::THREADS),
                        C::SMEM, stream, args, /*pdl=*/true);
 }
 

@@ -117,6 +117,8 @@ PartialParams make_partial(const void* q, const void* k_cache, const void* v_cac
   p.scale_log2 = sm_scale * k_scale * 1.4426950408889634f;
   p.v_scale = v_scale;
   p.cluster = kernel_is_tc(hd->kernel) ? 0 : (int)hd->cluster;
+  p.n_items = hd->n_items;
+  p.n_ctas = (int)hd->n_ctas;
   return p;
 }
 

@@ -15,8 +15,10 @@ constexpr uint32_t kPlanVersion = 1;
 // cut on multiples of it, so every tile starts on a page boundary whenever
 // page_size <= kTileKeys, and lies inside one page otherwise.
 constexpr int kTileKeys = 64;
-// Key tile of the tcgen05 variants (the MMA's N for S = Q K^T).
+// Key tile of the tcgen05 variants (the MMA's N for S = Q K^T), and the rows
+// of one of their Q tiles.
 constexpr int kTcTileKeys = 128;
+constexpr int kTcRowsPerTile = 128;
 
 // Kernel variants (values match VA_KERNEL_* in verify_attn.h).
 enum Kernel : int32_t {
@@ -36,10 +38,12 @@ inline int kernel_ctas_per_sm(int k) { return k == kKernelMma64 ? 2 : 1; }
 // head sit next to each other), against kv positions [kv_lo, kv_hi).
 // part_row < 0: the item covers the unit's whole kv range and writes the final
 // out / lse; otherwise it writes fp32 partials at rows part_row .. of the
-// workspace partial buffers.
+// workspace partial buffers.  next: for the persistent tcgen05 variants, the
+// index of the next item of the same CTA (-1 at the end of its chain; chain c
+// starts at item c); -1 for the others.
 struct WorkItem {
   int32_t b, h, row0, nrows;
-  int32_t kv_lo, kv_hi, part_row, pad;
+  int32_t kv_lo, kv_hi, part_row, next;
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
 
@@ -63,7 +67,8 @@ struct PlanHeader {
   uint64_t off_status, off_items, off_merge, off_part_lse, off_part_out, ws_bytes;
   uint64_t plan_bytes;
   int64_t cluster;  // > 1: splits of a unit form a thread-block cluster of this size
-  uint64_t reserved[3];
+  int64_t n_ctas;   // persistent tcgen05 variants: CTAs (item chains); 0 otherwise
+  uint64_t reserved[2];
 };
 static_assert(sizeof(PlanHeader) == 184, "PlanHeader layout (read by the Python binding)");
 

@@ -32,6 +32,8 @@ struct PartialParams {
   float v_scale;
   int cluster;                // > 1: the splits of a unit are the CTAs of one thread-block
                               // cluster (rank = split index) and merge through shared memory
+  int n_items;                // work items in `items`
+  int n_ctas;                 // persistent tcgen05 variants: item chains (see WorkItem::next)
 };
 
 struct MergeParams {

@@ -126,11 +126,13 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   int kernel = o.kernel;
   if ((kernel == VA_KERNEL_TC_128 || kernel == VA_KERNEL_TC_256) && !tc_ok) return VA_ERR_UNSUPPORTED;
   if (kernel == VA_KERNEL_AUTO) {
-    // Measured on GB300: the tcgen05 variant with two Q tiles per CTA wins
-    // once a KV head has >= 128 rows (prefill-like and wide trees, bf16 or fp8
-    // caches); the warp-level variant keeps verify-sized blocks, where the
-    // tcgen05 CTA's fixed pipeline fill would dominate.
-    if (tc_ok && max_rows >= 128) kernel = kKernelTc256;
+    // Measured on GB300: the tcgen05 variants beat the warp-level one on every
+    // shape they serve (mma.sync runs at a fraction of the tensor-core rate
+    // there, so even verify-sized blocks that fill half of the 128-row MMA
+    // come out ahead); two Q tiles per CTA once a KV head has > 128 rows.  The
+    // warp-level variant keeps head_dim 64, odd page sizes and groups that do
+    // not tile 128 rows.
+    if (tc_ok) kernel = max_rows > 128 ? kKernelTc256 : kKernelTc128;
     else kernel = max_rows <= 64 ? kKernelMma64 : kKernelMma128;
   }
   const int BM = kernel_rows(kernel);
@@ -278,7 +280,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
         for (int64_t s = 0; s < cluster; ++s) {
           const int64_t lo = s * cluster_chunk;
           const int64_t hi = std::min<int64_t>(lo + cluster_chunk, u.kv_end);
-          WorkItem w{u.b, h, u.row0, u.nrows, (int32_t)lo, (int32_t)hi, -1, 0};
+          WorkItem w{u.b, h, u.row0, u.nrows, (int32_t)lo, (int32_t)hi, -1, -1};
           items.push_back({w, 0, order++});
         }
       continue;
@@ -294,7 +296,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
       for (int64_t s = 0; s < n; ++s) {
         int64_t lo = s * cu, hi = std::min<int64_t>(lo + cu, u.kv_end);
         WorkItem w{u.b, h, u.row0, u.nrows, (int32_t)lo, (int32_t)hi,
-                   n > 1 ? (int32_t)(base + s * u.nrows) : -1, 0};
+                   n > 1 ? (int32_t)(base + s * u.nrows) : -1, -1};
         items.push_back({w, (hi - lo) * (int64_t)(u.nrows + 16), order++});
       }
     }
@@ -311,6 +313,41 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
       if (a.it.kv_lo != b.it.kv_lo) return a.it.kv_lo < b.it.kv_lo;
       return a.it.row0 < b.it.row0;
     });
+
+  // Persistent tcgen05 variants: one CTA per SM walks a chain of items.  The
+  // longest-first list is dealt onto the CTAs by LPT (each item to the
+  // least-loaded CTA, with a per-item overhead of one key tile), chain c's
+  // first item is put at index c and the rest follow, linked through next.
+  int64_t n_ctas = 0;
+  if (kernel_is_tc(kernel) && !items.empty()) {
+    n_ctas = std::min<int64_t>((int64_t)items.size(), num_sms);
+    std::vector<std::vector<int64_t>> chain(n_ctas);
+    std::priority_queue<std::pair<int64_t, int64_t>, std::vector<std::pair<int64_t, int64_t>>,
+                        std::greater<std::pair<int64_t, int64_t>>> load;
+    for (int64_t c = 0; c < n_ctas; ++c) load.push({0, c});
+    for (size_t i = 0; i < items.size(); ++i) {
+      const auto top = load.top();
+      load.pop();
+      chain[top.second].push_back((int64_t)i);
+      const WorkItem& w = items[i].it;
+      // key tiles plus one of overhead; a tile of two Q tiles costs 5/3 of one
+      const int64_t tiles = ceil_div(w.kv_hi - w.kv_lo, TK) + 1;
+      load.push({top.first + tiles * (w.nrows > kTcRowsPerTile ? 5 : 3), top.second});
+    }
+    std::vector<Tmp> out;
+    out.reserve(items.size());
+    for (int64_t c = 0; c < n_ctas; ++c) out.push_back(items[chain[c][0]]);
+    for (int64_t c = 0; c < n_ctas; ++c) {
+      int32_t prev = (int32_t)c;
+      for (size_t k = 1; k < chain[c].size(); ++k) {
+        out.push_back(items[chain[c][k]]);
+        out[prev].it.next = (int32_t)(out.size() - 1);
+        prev = (int32_t)(out.size() - 1);
+      }
+      out[prev].it.next = -1;
+    }
+    items.swap(out);
+  }
 
   size_t need = sizeof(PlanHeader) + items.size() * sizeof(WorkItem) +
                 merges.size() * sizeof(MergeItem);
@@ -349,6 +386,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   hd.ws_bytes = align_up(hd.off_part_out + (size_t)part_rows * head_dim * 4, kWsAlign);
   hd.plan_bytes = need;
   hd.cluster = cluster;
+  hd.n_ctas = n_ctas;
   if (cluster) hd.chunk = cluster_chunk;
 
   char* dst = static_cast<char*>(plan_h);

@@ -162,8 +162,8 @@ def test_plans_of_the_named_workloads(va, name):
     hd = plan.header()
     # kernel variant follows the rows per KV head (G * L) and the cache dtype
     rows = int((wl.group * wl.qo_lens).max())
-    if rows >= 128 and wl.d == 128 and 128 % wl.group == 0 and wl.page_size % 16 == 0:
-        assert hd["kernel"] == 4
+    if wl.d == 128 and 128 % wl.group == 0 and wl.page_size % 16 == 0:
+        assert hd["kernel"] == (4 if rows > 128 else 3)
     else:
         assert hd["kernel"] == (1 if rows <= 64 else 2)
 
@@ -184,10 +184,50 @@ def test_tcgen05_plans_cover_every_row_once(va, name, kernel):
     _check_cover(va, t, plan)
 
 
+@pytest.mark.parametrize("name", ["gqa_varlen_prefill", "wide_tree_fp8_verify",
+                                  "codellama34b_chain_verify"])
+def test_tcgen05_plans_chain_every_item_once(va, name):
+    """The persistent tcgen05 kernel walks one chain of items per CTA: chain c
+    starts at item c, links run through the last field, and together the
+    chains visit every item exactly once, with near-equal loads."""
+    wl = synthetic.make_workload(name, with_values=False)
+    plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
+                                    wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                    kv_dtype=wl.kv_dtype, num_sms=152, kernel=4)
+    hd = plan.header()
+    it = plan.items()
+    n = len(it)
+    assert hd["n_ctas"] == min(n, 152)
+    seen = np.zeros(n, dtype=np.int32)
+    loads = []
+    for c in range(hd["n_ctas"]):
+        i, load = c, 0
+        while i >= 0:
+            assert 0 <= i < n
+            seen[i] += 1
+            load += int(it[i, 5] - it[i, 4])
+            i = int(it[i, 7])
+        loads.append(load)
+    assert np.all(seen == 1)
+    # longest-processing-time dealing: no chain exceeds the mean by more than
+    # the longest item
+    longest = int((it[:, 5] - it[:, 4]).max())
+    assert max(loads) <= np.mean(loads) + longest + 256
+
+
+def test_warp_level_plans_have_no_chains(va):
+    wl = synthetic.make_workload("llama3_8b_tree_verify", with_values=False)
+    plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
+                                    wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                    num_sms=152, kernel=2)
+    assert plan.header()["n_ctas"] == 0 and np.all(plan.items()[:, 7] == -1)
+
+
 def test_plan_items_sorted_longest_first(va):
+    # the warp-level variant's list (the hardware hands it to SMs in order)
     wl = synthetic.make_workload("codellama34b_chain_verify", with_values=False)
     plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, None,
-                                    wl.h_q, wl.h_kv, wl.d, wl.page_size, num_sms=152)
+                                    wl.h_q, wl.h_kv, wl.d, wl.page_size, num_sms=152, kernel=1)
     it = plan.items()
     cost = (it[:, 5] - it[:, 4]) * (it[:, 3] + 16)
     assert np.all(np.diff(cost) <= 0)

@@ -222,8 +222,9 @@ def test_cluster_merge_matches_workspace_merge(va, case, cap):
     else:
         wl = synthetic.make_custom(seed=33, **case)
     dw = DeviceWorkload(wl)
-    oc, lc, pc = dw.run(cluster=cap)
-    ow, lw, pw = dw.run(cluster=-1)
+    # the in-cluster merge belongs to the warp-level variant
+    oc, lc, pc = dw.run(cluster=cap, kernel=2)
+    ow, lw, pw = dw.run(cluster=-1, kernel=2)
     torch.cuda.synchronize()
     assert pc.header()["cluster"] > 1 and pc.launches() == 1
     assert pw.header()["cluster"] == 0
@@ -238,7 +239,7 @@ def test_cluster_with_a_stale_plan_flags_and_finishes(va):
     barriers (no hang), writes nothing, and raises VA_DEV_BAD_TABLE."""
     wl = synthetic.make_workload("llama3_8b_tree_verify")
     dw = DeviceWorkload(wl)
-    plan = dw.plan(cluster=16)
+    plan = dw.plan(cluster=16, kernel=2)
     assert plan.header()["cluster"] > 1
     # one page fewer (kv_len 4112 instead of 4113): only the last split of each
     # cluster, which ends at 4113, finds its range past the tables
