@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * 4 + warp;
   grid_dependency_wait();  // the partials come from the preceding split kernel
+  grid_dependents_launch();  // the next kernel may be scheduled; it waits for our completion
   if (r >= it.nrows) return;
   const float* lse_base = p.part_lse + it.part_row0 + r;
   // Every lane reads one split's LSE (32 at a time), then a warp max.
@@ -88,6 +89,11 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) 
 // (token, KV head) row, for K and V: a bit-exact copy to slot pos % P of page
 // kv_indices[kv_indptr[b] + pos / P], pos = kv_len_b - n_b + i.
 __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams p) {
+  // Launched with programmatic serialization: the pages may still be read by
+  // the kernel before this one, so wait for it; the attention kernel after
+  // this one may be scheduled at once (it waits for our completion).
+  grid_dependency_wait();
+  grid_dependents_launch();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long per_tok = (long long)p.h_kv * p.row_chunks;
   if (idx >= p.total_new * per_tok) return;
@@ -150,8 +156,8 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const long long blocks = (threads + 255) / 256;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   void* args[] = {const_cast<AppendParams*>(&p)};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(paged_kv_append_kernel),
-                          dim3((unsigned)blocks), dim3(256), args, 0, stream);
+  return launch_kernel(reinterpret_cast<const void*>(paged_kv_append_kernel),
+                       dim3((unsigned)blocks), dim3(256), 0, stream, args, /*pdl=*/true);
 }
 
 }  // namespace va

@@ -209,8 +209,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // Inputs (pages appended by the previous kernel, q, tables) may come from
-  // the grid before this one in the stream.
+  // the grid before this one in the stream.  Every CTA of this persistent
+  // grid is resident, so the next kernel (the merge) may be scheduled now: it
+  // waits for our completion before reading anything.
   grid_dependency_wait();
+  grid_dependents_launch();
 
   // Operand u = 2 j (K_j) or 2 j + 1 (V_j) of the CTA's running tile count j
   // sits in ring slot u % NSLOT, on its (u / NSLOT)-th use of that slot.
@@ -725,7 +728,6 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
   }
 
   __syncthreads();
-  grid_dependents_launch();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
