@@ -172,10 +172,12 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
                                                 : kernel_ctas_per_sm(kernel));
   const int es = kv_dtype == VA_DTYPE_FP8_E4M3 ? 1 : 2;
   const int64_t key_bytes = 2LL * head_dim * es;
-  // fixed cost of a CTA (prologue, pipeline fill and drain, epilogue) in
-  // K/V-byte equivalents: measured about two to three key tiles' worth for the
-  // tcgen05 variants, under one tile for the warp-level ones
-  const int64_t fixed_bytes = kernel_is_tc(kernel) ? 152 * 1024 : 48 * 1024;
+  // fixed cost of a work item (prologue, pipeline fill and drain, epilogue)
+  // in K/V-byte equivalents: about one key tile for both variants (the
+  // persistent tcgen05 CTAs overlap part of it with the previous item); on
+  // GB300 the fp8 wide tree measured 407 us with 7 splits per unit against
+  // 447 us with 2, which a larger value would have chosen
+  const int64_t fixed_bytes = kernel_is_tc(kernel) ? 64 * 1024 : 48 * 1024;
   const int64_t partial_bytes_per_row = 4LL * head_dim;
   int64_t min_chunk = o.min_chunk > 0 ? o.min_chunk : 2 * TK;
   min_chunk = ceil_div(min_chunk, TK) * TK;
@@ -201,11 +203,25 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     chunk = chunk_for(slots);
     double best = -1.0;
     std::vector<int64_t> costs;
+    // candidates: 1-4 waves of CTA slots, equal or full-plus-remainder cuts;
+    // for the persistent tcgen05 variants (items dealt onto one chain per
+    // SM) also the longest unit cut into n = 1 .. 32 equal chunks, which lets
+    // the dealing find an item count that divides evenly
+    std::vector<std::pair<int64_t, bool>> cands;
     for (int cand = 0; cand < 8; ++cand) {
       const int waves = 1 + (cand >> 1);
-      const bool eq = (cand & 1) == 0;
       const int64_t target = std::min<int64_t>(waves * slots, kMaxTargetPerSm * num_sms);
-      const int64_t c = chunk_for(target);
+      cands.push_back({chunk_for(target), (cand & 1) == 0});
+    }
+    if (kernel_is_tc(kernel)) {
+      int64_t longest = 0;
+      for (const Unit& u : units) longest = std::max<int64_t>(longest, u.kv_end);
+      for (int64_t n = 1; n <= 32; ++n)
+        cands.push_back({std::max<int64_t>(min_chunk, ceil_div(ceil_div(longest, n), TK) * TK), true});
+    }
+    for (const auto& cand : cands) {
+      const int64_t c = cand.first;
+      const bool eq = cand.second;
       costs.clear();
       for (const Unit& u : units) {
         int64_t cu;
