@@ -404,3 +404,28 @@ def test_named_workload_matches_oracle(va, name):
         caches = (ok, ov)
     compare(wl, out, lse, rows=rows, caches=caches, strict=True)
 
+
+
+@pytest.mark.parametrize("num_sms", [1, 3, 7])
+@pytest.mark.parametrize("kernel", [3, 4], ids=["tc128", "tc256"])
+@pytest.mark.parametrize("case", [
+    dict(mask="tree"),
+    dict(mask="causal"),
+    dict(mask="tree", kv_dtype=synthetic.FP8),
+], ids=["tree", "causal", "fp8_tree"])
+def test_tcgen05_long_item_chains_match_oracle(va, num_sms, kernel, case):
+    """The persistent tcgen05 kernel with few CTAs: each walks a long chain of
+    items mixing one and two live Q tiles, split and whole kv ranges, prefix
+    and prefill requests; the streaming of Q, keys, S / P and O from one item
+    into the next must not leak anything across items."""
+    wl = synthetic.make_custom(batch=4, h_q=16, h_kv=2, d=128,
+                               prefix=("fixed", [700, 0, 90, 2000]),
+                               qo=("fixed", [40, 33, 3, 17]), seed=41, **case)
+    dw = DeviceWorkload(wl)
+    out, lse, plan = dw.run(kernel=kernel, num_sms=num_sms, target_ctas=40)
+    torch.cuda.synchronize()
+    hd = plan.header()
+    assert hd["kernel"] == kernel and hd["n_ctas"] == min(num_sms, hd["n_items"])
+    assert hd["n_items"] > 2 * hd["n_ctas"]
+    assert va.verify_attn_device_status(plan) == 0
+    compare(wl, out, lse)
