@@ -27,12 +27,11 @@
 //    layout; rows of V past the chunk end are zeroed before the PV MMA reads
 //    them (stale slots may hold NaN).
 //  * fp8-e4m3 caches: raw tiles land unswizzled; four converter warps widen
-//    them into swizzled f16 operand buffers with integer ops -- an e4m3 code
-//    with its exponent and mantissa bits moved into f16 position is the same
-//    value times 2^-8, subnormals included -- and zero rows past the chunk;
-//    the 2^8 goes back in the softmax scale and the final normalisation, next
-//    to k_scale / v_scale.  The MMAs run on f16 (Q converted once per CTA,
-//    P packed as f16).
+//    them into swizzled f16 operand buffers (cvt.rn.f16x2.e4m3x2: every e4m3
+//    value, subnormals included, is an f16 value) and zero rows past the
+//    chunk; k_scale / v_scale stay in the softmax scale and the final
+//    normalisation.  The MMAs run on f16 (Q converted once per item, P packed
+//    as f16).
 // All mbarrier waits are bounded; on expiry the CTA raises VA_DEV_TIMEOUT,
 // stops issuing work, frees its TMEM and exits.
 #include <cuda.h>
@@ -53,8 +52,11 @@ struct TcCfg {
   static constexpr int KEYS = 128;                       // keys per tile (MMA N of S, K of PV)
   static constexpr int BLOCK_ROWS = NQ * ROWS;
   static constexpr int CONV_WARP0 = 4 + 4 * NQ;          // after producer, MMA, 2 spare, softmax
-  static constexpr int CONV_WARPS = FP8 ? 4 : 0;         // one per SM sub-partition
-  static constexpr int THREADS = 32 * (CONV_WARP0 + CONV_WARPS);
+  // fp8 widening: warps 2, 3 and CONV_WARP0 + 2, + 3 -- all on the SM
+  // sub-partitions 2 and 3 (warp % 4), away from the producer's and the MMA
+  // issuer's; warps CONV_WARP0 and CONV_WARP0 + 1 stay idle
+  static constexpr int CONV_WARPS = FP8 ? 4 : 0;
+  static constexpr int THREADS = 32 * (CONV_WARP0 + CONV_WARPS);  // fp8: 4 warps past the softmax
   static constexpr int QT_BYTES = ROWS * D * 2;          // one Q tile: [2 halves][128 rows][128 B]
   static constexpr int Q_BYTES = NQ * QT_BYTES;
   static constexpr int OP_BYTES = KEYS * D * 2;          // 16-bit K (or V) operand tile
@@ -88,15 +90,6 @@ static_assert(8 * B_COUNT + 8 <= 512, "barrier area");
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
   return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
-}
-
-// Two e4m3 codes (bits 0-7 and 16-23 of x, the rest zero) -> two f16 equal to
-// the codes' values times 2^-8: sign to bit 15, exponent and mantissa shifted
-// up by 7 (an e4m3 subnormal lands on the f16 subnormal of the same scaled
-// value, since both formats keep 3 resp. 10 mantissa bits under a fixed
-// exponent offset).  The NaN code 0x7f / 0xff maps to a finite value.
-__device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint32_t x) {
-  return (x + (x & 0x00800080u)) << 7;
 }
 
 // TMEM column (relative to the Q tile's S / P columns) of P's keys
@@ -405,11 +398,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         }
       }
     }
-  } else if (FP8 && warp >= C::CONV_WARP0) {
+  } else if (FP8 && (warp == 2 || warp == 3 || warp >= C::CONV_WARP0 + 2)) {
     // ---------------- fp8 -> scaled f16 widening ----------------
     // Step i of an item widens K_i, then V_{i-1}: K runs a tile ahead, since
     // S_i needs only K_i while V's single buffer frees up one PV later.
-    const int ct = tid - 32 * C::CONV_WARP0;            // 0 .. 127
+    const int ct = (warp < 4 ? warp - 2 : warp - C::CONV_WARP0) * 32 + lane;  // 0 .. 127
     constexpr int NCT = 32 * C::CONV_WARPS;
     int u0 = 0, t0 = 0;
     bool go = true;
@@ -441,14 +434,14 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
             uint4 a = make_uint4(0u, 0u, 0u, 0u), bq = a;
             if (k0 + r < g.hi) {
               const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + ch * 16);
-              a.x = e4m3x2_scaled_f16x2(__byte_perm(w.x, 0u, 0x4140));
-              a.y = e4m3x2_scaled_f16x2(__byte_perm(w.x, 0u, 0x4342));
-              a.z = e4m3x2_scaled_f16x2(__byte_perm(w.y, 0u, 0x4140));
-              a.w = e4m3x2_scaled_f16x2(__byte_perm(w.y, 0u, 0x4342));
-              bq.x = e4m3x2_scaled_f16x2(__byte_perm(w.z, 0u, 0x4140));
-              bq.y = e4m3x2_scaled_f16x2(__byte_perm(w.z, 0u, 0x4342));
-              bq.z = e4m3x2_scaled_f16x2(__byte_perm(w.w, 0u, 0x4140));
-              bq.w = e4m3x2_scaled_f16x2(__byte_perm(w.w, 0u, 0x4342));
+              a.x = e4m3x2_to_f16x2((uint16_t)(w.x & 0xffff));
+              a.y = e4m3x2_to_f16x2((uint16_t)(w.x >> 16));
+              a.z = e4m3x2_to_f16x2((uint16_t)(w.y & 0xffff));
+              a.w = e4m3x2_to_f16x2((uint16_t)(w.y >> 16));
+              bq.x = e4m3x2_to_f16x2((uint16_t)(w.z & 0xffff));
+              bq.y = e4m3x2_to_f16x2((uint16_t)(w.z >> 16));
+              bq.z = e4m3x2_to_f16x2((uint16_t)(w.w & 0xffff));
+              bq.w = e4m3x2_to_f16x2((uint16_t)(w.w >> 16));
             }
             // 16 f16 = 2 chunks of the swizzled operand row (half = ch / 4)
             uint8_t* row = dst + (ch >> 2) * (C::KEYS * 128) + r * 128;
@@ -473,8 +466,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     const int quad = warp & 3;                      // TMEM lane quarter this warp may access
     const int r = quad * 32 + lane;                 // row of the Q tile = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16) + qt * C::QT_COLS;
-    // fp8 operands hold the codes' values times 2^-8 (see e4m3x2_scaled_f16x2)
-    const float c = FP8 ? p.scale_log2 * 256.f : p.scale_log2;
+    const float c = p.scale_log2;
     const uint32_t b_s_full = bar(B_S_FULL + qt), b_p_full = bar(B_P_FULL + qt);
     int ns = 0, no = 0, nit = 0, u0 = 0;            // S tiles seen, items done, items, ring base
     bool live = true;
@@ -680,7 +672,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE + qt), no & 1, abort_flag))) { live = false; break; }
       tc_fence_after();
       const float lse = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
-      const float inv = l > 0.f ? (FP8 ? p.v_scale * 256.f : p.v_scale) / l : 0.f;
+      const float inv = l > 0.f ? p.v_scale / l : 0.f;
       size_t orow = 0;
       if (row_ok) {
         const int gg = (g.row0 + br) - t * G;
