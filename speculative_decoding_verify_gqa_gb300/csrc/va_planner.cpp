@@ -205,19 +205,36 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     std::vector<int64_t> costs;
     // candidates: 1-4 waves of CTA slots, equal or full-plus-remainder cuts;
     // for the persistent tcgen05 variants (items dealt onto one chain per
-    // SM) also the longest unit cut into n = 1 .. 32 equal chunks, which lets
-    // the dealing find an item count that divides evenly
+    // SM), when the units alone would leave SMs idle, also the longest unit
+    // cut into n equal chunks for the n that make the item count land near a
+    // multiple of the SM count, so that the dealing can even the chains out.
+    // Chunks at least as long as the longest unit leave every unit whole and
+    // are scored once.
+    int64_t longest = 0;
+    for (const Unit& u : units) longest = std::max<int64_t>(longest, u.kv_end);
+    const int64_t whole = std::max<int64_t>(min_chunk, ceil_div(longest, TK) * TK);
     std::vector<std::pair<int64_t, bool>> cands;
+    auto add = [&](int64_t c, bool eq) {
+      if (c >= whole) {
+        c = whole;
+        eq = true;
+      }
+      for (const auto& x : cands)
+        if (x.first == c && x.second == eq) return;
+      cands.push_back({c, eq});
+    };
     for (int cand = 0; cand < 8; ++cand) {
       const int waves = 1 + (cand >> 1);
       const int64_t target = std::min<int64_t>(waves * slots, kMaxTargetPerSm * num_sms);
-      cands.push_back({chunk_for(target), (cand & 1) == 0});
+      add(chunk_for(target), (cand & 1) == 0);
     }
-    if (kernel_is_tc(kernel)) {
-      int64_t longest = 0;
-      for (const Unit& u : units) longest = std::max<int64_t>(longest, u.kv_end);
-      for (int64_t n = 1; n <= 32; ++n)
-        cands.push_back({std::max<int64_t>(min_chunk, ceil_div(ceil_div(longest, n), TK) * TK), true});
+    const int64_t unit_heads = std::max<int64_t>(1, (int64_t)units.size() * num_kv_heads);
+    if (kernel_is_tc(kernel) && unit_heads < slots) {
+      for (int64_t k = 1; k <= 6; ++k) {
+        const int64_t n0 = (k * slots + unit_heads / 2) / unit_heads;
+        for (int64_t n = std::max<int64_t>(1, n0 - 1); n <= std::min<int64_t>(32, n0 + 1); ++n)
+          add(std::max<int64_t>(min_chunk, ceil_div(ceil_div(longest, n), TK) * TK), true);
+      }
     }
     for (const auto& cand : cands) {
       const int64_t c = cand.first;
