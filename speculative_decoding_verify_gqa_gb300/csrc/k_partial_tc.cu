@@ -70,20 +70,25 @@ struct TcCfg {
   static constexpr int OFF_RING = OFF_CONV + CONV_BYTES;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * SLOT_BYTES;
   static constexpr int SMEM = OFF_BAR + 512;              // + barriers, TMEM address, abort flag
-  static constexpr uint32_t QT_COLS = 256;               // per Q tile: S / P (128) | O (128)
-  static constexpr uint32_t COL_O = 128;
-  static constexpr uint32_t TMEM_COLS = NQ * QT_COLS;
+  // S / P buffers per Q tile: one Q tile double-buffers S, so S_{j+1} is
+  // computed while the softmax works on S_j; two Q tiles fill tensor memory
+  // with one buffer each and alternate instead.
+  static constexpr int SBUF = NQ == 1 ? 2 : 1;
+  static constexpr uint32_t QT_COLS = 128 * (SBUF + 1);  // per Q tile: S / P (128 each) | O (128)
+  static constexpr uint32_t COL_O = 128 * SBUF;
+  static constexpr uint32_t TMEM_COLS = 512;             // NQ * QT_COLS, as a power of two
   static_assert(NSLOT >= 3, "ring depth");
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
-  static_assert(TMEM_COLS <= 512, "tensor memory budget");
+  static_assert(NQ * QT_COLS <= TMEM_COLS, "tensor memory budget");
 };
 
 constexpr float kLn2 = 0.6931471805599453f;
 
-// barrier slots (per-Q-tile barriers at base + qt)
+// barrier slots (per-Q-tile barriers at base + qt; S_FULL / P_FULL at base +
+// buffer when one Q tile double-buffers S)
 enum { B_Q = 0, B_Q_READY = 1, B_Q_FREE = 2, B_FULL = 3, B_EMPTY = 11, B_CK_FULL = 19,
        B_CK_FREE = 21, B_CV_FULL = 23, B_CV_FREE = 24, B_S_FULL = 25, B_P_FULL = 27, B_O_DONE = 29,
-       B_O_FREE = 31, B_COUNT = 33 };
+       B_O_FREE = 31, B_PV_DONE = 33, B_COUNT = 34 };
 static_assert(8 * B_COUNT + 8 <= 512, "barrier area");
 
 // Instruction descriptor, kind::f16 with f16 A and B (fp32 accumulator).
@@ -188,12 +193,15 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     }
     mbar_init(bar(B_CV_FULL), C::CONV_WARPS > 0 ? C::CONV_WARPS : 1);
     mbar_init(bar(B_CV_FREE), 1);
+    for (int s = 0; s < NQ * C::SBUF; ++s) {
+      mbar_init(bar(B_S_FULL + s), 1);
+      mbar_init(bar(B_P_FULL + s), 4);
+    }
     for (int qt = 0; qt < NQ; ++qt) {
-      mbar_init(bar(B_S_FULL + qt), 1);
-      mbar_init(bar(B_P_FULL + qt), 4);
       mbar_init(bar(B_O_DONE + qt), 1);
       mbar_init(bar(B_O_FREE + qt), 4);
     }
+    mbar_init(bar(B_PV_DONE), 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -294,7 +302,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       constexpr uint32_t id_o = FP8 ? idesc_f16(C::ROWS, C::D, true) : idesc_bf16(C::ROWS, C::D, true);
       // running counts: ring operands (u0), tiles (t0), items (nit); per Q tile
       // the S tiles issued (ns) and items completed (no)
-      int u0 = 0, t0 = 0, nit = 0;
+      int u0 = 0, t0 = 0, nit = 0, npv = 0;  // npv: PVs issued (one Q tile, double-buffered S)
       int ns[NQ], no[NQ];
 #pragma unroll
       for (int qt = 0; qt < NQ; ++qt) ns[qt] = no[qt] = 0;
@@ -332,50 +340,95 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         const ItemGeo g = decode(i);
         if (!g.ok) continue;
         if (!mbar_wait(bar(FP8 ? B_Q_READY : B_Q), nit & 1, abort_flag)) break;
-        for (int j = 0; live && j <= g.n_tiles; ++j) {
-          // step j: PV of tile j - 1 and S of tile j, Q tile by Q tile
-          if (j < g.n_tiles && !wait_k(j)) { live = false; break; }
-          if (j >= 1 && !wait_v(j - 1)) { live = false; break; }
-          const uint64_t dk = j < g.n_tiles ? smem_desc_sw128(k_addr(j), 16, 1024) : 0;
-          const uint64_t dv = j >= 1 ? smem_desc_sw128(v_addr(j - 1), C::KEYS * 128, 1024) : 0;
-#pragma unroll
-          for (int qt = 0; qt < NQ; ++qt) {
-            if (qt >= g.nq) break;
-            const uint32_t ts = tmem + qt * C::QT_COLS;  // S_qt / P_qt columns
-            if (j >= 1) {
-              // the first PV of an item overwrites O: the previous item's
-              // epilogue must have read it out
-              if (j == 1 && no[qt] >= 1 &&
-                  !mbar_wait(bar(B_O_FREE + qt), (no[qt] - 1) & 1, abort_flag)) {
-                live = false;
-                break;
-              }
-              if (!mbar_wait(bar(B_P_FULL + qt), (ns[qt] - 1) & 1, abort_flag)) {
-                live = false;
-                break;
-              }
-              tc_fence_after();
-#pragma unroll
-              for (int kk = 0; kk < C::KEYS / 16; ++kk)
-                umma_ts(ts + C::COL_O, ts + p_col(kk), dv + (uint64_t)((kk * 16 * 128) >> 4), id_o,
-                        (j > 1 || kk > 0) ? 1u : 0u);
-              if (j == g.n_tiles) umma_commit(bar(B_O_DONE + qt));
-            }
+        if constexpr (C::SBUF == 2) {
+          // One Q tile, S double-buffered: step j issues S_j into buffer
+          // (S count) % 2 before it waits for P_{j-1}, so the tensor core
+          // computes S_j while the softmax still works on S_{j-1}.  S_j
+          // overwrites P_{j-2}, whose PV was issued one step earlier (the MMAs
+          // of this thread run in issue order).
+          for (int j = 0; live && j <= g.n_tiles; ++j) {
             if (j < g.n_tiles) {
-              const uint64_t dq = dq0 + (uint64_t)(qt * (C::QT_BYTES >> 4));
+              if (!wait_k(j)) { live = false; break; }
+              const int b = ns[0] & 1;
+              const uint64_t dk = smem_desc_sw128(k_addr(j), 16, 1024);
 #pragma unroll
               for (int kk = 0; kk < C::D / 16; ++kk)
-                umma_bf16(ts, dq + (uint64_t)((((kk >> 2) * (C::ROWS * 128)) + (kk & 3) * 32) >> 4),
+                umma_bf16(tmem + b * 128, dq0 + (uint64_t)((((kk >> 2) * (C::ROWS * 128)) + (kk & 3) * 32) >> 4),
                           dk + (uint64_t)((((kk >> 2) * (C::KEYS * 128)) + (kk & 3) * 32) >> 4), id_s,
                           kk > 0 ? 1u : 0u);
-              umma_commit(bar(B_S_FULL + qt));
-              ++ns[qt];
+              umma_commit(bar(B_S_FULL + b));
+              ++ns[0];
+              if (j == g.n_tiles - 1) umma_commit(bar(B_Q_FREE));  // Q read by this item's last S
+              umma_commit(k_free_bar(j));
+            }
+            if (j >= 1) {
+              if (!wait_v(j - 1)) { live = false; break; }
+              // the first PV of an item overwrites O: the previous item's
+              // epilogue must have read it out
+              if (j == 1 && no[0] >= 1 && !mbar_wait(bar(B_O_FREE), (no[0] - 1) & 1, abort_flag)) {
+                live = false;
+                break;
+              }
+              const int b = npv & 1;  // buffer of S_{j-1} / P_{j-1}
+              if (!mbar_wait(bar(B_P_FULL + b), (npv >> 1) & 1, abort_flag)) { live = false; break; }
+              tc_fence_after();
+              const uint64_t dv = smem_desc_sw128(v_addr(j - 1), C::KEYS * 128, 1024);
+#pragma unroll
+              for (int kk = 0; kk < C::KEYS / 16; ++kk)
+                umma_ts(tmem + C::COL_O, tmem + b * 128 + p_col(kk), dv + (uint64_t)((kk * 16 * 128) >> 4),
+                        id_o, (j > 1 || kk > 0) ? 1u : 0u);
+              umma_commit(bar(B_PV_DONE));
+              if (j == g.n_tiles) umma_commit(bar(B_O_DONE));
+              umma_commit(v_free_bar(j - 1));
+              ++npv;
             }
           }
-          if (!live) break;
-          if (j == g.n_tiles - 1) umma_commit(bar(B_Q_FREE));  // Q read by this item's last S
-          if (j >= 1) umma_commit(v_free_bar(j - 1));
-          if (j < g.n_tiles) umma_commit(k_free_bar(j));
+        } else {
+          for (int j = 0; live && j <= g.n_tiles; ++j) {
+            // step j: PV of tile j - 1 and S of tile j, Q tile by Q tile
+            if (j < g.n_tiles && !wait_k(j)) { live = false; break; }
+            if (j >= 1 && !wait_v(j - 1)) { live = false; break; }
+            const uint64_t dk = j < g.n_tiles ? smem_desc_sw128(k_addr(j), 16, 1024) : 0;
+            const uint64_t dv = j >= 1 ? smem_desc_sw128(v_addr(j - 1), C::KEYS * 128, 1024) : 0;
+#pragma unroll
+            for (int qt = 0; qt < NQ; ++qt) {
+              if (qt >= g.nq) break;
+              const uint32_t ts = tmem + qt * C::QT_COLS;  // S_qt / P_qt columns
+              if (j >= 1) {
+                // the first PV of an item overwrites O: the previous item's
+                // epilogue must have read it out
+                if (j == 1 && no[qt] >= 1 &&
+                    !mbar_wait(bar(B_O_FREE + qt), (no[qt] - 1) & 1, abort_flag)) {
+                  live = false;
+                  break;
+                }
+                if (!mbar_wait(bar(B_P_FULL + qt), (ns[qt] - 1) & 1, abort_flag)) {
+                  live = false;
+                  break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C::KEYS / 16; ++kk)
+                  umma_ts(ts + C::COL_O, ts + p_col(kk), dv + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                          (j > 1 || kk > 0) ? 1u : 0u);
+                if (j == g.n_tiles) umma_commit(bar(B_O_DONE + qt));
+              }
+              if (j < g.n_tiles) {
+                const uint64_t dq = dq0 + (uint64_t)(qt * (C::QT_BYTES >> 4));
+#pragma unroll
+                for (int kk = 0; kk < C::D / 16; ++kk)
+                  umma_bf16(ts, dq + (uint64_t)((((kk >> 2) * (C::ROWS * 128)) + (kk & 3) * 32) >> 4),
+                            dk + (uint64_t)((((kk >> 2) * (C::KEYS * 128)) + (kk & 3) * 32) >> 4), id_s,
+                            kk > 0 ? 1u : 0u);
+                umma_commit(bar(B_S_FULL + qt));
+                ++ns[qt];
+              }
+            }
+            if (!live) break;
+            if (j == g.n_tiles - 1) umma_commit(bar(B_Q_FREE));  // Q read by this item's last S
+            if (j >= 1) umma_commit(v_free_bar(j - 1));
+            if (j < g.n_tiles) umma_commit(k_free_bar(j));
+          }
         }
         if (!live) break;
 #pragma unroll
@@ -467,7 +520,6 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     const int r = quad * 32 + lane;                 // row of the Q tile = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16) + qt * C::QT_COLS;
     const float c = p.scale_log2;
-    const uint32_t b_s_full = bar(B_S_FULL + qt), b_p_full = bar(B_P_FULL + qt);
     int ns = 0, no = 0, nit = 0, u0 = 0;            // S tiles seen, items done, items, ring base
     bool live = true;
     int slot = blockIdx.x, steps = 0;
@@ -535,7 +587,16 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
             fence_proxy_async();
           }
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(b_s_full, ns & 1, abort_flag))) { live = false; break; }
+        // S_j: buffer ns % 2 of the one Q tile (double-buffered), else the Q
+        // tile's only buffer
+        const int sb = C::SBUF == 2 ? (ns & 1) : 0;
+        const uint32_t s_addr = lane_addr + sb * 128;
+        const uint32_t b_sp = C::SBUF == 2 ? sb : qt;  // S_FULL / P_FULL of this buffer
+        const uint32_t s_par = C::SBUF == 2 ? (ns >> 1) & 1 : ns & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S_FULL + b_sp), s_par, abort_flag))) {
+          live = false;
+          break;
+        }
         ++ns;
         tc_fence_after();
         // Visibility of the tile's keys for this row.  Causal drafts: keys below
@@ -590,9 +651,10 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
           }
           return q == 0 ? vis[0] : q == 1 ? vis[1] : q == 2 ? vis[2] : vis[3];
         };
-        // the row's new reference max from this tile's max (log2 units); O is
-        // idle here (PV_{j-1} of this Q tile completed before S_j did), so a
-        // raised max rescales it at once
+        // the row's new reference max from this tile's max (log2 units); a
+        // raised max rescales O at once, once PV_{j-1} is done with it (with
+        // a single S buffer it completed before S_j did; a double-buffered S_j
+        // may complete first, so the softmax waits for that PV)
         float alpha = 1.f, base = 0.f;
         auto new_max = [&](float mx) {
           mx *= c;  // c > 0
@@ -601,6 +663,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
           alpha = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
           base = m_new == -INFINITY ? 0.f : m_new;
           if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            if (C::SBUF == 2) {
+              // PV of the previous S tile (global count ns - 2) has completed
+              if (!__all_sync(0xffffffffu, mbar_wait(bar(B_PV_DONE), (ns - 2) & 1, abort_flag))) live = false;
+              tc_fence_after();
+            }
             for (int q = 0; q < C::D / 32; ++q) {
               uint32_t ov[32];
               tmem_ld32(lane_addr + C::COL_O + q * 32, ov);
@@ -628,7 +695,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
             sums[i & 3] += p0 + p1;
             pk[i] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
-          tmem_st16(lane_addr + 32 * q, pk);
+          tmem_st16(s_addr + 32 * q, pk);
         };
         // Both passes walk the row 32 logits at a time in rolled loops: a
         // small loop body keeps every warp's code in the instruction cache.
@@ -637,7 +704,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
 #pragma unroll 1
           for (int q = 0; q < C::KEYS / 32; ++q) {
             uint32_t raw[32];
-            tmem_ld32(lane_addr + q * 32, raw);
+            tmem_ld32(s_addr + q * 32, raw);
             tmem_wait_ld();
             if (full) {
 #pragma unroll
@@ -655,7 +722,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
 #pragma unroll 1
           for (int q = 0; q < C::KEYS / 32; ++q) {
             uint32_t raw[32];
-            tmem_ld32(lane_addr + q * 32, raw);
+            tmem_ld32(s_addr + q * 32, raw);
             tmem_wait_ld();
             exp_chunk(raw, q, full ? 0xffffffffu : vis_word(q), !full);
           }
@@ -665,7 +732,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(b_p_full);
+        if (lane == 0) mbar_arrive(bar(B_P_FULL + b_sp));
       }
       if (!live) break;
       // epilogue
