@@ -13,11 +13,14 @@ namespace {
 // kernel): for each row, m = max_s lse_s, w_s = e^(lse_s - m), out =
 // sum_s w_s out_s / sum_s w_s, lse = m + ln sum_s w_s; splits with lse = -inf
 // carry no mass, and a row with no mass at all gets out = 0, lse = -inf.
-// One warp per row; each lane owns D / 32 consecutive output elements.
+// One warp per row; each lane owns D / 32 consecutive output elements.  The
+// splits are read CH at a time, LSE and partial output together, with a
+// running max (sums rescaled when it rises), so a row of up to CH splits costs
+// one round trip to memory.
 template <int D>
 __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) {
   constexpr int V = D / 32;
-  constexpr int CH = 16;  // splits whose loads are issued together
+  constexpr int CH = 24;  // splits whose loads are issued together
   const MergeItem it = p.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * 4 + warp;
@@ -25,47 +28,49 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) 
   grid_dependents_launch();  // the next kernel may be scheduled; it waits for our completion
   if (r >= it.nrows) return;
   const float* lse_base = p.part_lse + it.part_row0 + r;
-  // Every lane reads one split's LSE (32 at a time), then a warp max.
-  float m = -INFINITY;
-  for (int s0 = 0; s0 < it.nsplit; s0 += 32) {
-    const int s = s0 + lane;
-    if (s < it.nsplit) m = fmaxf(m, lse_base[(size_t)s * it.nrows]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float m = -INFINITY, den = 0.f;
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
-  float den = 0.f;
-  if (m != -INFINITY) {
-    for (int s0 = 0; s0 < it.nsplit; s0 += CH) {
-      float ls[CH];
-      float x[CH][V];
+  for (int s0 = 0; s0 < it.nsplit; s0 += CH) {
+    float ls[CH];
+    float x[CH][V];
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int s = s0 + c;
-        ls[c] = -INFINITY;
-        if (s < it.nsplit) {
-          ls[c] = lse_base[(size_t)s * it.nrows];
-          const float* src =
-              p.part_out + ((size_t)it.part_row0 + (size_t)s * it.nrows + r) * D + lane * V;
-          if constexpr (V == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src);
-            x[c][0] = v.x; x[c][1] = v.y; x[c][2] = v.z; x[c][3] = v.w;
-          } else {
-            const float2 v = *reinterpret_cast<const float2*>(src);
-            x[c][0] = v.x; x[c][1] = v.y;
-          }
+    for (int c = 0; c < CH; ++c) {
+      const int s = s0 + c;
+      ls[c] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < V; ++i) x[c][i] = 0.f;
+      if (s < it.nsplit) {
+        ls[c] = lse_base[(size_t)s * it.nrows];
+        const float* src = p.part_out + ((size_t)it.part_row0 + (size_t)s * it.nrows + r) * D + lane * V;
+        if constexpr (V == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          x[c][0] = v.x; x[c][1] = v.y; x[c][2] = v.z; x[c][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          x[c][0] = v.x; x[c][1] = v.y;
         }
       }
+    }
+    float cm = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        if (ls[c] == -INFINITY) continue;  // an empty split carries no mass
-        const float w = ex2((ls[c] - m) * kLog2e);
-        den += w;
+    for (int c = 0; c < CH; ++c) cm = fmaxf(cm, ls[c]);
+    if (cm == -INFINITY) continue;  // no split of this chunk carries mass
+    if (cm > m) {
+      const float sc = ex2((m - cm) * kLog2e);  // 0 while m = -inf
+      den *= sc;
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] += w * x[c][i];
-      }
+      for (int i = 0; i < V; ++i) acc[i] *= sc;
+      m = cm;
+    }
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      if (ls[c] == -INFINITY) continue;  // an empty split carries no mass
+      const float w = ex2((ls[c] - m) * kLog2e);
+      den += w;
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] += w * x[c][i];
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;

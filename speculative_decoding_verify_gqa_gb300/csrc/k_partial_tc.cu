@@ -8,9 +8,11 @@
 // partial + LSE), laid out for sm_103a:
 //  * warp 0, one thread: TMA producer.  Q arrives as one 3-D box per 64-column
 //    half and Q tile (G heads x 128/G tokens: the tile's token-major rows);
-//    key tiles of 128 keys arrive as 16-row page boxes of the 4-D cache
-//    [page, head, slot, dim] (page ids read one tile ahead; boxes past the
-//    chunk point outside the pool, so TMA zero-fills them) into one ring of
+//    key tiles of 128 keys arrive as one 4 KB box per 16 keys of a page
+//    (bf16: the cache viewed as [page * h_kv + head][slot / 8][half][slot % 8]
+//    [64], which lands in the MMAs' swizzled operand layout; fp8: 2 KB raw
+//    boxes) -- page ids read two tiles ahead; boxes past the chunk point
+//    outside the pool, so TMA zero-fills them -- into one ring of
 //    mbarrier-tracked slots holding K_0, V_0, K_1, V_1, ...
 //  * warp 1, one thread: tcgen05.mma issuer.  Per Q tile and key tile j it
 //    issues O += P_{j-1} V_{j-1} (P read from tensor memory, V MN-major from
@@ -240,9 +242,10 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
           for (int half = 0; half < 2; ++half)
             tma_load_3d(sbase + C::OFF_Q + qt * C::QT_BYTES + half * (C::QT_BYTES / 2), &maps.q,
                         half * 64, g.h * G, tok0 + qt * (C::ROWS / G), bar(B_Q));
-        // Page ids of a tile's 16-key boxes (-1 past the chunk), loaded one
-        // tile ahead so their latency hides behind the previous tile's wait.
-        int cur[NG], nxt[NG];
+        // Page ids of a tile's 16-key boxes (-1 past the chunk), loaded two
+        // tiles ahead so their latency hides behind the previous tiles' waits
+        // (and an item's first two tiles wait for one round trip, not two).
+        int cur[NG], nxt[NG], nx2[NG];
         auto load_pages = [&](int j, int* pg) {
           const int k0 = g.lo + j * C::KEYS;
 #pragma unroll
@@ -252,8 +255,9 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
           }
         };
         load_pages(0, cur);
+        load_pages(1, nxt);
         for (int j = 0; live && j < g.n_tiles; ++j) {
-          load_pages(j + 1, nxt);
+          load_pages(j + 2, nx2);
           const int k0 = g.lo + j * C::KEYS;
           for (int v = 0; v < 2; ++v, ++u) {
             const int s = u % C::NSLOT, n = u / C::NSLOT;
@@ -281,13 +285,15 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
               if constexpr (FP8) {
                 tma_load_4d(dst + q * 2048, map, 0, slot, g.h, page, bar(B_FULL + s));
               } else {
-                tma_load_4d(dst + q * 2048, map, 0, slot, g.h, page, bar(B_FULL + s));
-                tma_load_4d(dst + C::KEYS * 128 + q * 2048, map, 64, slot, g.h, page, bar(B_FULL + s));
+                tma_load_5d(dst + q * 4096, map, 0, 0, 0, slot >> 3, page * p.h_kv + g.h, bar(B_FULL + s));
               }
             }
           }
 #pragma unroll
-          for (int q = 0; q < NG; ++q) cur[q] = nxt[q];
+          for (int q = 0; q < NG; ++q) {
+            cur[q] = nxt[q];
+            nxt[q] = nx2[q];
+          }
         }
         ++nit;
       }
@@ -310,6 +316,12 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         return FP8 ? sbase + C::OFF_CONV + ((t0 + j) & 1) * C::OP_BYTES
                    : sbase + C::OFF_RING + ((u0 + 2 * j) % C::NSLOT) * C::SLOT_BYTES;
       };
+      // K / V operand layouts: widened fp8 in 64-column halves [half][keys][64]
+      // (halves KEYS * 128 bytes apart, 8-key groups 1024); bf16 as the TMA
+      // boxes land, [8-key group][half][8][64] (groups 2048 apart, halves 1024)
+      constexpr uint32_t KV_SBO = FP8 ? 1024 : 2048;         // 8-key group stride
+      constexpr uint32_t KV_HALF = FP8 ? C::KEYS * 128 : 1024;  // 64-column half stride
+      constexpr uint32_t V_LBO = KV_HALF, V_KK = 2 * KV_SBO;  // PV: 16 keys per MMA
       auto v_addr = [&](int j) {
         return FP8 ? sbase + C::OFF_CONV + 2 * C::OP_BYTES
                    : sbase + C::OFF_RING + ((u0 + 2 * j + 1) % C::NSLOT) * C::SLOT_BYTES;
@@ -350,11 +362,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
             if (j < g.n_tiles) {
               if (!wait_k(j)) { live = false; break; }
               const int b = ns[0] & 1;
-              const uint64_t dk = smem_desc_sw128(k_addr(j), 16, 1024);
+              const uint64_t dk = smem_desc_sw128(k_addr(j), 16, KV_SBO);
 #pragma unroll
               for (int kk = 0; kk < C::D / 16; ++kk)
                 umma_bf16(tmem + b * 128, dq0 + (uint64_t)((((kk >> 2) * (C::ROWS * 128)) + (kk & 3) * 32) >> 4),
-                          dk + (uint64_t)((((kk >> 2) * (C::KEYS * 128)) + (kk & 3) * 32) >> 4), id_s,
+                          dk + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4), id_s,
                           kk > 0 ? 1u : 0u);
               umma_commit(bar(B_S_FULL + b));
               ++ns[0];
@@ -372,10 +384,10 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
               const int b = npv & 1;  // buffer of S_{j-1} / P_{j-1}
               if (!mbar_wait(bar(B_P_FULL + b), (npv >> 1) & 1, abort_flag)) { live = false; break; }
               tc_fence_after();
-              const uint64_t dv = smem_desc_sw128(v_addr(j - 1), C::KEYS * 128, 1024);
+              const uint64_t dv = smem_desc_sw128(v_addr(j - 1), V_LBO, KV_SBO);
 #pragma unroll
               for (int kk = 0; kk < C::KEYS / 16; ++kk)
-                umma_ts(tmem + C::COL_O, tmem + b * 128 + p_col(kk), dv + (uint64_t)((kk * 16 * 128) >> 4),
+                umma_ts(tmem + C::COL_O, tmem + b * 128 + p_col(kk), dv + (uint64_t)((kk * V_KK) >> 4),
                         id_o, (j > 1 || kk > 0) ? 1u : 0u);
               umma_commit(bar(B_PV_DONE));
               if (j == g.n_tiles) umma_commit(bar(B_O_DONE));
@@ -388,8 +400,8 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
             // step j: PV of tile j - 1 and S of tile j, Q tile by Q tile
             if (j < g.n_tiles && !wait_k(j)) { live = false; break; }
             if (j >= 1 && !wait_v(j - 1)) { live = false; break; }
-            const uint64_t dk = j < g.n_tiles ? smem_desc_sw128(k_addr(j), 16, 1024) : 0;
-            const uint64_t dv = j >= 1 ? smem_desc_sw128(v_addr(j - 1), C::KEYS * 128, 1024) : 0;
+            const uint64_t dk = j < g.n_tiles ? smem_desc_sw128(k_addr(j), 16, KV_SBO) : 0;
+            const uint64_t dv = j >= 1 ? smem_desc_sw128(v_addr(j - 1), V_LBO, KV_SBO) : 0;
 #pragma unroll
             for (int qt = 0; qt < NQ; ++qt) {
               if (qt >= g.nq) break;
@@ -409,7 +421,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < C::KEYS / 16; ++kk)
-                  umma_ts(ts + C::COL_O, ts + p_col(kk), dv + (uint64_t)((kk * 16 * 128) >> 4), id_o,
+                  umma_ts(ts + C::COL_O, ts + p_col(kk), dv + (uint64_t)((kk * V_KK) >> 4), id_o,
                           (j > 1 || kk > 0) ? 1u : 0u);
                 if (j == g.n_tiles) umma_commit(bar(B_O_DONE + qt));
               }
@@ -418,7 +430,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < C::D / 16; ++kk)
                   umma_bf16(ts, dq + (uint64_t)((((kk >> 2) * (C::ROWS * 128)) + (kk & 3) * 32) >> 4),
-                            dk + (uint64_t)((((kk >> 2) * (C::KEYS * 128)) + (kk & 3) * 32) >> 4), id_s,
+                            dk + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4), id_s,
                             kk > 0 ? 1u : 0u);
                 umma_commit(bar(B_S_FULL + qt));
                 ++ns[qt];
@@ -581,8 +593,8 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
             uint8_t* vt = smem + C::OFF_RING + s * C::SLOT_BYTES;
             for (int z = r; z < (zhi - zlo) * 16; z += C::ROWS) {
               const int row = zlo + z / 16, half = (z / 8) & 1, ch = z & 7;
-              *reinterpret_cast<uint4*>(vt + half * (C::KEYS * 128) + row * 128 + (ch << 4)) =
-                  make_uint4(0u, 0u, 0u, 0u);
+              const int off = (row >> 3) * 2048 + half * 1024 + (row & 7) * 128;
+              *reinterpret_cast<uint4*>(vt + off + (ch << 4)) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async();
           }

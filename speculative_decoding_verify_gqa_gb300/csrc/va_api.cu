@@ -143,6 +143,8 @@ int make_tc_maps(const void* q, int64_t total_qo, const void* k_cache, const voi
   if (!enc) return VA_ERR_CUDA;
   const int G = hd->group, D = hd->head_dim, P = hd->page_size;
   if (total_qo <= 0 || num_pages <= 0) return VA_ERR_INVALID_ARGUMENT;
+  // the bf16 view indexes page * h_kv + head (plus one past the pool) in int
+  if ((int64_t)(num_pages + 1) * hd->h_kv > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
   cuuint32_t estr[4] = {1, 1, 1, 1};
   {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hd->h_q, (cuuint64_t)total_qo};
@@ -161,12 +163,25 @@ int make_tc_maps(const void* q, int64_t total_qo, const void* k_cache, const voi
   cuuint32_t box[4] = {fp8 ? 128u : 64u, 16, 1, 1};
   const void* src[2] = {k_cache, v_cache};
   CUtensorMap* dst[2] = {&m->k, &m->v};
-  for (int i = 0; i < 2; ++i)
+  for (int i = 0; i < 2; ++i) {
+    if (!fp8) {
+      // [page * h_kv + head][slot / 8][half][slot % 8][64], one box per 16 keys
+      cuuint64_t vd[5] = {64, 8, 2, (cuuint64_t)P / 8, (cuuint64_t)hd->h_kv * (cuuint64_t)num_pages};
+      cuuint64_t vs[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)8 * D * 2, (cuuint64_t)P * D * 2};
+      cuuint32_t vb[5] = {64, 8, 2, 2, 1};
+      cuuint32_t ve[5] = {1, 1, 1, 1, 1};
+      if (enc(dst[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(src[i]), vd, vs, vb, ve,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return VA_ERR_CUDA;
+      continue;
+    }
     if (enc(dst[i], fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
             const_cast<void*>(src[i]), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return VA_ERR_CUDA;
+  }
   return VA_OK;
 }
 

@@ -105,9 +105,16 @@ cudaError_t launch_partial_mma(const PartialParams& p, int kernel, int head_dim,
                                int n_items, cudaStream_t stream);
 
 // TMA descriptors of the tensor-core variant: q as [total_qo, h_q, 128] bf16
-// with 64 x G x (128 / G) boxes, 128-byte swizzle; the caches as
-// [num_pages, h_kv, P, 128] with 64 x 16 x 1 x 1 bf16 boxes (128-byte swizzle)
-// or 128 x 16 x 1 x 1 fp8 boxes (no swizzle); zero fill out of bounds.
+// with 64 x G x (128 / G) boxes, 128-byte swizzle.  A bf16 cache
+// [num_pages, h_kv, P, 128] is viewed as the 5-D tensor
+// [num_pages * h_kv][P / 8][2][8][64] (page-and-head, 8-slot group, 64-column
+// half, slot in group, column; the half stride, 128 bytes, is below the slot
+// stride) with 64 x 8 x 2 x 2 x 1 boxes and 128-byte swizzle: one box per 16
+// keys lands as [8-key group][half][8 keys][128 bytes], 8-key groups 2048
+// bytes apart and halves 1024 -- a uniform layout that both MMAs read (K
+// K-major, V MN-major), in one 4 KB copy per 16 keys.  An fp8 cache keeps the
+// 4-D view [num_pages, h_kv, P, 128] with 128 x 16 x 1 x 1 boxes (no swizzle).
+// Zero fill out of bounds.
 struct TcMaps {
   CUtensorMap q, k, v;
 };
