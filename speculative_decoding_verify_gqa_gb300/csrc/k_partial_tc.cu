@@ -663,58 +663,85 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
           }
           return q == 0 ? vis[0] : q == 1 ? vis[1] : q == 2 ? vis[2] : vis[3];
         };
-        // the row's new reference max from this tile's max (log2 units); a
-        // raised max rescales O at once, once PV_{j-1} is done with it (with
-        // a single S buffer it completed before S_j did; a double-buffered S_j
-        // may complete first, so the softmax waits for that PV)
-        float alpha = 1.f, base = 0.f;
-        auto new_max = [&](float mx) {
-          mx *= c;  // c > 0
-          float m_new = m_used;
-          if (mx > m_used + 8.f) m_new = mx;   // also taken when m_used = -inf and mx is finite
-          alpha = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
-          base = m_new == -INFINITY ? 0.f : m_new;
-          if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-            if (C::SBUF == 2) {
-              // PV of the previous S tile (global count ns - 2) has completed
-              if (!__all_sync(0xffffffffu, mbar_wait(bar(B_PV_DONE), (ns - 2) & 1, abort_flag))) live = false;
-              tc_fence_after();
-            }
-            for (int q = 0; q < C::D / 32; ++q) {
-              uint32_t ov[32];
-              tmem_ld32(lane_addr + C::COL_O + q * 32, ov);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-              tmem_st32(lane_addr + C::COL_O + q * 32, ov);
-            }
-          }
-          m_used = m_new;
-        };
-        // P of 32 logits (with visibility word vw) into columns 32 q .. 32 q + 15.
-        // With bf16 caches the scale-and-shift and the sums run two logits per
-        // instruction (fp32x2), which leaves more issue slots to the MMA
-        // issuer sharing this warp's sub-partition (1-1.5 % on GB300); the fp8
-        // variant measured 1.7 % slower that way and keeps scalar fp32.
+        // One pass over the tile, 32 logits at a time (a rolled loop: a small
+        // body keeps every warp's code in the instruction cache).  P is taken
+        // against the row's reference max m_used (log2 units); a chunk whose
+        // max exceeds it by more than 8 raises it by the least multiple of 8
+        // that covers the chunk (the row's first visible chunk sets it to the
+        // chunk max), so every P stays <= 2^8 and every rescale factor is an
+        // exact power of two: the tile's P chunks written so far, the sums and
+        // (once the tile is done) O are multiplied by it.  With bf16 caches
+        // the scale-and-shift and the sums run two logits per instruction
+        // (fp32x2), which leaves more issue slots to the MMA issuer sharing
+        // this warp's sub-partition; the fp8 variant measured slower that way
+        // and keeps scalar fp32.
         float sums[4] = {0.f, 0.f, 0.f, 0.f};  // fp8
         uint64_t sums2[2] = {0ull, 0ull};      // bf16: fp32x2 pairs
-        auto exp_chunk = [&](const uint32_t (&raw)[32], int q, uint32_t vw, bool masked) {
+        float o_scale = 1.f;                   // product of this tile's rescale factors
+#pragma unroll 1
+        for (int q = 0; q < C::KEYS / 32; ++q) {
+          uint32_t raw[32];
+          tmem_ld32(s_addr + q * 32, raw);
+          tmem_wait_ld();
+          float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (full) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
+          } else {
+            const uint32_t vw = vis_word(q);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              raw[2 * i] = ((vw >> (2 * i)) & 1u) ? raw[2 * i] : __float_as_uint(-INFINITY);
+              raw[2 * i + 1] = ((vw >> (2 * i + 1)) & 1u) ? raw[2 * i + 1] : __float_as_uint(-INFINITY);
+              mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
+            }
+          }
+          const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * c;  // c > 0
+          const bool raise = mx > m_used + 8.f;  // also when m_used = -inf and mx is finite
+          if (__any_sync(0xffffffffu, raise)) {
+            float a = 1.f;
+            if (raise) {
+              if (m_used == -INFINITY) {
+                a = 0.f;  // nothing seen yet: every sum so far is 0
+                m_used = mx;
+              } else {
+                const int k = (int)ceilf((mx - m_used - 8.f) * 0.125f);  // >= 1
+                a = k < 15 ? __int_as_float((127 - 8 * k) << 23) : 0.f;   // 2^-8k
+                m_used += 8.f * (float)k;
+              }
+            }
+            if (q > 0) {
+              // this tile's P chunks 0 .. q-1, already in tensor memory
+              tmem_wait_st();
+              for (int q2 = 0; q2 < q; ++q2) {
+                uint32_t pk[16];
+                tmem_ld16(s_addr + 32 * q2, pk);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = FP8 ? scale_f16x2(pk[i], a) : scale_bf16x2(pk[i], a);
+                tmem_st16(s_addr + 32 * q2, pk);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sums[i] *= a;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) sums2[i] = f32x2(f32x2_lo(sums2[i]) * a, f32x2_hi(sums2[i]) * a);
+            o_scale *= a;
+          }
+          // P of these 32 logits into columns 32 q .. 32 q + 15
+          const float base = m_used == -INFINITY ? 0.f : m_used;
           const uint64_t cc = f32x2(c, c), nb = f32x2(-base, -base);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            float s0 = __uint_as_float(raw[2 * i]), s1 = __uint_as_float(raw[2 * i + 1]);
-            if (masked) {
-              s0 = ((vw >> (2 * i)) & 1u) ? s0 : -INFINITY;
-              s1 = ((vw >> (2 * i + 1)) & 1u) ? s1 : -INFINITY;
-            }
             float p0, p1;
             if constexpr (FP8) {
-              p0 = ex2(fmaf(s0, c, -base));
-              p1 = ex2(fmaf(s1, c, -base));
+              p0 = ex2(fmaf(__uint_as_float(raw[2 * i]), c, -base));
+              p1 = ex2(fmaf(__uint_as_float(raw[2 * i + 1]), c, -base));
               sums[i & 3] += p0 + p1;
             } else {
-              const uint64_t x = fma_f32x2(f32x2(s0, s1), cc, nb);
+              const uint64_t x = fma_f32x2(f32x2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])), cc, nb);
               p0 = ex2(f32x2_lo(x));
               p1 = ex2(f32x2_hi(x));
               sums2[i & 1] = add_f32x2(sums2[i & 1], f32x2(p0, p1));
@@ -722,40 +749,28 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
             pk[i] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
           tmem_st16(s_addr + 32 * q, pk);
-        };
-        // Both passes walk the row 32 logits at a time in rolled loops: a
-        // small loop body keeps every warp's code in the instruction cache.
-        {
-          float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-          for (int q = 0; q < C::KEYS / 32; ++q) {
-            uint32_t raw[32];
-            tmem_ld32(s_addr + q * 32, raw);
-            tmem_wait_ld();
-            if (full) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
-            } else {
-              const uint32_t vw = vis_word(q);
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                mxs[i & 3] = fmax3(mxs[i & 3], ((vw >> (2 * i)) & 1u) ? __uint_as_float(raw[2 * i]) : -INFINITY,
-                                   ((vw >> (2 * i + 1)) & 1u) ? __uint_as_float(raw[2 * i + 1]) : -INFINITY);
-            }
-          }
-          new_max(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])));
-#pragma unroll 1
-          for (int q = 0; q < C::KEYS / 32; ++q) {
-            uint32_t raw[32];
-            tmem_ld32(s_addr + q * 32, raw);
-            tmem_wait_ld();
-            exp_chunk(raw, q, full ? 0xffffffffu : vis_word(q), !full);
-          }
         }
         const float sum = FP8 ? (sums[0] + sums[1]) + (sums[2] + sums[3])
                               : (f32x2_lo(sums2[0]) + f32x2_hi(sums2[0])) + (f32x2_lo(sums2[1]) + f32x2_hi(sums2[1]));
-        l = l * alpha + sum;
+        l = l * o_scale + sum;
+        // O holds P_0 V .. P_{j-1} V against the old reference: rescale it once
+        // PV_{j-1} is done with it (with a single S buffer it completed before
+        // S_j did; a double-buffered S_j may complete first, so wait for it)
+        if (j >= 1 && __any_sync(0xffffffffu, o_scale != 1.f)) {
+          if (C::SBUF == 2) {
+            // PV of the previous S tile (global count ns - 2) has completed
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(B_PV_DONE), (ns - 2) & 1, abort_flag))) live = false;
+            tc_fence_after();
+          }
+          for (int q = 0; q < C::D / 32; ++q) {
+            uint32_t ov[32];
+            tmem_ld32(lane_addr + C::COL_O + q * 32, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * o_scale);
+            tmem_st32(lane_addr + C::COL_O + q * 32, ov);
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();

@@ -155,6 +155,17 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
+// Both halves of a packed bf16 / f16 pair times a (a power of two in the
+// softmax, so exact down to the formats' subnormal range).
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float a) {
+  return pack_bf16x2(__uint_as_float(v << 16) * a, __uint_as_float(v & 0xffff0000u) * a);
+}
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t v, float a) {
+  __half2 h = *reinterpret_cast<__half2*>(&v);
+  const float2 f = __half22float2(h);
+  return pack_f16x2(f.x * a, f.y * a);
+}
+
 // bf16x2 -> f16x2 (exact for values inside f16's normal range).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
