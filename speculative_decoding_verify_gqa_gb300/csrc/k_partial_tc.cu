@@ -306,46 +306,97 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       constexpr uint32_t id_s = FP8 ? idesc_f16(C::ROWS, C::KEYS, false)
                                     : idesc_bf16(C::ROWS, C::KEYS, false);
       constexpr uint32_t id_o = FP8 ? idesc_f16(C::ROWS, C::D, true) : idesc_bf16(C::ROWS, C::D, true);
-      // running counts: ring operands (u0), tiles (t0), items (nit); per Q tile
-      // the S tiles issued (ns) and items completed (no)
-      int u0 = 0, t0 = 0, nit = 0, npv = 0;  // npv: PVs issued (one Q tile, double-buffered S)
-      int ns[NQ], no[NQ];
-#pragma unroll
-      for (int qt = 0; qt < NQ; ++qt) ns[qt] = no[qt] = 0;
-      auto k_addr = [&](int j) {
-        return FP8 ? sbase + C::OFF_CONV + ((t0 + j) & 1) * C::OP_BYTES
-                   : sbase + C::OFF_RING + ((u0 + 2 * j) % C::NSLOT) * C::SLOT_BYTES;
-      };
       // K / V operand layouts: widened fp8 in 64-column halves [half][keys][64]
       // (halves KEYS * 128 bytes apart, 8-key groups 1024); bf16 as the TMA
       // boxes land, [8-key group][half][8][64] (groups 2048 apart, halves 1024)
-      constexpr uint32_t KV_SBO = FP8 ? 1024 : 2048;         // 8-key group stride
+      constexpr uint32_t KV_SBO = FP8 ? 1024 : 2048;            // 8-key group stride
       constexpr uint32_t KV_HALF = FP8 ? C::KEYS * 128 : 1024;  // 64-column half stride
-      constexpr uint32_t V_LBO = KV_HALF, V_KK = 2 * KV_SBO;  // PV: 16 keys per MMA
-      auto v_addr = [&](int j) {
-        return FP8 ? sbase + C::OFF_CONV + 2 * C::OP_BYTES
-                   : sbase + C::OFF_RING + ((u0 + 2 * j + 1) % C::NSLOT) * C::SLOT_BYTES;
+      constexpr uint32_t V_LBO = KV_HALF, V_KK = 2 * KV_SBO;    // PV: 16 keys per MMA
+      // tcgen05.mma issue is close to synchronous: whatever this thread runs
+      // between two MMAs (an mbarrier poll costs about as much as an N = 128
+      // MMA) leaves the tensor core idle, and the thread shares its
+      // sub-partition with two softmax warps.  So the loop keeps its
+      // bookkeeping small: Q descriptors are built once, ring slots and
+      // phases advance incrementally, and each batch of MMAs is issued from
+      // one asm block with its descriptors already in registers.  The
+      // descriptor of an operand at shared address x is the base descriptor
+      // + (x >> 4) (every operand lies below 256 KB: the address field never
+      // carries).
+      const uint64_t KD0 = smem_desc_sw128(0, 16, KV_SBO), VD0 = smem_desc_sw128(0, V_LBO, KV_SBO);
+      uint64_t dq[NQ][8];
+#pragma unroll
+      for (int qt = 0; qt < NQ; ++qt)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          dq[qt][kk] = smem_desc_sw128(sbase + C::OFF_Q + qt * C::QT_BYTES + (kk >> 2) * (C::ROWS * 128) + (kk & 3) * 32,
+                                       16, 1024);
+      // S = Q_qt K^T into TMEM column d (K at shared address kx)
+      auto s_batch = [&](uint32_t d, const uint64_t (&aq)[8], uint32_t kx) {
+        const uint64_t dk = KD0 + (uint64_t)(kx >> 4);
+        uint64_t bk[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) bk[kk] = dk + (uint64_t)(((kk >> 2) * KV_HALF + (kk & 3) * 32) >> 4);
+        umma_ss_x8(d, aq, bk, id_s);
       };
-      auto wait_k = [&](int j) {
-        if (FP8) return mbar_wait(bar(B_CK_FULL + ((t0 + j) & 1)), ((t0 + j) >> 1) & 1, abort_flag);
-        const int u = u0 + 2 * j;
-        return mbar_wait(bar(B_FULL + u % C::NSLOT), (u / C::NSLOT) & 1, abort_flag);
+      // O (+)= P V: O at TMEM column d, P at column pc, V at shared address vx
+      auto pv_batch = [&](uint32_t d, uint32_t pc, uint32_t vx, uint32_t acc0) {
+        const uint64_t dv = VD0 + (uint64_t)(vx >> 4);
+        uint64_t bv[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) bv[kk] = dv + (uint64_t)((kk * V_KK) >> 4);
+        umma_ts_x4(d, pc + p_col(0), bv, id_o, acc0);
+        umma_ts_x4(d, pc + p_col(4), bv + 4, id_o, 1u);
       };
-      auto wait_v = [&](int j) {
-        if (FP8) return mbar_wait(bar(B_CV_FULL), (t0 + j) & 1, abort_flag);
-        const int u = u0 + 2 * j + 1;
-        return mbar_wait(bar(B_FULL + u % C::NSLOT), (u / C::NSLOT) & 1, abort_flag);
+      // Ring cursors of the next K and V operands: bf16 operand u = 2 t (K_t)
+      // or 2 t + 1 (V_t) of the running key tile count t sits in slot u % NSLOT,
+      // FULL / EMPTY parity (u / NSLOT) & 1; fp8 K_t in widened buffer t % 2
+      // (parity (t / 2) & 1), V_t in the one V buffer (parity t & 1).
+      struct Cur {
+        int slot;
+        uint32_t par;
+        int t;
       };
-      auto k_free_bar = [&](int j) {
-        return FP8 ? bar(B_CK_FREE + ((t0 + j) & 1)) : bar(B_EMPTY + (u0 + 2 * j) % C::NSLOT);
+      Cur kc{0, 0u, 0}, vc{1, 0u, 0};  // K_0: operand 0, V_0: operand 1 (NSLOT >= 3)
+      auto advance = [&](Cur& cu) {
+        cu.slot += 2;
+        if (cu.slot >= C::NSLOT) {
+          cu.slot -= C::NSLOT;
+          cu.par ^= 1u;
+        }
+        ++cu.t;
       };
-      auto v_free_bar = [&](int j) {
-        return FP8 ? bar(B_CV_FREE) : bar(B_EMPTY + (u0 + 2 * j + 1) % C::NSLOT);
+      auto k_full = [&](const Cur& cu) { return FP8 ? bar(B_CK_FULL + (cu.t & 1)) : bar(B_FULL + cu.slot); };
+      auto k_par = [&](const Cur& cu) -> uint32_t { return FP8 ? (uint32_t)(cu.t >> 1) & 1u : cu.par; };
+      auto k_free = [&](const Cur& cu) { return FP8 ? bar(B_CK_FREE + (cu.t & 1)) : bar(B_EMPTY + cu.slot); };
+      auto k_base = [&](const Cur& cu) -> uint32_t {
+        return FP8 ? sbase + C::OFF_CONV + (cu.t & 1) * C::OP_BYTES : sbase + C::OFF_RING + cu.slot * C::SLOT_BYTES;
       };
-      // The issue loop is this thread's critical path: descriptors are built
-      // once per operand and advanced by adding byte offsets >> 4 to their
-      // start-address field (every operand lies below 256 KB: no carry).
-      const uint64_t dq0 = smem_desc_sw128(sbase + C::OFF_Q, 16, 1024);
+      auto v_full = [&](const Cur& cu) { return FP8 ? bar(B_CV_FULL) : bar(B_FULL + cu.slot); };
+      auto v_par = [&](const Cur& cu) -> uint32_t { return FP8 ? (uint32_t)cu.t & 1u : cu.par; };
+      auto v_free = [&](const Cur& cu) { return FP8 ? bar(B_CV_FREE) : bar(B_EMPTY + cu.slot); };
+      auto v_base = [&](const Cur& cu) -> uint32_t {
+        return FP8 ? sbase + C::OFF_CONV + 2 * C::OP_BYTES : sbase + C::OFF_RING + cu.slot * C::SLOT_BYTES;
+      };
+      // releases of the last K / V operand (the exit waits for them)
+      uint32_t last_k = 0, last_kp = 0, last_v = 0, last_vp = 0;
+      auto free_k = [&]() {
+        umma_commit(k_free(kc));
+        last_k = k_free(kc);
+        last_kp = k_par(kc);
+        advance(kc);
+      };
+      auto free_v = [&]() {
+        umma_commit(v_free(vc));
+        last_v = v_free(vc);
+        last_vp = v_par(vc);
+        advance(vc);
+      };
+      // items (nit); per Q tile the S tiles issued (ns) and items completed
+      // (no); PVs issued (npv, one Q tile with double-buffered S)
+      int nit = 0, npv = 0;
+      int ns[NQ], no[NQ];
+#pragma unroll
+      for (int qt = 0; qt < NQ; ++qt) ns[qt] = no[qt] = 0;
       bool live = true;
       int slot = blockIdx.x, steps = 0;
       for (int i = first_item(slot); live && i >= 0; i = next_item(i, slot, steps)) {
@@ -360,21 +411,16 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
           // of this thread run in issue order).
           for (int j = 0; live && j <= g.n_tiles; ++j) {
             if (j < g.n_tiles) {
-              if (!wait_k(j)) { live = false; break; }
+              if (!mbar_wait(k_full(kc), k_par(kc), abort_flag)) { live = false; break; }
               const int b = ns[0] & 1;
-              const uint64_t dk = smem_desc_sw128(k_addr(j), 16, KV_SBO);
-#pragma unroll
-              for (int kk = 0; kk < C::D / 16; ++kk)
-                umma_bf16(tmem + b * 128, dq0 + (uint64_t)((((kk >> 2) * (C::ROWS * 128)) + (kk & 3) * 32) >> 4),
-                          dk + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4), id_s,
-                          kk > 0 ? 1u : 0u);
+              s_batch(tmem + b * 128, dq[0], k_base(kc));
               umma_commit(bar(B_S_FULL + b));
               ++ns[0];
               if (j == g.n_tiles - 1) umma_commit(bar(B_Q_FREE));  // Q read by this item's last S
-              umma_commit(k_free_bar(j));
+              free_k();
             }
             if (j >= 1) {
-              if (!wait_v(j - 1)) { live = false; break; }
+              if (!mbar_wait(v_full(vc), v_par(vc), abort_flag)) { live = false; break; }
               // the first PV of an item overwrites O: the previous item's
               // epilogue must have read it out
               if (j == 1 && no[0] >= 1 && !mbar_wait(bar(B_O_FREE), (no[0] - 1) & 1, abort_flag)) {
@@ -384,24 +430,19 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
               const int b = npv & 1;  // buffer of S_{j-1} / P_{j-1}
               if (!mbar_wait(bar(B_P_FULL + b), (npv >> 1) & 1, abort_flag)) { live = false; break; }
               tc_fence_after();
-              const uint64_t dv = smem_desc_sw128(v_addr(j - 1), V_LBO, KV_SBO);
-#pragma unroll
-              for (int kk = 0; kk < C::KEYS / 16; ++kk)
-                umma_ts(tmem + C::COL_O, tmem + b * 128 + p_col(kk), dv + (uint64_t)((kk * V_KK) >> 4),
-                        id_o, (j > 1 || kk > 0) ? 1u : 0u);
+              pv_batch(tmem + C::COL_O, tmem + b * 128, v_base(vc), j > 1 ? 1u : 0u);
               umma_commit(bar(B_PV_DONE));
               if (j == g.n_tiles) umma_commit(bar(B_O_DONE));
-              umma_commit(v_free_bar(j - 1));
+              free_v();
               ++npv;
             }
           }
         } else {
           for (int j = 0; live && j <= g.n_tiles; ++j) {
             // step j: PV of tile j - 1 and S of tile j, Q tile by Q tile
-            if (j < g.n_tiles && !wait_k(j)) { live = false; break; }
-            if (j >= 1 && !wait_v(j - 1)) { live = false; break; }
-            const uint64_t dk = j < g.n_tiles ? smem_desc_sw128(k_addr(j), 16, KV_SBO) : 0;
-            const uint64_t dv = j >= 1 ? smem_desc_sw128(v_addr(j - 1), V_LBO, KV_SBO) : 0;
+            if (j < g.n_tiles && !mbar_wait(k_full(kc), k_par(kc), abort_flag)) { live = false; break; }
+            if (j >= 1 && !mbar_wait(v_full(vc), v_par(vc), abort_flag)) { live = false; break; }
+            const uint32_t kx = k_base(kc), vx = v_base(vc);
 #pragma unroll
             for (int qt = 0; qt < NQ; ++qt) {
               if (qt >= g.nq) break;
@@ -419,48 +460,31 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
                   break;
                 }
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < C::KEYS / 16; ++kk)
-                  umma_ts(ts + C::COL_O, ts + p_col(kk), dv + (uint64_t)((kk * V_KK) >> 4), id_o,
-                          (j > 1 || kk > 0) ? 1u : 0u);
+                pv_batch(ts + C::COL_O, ts, vx, j > 1 ? 1u : 0u);
                 if (j == g.n_tiles) umma_commit(bar(B_O_DONE + qt));
               }
               if (j < g.n_tiles) {
-                const uint64_t dq = dq0 + (uint64_t)(qt * (C::QT_BYTES >> 4));
-#pragma unroll
-                for (int kk = 0; kk < C::D / 16; ++kk)
-                  umma_bf16(ts, dq + (uint64_t)((((kk >> 2) * (C::ROWS * 128)) + (kk & 3) * 32) >> 4),
-                            dk + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4), id_s,
-                            kk > 0 ? 1u : 0u);
+                s_batch(ts, dq[qt], kx);
                 umma_commit(bar(B_S_FULL + qt));
                 ++ns[qt];
               }
             }
             if (!live) break;
             if (j == g.n_tiles - 1) umma_commit(bar(B_Q_FREE));  // Q read by this item's last S
-            if (j >= 1) umma_commit(v_free_bar(j - 1));
-            if (j < g.n_tiles) umma_commit(k_free_bar(j));
+            if (j >= 1) free_v();
+            if (j < g.n_tiles) free_k();
           }
         }
         if (!live) break;
 #pragma unroll
         for (int qt = 0; qt < NQ; ++qt)
           if (qt < g.nq) ++no[qt];
-        u0 += 2 * g.n_tiles;
-        t0 += g.n_tiles;
         ++nit;
       }
       // the last slot releases land before the CTA's shared memory goes away
-      if (live && !*abort_flag && t0 >= 1) {
-        const int jt = t0 - 1;  // the CTA's last tile (running count)
-        if (FP8) {
-          mbar_wait(bar(B_CV_FREE), jt & 1, abort_flag);
-          mbar_wait(bar(B_CK_FREE + (jt & 1)), (jt >> 1) & 1, abort_flag);
-        } else {
-          const int uk = 2 * jt, uv = 2 * jt + 1;
-          mbar_wait(bar(B_EMPTY + uv % C::NSLOT), (uv / C::NSLOT) & 1, abort_flag);
-          mbar_wait(bar(B_EMPTY + uk % C::NSLOT), (uk / C::NSLOT) & 1, abort_flag);
-        }
+      if (live && !*abort_flag && kc.t >= 1) {
+        mbar_wait(last_v, last_vp, abort_flag);
+        mbar_wait(last_k, last_kp, abort_flag);
       }
     }
   } else if (FP8 && (warp == 2 || warp == 3 || warp >= C::CONV_WARP0 + 2)) {

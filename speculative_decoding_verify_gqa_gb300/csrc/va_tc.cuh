@@ -135,6 +135,41 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Eight MMAs D (+)= A_k B_k^T, k = 0..7 (one K = 128 contraction of 16-bit
+// operands from shared-memory descriptors), issued back to back from one asm
+// block: the first overwrites D, the rest accumulate.
+__device__ __forceinline__ void umma_ss_x8(uint32_t d, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                           uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %17, %17;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, 1;\n}\n" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
+      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc)
+      : "memory");
+}
+// Four MMAs D += A_k B_k, k = 0..3, A from tensor memory: 16 keys each, packed
+// two per column at columns a, a + 8, a + 32, a + 40 (the P layout that puts
+// the P of 32 logits over the first half of their own S columns); the first
+// accumulates only if acc0 != 0.
+__device__ __forceinline__ void umma_ts_x4(uint32_t d, uint32_t a, const uint64_t* b, uint32_t idesc,
+                                           uint32_t acc0) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b32 a1, a2, a3;\n setp.ne.b32 p, %6, 0;\n"
+      " add.u32 a1, %1, 8;\n add.u32 a2, %1, 32;\n add.u32 a3, %1, 40;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %7, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %3, %7, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], %4, %7, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], %5, %7, 1;\n}\n" ::"r"(d),
+      "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc0), "r"(idesc)
+      : "memory");
+}
 // Arrive once on the mbarrier when every MMA this thread issued so far is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
