@@ -181,6 +181,16 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
   };
   auto decode = [&](int i) { return decode_item<C::BLOCK_ROWS, C::ROWS, C::KEYS>(p, i); };
 
+  // While the previous kernel may still run: fetch the three TMA descriptors
+  // (kernel parameters) and this CTA's first work item (uploaded with the
+  // plan, never written by a kernel) towards the SM, so the first loads after
+  // the dependency wait do not each pay a round trip to memory.
+  if (tid == 0) {
+    tma_prefetch_desc(&maps.q);
+    tma_prefetch_desc(&maps.k);
+    tma_prefetch_desc(&maps.v);
+    if ((int)blockIdx.x < p.n_items) prefetch_l1(p.items + blockIdx.x);
+  }
   if (tid == 0) {
     mbar_init(bar(B_Q), 1);
     mbar_init(bar(B_Q_READY), 4 * NQ);
