@@ -299,44 +299,58 @@ class Bench:
 
     def e2e(self, steps):
         """End to end through the public API: pinned host inputs copied in,
-        plan on the host, append, attention, out / LSE copied back, every step."""
+        plan on the host, append, attention, out / LSE copied back, every step.
+        The step's inputs sit in one pinned staging buffer and go over in one
+        copy (each at a 256-byte offset, the device side carved the same way);
+        out and LSE share one device buffer and come back in one copy."""
         torch, va, wl = self.torch, self.va, self.wl
 
-        def pin(t):
-            return t.cpu().pin_memory()
-
-        h = dict(q=pin(self.q), k_new=pin(self.k_new.view(torch.uint8)),
-                 v_new=pin(self.v_new.view(torch.uint8)), kv_indptr=pin(self.kv_indptr),
-                 kv_indices=pin(self.kv_indices), last_page_len=pin(self.last_page_len),
-                 qo_indptr=pin(self.qo_indptr))
+        src = dict(q=self.q, k_new=self.k_new, v_new=self.v_new, kv_indptr=self.kv_indptr,
+                   kv_indices=self.kv_indices, last_page_len=self.last_page_len,
+                   qo_indptr=self.qo_indptr)
         if self.mask is not None:
-            h["mask"], h["mask_indptr"] = pin(self.mask), pin(self.mask_indptr)
-        d = {k: torch.empty_like(v, device=self.dev) for k, v in h.items()}
-        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        lse_h = torch.empty(self.lse.shape, dtype=self.lse.dtype).pin_memory()
-        h2d = sum(v.numel() * v.element_size() for v in h.values())
-        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
-        np_tables = {k: h[k].numpy() for k in ("kv_indptr", "qo_indptr", "last_page_len")}
-        np_mask_indptr = h["mask_indptr"].numpy() if "mask_indptr" in h else None
+            src["mask"], src["mask_indptr"] = self.mask, self.mask_indptr
+        offs, total = {}, 0
+        for k, t in src.items():
+            offs[k] = total
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+        stage_d = torch.empty(total, dtype=torch.uint8, device=self.dev)
+
+        def carve(buf, k):
+            t = src[k]
+            n = t.numel() * t.element_size()
+            return buf[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+
+        for k, t in src.items():
+            carve(stage_h, k).copy_(t.cpu())
+        d = {k: carve(stage_d, k) for k in src}
+        n_out = self.out.numel() * self.out.element_size()
+        n_lse = self.lse.numel() * self.lse.element_size()
+        lse_off = (n_out + 255) // 256 * 256
+        res_d = torch.empty(lse_off + n_lse, dtype=torch.uint8, device=self.dev)
+        res_h = torch.empty(lse_off + n_lse, dtype=torch.uint8).pin_memory()
+        out_d = res_d[:n_out].view(self.out.dtype).view(self.out.shape)
+        lse_d = res_d[lse_off:].view(self.lse.dtype).view(self.lse.shape)
+        h2d, d2h = int(total), int(lse_off + n_lse)
+        hv = {k: carve(stage_h, k).numpy() for k in ("kv_indptr", "qo_indptr", "last_page_len")}
+        np_mask_indptr = carve(stage_h, "mask_indptr").numpy() if self.mask is not None else None
         ws = self.plan.workspace
 
         def one(i):
-            for k in h:
-                d[k].copy_(h[k], non_blocking=True)
-            plan = va.verify_attn_plan(np_tables["kv_indptr"], np_tables["qo_indptr"],
-                                       np_tables["last_page_len"], np_mask_indptr, wl.h_q,
-                                       wl.h_kv, wl.d, wl.page_size, kv_dtype=wl.kv_dtype,
-                                       workspace=ws, device=self.dev, **self.plan_opts)
+            stage_d.copy_(stage_h, non_blocking=True)
+            plan = va.verify_attn_plan(hv["kv_indptr"], hv["qo_indptr"], hv["last_page_len"],
+                                       np_mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                       kv_dtype=wl.kv_dtype, workspace=ws, device=self.dev,
+                                       **self.plan_opts)
             kc, vc = self.pools[i % self.n_copies]
-            va.paged_kv_append(d["k_new"].view(self.kvd), d["v_new"].view(self.kvd),
-                               d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
-                               d["last_page_len"], kc, vc)
+            va.paged_kv_append(d["k_new"], d["v_new"], d["qo_indptr"], d["kv_indptr"],
+                               d["kv_indices"], d["last_page_len"], kc, vc)
             va.verify_attn_run(d["q"], kc, vc, d["kv_indptr"], d["kv_indices"],
                                d["last_page_len"], d["qo_indptr"], d.get("mask"),
                                d.get("mask_indptr"), plan, sm_scale=wl.sm_scale,
-                               k_scale=wl.k_scale, v_scale=wl.v_scale, out=self.out, lse=self.lse)
-            out_h.copy_(self.out, non_blocking=True)
-            lse_h.copy_(self.lse, non_blocking=True)
+                               k_scale=wl.k_scale, v_scale=wl.v_scale, out=out_d, lse=lse_d)
+            res_h.copy_(res_d, non_blocking=True)
             torch.cuda.synchronize()
 
         for i in range(5):
@@ -345,8 +359,8 @@ class Bench:
         for i in range(steps):
             one(i)
         dt_s = (time.perf_counter() - t0) / steps
-        return dict(value=wl.total_qo / dt_s, unit="tokens/s", h2d_bytes_per_step=int(h2d),
-                    d2h_bytes_per_step=int(d2h), ms_per_step=dt_s * 1e3)
+        return dict(value=wl.total_qo / dt_s, unit="tokens/s", h2d_bytes_per_step=h2d,
+                    d2h_bytes_per_step=d2h, ms_per_step=dt_s * 1e3)
 
     def plan_us(self, n=50):
         va, wl = self.va, self.wl
