@@ -65,13 +65,14 @@ struct TcCfg {
   static constexpr int RAW_BYTES = KEYS * D;             // fp8 K (or V) tile [keys][128 B]
   static constexpr int SLOT_BYTES = FP8 ? RAW_BYTES : OP_BYTES;
   static constexpr int CONV_BYTES = FP8 ? 3 * OP_BYTES : 0;  // widened K (two) and V (one)
-  static constexpr int RING_AVAIL = 227 * 1024 - 512 - Q_BYTES - CONV_BYTES;
+  static constexpr int BAR_BYTES = 1024;                 // barriers, TMEM address, item queue
+  static constexpr int RING_AVAIL = 227 * 1024 - BAR_BYTES - Q_BYTES - CONV_BYTES;
   static constexpr int NSLOT = RING_AVAIL / SLOT_BYTES > 8 ? 8 : RING_AVAIL / SLOT_BYTES;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_CONV = OFF_Q + Q_BYTES;
   static constexpr int OFF_RING = OFF_CONV + CONV_BYTES;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * SLOT_BYTES;
-  static constexpr int SMEM = OFF_BAR + 512;              // + barriers, TMEM address, abort flag
+  static constexpr int SMEM = OFF_BAR + BAR_BYTES;
   // S / P buffers per Q tile: one Q tile double-buffers S, so S_{j+1} is
   // computed while the softmax works on S_j; two Q tiles fill tensor memory
   // with one buffer each and alternate instead.
@@ -90,8 +91,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 // buffer when one Q tile double-buffers S)
 enum { B_Q = 0, B_Q_READY = 1, B_Q_FREE = 2, B_FULL = 3, B_EMPTY = 11, B_CK_FULL = 19,
        B_CK_FREE = 21, B_CV_FULL = 23, B_CV_FREE = 24, B_S_FULL = 25, B_P_FULL = 27, B_O_DONE = 29,
-       B_O_FREE = 31, B_PV_DONE = 33, B_COUNT = 34 };
-static_assert(8 * B_COUNT + 8 <= 512, "barrier area");
+       B_O_FREE = 31, B_PV_DONE = 33, B_GQ_FULL = 34, B_GQ_FREE = 38, B_COUNT = 42 };
+constexpr int kGeoQueue = 4;  // entries of the shared item-geometry queue (B_GQ_FULL / B_GQ_FREE + e)
 
 // Instruction descriptor, kind::f16 with f16 A and B (fp32 accumulator).
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
@@ -114,9 +115,16 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 // One work item's geometry, as every role of the CTA decodes it.
 struct ItemGeo {
-  int b, h, row0, nrows, lo, hi, part_row, qo0, L, pg0, prefix, n_tiles, nq;
+  int b, h, row0, nrows, lo, hi, part_row, qo0, L, pg0, prefix, n_tiles, nq, moff;
   bool ok;
 };
+// One entry of the item-geometry queue: the producer decodes each item of the
+// CTA's chain once and posts it; end marks the end of the chain.
+struct GeoSlot {
+  ItemGeo g;
+  int end;
+};
+static_assert(8 * B_COUNT + 16 + kGeoQueue * sizeof(GeoSlot) <= 1024, "barrier area");
 
 template <int BLOCK_ROWS, int ROWS, int KEYS>
 __device__ __forceinline__ ItemGeo decode_item(const PartialParams& p, int i) {
@@ -141,6 +149,7 @@ __device__ __forceinline__ ItemGeo decode_item(const PartialParams& p, int i) {
          g.row0 % BLOCK_ROWS == 0 && (long long)g.row0 + g.nrows <= (long long)p.group * g.L &&
          g.lo >= 0 && g.lo % 16 == 0 && g.lo < g.hi && g.hi <= kv_len;
   g.n_tiles = g.ok ? (g.hi - g.lo + KEYS - 1) / KEYS : 0;
+  g.moff = g.ok && p.mask ? p.mask_indptr[g.b] : 0;
   g.nq = (g.nrows + ROWS - 1) / ROWS;  // live Q tiles (1 .. NQ)
   return g;
 }
@@ -165,6 +174,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
   auto bar = [&](int i) { return bar0 + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 8 * B_COUNT + 4);
+  GeoSlot* geoq = reinterpret_cast<GeoSlot*>(smem + C::OFF_BAR + 8 * B_COUNT + 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.group;
@@ -180,6 +190,28 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     return first_item(slot);
   };
   auto decode = [&](int i) { return decode_item<C::BLOCK_ROWS, C::ROWS, C::KEYS>(p, i); };
+  // The producer walks the chain and decodes each item (a few dependent
+  // global loads) once; the MMA issuer, the softmax and converter warps read
+  // the decoded geometry from a small shared queue, so none of them stalls
+  // on those loads between items.
+  constexpr int GQ_USERS = 1 + 4 * NQ + C::CONV_WARPS;
+  auto take_geo_thread = [&](int k, ItemGeo& g) -> bool {  // false: end of chain (or timeout)
+    const int e = k % kGeoQueue;
+    if (!mbar_wait(bar(B_GQ_FULL + e), (k / kGeoQueue) & 1, abort_flag)) return false;
+    g = geoq[e].g;
+    const int end = geoq[e].end;
+    mbar_arrive(bar(B_GQ_FREE + e));
+    return !end;
+  };
+  auto take_geo_warp = [&](int k, ItemGeo& g) -> bool {
+    const int e = k % kGeoQueue;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar(B_GQ_FULL + e), (k / kGeoQueue) & 1, abort_flag))) return false;
+    g = geoq[e].g;
+    const int end = geoq[e].end;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(B_GQ_FREE + e));
+    return !end;
+  };
 
   // While the previous kernel may still run: fetch the three TMA descriptors
   // (kernel parameters) and this CTA's first work item (uploaded with the
@@ -214,6 +246,10 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       mbar_init(bar(B_O_FREE + qt), 4);
     }
     mbar_init(bar(B_PV_DONE), 1);
+    for (int e = 0; e < kGeoQueue; ++e) {
+      mbar_init(bar(B_GQ_FULL + e), 1);
+      mbar_init(bar(B_GQ_FREE + e), GQ_USERS);
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -237,9 +273,24 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       int u = 0;
       bool live = true;
       constexpr int NG = C::KEYS / 16;
+      int k = 0;
+      auto post = [&](const ItemGeo& g, int end) -> bool {
+        const int e = k % kGeoQueue;
+        if (k >= kGeoQueue && !mbar_wait(bar(B_GQ_FREE + e), ((k / kGeoQueue) - 1) & 1, abort_flag))
+          return false;
+        geoq[e].g = g;
+        geoq[e].end = end;
+        mbar_arrive(bar(B_GQ_FULL + e));  // release: the entry is visible to the waiters
+        ++k;
+        return true;
+      };
       int slot = blockIdx.x, steps = 0;
       for (int i = first_item(slot); live && i >= 0; i = next_item(i, slot, steps)) {
         const ItemGeo g = decode(i);
+        if (!post(g, 0)) {
+          live = false;
+          break;
+        }
         if (!g.ok) {
           bad_item = 1;
           continue;
@@ -307,6 +358,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         }
         ++nit;
       }
+      if (live) post(ItemGeo{}, 1);  // end of the chain
       if (bad) atomicOr(p.status, VA_DEV_BAD_PAGE);
       if (bad_item) atomicOr(p.status, VA_DEV_BAD_TABLE);
     }
@@ -408,9 +460,8 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
 #pragma unroll
       for (int qt = 0; qt < NQ; ++qt) ns[qt] = no[qt] = 0;
       bool live = true;
-      int slot = blockIdx.x, steps = 0;
-      for (int i = first_item(slot); live && i >= 0; i = next_item(i, slot, steps)) {
-        const ItemGeo g = decode(i);
+      ItemGeo g;
+      for (int k = 0; live && take_geo_thread(k, g); ++k) {
         if (!g.ok) continue;
         if (!mbar_wait(bar(FP8 ? B_Q_READY : B_Q), nit & 1, abort_flag)) break;
         if constexpr (C::SBUF == 2) {
@@ -505,9 +556,8 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     constexpr int NCT = 32 * C::CONV_WARPS;
     int u0 = 0, t0 = 0;
     bool go = true;
-    int slot = blockIdx.x, steps = 0;
-    for (int it_i = first_item(slot); go && it_i >= 0; it_i = next_item(it_i, slot, steps)) {
-      const ItemGeo g = decode(it_i);
+    ItemGeo g;
+    for (int k = 0; go && take_geo_warp(k, g); ++k) {
       if (!g.ok) continue;
       for (int i = 0; go && i <= g.n_tiles; ++i) {
         for (int v = 0; v < 2; ++v) {
@@ -568,9 +618,8 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     const float c = p.scale_log2;
     int ns = 0, no = 0, nit = 0, u0 = 0;            // S tiles seen, items done, items, ring base
     bool live = true;
-    int slot = blockIdx.x, steps = 0;
-    for (int it_i = first_item(slot); live && it_i >= 0; it_i = next_item(it_i, slot, steps)) {
-      const ItemGeo g = decode(it_i);
+    ItemGeo g;
+    for (int k = 0; live && take_geo_warp(k, g); ++k) {
       if (!g.ok) continue;
       const bool mine = qt < g.nq;
       if (FP8) {
@@ -605,7 +654,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       const int br = qt * C::ROWS + r;              // row of the block
       const bool row_ok = br < g.nrows;
       const int t = (g.row0 + br) / G;              // draft token of the row
-      const int moff = p.mask ? p.mask_indptr[g.b] : 0;
+      const int moff = g.moff;
       const int L = g.L, prefix = g.prefix, hi = g.hi;
       float m_used = -INFINITY;                     // in units of s * c (log2 domain)
       float l = 0.f;
