@@ -93,12 +93,12 @@ def bf16_half_spacing(x):
     return np.where(ax > 0, np.exp2(e - 8), 0.0)
 
 
-def compare(wl, out, lse, rows=None, caches=None, nthreads=None, strict=False):
+def compare(wl, out, lse, rows=None, caches=None, nthreads=None, strict=False, out_tol=OUT_TOL):
     """Errors of the device result (all rows, or the flat rows given) against
     the oracle.  Asserts -inf agreement, |lse - oracle| <= 1e-3 and
-    |out - oracle| <= 1e-2 + half the bf16 spacing at the oracle value (the
-    output is bf16: where |out| >= 4 that spacing alone exceeds 1e-2);
-    strict=True asserts the plain 1e-2 on every element."""
+    |out - oracle| <= out_tol (1e-2 unless given) + half the bf16 spacing at
+    the oracle value (the output is bf16: where |out| >= 4 that spacing alone
+    exceeds 1e-2); strict=True asserts the plain out_tol on every element."""
     o, l = host_out(out, lse, wl.d)
     ref_o, ref_l = oracle.verify_attn_workload(wl, rows=rows, caches=caches, nthreads=nthreads)
     if rows is not None:
@@ -111,10 +111,10 @@ def compare(wl, out, lse, rows=None, caches=None, nthreads=None, strict=False):
     err_o = float(diff.max()) if o.size else 0.0
     err_l = float(np.abs(l[fin] - ref_l[fin]).max()) if fin.any() else 0.0
     if strict:
-        assert err_o <= OUT_TOL, "max |out - oracle| = %g" % err_o
+        assert err_o <= out_tol, "max |out - oracle| = %g" % err_o
     else:
-        excess = diff - (OUT_TOL + bf16_half_spacing(ref_o))
+        excess = diff - (out_tol + bf16_half_spacing(ref_o))
         assert o.size == 0 or excess.max() <= 0, \
-            "max |out - oracle| = %g exceeds 1e-2 + bf16 half-spacing" % err_o
+            "max |out - oracle| = %g exceeds %g + bf16 half-spacing" % (err_o, out_tol)
     assert err_l <= LSE_TOL, "max |lse - oracle| = %g" % err_l
     return err_o, err_l

@@ -429,3 +429,37 @@ def test_tcgen05_long_item_chains_match_oracle(va, num_sms, kernel, case):
     assert hd["n_items"] > 2 * hd["n_ctas"]
     assert va.verify_attn_device_status(plan) == 0
     compare(wl, out, lse)
+
+
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4], ids=["mma64", "mma128", "tc128", "tc256"])
+@pytest.mark.parametrize("case", [
+    dict(mask="causal", value_std=3.0),
+    dict(mask="tree", value_std=3.0),
+    dict(mask="tree", value_std=3.0, kv_dtype=synthetic.FP8),
+    dict(mask="causal", value_std=5.0),
+], ids=["causal_std3", "tree_std3", "fp8_tree_std3", "causal_std5"])
+def test_large_logits_match_oracle(va, kernel, case):
+    """Logits with a standard deviation of 9 to 25 (q, k, v drawn with
+    standard deviation 3 or 5): a row's running max keeps rising by far more
+    than 2^8 from one 32-key chunk to the next, inside a key tile and from
+    tile to tile, so every rescale path of the online softmax runs (the
+    tcgen05 kernel's in-tile rescale of P already written to tensor memory,
+    its rescale of O, a first visible chunk after fully masked ones) and
+    must still match the fp64 oracle.  The output bound scales with the
+    values: P is rounded to 16 bits (relative error <= 2^-8 for bf16, 2^-11
+    for the fp8 variant's f16) before P V while the row sum keeps fp32, so
+    |out - oracle| <= 2^-8 max|v| + fp32 rounding; a missing or wrong
+    rescale is off by a factor 2^8 or more on some weights instead."""
+    wl = synthetic.make_custom(batch=3, h_q=16, h_kv=2, d=128,
+                               prefix=("fixed", [700, 300, 1500]),
+                               qo=("fixed", [17, 40, 9]), seed=53, **case)
+    v = oracle.decode_e4m3(wl.v_tok) * wl.v_scale if wl.kv_dtype == synthetic.FP8 \
+        else oracle.decode_bf16(wl.v_tok)
+    tol = 2.0 ** -8 * float(np.abs(v).max()) + 1e-3
+    dw = DeviceWorkload(wl)
+    for splits in (1, 0):
+        out, lse, plan = dw.run(kernel=kernel, max_splits=splits)
+        torch.cuda.synchronize()
+        assert plan.header()["kernel"] == kernel
+        assert va.verify_attn_device_status(plan) == 0
+        compare(wl, out, lse, out_tol=tol)
