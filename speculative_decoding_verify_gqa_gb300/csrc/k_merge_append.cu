@@ -27,6 +27,12 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) 
   grid_dependency_wait();  // the partials come from the preceding split kernel
   grid_dependents_launch();  // the next kernel may be scheduled; it waits for our completion
   if (r >= it.nrows) return;
+  // a merge list left in the workspace by another plan: nothing outside this
+  // call's tables and partial rows is read or written
+  if (it.b < 0 || it.b >= p.batch || it.h < 0 || it.h >= p.h_kv || it.part_row0 < 0 || it.nsplit < 1 ||
+      (long long)it.part_row0 + (long long)it.nsplit * it.nrows > p.part_rows || it.row0 < 0)
+    return;
+  if ((it.row0 + r) / p.group >= p.qo_indptr[it.b + 1] - p.qo_indptr[it.b]) return;
   const float* lse_base = p.part_lse + it.part_row0 + r;
   float m = -INFINITY, den = 0.f;
   float acc[V];

@@ -66,11 +66,14 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
   const int b = it.b, h = it.h;
   const int G = p.group;
 
-  // Request geometry, from the device tables the caller passed.
-  const int qo0 = p.qo_indptr[b];
-  const int L = p.qo_indptr[b + 1] - qo0;
-  const int pg0 = p.kv_indptr[b];
-  const int npg = p.kv_indptr[b + 1] - pg0;
+  // Request geometry, from the device tables the caller passed (nothing is
+  // read for a work item that names a request or head outside this call's
+  // tables, as one left in the workspace by another plan may).
+  const bool idx_ok = b >= 0 && b < p.batch && h >= 0 && h < p.h_kv;
+  const int qo0 = idx_ok ? p.qo_indptr[b] : 0;
+  const int L = idx_ok ? p.qo_indptr[b + 1] - qo0 : -1;
+  const int pg0 = idx_ok ? p.kv_indptr[b] : 0;
+  const int npg = idx_ok ? p.kv_indptr[b + 1] - pg0 : -1;
   const int lpl = npg > 0 ? p.last_page_len[b] : 1;
   const long long kv_len_ll = npg > 0 ? (long long)(npg - 1) * p.page_size + lpl : 0;
   const int kv_len = (int)kv_len_ll;
@@ -78,7 +81,8 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
   const bool ok = L >= 0 && npg >= 0 && lpl >= 1 && lpl <= p.page_size && prefix >= 0 &&
                   it.row0 >= 0 && it.nrows > 0 && it.nrows <= C::BM &&
                   (long long)it.row0 + it.nrows <= (long long)G * L && it.kv_lo >= 0 &&
-                  it.kv_lo < it.kv_hi && it.kv_hi <= kv_len && kv_len_ll <= 0x7fffffffLL;
+                  it.kv_lo < it.kv_hi && it.kv_hi <= kv_len && kv_len_ll <= 0x7fffffffLL &&
+                  (it.part_row < 0 || (long long)it.part_row + it.nrows <= p.part_rows);
   const bool clustered = p.cluster > 1;
   if (!ok) {
     if (tid == 0) atomicOr(p.status, VA_DEV_BAD_TABLE);

@@ -137,17 +137,21 @@ __device__ __forceinline__ ItemGeo decode_item(const PartialParams& p, int i) {
   g.lo = it.kv_lo;
   g.hi = it.kv_hi;
   g.part_row = it.part_row;
-  g.qo0 = p.qo_indptr[g.b];
-  g.L = p.qo_indptr[g.b + 1] - g.qo0;
-  g.pg0 = p.kv_indptr[g.b];
-  const int npg = p.kv_indptr[g.b + 1] - g.pg0;
+  // a work list left in the workspace by another plan may name requests
+  // past this call's tables: nothing is read for those
+  const bool idx_ok = g.b >= 0 && g.b < p.batch && g.h >= 0 && g.h < p.h_kv;
+  g.qo0 = idx_ok ? p.qo_indptr[g.b] : 0;
+  g.L = idx_ok ? p.qo_indptr[g.b + 1] - g.qo0 : -1;
+  g.pg0 = idx_ok ? p.kv_indptr[g.b] : 0;
+  const int npg = idx_ok ? p.kv_indptr[g.b + 1] - g.pg0 : -1;
   const int lpl = npg > 0 ? p.last_page_len[g.b] : 1;
   const long long kv_len = npg > 0 ? (long long)(npg - 1) * p.page_size + lpl : 0;
   g.prefix = (int)kv_len - g.L;
   g.ok = g.L >= 0 && npg >= 0 && lpl >= 1 && lpl <= p.page_size && kv_len <= 0x7fffffffLL &&
          g.prefix >= 0 && g.row0 >= 0 && g.nrows > 0 && g.nrows <= BLOCK_ROWS &&
          g.row0 % BLOCK_ROWS == 0 && (long long)g.row0 + g.nrows <= (long long)p.group * g.L &&
-         g.lo >= 0 && g.lo % 16 == 0 && g.lo < g.hi && g.hi <= kv_len;
+         g.lo >= 0 && g.lo % 16 == 0 && g.lo < g.hi && g.hi <= kv_len &&
+         (g.part_row < 0 || (long long)g.part_row + g.nrows <= p.part_rows);
   g.n_tiles = g.ok ? (g.hi - g.lo + KEYS - 1) / KEYS : 0;
   g.moff = g.ok && p.mask ? p.mask_indptr[g.b] : 0;
   g.nq = (g.nrows + ROWS - 1) / ROWS;  // live Q tiles (1 .. NQ)

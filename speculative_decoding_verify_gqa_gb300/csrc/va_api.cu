@@ -107,6 +107,8 @@ PartialParams make_partial(const void* q, const void* k_cache, const void* v_cac
   p.part_out = reinterpret_cast<float*>(ws + hd->off_part_out);
   p.part_lse = reinterpret_cast<float*>(ws + hd->off_part_lse);
   p.status = reinterpret_cast<int*>(ws + hd->off_status);
+  p.batch = hd->batch;
+  p.part_rows = hd->part_rows;
   p.h_q = hd->h_q;
   p.h_kv = hd->h_kv;
   p.group = hd->group;
@@ -319,7 +321,10 @@ int verify_attn_merge(const int32_t* qo_indptr, int num_qo_heads, int num_kv_hea
   m.qo_indptr = qo_indptr;
   m.out = out;
   m.lse = lse;
+  m.batch = hd->batch;
+  m.part_rows = hd->part_rows;
   m.h_q = hd->h_q;
+  m.h_kv = hd->h_kv;
   m.group = hd->group;
   cudaError_t e = launch_merge(m, hd->head_dim, hd->n_merge, hd->block_rows,
                                static_cast<cudaStream_t>(stream));

@@ -26,6 +26,8 @@ struct PartialParams {
   float* part_out;            // [part_rows, D]
   float* part_lse;            // [part_rows]
   int* status;                // device status word
+  int batch;                  // requests in the plan: a work item's b must be below it
+  int64_t part_rows;          // partial rows in the workspace: a split item's rows lie below
   int h_q, h_kv, group, page_size, log2_page, num_pages;
   float scale_log2;           // sm_scale * k_scale * log2(e)
   float scale_nat;            // sm_scale * k_scale
@@ -43,7 +45,8 @@ struct MergeParams {
   const int32_t* qo_indptr;
   void* out;
   float* lse;                 // nullable
-  int h_q, group;
+  int64_t part_rows;          // partial rows in the workspace
+  int batch, h_q, h_kv, group;
 };
 
 struct AppendParams {

@@ -463,3 +463,37 @@ def test_large_logits_match_oracle(va, kernel, case):
         assert plan.header()["kernel"] == kernel
         assert va.verify_attn_device_status(plan) == 0
         compare(wl, out, lse, out_tol=tol)
+
+
+@pytest.mark.parametrize("kernel", [2, 3, 4], ids=["mma128", "tc128", "tc256"])
+def test_work_list_of_another_plan_is_flagged_not_read(va, kernel):
+    """A workspace whose work list was overwritten by a later plan for a
+    larger batch, then run with the earlier plan: the kernels must not index
+    the call's tables with the foreign requests (they flag the items as a bad
+    table instead), and the merge skips them.  Every index a kernel takes
+    from the work list is checked against this call's plan before use, so
+    the run is safe whatever the list holds."""
+    small = synthetic.make_custom(batch=2, h_q=8, h_kv=2, d=128, prefix=("fixed", [300, 200]),
+                                  qo=("fixed", [5, 9]), seed=61)
+    # later requests longer: the longest-first list starts with requests >= 2
+    big = synthetic.make_custom(batch=8, h_q=8, h_kv=2, d=128,
+                                prefix=("fixed", [200 * (i + 1) for i in range(8)]),
+                                qo=("fixed", [7] * 8), seed=62, with_values=False)
+    dw = DeviceWorkload(small)
+    opts = dict(kernel=kernel, num_sms=8)
+    args_big = (big.kv_indptr, big.qo_indptr, big.last_page_len, big.mask_indptr, big.h_q, big.h_kv,
+                big.d, big.page_size)
+    args_small = (small.kv_indptr, small.qo_indptr, small.last_page_len, small.mask_indptr,
+                  small.h_q, small.h_kv, small.d, small.page_size)
+    # one workspace large enough for both plans, so that both upload into it
+    need = max(va.verify_attn_plan_host(*args_big, **opts).workspace_bytes,
+               va.verify_attn_plan_host(*args_small, **opts).workspace_bytes)
+    ws = torch.empty(need, dtype=torch.uint8, device=dw.dev)
+    plan_small = va.verify_attn_plan(*args_small, workspace=ws, device=dw.dev, **opts)
+    plan_big = va.verify_attn_plan(*args_big, workspace=ws, device=dw.dev, **opts)
+    assert plan_small.workspace.data_ptr() == plan_big.workspace.data_ptr() == ws.data_ptr()
+    items = plan_big.items()
+    assert (items[:plan_small.header()["n_items"], 0] >= small.batch).any()
+    dw.run(plan=plan_small)
+    torch.cuda.synchronize()
+    assert va.verify_attn_device_status(plan_small) & 2
