@@ -251,14 +251,20 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
         }
       }
       std::sort(costs.begin(), costs.end(), std::greater<int64_t>());
-      std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> load;
-      for (int64_t i = 0; i < slots; ++i) load.push(0);
-      int64_t finish = 0;
-      for (int64_t cst : costs) {
-        int64_t t = load.top() + cst;
-        load.pop();
-        load.push(t);
-        finish = std::max(finish, t);
+      // longest-first onto the least-loaded slot: the first `slots` items
+      // each get an empty slot, so with no more items than slots the finish
+      // is the longest item; otherwise a min-heap of the slot loads takes the
+      // rest
+      int64_t finish = costs.empty() ? 0 : costs[0];
+      if ((int64_t)costs.size() > slots) {
+        std::vector<int64_t> load(costs.begin(), costs.begin() + slots);
+        std::make_heap(load.begin(), load.end(), std::greater<int64_t>());
+        for (size_t k = (size_t)slots; k < costs.size(); ++k) {
+          std::pop_heap(load.begin(), load.end(), std::greater<int64_t>());
+          load.back() += costs[k];
+          finish = std::max(finish, load.back());
+          std::push_heap(load.begin(), load.end(), std::greater<int64_t>());
+        }
       }
       if (best < 0 || (double)finish < best * 0.97) {
         best = (double)finish;
