@@ -185,7 +185,12 @@ int verify_attn_plan(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h,
  * Verify attention (flashmap's partial kernel followed by its LSE merge).
  * All array arguments are DEVICE pointers with the layouts above; the index
  * arrays must hold the same values the plan was built from (a kernel that
- * finds otherwise skips the item and raises VA_DEV_BAD_TABLE).  mask /
+ * finds otherwise skips the item and raises VA_DEV_BAD_TABLE).  The
+ * workspace must hold this plan's work list (the last plan uploaded into
+ * it); an item of another plan that names a request, KV head or partial row
+ * outside this plan is skipped and raises VA_DEV_BAD_TABLE, so a mismatched
+ * workspace never makes a kernel read or write outside the call's arrays or
+ * the workspace.  mask /
  * mask_indptr are NULL iff the plan was made with has_mask = 0.
  * sm_scale <= 0 selects head_dim^-1/2.  k_scale / v_scale multiply the
  * stored keys / values (1 for bf16 caches); both must be finite and > 0.
