@@ -151,6 +151,61 @@ def test_plan_covers_rows_and_keys_exactly_once(va, case, num_sms):
         assert 184 + 32 * (plan.header()["n_items"] + plan.header()["n_merge"]) <= pb
 
 
+def _check_chains(plan):
+    """Persistent tcgen05 plans: chain c starts at item c, links run through
+    the last field, and the chains visit every item exactly once."""
+    hd = plan.header()
+    it = plan.items()
+    n = len(it)
+    assert hd["n_ctas"] == min(n, hd["num_sms"])
+    seen = np.zeros(n, dtype=np.int32)
+    for c in range(hd["n_ctas"]):
+        i = c
+        while i >= 0:
+            assert 0 <= i < n
+            seen[i] += 1
+            i = int(it[i, 7])
+    assert np.all(seen == 1)
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_random_plans_cover_rows_and_keys(va, seed):
+    """Random batches (group size, KV heads, page size, prefix and draft
+    lengths, masks, head_dim, SM count) planned for every variant that can
+    serve them, under random split options: every (request, KV head) row is
+    covered once, each unit's kv range exactly once in order, partial rows
+    once, the persistent variants' chains visit every item once, and the plan
+    fits the sizes verify_attn_plan_bounds promises."""
+    rng = np.random.default_rng(9000 + seed)
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    page_size = int(rng.choice([16, 32, 64]))
+    t = _tables(seed=seed, batch=int(rng.integers(1, 40)), G=G, h_kv=int(rng.integers(1, 5)),
+                page_size=page_size, max_prefix=int(rng.choice([0, 100, 3000])),
+                max_L=int(rng.choice([1, 8, 40, 200])), masked=bool(rng.integers(0, 2)))
+    d = int(rng.choice([64, 128]))
+    num_sms = int(rng.choice([152, 13, 1]))
+    kernels = [0, 1, 2] + ([3, 4] if d == 128 and 128 % G == 0 else [])
+    for kernel in kernels:
+        opts = dict(kernel=kernel, max_splits=int(rng.choice([0, 1, 2, 5])),
+                    min_chunk=int(rng.choice([0, 64, 256])),
+                    target_ctas=int(rng.choice([0, 50, 5000])))
+        plan = va.verify_attn_plan_host(t["kv_indptr"], t["qo_indptr"], t["last"],
+                                        t["mask_indptr"], t["h_q"], t["h_kv"], d, page_size,
+                                        num_sms=num_sms, **opts)
+        hd = plan.header()
+        if kernel:
+            assert hd["kernel"] == kernel
+        _check_cover(va, t, plan)
+        if hd["kernel"] in (3, 4):
+            _check_chains(plan)
+        else:
+            assert hd["n_ctas"] == 0 and np.all(plan.items()[:, 7] == -1)
+        pb, wb = va.verify_attn_plan_bounds(len(t["L"]), int(t["qo_indptr"][-1]), t["h_q"],
+                                            t["h_kv"], d, num_sms)
+        assert plan.workspace_bytes <= wb
+        assert 184 + 32 * (hd["n_items"] + hd["n_merge"]) <= pb
+
+
 @pytest.mark.parametrize("name", synthetic.WORKLOAD_ORDER)
 def test_plans_of_the_named_workloads(va, name):
     wl = synthetic.make_workload(name, with_values=False)
