@@ -77,8 +77,8 @@ def algorithmic(wl):
             draft = L * (L + 1) // 2
         visible += L * pre + draft
     flops = 4 * wl.d * visible * wl.h_q
-    return dict(kv_bytes=kv, read_bytes=kv + q + idx + mask, total_bytes=kv + q + out + lse + idx + mask,
-                flops=flops, tokens=wl.total_qo)
+    return dict(kv_bytes=kv, read_bytes=kv + q + idx + mask,
+                total_bytes=kv + q + out + lse + idx + mask, flops=flops, tokens=wl.total_qo)
 
 
 def kernel_source_sha(kernel=0):
@@ -118,7 +118,10 @@ class ClockSampler:
         self.index = index
         self.proc = None
 
-    def start(self):
+    def start(self, background=None, seconds=0.5):
+        """Start sampling; `background` (one short unit of GPU work) is
+        replayed meanwhile for about `seconds`, so the first samples are
+        taken under load."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
@@ -126,7 +129,14 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+        t0 = time.perf_counter()
+        if background is None:
+            time.sleep(seconds)
+            return
+        import torch
+        while time.perf_counter() - t0 < seconds:
+            background()
+            torch.cuda.synchronize()
 
     def stop(self):
         if self.proc is None:
@@ -216,14 +226,16 @@ class Bench:
         self.launches_per_step = 1 + self.plan.launches()
         torch.cuda.synchronize()
 
-    # one step on pool copy i; ev: optional 4 events around append / partial / merge
-    def step(self, i, ev=None):
+    # one step on pool copy i; ev: optional 4 events around append / partial /
+    # merge; verify_only: the attention call alone (no append)
+    def step(self, i, ev=None, verify_only=False):
         va, wl = self.va, self.wl
         kc, vc = self.pools[i % self.n_copies]
         if ev:
             ev[0].record()
-        va.paged_kv_append(self.k_new, self.v_new, self.qo_indptr, self.kv_indptr,
-                           self.kv_indices, self.last_page_len, kc, vc)
+        if not verify_only:
+            va.paged_kv_append(self.k_new, self.v_new, self.qo_indptr, self.kv_indptr,
+                               self.kv_indices, self.last_page_len, kc, vc)
         if ev:
             ev[1].record()
         va.verify_attn_partial(self.q, kc, vc, self.kv_indptr, self.kv_indices,
@@ -236,44 +248,55 @@ class Bench:
         if ev:
             ev[3].record()
 
-    def capture(self, n, start=0, events=None):
+    def capture(self, n, start=0, events=None, verify_only=False, rotate=True):
         torch = self.torch
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
             for i in range(2):
-                self.step(start + i)
+                self.step(start + i if rotate else 0, verify_only=verify_only)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for i in range(n):
-                self.step(start + i, events[i] if events else None)
+                self.step(start + i if rotate else 0, events[i] if events else None,
+                          verify_only=verify_only)
         return g
 
-    def run_steps(self, k, graphs):
-        """Exactly k steps via graph replays (graphs: full GRAPH_STEPS graph,
-        remainder graph)."""
-        full, rem = graphs
-        for _ in range(k // GRAPH_STEPS):
-            full.replay()
-        if k % GRAPH_STEPS:
-            rem.replay()
-
-    def time_steps(self, k, warmup, sampler=None, barrier=None):
+    def time_steps(self, k, warmup, sampler=None, barrier=None, verify_only=False, rotate=True):
+        """Exactly k steps, timed with CUDA events around replays of captured
+        graphs (k // GRAPH_STEPS replays of a GRAPH_STEPS-step graph and one
+        of a k % GRAPH_STEPS-step graph).  The warm-up replays THOSE graphs
+        (each at least once, so no graph upload or first launch lands in the
+        timed region) for at least `warmup` steps, then keeps the GPU busy
+        with them for about half a second while the clock sampler starts, so
+        its samples see the part under load."""
         torch = self.torch
-        graphs = (self.capture(GRAPH_STEPS), self.capture(k % GRAPH_STEPS) if k % GRAPH_STEPS else None)
-        self.run_steps(warmup, (graphs[0], self.capture(warmup % GRAPH_STEPS)
-                                if warmup % GRAPH_STEPS else None))
+        n_full, rem = divmod(k, GRAPH_STEPS)
+        full = self.capture(GRAPH_STEPS, verify_only=verify_only, rotate=rotate) if n_full else None
+        part = self.capture(rem, verify_only=verify_only, rotate=rotate) if rem else None
+        graphs = [(g, n) for g, n in ((full, GRAPH_STEPS), (part, rem)) if g is not None]
+        done = 0
+        for g, n in graphs:
+            g.replay()
+            done += n
+        small, n_small = graphs[-1]
+        while done < warmup:
+            small.replay()
+            done += n_small
         torch.cuda.synchronize()
         if barrier:
             barrier()
         if sampler:
-            sampler.start()
+            sampler.start(background=lambda: small.replay())
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        self.run_steps(k, graphs)
+        for _ in range(n_full):
+            full.replay()
+        if part is not None:
+            part.replay()
         e1.record()
         torch.cuda.synchronize()
         clocks = sampler.stop() if sampler else None
@@ -336,13 +359,15 @@ class Bench:
         hv = {k: carve(stage_h, k).numpy() for k in ("kv_indptr", "qo_indptr", "last_page_len")}
         np_mask_indptr = carve(stage_h, "mask_indptr").numpy() if self.mask is not None else None
         ws = self.plan.workspace
+        n_sms = self.plan.header()["num_sms"]
+        plan_buf = np.zeros(self.plan.host.nbytes, dtype=np.uint8)
 
         def one(i):
             stage_d.copy_(stage_h, non_blocking=True)
             plan = va.verify_attn_plan(hv["kv_indptr"], hv["qo_indptr"], hv["last_page_len"],
                                        np_mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
                                        kv_dtype=wl.kv_dtype, workspace=ws, device=self.dev,
-                                       **self.plan_opts)
+                                       num_sms=n_sms, plan_buffer=plan_buf, **self.plan_opts)
             kc, vc = self.pools[i % self.n_copies]
             va.paged_kv_append(d["k_new"], d["v_new"], d["qo_indptr"], d["kv_indptr"],
                                d["kv_indices"], d["last_page_len"], kc, vc)
@@ -377,12 +402,18 @@ KERNEL_NAMES = {1: "verify_partial_mma_kernel<4 warps>", 2: "verify_partial_mma_
 
 
 def roofline_for(wl, kt, peaks, peak_kind, kernel=0):
+    """Roofline of the split-attention kernel: algorithmic bytes (K + V + Q
+    read once, out + LSE written once, tables and mask) or FLOPs per launch
+    over its CUDA-event duration, against the measured copy bandwidth or
+    bf16 tensor throughput.  The bound is the one the workload's arithmetic
+    intensity selects."""
     alg = algorithmic(wl)
     t = kt["partial_ms"] * 1e-3
-    hbm = alg["read_bytes"] / t / 1e9
+    hbm = alg["total_bytes"] / t / 1e9
     tfl = alg["flops"] / t / 1e12
     rows_per_kv_head = int((wl.group * wl.qo_lens).max())
-    tensor_bound = alg["flops"] / alg["read_bytes"] > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tensor_bound = alg["flops"] / alg["total_bytes"] > ridge
     if tensor_bound:
         rf = {"bound": "tensor", "achieved": round(tfl, 2), "peak": peaks["bf16_tflops"],
               "unit": "TFLOP/s", "frac": round(tfl / peaks["bf16_tflops"], 4)}
@@ -391,10 +422,11 @@ def roofline_for(wl, kt, peaks, peak_kind, kernel=0):
               "unit": "GB/s", "frac": round(hbm / peaks["hbm_gbs"], 4)}
     rf.update({"kernel": KERNEL_NAMES.get(kernel, "verify_partial"),
                "peak_source": "MEASURED_PEAKS.json (of %s)" % peak_kind,
-               "algorithmic_bytes_per_launch": alg["read_bytes"],
+               "algorithmic_bytes_per_launch": alg["total_bytes"],
                "algorithmic_flops_per_launch": alg["flops"],
                "kernel_ms": round(kt["partial_ms"], 5),
-               "hbm_gbs": round(hbm, 1), "tflops": round(tfl, 2),
+               "hbm_gbs": round(hbm, 1), "hbm_frac": round(hbm / peaks["hbm_gbs"], 4),
+               "tflops": round(tfl, 2), "tensor_frac": round(tfl / peaks["bf16_tflops"], 4),
                "rows_per_kv_head_max": rows_per_kv_head})
     return rf
 
@@ -467,6 +499,28 @@ def workload_config(wl, bench=None):
     return cfg
 
 
+def timing_block(bench, peaks, peak_kind, steps, warmup, sampler=None, barrier=None):
+    """Times one workload: the step (append + attention), the attention call
+    alone (append excluded: verify-attn tokens/s), per-kernel CUDA-event
+    durations, and the split kernel's roofline."""
+    wl = bench.wl
+    ms, clocks = bench.time_steps(steps, warmup, sampler=sampler, barrier=barrier)
+    ms_v, _ = bench.time_steps(steps, warmup, verify_only=True)
+    kt = bench.kernel_times()
+    kernel = bench.plan.header()["kernel"]
+    rf = roofline_for(wl, kt, peaks, peak_kind, kernel)
+    rf["traffic"] = profiled_traffic(wl.name, kernel)
+    alg = algorithmic(wl)
+    return ms, clocks, {
+        "verify_only": {"tokens_per_s": round(wl.total_qo / (ms_v * 1e-3), 1),
+                        "us_per_call": round(ms_v * 1e3, 3),
+                        "hbm_gbs": round(alg["total_bytes"] / (ms_v * 1e-3) / 1e9, 1),
+                        "note": "split attention + merge per call, paged append excluded"},
+        "kernel_us": {k.replace("_ms", ""): round(v * 1e3, 3) for k, v in kt.items()},
+        "roofline": rf,
+    }
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_setup(args.gpus)
@@ -478,13 +532,9 @@ def run_ours(args):
     bench = Bench(args.workload, dev, seed=0, plan_opts=plan_opts)
     wl = bench.wl
     sampler = ClockSampler(local)
-    ms, clocks = bench.time_steps(args.steps, args.warmup, sampler=sampler,
-                                  barrier=barrier_fn(world))
+    ms, clocks, extra = timing_block(bench, peaks, peak_kind, args.steps, args.warmup,
+                                     sampler=sampler, barrier=barrier_fn(world))
     ms_max = reduce_max(ms, world)
-    kt = bench.kernel_times()
-    rf = roofline_for(wl, kt, peaks, peak_kind, bench.plan.header()["kernel"])
-    rf["traffic"] = profiled_traffic(wl.name, bench.plan.header()["kernel"])
-    alg = algorithmic(wl)
     value = world * wl.total_qo / (ms_max * 1e-3)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -493,12 +543,17 @@ def run_ours(args):
         "dtype": "bf16 q/out, %s kv, fp32 accumulate" % wl.kv_dtype, "data": "synthetic",
         "config": workload_config(wl, bench),
         "gpu_launches": args.steps * bench.launches_per_step,
-        "roofline": rf, "clocks": clocks,
-        "us_per_call": round((kt["partial_ms"] + kt["merge_ms"]) * 1e3, 3),
-        "kernel_us": {k.replace("_ms", ""): round(v * 1e3, 3) for k, v in kt.items()},
-        "attention_hbm_gbs": round(alg["total_bytes"] / ((kt["partial_ms"] + kt["merge_ms"]) * 1e-3) / 1e9, 1),
+        "roofline": extra["roofline"], "clocks": clocks,
+        "verify_only": extra["verify_only"], "kernel_us": extra["kernel_us"],
         "plan_host_us": round(bench.plan_us(), 2),
     }
+    # L2-warm: the same pool copy every step (its 21 MB stay in the 129 MB L2)
+    ms_w, _ = bench.time_steps(args.steps, args.warmup, rotate=False)
+    ms_wv, _ = bench.time_steps(args.steps, args.warmup, rotate=False, verify_only=True)
+    line["l2_warm"] = {"ms_per_step": round(ms_w, 6),
+                       "tokens_per_s": round(wl.total_qo / (ms_w * 1e-3), 1),
+                       "verify_only_us_per_call": round(ms_wv * 1e3, 3),
+                       "note": "every step on one KV-pool copy, which stays resident in L2"}
     if not args.no_e2e:
         line["e2e"] = bench.e2e(args.e2e_steps)
         line["e2e"]["value"] = round(world * line["e2e"]["value"], 1)
@@ -511,17 +566,18 @@ def run_ours(args):
                 continue
             b = Bench(name, dev, seed=0)
             steps = 256 if name != "tiny_verify" else 1024
-            ms_o, _ = b.time_steps(steps, 16)
-            kto = b.kernel_times(32)
-            rfo = roofline_for(b.wl, kto, peaks, peak_kind, b.plan.header()["kernel"])
-            rfo["traffic"] = profiled_traffic(name, b.plan.header()["kernel"])
-            others[name] = {"tokens_per_s": round(b.wl.total_qo / (ms_o * 1e-3), 1),
-                            "ms_per_step": round(ms_o, 6),
-                            "us_per_call": round((kto["partial_ms"] + kto["merge_ms"]) * 1e3, 3),
-                            "kernel_us": {k.replace("_ms", ""): round(v * 1e3, 3) for k, v in kto.items()},
-                            "roofline": rfo, "config": workload_config(b.wl, b)}
+            ms_o, _, ex = timing_block(b, peaks, peak_kind, steps, 16)
+            entry = {"tokens_per_s": round(b.wl.total_qo / (ms_o * 1e-3), 1),
+                     "ms_per_step": round(ms_o, 6)}
+            entry.update(ex)
+            entry["config"] = workload_config(b.wl, b)
+            others[name] = entry
             del b
             torch.cuda.empty_cache()
+        if rank == 0 and not args.no_cpu_baseline:
+            for name, entry in others.items():
+                entry["cpu_baseline"] = cpu_baseline(synthetic.make_workload(name),
+                                                     seconds=args.cpu_seconds_per_config)
         line["configs"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
@@ -590,6 +646,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds-per-config", type=float, default=3.0,
+                    help="oracle time per other workload (at least one full call)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--kernel", type=int, default=0,
                     help="force a split-kernel variant (1: mma 64 rows, 2: mma 128 rows, "

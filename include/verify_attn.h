@@ -96,9 +96,11 @@ extern "C" {
 #define VA_ERR_PLAN_BUFFER_TOO_SMALL (-7)
 #define VA_ERR_STATIC_SCRATCH_TOO_SMALL (-8) /* plan needs more than VA_STATIC_SCRATCH_BYTES */
 
-/* Element types. */
-#define VA_DTYPE_BF16 0
-#define VA_DTYPE_FP8_E4M3 1
+/* Element types (FlashInfer PR #286: the query dtype and the KV-cache dtype
+ * are separate arguments of begin_forward; the cache may be fp8). */
+typedef enum { VA_BF16 = 0, VA_FP8_E4M3 = 1 } va_dtype;
+#define VA_DTYPE_BF16 VA_BF16
+#define VA_DTYPE_FP8_E4M3 VA_FP8_E4M3
 
 /* Device-side check bits reported by verify_attn_device_status(). */
 #define VA_DEV_BAD_PAGE 1        /* a page id outside [0, num_pages): read as zeros / skipped */
@@ -113,12 +115,7 @@ typedef struct {
     int min_chunk;       /* smallest kv chunk (keys) a split may hold; 0 = default */
     int target_ctas;     /* CTAs the plan aims to fill; 0 = derived from the SM count */
     int kernel;          /* force a kernel variant (VA_KERNEL_*); 0 = automatic */
-    int cluster;         /* 0 or -1 = off (the default: measured slower on GB300), 2..16 =
-                            largest cluster size: with the warp-level variant, when every
-                            (request, KV head, row block) has the same kv range, its splits
-                            run as one thread-block cluster and merge through distributed
-                            shared memory (no merge kernel, no partials in the workspace) */
-    int reserved[3];     /* must be zero */
+    int reserved[4];     /* must be zero */
 } va_plan_options_t;
 
 #define VA_KERNEL_AUTO 0
@@ -130,7 +127,9 @@ typedef struct {
 #define VA_KERNEL_TC_256 4      /* as VA_KERNEL_TC_128 with two 128-row Q tiles per CTA sharing
                                    every K/V tile (256-row blocks, one CTA per SM) */
 
-/* Name of a status code (static string). */
+/* Name of a status code (static string).  FlashInfer PR #286's BeginForward
+ * turns a failed check into an error message; here every check returns a
+ * code, and this names it. */
 const char* verify_attn_status_string(int status);
 
 /* Number of SMs of the current CUDA device (or an error). */
@@ -147,6 +146,18 @@ int verify_attn_plan_bounds(int batch, int64_t total_qo, int num_qo_heads, int n
                             size_t* workspace_bytes);
 
 /*
+ * Device workspace that suffices for every plan of a batch of at most
+ * `batch` requests with at most `max_qo_len` query tokens each (FlashInfer
+ * PR #286: the caller allocates the workspace once and hands it to
+ * begin_forward).  Equals verify_attn_plan_bounds' workspace bound for
+ * total_qo = batch * max_qo_len.  num_sms <= 0 queries the current device.
+ * Errors: VA_ERR_INVALID_ARGUMENT (negative sizes, heads that do not divide,
+ * null `bytes`), VA_ERR_CUDA (device query).
+ */
+int verify_attn_workspace_size(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                               int max_qo_len, int num_sms, size_t* bytes);
+
+/*
  * Host half of the plan (flashmap's split planner and FlashInfer's
  * begin_forward): from HOST copies of the index arrays, cut the work into
  * items (request b, KV head h, row block, kv chunk [lo, hi)) that fill the
@@ -161,13 +172,16 @@ int verify_attn_plan_bounds(int batch, int64_t total_qo, int num_qo_heads, int n
 int verify_attn_plan_host(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h,
                           const int32_t* last_page_len_h, const int32_t* mask_indptr_h,
                           int batch, int num_qo_heads, int num_kv_heads, int head_dim,
-                          int page_size, int q_dtype, int kv_dtype, int has_mask, int num_sms,
+                          int page_size, va_dtype q_dtype, va_dtype kv_dtype, int has_mask,
+                          int num_sms,
                           const va_plan_options_t* options, void* plan_h, size_t plan_bytes,
                           size_t* workspace_bytes);
 
 /*
- * verify_attn_plan_host() followed by an asynchronous upload of the plan's
- * work list into the device workspace on `stream`.  The workspace must hold
+ * FlashInfer PR #286's begin_forward: plan once from host copies of the
+ * index arrays, then run many times.  verify_attn_plan_host() followed by an
+ * asynchronous upload of the plan's work list into the device workspace on
+ * `stream`.  The workspace must hold
  * at least the bytes verify_attn_plan_host reports (else
  * VA_ERR_WORKSPACE_TOO_SMALL).  It also clears the workspace's device status
  * word.  If plan_h is pinned host memory it must not change until the
@@ -177,7 +191,7 @@ int verify_attn_plan_host(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h
 int verify_attn_plan(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h,
                      const int32_t* last_page_len_h, const int32_t* mask_indptr_h, int batch,
                      int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
-                     int q_dtype, int kv_dtype, int has_mask, int num_sms,
+                     va_dtype q_dtype, va_dtype kv_dtype, int has_mask, int num_sms,
                      const va_plan_options_t* options, void* plan_h, size_t plan_bytes,
                      void* workspace_d, size_t workspace_bytes, void* stream);
 
@@ -228,6 +242,18 @@ int verify_attn_merge(const int32_t* qo_indptr, int num_qo_heads, int num_kv_hea
                       void* out, float* lse, const void* plan_h, void* workspace_d,
                       size_t workspace_bytes, void* stream);
 
+/*
+ * The device half of verify_attn_plan for a plan made by
+ * verify_attn_plan_host: asynchronously copy its work list into the device
+ * workspace on `stream` and clear the workspace's device status word, so a
+ * caller can size the workspace from the plan it already has (plan once,
+ * allocate exactly, upload).  Same contract for plan_h and the workspace as
+ * verify_attn_plan.  Errors: VA_ERR_INVALID_ARGUMENT (no valid plan, a
+ * misaligned workspace), VA_ERR_WORKSPACE_TOO_SMALL, VA_ERR_CUDA.
+ */
+int verify_attn_plan_upload(const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                            void* stream);
+
 /* Number of kernel launches verify_attn_run makes for this plan (1 or 2; 0
  * when the batch has no query token). */
 int verify_attn_plan_launches(const void* plan_h, int* launches);
@@ -254,8 +280,52 @@ int verify_attn_device_status(void* workspace_d, int* bits, void* stream);
 int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_indptr,
                     const int32_t* kv_indptr, const int32_t* kv_indices,
                     const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
-                    int num_kv_heads, int head_dim, int page_size, int num_pages, int kv_dtype,
-                    int64_t total_new, int* status_d, void* stream);
+                    int num_kv_heads, int head_dim, int page_size, int num_pages,
+                    va_dtype kv_dtype, int64_t total_new, int* status_d, void* stream);
+
+/* KV-cache layouts (FlashInfer PR #286's kv_layout argument):
+ *   HND  [num_pages, num_kv_heads, page_size, head_dim]  (the default)
+ *   NHD  [num_pages, page_size, num_kv_heads, head_dim] */
+typedef enum { VA_LAYOUT_HND = 0, VA_LAYOUT_NHD = 1 } va_kv_layout;
+
+/* Options of paged_kv_append_ex (all-zero = a plain bit copy into an HND
+ * cache, as paged_kv_append). */
+typedef struct {
+    int quantize;            /* 1: k_new / v_new are bf16 and the cache is fp8-e4m3; each
+                                element x is stored as e4m3(x / scale): the correctly rounded
+                                binary32 quotient, rounded to nearest even, finite overflow
+                                saturated to +-448 (FlashInfer PR #286's fp8 cache with a
+                                per-tensor scale: dequantised value = stored * scale) */
+    float k_scale, v_scale;  /* the per-tensor scales of the quantising append (> 0, finite) */
+    va_kv_layout kv_layout;
+    const int32_t* positions; /* device [total_new], or NULL: rotate each new K row by RoPE at
+                                this position before storing it (LLaMA's rotate-half pairing
+                                of elements i and i + head_dim/2 at angle position /
+                                rope_scale * rope_theta^(-2i / head_dim); FlashInfer PR #286's
+                                ROPE_LLAMA, applied at the draft's own -- tree -- position as
+                                FlashInfer issue #152 asks).  V rows are not rotated. */
+    float rope_theta;        /* RoPE base (> 0, finite; e.g. 1e4, Llama-3: 5e5) */
+    float rope_scale;        /* linear position scaling (> 0, finite); 0 means 1 */
+    int reserved[4];         /* must be zero */
+} va_append_options_t;
+
+/*
+ * paged_kv_append with options: a quantising append into an fp8 cache, RoPE
+ * at given positions for the new keys, and the NHD layout.  The page walk,
+ * the checks and the status bits are those of paged_kv_append; k_new / v_new
+ * are bf16 when options->quantize, else in the cache dtype.  Rotated or
+ * quantised rows are computed in fp32 and rounded once to the cache dtype
+ * (round to nearest even; e4m3 saturating).  NULL options = paged_kv_append.
+ * Errors: VA_ERR_INVALID_ARGUMENT (bad scales, theta, layout, non-zero
+ * reserved fields, quantize without an fp8 cache), VA_ERR_UNSUPPORTED,
+ * VA_ERR_CUDA.
+ */
+int paged_kv_append_ex(const void* k_new, const void* v_new, const int32_t* append_indptr,
+                       const int32_t* kv_indptr, const int32_t* kv_indices,
+                       const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
+                       int num_kv_heads, int head_dim, int page_size, int num_pages,
+                       va_dtype kv_dtype, int64_t total_new, const va_append_options_t* options,
+                       int* status_d, void* stream);
 
 /*
  * verify_attn_run for callers that cannot allocate device memory.
@@ -277,16 +347,19 @@ int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_
  *    with VA_ERR_STATIC_SCRATCH_TOO_SMALL before anything is enqueued.
  *  - Memory: every GPU that loads the library holds the array until the
  *    process exits.
- *  - Set-up: the first call on each device (with that device current) looks
- *    up the array's device address with cudaGetSymbolAddress; make that first
- *    call before any stream capture begins.
+ *  - Set-up: the first call in each CUDA context (normally: on each device,
+ *    with that device current) looks up the array's device address with
+ *    cudaGetSymbolAddress and keeps it for that context; make that first call
+ *    before any stream capture begins.  A context created later (after
+ *    cudaDeviceReset, or a driver context the caller makes current) gets its
+ *    own look-up.
  *  - Every call copies the plan's work list from plan_h into the array and
- *    clears its status word on `stream` (so plan_h, if pinned, must stay
- *    unchanged until the copy has run), then launches the kernels.  All calls
- *    share the one array, which keeps the last call's contents: calls that can
- *    overlap on the GPU (different streams, or devices sharing the array's
- *    context) race and must be serialised by the caller.  Device-side check
- *    bits are not reported by this entry point.
+ *    clears its status word on `stream` with asynchronous copies (so plan_h,
+ *    if pinned, must stay unchanged until the copy has run), then launches the
+ *    kernels.  All calls share the one array, which keeps the last call's
+ *    contents: calls that can overlap on the GPU (different streams, or
+ *    devices sharing the array's context) race and must be serialised by the
+ *    caller.  Device-side check bits are not reported by this entry point.
  * Errors: as verify_attn_run, plus VA_ERR_STATIC_SCRATCH_TOO_SMALL, and
  * VA_ERR_CUDA if the address look-up or an enqueue fails.
  */

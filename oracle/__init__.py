@@ -74,6 +74,13 @@ def _load():
         lib.oracle_paged_kv_append.restype = i32
         lib.oracle_paged_kv_append.argtypes = [P, P, i32, P, P, P, P, i32, i32, i32, i32, i32,
                                                P, P]
+        lib.oracle_encode_e4m3_satfinite.restype = ctypes.c_uint8
+        lib.oracle_encode_e4m3_satfinite.argtypes = [ctypes.c_float]
+        lib.oracle_div_f32.restype = ctypes.c_float
+        lib.oracle_div_f32.argtypes = [ctypes.c_float, ctypes.c_float]
+        lib.oracle_paged_kv_append_quant.restype = i32
+        lib.oracle_paged_kv_append_quant.argtypes = [P, P, ctypes.c_float, ctypes.c_float, P, P,
+                                                     P, P, i32, i32, i32, i32, i32, P, P]
         _lib = lib
         return lib
 
@@ -187,6 +194,38 @@ def paged_kv_append(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_pag
                                     _p(k_cache), _p(v_cache))
     if rc != 0:
         raise ValueError("oracle_paged_kv_append rejected its inputs (status %d)" % rc)
+
+
+def encode_e4m3_satfinite(x) -> np.ndarray:
+    """fp8-e4m3 codes (uint8) of binary32 values: round to nearest even,
+    saturating finite overflow and infinities to +-448, NaN -> 0x7F."""
+    lib = _load()
+    flat = np.asarray(x, dtype=np.float32).reshape(-1)
+    return np.array([lib.oracle_encode_e4m3_satfinite(float(v)) for v in flat],
+                    dtype=np.uint8).reshape(np.shape(x))
+
+
+def div_f32(x: float, scale: float) -> float:
+    """The correctly rounded binary32 quotient x / scale."""
+    return float(_load().oracle_div_f32(float(x), float(scale)))
+
+
+def paged_kv_append_quant(k_new, v_new, k_scale, v_scale, append_indptr, kv_indptr, kv_indices,
+                          last_page_len, page_size, num_pages, k_cache, v_cache):
+    """Quantising host scatter: bf16 rows (uint16 bits) into an fp8-e4m3 pool
+    (uint8 [pages, h_kv, P, d], in place), stored = e4m3(x / scale)."""
+    lib = _load()
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    h_kv, d = k_cache.shape[1], k_cache.shape[3]
+    idx = [_c(a, np.int32) for a in (append_indptr, kv_indptr, kv_indices, last_page_len)]
+    rc = lib.oracle_paged_kv_append_quant(_p(k_new), _p(v_new), float(k_scale), float(v_scale),
+                                          *[_p(a) for a in idx], len(idx[0]) - 1, h_kv, d,
+                                          page_size, num_pages, _p(k_cache), _p(v_cache))
+    if rc != 0:
+        raise ValueError("oracle_paged_kv_append_quant rejected its inputs (status %d)" % rc)
 
 
 # ---- convenience over synthetic.Workload (inputs only; no arithmetic here) ----

@@ -69,6 +69,43 @@ double oracle_decode_e4m3(uint8_t bits) {
     return sign ? -v : v;
 }
 
+/* fp8-e4m3 code of a binary32 value, on the grid oracle_decode_e4m3 defines
+ * (subnormals m * 2^-9, m = 0..7; normals (8 + m) * 2^(e - 10), e = 1..15):
+ * the nearest grid value, a tie going to the code whose last mantissa bit is
+ * 0 (round to nearest even); finite overflow and infinities saturate to
+ * +-448, the largest finite value ("satfinite"); NaN gives the NaN code
+ * 0x7F. */
+uint8_t oracle_encode_e4m3_satfinite(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: multiples of 2^-9; 8 * 2^-9 = 2^-6 is code 0x08 */
+        double m = nearbyint(ldexp(a, 9));
+        return sign | (uint8_t)m;
+    }
+    int ex;
+    (void)frexp(a, &ex);              /* a = f * 2^ex, f in [0.5, 1) */
+    int e = ex - 1;                   /* 2^e <= a < 2^(e+1), e in [-6, 8] */
+    double m = nearbyint(ldexp(a, 3 - e));   /* in [8, 16] */
+    if (m == 16.0) {
+        m = 8.0;
+        e += 1;
+    }
+    if (e > 8 || (e == 8 && m > 14.0)) return sign | 0x7E;
+    return sign | (uint8_t)(((e + 7) << 3) | ((int)m - 8));
+}
+
+/* The binary32 quotient x / scale, correctly rounded: the quotient of two
+ * binary32 values computed in binary64 and rounded once more to binary32
+ * equals the correctly rounded binary32 quotient, because 53 >= 2 * 24 + 2
+ * (double rounding is innocuous for division at that precision; Figueroa,
+ * "When is double rounding innocuous?", SIGNUM 1995). */
+float oracle_div_f32(float x, float scale) {
+    return (float)((double)x / (double)scale);
+}
+
 static double decode_kv(const void* base, int64_t idx, int kv_fp8) {
     if (kv_fp8) return oracle_decode_e4m3(((const uint8_t*)base)[idx]);
     return oracle_decode_bf16(((const uint16_t*)base)[idx]);
@@ -422,6 +459,48 @@ void oracle_merge_partials(int n_parts, int n_rows, int d, const double* outs,
  * k_new[append_indptr[b] + i, h, :] are copied unchanged (elem_bytes per
  * element) to k_cache[page, h, slot, :]; likewise for V.
  */
+/*
+ * Quantising append: the walk of oracle_paged_kv_append, with bf16 new rows
+ * and an fp8-e4m3 cache; element x of a K row is stored as
+ * oracle_encode_e4m3_satfinite(oracle_div_f32(x, k_scale)) (likewise V with
+ * v_scale): the per-tensor scale of FlashInfer PR #286's fp8 cache
+ * (dequantised value = stored * scale), rounded to nearest even, saturated.
+ */
+int oracle_paged_kv_append_quant(const uint16_t* k_new, const uint16_t* v_new, float k_scale,
+                                 float v_scale, const int32_t* append_indptr,
+                                 const int32_t* kv_indptr, const int32_t* kv_indices,
+                                 const int32_t* last_page_len, int batch, int h_kv, int d,
+                                 int page_size, int num_pages, uint8_t* k_cache,
+                                 uint8_t* v_cache) {
+    if (batch < 0 || h_kv <= 0 || d <= 0 || page_size <= 0) return OR_EINVAL;
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f)) return OR_EINVAL;
+    for (int b = 0; b < batch; ++b) {
+        int64_t n = (int64_t)append_indptr[b + 1] - append_indptr[b];
+        int64_t kv_len = oracle_kv_len(kv_indptr, last_page_len, b, page_size);
+        if (n < 0 || n > kv_len) return OR_EINVAL;
+        for (int64_t i = 0; i < n; ++i) {
+            int64_t pos = kv_len - n + i;
+            int64_t pidx = (int64_t)kv_indptr[b] + pos / page_size;
+            if (pidx >= kv_indptr[b + 1]) return OR_EINVAL;
+            int32_t page = kv_indices[pidx];
+            if (page < 0 || page >= num_pages) return OR_EINVAL;
+            int64_t slot = pos % page_size;
+            int64_t tok = (int64_t)append_indptr[b] + i;
+            for (int h = 0; h < h_kv; ++h) {
+                size_t dst = (((size_t)page * h_kv + h) * page_size + slot) * (size_t)d;
+                size_t src = ((size_t)tok * h_kv + h) * (size_t)d;
+                for (int e = 0; e < d; ++e) {
+                    float xk = (float)oracle_decode_bf16(k_new[src + e]);
+                    float xv = (float)oracle_decode_bf16(v_new[src + e]);
+                    k_cache[dst + e] = oracle_encode_e4m3_satfinite(oracle_div_f32(xk, k_scale));
+                    v_cache[dst + e] = oracle_encode_e4m3_satfinite(oracle_div_f32(xv, v_scale));
+                }
+            }
+        }
+    }
+    return OR_OK;
+}
+
 int oracle_paged_kv_append(const void* k_new, const void* v_new, int elem_bytes,
                            const int32_t* append_indptr, const int32_t* kv_indptr,
                            const int32_t* kv_indices, const int32_t* last_page_len, int batch,

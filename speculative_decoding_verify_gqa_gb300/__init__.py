@@ -32,6 +32,7 @@ __all__ = [
     "VerifyAttnError", "Plan", "lib", "verify_attn_plan", "verify_attn_run",
     "verify_attn_partial", "verify_attn_merge", "paged_kv_append",
     "verify_attn_device_status", "verify_attn_plan_bounds", "verify_attn_plan_host",
+    "verify_attn_workspace_size", "verify_attn_run_static_scratch",
     "status_string", "num_sms", "KV_BF16", "KV_FP8_E4M3", "library_path",
 ]
 
@@ -60,7 +61,7 @@ class VerifyAttnError(RuntimeError):
 class PlanOptions(ctypes.Structure):
     _fields_ = [("max_splits", ctypes.c_int), ("min_chunk", ctypes.c_int),
                 ("target_ctas", ctypes.c_int), ("kernel", ctypes.c_int),
-                ("cluster", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("reserved", ctypes.c_int * 4)]
 
 
 def lib():
@@ -81,6 +82,7 @@ def lib():
         "verify_attn_status_string": (ctypes.c_char_p, [i32]),
         "verify_attn_num_sms": (i32, [Pi]),
         "verify_attn_plan_bounds": (i32, [i32, i64, i32, i32, i32, i32, Psz, Psz]),
+        "verify_attn_workspace_size": (i32, [i32, i32, i32, i32, i32, i32, Psz]),
         "verify_attn_plan_host": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                         P, P, sz, Psz]),
         "verify_attn_plan": (i32, [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, P, P,
@@ -91,6 +93,7 @@ def lib():
                                       f32, P, P, i32, P, P, sz, P]),
         "verify_attn_merge": (i32, [P, i32, i32, i32, P, P, P, P, sz, P]),
         "verify_attn_plan_launches": (i32, [P, Pi]),
+        "verify_attn_plan_upload": (i32, [P, P, sz, P]),
         "verify_attn_device_status": (i32, [P, Pi, P]),
         "paged_kv_append": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, P,
                                   P]),
@@ -154,11 +157,10 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0, cluster=0):
+def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0):
     o = PlanOptions()
     o.max_splits, o.min_chunk, o.target_ctas, o.kernel = (int(max_splits), int(min_chunk),
                                                           int(target_ctas), int(kernel))
-    o.cluster = int(cluster)
     return o
 
 
@@ -186,7 +188,7 @@ class Plan:
                     tile_keys=int(ints[13]), n_items=int(ints[14]), n_merge=int(ints[15]),
                     n_units=int(ints[16]), num_sms=int(ints[17]), total_qo=int(i64[0]),
                     part_rows=int(i64[1]), chunk=int(i64[2]),
-                    cluster=int(np.frombuffer(h[152:160].tobytes(), dtype=np.int64)[0]),
+                    ws_bytes=int(np.frombuffer(h[136:144].tobytes(), dtype=np.uint64)[0]),
                     n_ctas=int(np.frombuffer(h[160:168].tobytes(), dtype=np.int64)[0]))
 
     def launches(self) -> int:
@@ -245,30 +247,61 @@ def verify_attn_plan_host(kv_indptr_h, qo_indptr_h, last_page_len_h, mask_indptr
                 _kv_code(kv_dtype), bool(has_mask), total_qo)
 
 
+def verify_attn_workspace_size(batch, num_qo_heads, num_kv_heads, head_dim, max_qo_len,
+                               num_sms=0) -> int:
+    """Device workspace bytes that serve every plan of a batch of at most
+    `batch` requests with at most `max_qo_len` query tokens each."""
+    n = ctypes.c_size_t(0)
+    _check("verify_attn_workspace_size",
+           lib().verify_attn_workspace_size(int(batch), int(num_qo_heads), int(num_kv_heads),
+                                            int(head_dim), int(max_qo_len), int(num_sms),
+                                            ctypes.byref(n)))
+    return n.value
+
+
 def verify_attn_plan(kv_indptr_h, qo_indptr_h, last_page_len_h, mask_indptr_h, num_qo_heads,
                      num_kv_heads, head_dim, page_size, kv_dtype="bf16", has_mask=None,
                      workspace: Optional[torch.Tensor] = None, device=None, stream=None,
-                     num_sms=0, **options) -> Plan:
+                     num_sms=0, plan_buffer: Optional[np.ndarray] = None, **options) -> Plan:
     """Plan a batch from HOST index arrays and upload the work list to a
-    device workspace (allocated here with torch if not given)."""
-    plan = verify_attn_plan_host(kv_indptr_h, qo_indptr_h, last_page_len_h, mask_indptr_h,
-                                 num_qo_heads, num_kv_heads, head_dim, page_size, kv_dtype,
-                                 has_mask, num_sms, **options)
-    if workspace is None or workspace.numel() < plan.workspace_bytes:
-        workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8,
-                                device=device or "cuda")
+    device workspace, planning once: with a workspace given (it must hold the
+    plan), one call of the library's verify_attn_plan; without, the host plan
+    is made first, a workspace of exactly its size is allocated here with
+    torch, and the plan is uploaded.  plan_buffer (uint8, at least
+    verify_attn_plan_bounds' plan bytes) may be passed to reuse a host
+    buffer."""
     kvp, qop, lpl, mip = (_host_i32(kv_indptr_h), _host_i32(qo_indptr_h),
                           _host_i32(last_page_len_h), _host_i32(mask_indptr_h))
+    batch = len(qop) - 1
+    if has_mask is None:
+        has_mask = mip is not None
+    total_qo = int(qop[-1]) if batch >= 0 else 0
+    if num_sms <= 0:
+        num_sms = globals()["num_sms"]()
     opt = _options(**options)
-    host = np.zeros_like(plan.host)
-    rc = lib().verify_attn_plan(_hp(kvp), _hp(qop), _hp(lpl), _hp(mip), plan.batch,
+    if workspace is None:
+        # plan on the host, allocate the workspace this plan needs, upload
+        plan = verify_attn_plan_host(kvp, qop, lpl, mip, num_qo_heads, num_kv_heads, head_dim,
+                                     page_size, kv_dtype, has_mask, num_sms, **options)
+        plan.workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8,
+                                     device=device or "cuda")
+        _check("verify_attn_plan_upload",
+               lib().verify_attn_plan_upload(_hp(plan.host), _dp(plan.workspace),
+                                             plan.workspace.numel(), _stream(stream)))
+        return plan
+    pb, _ = verify_attn_plan_bounds(batch, total_qo, num_qo_heads, num_kv_heads, head_dim,
+                                    num_sms)
+    host = plan_buffer if plan_buffer is not None and plan_buffer.nbytes >= pb else \
+        np.zeros(pb, dtype=np.uint8)
+    rc = lib().verify_attn_plan(_hp(kvp), _hp(qop), _hp(lpl), _hp(mip), batch,
                                 int(num_qo_heads), int(num_kv_heads), int(head_dim),
-                                int(page_size), 0, plan.kv_dtype, int(plan.has_mask),
+                                int(page_size), 0, _kv_code(kv_dtype), int(bool(has_mask)),
                                 int(num_sms), ctypes.byref(opt), _hp(host), host.nbytes,
                                 _dp(workspace), workspace.numel(), _stream(stream))
     _check("verify_attn_plan", rc)
-    plan.host = host
-    plan.workspace = workspace
+    plan = Plan(host, workspace, 0, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                _kv_code(kv_dtype), bool(has_mask), total_qo)
+    plan.workspace_bytes = plan.header()["ws_bytes"]
     return plan
 
 

@@ -97,8 +97,44 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) 
 
 // Paged append (vLLM PR #1679: every draft's K/V is cached before attention;
 // FlashInfer PR #286's page table).  One thread per 16-byte chunk of one
-// (token, KV head) row, for K and V: a bit-exact copy to slot pos % P of page
-// kv_indices[kv_indptr[b] + pos / P], pos = kv_len_b - n_b + i.
+// (token, KV head) cache row, for K and V: slot pos % P of page
+// kv_indices[kv_indptr[b] + pos / P], pos = kv_len_b - n_b + i, in the HND
+// ([page][head][slot]) or NHD ([page][slot][head]) layout.  A plain append is
+// a bit-exact copy.  A quantising append (FlashInfer PR #286's fp8 cache with
+// a per-tensor scale) reads bf16 rows and stores e4m3(x / scale): the
+// correctly rounded binary32 quotient converted with round-to-nearest-even
+// and saturation to +-448.  With positions, K rows are rotated first (RoPE,
+// LLaMA's rotate-half pairing (i, i + d/2) at angle position * theta^(-2i/d)
+// / rope_scale, FlashInfer PR #286's ROPE_LLAMA, at the tree positions
+// FlashInfer issue #152 asks for), in fp32, then rounded to the cache dtype.
+__device__ __forceinline__ void load_f32(const uint8_t* row, int bf16_src, int e0, int n, float* x) {
+  if (bf16_src) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(row + 2 * e0);
+    for (int c = 0; c < n / 8; ++c) {
+      const uint4 w = s4[c];
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        x[8 * c + 2 * k] = __uint_as_float(u[k] << 16);
+        x[8 * c + 2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
+      }
+    }
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4*>(row + e0);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t hv = e4m3x2_to_f16x2((uint16_t)(u[k] >> (16 * j)));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hv));
+        x[4 * k + 2 * j] = f.x;
+        x[4 * k + 2 * j + 1] = f.y;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams p) {
   // Launched with programmatic serialization: the pages may still be read by
   // the kernel before this one, so wait for it; the attention kernel after
@@ -136,13 +172,67 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
     return;
   }
   const size_t row_bytes = (size_t)p.row_chunks * 16;
-  const size_t dst = (((size_t)page * p.h_kv + h) * p.page_size + (size_t)(pos & (p.page_size - 1))) *
-                         row_bytes + (size_t)ch * 16;
-  const size_t src = ((size_t)i * p.h_kv + h) * row_bytes + (size_t)ch * 16;
-  const uint4 kv = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.k_new) + src);
-  const uint4 vv = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.v_new) + src);
-  *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_cache) + dst) = kv;
-  *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_cache) + dst) = vv;
+  const size_t slot = (size_t)(pos & (p.page_size - 1));
+  const size_t row = p.nhd ? ((size_t)page * p.page_size + slot) * p.h_kv + h
+                           : ((size_t)page * p.h_kv + h) * p.page_size + slot;
+  const size_t dst = row * row_bytes + (size_t)ch * 16;
+  uint8_t* kd = static_cast<uint8_t*>(p.k_cache) + dst;
+  uint8_t* vd = static_cast<uint8_t*>(p.v_cache) + dst;
+  const int D = p.head_dim;
+  const bool bf16_src = p.quant || !p.cache_fp8;
+  const size_t src_row = ((size_t)i * p.h_kv + h) * (size_t)D * (bf16_src ? 2 : 1);
+  const uint8_t* ks = static_cast<const uint8_t*>(p.k_new) + src_row;
+  const uint8_t* vs = static_cast<const uint8_t*>(p.v_new) + src_row;
+  if (!p.quant && !p.positions) {  // a bit-exact copy
+    *reinterpret_cast<uint4*>(kd) = *reinterpret_cast<const uint4*>(ks + (size_t)ch * 16);
+    *reinterpret_cast<uint4*>(vd) = *reinterpret_cast<const uint4*>(vs + (size_t)ch * 16);
+    return;
+  }
+  // elements e0 .. e0 + E - 1 of the row: 8 for a bf16 cache, 16 for fp8
+  const int E = p.cache_fp8 ? 16 : 8;
+  const int e0 = ch * E;
+  float xk[16], xv[16];
+  load_f32(ks, bf16_src, e0, E, xk);
+  load_f32(vs, bf16_src, e0, E, xv);
+  if (p.positions) {
+    const int half = D / 2;
+    const int partner = e0 < half ? e0 + half : e0 - half;
+    float yk[16];
+    load_f32(ks, bf16_src, partner, E, yk);
+    const int kpos = __ldg(p.positions + i);
+    const float sgn = e0 < half ? -1.f : 1.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      if (e >= E) break;
+      const int j = (e0 + e) & (half - 1);
+      float c, s;
+      rope_cos_sin(kpos, p.rope.hi[j], p.rope.lo[j], &c, &s);
+      xk[e] = fmaf(xk[e], c, sgn * yk[e] * s);
+    }
+  }
+  if (!p.cache_fp8) {
+    uint4 wk, wv;
+    wk.x = pack_bf16x2(xk[0], xk[1]); wk.y = pack_bf16x2(xk[2], xk[3]);
+    wk.z = pack_bf16x2(xk[4], xk[5]); wk.w = pack_bf16x2(xk[6], xk[7]);
+    wv.x = pack_bf16x2(xv[0], xv[1]); wv.y = pack_bf16x2(xv[2], xv[3]);
+    wv.z = pack_bf16x2(xv[4], xv[5]); wv.w = pack_bf16x2(xv[6], xv[7]);
+    *reinterpret_cast<uint4*>(kd) = wk;
+    *reinterpret_cast<uint4*>(vd) = wv;
+    return;
+  }
+  // e4m3 codes: quantising appends divide by the per-tensor scale first (a
+  // copy of fp8 rows that were only rotated keeps their scale)
+  const float ksc = p.quant ? p.k_scale : 1.f, vsc = p.quant ? p.v_scale : 1.f;
+  uint32_t ck[4], cv[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ck[k] = e4m3x4_rn_satfinite(__fdiv_rn(xk[4 * k], ksc), __fdiv_rn(xk[4 * k + 1], ksc),
+                                __fdiv_rn(xk[4 * k + 2], ksc), __fdiv_rn(xk[4 * k + 3], ksc));
+    cv[k] = e4m3x4_rn_satfinite(__fdiv_rn(xv[4 * k], vsc), __fdiv_rn(xv[4 * k + 1], vsc),
+                                __fdiv_rn(xv[4 * k + 2], vsc), __fdiv_rn(xv[4 * k + 3], vsc));
+  }
+  *reinterpret_cast<uint4*>(kd) = make_uint4(ck[0], ck[1], ck[2], ck[3]);
+  *reinterpret_cast<uint4*>(vd) = make_uint4(cv[0], cv[1], cv[2], cv[3]);
 }
 
 }  // namespace

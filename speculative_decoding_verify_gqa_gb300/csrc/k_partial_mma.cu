@@ -83,17 +83,14 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
                   (long long)it.row0 + it.nrows <= (long long)G * L && it.kv_lo >= 0 &&
                   it.kv_lo < it.kv_hi && it.kv_hi <= kv_len && kv_len_ll <= 0x7fffffffLL &&
                   (it.part_row < 0 || (long long)it.part_row + it.nrows <= p.part_rows);
-  const bool clustered = p.cluster > 1;
   if (!ok) {
     if (tid == 0) atomicOr(p.status, VA_DEV_BAD_TABLE);
-    // A CTA of a cluster must still reach the cluster barriers: it runs with
-    // no rows and no keys (its partial is empty) and writes nothing.
-    if (!clustered) return;
+    return;
   }
 
-  const int nrows = ok ? it.nrows : 0, row0 = it.row0;
+  const int nrows = it.nrows, row0 = it.row0;
   const int lo = it.kv_lo, hi = it.kv_hi;
-  const int n_tiles = ok ? (hi - lo + C::BN - 1) / C::BN : 0;
+  const int n_tiles = (hi - lo + C::BN - 1) / C::BN;
   const size_t head_stride = (size_t)p.page_size * C::KVROW;
   const size_t page_stride = (size_t)p.h_kv * head_stride;
   const uint8_t* kbase = static_cast<const uint8_t*>(p.k_cache) + (size_t)h * head_stride;
@@ -340,95 +337,6 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
   grid_dependents_launch();
   if (bad_page) atomicOr(p.status, VA_DEV_BAD_PAGE);
 
-  if (clustered) {
-    // ---- merge inside the cluster: every split of this unit is a CTA of
-    // the cluster (rank = split index).  Each stages its normalised rows and
-    // their LSE in its own shared memory; after a cluster barrier, rank c
-    // merges rows [c * per, (c + 1) * per) by reading every peer's copy
-    // ("flashmap ... verify_attention.py" merge rule: weights e^(lse_s - m)).
-    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-    __syncthreads();  // the stage buffers and Q are free
-    float* sO = reinterpret_cast<float*>(sStage);  // [BM][D] fp32
-    float* sL = reinterpret_cast<float*>(sQ);      // [BM]
-    static_assert(C::BM * D * 4 <= STAGES * C::STAGE_BYTES, "staged rows fit the stage ring");
-    if (!ok)
-      for (int r = tid; r < C::BM; r += C::NT) sL[r] = -INFINITY;
-    if (warp_active) {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int rl = wrow + g4 + half * 8;
-        if (rl >= nrows) continue;
-        const float m = half ? m_hi : m_lo;
-        const float l = half ? l_hi : l_lo;
-        const float inv = l > 0.f ? p.v_scale / l : 0.f;
-        float2* dst = reinterpret_cast<float2*>(sO + (size_t)rl * D);
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j)
-          dst[j * 4 + tq] = make_float2(o[j][2 * half] * inv, o[j][2 * half + 1] * inv);
-        if (tq == 0) sL[rl] = l > 0.f ? m * p.scale_nat + logf(l) : -INFINITY;
-      }
-    }
-    cluster_sync_all();
-    constexpr int V = D / 32;
-    const int nsplit = p.cluster;
-    const int R = it.nrows;
-    const int per = (R + nsplit - 1) / nsplit;
-    const int rank = (int)cluster_ctarank();
-    const int r_end = min(R, (rank + 1) * per);
-    const uint32_t sl_addr = smem_u32(sL), so_addr = smem_u32(sO);
-    for (int rl = rank * per + warp; rl < r_end; rl += NW) {
-      float ls = -INFINITY;
-      if (lane < nsplit) ls = ld_cluster_f32(cluster_map(sl_addr + rl * 4, lane));
-      float m = ls;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      const float w = (ls == -INFINITY) ? 0.f : ex2((ls - m) * kLog2e);
-      float den = w;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-      float acc[V];
-#pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] = 0.f;
-      const uint32_t src = so_addr + (uint32_t)(rl * D + lane * V) * 4;
-#pragma unroll
-      for (int s = 0; s < 16; ++s) {
-        if (s < nsplit) {
-          const float ws = __shfl_sync(0xffffffffu, w, s);
-          if (ws != 0.f) {
-            const uint32_t a = cluster_map(src, (uint32_t)s);
-            if constexpr (V == 4) {
-              const float4 x = ld_cluster_f32x4(a);
-              acc[0] += ws * x.x; acc[1] += ws * x.y; acc[2] += ws * x.z; acc[3] += ws * x.w;
-            } else {
-              const float2 x = ld_cluster_f32x2(a);
-              acc[0] += ws * x.x; acc[1] += ws * x.y;
-            }
-          }
-        }
-      }
-      if (ok) {
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        const int rr = row0 + rl;
-        const int t = rr / G, g = rr - t * G;
-        const size_t orow = (size_t)(qo0 + t) * p.h_q + (size_t)h * G + g;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + orow * D + lane * V;
-        if constexpr (V == 4) {
-          uint2 v2;
-          v2.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-          v2.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-          *reinterpret_cast<uint2*>(dst) = v2;
-        } else {
-          *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        }
-        if (p.lse && lane == 0) p.lse[orow] = den > 0.f ? m + logf(den) : -INFINITY;
-      }
-    }
-    cluster_sync_all();  // no CTA leaves while a peer may still read its rows
-    return;
-  }
   if (!warp_active) return;
 
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
@@ -475,7 +383,7 @@ cudaError_t launch_variant(const PartialParams& p, int n_items, cudaStream_t str
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PartialParams*>(&p)};
   return launch_kernel(reinterpret_cast<const void*>(kern), dim3(n_items), dim3(C::NT), C::SMEM,
-                       stream, args, /*pdl=*/true, p.cluster);
+                       stream, args, /*pdl=*/true);
 }
 
 }  // namespace

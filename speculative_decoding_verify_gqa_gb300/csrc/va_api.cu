@@ -118,10 +118,21 @@ PartialParams make_partial(const void* q, const void* k_cache, const void* v_cac
   p.scale_nat = sm_scale * k_scale;
   p.scale_log2 = sm_scale * k_scale * 1.4426950408889634f;
   p.v_scale = v_scale;
-  p.cluster = kernel_is_tc(hd->kernel) ? 0 : (int)hd->cluster;
   p.n_items = hd->n_items;
   p.n_ctas = (int)hd->n_ctas;
   return p;
+}
+
+// RoPE frequencies theta^(-2i/d) / scale for i < d/2, in double, each split
+// into a float head and the float nearest to the rest.
+void rope_frequencies(float theta, float scale, int head_dim, RopeFreq* f) {
+  for (int i = 0; i < 64; ++i) {
+    f->hi[i] = f->lo[i] = 0.f;
+    if (2 * i >= head_dim) continue;
+    const double v = pow((double)theta, -2.0 * i / head_dim) / (double)scale;
+    f->hi[i] = (float)v;
+    f->lo[i] = (float)(v - (double)f->hi[i]);
+  }
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
@@ -223,12 +234,20 @@ int verify_attn_plan_bounds(int batch, int64_t total_qo, int num_qo_heads, int n
                      workspace_bytes);
 }
 
+int verify_attn_workspace_size(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                               int max_qo_len, int num_sms, size_t* bytes) {
+  if (!bytes || batch < 0 || max_qo_len < 0) return VA_ERR_INVALID_ARGUMENT;
+  size_t plan_bytes = 0;
+  return verify_attn_plan_bounds(batch, (int64_t)batch * max_qo_len, num_qo_heads, num_kv_heads,
+                                 head_dim, num_sms, &plan_bytes, bytes);
+}
+
 int verify_attn_plan_host(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h,
                           const int32_t* last_page_len_h, const int32_t* mask_indptr_h,
                           int batch, int num_qo_heads, int num_kv_heads, int head_dim,
-                          int page_size, int q_dtype, int kv_dtype, int has_mask, int num_sms,
-                          const va_plan_options_t* options, void* plan_h, size_t plan_bytes,
-                          size_t* workspace_bytes) {
+                          int page_size, va_dtype q_dtype, va_dtype kv_dtype, int has_mask,
+                          int num_sms, const va_plan_options_t* options, void* plan_h,
+                          size_t plan_bytes, size_t* workspace_bytes) {
   if (num_sms <= 0) {
     int rc = query_sms(&num_sms);
     if (rc) return rc;
@@ -241,7 +260,7 @@ int verify_attn_plan_host(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h
 int verify_attn_plan(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h,
                      const int32_t* last_page_len_h, const int32_t* mask_indptr_h, int batch,
                      int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
-                     int q_dtype, int kv_dtype, int has_mask, int num_sms,
+                     va_dtype q_dtype, va_dtype kv_dtype, int has_mask, int num_sms,
                      const va_plan_options_t* options, void* plan_h, size_t plan_bytes,
                      void* workspace_d, size_t workspace_bytes, void* stream) {
   size_t need = 0;
@@ -250,8 +269,15 @@ int verify_attn_plan(const int32_t* kv_indptr_h, const int32_t* qo_indptr_h,
                                  kv_dtype, has_mask, num_sms, options, plan_h, plan_bytes, &need);
   if (rc) return rc;
   if (!workspace_d || workspace_bytes < need) return VA_ERR_WORKSPACE_TOO_SMALL;
+  return verify_attn_plan_upload(plan_h, workspace_d, workspace_bytes, stream);
+}
+
+int verify_attn_plan_upload(const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                            void* stream) {
+  const PlanHeader* hd = plan_header(plan_h);
+  if (!hd) return VA_ERR_INVALID_ARGUMENT;
+  if (!workspace_d || workspace_bytes < hd->ws_bytes) return VA_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(workspace_d)) return VA_ERR_INVALID_ARGUMENT;
-  const PlanHeader* hd = static_cast<const PlanHeader*>(plan_h);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace_d);
   if (cudaMemsetAsync(ws + hd->off_status, 0, sizeof(int), s) != cudaSuccess) return VA_ERR_CUDA;
@@ -353,25 +379,60 @@ int verify_attn_run(const void* q, const void* k_cache, const void* v_cache,
 // One file-scope device array serves every verify_attn_run_static_scratch call
 // (work list, split partials, status word).  In host code its name is only a
 // host-side stand-in for the symbol; its device address comes from
-// cudaGetSymbolAddress, looked up once per device.
+// cudaGetSymbolAddress, looked up once per CUDA context.
 static __device__ __align__(256) unsigned char g_static_scratch[VA_STATIC_SCRATCH_BYTES];
 
 namespace {
 
-constexpr int kMaxDevices = 64;
+// Address of g_static_scratch in the current context.  The symbol's address
+// is a property of the context that loaded this library's module (the
+// device's primary context, or another driver context made current by the
+// caller), and a context destroyed by cudaDeviceReset takes it along, so the
+// look-up is cached per context under the driver's unique context id -- not
+// per device ordinal -- and made afresh for a context not seen before.  Before
+// any context exists the runtime call creates the primary context, and the
+// result is not cached that time.
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename F>
+F driver_fn(const char* name, int version) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(f);
+}
+
+constexpr int kScratchCache = 16;
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kScratchCache] = {};
+void* g_scratch_ptr[kScratchCache] = {};
+int g_scratch_next = 0;
 
 int static_scratch_address(void** ptr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VA_ERR_CUDA;
+  static const PfnCtxGetCurrent ctx_current = driver_fn<PfnCtxGetCurrent>("cuCtxGetCurrent", 4000);
+  static const PfnCtxGetId ctx_id = driver_fn<PfnCtxGetId>("cuCtxGetId", 12000);
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  const bool keyed = ctx_current && ctx_id && ctx_current(&ctx) == CUDA_SUCCESS && ctx &&
+                     ctx_id(ctx, &id) == CUDA_SUCCESS;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return VA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+  if (keyed)
+    for (int i = 0; i < kScratchCache; ++i)
+      if (g_scratch_ptr[i] && g_scratch_ctx[i] == id) {
+        *ptr = g_scratch_ptr[i];
+        return VA_OK;
+      }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return VA_ERR_CUDA;
+  if (keyed) {
+    g_scratch_ctx[g_scratch_next] = id;
+    g_scratch_ptr[g_scratch_next] = p;
+    g_scratch_next = (g_scratch_next + 1) % kScratchCache;
   }
-  *ptr = g_scratch_ptr[dev];
+  *ptr = p;
   return VA_OK;
 }
 
@@ -421,14 +482,29 @@ int verify_attn_device_status(void* workspace_d, int* bits, void* stream) {
   return v ? VA_ERR_DEVICE_CHECK : VA_OK;
 }
 
-int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_indptr,
-                    const int32_t* kv_indptr, const int32_t* kv_indices,
-                    const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
-                    int num_kv_heads, int head_dim, int page_size, int num_pages, int kv_dtype,
-                    int64_t total_new, int* status_d, void* stream) {
+int paged_kv_append_ex(const void* k_new, const void* v_new, const int32_t* append_indptr,
+                       const int32_t* kv_indptr, const int32_t* kv_indices,
+                       const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
+                       int num_kv_heads, int head_dim, int page_size, int num_pages,
+                       va_dtype kv_dtype, int64_t total_new, const va_append_options_t* options,
+                       int* status_d, void* stream) {
+  va_append_options_t o;
+  memset(&o, 0, sizeof(o));
+  if (options) o = *options;
+  for (int r : o.reserved)
+    if (r) return VA_ERR_INVALID_ARGUMENT;
   if (batch < 0 || total_new < 0 || num_kv_heads <= 0) return VA_ERR_INVALID_ARGUMENT;
   int rc = check_common(num_kv_heads, num_kv_heads, head_dim, page_size, VA_DTYPE_BF16, kv_dtype);
   if (rc) return rc;
+  if (o.kv_layout != VA_LAYOUT_HND && o.kv_layout != VA_LAYOUT_NHD) return VA_ERR_INVALID_ARGUMENT;
+  if (o.quantize != 0 && o.quantize != 1) return VA_ERR_INVALID_ARGUMENT;
+  if (o.quantize && (kv_dtype != VA_DTYPE_FP8_E4M3 || !(isfinite(o.k_scale) && o.k_scale > 0.f) ||
+                     !(isfinite(o.v_scale) && o.v_scale > 0.f)))
+    return VA_ERR_INVALID_ARGUMENT;
+  float rope_scale = o.rope_scale == 0.f ? 1.f : o.rope_scale;
+  if (o.positions && !(isfinite(o.rope_theta) && o.rope_theta > 0.f && isfinite(rope_scale) &&
+                       rope_scale > 0.f))
+    return VA_ERR_INVALID_ARGUMENT;
   if (total_new == 0) return VA_OK;
   if (batch == 0) return VA_ERR_INVALID_ARGUMENT;
   if (!k_new || !v_new || !append_indptr || !kv_indptr || !kv_indices || !last_page_len ||
@@ -438,6 +514,7 @@ int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_
     return VA_ERR_INVALID_ARGUMENT;
   if (total_new > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
   AppendParams p;
+  memset(&p, 0, sizeof(p));
   p.k_new = k_new;
   p.v_new = v_new;
   p.append_indptr = append_indptr;
@@ -447,15 +524,33 @@ int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_
   p.k_cache = k_cache;
   p.v_cache = v_cache;
   p.status = status_d;
+  p.positions = o.positions;
   p.batch = batch;
   p.h_kv = num_kv_heads;
   p.page_size = page_size;
   p.log2_page = log2_int(page_size);
   p.num_pages = num_pages;
-  p.row_chunks = head_dim * (kv_dtype == VA_DTYPE_FP8_E4M3 ? 1 : 2) / 16;
+  p.cache_fp8 = kv_dtype == VA_DTYPE_FP8_E4M3;
+  p.row_chunks = head_dim * (p.cache_fp8 ? 1 : 2) / 16;
+  p.head_dim = head_dim;
+  p.quant = o.quantize;
+  p.nhd = o.kv_layout == VA_LAYOUT_NHD;
+  p.k_scale = o.k_scale;
+  p.v_scale = o.v_scale;
   p.total_new = total_new;
+  if (o.positions) rope_frequencies(o.rope_theta, rope_scale, head_dim, &p.rope);
   cudaError_t e = launch_append(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
+int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_indptr,
+                    const int32_t* kv_indptr, const int32_t* kv_indices,
+                    const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
+                    int num_kv_heads, int head_dim, int page_size, int num_pages,
+                    va_dtype kv_dtype, int64_t total_new, int* status_d, void* stream) {
+  return paged_kv_append_ex(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_page_len,
+                            k_cache, v_cache, batch, num_kv_heads, head_dim, page_size,
+                            num_pages, kv_dtype, total_new, nullptr, status_d, stream);
 }
 
 }  // extern "C"

@@ -61,46 +61,6 @@ __device__ __forceinline__ void grid_dependents_launch() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
-// ---- thread-block clusters / distributed shared memory ----
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-  return r;
-}
-// Hardware barrier over every thread of every CTA in the cluster (release /
-// acquire: shared-memory writes before it are visible to the peers after it).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
-                   : "memory");
-}
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n"
-               : "=f"(v.x), "=f"(v.y)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
 // Two fp32 lanes in one 64-bit register (low word = first) and the packed
 // fp32x2 FMA / add of sm_100+: one instruction for two elements.
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
@@ -149,6 +109,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
   return r;
 }
 
+// Four floats -> four fp8-e4m3 codes (first in the low byte), round to
+// nearest even, finite overflow and infinities saturated to +-448.
+__device__ __forceinline__ uint32_t e4m3x4_rn_satfinite(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -170,6 +139,29 @@ __device__ __forceinline__ uint32_t scale_f16x2(uint32_t v, float a) {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
   return pack_f16x2(lo, hi);
+}
+
+// cos and sin of one RoPE angle, position * (hi + lo), where hi + lo is a
+// frequency held as a float pair.  The product keeps ~46 bits (its rounding
+// error recovered exactly by an FMA) and is reduced modulo 2 pi by the
+// Cody-Waite method (Cody and Waite, "Software Manual for the Elementary
+// Functions", 1980: 2 pi split into a float head and tail, each product
+// with the multiple k taken exactly inside an FMA) before sincosf sees it,
+// so for positions below 2^24 the reduced angle is good to ~1e-7 rad where a
+// plain float product would be off by up to position * 2^-24.
+__device__ __forceinline__ void rope_cos_sin(int pos, float hi, float lo, float* c, float* s) {
+  constexpr float kTwoPiHi = 6.2831854820251465f;      // float nearest to 2 pi
+  constexpr float kTwoPiLo = -1.7484555314695172e-07f;  // 2 pi - kTwoPiHi
+  constexpr float kInvTwoPi = 0.15915493667125702f;
+  const float p = (float)pos;                           // exact below 2^24
+  const float a_hi = p * hi;
+  const float a_err = fmaf(p, hi, -a_hi);               // p * hi - a_hi, exactly
+  const float a_lo = fmaf(p, lo, a_err);
+  const float k = rintf(a_hi * kInvTwoPi);
+  float r = fmaf(-k, kTwoPiHi, a_hi);
+  r = fmaf(-k, kTwoPiLo, r);
+  r += a_lo;
+  sincosf(r, s, c);
 }
 
 // Byte offset of 16-byte chunk `ch` of row `r` in a row-major shared tile of

@@ -9,7 +9,7 @@
 namespace va {
 
 constexpr uint32_t kPlanMagic = 0x31504156u;  // "VAP1"
-constexpr uint32_t kPlanVersion = 1;
+constexpr uint32_t kPlanVersion = 2;
 
 // Key tile of the partial kernels (keys per pipeline stage).  Split chunks are
 // cut on multiples of it, so every tile starts on a page boundary whenever
@@ -66,7 +66,7 @@ struct PlanHeader {
   int64_t total_qo, part_rows, chunk;
   uint64_t off_status, off_items, off_merge, off_part_lse, off_part_out, ws_bytes;
   uint64_t plan_bytes;
-  int64_t cluster;  // > 1: splits of a unit form a thread-block cluster of this size
+  int64_t flags;    // feature bits of the call the plan serves (0: none)
   int64_t n_ctas;   // persistent tcgen05 variants: CTAs (item chains); 0 otherwise
   uint64_t reserved[2];
 };

@@ -32,8 +32,6 @@ struct PartialParams {
   float scale_log2;           // sm_scale * k_scale * log2(e)
   float scale_nat;            // sm_scale * k_scale
   float v_scale;
-  int cluster;                // > 1: the splits of a unit are the CTAs of one thread-block
-                              // cluster (rank = split index) and merge through shared memory
   int n_items;                // work items in `items`
   int n_ctas;                 // persistent tcgen05 variants: item chains (see WorkItem::next)
 };
@@ -49,6 +47,13 @@ struct MergeParams {
   int batch, h_q, h_kv, group;
 };
 
+// RoPE frequencies theta^(-2i/d) / rope_scale, i < d/2, as float pairs hi + lo
+// (computed in double on the host), so that position * frequency keeps ~46
+// bits before the angle is reduced.
+struct RopeFreq {
+  float hi[64], lo[64];
+};
+
 struct AppendParams {
   const void* k_new;
   const void* v_new;
@@ -59,46 +64,36 @@ struct AppendParams {
   void* k_cache;
   void* v_cache;
   int* status;                // nullable
-  int batch, h_kv, page_size, log2_page, num_pages, row_chunks;  // row_chunks: 16-byte chunks per row
+  const int32_t* positions;   // nullable: RoPE position of each new token's key
+  int batch, h_kv, page_size, log2_page, num_pages, row_chunks;  // row_chunks: 16-byte chunks per cache row
+  int head_dim;
+  int cache_fp8;              // cache dtype e4m3 (else bf16)
+  int quant;                  // bf16 source rows into an e4m3 cache
+  int nhd;                    // cache layout [pages, P, h_kv, d] (else [pages, h_kv, P, d])
+  float k_scale, v_scale;     // quantising append: stored = e4m3(x / scale)
   int64_t total_new;
+  RopeFreq rope;
 };
 
 // Launch `func` with void** args; pdl = true lets the grid be scheduled
 // before the previous kernel in the stream finishes (programmatic dependent
 // launch); such kernels call grid_dependency_wait() before touching memory.
 inline cudaError_t launch_kernel(const void* func, dim3 grid, dim3 block, size_t smem,
-                                 cudaStream_t stream, void** args, bool pdl, int cluster = 1) {
+                                 cudaStream_t stream, void** args, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   int n = 0;
   if (pdl) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
   }
-  if (cluster > 1) {  // grid.x is a multiple of the cluster size (the planner makes it so)
-    if (cluster > 8) {
-      cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-    }
-    attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = (unsigned)cluster;
-    attr[n].val.clusterDim.y = 1;
-    attr[n].val.clusterDim.z = 1;
-    ++n;
-  }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  if (cluster > 1) {  // refuse a cluster shape the GPU cannot co-schedule
-    int fit = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&fit, func, &cfg);
-    if (e != cudaSuccess) return e;
-    if (fit < 1) return cudaErrorLaunchOutOfResources;
-  }
   return cudaLaunchKernelExC(&cfg, func, args);
 }
 

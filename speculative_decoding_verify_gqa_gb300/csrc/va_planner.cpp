@@ -62,8 +62,9 @@ int plan_bounds(int batch, int64_t total_qo, int num_qo_heads, int num_kv_heads,
   int64_t target = (int64_t)kMaxTargetPerSm * num_sms;
   // sum_u ceil(kv_end_u / C) <= W / C + units <= target + units.
   int64_t items = target + units;
-  // Split units hold kv_end > C keys, so their split counts total < 2 W / C.
-  int64_t part_rows = 128 * 2 * target;
+  // Split units hold kv_end > C keys, so their split counts total < 2 W / C
+  // <= 2 target, each with at most the largest block's rows (256).
+  int64_t part_rows = 256 * 2 * target;
   size_t pb = sizeof(PlanHeader) + (size_t)(items + units) * 32;
   size_t ws = kWsAlign + (size_t)(items + units) * 32;
   ws = align_up(ws, kWsAlign) + (size_t)part_rows * 4;
@@ -88,9 +89,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   if (opts) o = *opts;
   for (int r : o.reserved)
     if (r) return VA_ERR_INVALID_ARGUMENT;
-  if (o.max_splits < 0 || o.min_chunk < 0 || o.target_ctas < 0 || o.cluster < -1 ||
-      o.cluster == 1 || o.cluster > 16)
-    return VA_ERR_INVALID_ARGUMENT;
+  if (o.max_splits < 0 || o.min_chunk < 0 || o.target_ctas < 0) return VA_ERR_INVALID_ARGUMENT;
   if (o.kernel != VA_KERNEL_AUTO && o.kernel != VA_KERNEL_MMA_64 && o.kernel != VA_KERNEL_MMA_128 &&
       o.kernel != VA_KERNEL_TC_128 && o.kernel != VA_KERNEL_TC_256)
     return VA_ERR_INVALID_ARGUMENT;
@@ -274,56 +273,14 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     }
   }
 
-  // Cluster merge (warp-level variant, on request): when every unit has the
-  // same kv range and the units fill at most half the CTA slots, each (unit,
-  // KV head) is cut into the same number n in [2, cap] of chunks of >= 64
-  // keys, and its n CTAs run as one thread-block cluster that merges in shared
-  // memory -- no merge launch and no partials.  Not the default: on GB300 the
-  // Llama-3-8B-shaped tree verify step measured 19.4 us with the workspace
-  // merge against 28.9 us (cap 8) to 75.9 us (cap 2) with clusters, since a
-  // cluster of one-CTA-per-SM blocks must find its SMs free in one GPC.
-  int64_t cluster = 0;
-  int64_t cluster_chunk = 0;
-  if (o.cluster > 1 && !o.target_ctas && (kernel == kKernelMma64 || kernel == kKernelMma128) &&
-      !units.empty()) {
-    bool uniform = true;
-    for (const Unit& u : units) uniform = uniform && u.kv_end == units[0].kv_end;
-    const int64_t unit_heads = (int64_t)units.size() * num_kv_heads;
-    const int64_t cap = o.cluster;
-    if (uniform && unit_heads * 2 <= slots) {
-      int64_t n = std::min<int64_t>(cap, slots / unit_heads);
-      if (o.max_splits > 0) n = std::min<int64_t>(n, o.max_splits);
-      const int64_t kv = units[0].kv_end;
-      const int64_t cu =
-          std::max<int64_t>(64, ceil_div(ceil_div(kv, std::max<int64_t>(n, 1)), 16) * 16);
-      n = ceil_div(kv, cu);
-      if (n >= 2) {
-        cluster = n;
-        cluster_chunk = cu;
-      }
-    }
-  }
-
   struct Tmp {
     WorkItem it;
     int64_t cost;
-    int64_t order;
   };
   std::vector<Tmp> items;
   std::vector<MergeItem> merges;
   int64_t part_rows = 0;
-  int64_t order = 0;
   for (const Unit& u : units) {
-    if (cluster) {  // rank = split index; the cluster's CTAs are contiguous
-      for (int h = 0; h < num_kv_heads; ++h)
-        for (int64_t s = 0; s < cluster; ++s) {
-          const int64_t lo = s * cluster_chunk;
-          const int64_t hi = std::min<int64_t>(lo + cluster_chunk, u.kv_end);
-          WorkItem w{u.b, h, u.row0, u.nrows, (int32_t)lo, (int32_t)hi, -1, -1};
-          items.push_back({w, 0, order++});
-        }
-      continue;
-    }
     int64_t cu;
     const int64_t n = split_of(u, chunk, equal, &cu);
     for (int h = 0; h < num_kv_heads; ++h) {
@@ -336,7 +293,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
         int64_t lo = s * cu, hi = std::min<int64_t>(lo + cu, u.kv_end);
         WorkItem w{u.b, h, u.row0, u.nrows, (int32_t)lo, (int32_t)hi,
                    n > 1 ? (int32_t)(base + s * u.nrows) : -1, -1};
-        items.push_back({w, (hi - lo) * (int64_t)(u.nrows + 16), order++});
+        items.push_back({w, (hi - lo) * (int64_t)(u.nrows + 16)});
       }
     }
   }
@@ -344,8 +301,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   // Longest first; among equals, row blocks that read the same (request, KV
   // head, kv chunk) sit next to each other so they run together and the
   // later ones find the chunk in L2.
-  if (!cluster)
-    std::stable_sort(items.begin(), items.end(), [](const Tmp& a, const Tmp& b) {
+  std::stable_sort(items.begin(), items.end(), [](const Tmp& a, const Tmp& b) {
       if (a.cost != b.cost) return a.cost > b.cost;
       if (a.it.b != b.it.b) return a.it.b < b.it.b;
       if (a.it.h != b.it.h) return a.it.h < b.it.h;
@@ -424,9 +380,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   hd.off_part_out = align_up(hd.off_part_lse + (size_t)part_rows * 4, kWsAlign);
   hd.ws_bytes = align_up(hd.off_part_out + (size_t)part_rows * head_dim * 4, kWsAlign);
   hd.plan_bytes = need;
-  hd.cluster = cluster;
   hd.n_ctas = n_ctas;
-  if (cluster) hd.chunk = cluster_chunk;
 
   char* dst = static_cast<char*>(plan_h);
   std::memcpy(dst, &hd, sizeof(hd));

@@ -36,7 +36,8 @@ def test_header_declares_the_boundary_calls():
     names = _declared_functions()
     for must in ("verify_attn_plan", "verify_attn_run", "paged_kv_append",
                  "verify_attn_plan_host", "verify_attn_partial", "verify_attn_merge",
-                 "verify_attn_device_status", "verify_attn_status_string"):
+                 "verify_attn_device_status", "verify_attn_status_string",
+                 "verify_attn_workspace_size"):
         assert must in names
 
 
@@ -48,7 +49,7 @@ def test_library_exports_every_declared_symbol(va):
 
 def test_status_strings(va):
     assert va.status_string(0) == "ok"
-    for code in range(-7, 0):
+    for code in range(-8, 0):
         assert va.status_string(code) != "unknown status"
     assert va.status_string(-99) == "unknown status"
 
@@ -77,20 +78,13 @@ def _check_cover(va, t, plan):
     assert hd["n_items"] == len(items) and hd["n_merge"] == len(merges)
     BM = hd["block_rows"]
     G = t["G"]
-    cl = hd["cluster"]
     units = {}
     for i, it in enumerate(items):
         b, h, row0, nrows, lo, hi, part_row, _ = (int(x) for x in it)
         assert 0 <= b < len(t["L"]) and 0 <= h < t["h_kv"]
         assert 0 < nrows <= BM and row0 % BM == 0
-        assert lo % (16 if cl else 64) == 0 and lo < hi
-        if cl:   # a cluster's CTAs are contiguous, rank = split index
-            first = items[i - i % cl]
-            assert (first[0], first[1], first[2]) == (b, h, row0) and part_row == -1
-            assert lo == (i % cl) * hd["chunk"]
+        assert lo % 64 == 0 and lo < hi
         units.setdefault((b, h, row0, nrows), []).append((lo, hi, part_row))
-    if cl:
-        assert 2 <= cl <= 16 and len(items) % cl == 0 and hd["n_merge"] == 0
     for b in range(len(t["L"])):
         R = G * int(t["L"][b])
         for h in range(t["h_kv"]):
@@ -114,7 +108,7 @@ def _check_cover(va, t, plan):
             assert lo == pos
             pos = hi
         assert pos == kv_end
-        if len(chunks) == 1 or cl:
+        if len(chunks) == 1:
             assert all(c[2] == -1 for c in chunks) and (b, h, row0, nrows) not in merge_by_unit
         else:
             m = merge_by_unit[(b, h, row0, nrows)]
@@ -286,6 +280,31 @@ def test_plan_items_sorted_longest_first(va):
     it = plan.items()
     cost = (it[:, 5] - it[:, 4]) * (it[:, 3] + 16)
     assert np.all(np.diff(cost) <= 0)
+
+
+@pytest.mark.parametrize("name", synthetic.WORKLOAD_ORDER)
+def test_workspace_size_covers_the_named_workloads(va, name):
+    """verify_attn_workspace_size(batch, heads, head_dim, max_qo_len, SMs),
+    through the C ABI, is at least what the planner needs for each named
+    workload, whatever kernel variant or split option the plan takes."""
+    wl = synthetic.make_workload(name, with_values=False)
+    n = ctypes.c_size_t(0)
+    rc = va.lib().verify_attn_workspace_size(wl.batch, wl.h_q, wl.h_kv, wl.d,
+                                             int(wl.qo_lens.max()), 152, ctypes.byref(n))
+    assert rc == 0 and n.value > 0
+    kernels = [0, 1, 2] + ([3, 4] if wl.d == 128 and 128 % wl.group == 0 else [])
+    for kernel in kernels:
+        for opts in (dict(), dict(max_splits=1), dict(target_ctas=5000, min_chunk=64)):
+            plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
+                                            wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                            kv_dtype=wl.kv_dtype, num_sms=152, kernel=kernel,
+                                            **opts)
+            assert plan.workspace_bytes <= n.value
+    assert va.verify_attn_workspace_size(wl.batch, wl.h_q, wl.h_kv, wl.d,
+                                         int(wl.qo_lens.max()), 152) == n.value
+    assert va.lib().verify_attn_workspace_size(-1, 4, 2, 128, 1, 152, ctypes.byref(n)) == -1
+    assert va.lib().verify_attn_workspace_size(1, 5, 2, 128, 1, 152, ctypes.byref(n)) == -1
+    assert va.lib().verify_attn_workspace_size(1, 4, 2, 128, 1, 152, None) == -1
 
 
 # ------------------------------------------------------------------ validation

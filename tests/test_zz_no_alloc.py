@@ -34,11 +34,9 @@ def test_static_scratch_matches_run_twice_in_a_row(va, name):
     ref_out, ref_lse, plan = dw.run()            # the existing entry point, caller workspace
     torch.cuda.synchronize()
     # a host-only plan: this caller never allocates a device workspace
-    # (workspace merge rather than the in-cluster merge, so that the split
-    # partials really live in the static array)
     hplan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
                                      wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
-                                     kv_dtype=wl.kv_dtype, cluster=-1)
+                                     kv_dtype=wl.kv_dtype)
     if name == "llama3_8b_tree_verify":
         assert hplan.header()["n_merge"] > 0     # the split partials live in the static array
     assert hplan.workspace_bytes <= va.STATIC_SCRATCH_BYTES
@@ -63,6 +61,37 @@ def test_static_scratch_matches_run_twice_in_a_row(va, name):
         assert np.abs(o - ref_o).max() <= 1e-2
         assert np.abs(l - ref_l).max() <= 1e-3
         compare(wl, out, lse, rows=None if name == "tiny_verify" else synthetic.sample_rows(wl, 64))
+
+
+def test_static_scratch_wrapper_fp8_two_q_tiles_with_merge(va):
+    """The Python wrapper of the same entry point, on an fp8 cache with the
+    two-Q-tile tcgen05 kernel and a plan forced to split (so the merge reads
+    partials from the static array), twice in a row: equal to
+    verify_attn_run with a caller workspace, and to the oracle."""
+    wl = synthetic.make_custom(batch=2, h_q=16, h_kv=2, d=128, prefix=("fixed", [900, 130]),
+                               qo=("fixed", [40, 20]), mask="tree", kv_dtype=synthetic.FP8,
+                               seed=71)
+    dw = DeviceWorkload(wl)
+    opts = dict(kernel=4, target_ctas=64, min_chunk=128)
+    ref_out, ref_lse, _ = dw.run(**opts)
+    torch.cuda.synchronize()
+    hplan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
+                                     wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                     kv_dtype=wl.kv_dtype, **opts)
+    hd = hplan.header()
+    assert hd["kernel"] == 4 and hd["n_merge"] > 0
+    for call in range(2):
+        out = torch.full_like(dw.q, float("nan"))
+        lse = torch.full(dw.q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+        va.verify_attn_run_static_scratch(dw.q, dw.k_cache, dw.v_cache, dw.kv_indptr,
+                                          dw.kv_indices, dw.last_page_len, dw.qo_indptr,
+                                          dw.mask, dw.mask_indptr, hplan, sm_scale=wl.sm_scale,
+                                          k_scale=wl.k_scale, v_scale=wl.v_scale, out=out,
+                                          lse=lse)
+        torch.cuda.synchronize()
+        assert float((out.float() - ref_out.float()).abs().max()) <= 1e-2
+        assert float((lse - ref_lse).abs().max()) <= 1e-3
+        compare(wl, out, lse)
 
 
 def test_static_scratch_refuses_plans_beyond_its_size(va):
