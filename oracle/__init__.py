@@ -81,6 +81,18 @@ def _load():
         lib.oracle_paged_kv_append_quant.restype = i32
         lib.oracle_paged_kv_append_quant.argtypes = [P, P, ctypes.c_float, ctypes.c_float, P, P,
                                                      P, P, i32, i32, i32, i32, i32, P, P]
+        lib.oracle_encode_bf16.restype = ctypes.c_uint16
+        lib.oracle_encode_bf16.argtypes = [dbl]
+        lib.oracle_rope_vec.restype = None
+        lib.oracle_rope_vec.argtypes = [P, i32, dbl, dbl, dbl]
+        lib.oracle_paged_kv_append_ex.restype = i32
+        lib.oracle_paged_kv_append_ex.argtypes = [P, P, i32, i32, ctypes.c_float, ctypes.c_float,
+                                                  i32, P, dbl, dbl, P, P, P, P, i32, i32, i32,
+                                                  i32, i32, P, P]
+        lib.oracle_verify_attn_ex.restype = i32
+        lib.oracle_verify_attn_ex.argtypes = [P, P, P, i32, i32, P, P, P, P, P, P, i32, P, dbl,
+                                              dbl, i32, i32, i32, i32, i32, i32, dbl, dbl, dbl,
+                                              P, i64, P, P, i32]
         _lib = lib
         return lib
 
@@ -149,6 +161,87 @@ def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_le
     if rc != 0:
         raise ValueError("oracle_verify_attn rejected its inputs (status %d)" % rc)
     return out[:n], lse[:n]
+
+
+def verify_attn_ex(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_len,
+                   qo_indptr, mask, mask_indptr, h_q, h_kv, d, page_size, num_pages, sm_scale,
+                   k_scale=1.0, v_scale=1.0, kv_layout=0, mask_layout=0, q_pos=None,
+                   rope_theta=0.0, rope_scale=1.0, rows=None, nthreads=None):
+    """verify_attn with the cache layout (0 HND, 1 NHD), the mask layout (0:
+    L x L draft blocks, 1: L x kv_len rows) and optional query positions for
+    the rotary embedding of the queries (the cache holds keys as stored)."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint8 if kv_fp8 else np.uint16)
+    vc = _c(v_cache, np.uint8 if kv_fp8 else np.uint16)
+    kv_indptr = _c(kv_indptr, np.int32); kv_indices = _c(kv_indices, np.int32)
+    last_page_len = _c(last_page_len, np.int32); qo_indptr = _c(qo_indptr, np.int32)
+    mask = _c(mask, np.uint8); mask_indptr = _c(mask_indptr, np.int32)
+    q_pos = _c(q_pos, np.int32)
+    batch = len(qo_indptr) - 1
+    total_qo = int(qo_indptr[-1])
+    sel = _c(rows, np.int32)
+    n = total_qo * h_q if sel is None else len(sel)
+    out = np.zeros((max(n, 1), d)); lse = np.zeros(max(n, 1))
+    rc = lib.oracle_verify_attn_ex(_p(q), _p(kc), _p(vc), int(bool(kv_fp8)), int(kv_layout),
+                                   _p(kv_indptr), _p(kv_indices), _p(last_page_len),
+                                   _p(qo_indptr), _p(mask), _p(mask_indptr), int(mask_layout),
+                                   _p(q_pos), float(rope_theta), float(rope_scale), batch, h_q,
+                                   h_kv, d, page_size, num_pages, float(sm_scale),
+                                   float(k_scale), float(v_scale), _p(sel), int(n), _p(out),
+                                   _p(lse), int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_verify_attn_ex rejected its inputs (status %d)" % rc)
+    return out[:n], lse[:n]
+
+
+def encode_bf16(x) -> np.ndarray:
+    """bf16 bits (uint16) of the values nearest to x (ties to even)."""
+    lib = _load()
+    flat = np.asarray(x, dtype=np.float64).reshape(-1)
+    return np.array([lib.oracle_encode_bf16(float(v)) for v in flat],
+                    dtype=np.uint16).reshape(np.shape(x))
+
+
+def rope(x, pos, theta, scale=1.0) -> np.ndarray:
+    """LLaMA rotate-half rotary embedding of the last axis of x (fp64) at
+    position pos."""
+    lib = _load()
+    a = np.array(x, dtype=np.float64)
+    flat = a.reshape(-1, a.shape[-1])
+    for r in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[r])
+        lib.oracle_rope_vec(_p(row), row.shape[0], float(pos), float(theta), float(scale))
+        flat[r] = row
+    return flat.reshape(a.shape)
+
+
+def paged_kv_append_ex(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_page_len,
+                       page_size, num_pages, k_cache, v_cache, cache_fp8, quantize=False,
+                       k_scale=1.0, v_scale=1.0, kv_layout=0, positions=None, rope_theta=0.0,
+                       rope_scale=1.0):
+    """Host scatter with the extended append's options (in place on k_cache /
+    v_cache: numpy pools [pages, h_kv, P, d] (HND) or [pages, P, h_kv, d]
+    (NHD) of the cache dtype's bits)."""
+    lib = _load()
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    src_dt = np.uint16 if (quantize or not cache_fp8) else np.uint8
+    k_new = np.ascontiguousarray(k_new, dtype=src_dt)
+    v_new = np.ascontiguousarray(v_new, dtype=src_dt)
+    if kv_layout == 1:
+        h_kv, d = k_cache.shape[2], k_cache.shape[3]
+    else:
+        h_kv, d = k_cache.shape[1], k_cache.shape[3]
+    idx = [_c(a, np.int32) for a in (append_indptr, kv_indptr, kv_indices, last_page_len)]
+    pos = _c(positions, np.int32)
+    rc = lib.oracle_paged_kv_append_ex(_p(k_new), _p(v_new), int(bool(cache_fp8)),
+                                       int(bool(quantize)), float(k_scale), float(v_scale),
+                                       int(kv_layout), _p(pos), float(rope_theta),
+                                       float(rope_scale), *[_p(a) for a in idx],
+                                       len(idx[0]) - 1, h_kv, d, page_size, num_pages,
+                                       _p(k_cache), _p(v_cache))
+    if rc != 0:
+        raise ValueError("oracle_paged_kv_append_ex rejected its inputs (status %d)" % rc)
 
 
 def attn_range(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_len, qo_indptr,
@@ -232,18 +325,33 @@ def paged_kv_append_quant(k_new, v_new, k_scale, v_scale, append_indptr, kv_indp
 
 def build_cache(wl):
     """The workload's page pool, written by the oracle's own host scatter:
-    sentinel-filled (NaN bytes), then every token of every request appended."""
+    sentinel-filled (NaN bytes), then every token of every request appended
+    (in the workload's cache layout; keys rotated at their positions when the
+    workload uses rotary positions)."""
     import synthetic
     kc = synthetic.sentinel_pool(wl)
     vc = synthetic.sentinel_pool(wl)
-    paged_kv_append(wl.k_tok, wl.v_tok, wl.tok_append_indptr(), wl.kv_indptr, wl.kv_indices,
-                    wl.last_page_len, wl.page_size, wl.num_pages, kc, vc)
+    if not wl.nhd and wl.kv_pos is None:
+        paged_kv_append(wl.k_tok, wl.v_tok, wl.tok_append_indptr(), wl.kv_indptr, wl.kv_indices,
+                        wl.last_page_len, wl.page_size, wl.num_pages, kc, vc)
+        return kc, vc
+    paged_kv_append_ex(wl.k_tok, wl.v_tok, wl.tok_append_indptr(), wl.kv_indptr, wl.kv_indices,
+                       wl.last_page_len, wl.page_size, wl.num_pages, kc, vc,
+                       cache_fp8=wl.kv_dtype == "fp8_e4m3", kv_layout=1 if wl.nhd else 0,
+                       positions=wl.kv_pos, rope_theta=wl.rope_theta or 0.0)
     return kc, vc
 
 
 def verify_attn_workload(wl, rows=None, nthreads=None, caches=None):
     kc, vc = caches if caches is not None else build_cache(wl)
-    return verify_attn(wl.q, kc, vc, wl.kv_dtype == "fp8_e4m3", wl.kv_indptr, wl.kv_indices,
-                       wl.last_page_len, wl.qo_indptr, wl.mask, wl.mask_indptr, wl.h_q, wl.h_kv,
-                       wl.d, wl.page_size, wl.num_pages, wl.sm_scale, wl.k_scale, wl.v_scale,
-                       rows=rows, nthreads=nthreads)
+    if not wl.nhd and wl.mask_layout == "qlen" and wl.q_pos is None:
+        return verify_attn(wl.q, kc, vc, wl.kv_dtype == "fp8_e4m3", wl.kv_indptr, wl.kv_indices,
+                           wl.last_page_len, wl.qo_indptr, wl.mask, wl.mask_indptr, wl.h_q,
+                           wl.h_kv, wl.d, wl.page_size, wl.num_pages, wl.sm_scale, wl.k_scale,
+                           wl.v_scale, rows=rows, nthreads=nthreads)
+    return verify_attn_ex(wl.q, kc, vc, wl.kv_dtype == "fp8_e4m3", wl.kv_indptr, wl.kv_indices,
+                          wl.last_page_len, wl.qo_indptr, wl.mask, wl.mask_indptr, wl.h_q,
+                          wl.h_kv, wl.d, wl.page_size, wl.num_pages, wl.sm_scale, wl.k_scale,
+                          wl.v_scale, kv_layout=1 if wl.nhd else 0,
+                          mask_layout=1 if wl.mask_layout == "full" else 0, q_pos=wl.q_pos,
+                          rope_theta=wl.rope_theta or 0.0, rows=rows, nthreads=nthreads)

@@ -26,11 +26,31 @@ def _decode(bits: np.ndarray, kv_fp8: bool) -> np.ndarray:
     return t.view(torch.int16).view(torch.bfloat16).to(torch.float64).numpy()
 
 
+def _rotate(x, pos, theta, scale):
+    """Rotary embedding of one row, pair (i, i + d/2) as a point in the plane
+    turned by pos / scale * theta^(-2i/d) radians counter-clockwise."""
+    d = len(x)
+    h = d // 2
+    y = list(x)
+    for i in range(h):
+        a = pos / scale * theta ** (-2.0 * i / d)
+        y[i] = x[i] * math.cos(a) - x[i + h] * math.sin(a)
+        y[i + h] = x[i] * math.sin(a) + x[i + h] * math.cos(a)
+    return y
+
+
 def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_len, qo_indptr,
-                mask, mask_indptr, h_q, h_kv, d, page_size, sm_scale, k_scale=1.0, v_scale=1.0):
+                mask, mask_indptr, h_q, h_kv, d, page_size, sm_scale, k_scale=1.0, v_scale=1.0,
+                kv_layout=0, mask_layout=0, q_pos=None, rope_theta=0.0, rope_scale=1.0):
+    """kv_layout 1: the cache is [pages, page_size, h_kv, d]; mask_layout 1:
+    request b's mask is L rows of kv_len bits (prefix included); q_pos: each
+    query row is rotated at its token's position before the dot products."""
     qd = _decode(q, False)
     kd = _decode(k_cache, kv_fp8)
     vd = _decode(v_cache, kv_fp8)
+    if kv_layout == 1:   # view as [pages, h_kv, P, d] by swapping the middle axes
+        kd = kd.transpose(0, 2, 1, 3)
+        vd = vd.transpose(0, 2, 1, 3)
     G = h_q // h_kv
     total = int(qo_indptr[-1])
     out = np.zeros((total * h_q, d))
@@ -45,8 +65,15 @@ def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_le
             for qh in range(h_q):
                 h = qh // G
                 logits, values = [], []
+                qrow = [float(qd[tok, qh, e]) for e in range(d)]
+                if q_pos is not None:
+                    qrow = _rotate(qrow, float(q_pos[tok]), rope_theta, rope_scale)
                 for j in range(kv_len):
-                    if j >= prefix:
+                    if mask is not None and mask_layout == 1:
+                        bit = int(mask_indptr[b]) + t * kv_len + j
+                        if (int(mask[bit // 8]) >> (bit % 8)) & 1 == 0:
+                            continue
+                    elif j >= prefix:
                         u = j - prefix
                         if mask is None:
                             vis = u <= t
@@ -57,7 +84,7 @@ def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_le
                             continue
                     page = int(kv_indices[int(kv_indptr[b]) + j // page_size])
                     slot = j % page_size
-                    dot = math.fsum(float(qd[tok, qh, e]) * float(kd[page, h, slot, e]) * k_scale
+                    dot = math.fsum(qrow[e] * float(kd[page, h, slot, e]) * k_scale
                                     for e in range(d))
                     logits.append(sm_scale * dot)
                     values.append([float(vd[page, h, slot, e]) * v_scale for e in range(d)])

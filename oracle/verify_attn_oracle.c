@@ -75,10 +75,10 @@ double oracle_decode_e4m3(uint8_t bits) {
  * 0 (round to nearest even); finite overflow and infinities saturate to
  * +-448, the largest finite value ("satfinite"); NaN gives the NaN code
  * 0x7F. */
-uint8_t oracle_encode_e4m3_satfinite(float x) {
+static uint8_t encode_e4m3_value(double x) {
     if (isnan(x)) return 0x7F;
     uint8_t sign = signbit(x) ? 0x80 : 0x00;
-    double a = fabs((double)x);
+    double a = fabs(x);
     if (a >= 448.0) return sign | 0x7E;
     if (a < ldexp(1.0, -6)) {
         /* subnormal range: multiples of 2^-9; 8 * 2^-9 = 2^-6 is code 0x08 */
@@ -95,6 +95,50 @@ uint8_t oracle_encode_e4m3_satfinite(float x) {
     }
     if (e > 8 || (e == 8 && m > 14.0)) return sign | 0x7E;
     return sign | (uint8_t)(((e + 7) << 3) | ((int)m - 8));
+}
+
+uint8_t oracle_encode_e4m3_satfinite(float x) { return encode_e4m3_value((double)x); }
+
+/* bf16 bits of the value nearest to x (ties to the even code): 8 significant
+ * bits, exponents down to 2^-126 with subnormals at multiples of 2^-133,
+ * overflow to infinity (binary32's exponent range). */
+uint16_t oracle_encode_bf16(double x) {
+    union { float f; uint32_t u; } v;
+    if (isnan(x)) return 0x7FC0;
+    double a = fabs(x);
+    double r;
+    if (a == 0.0 || isinf(a)) {
+        r = a;
+    } else {
+        int ex;
+        (void)frexp(a, &ex);
+        int e = ex - 1;
+        if (e < -126) e = -126;
+        double m = nearbyint(ldexp(a, 7 - e));
+        r = ldexp(m, e - 7);
+        /* the largest finite bf16 is (2 - 2^-7) * 2^127; a tie above it rounds up */
+        if (r >= ldexp(1.0, 128)) r = INFINITY;
+    }
+    v.f = (float)r;                   /* exact: r is on the bf16 grid */
+    uint16_t bits = (uint16_t)(v.u >> 16);
+    return signbit(x) ? (uint16_t)(bits | 0x8000) : bits;
+}
+
+/* LLaMA-style rotary position embedding of one d-vector in place ("rotate
+ * half": element i pairs with i + d/2): for i < d/2, with angle
+ * a_i = pos / scale * theta^(-2i/d),
+ *   y_i = x_i cos a_i - x_{i+d/2} sin a_i,  y_{i+d/2} = x_{i+d/2} cos a_i + x_i sin a_i.
+ * FlashInfer PR #286 names it ROPE_LLAMA (rope_theta, rope_scale); FlashInfer
+ * issue #152 asks for it at each draft's tree position. */
+void oracle_rope_vec(double* x, int d, double pos, double theta, double scale) {
+    int half = d / 2;
+    for (int i = 0; i < half; ++i) {
+        double a = pos / scale * pow(theta, -2.0 * i / d);
+        double c = cos(a), sn = sin(a);
+        double x0 = x[i], x1 = x[i + half];
+        x[i] = x0 * c - x1 * sn;
+        x[i + half] = x1 * c + x0 * sn;
+    }
 }
 
 /* The binary32 quotient x / scale, correctly rounded: the quotient of two
@@ -178,9 +222,17 @@ void oracle_dense_attention(int n_rows, int n_keys, int d, const double* Q, int6
     }
 }
 
+/* Row index of (page, head, slot) in a cache of the given layout: HND
+ * [pages][h_kv][P][d] or NHD [pages][P][h_kv][d] (FlashInfer PR #286's
+ * kv_layout). */
+static int64_t cache_row(int layout, int64_t page, int h, int64_t slot, int h_kv, int page_size) {
+    if (layout == 1) return (page * page_size + slot) * h_kv + h;
+    return (page * h_kv + h) * page_size + slot;
+}
+
 /* Gather request b's K and V into [kv_len][h_kv][d] doubles (decoded and
  * scaled), walking its pages in order and stopping at kv_len. */
-static void gather_request(const void* k_cache, const void* v_cache, int kv_fp8,
+static void gather_request(const void* k_cache, const void* v_cache, int kv_fp8, int layout,
                            const int32_t* kv_indptr, const int32_t* kv_indices, int b,
                            int64_t kv_len, int h_kv, int d, int page_size, double k_scale,
                            double v_scale, double* K, double* V) {
@@ -188,7 +240,7 @@ static void gather_request(const void* k_cache, const void* v_cache, int kv_fp8,
         int32_t page = kv_indices[kv_indptr[b] + j / page_size];
         int64_t slot = j % page_size;
         for (int h = 0; h < h_kv; ++h) {
-            int64_t src = (((int64_t)page * h_kv + h) * page_size + slot) * d;
+            int64_t src = cache_row(layout, page, h, slot, h_kv, page_size) * d;
             int64_t dst = (j * h_kv + h) * d;
             for (int e = 0; e < d; ++e) {
                 K[dst + e] = decode_kv(k_cache, src + e, kv_fp8) * k_scale;
@@ -202,16 +254,21 @@ static int mask_bit(const uint8_t* mask, int64_t bit) {
     return (mask[bit >> 3] >> (bit & 7)) & 1;
 }
 
-/* Request b's explicit [L][kv_len] additive mask: prefix columns 0; draft
- * column prefix + u is 0 when visible to token t (mask bit (t, u), or u <= t
- * with no mask) and -inf otherwise. */
-static void build_mask(const uint8_t* mask, const int32_t* mask_indptr, int b, int64_t L,
-                       int64_t kv_len, double* M) {
+/* Request b's explicit [L][kv_len] additive mask.  Layout 0 (each request's
+ * L x L draft block, as flashmap's QLEN_ONLY custom mask): prefix columns 0;
+ * draft column prefix + u is 0 when visible to token t (mask bit (t, u) at
+ * mask_indptr[b] + t * L + u, or u <= t with no mask) and -inf otherwise.
+ * Layout 1 (flashmap's full custom mask: L rows of kv_len bits): column j is
+ * 0 iff bit mask_indptr[b] + t * kv_len + j is set, prefix columns included. */
+static void build_mask(const uint8_t* mask, const int32_t* mask_indptr, int mask_layout, int b,
+                       int64_t L, int64_t kv_len, double* M) {
     int64_t prefix = kv_len - L;
     for (int64_t t = 0; t < L; ++t) {
         for (int64_t j = 0; j < kv_len; ++j) {
             int visible;
-            if (j < prefix) {
+            if (mask && mask_layout == 1) {
+                visible = mask_bit(mask, (int64_t)mask_indptr[b] + t * kv_len + j);
+            } else if (j < prefix) {
                 visible = 1;
             } else {
                 int64_t u = j - prefix;
@@ -232,6 +289,8 @@ typedef struct {
     int64_t kv_len, L, qo_start;
     int h_q, h_kv, d, group;
     double sm_scale;
+    const int32_t* q_pos;  /* NULL: no rotary embedding of the queries */
+    double rope_theta, rope_scale;
     const int64_t* rows;   /* flat row ids token*h_q+head of this request */
     const int64_t* dest;   /* where each row's result goes */
     int64_t n_rows;
@@ -260,6 +319,8 @@ static void* run_rows(void* arg) {
         int64_t t = tok - jb->qo_start;
         for (int e = 0; e < jb->d; ++e)
             qrow[e] = oracle_decode_bf16(jb->q[flat * jb->d + e]);
+        if (jb->q_pos)
+            oracle_rope_vec(qrow, jb->d, (double)jb->q_pos[tok], jb->rope_theta, jb->rope_scale);
         /* One query row against the request's keys of KV head h: K/V rows are
          * [j][h][:] so the row stride is h_kv * d and the base is offset by h. */
         oracle_dense_attention(1, (int)jb->kv_len, jb->d, qrow, jb->d,
@@ -276,21 +337,33 @@ static void* run_rows(void* arg) {
 /*
  * The whole verify attention of a batch, or of a selection of output rows.
  *  q        [total_qo, h_q, d] bf16 bits
- *  k_cache, v_cache [num_pages, h_kv, page_size, d] bf16 (kv_fp8 = 0) or
- *           fp8-e4m3 (kv_fp8 = 1) bit patterns
+ *  k_cache, v_cache bf16 (kv_fp8 = 0) or fp8-e4m3 (kv_fp8 = 1) bit patterns
+ *           in the HND (kv_layout 0: [num_pages, h_kv, page_size, d]) or NHD
+ *           (kv_layout 1: [num_pages, page_size, h_kv, d]) layout; the cache
+ *           holds keys as stored (rotated by the append when RoPE is used)
+ *  mask_layout: 0 = each request's L x L draft block, 1 = L rows of kv_len
+ *           bits (see build_mask)
+ *  q_pos    NULL, or [total_qo] positions: each query row is rotated by
+ *           oracle_rope_vec at its token's position (rope_theta, rope_scale)
+ *           before the dot products
  *  sel / n_sel: flat row ids token * h_q + head to compute (NULL = all rows,
  *           in flat order); out [n, d] and lse [n] follow the selection order.
  *  nthreads: worker threads (>= 1).
  * Returns 0, or a negative code on an inconsistent page table.
  */
-int oracle_verify_attn(const uint16_t* q, const void* k_cache, const void* v_cache, int kv_fp8,
-                       const int32_t* kv_indptr, const int32_t* kv_indices,
-                       const int32_t* last_page_len, const int32_t* qo_indptr,
-                       const uint8_t* mask, const int32_t* mask_indptr, int batch, int h_q,
-                       int h_kv, int d, int page_size, int num_pages, double sm_scale,
-                       double k_scale, double v_scale, const int32_t* sel, int64_t n_sel,
-                       double* out, double* lse, int nthreads) {
+int oracle_verify_attn_ex(const uint16_t* q, const void* k_cache, const void* v_cache,
+                          int kv_fp8, int kv_layout, const int32_t* kv_indptr,
+                          const int32_t* kv_indices, const int32_t* last_page_len,
+                          const int32_t* qo_indptr, const uint8_t* mask,
+                          const int32_t* mask_indptr, int mask_layout, const int32_t* q_pos,
+                          double rope_theta, double rope_scale, int batch, int h_q, int h_kv,
+                          int d, int page_size, int num_pages, double sm_scale, double k_scale,
+                          double v_scale, const int32_t* sel, int64_t n_sel, double* out,
+                          double* lse, int nthreads) {
     if (h_kv <= 0 || h_q <= 0 || h_q % h_kv != 0 || d <= 0 || nthreads < 1) return OR_EINVAL;
+    if ((kv_layout != 0 && kv_layout != 1) || (mask_layout != 0 && mask_layout != 1))
+        return OR_EINVAL;
+    if (q_pos && !(rope_theta > 0.0 && rope_scale > 0.0)) return OR_EINVAL;
     int rc = check_tables(kv_indptr, kv_indices, last_page_len, qo_indptr, batch, page_size,
                           num_pages);
     if (rc) return rc;
@@ -298,7 +371,8 @@ int oracle_verify_attn(const uint16_t* q, const void* k_cache, const void* v_cac
         if (!mask_indptr) return OR_EINVAL;
         for (int b = 0; b < batch; ++b) {
             int64_t L = qo_indptr[b + 1] - qo_indptr[b];
-            if ((int64_t)mask_indptr[b + 1] - mask_indptr[b] != L * L) return OR_EINVAL;
+            int64_t cols = mask_layout == 1 ? oracle_kv_len(kv_indptr, last_page_len, b, page_size) : L;
+            if ((int64_t)mask_indptr[b + 1] - mask_indptr[b] != L * cols) return OR_EINVAL;
         }
     }
     int64_t total_qo = qo_indptr[batch];
@@ -344,9 +418,9 @@ int oracle_verify_attn(const uint16_t* q, const void* k_cache, const void* v_cac
             status = OR_ENOMEM;
             break;
         }
-        gather_request(k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, b, kv_len, h_kv, d,
-                       page_size, k_scale, v_scale, K, V);
-        build_mask(mask, mask_indptr, b, L, kv_len, M);
+        gather_request(k_cache, v_cache, kv_fp8, kv_layout, kv_indptr, kv_indices, b, kv_len,
+                       h_kv, d, page_size, k_scale, v_scale, K, V);
+        build_mask(mask, mask_indptr, mask_layout, b, L, kv_len, M);
         int nt = nthreads;
         if (nt > nr) nt = (int)nr;
         for (int i = 0; i < nt; ++i) {
@@ -355,6 +429,7 @@ int oracle_verify_attn(const uint16_t* q, const void* k_cache, const void* v_cac
             jb->kv_len = kv_len; jb->L = L; jb->qo_start = qo0;
             jb->h_q = h_q; jb->h_kv = h_kv; jb->d = d; jb->group = group;
             jb->sm_scale = sm_scale; jb->rows = rows; jb->dest = dest; jb->n_rows = nr;
+            jb->q_pos = q_pos; jb->rope_theta = rope_theta; jb->rope_scale = rope_scale;
             jb->out = out; jb->lse = lse;
             jb->lo = nr * i / nt; jb->hi = nr * (i + 1) / nt;
             jb->status = OR_OK;
@@ -368,6 +443,21 @@ int oracle_verify_attn(const uint16_t* q, const void* k_cache, const void* v_cac
     }
     free(rows); free(dest); free(th); free(jobs);
     return status;
+}
+
+/* oracle_verify_attn_ex for an HND cache, each request's L x L mask block and
+ * no rotary embedding. */
+int oracle_verify_attn(const uint16_t* q, const void* k_cache, const void* v_cache, int kv_fp8,
+                       const int32_t* kv_indptr, const int32_t* kv_indices,
+                       const int32_t* last_page_len, const int32_t* qo_indptr,
+                       const uint8_t* mask, const int32_t* mask_indptr, int batch, int h_q,
+                       int h_kv, int d, int page_size, int num_pages, double sm_scale,
+                       double k_scale, double v_scale, const int32_t* sel, int64_t n_sel,
+                       double* out, double* lse, int nthreads) {
+    return oracle_verify_attn_ex(q, k_cache, v_cache, kv_fp8, 0, kv_indptr, kv_indices,
+                                 last_page_len, qo_indptr, mask, mask_indptr, 0, NULL, 0.0, 0.0,
+                                 batch, h_q, h_kv, d, page_size, num_pages, sm_scale, k_scale,
+                                 v_scale, sel, n_sel, out, lse, nthreads);
 }
 
 /*
@@ -401,9 +491,9 @@ int oracle_attn_range(const uint16_t* q, const void* k_cache, const void* v_cach
         free(K); free(V); free(M); free(s); free(qrow);
         return OR_ENOMEM;
     }
-    gather_request(k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, b, kv_len, h_kv, d,
+    gather_request(k_cache, v_cache, kv_fp8, 0, kv_indptr, kv_indices, b, kv_len, h_kv, d,
                    page_size, k_scale, v_scale, K, V);
-    build_mask(mask, mask_indptr, b, L, kv_len, M);
+    build_mask(mask, mask_indptr, 0, b, L, kv_len, M);
     int64_t tok = qo_indptr[b] + t;
     for (int e = 0; e < d; ++e) qrow[e] = oracle_decode_bf16(q[(tok * h_q + qh) * d + e]);
     int h = qh / (h_q / h_kv);
@@ -498,6 +588,85 @@ int oracle_paged_kv_append_quant(const uint16_t* k_new, const uint16_t* v_new, f
             }
         }
     }
+    return OR_OK;
+}
+
+/*
+ * The append with options, as the library's extended append defines it:
+ *  - layout 0 / 1: HND or NHD destination rows (cache_row);
+ *  - quantize: bf16 new rows into an fp8-e4m3 cache; without positions each
+ *    element is stored exactly as oracle_paged_kv_append_quant stores it;
+ *  - positions (nullable, [total_new]): each new K row is first rotated by
+ *    oracle_rope_vec at its token's position, in fp64, then rounded once to
+ *    the cache dtype: bf16 to nearest even, or e4m3 to nearest even with
+ *    saturation (after the division by k_scale when quantizing; an fp8 row
+ *    copied without quantizing is rotated in its stored units).  V rows are
+ *    never rotated.
+ * Without quantize or positions this is oracle_paged_kv_append's bit copy.
+ */
+int oracle_paged_kv_append_ex(const void* k_new, const void* v_new, int cache_fp8, int quantize,
+                              float k_scale, float v_scale, int layout, const int32_t* positions,
+                              double theta, double rope_scale, const int32_t* append_indptr,
+                              const int32_t* kv_indptr, const int32_t* kv_indices,
+                              const int32_t* last_page_len, int batch, int h_kv, int d,
+                              int page_size, int num_pages, void* k_cache, void* v_cache) {
+    if (batch < 0 || h_kv <= 0 || d <= 0 || page_size <= 0) return OR_EINVAL;
+    if (layout != 0 && layout != 1) return OR_EINVAL;
+    if (quantize && (!cache_fp8 || !(k_scale > 0.0f) || !(v_scale > 0.0f))) return OR_EINVAL;
+    if (positions && !(theta > 0.0 && rope_scale > 0.0)) return OR_EINVAL;
+    const int src_bf16 = quantize || !cache_fp8;
+    double* row = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!row) return OR_ENOMEM;
+    for (int b = 0; b < batch; ++b) {
+        int64_t n = (int64_t)append_indptr[b + 1] - append_indptr[b];
+        int64_t kv_len = oracle_kv_len(kv_indptr, last_page_len, b, page_size);
+        if (n < 0 || n > kv_len) { free(row); return OR_EINVAL; }
+        for (int64_t i = 0; i < n; ++i) {
+            int64_t pos = kv_len - n + i;
+            int64_t pidx = (int64_t)kv_indptr[b] + pos / page_size;
+            if (pidx >= kv_indptr[b + 1]) { free(row); return OR_EINVAL; }
+            int32_t page = kv_indices[pidx];
+            if (page < 0 || page >= num_pages) { free(row); return OR_EINVAL; }
+            int64_t slot = pos % page_size;
+            int64_t tok = (int64_t)append_indptr[b] + i;
+            for (int h = 0; h < h_kv; ++h) {
+                size_t dst = (size_t)cache_row(layout, page, h, slot, h_kv, page_size) * (size_t)d;
+                size_t src = ((size_t)tok * h_kv + h) * (size_t)d;
+                for (int kv = 0; kv < 2; ++kv) {
+                    const void* in = kv ? v_new : k_new;
+                    void* cache = kv ? v_cache : k_cache;
+                    const float scale = kv ? v_scale : k_scale;
+                    const int rotate = positions && kv == 0;
+                    if (!rotate) {
+                        for (int e = 0; e < d; ++e) {
+                            if (quantize) {
+                                float x = (float)oracle_decode_bf16(((const uint16_t*)in)[src + e]);
+                                ((uint8_t*)cache)[dst + e] =
+                                    oracle_encode_e4m3_satfinite(oracle_div_f32(x, scale));
+                            } else if (cache_fp8) {
+                                ((uint8_t*)cache)[dst + e] = ((const uint8_t*)in)[src + e];
+                            } else {
+                                ((uint16_t*)cache)[dst + e] = ((const uint16_t*)in)[src + e];
+                            }
+                        }
+                        continue;
+                    }
+                    for (int e = 0; e < d; ++e)
+                        row[e] = src_bf16 ? oracle_decode_bf16(((const uint16_t*)in)[src + e])
+                                          : oracle_decode_e4m3(((const uint8_t*)in)[src + e]);
+                    oracle_rope_vec(row, d, (double)positions[tok], theta, rope_scale);
+                    for (int e = 0; e < d; ++e) {
+                        if (!cache_fp8)
+                            ((uint16_t*)cache)[dst + e] = oracle_encode_bf16(row[e]);
+                        else
+                            ((uint8_t*)cache)[dst + e] =
+                                encode_e4m3_value(quantize ? row[e] / (double)scale : row[e]);
+                    }
+                }
+            }
+        }
+    }
+    free(row);
     return OR_OK;
 }
 

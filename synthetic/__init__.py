@@ -96,6 +96,12 @@ class Workload:
     mask: Optional[np.ndarray] = None  # bit-packed uint8
     mask_indptr: Optional[np.ndarray] = None  # [B+1] int32 bit offsets
     extra: dict = field(default_factory=dict)
+    kv_layout: str = "hnd"           # "hnd" [pages, h_kv, P, d] or "nhd" [pages, P, h_kv, d]
+    mask_layout: str = "qlen"        # "qlen": L x L draft blocks; "full": L x kv_len rows
+    mask_full: Optional[list] = None  # per request bool [L, kv_len] (mask_layout "full")
+    rope_theta: Optional[float] = None  # RoPE base when the workload uses rotary positions
+    q_pos: Optional[np.ndarray] = None  # [sum L] int32 position of each query token
+    kv_pos: Optional[np.ndarray] = None  # [sum kv_len] int32 position of each key, k_tok order
 
     @property
     def group(self) -> int:
@@ -112,6 +118,20 @@ class Workload:
     @property
     def has_mask(self) -> bool:
         return self.mask is not None
+
+    @property
+    def nhd(self) -> bool:
+        return self.kv_layout == "nhd"
+
+    def new_positions(self):
+        """Positions of the draft tokens' keys, in qo_indptr order (what an
+        append with RoPE rotates the new keys by)."""
+        if self.kv_pos is None:
+            return None
+        sel = np.concatenate([
+            np.arange(self.tok_indptr[b + 1] - self.qo_lens[b], self.tok_indptr[b + 1])
+            for b in range(self.batch)]) if self.batch else np.zeros(0, np.int64)
+        return self.kv_pos[sel].astype(np.int32)
 
     def new_tokens(self):
         """The draft tokens' K/V (the last L_b tokens of each request), laid
@@ -167,8 +187,9 @@ def ancestor_mask(parents) -> np.ndarray:
 
 
 def pack_masks(dense_list):
-    """Bit-pack per-request [L_b, L_b] bool blocks LSB-first into one uint8
-    array; returns (bytes, bit offsets [B+1])."""
+    """Bit-pack per-request bool blocks ([L_b, L_b], or [L_b, kv_len_b] for the
+    full layout) LSB-first into one uint8 array; returns (bytes, bit offsets
+    [B+1])."""
     offs = [0]
     for m in dense_list:
         offs.append(offs[-1] + m.size)
@@ -191,10 +212,19 @@ def make_workload(name: str, seed: int = 0, **overrides) -> Workload:
 def make_custom(name="custom", seed=0, batch=2, h_q=4, h_kv=2, d=64, page_size=16,
                 kv_dtype=BF16, prefix=("fixed", [37, 70]), qo=("fixed", [5, 5]),
                 mask="causal", pool_pages=None, pool_factor=1.25, sm_scale=None,
-                shuffle_pages=True, value_std=1.0, with_values=True) -> Workload:
+                shuffle_pages=True, value_std=1.0, with_values=True, kv_layout="hnd",
+                mask_layout="qlen", prefix_visible="all", rope_theta=None) -> Workload:
     """A workload from explicit parameters.  with_values=False draws only the
     tables (lengths, trees, pages; q / k / v come last in the draw order, so the
-    tables are the same either way) and leaves q / k_tok / v_tok empty."""
+    tables are the same either way) and leaves q / k_tok / v_tok empty.
+
+    kv_layout "nhd" lays the page pool out [pages, P, h_kv, d].  mask_layout
+    "full" packs each request's mask as L rows of kv_len bits (prefix
+    columns included): prefix_visible "all" sets every prefix bit, "random"
+    draws them (after every other draw).  rope_theta gives the workload rotary
+    positions: a prefix key at index j has position j, draft u has position
+    prefix + depth(u) (its tree depth; u itself for chains and masks without
+    a tree), and each query token has its draft's position."""
     gen = torch.Generator().manual_seed(seed)
     prefix_lens = _draw_lengths(prefix, batch, gen)
     qo_lens = _draw_lengths(qo, batch, gen)
@@ -276,8 +306,38 @@ def make_custom(name="custom", seed=0, batch=2, h_q=4, h_kv=2, d=64, page_size=1
     sm_scale = float(np.float32(sm_scale))
 
     packed, mask_indptr = (None, None)
-    if dense is not None:
+    mask_full = None
+    if dense is not None and mask_layout == "full":
+        mask_full = []
+        for b in range(batch):
+            L, pre = int(qo_lens[b]), int(prefix_lens[b])
+            m = np.zeros((L, pre + L), dtype=bool)
+            if prefix_visible == "random":
+                m[:, :pre] = torch.rand((L, pre), generator=gen).numpy() < 0.5
+            else:
+                m[:, :pre] = True
+            m[:, pre:] = dense[b]
+            mask_full.append(m)
+        packed, mask_indptr = pack_masks(mask_full)
+    elif dense is not None:
         packed, mask_indptr = pack_masks(dense)
+    elif mask_layout != "qlen":
+        raise ValueError("a full-layout mask needs a mask kind other than causal")
+
+    q_pos = kv_pos = None
+    if rope_theta is not None:
+        kv_pos = np.zeros(int(tok_indptr[-1]), dtype=np.int32)
+        q_pos = np.zeros(int(qo_indptr[-1]), dtype=np.int32)
+        for b in range(batch):
+            L, pre = int(qo_lens[b]), int(prefix_lens[b])
+            depth = list(range(L))
+            if parents is not None and parents[b] is not None:
+                for u in range(L):
+                    depth[u] = 0 if parents[b][u] < 0 else depth[parents[b][u]] + 1
+            t0 = int(tok_indptr[b])
+            kv_pos[t0:t0 + pre] = np.arange(pre)
+            kv_pos[t0 + pre:t0 + pre + L] = pre + np.asarray(depth, dtype=np.int64)
+            q_pos[int(qo_indptr[b]):int(qo_indptr[b]) + L] = pre + np.asarray(depth, dtype=np.int64)
 
     return Workload(
         name=name, batch=batch, h_q=h_q, h_kv=h_kv, d=d, page_size=page_size,
@@ -286,7 +346,8 @@ def make_custom(name="custom", seed=0, batch=2, h_q=4, h_kv=2, d=64, page_size=1
         last_page_len=last_page_len, num_pages=int(pool_pages), tok_indptr=tok_indptr,
         q=q, k_tok=k_tok, v_tok=v_tok, sm_scale=sm_scale, k_scale=k_scale,
         v_scale=v_scale, mask_kind=mask, parents=parents, mask_dense=dense,
-        mask=packed, mask_indptr=mask_indptr)
+        mask=packed, mask_indptr=mask_indptr, kv_layout=kv_layout, mask_layout=mask_layout,
+        mask_full=mask_full, rope_theta=rope_theta, q_pos=q_pos, kv_pos=kv_pos)
 
 
 def sentinel_pool(wl: Workload) -> np.ndarray:
@@ -295,6 +356,8 @@ def sentinel_pool(wl: Workload) -> np.ndarray:
     shows up in the result."""
     dt = np.uint8 if wl.kv_dtype == FP8 else np.uint16
     fill = 0xFF if wl.kv_dtype == FP8 else 0xFFFF
+    if wl.nhd:
+        return np.full((wl.num_pages, wl.page_size, wl.h_kv, wl.d), fill, dtype=dt)
     return np.full((wl.num_pages, wl.h_kv, wl.page_size, wl.d), fill, dtype=dt)
 
 
