@@ -46,8 +46,9 @@
  *  Layouts (all contiguous, row-major):
  *   q, out         [total_qo, num_qo_heads, head_dim]   bf16
  *   lse            [total_qo, num_qo_heads]             fp32, natural log
- *   k_cache/v_cache[num_pages, num_kv_heads, page_size, head_dim]  ("HND")
- *                  bf16 or fp8-e4m3 (the KV dtype)
+ *   k_cache/v_cache[num_pages, num_kv_heads, page_size, head_dim]  ("HND", the
+ *                  default) or [num_pages, page_size, num_kv_heads, head_dim]
+ *                  ("NHD", plan option kv_layout); bf16 or fp8-e4m3 (the KV dtype)
  *   k_new / v_new  [total_new, num_kv_heads, head_dim]  KV dtype
  *   kv_indptr      [batch+1] int32: request b's pages are
  *                  kv_indices[kv_indptr[b] .. kv_indptr[b+1])
@@ -63,7 +64,9 @@
  *                  token t may attend to draft token u.  NULL = causal
  *                  (u <= t).  Prefix keys are always visible.
  *   mask_indptr    [batch+1] int32 bit offsets, mask_indptr[b+1] -
- *                  mask_indptr[b] = L_b * L_b.
+ *                  mask_indptr[b] = L_b * L_b.  (The plan option
+ *                  mask_layout = VA_MASK_FULL selects flashmap's full layout
+ *                  instead: L_b rows of kv_len_b bits, prefix included.)
  *  The drafts are the LAST L_b positions of each request's kv range, so the
  *  prefix length is kv_len_b - L_b (kv_len_b >= L_b is required).
  *
@@ -72,8 +75,10 @@
  *  num_kv_heads; a request's G * L_b rows are cut into row blocks); q / out
  *  bf16; KV bf16 or fp8-e4m3 (OCP "fn": no infinities).  Device pointers
  *  must be 16-byte aligned.
+ *  RoPE (LLaMA rotate-half) at caller-given positions: new keys rotated by
+ *  paged_kv_append_ex, queries by verify_attn_run_ex.
  *  Unsupported requests (other head dims, page sizes, dtypes; logit caps,
- *  sinks, sliding windows, RoPE) return VA_ERR_UNSUPPORTED -- there is no
+ *  sinks, sliding windows) return VA_ERR_UNSUPPORTED -- there is no
  *  fallback path.
  */
 #ifndef VERIFY_ATTN_H
@@ -108,14 +113,33 @@ typedef enum { VA_BF16 = 0, VA_FP8_E4M3 = 1 } va_dtype;
 #define VA_DEV_BAD_APPEND 4      /* append position outside the request's pages: skipped */
 #define VA_DEV_TIMEOUT 8         /* a bounded wait gave up */
 
-/* Optional planner knobs (pass NULL for the defaults). */
+/* KV-cache layouts (FlashInfer PR #286's kv_layout argument):
+ *   HND  [num_pages, num_kv_heads, page_size, head_dim]  (the default)
+ *   NHD  [num_pages, page_size, num_kv_heads, head_dim] */
+typedef enum { VA_LAYOUT_HND = 0, VA_LAYOUT_NHD = 1 } va_kv_layout;
+
+/* Custom-mask layouts.  QLEN: request b's L_b x L_b draft block (prefix keys
+ * always visible).  FULL (flashmap's full custom mask): L_b rows of kv_len_b
+ * bits, one per key of the request, prefix included, row t starting at bit
+ * mask_indptr[b] + t * kv_len_b; mask_indptr[b+1] - mask_indptr[b] =
+ * L_b * kv_len_b. */
+#define VA_MASK_QLEN 0
+#define VA_MASK_FULL 1
+
+/* Optional planner knobs and call features (pass NULL for the defaults). */
 typedef struct {
     int max_splits;      /* upper bound on kv splits per (request, KV head, row block);
                             0 = planner's choice, 1 = never split */
     int min_chunk;       /* smallest kv chunk (keys) a split may hold; 0 = default */
     int target_ctas;     /* CTAs the plan aims to fill; 0 = derived from the SM count */
     int kernel;          /* force a kernel variant (VA_KERNEL_*); 0 = automatic */
-    int reserved[4];     /* must be zero */
+    int mask_layout;     /* VA_MASK_QLEN (default) or VA_MASK_FULL */
+    int kv_layout;       /* va_kv_layout of k_cache / v_cache: VA_LAYOUT_HND (default) or NHD */
+    int rope;            /* 1: rotate each query row by RoPE at its token's position
+                            (verify_attn_run_ex's q_position) before Q K^T; the cache holds
+                            keys already rotated at their own positions (paged_kv_append_ex
+                            with positions) */
+    int reserved[1];     /* must be zero */
 } va_plan_options_t;
 
 #define VA_KERNEL_AUTO 0
@@ -222,6 +246,44 @@ int verify_attn_run(const void* q, const void* k_cache, const void* v_cache,
                     float* lse, int num_pages, const void* plan_h, void* workspace_d,
                     size_t workspace_bytes, void* stream);
 
+/* Per-call arguments of verify_attn_run_ex / verify_attn_partial_ex. */
+typedef struct {
+    const int32_t* q_position; /* device [total_qo]: with a plan made with rope = 1, the
+                                  position of each query token (for a draft tree: prefix +
+                                  the draft's depth, the position its key was appended at);
+                                  must be NULL otherwise */
+    float rope_theta;          /* RoPE base (> 0, finite) when q_position is given */
+    float rope_scale;          /* linear position scaling (> 0, finite); 0 means 1 */
+    int reserved[4];           /* must be zero */
+} va_run_options_t;
+
+/*
+ * verify_attn_run with per-call options (RoPE positions of the queries).
+ * With a plan made for RoPE, each query row is rotated at q_position[token]
+ * (LLaMA rotate-half, angle position / rope_scale * rope_theta^(-2i /
+ * head_dim); FlashInfer PR #286's ROPE_LLAMA at the tree positions of
+ * FlashInfer issue #152) in fp32 and rounded to the MMA operand type (bf16,
+ * or f16 with an fp8 cache) before Q K^T.  NULL options = verify_attn_run.
+ * Errors: as verify_attn_run; VA_ERR_PLAN_MISMATCH when q_position is given
+ * without a RoPE plan or missing with one.
+ */
+int verify_attn_run_ex(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* kv_indptr, const int32_t* kv_indices,
+                       const int32_t* last_page_len, const int32_t* qo_indptr,
+                       const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads,
+                       int num_kv_heads, int head_dim, int page_size, float sm_scale,
+                       float k_scale, float v_scale, void* out, float* lse, int num_pages,
+                       const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                       const va_run_options_t* options, void* stream);
+int verify_attn_partial_ex(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* kv_indptr, const int32_t* kv_indices,
+                           const int32_t* last_page_len, const int32_t* qo_indptr,
+                           const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads,
+                           int num_kv_heads, int head_dim, int page_size, float sm_scale,
+                           float k_scale, float v_scale, void* out, float* lse, int num_pages,
+                           const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                           const va_run_options_t* options, void* stream);
+
 /*
  * The two halves of verify_attn_run, for callers that time or schedule them
  * apart: the split attention kernel (it writes the final out / lse of every
@@ -282,11 +344,6 @@ int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_
                     const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
                     int num_kv_heads, int head_dim, int page_size, int num_pages,
                     va_dtype kv_dtype, int64_t total_new, int* status_d, void* stream);
-
-/* KV-cache layouts (FlashInfer PR #286's kv_layout argument):
- *   HND  [num_pages, num_kv_heads, page_size, head_dim]  (the default)
- *   NHD  [num_pages, page_size, num_kv_heads, head_dim] */
-typedef enum { VA_LAYOUT_HND = 0, VA_LAYOUT_NHD = 1 } va_kv_layout;
 
 /* Options of paged_kv_append_ex (all-zero = a plain bit copy into an HND
  * cache, as paged_kv_append). */

@@ -61,7 +61,26 @@ class VerifyAttnError(RuntimeError):
 class PlanOptions(ctypes.Structure):
     _fields_ = [("max_splits", ctypes.c_int), ("min_chunk", ctypes.c_int),
                 ("target_ctas", ctypes.c_int), ("kernel", ctypes.c_int),
-                ("reserved", ctypes.c_int * 4)]
+                ("mask_layout", ctypes.c_int), ("kv_layout", ctypes.c_int),
+                ("rope", ctypes.c_int), ("reserved", ctypes.c_int * 1)]
+
+
+class RunOptions(ctypes.Structure):
+    _fields_ = [("q_position", ctypes.c_void_p), ("rope_theta", ctypes.c_float),
+                ("rope_scale", ctypes.c_float), ("reserved", ctypes.c_int * 4)]
+
+
+class AppendOptions(ctypes.Structure):
+    _fields_ = [("quantize", ctypes.c_int), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float), ("kv_layout", ctypes.c_int),
+                ("positions", ctypes.c_void_p), ("rope_theta", ctypes.c_float),
+                ("rope_scale", ctypes.c_float), ("reserved", ctypes.c_int * 4)]
+
+
+MASK_QLEN, MASK_FULL = 0, 1
+LAYOUT_HND, LAYOUT_NHD = 0, 1
+_LAYOUTS = {"hnd": LAYOUT_HND, "nhd": LAYOUT_NHD, LAYOUT_HND: LAYOUT_HND, LAYOUT_NHD: LAYOUT_NHD}
+_MASK_LAYOUTS = {"qlen": MASK_QLEN, "full": MASK_FULL, MASK_QLEN: MASK_QLEN, MASK_FULL: MASK_FULL}
 
 
 def lib():
@@ -91,6 +110,12 @@ def lib():
                                   P, P, i32, P, P, sz, P]),
         "verify_attn_partial": (i32, [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, f32, f32,
                                       f32, P, P, i32, P, P, sz, P]),
+        "verify_attn_run_ex": (i32, [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, f32, f32,
+                                     f32, P, P, i32, P, P, sz, P, P]),
+        "verify_attn_partial_ex": (i32, [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, f32,
+                                         f32, f32, P, P, i32, P, P, sz, P, P]),
+        "paged_kv_append_ex": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
+                                     P, P, P]),
         "verify_attn_merge": (i32, [P, i32, i32, i32, P, P, P, P, sz, P]),
         "verify_attn_plan_launches": (i32, [P, Pi]),
         "verify_attn_plan_upload": (i32, [P, P, sz, P]),
@@ -157,10 +182,14 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0):
+def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0, mask_layout="qlen",
+             kv_layout="hnd", rope=False):
     o = PlanOptions()
     o.max_splits, o.min_chunk, o.target_ctas, o.kernel = (int(max_splits), int(min_chunk),
                                                           int(target_ctas), int(kernel))
+    o.mask_layout = _MASK_LAYOUTS[mask_layout]
+    o.kv_layout = _LAYOUTS[kv_layout]
+    o.rope = int(bool(rope))
     return o
 
 
@@ -330,24 +359,48 @@ def _alloc_out(q, plan, out, lse, want_lse):
     return out, lse
 
 
+def _run_options(q_position, rope_theta, rope_scale):
+    if q_position is None:
+        return None
+    o = RunOptions()
+    o.q_position = _dp(q_position)
+    o.rope_theta = float(rope_theta)
+    o.rope_scale = float(rope_scale)
+    return o
+
+
 def verify_attn_run(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr,
                     mask, mask_indptr, plan: Plan, sm_scale=0.0, k_scale=1.0, v_scale=1.0,
-                    out=None, lse=None, want_lse=True, num_pages=None, stream=None):
-    """out = softmax(q k^T * sm_scale * k_scale + mask) v * v_scale, and its LSE."""
+                    out=None, lse=None, want_lse=True, num_pages=None, stream=None,
+                    q_position=None, rope_theta=10000.0, rope_scale=1.0):
+    """out = softmax(q k^T * sm_scale * k_scale + mask) v * v_scale, and its LSE.
+    q_position (int32 device tensor [total_qo]) rotates the queries by RoPE
+    at those positions; the plan must have been made with rope=True."""
     out, lse = _alloc_out(q, plan, out, lse, want_lse)
     args = _run_args(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
                      mask_indptr, plan, sm_scale, k_scale, v_scale, out, lse, num_pages)
-    _check("verify_attn_run", lib().verify_attn_run(*args, _stream(stream)))
+    ro = _run_options(q_position, rope_theta, rope_scale)
+    if ro is None:
+        _check("verify_attn_run", lib().verify_attn_run(*args, _stream(stream)))
+    else:
+        _check("verify_attn_run_ex",
+               lib().verify_attn_run_ex(*args, ctypes.byref(ro), _stream(stream)))
     return out, lse
 
 
 def verify_attn_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr,
                         mask, mask_indptr, plan: Plan, sm_scale=0.0, k_scale=1.0, v_scale=1.0,
-                        out=None, lse=None, want_lse=True, num_pages=None, stream=None):
+                        out=None, lse=None, want_lse=True, num_pages=None, stream=None,
+                        q_position=None, rope_theta=10000.0, rope_scale=1.0):
     out, lse = _alloc_out(q, plan, out, lse, want_lse)
     args = _run_args(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
                      mask_indptr, plan, sm_scale, k_scale, v_scale, out, lse, num_pages)
-    _check("verify_attn_partial", lib().verify_attn_partial(*args, _stream(stream)))
+    ro = _run_options(q_position, rope_theta, rope_scale)
+    if ro is None:
+        _check("verify_attn_partial", lib().verify_attn_partial(*args, _stream(stream)))
+    else:
+        _check("verify_attn_partial_ex",
+               lib().verify_attn_partial_ex(*args, ctypes.byref(ro), _stream(stream)))
     return out, lse
 
 
@@ -369,24 +422,49 @@ def verify_attn_device_status(plan: Plan, stream=None) -> int:
 
 
 def paged_kv_append(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_page_len, k_cache,
-                    v_cache, total_new=None, num_pages=None, status=None, stream=None):
-    """Copy new tokens' K/V into their pages (bit-exact).  total_new defaults
-    to k_new.shape[0]."""
-    if k_cache.dtype != k_new.dtype or v_cache.dtype != v_new.dtype:
-        raise ValueError("k_new / v_new must be in the cache dtype")
-    kv_dtype = KV_FP8_E4M3 if k_cache.element_size() == 1 else KV_BF16
+                    v_cache, total_new=None, num_pages=None, status=None, stream=None,
+                    kv_layout="hnd", k_scale=None, v_scale=None, positions=None,
+                    rope_theta=10000.0, rope_scale=1.0):
+    """Write new tokens' K/V into their pages.  By default a bit-exact copy
+    (k_new / v_new in the cache dtype).  With a bf16 k_new / v_new and an fp8
+    cache, a quantising append (k_scale / v_scale required).  positions
+    (int32 device tensor [total_new]) rotates the new keys by RoPE first.
+    kv_layout "nhd" for a [pages, P, h_kv, d] cache.  total_new defaults to
+    k_new.shape[0]."""
+    fp8_cache = k_cache.element_size() == 1
+    quantize = fp8_cache and k_new.dtype == torch.bfloat16
+    if not quantize and (k_cache.dtype != k_new.dtype or v_cache.dtype != v_new.dtype):
+        raise ValueError("k_new / v_new must be in the cache dtype (or bf16 into an fp8 cache)")
+    if quantize and (k_scale is None or v_scale is None or v_new.dtype != torch.bfloat16):
+        raise ValueError("a quantising append needs bf16 k_new / v_new and k_scale / v_scale")
+    kv_dtype = KV_FP8_E4M3 if fp8_cache else KV_BF16
     batch = append_indptr.shape[0] - 1
     if total_new is None:
         total_new = k_new.shape[0]
     if num_pages is None:
         num_pages = k_cache.shape[0]
-    h_kv, page_size, head_dim = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
-    rc = lib().paged_kv_append(_dp(k_new), _dp(v_new), _dp(append_indptr), _dp(kv_indptr),
-                               _dp(kv_indices), _dp(last_page_len), _dp(k_cache), _dp(v_cache),
-                               int(batch), int(h_kv), int(head_dim), int(page_size),
-                               int(num_pages), kv_dtype, int(total_new), _dp(status),
-                               _stream(stream))
-    _check("paged_kv_append", rc)
+    layout = _LAYOUTS[kv_layout]
+    if layout == LAYOUT_NHD:
+        page_size, h_kv, head_dim = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
+    else:
+        h_kv, page_size, head_dim = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
+    common = (_dp(k_new), _dp(v_new), _dp(append_indptr), _dp(kv_indptr), _dp(kv_indices),
+              _dp(last_page_len), _dp(k_cache), _dp(v_cache), int(batch), int(h_kv),
+              int(head_dim), int(page_size), int(num_pages), kv_dtype, int(total_new))
+    if not quantize and positions is None and layout == LAYOUT_HND:
+        rc = lib().paged_kv_append(*common, _dp(status), _stream(stream))
+        _check("paged_kv_append", rc)
+        return
+    o = AppendOptions()
+    o.quantize = int(quantize)
+    o.k_scale = float(k_scale) if quantize else 0.0
+    o.v_scale = float(v_scale) if quantize else 0.0
+    o.kv_layout = layout
+    o.positions = _dp(positions) if positions is not None else None
+    o.rope_theta = float(rope_theta) if positions is not None else 0.0
+    o.rope_scale = float(rope_scale) if positions is not None else 0.0
+    rc = lib().paged_kv_append_ex(*common, ctypes.byref(o), _dp(status), _stream(stream))
+    _check("paged_kv_append_ex", rc)
 
 
 STATIC_SCRATCH_BYTES = 32 << 20

@@ -91,10 +91,12 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
   const int nrows = it.nrows, row0 = it.row0;
   const int lo = it.kv_lo, hi = it.kv_hi;
   const int n_tiles = (hi - lo + C::BN - 1) / C::BN;
-  const size_t head_stride = (size_t)p.page_size * C::KVROW;
-  const size_t page_stride = (size_t)p.h_kv * head_stride;
-  const uint8_t* kbase = static_cast<const uint8_t*>(p.k_cache) + (size_t)h * head_stride;
-  const uint8_t* vbase = static_cast<const uint8_t*>(p.v_cache) + (size_t)h * head_stride;
+  // HND [page][head][slot][d] or NHD [page][slot][head][d]
+  const size_t slot_stride = p.nhd ? (size_t)p.h_kv * C::KVROW : (size_t)C::KVROW;
+  const size_t head_off = p.nhd ? (size_t)h * C::KVROW : (size_t)h * p.page_size * C::KVROW;
+  const size_t page_stride = (size_t)p.h_kv * p.page_size * C::KVROW;
+  const uint8_t* kbase = static_cast<const uint8_t*>(p.k_cache) + head_off;
+  const uint8_t* vbase = static_cast<const uint8_t*>(p.v_cache) + head_off;
   const int pmask = p.page_size - 1;
   int bad_page = 0;
 
@@ -134,7 +136,7 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
       if (key < hi) {
         const int page = pages[r];
         if ((unsigned)page < (unsigned)p.num_pages) {
-          const size_t off = (size_t)page * page_stride + (size_t)(key & pmask) * C::KVROW + ch * 16;
+          const size_t off = (size_t)page * page_stride + (size_t)(key & pmask) * slot_stride + ch * 16;
           ks = kbase + off;
           vs = vbase + off;
           bytes = 16;
@@ -155,6 +157,39 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
   for (int s = 0; s < STAGES - 1; ++s) {
     if (s < n_tiles) issue_tile(s, s);
     cp_async_commit();
+  }
+
+  // RoPE: once Q has landed, each thread rotates (row, chunk) pairs of its
+  // rows in place -- element i with element i + D/2, i.e. chunk ch with
+  // chunk ch + D/16 -- at the row's position, rounding to bf16.
+  if (p.q_position) {
+    cp_async_wait<STAGES - 1>();   // the Q group (committed first) is complete
+    __syncthreads();
+    constexpr int HC = D / 16;     // chunks per half row
+    for (int c = tid; c < C::BM * HC; c += C::NT) {
+      const int r = c / HC, ch = c % HC;
+      if (r >= nrows) continue;
+      const int qpos = __ldg(p.q_position + qo0 + (row0 + r) / G);
+      uint4* pa = reinterpret_cast<uint4*>(sQ + swz(r, ch, C::QROW));
+      uint4* pb = reinterpret_cast<uint4*>(sQ + swz(r, ch + HC, C::QROW));
+      uint4 a = *pa, bq = *pb;
+      uint32_t* wa = reinterpret_cast<uint32_t*>(&a);
+      uint32_t* wb = reinterpret_cast<uint32_t*>(&bq);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = ch * 8 + 2 * k;
+        float c0, s0, c1, s1;
+        rope_cos_sin(qpos, p.rope.hi[i], p.rope.lo[i], &c0, &s0);
+        rope_cos_sin(qpos, p.rope.hi[i + 1], p.rope.lo[i + 1], &c1, &s1);
+        const float a0 = __uint_as_float(wa[k] << 16), a1 = __uint_as_float(wa[k] & 0xffff0000u);
+        const float b0 = __uint_as_float(wb[k] << 16), b1 = __uint_as_float(wb[k] & 0xffff0000u);
+        wa[k] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
+        wb[k] = pack_bf16x2(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1));
+      }
+      *pa = a;
+      *pb = bq;
+    }
+    __syncthreads();
   }
 
   // This warp's rows: local rows wrow + g and wrow + g + 8 (g = lane / 4).
@@ -242,7 +277,23 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
       }
       // Visibility: keys < prefix always; draft key prefix + u when the mask
       // bit (t, u) is set (or u <= t without a mask); nothing at or past hi.
-      if (!p.mask && (k0 + C::BN > prefix || k0 + C::BN > hi)) {
+      if (p.mask_full) {
+        // one row of kv_len bits per token, prefix included
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = k0 + j * 8 + 2 * tq + (e & 1);
+            const int t = e < 2 ? t_lo : t_hi;
+            bool vis = key < hi && t < L;
+            if (vis) {
+              const long long bit = (long long)moff + (long long)t * kv_len + key;
+              vis = (__ldg(p.mask + (bit >> 3)) >> (bit & 7)) & 1;
+            }
+            if (!vis) s[j][e] = -INFINITY;
+          }
+        }
+      } else if (!p.mask && (k0 + C::BN > prefix || k0 + C::BN > hi)) {
         // causal drafts: a row sees keys below min(hi, prefix + t + 1)
         const int lim_lo = min(hi, prefix + t_lo + 1) - k0;
         const int lim_hi = min(hi, prefix + t_hi + 1) - k0;

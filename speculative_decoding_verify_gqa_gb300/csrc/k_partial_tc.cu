@@ -182,6 +182,9 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.group;
+  // Q is rewritten in shared memory by the softmax warps before the first S
+  // MMA reads it: to f16 for an fp8 cache, rotated at its positions for RoPE
+  const bool q_pass = FP8 || p.q_position != nullptr;
   // This CTA's items: chain blockIdx.x (then blockIdx.x + gridDim.x, ... if
   // the grid is smaller than the plan's chain count), linked through next; a
   // malformed link ends its chain.
@@ -350,7 +353,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
               if constexpr (FP8) {
                 tma_load_4d(dst + q * 2048, map, 0, slot, g.h, page, bar(B_FULL + s));
               } else {
-                tma_load_5d(dst + q * 4096, map, 0, 0, 0, slot >> 3, page * p.h_kv + g.h, bar(B_FULL + s));
+                if (p.nhd)
+                  tma_load_5d(dst + q * 4096, map, 0, 0, 0, g.h, page * (p.page_size >> 3) + (slot >> 3),
+                              bar(B_FULL + s));
+                else
+                  tma_load_5d(dst + q * 4096, map, 0, 0, 0, slot >> 3, page * p.h_kv + g.h, bar(B_FULL + s));
               }
             }
           }
@@ -467,7 +474,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       ItemGeo g;
       for (int k = 0; live && take_geo_thread(k, g); ++k) {
         if (!g.ok) continue;
-        if (!mbar_wait(bar(FP8 ? B_Q_READY : B_Q), nit & 1, abort_flag)) break;
+        if (!mbar_wait(bar(q_pass ? B_Q_READY : B_Q), nit & 1, abort_flag)) break;
         if constexpr (C::SBUF == 2) {
           // One Q tile, S double-buffered: step j issues S_j into buffer
           // (S count) % 2 before it waits for P_{j-1}, so the tensor core
@@ -626,24 +633,51 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     for (int k = 0; live && take_geo_warp(k, g); ++k) {
       if (!g.ok) continue;
       const bool mine = qt < g.nq;
-      if (FP8) {
-        // Q to f16, in place (each thread its own row); a Q tile the item
-        // does not use still counts its arrival
+      if (q_pass) {
+        // Q in place, each thread its own row of its Q tile: rotated at the
+        // row's position (RoPE: element i with i + 64, i.e. chunk j of the
+        // first 64-column half with chunk j of the second, the same swizzled
+        // slot), then rounded to the MMA's operand type (f16 for an fp8
+        // cache).  A Q tile the item does not use still counts its arrival.
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q), nit & 1, abort_flag))) { live = false; break; }
         if (mine) {
+          const int brq = qt * C::ROWS + r;
+          const bool rot = p.q_position != nullptr && brq < g.nrows;
+          const int qpos = rot ? __ldg(p.q_position + g.qo0 + (g.row0 + brq) / G) : 0;
+          uint8_t* h0 = smem + C::OFF_Q + qt * C::QT_BYTES + r * 128;
+          uint8_t* h1 = h0 + C::QT_BYTES / 2;
+#pragma unroll 1
+          for (int jp = 0; jp < 8; ++jp) {
+            uint4 a = *reinterpret_cast<uint4*>(h0 + jp * 16);
+            uint4 b = *reinterpret_cast<uint4*>(h1 + jp * 16);
+            if (rot) {
+              const int i0 = (jp ^ (r & 7)) << 3;   // frequency index of the chunk's first element
+              uint32_t* wa = reinterpret_cast<uint32_t*>(&a);
+              uint32_t* wb = reinterpret_cast<uint32_t*>(&b);
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint4* q4 = reinterpret_cast<uint4*>(smem + C::OFF_Q + qt * C::QT_BYTES +
-                                                 half * (C::QT_BYTES / 2) + r * 128);
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-              uint4 v = q4[ch];
-              v.x = bf16x2_to_f16x2(v.x);
-              v.y = bf16x2_to_f16x2(v.y);
-              v.z = bf16x2_to_f16x2(v.z);
-              v.w = bf16x2_to_f16x2(v.w);
-              q4[ch] = v;
+              for (int k = 0; k < 4; ++k) {
+                float c0, s0, c1, s1;
+                rope_cos_sin(qpos, p.rope.hi[i0 + 2 * k], p.rope.lo[i0 + 2 * k], &c0, &s0);
+                rope_cos_sin(qpos, p.rope.hi[i0 + 2 * k + 1], p.rope.lo[i0 + 2 * k + 1], &c1, &s1);
+                const float a0 = __uint_as_float(wa[k] << 16), a1 = __uint_as_float(wa[k] & 0xffff0000u);
+                const float b0 = __uint_as_float(wb[k] << 16), b1 = __uint_as_float(wb[k] & 0xffff0000u);
+                const float ya0 = fmaf(a0, c0, -b0 * s0), ya1 = fmaf(a1, c1, -b1 * s1);
+                const float yb0 = fmaf(b0, c0, a0 * s0), yb1 = fmaf(b1, c1, a1 * s1);
+                wa[k] = FP8 ? pack_f16x2(ya0, ya1) : pack_bf16x2(ya0, ya1);
+                wb[k] = FP8 ? pack_f16x2(yb0, yb1) : pack_bf16x2(yb0, yb1);
+              }
+            } else if (FP8) {
+              a.x = bf16x2_to_f16x2(a.x);
+              a.y = bf16x2_to_f16x2(a.y);
+              a.z = bf16x2_to_f16x2(a.z);
+              a.w = bf16x2_to_f16x2(a.w);
+              b.x = bf16x2_to_f16x2(b.x);
+              b.y = bf16x2_to_f16x2(b.y);
+              b.z = bf16x2_to_f16x2(b.z);
+              b.w = bf16x2_to_f16x2(b.w);
             }
+            *reinterpret_cast<uint4*>(h0 + jp * 16) = a;
+            *reinterpret_cast<uint4*>(h1 + jp * 16) = b;
           }
           fence_proxy_async();
         }
@@ -707,6 +741,26 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         bool full;
         if (!p.mask) {
           full = __all_sync(0xffffffffu, lim >= C::KEYS);
+        } else if (p.mask_full) {
+          // one row of kv_len = prefix + L bits per token, prefix included
+          uint32_t all = 0xffffffffu;
+#pragma unroll
+          for (int q = 0; q < C::KEYS / 32; ++q) {
+            const int g0 = k0 + 32 * q;
+            uint32_t w32 = 0;
+            if (g0 < hi && t < L) {
+              const int nbits = min(32, hi - g0);
+              const long long bit0 = (long long)moff + (long long)t * (prefix + L) + g0;
+              const int nbytes = (int)((((bit0 & 7) + nbits) + 7) >> 3);
+              uint64_t w = 0;
+              for (int k = 0; k < nbytes; ++k) w |= (uint64_t)__ldg(p.mask + (bit0 >> 3) + k) << (8 * k);
+              w >>= (bit0 & 7);
+              w32 = (uint32_t)(w & (nbits >= 32 ? 0xffffffffull : ((1ull << nbits) - 1ull)));
+            }
+            vis[q] = w32;
+            all &= w32;
+          }
+          full = __all_sync(0xffffffffu, all == 0xffffffffu);
         } else if (k0 + C::KEYS <= prefix && k0 + C::KEYS <= hi) {
           full = true;
         } else {

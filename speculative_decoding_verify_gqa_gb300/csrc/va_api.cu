@@ -54,15 +54,40 @@ const PlanHeader* plan_header(const void* plan_h) {
   return hd;
 }
 
+// RoPE frequencies theta^(-2i/d) / scale for i < d/2, in double, each split
+// into a float head and the float nearest to the rest.
+void rope_frequencies(float theta, float scale, int head_dim, RopeFreq* f) {
+  for (int i = 0; i < 64; ++i) {
+    f->hi[i] = f->lo[i] = 0.f;
+    if (2 * i >= head_dim) continue;
+    const double v = pow((double)theta, -2.0 * i / head_dim) / (double)scale;
+    f->hi[i] = (float)v;
+    f->lo[i] = (float)(v - (double)f->hi[i]);
+  }
+}
+
 // Shared checks of verify_attn_run / _partial: the plan matches the call.
 int check_run(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
               const int32_t* kv_indices, const int32_t* last_page_len, const int32_t* qo_indptr,
               const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads, int num_kv_heads,
               int head_dim, int page_size, float* sm_scale, float k_scale, float v_scale,
               const void* out, const float* lse, int num_pages, const void* plan_h,
-              const void* workspace_d, size_t workspace_bytes, const PlanHeader** hd_out) {
+              const void* workspace_d, size_t workspace_bytes, const va_run_options_t* o,
+              const PlanHeader** hd_out) {
   const PlanHeader* hd = plan_header(plan_h);
   if (!hd) return VA_ERR_INVALID_ARGUMENT;
+  if (o) {
+    for (int r : o->reserved)
+      if (r) return VA_ERR_INVALID_ARGUMENT;
+  }
+  const bool rope = (hd->flags & kPlanRope) != 0;
+  const int32_t* q_position = o ? o->q_position : nullptr;
+  if (rope != (q_position != nullptr)) return VA_ERR_PLAN_MISMATCH;
+  if (rope) {
+    const float sc = o->rope_scale == 0.f ? 1.f : o->rope_scale;
+    if (!(isfinite(o->rope_theta) && o->rope_theta > 0.f && isfinite(sc) && sc > 0.f))
+      return VA_ERR_INVALID_ARGUMENT;
+  }
   if (hd->h_q != num_qo_heads || hd->h_kv != num_kv_heads || hd->head_dim != head_dim ||
       hd->page_size != page_size || hd->has_mask != (mask != nullptr ? 1 : 0))
     return VA_ERR_PLAN_MISMATCH;
@@ -89,9 +114,10 @@ PartialParams make_partial(const void* q, const void* k_cache, const void* v_cac
                            const int32_t* last_page_len, const int32_t* qo_indptr,
                            const uint8_t* mask, const int32_t* mask_indptr, float sm_scale,
                            float k_scale, float v_scale, void* out, float* lse, int num_pages,
-                           const PlanHeader* hd, void* workspace_d) {
+                           const PlanHeader* hd, void* workspace_d, const va_run_options_t* o) {
   char* ws = static_cast<char*>(workspace_d);
   PartialParams p;
+  memset(&p, 0, sizeof(p));
   p.q = q;
   p.k_cache = k_cache;
   p.v_cache = v_cache;
@@ -120,19 +146,14 @@ PartialParams make_partial(const void* q, const void* k_cache, const void* v_cac
   p.v_scale = v_scale;
   p.n_items = hd->n_items;
   p.n_ctas = (int)hd->n_ctas;
-  return p;
-}
-
-// RoPE frequencies theta^(-2i/d) / scale for i < d/2, in double, each split
-// into a float head and the float nearest to the rest.
-void rope_frequencies(float theta, float scale, int head_dim, RopeFreq* f) {
-  for (int i = 0; i < 64; ++i) {
-    f->hi[i] = f->lo[i] = 0.f;
-    if (2 * i >= head_dim) continue;
-    const double v = pow((double)theta, -2.0 * i / head_dim) / (double)scale;
-    f->hi[i] = (float)v;
-    f->lo[i] = (float)(v - (double)f->hi[i]);
+  p.mask_full = (hd->flags & kPlanMaskFull) ? 1 : 0;
+  p.nhd = (hd->flags & kPlanNhd) ? 1 : 0;
+  if ((hd->flags & kPlanRope) && o && o->q_position) {
+    p.q_position = o->q_position;
+    rope_frequencies(o->rope_theta, o->rope_scale == 0.f ? 1.f : o->rope_scale, hd->head_dim,
+                     &p.rope);
   }
+  return p;
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
@@ -156,8 +177,11 @@ int make_tc_maps(const void* q, int64_t total_qo, const void* k_cache, const voi
   if (!enc) return VA_ERR_CUDA;
   const int G = hd->group, D = hd->head_dim, P = hd->page_size;
   if (total_qo <= 0 || num_pages <= 0) return VA_ERR_INVALID_ARGUMENT;
-  // the bf16 view indexes page * h_kv + head (plus one past the pool) in int
-  if ((int64_t)(num_pages + 1) * hd->h_kv > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
+  // the bf16 views index page * h_kv + head, or page * P / 8 + slot / 8 (plus
+  // one page past the pool), in int
+  if ((int64_t)(num_pages + 1) * hd->h_kv > 0x7fffffffLL ||
+      (int64_t)(num_pages + 1) * hd->page_size / 8 > 0x7fffffffLL)
+    return VA_ERR_UNSUPPORTED;
   cuuint32_t estr[4] = {1, 1, 1, 1};
   {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hd->h_q, (cuuint64_t)total_qo};
@@ -169,19 +193,34 @@ int make_tc_maps(const void* q, int64_t total_qo, const void* k_cache, const voi
       return VA_ERR_CUDA;
   }
   const bool fp8 = hd->kv_dtype == VA_DTYPE_FP8_E4M3;
+  const bool nhd = (hd->flags & kPlanNhd) != 0;
   const cuuint64_t es = fp8 ? 1 : 2;
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)P, (cuuint64_t)hd->h_kv, (cuuint64_t)num_pages};
-  cuuint64_t strides[3] = {(cuuint64_t)D * es, (cuuint64_t)P * D * es,
-                           (cuuint64_t)hd->h_kv * P * D * es};
+  const cuuint64_t H = (cuuint64_t)hd->h_kv;
+  // element strides of a slot and of a head: HND [page][head][slot][d],
+  // NHD [page][slot][head][d]
+  const cuuint64_t slot_st = nhd ? H * D : (cuuint64_t)D;
+  const cuuint64_t head_st = nhd ? (cuuint64_t)D : (cuuint64_t)P * D;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)P, H, (cuuint64_t)num_pages};
+  cuuint64_t strides[3] = {slot_st * es, head_st * es, H * P * D * es};
   cuuint32_t box[4] = {fp8 ? 128u : 64u, 16, 1, 1};
   const void* src[2] = {k_cache, v_cache};
   CUtensorMap* dst[2] = {&m->k, &m->v};
   for (int i = 0; i < 2; ++i) {
     if (!fp8) {
-      // [page * h_kv + head][slot / 8][half][slot % 8][64], one box per 16 keys
-      cuuint64_t vd[5] = {64, 8, 2, (cuuint64_t)P / 8, (cuuint64_t)hd->h_kv * (cuuint64_t)num_pages};
-      cuuint64_t vs[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)8 * D * 2, (cuuint64_t)P * D * 2};
+      // HND: [page * h_kv + head][slot / 8][half][slot % 8][64]; NHD: [page * P / 8
+      // + slot / 8][head][half][slot % 8][64]; one box per 16 keys of one head
+      cuuint64_t vd[5], vs[4];
       cuuint32_t vb[5] = {64, 8, 2, 2, 1};
+      vd[0] = 64; vd[1] = 8; vd[2] = 2;
+      vs[0] = slot_st * 2; vs[1] = 128;
+      if (nhd) {
+        vd[3] = H; vd[4] = (cuuint64_t)num_pages * P / 8;
+        vs[2] = (cuuint64_t)D * 2; vs[3] = 8 * slot_st * 2;
+        vb[3] = 1; vb[4] = 2;
+      } else {
+        vd[3] = (cuuint64_t)P / 8; vd[4] = H * (cuuint64_t)num_pages;
+        vs[2] = 8 * slot_st * 2; vs[3] = (cuuint64_t)P * D * 2;
+      }
       cuuint32_t ve[5] = {1, 1, 1, 1, 1};
       if (enc(dst[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(src[i]), vd, vs, vb, ve,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -296,24 +335,24 @@ int verify_attn_plan_launches(const void* plan_h, int* launches) {
   return VA_OK;
 }
 
-int verify_attn_partial(const void* q, const void* k_cache, const void* v_cache,
-                        const int32_t* kv_indptr, const int32_t* kv_indices,
-                        const int32_t* last_page_len, const int32_t* qo_indptr,
-                        const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads,
-                        int num_kv_heads, int head_dim, int page_size, float sm_scale,
-                        float k_scale, float v_scale, void* out, float* lse, int num_pages,
-                        const void* plan_h, void* workspace_d, size_t workspace_bytes,
-                        void* stream) {
+int verify_attn_partial_ex(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* kv_indptr, const int32_t* kv_indices,
+                           const int32_t* last_page_len, const int32_t* qo_indptr,
+                           const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads,
+                           int num_kv_heads, int head_dim, int page_size, float sm_scale,
+                           float k_scale, float v_scale, void* out, float* lse, int num_pages,
+                           const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                           const va_run_options_t* options, void* stream) {
   const PlanHeader* hd = nullptr;
   int rc = check_run(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
                      mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size, &sm_scale,
                      k_scale, v_scale, out, lse, num_pages, plan_h, workspace_d, workspace_bytes,
-                     &hd);
+                     options, &hd);
   if (rc) return rc;
   if (hd->n_items == 0) return VA_OK;
   PartialParams p = make_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len,
                                  qo_indptr, mask, mask_indptr, sm_scale, k_scale, v_scale, out,
-                                 lse, num_pages, hd, workspace_d);
+                                 lse, num_pages, hd, workspace_d, options);
   cudaError_t e;
   if (kernel_is_tc(hd->kernel)) {
     TcMaps maps;
@@ -326,6 +365,20 @@ int verify_attn_partial(const void* q, const void* k_cache, const void* v_cache,
                            hd->n_items, static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
+int verify_attn_partial(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* kv_indptr, const int32_t* kv_indices,
+                        const int32_t* last_page_len, const int32_t* qo_indptr,
+                        const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads,
+                        int num_kv_heads, int head_dim, int page_size, float sm_scale,
+                        float k_scale, float v_scale, void* out, float* lse, int num_pages,
+                        const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                        void* stream) {
+  return verify_attn_partial_ex(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len,
+                                qo_indptr, mask, mask_indptr, num_qo_heads, num_kv_heads,
+                                head_dim, page_size, sm_scale, k_scale, v_scale, out, lse,
+                                num_pages, plan_h, workspace_d, workspace_bytes, nullptr, stream);
 }
 
 int verify_attn_merge(const int32_t* qo_indptr, int num_qo_heads, int num_kv_heads, int head_dim,
@@ -357,6 +410,24 @@ int verify_attn_merge(const int32_t* qo_indptr, int num_qo_heads, int num_kv_hea
   return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
 }
 
+int verify_attn_run_ex(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* kv_indptr, const int32_t* kv_indices,
+                       const int32_t* last_page_len, const int32_t* qo_indptr,
+                       const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads,
+                       int num_kv_heads, int head_dim, int page_size, float sm_scale,
+                       float k_scale, float v_scale, void* out, float* lse, int num_pages,
+                       const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                       const va_run_options_t* options, void* stream) {
+  int rc = verify_attn_partial_ex(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len,
+                                  qo_indptr, mask, mask_indptr, num_qo_heads, num_kv_heads,
+                                  head_dim, page_size, sm_scale, k_scale, v_scale, out, lse,
+                                  num_pages, plan_h, workspace_d, workspace_bytes, options,
+                                  stream);
+  if (rc) return rc;
+  return verify_attn_merge(qo_indptr, num_qo_heads, num_kv_heads, head_dim, out, lse, plan_h,
+                           workspace_d, workspace_bytes, stream);
+}
+
 int verify_attn_run(const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* kv_indptr, const int32_t* kv_indices,
                     const int32_t* last_page_len, const int32_t* qo_indptr, const uint8_t* mask,
@@ -364,13 +435,10 @@ int verify_attn_run(const void* q, const void* k_cache, const void* v_cache,
                     int page_size, float sm_scale, float k_scale, float v_scale, void* out,
                     float* lse, int num_pages, const void* plan_h, void* workspace_d,
                     size_t workspace_bytes, void* stream) {
-  int rc = verify_attn_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len,
-                               qo_indptr, mask, mask_indptr, num_qo_heads, num_kv_heads, head_dim,
-                               page_size, sm_scale, k_scale, v_scale, out, lse, num_pages, plan_h,
-                               workspace_d, workspace_bytes, stream);
-  if (rc) return rc;
-  return verify_attn_merge(qo_indptr, num_qo_heads, num_kv_heads, head_dim, out, lse, plan_h,
-                           workspace_d, workspace_bytes, stream);
+  return verify_attn_run_ex(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr,
+                            mask, mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size,
+                            sm_scale, k_scale, v_scale, out, lse, num_pages, plan_h, workspace_d,
+                            workspace_bytes, nullptr, stream);
 }
 
 }  // extern "C"

@@ -148,7 +148,8 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
 // Functions", 1980: 2 pi split into a float head and tail, each product
 // with the multiple k taken exactly inside an FMA) before sincosf sees it,
 // so for positions below 2^24 the reduced angle is good to ~1e-7 rad where a
-// plain float product would be off by up to position * 2^-24.
+// plain float product would be off by up to position * 2^-24 (4e-3 rad at
+// position 32768).
 __device__ __forceinline__ void rope_cos_sin(int pos, float hi, float lo, float* c, float* s) {
   constexpr float kTwoPiHi = 6.2831854820251465f;      // float nearest to 2 pi
   constexpr float kTwoPiLo = -1.7484555314695172e-07f;  // 2 pi - kTwoPiHi
@@ -161,7 +162,9 @@ __device__ __forceinline__ void rope_cos_sin(int pos, float hi, float lo, float*
   float r = fmaf(-k, kTwoPiHi, a_hi);
   r = fmaf(-k, kTwoPiLo, r);
   r += a_lo;
-  sincosf(r, s, c);
+  // |r| <= pi + a few ulps: the hardware approximations are good to ~4e-7
+  // absolute there, far below the 2^-9 relative rounding of the bf16 result
+  __sincosf(r, s, c);
 }
 
 // Byte offset of 16-byte chunk `ch` of row `r` in a row-major shared tile of

@@ -58,6 +58,11 @@ static_assert(sizeof(MergeItem) == 32, "MergeItem layout");
 // Host plan buffer: PlanHeader, then n_items WorkItems, then n_merge
 // MergeItems.  The WorkItems and MergeItems are uploaded verbatim to the
 // device workspace at off_items.
+// PlanHeader::flags: the call features the plan was made for.
+constexpr int64_t kPlanMaskFull = 1;  // mask rows of kv_len bits (prefix included)
+constexpr int64_t kPlanNhd = 2;       // cache layout [pages, P, h_kv, d]
+constexpr int64_t kPlanRope = 4;      // queries rotated at their positions
+
 struct PlanHeader {
   uint32_t magic, version;
   int32_t batch, h_q, h_kv, head_dim, page_size, q_dtype, kv_dtype, has_mask;

@@ -10,6 +10,13 @@
 
 namespace va {
 
+// RoPE frequencies theta^(-2i/d) / rope_scale, i < d/2, as float pairs hi + lo
+// (computed in double on the host), so that position * frequency keeps ~46
+// bits before the angle is reduced.
+struct RopeFreq {
+  float hi[64], lo[64];
+};
+
 struct PartialParams {
   const void* q;              // [total_qo, h_q, D] bf16
   const void* k_cache;        // [num_pages, h_kv, P, D] bf16 / fp8
@@ -34,6 +41,10 @@ struct PartialParams {
   float v_scale;
   int n_items;                // work items in `items`
   int n_ctas;                 // persistent tcgen05 variants: item chains (see WorkItem::next)
+  int mask_full;              // mask rows hold kv_len bits, prefix included
+  int nhd;                    // cache layout [pages, P, h_kv, d]
+  const int32_t* q_position;  // nullable: RoPE position of each query token
+  RopeFreq rope;              // frequencies when q_position is set
 };
 
 struct MergeParams {
@@ -45,13 +56,6 @@ struct MergeParams {
   float* lse;                 // nullable
   int64_t part_rows;          // partial rows in the workspace
   int batch, h_q, h_kv, group;
-};
-
-// RoPE frequencies theta^(-2i/d) / rope_scale, i < d/2, as float pairs hi + lo
-// (computed in double on the host), so that position * frequency keeps ~46
-// bits before the angle is reduced.
-struct RopeFreq {
-  float hi[64], lo[64];
 };
 
 struct AppendParams {

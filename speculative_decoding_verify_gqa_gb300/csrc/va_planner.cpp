@@ -90,6 +90,11 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   for (int r : o.reserved)
     if (r) return VA_ERR_INVALID_ARGUMENT;
   if (o.max_splits < 0 || o.min_chunk < 0 || o.target_ctas < 0) return VA_ERR_INVALID_ARGUMENT;
+  if ((o.mask_layout != VA_MASK_QLEN && o.mask_layout != VA_MASK_FULL) ||
+      (o.kv_layout != VA_LAYOUT_HND && o.kv_layout != VA_LAYOUT_NHD) || (o.rope != 0 && o.rope != 1))
+    return VA_ERR_INVALID_ARGUMENT;
+  const bool full_mask = o.mask_layout == VA_MASK_FULL;
+  if (full_mask && !has_mask) return VA_ERR_INVALID_ARGUMENT;
   if (o.kernel != VA_KERNEL_AUTO && o.kernel != VA_KERNEL_MMA_64 && o.kernel != VA_KERNEL_MMA_128 &&
       o.kernel != VA_KERNEL_TC_128 && o.kernel != VA_KERNEL_TC_256)
     return VA_ERR_INVALID_ARGUMENT;
@@ -110,7 +115,8 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     if (kv_len > INT32_MAX) return VA_ERR_UNSUPPORTED;
     if (kv_len < L) return VA_ERR_INVALID_ARGUMENT;
     if (has_mask) {
-      if (mask_indptr[b] < 0 || (int64_t)mask_indptr[b + 1] - mask_indptr[b] != L * L)
+      const int64_t cols = full_mask ? kv_len : L;
+      if (mask_indptr[b] < 0 || (int64_t)mask_indptr[b + 1] - mask_indptr[b] != L * cols)
         return VA_ERR_INVALID_ARGUMENT;
     }
     if ((int64_t)G * L > INT32_MAX) return VA_ERR_UNSUPPORTED;
@@ -381,6 +387,8 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   hd.ws_bytes = align_up(hd.off_part_out + (size_t)part_rows * head_dim * 4, kWsAlign);
   hd.plan_bytes = need;
   hd.n_ctas = n_ctas;
+  hd.flags = (full_mask ? kPlanMaskFull : 0) | (o.kv_layout == VA_LAYOUT_NHD ? kPlanNhd : 0) |
+             (o.rope ? kPlanRope : 0);
 
   char* dst = static_cast<char*>(plan_h);
   std::memcpy(dst, &hd, sizeof(hd));

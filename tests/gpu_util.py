@@ -35,7 +35,11 @@ class DeviceWorkload:
         self.qo_indptr = to_dev(wl.qo_indptr, dev)
         self.mask = None if wl.mask is None else to_dev(wl.mask, dev)
         self.mask_indptr = None if wl.mask_indptr is None else to_dev(wl.mask_indptr, dev)
-        shape = (wl.num_pages, wl.h_kv, wl.page_size, wl.d)
+        shape = ((wl.num_pages, wl.page_size, wl.h_kv, wl.d) if wl.nhd
+                 else (wl.num_pages, wl.h_kv, wl.page_size, wl.d))
+        self.q_pos = None if wl.q_pos is None else to_dev(wl.q_pos, dev)
+        self.kv_pos = None if wl.kv_pos is None else to_dev(wl.kv_pos, dev)
+        self.new_pos = None if wl.kv_pos is None else to_dev(wl.new_positions(), dev)
         # 0xFF bytes: NaN in bf16 and in fp8-e4m3
         if fp8:
             self.k_cache = torch.full(shape, 0xFF, dtype=torch.uint8, device=dev).view(self.kvd)
@@ -51,22 +55,33 @@ class DeviceWorkload:
             v_tok = to_dev(wl.v_tok.view(raw), dev, self.kvd)
             tok_indptr = to_dev(wl.tok_indptr.astype(np.int32), dev)
             va.paged_kv_append(k_tok, v_tok, tok_indptr, self.kv_indptr, self.kv_indices,
-                               self.last_page_len, self.k_cache, self.v_cache)
+                               self.last_page_len, self.k_cache, self.v_cache,
+                               kv_layout=wl.kv_layout, positions=self.kv_pos,
+                               rope_theta=wl.rope_theta or 0.0)
             del k_tok, v_tok
             self.append_drafts()
 
     def append_drafts(self, status=None):
         import speculative_decoding_verify_gqa_gb300 as va
+        wl = self.wl
         va.paged_kv_append(self.k_new, self.v_new, self.qo_indptr, self.kv_indptr,
                            self.kv_indices, self.last_page_len, self.k_cache, self.v_cache,
-                           status=status)
+                           status=status, kv_layout=wl.kv_layout, positions=self.new_pos,
+                           rope_theta=wl.rope_theta or 0.0)
+
+    def features(self):
+        wl = self.wl
+        return dict(kv_layout=wl.kv_layout, mask_layout=wl.mask_layout,
+                    rope=wl.q_pos is not None)
 
     def plan(self, **opts):
         import speculative_decoding_verify_gqa_gb300 as va
         wl = self.wl
+        o = self.features()
+        o.update(opts)
         return va.verify_attn_plan(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, wl.mask_indptr,
                                    wl.h_q, wl.h_kv, wl.d, wl.page_size, kv_dtype=wl.kv_dtype,
-                                   device=self.dev, **opts)
+                                   device=self.dev, **o)
 
     def run(self, plan=None, out=None, lse=None, **opts):
         import speculative_decoding_verify_gqa_gb300 as va
@@ -76,7 +91,8 @@ class DeviceWorkload:
         out, lse = va.verify_attn_run(self.q, self.k_cache, self.v_cache, self.kv_indptr,
                                       self.kv_indices, self.last_page_len, self.qo_indptr,
                                       self.mask, self.mask_indptr, plan, sm_scale=wl.sm_scale,
-                                      k_scale=wl.k_scale, v_scale=wl.v_scale, out=out, lse=lse)
+                                      k_scale=wl.k_scale, v_scale=wl.v_scale, out=out, lse=lse,
+                                      q_position=self.q_pos, rope_theta=wl.rope_theta or 0.0)
         return out, lse, plan
 
 

@@ -1,0 +1,237 @@
+"""GPU parity of the interface-breadth features against the fp64 oracle:
+the quantising append into an fp8 cache (bit-exact), the NHD cache layout,
+flashmap's full-prefix custom-mask layout, and RoPE at the drafts' tree
+positions (new keys rotated by the append, queries inside the attention
+kernels), on every kernel variant that serves each shape."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from gpu_util import DeviceWorkload, compare, to_dev
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = [(1, "mma64"), (2, "mma128"), (3, "tc128"), (4, "tc256")]
+
+
+@pytest.fixture(scope="module")
+def va():
+    import __graft_entry__
+    __graft_entry__.build()
+    import speculative_decoding_verify_gqa_gb300 as m
+    return m
+
+
+def _raw(t, fp8):
+    return t.view(torch.uint8).cpu().numpy().view(np.uint8 if fp8 else np.uint16)
+
+
+# ------------------------------------------------------------------ quantising append
+
+@pytest.mark.parametrize("layout", ["hnd", "nhd"])
+@pytest.mark.parametrize("case", [
+    dict(batch=3, h_q=4, h_kv=2, d=64, page_size=16, prefix=("fixed", [37, 0, 70]),
+         qo=("fixed", [5, 3, 1])),
+    dict(batch=2, h_q=8, h_kv=8, d=128, page_size=64, prefix=("fixed", [100, 1]),
+         qo=("fixed", [30, 64]), value_std=40.0),
+], ids=["d64", "d128_saturating"])
+def test_quantising_append_is_bit_exact(va, case, layout):
+    """bf16 drafts into an fp8-e4m3 cache: stored = e4m3(x / scale), the
+    correctly rounded binary32 quotient rounded to nearest even and saturated
+    (value_std 40 with a small scale drives some codes past 448), bit for bit
+    equal to the oracle's quantiser; no other byte changes."""
+    wb = synthetic.make_custom(seed=5, kv_layout=layout, **case)
+    wf = synthetic.make_custom(seed=5, kv_layout=layout, kv_dtype=synthetic.FP8, **case)
+    kn, vn = wb.new_tokens()
+    ks, vs = float(np.float32(wf.k_scale * 0.25)), float(np.float32(wf.v_scale))
+    kc = synthetic.sentinel_pool(wf)
+    vc = synthetic.sentinel_pool(wf)
+    oracle.paged_kv_append_ex(kn, vn, wb.qo_indptr, wb.kv_indptr, wb.kv_indices,
+                              wb.last_page_len, wb.page_size, wb.num_pages, kc, vc,
+                              cache_fp8=True, quantize=True, k_scale=ks, v_scale=vs,
+                              kv_layout=1 if layout == "nhd" else 0)
+    assert (kc == 0x7E).any() or case["d"] == 64
+    dk = torch.from_numpy(kc.copy()).fill_(0xFF).cuda().view(torch.float8_e4m3fn)
+    dv = torch.from_numpy(vc.copy()).fill_(0xFF).cuda().view(torch.float8_e4m3fn)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    va.paged_kv_append(to_dev(kn.view(np.int16), "cuda", torch.bfloat16),
+                       to_dev(vn.view(np.int16), "cuda", torch.bfloat16),
+                       to_dev(wb.qo_indptr, "cuda"), to_dev(wb.kv_indptr, "cuda"),
+                       to_dev(wb.kv_indices, "cuda"), to_dev(wb.last_page_len, "cuda"), dk, dv,
+                       k_scale=ks, v_scale=vs, kv_layout=layout, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(_raw(dk, True), kc)
+    assert np.array_equal(_raw(dv, True), vc)
+
+
+def test_quantising_append_then_attention_over_the_fresh_drafts(va):
+    """The wide-tree fp8 shape in small: an fp8 prefix, the bf16 drafts
+    quantised into the cache by the append, then verify attention (both
+    tcgen05 variants) over the cache the append just wrote, against the
+    oracle over its own quantised cache."""
+    base = dict(batch=2, h_q=32, h_kv=8, d=128, prefix=("fixed", [1000, 300]),
+                qo=("fixed", [64, 20]), mask="tree", seed=91)
+    wf = synthetic.make_custom(kv_dtype=synthetic.FP8, **base)
+    wb = synthetic.make_custom(**base)
+    kn, vn = wb.new_tokens()
+    # the oracle's pool: every token from the fp8 workload, then the drafts
+    # quantised from bf16 over them
+    kc, vc = oracle.build_cache(wf)
+    oracle.paged_kv_append_quant(kn, vn, wf.k_scale, wf.v_scale, wf.qo_indptr, wf.kv_indptr,
+                                 wf.kv_indices, wf.last_page_len, wf.page_size, wf.num_pages,
+                                 kc, vc)
+    dw = DeviceWorkload(wf)
+    va.paged_kv_append(to_dev(kn.view(np.int16), "cuda", torch.bfloat16),
+                       to_dev(vn.view(np.int16), "cuda", torch.bfloat16), dw.qo_indptr,
+                       dw.kv_indptr, dw.kv_indices, dw.last_page_len, dw.k_cache, dw.v_cache,
+                       k_scale=wf.k_scale, v_scale=wf.v_scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(_raw(dw.k_cache, True), kc)
+    assert np.array_equal(_raw(dw.v_cache, True), vc)
+    for kernel in (3, 4):
+        out, lse, plan = dw.run(kernel=kernel)
+        torch.cuda.synchronize()
+        assert va.verify_attn_device_status(plan) == 0
+        compare(wf, out, lse, caches=(kc, vc))
+
+
+# ------------------------------------------------------------------ NHD layout
+
+@pytest.mark.parametrize("kernel,kname", KERNELS, ids=[k[1] for k in KERNELS])
+@pytest.mark.parametrize("kvd", [synthetic.BF16, synthetic.FP8])
+def test_nhd_layout_matches_oracle(va, kernel, kname, kvd):
+    wl = synthetic.make_custom(batch=3, h_q=16, h_kv=2, d=128, prefix=("fixed", [700, 0, 90]),
+                               qo=("fixed", [17, 40, 3]), mask="tree", kv_dtype=kvd,
+                               kv_layout="nhd", seed=93)
+    dw = DeviceWorkload(wl)
+    kc, vc = oracle.build_cache(wl)
+    assert np.array_equal(_raw(dw.k_cache, kvd == synthetic.FP8), kc)   # the NHD append, bit-exact
+    assert np.array_equal(_raw(dw.v_cache, kvd == synthetic.FP8), vc)
+    for splits in (1, 0):
+        out, lse, plan = dw.run(kernel=kernel, max_splits=splits)
+        torch.cuda.synchronize()
+        assert plan.header()["kernel"] == kernel
+        assert va.verify_attn_device_status(plan) == 0
+        compare(wl, out, lse, caches=(kc, vc))
+
+
+def test_nhd_layout_d64_page4(va):
+    wl = synthetic.make_custom(batch=2, h_q=4, h_kv=2, d=64, page_size=4, prefix=("fixed", [77, 3]),
+                               qo=("fixed", [9, 5]), mask="causal", kv_layout="nhd", seed=94)
+    dw = DeviceWorkload(wl)
+    out, lse, plan = dw.run()
+    torch.cuda.synchronize()
+    compare(wl, out, lse)
+
+
+# ------------------------------------------------------------------ full-prefix mask
+
+@pytest.mark.parametrize("kernel,kname", KERNELS, ids=[k[1] for k in KERNELS])
+@pytest.mark.parametrize("case", [
+    dict(mask="tree", prefix_visible="random"),
+    dict(mask="random", prefix_visible="random", kv_dtype=synthetic.FP8),
+    dict(mask="tree", prefix_visible="all"),
+], ids=["tree_random_prefix", "fp8_random", "tree_visible_prefix"])
+def test_full_prefix_mask_matches_oracle(va, kernel, kname, case):
+    """flashmap's full custom mask: L rows of (prefix + L) bits, so prefix
+    keys can be hidden too (random bits here); every key tile takes its
+    visibility from the row's bits."""
+    wl = synthetic.make_custom(batch=3, h_q=16, h_kv=2, d=128, prefix=("fixed", [300, 0, 45]),
+                               qo=("fixed", [17, 40, 6]), mask_layout="full", seed=95, **case)
+    dw = DeviceWorkload(wl)
+    for splits in (1, 0):
+        out, lse, plan = dw.run(kernel=kernel, max_splits=splits, target_ctas=300)
+        torch.cuda.synchronize()
+        assert plan.header()["kernel"] == kernel
+        assert va.verify_attn_device_status(plan) == 0
+        compare(wl, out, lse)
+
+
+def test_full_prefix_mask_d64(va):
+    wl = synthetic.make_custom(batch=2, h_q=4, h_kv=2, d=64, prefix=("fixed", [60, 200]),
+                               qo=("fixed", [12, 33]), mask="random", mask_layout="full",
+                               prefix_visible="random", seed=96)
+    dw = DeviceWorkload(wl)
+    out, lse, plan = dw.run()
+    torch.cuda.synchronize()
+    compare(wl, out, lse)
+
+
+# ------------------------------------------------------------------ RoPE
+
+@pytest.mark.parametrize("kernel,kname", KERNELS, ids=[k[1] for k in KERNELS])
+@pytest.mark.parametrize("case", [
+    dict(mask="tree", rope_theta=10000.0),
+    dict(mask="tree", rope_theta=500000.0, kv_dtype=synthetic.FP8),
+    dict(mask="causal", rope_theta=10000.0, kv_layout="nhd"),
+], ids=["tree_bf16", "tree_fp8_llama3_theta", "chain_nhd"])
+def test_rope_at_tree_positions_matches_oracle(va, kernel, kname, case):
+    """RoPE at the drafts' tree positions (prefix + depth): the append
+    rotates every key at its position, the attention kernel rotates each
+    query row at its token's position; compared with the oracle, which
+    rotates in fp64 (its cache is its own rotated append)."""
+    wl = synthetic.make_custom(batch=3, h_q=16, h_kv=2, d=128,
+                               prefix=("fixed", [2000, 0, 130]), qo=("fixed", [17, 40, 6]),
+                               seed=97, **case)
+    dw = DeviceWorkload(wl)
+    for splits in (1, 0):
+        out, lse, plan = dw.run(kernel=kernel, max_splits=splits, target_ctas=300)
+        torch.cuda.synchronize()
+        assert plan.header()["kernel"] == kernel
+        assert va.verify_attn_device_status(plan) == 0
+        compare(wl, out, lse)
+
+
+def test_rope_d64_and_long_positions(va):
+    """Warp-level kernel at head_dim 64, positions past 32K (the angle
+    reduction matters there)."""
+    wl = synthetic.make_custom(batch=2, h_q=8, h_kv=2, d=64, prefix=("fixed", [33000, 5]),
+                               qo=("fixed", [9, 4]), mask="tree", rope_theta=10000.0, seed=98)
+    dw = DeviceWorkload(wl)
+    out, lse, plan = dw.run()
+    torch.cuda.synchronize()
+    compare(wl, out, lse)
+
+
+def test_rope_append_rounds_within_one_step(va):
+    """The append's rotated keys against the oracle's fp64 rotation rounded
+    once: equal, or one step of the cache dtype apart where the fp32 and
+    fp64 rotations fall on the two sides of a rounding boundary."""
+    for kvd in (synthetic.BF16, synthetic.FP8):
+        wl = synthetic.make_custom(batch=2, h_q=8, h_kv=2, d=128, prefix=("fixed", [4000, 31]),
+                                   qo=("fixed", [17, 9]), mask="tree", rope_theta=10000.0,
+                                   kv_dtype=kvd, seed=99)
+        dw = DeviceWorkload(wl)
+        torch.cuda.synchronize()
+        kc, vc = oracle.build_cache(wl)
+        fp8 = kvd == synthetic.FP8
+        gk = _raw(dw.k_cache, fp8)
+        assert np.array_equal(_raw(dw.v_cache, fp8), vc)      # values are not rotated
+        dec = oracle.decode_e4m3 if fp8 else oracle.decode_bf16
+        written = kc != (0xFF if fp8 else 0xFFFF)
+        a, b = dec(gk[written]), dec(kc[written])
+        # one step of the format at b: 3 (e4m3) or 7 (bf16) fraction bits,
+        # subnormal steps below 2^-6 (e4m3) or 2^-126 (bf16)
+        emin = -6.0 if fp8 else -126.0
+        e = np.floor(np.log2(np.maximum(np.abs(b), 2.0 ** emin)))
+        spacing = np.exp2(e - (3 if fp8 else 7))
+        assert np.all(np.abs(a - b) <= spacing * 1.0001)
+        assert np.mean(gk[written] == kc[written]) > 0.99
+
+
+def test_rope_plan_needs_positions(va):
+    wl = synthetic.make_custom(batch=1, h_q=4, h_kv=2, d=128, prefix=("fixed", [40]),
+                               qo=("fixed", [3]), mask="causal", rope_theta=10000.0, seed=100)
+    dw = DeviceWorkload(wl)
+    plan = dw.plan()
+    with pytest.raises(va.VerifyAttnError):
+        va.verify_attn_run(dw.q, dw.k_cache, dw.v_cache, dw.kv_indptr, dw.kv_indices,
+                           dw.last_page_len, dw.qo_indptr, None, None, plan)
+    plain = dw.plan(rope=False)
+    with pytest.raises(va.VerifyAttnError):
+        va.verify_attn_run(dw.q, dw.k_cache, dw.v_cache, dw.kv_indptr, dw.kv_indices,
+                           dw.last_page_len, dw.qo_indptr, None, None, plain,
+                           q_position=dw.q_pos)
