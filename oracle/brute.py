@@ -39,12 +39,22 @@ def _rotate(x, pos, theta, scale):
     return y
 
 
+def _round_bf16(x: float) -> float:
+    """x rounded to the nearest bf16 value (8 significant bits; ties to even,
+    Python's round()), normal range only."""
+    if x == 0.0 or not math.isfinite(x):
+        return x
+    m, e = math.frexp(x)            # x = m * 2^e, 0.5 <= |m| < 1
+    return math.ldexp(round(m * 256.0), e - 8)
+
+
 def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_len, qo_indptr,
                 mask, mask_indptr, h_q, h_kv, d, page_size, sm_scale, k_scale=1.0, v_scale=1.0,
                 kv_layout=0, mask_layout=0, q_pos=None, rope_theta=0.0, rope_scale=1.0):
     """kv_layout 1: the cache is [pages, page_size, h_kv, d]; mask_layout 1:
     request b's mask is L rows of kv_len bits (prefix included); q_pos: each
-    query row is rotated at its token's position before the dot products."""
+    query row is rotated at its token's position and rounded to bf16 before
+    the dot products."""
     qd = _decode(q, False)
     kd = _decode(k_cache, kv_fp8)
     vd = _decode(v_cache, kv_fp8)
@@ -67,7 +77,8 @@ def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_le
                 logits, values = [], []
                 qrow = [float(qd[tok, qh, e]) for e in range(d)]
                 if q_pos is not None:
-                    qrow = _rotate(qrow, float(q_pos[tok]), rope_theta, rope_scale)
+                    qrow = [_round_bf16(v) for v in
+                            _rotate(qrow, float(q_pos[tok]), rope_theta, rope_scale)]
                 for j in range(kv_len):
                     if mask is not None and mask_layout == 1:
                         bit = int(mask_indptr[b]) + t * kv_len + j

@@ -319,8 +319,15 @@ static void* run_rows(void* arg) {
         int64_t t = tok - jb->qo_start;
         for (int e = 0; e < jb->d; ++e)
             qrow[e] = oracle_decode_bf16(jb->q[flat * jb->d + e]);
-        if (jb->q_pos)
+        if (jb->q_pos) {
+            /* RoPE maps the bf16 query tensor to a bf16 query tensor: the
+             * rotated row is rounded once to bf16 (nearest even) before the
+             * dot products, as the rotated queries the pages' kernels feed
+             * to their bf16 matrix units are */
             oracle_rope_vec(qrow, jb->d, (double)jb->q_pos[tok], jb->rope_theta, jb->rope_scale);
+            for (int e = 0; e < jb->d; ++e)
+                qrow[e] = oracle_decode_bf16(oracle_encode_bf16(qrow[e]));
+        }
         /* One query row against the request's keys of KV head h: K/V rows are
          * [j][h][:] so the row stride is h_kv * d and the base is offset by h. */
         oracle_dense_attention(1, (int)jb->kv_len, jb->d, qrow, jb->d,
@@ -345,7 +352,7 @@ static void* run_rows(void* arg) {
  *           bits (see build_mask)
  *  q_pos    NULL, or [total_qo] positions: each query row is rotated by
  *           oracle_rope_vec at its token's position (rope_theta, rope_scale)
- *           before the dot products
+ *           and rounded to bf16 (the query dtype) before the dot products
  *  sel / n_sel: flat row ids token * h_q + head to compute (NULL = all rows,
  *           in flat order); out [n, d] and lse [n] follow the selection order.
  *  nthreads: worker threads (>= 1).

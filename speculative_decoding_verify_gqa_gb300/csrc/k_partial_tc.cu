@@ -637,8 +637,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         // Q in place, each thread its own row of its Q tile: rotated at the
         // row's position (RoPE: element i with i + 64, i.e. chunk j of the
         // first 64-column half with chunk j of the second, the same swizzled
-        // slot), then rounded to the MMA's operand type (f16 for an fp8
-        // cache).  A Q tile the item does not use still counts its arrival.
+        // slot) and rounded to bf16, then widened to f16 for an fp8 cache.  A Q tile the item does not use still counts its arrival.
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q), nit & 1, abort_flag))) { live = false; break; }
         if (mine) {
           const int brq = qt * C::ROWS + r;
@@ -663,8 +662,14 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
                 const float b0 = __uint_as_float(wb[k] << 16), b1 = __uint_as_float(wb[k] & 0xffff0000u);
                 const float ya0 = fmaf(a0, c0, -b0 * s0), ya1 = fmaf(a1, c1, -b1 * s1);
                 const float yb0 = fmaf(b0, c0, a0 * s0), yb1 = fmaf(b1, c1, a1 * s1);
-                wa[k] = FP8 ? pack_f16x2(ya0, ya1) : pack_bf16x2(ya0, ya1);
-                wb[k] = FP8 ? pack_f16x2(yb0, yb1) : pack_bf16x2(yb0, yb1);
+                // the rotated query is a bf16 tensor; an fp8 cache's f16
+                // MMAs take it widened (exactly) to f16
+                wa[k] = pack_bf16x2(ya0, ya1);
+                wb[k] = pack_bf16x2(yb0, yb1);
+                if (FP8) {
+                  wa[k] = bf16x2_to_f16x2(wa[k]);
+                  wb[k] = bf16x2_to_f16x2(wb[k]);
+                }
               }
             } else if (FP8) {
               a.x = bf16x2_to_f16x2(a.x);
