@@ -21,18 +21,24 @@ template <int D>
 __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) {
   constexpr int V = D / 32;
   constexpr int CH = 24;  // splits whose loads are issued together
+  // The merge list (uploaded with the plan) and qo_indptr are read before
+  // the wait for the split kernel: no kernel of the step writes them.
+  grid_dependents_launch();  // the next kernel may be scheduled; it waits for our completion
   const MergeItem it = p.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * 4 + warp;
-  grid_dependency_wait();  // the partials come from the preceding split kernel
-  grid_dependents_launch();  // the next kernel may be scheduled; it waits for our completion
-  if (r >= it.nrows) return;
   // a merge list left in the workspace by another plan: nothing outside this
   // call's tables and partial rows is read or written
-  if (it.b < 0 || it.b >= p.batch || it.h < 0 || it.h >= p.h_kv || it.part_row0 < 0 || it.nsplit < 1 ||
-      (long long)it.part_row0 + (long long)it.nsplit * it.nrows > p.part_rows || it.row0 < 0)
-    return;
-  if ((it.row0 + r) / p.group >= p.qo_indptr[it.b + 1] - p.qo_indptr[it.b]) return;
+  const bool item_ok = it.b >= 0 && it.b < p.batch && it.h >= 0 && it.h < p.h_kv &&
+                       it.part_row0 >= 0 && it.nsplit >= 1 && it.row0 >= 0 &&
+                       (long long)it.part_row0 + (long long)it.nsplit * it.nrows <= p.part_rows;
+  const int qo0 = item_ok ? p.qo_indptr[it.b] : 0;
+  const bool row_ok = item_ok && r < it.nrows &&
+                      (it.row0 + r) / p.group < p.qo_indptr[it.b + 1] - qo0;
+  // the partials come from the preceding split kernel; every thread waits,
+  // so that this grid's completion implies that kernel's
+  grid_dependency_wait();
+  if (!row_ok) return;
   const float* lse_base = p.part_lse + it.part_row0 + r;
   float m = -INFINITY, den = 0.f;
   float acc[V];
@@ -82,7 +88,7 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) 
   const float inv = den > 0.f ? 1.f / den : 0.f;
   const int rr = it.row0 + r;
   const int t = rr / p.group, g = rr - t * p.group;
-  const size_t orow = (size_t)(p.qo_indptr[it.b] + t) * p.h_q + (size_t)it.h * p.group + g;
+  const size_t orow = (size_t)(qo0 + t) * p.h_q + (size_t)it.h * p.group + g;
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + orow * D + lane * V;
   if constexpr (V == 4) {
     uint2 v;
@@ -136,10 +142,11 @@ __device__ __forceinline__ void load_f32(const uint8_t* row, int bf16_src, int e
 }
 
 __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams p) {
-  // Launched with programmatic serialization: the pages may still be read by
-  // the kernel before this one, so wait for it; the attention kernel after
-  // this one may be scheduled at once (it waits for our completion).
-  grid_dependency_wait();
+  // Launched with programmatic serialization: the attention kernel after this
+  // one may be scheduled at once (it waits for our completion before it reads
+  // a draft's slot).  The index tables are read before the wait for the
+  // kernel before this one; the new rows (which that kernel may produce) are
+  // read, and the cache slots (which it may still be reading) written, after.
   grid_dependents_launch();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long per_tok = (long long)p.h_kv * p.row_chunks;
@@ -161,12 +168,16 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
   const int lpl = npg > 0 ? __ldg(p.last_page_len + b) : 0;
   const long long kv_len = npg > 0 ? (long long)(npg - 1) * p.page_size + lpl : 0;
   const long long pos = kv_len - n + (i - a0);
-  if (i < a0 || i - a0 >= n || pos < 0 || (npg > 0 && (lpl < 1 || lpl > p.page_size)) ||
-      (pos >> p.log2_page) >= npg) {
+  const bool pos_ok = !(i < a0 || i - a0 >= n || pos < 0 || (npg > 0 && (lpl < 1 || lpl > p.page_size)) ||
+                        (pos >> p.log2_page) >= npg);
+  const int page = pos_ok ? __ldg(p.kv_indices + pg0 + (int)(pos >> p.log2_page)) : -1;
+  // every thread with a token waits, so that this grid's completion implies
+  // the previous grid's
+  grid_dependency_wait();
+  if (!pos_ok) {
     if (p.status) atomicOr(p.status, VA_DEV_BAD_APPEND);
     return;
   }
-  const int page = __ldg(p.kv_indices + pg0 + (int)(pos >> p.log2_page));
   if ((unsigned)page >= (unsigned)p.num_pages) {
     if (p.status) atomicOr(p.status, VA_DEV_BAD_PAGE);
     return;

@@ -264,11 +264,12 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Inputs (pages appended by the previous kernel, q, tables) may come from
-  // the grid before this one in the stream.  Every CTA of this persistent
-  // grid is resident, so the next kernel (the merge) may be scheduled now: it
-  // waits for our completion before reading anything.
-  grid_dependency_wait();
+  // Every CTA of this persistent grid is resident, so the next kernel (the
+  // merge) may be scheduled now: it waits for our completion before reading
+  // anything.  The wait for the grid before this one in the stream (which
+  // may still be writing q or the drafts' pages) is the producer's alone: it
+  // is taken before the first load of q or of a key tile holding draft keys,
+  // and every other role consumes what the producer loads after it.
   grid_dependents_launch();
 
   // Operand u = 2 j (K_j) or 2 j + 1 (V_j) of the CTA's running tile count j
@@ -292,6 +293,9 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         return true;
       };
       int slot = blockIdx.x, steps = 0;
+      bool waited = false;  // the dependency on the previous grid has been waited for
+      const bool nhd = p.nhd != 0;
+      const int ps8 = p.page_size >> 3;
       for (int i = first_item(slot); live && i >= 0; i = next_item(i, slot, steps)) {
         const ItemGeo g = decode(i);
         if (!post(g, 0)) {
@@ -302,14 +306,6 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
           bad_item = 1;
           continue;
         }
-        // Q of this item once the previous item's S MMAs are done with Q
-        if (nit >= 1 && !mbar_wait(bar(B_Q_FREE), (nit - 1) & 1, abort_flag)) break;
-        mbar_expect_tx(bar(B_Q), g.nq * C::QT_BYTES);
-        const int tok0 = g.qo0 + g.row0 / G;
-        for (int qt = 0; qt < g.nq; ++qt)
-          for (int half = 0; half < 2; ++half)
-            tma_load_3d(sbase + C::OFF_Q + qt * C::QT_BYTES + half * (C::QT_BYTES / 2), &maps.q,
-                        half * 64, g.h * G, tok0 + qt * (C::ROWS / G), bar(B_Q));
         // Page ids of a tile's 16-key boxes (-1 past the chunk), loaded two
         // tiles ahead so their latency hides behind the previous tiles' waits
         // (and an item's first two tiles wait for one round trip, not two).
@@ -322,9 +318,39 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
             pg[q] = (j < g.n_tiles && key < g.hi) ? __ldg(p.kv_indices + g.pg0 + (key >> p.log2_page)) : -1;
           }
         };
+        // Q of this item once the previous item's S MMAs are done with Q
+        auto issue_q = [&]() -> bool {
+          if (nit >= 1 && !mbar_wait(bar(B_Q_FREE), (nit - 1) & 1, abort_flag)) return false;
+          mbar_expect_tx(bar(B_Q), g.nq * C::QT_BYTES);
+          const int tok0 = g.qo0 + g.row0 / G;
+          for (int qt = 0; qt < g.nq; ++qt)
+            for (int half = 0; half < 2; ++half)
+              tma_load_3d(sbase + C::OFF_Q + qt * C::QT_BYTES + half * (C::QT_BYTES / 2), &maps.q,
+                          half * 64, g.h * G, tok0 + qt * (C::ROWS / G), bar(B_Q));
+          return true;
+        };
         load_pages(0, cur);
         load_pages(1, nxt);
+        // The CTA's first item issues its key tiles that hold prefix keys only
+        // (no kernel of this step writes them: an append writes the drafts'
+        // slots) before the dependency wait, as far as the empty ring holds
+        // them, so they stream in while the previous grid (the append)
+        // finishes; q and any tile with draft keys wait for it.
+        bool q_sent = false;
+        if (waited) {
+          if (!issue_q()) break;
+          q_sent = true;
+        }
         for (int j = 0; live && j < g.n_tiles; ++j) {
+          if (!q_sent && (u + 2 > C::NSLOT || min(g.lo + (j + 1) * C::KEYS, g.hi) > g.prefix)) {
+            grid_dependency_wait();
+            waited = true;
+            if (!issue_q()) {
+              live = false;
+              break;
+            }
+            q_sent = true;
+          }
           load_pages(j + 2, nx2);
           const int k0 = g.lo + j * C::KEYS;
           for (int v = 0; v < 2; ++v, ++u) {
@@ -353,11 +379,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
               if constexpr (FP8) {
                 tma_load_4d(dst + q * 2048, map, 0, slot, g.h, page, bar(B_FULL + s));
               } else {
-                if (p.nhd)
-                  tma_load_5d(dst + q * 4096, map, 0, 0, 0, g.h, page * (p.page_size >> 3) + (slot >> 3),
-                              bar(B_FULL + s));
-                else
-                  tma_load_5d(dst + q * 4096, map, 0, 0, 0, slot >> 3, page * p.h_kv + g.h, bar(B_FULL + s));
+                // HND view [page * h_kv + head][slot / 8]...; NHD view
+                // [page * P / 8 + slot / 8][head]...
+                const int c3 = nhd ? g.h : (slot >> 3);
+                const int c4 = nhd ? page * ps8 + (slot >> 3) : page * p.h_kv + g.h;
+                tma_load_5d(dst + q * 4096, map, 0, 0, 0, c3, c4, bar(B_FULL + s));
               }
             }
           }
@@ -367,8 +393,17 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
             nxt[q] = nx2[q];
           }
         }
+        if (!live) break;
+        if (!q_sent) {  // every tile went out before the wait
+          grid_dependency_wait();
+          waited = true;
+          if (!issue_q()) break;
+        }
         ++nit;
       }
+      // A CTA that met no valid item still waits once, so that this grid's
+      // completion implies the previous grid's (the next kernel relies on it)
+      if (!waited) grid_dependency_wait();
       if (live) post(ItemGeo{}, 1);  // end of the chain
       if (bad) atomicOr(p.status, VA_DEV_BAD_PAGE);
       if (bad_item) atomicOr(p.status, VA_DEV_BAD_TABLE);
@@ -645,11 +680,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
           const int qpos = rot ? __ldg(p.q_position + g.qo0 + (g.row0 + brq) / G) : 0;
           uint8_t* h0 = smem + C::OFF_Q + qt * C::QT_BYTES + r * 128;
           uint8_t* h1 = h0 + C::QT_BYTES / 2;
+          if (rot) {
 #pragma unroll 1
-          for (int jp = 0; jp < 8; ++jp) {
-            uint4 a = *reinterpret_cast<uint4*>(h0 + jp * 16);
-            uint4 b = *reinterpret_cast<uint4*>(h1 + jp * 16);
-            if (rot) {
+            for (int jp = 0; jp < 8; ++jp) {
+              uint4 a = *reinterpret_cast<uint4*>(h0 + jp * 16);
+              uint4 b = *reinterpret_cast<uint4*>(h1 + jp * 16);
               const int i0 = (jp ^ (r & 7)) << 3;   // frequency index of the chunk's first element
               uint32_t* wa = reinterpret_cast<uint32_t*>(&a);
               uint32_t* wb = reinterpret_cast<uint32_t*>(&b);
@@ -671,18 +706,23 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
                   wb[k] = bf16x2_to_f16x2(wb[k]);
                 }
               }
-            } else if (FP8) {
-              a.x = bf16x2_to_f16x2(a.x);
-              a.y = bf16x2_to_f16x2(a.y);
-              a.z = bf16x2_to_f16x2(a.z);
-              a.w = bf16x2_to_f16x2(a.w);
-              b.x = bf16x2_to_f16x2(b.x);
-              b.y = bf16x2_to_f16x2(b.y);
-              b.z = bf16x2_to_f16x2(b.z);
-              b.w = bf16x2_to_f16x2(b.w);
+              *reinterpret_cast<uint4*>(h0 + jp * 16) = a;
+              *reinterpret_cast<uint4*>(h1 + jp * 16) = b;
             }
-            *reinterpret_cast<uint4*>(h0 + jp * 16) = a;
-            *reinterpret_cast<uint4*>(h1 + jp * 16) = b;
+          } else if (FP8) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              uint4* q4 = reinterpret_cast<uint4*>(half ? h1 : h0);
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch) {
+                uint4 v = q4[ch];
+                v.x = bf16x2_to_f16x2(v.x);
+                v.y = bf16x2_to_f16x2(v.y);
+                v.z = bf16x2_to_f16x2(v.z);
+                v.w = bf16x2_to_f16x2(v.w);
+                q4[ch] = v;
+              }
+            }
           }
           fence_proxy_async();
         }
@@ -928,40 +968,61 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       tc_fence_after();
       const float lse = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
       const float inv = l > 0.f ? p.v_scale / l : 0.f;
-      size_t orow = 0;
-      if (row_ok) {
-        const int gg = (g.row0 + br) - t * G;
-        orow = (size_t)(g.qo0 + t) * p.h_q + (size_t)g.h * G + gg;
-      }
-      for (int q = 0; q < C::D / 32; ++q) {
-        uint32_t ov[32];
-        tmem_ld32(lane_addr + C::COL_O + q * 32, ov);
-        tmem_wait_ld();
-        if (!row_ok) continue;
-        if (g.part_row < 0) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * C::D + q * 32);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv, __uint_as_float(ov[8 * e + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv, __uint_as_float(ov[8 * e + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv, __uint_as_float(ov[8 * e + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv, __uint_as_float(ov[8 * e + 7]) * inv);
-            dst[e] = w;
-          }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(p.part_out + ((size_t)g.part_row + br) * C::D + q * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
-                                 __uint_as_float(ov[4 * e + 2]) * inv, __uint_as_float(ov[4 * e + 3]) * inv);
-        }
-      }
+      // Output row of block row br (token-major: token br / G, head h G + br % G).
+      auto out_row = [&](int brr) -> size_t {
+        const int tt = (g.row0 + brr) / G;
+        return (size_t)(g.qo0 + tt) * p.h_q + (size_t)g.h * G + ((g.row0 + brr) - tt * G);
+      };
       if (row_ok) {
         if (g.part_row < 0) {
-          if (p.lse) p.lse[orow] = lse;
+          if (p.lse) p.lse[out_row(br)] = lse;
         } else {
           p.part_lse[(size_t)g.part_row + br] = lse;
+        }
+      }
+      // O read as 16-lane x 256-bit fragments: four neighbouring threads
+      // hold eight consecutive columns of one row, so a warp's store covers
+      // eight rows in 32-byte (fp32) or 16-byte (bf16) runs instead of 32
+      // rows in 16-byte pieces.  Rows ra = 32 quad + 16 hl + lane / 4 and
+      // ra + 8; their scale comes from the lanes that own them.
+#pragma unroll 1
+      for (int hl = 0; hl < 2; ++hl) {
+        const int rl = 16 * hl + (lane >> 2);
+        const float inv_a = __shfl_sync(0xffffffffu, inv, rl);
+        const float inv_b = __shfl_sync(0xffffffffu, inv, rl + 8);
+        const int br_a = qt * C::ROWS + quad * 32 + rl, br_b = br_a + 8;
+        const bool ok_a = br_a < g.nrows, ok_b = br_b < g.nrows;
+        const int c_lo = 2 * (lane & 3);
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t ov[32];
+          tmem_ld_16x256b_x8(tmem + ((uint32_t)(quad * 32 + 16 * hl) << 16) + qt * C::QT_COLS + C::COL_O + 64 * cc, ov);
+          tmem_wait_ld();
+          if (g.part_row < 0) {
+            __nv_bfloat16* da = static_cast<__nv_bfloat16*>(p.out) + (ok_a ? out_row(br_a) : 0) * C::D + 64 * cc + c_lo;
+            __nv_bfloat16* db = static_cast<__nv_bfloat16*>(p.out) + (ok_b ? out_row(br_b) : 0) * C::D + 64 * cc + c_lo;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (ok_a)
+                *reinterpret_cast<uint32_t*>(da + 8 * k) =
+                    pack_bf16x2(__uint_as_float(ov[4 * k]) * inv_a, __uint_as_float(ov[4 * k + 1]) * inv_a);
+              if (ok_b)
+                *reinterpret_cast<uint32_t*>(db + 8 * k) =
+                    pack_bf16x2(__uint_as_float(ov[4 * k + 2]) * inv_b, __uint_as_float(ov[4 * k + 3]) * inv_b);
+            }
+          } else {
+            float* da = p.part_out + ((size_t)g.part_row + br_a) * C::D + 64 * cc + c_lo;
+            float* db = p.part_out + ((size_t)g.part_row + br_b) * C::D + 64 * cc + c_lo;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (ok_a)
+                *reinterpret_cast<float2*>(da + 8 * k) =
+                    make_float2(__uint_as_float(ov[4 * k]) * inv_a, __uint_as_float(ov[4 * k + 1]) * inv_a);
+              if (ok_b)
+                *reinterpret_cast<float2*>(db + 8 * k) =
+                    make_float2(__uint_as_float(ov[4 * k + 2]) * inv_b, __uint_as_float(ov[4 * k + 3]) * inv_b);
+            }
+          }
         }
       }
       // O has been read: the next item's first PV may overwrite it
