@@ -5,7 +5,7 @@
 
 One step is one pass of the hot path over one batch: the paged append of
 the batch's draft K/V into the cache, then verify attention (split kernel +
-LSE merge).  The plan (host) is built once before the timed region and
+LSE merge), in one verify_attn_append_run call.  The plan (host) is built once before the timed region and
 reused, as a serving step shares it across layers; the end-to-end number
 re-plans every step.  Inputs are synthetic (seeded, shaped like the
 workload) and resident in HBM when the timed region starts.  L2 (129 MB) is
@@ -223,14 +223,22 @@ class Bench:
                                         kv_dtype=wl.kv_dtype, device=device, **self.plan_opts)
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
-        self.launches_per_step = 1 + self.plan.launches()
+        self.launches_per_step = 1 + self.plan.launches()   # append, split, merge
         torch.cuda.synchronize()
 
-    # one step on pool copy i; ev: optional 4 events around append / partial /
-    # merge; verify_only: the attention call alone (no append)
+    # one step on pool copy i: the drafts appended and attended in one call
+    # (verify_attn_append_run); verify_only: the attention call alone;
+    # ev: the three kernels as separate calls with 4 events around them
     def step(self, i, ev=None, verify_only=False):
         va, wl = self.va, self.wl
         kc, vc = self.pools[i % self.n_copies]
+        if not verify_only and not ev:
+            va.verify_attn_append_run(self.k_new, self.v_new, self.q, kc, vc, self.kv_indptr,
+                                      self.kv_indices, self.last_page_len, self.qo_indptr,
+                                      self.mask, self.mask_indptr, self.plan,
+                                      sm_scale=wl.sm_scale, k_scale=wl.k_scale,
+                                      v_scale=wl.v_scale, out=self.out, lse=self.lse)
+            return
         if ev:
             ev[0].record()
         if not verify_only:
@@ -305,20 +313,55 @@ class Bench:
         return e0.elapsed_time(e1) / k, clocks
 
     def kernel_times(self, n=64):
-        """Per-kernel average durations (ms) from CUDA events recorded around
-        each launch inside a captured graph of n steps."""
-        torch = self.torch
-        ev = [[make_event(torch) for _ in range(4)] for _ in range(n)]
-        g = self.capture(n, events=ev)
-        g.replay()
-        torch.cuda.synchronize()
-        g.replay()
-        torch.cuda.synchronize()
-        app = [e[0].elapsed_time(e[1]) for e in ev]
-        part = [e[1].elapsed_time(e[2]) for e in ev]
-        mrg = [e[2].elapsed_time(e[3]) for e in ev]
-        return dict(append_ms=statistics.mean(app), partial_ms=statistics.mean(part),
-                    merge_ms=statistics.mean(mrg), partial_median_ms=statistics.median(part))
+        """Average duration (ms) of each kernel of the step: CUDA events
+        around a captured graph of n back-to-back launches of that kernel
+        alone (its own calls: verify_attn_partial, verify_attn_merge,
+        paged_kv_append), divided by n, on pool copies rotated as in the
+        step; median of 5 replays."""
+        torch, va, wl = self.torch, self.va, self.wl
+
+        def one(kind, i):
+            kc, vc = self.pools[i % self.n_copies]
+            if kind == "append":
+                va.paged_kv_append(self.k_new, self.v_new, self.qo_indptr, self.kv_indptr,
+                                   self.kv_indices, self.last_page_len, kc, vc)
+            elif kind == "partial":
+                va.verify_attn_partial(self.q, kc, vc, self.kv_indptr, self.kv_indices,
+                                       self.last_page_len, self.qo_indptr, self.mask,
+                                       self.mask_indptr, self.plan, sm_scale=wl.sm_scale,
+                                       k_scale=wl.k_scale, v_scale=wl.v_scale, out=self.out,
+                                       lse=self.lse)
+            else:
+                va.verify_attn_merge(self.qo_indptr, self.plan, self.out, self.lse)
+
+        res = {}
+        for kind in ("append", "partial", "merge"):
+            if kind == "merge" and self.plan.header()["n_merge"] == 0:
+                res["merge_ms"] = 0.0
+                continue
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                for i in range(2):
+                    one(kind, i)
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    one(kind, i)
+            g.replay()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(5):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) / n)
+            res[kind + "_ms"] = statistics.median(ts)
+        return res
 
     def e2e(self, steps):
         """End to end through the public API: pinned host inputs copied in,
@@ -369,12 +412,11 @@ class Bench:
                                        kv_dtype=wl.kv_dtype, workspace=ws, device=self.dev,
                                        num_sms=n_sms, plan_buffer=plan_buf, **self.plan_opts)
             kc, vc = self.pools[i % self.n_copies]
-            va.paged_kv_append(d["k_new"], d["v_new"], d["qo_indptr"], d["kv_indptr"],
-                               d["kv_indices"], d["last_page_len"], kc, vc)
-            va.verify_attn_run(d["q"], kc, vc, d["kv_indptr"], d["kv_indices"],
-                               d["last_page_len"], d["qo_indptr"], d.get("mask"),
-                               d.get("mask_indptr"), plan, sm_scale=wl.sm_scale,
-                               k_scale=wl.k_scale, v_scale=wl.v_scale, out=out_d, lse=lse_d)
+            va.verify_attn_append_run(d["k_new"], d["v_new"], d["q"], kc, vc, d["kv_indptr"],
+                                      d["kv_indices"], d["last_page_len"], d["qo_indptr"],
+                                      d.get("mask"), d.get("mask_indptr"), plan,
+                                      sm_scale=wl.sm_scale, k_scale=wl.k_scale,
+                                      v_scale=wl.v_scale, out=out_d, lse=lse_d)
             res_h.copy_(res_d, non_blocking=True)
             torch.cuda.synchronize()
 

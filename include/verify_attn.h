@@ -385,6 +385,33 @@ int paged_kv_append_ex(const void* k_new, const void* v_new, const int32_t* appe
                        int* status_d, void* stream);
 
 /*
+ * One verification step in one call (vLLM PR #1679: cache the drafts, then
+ * attend): paged_kv_append_ex of the drafts' K/V -- k_new / v_new hold the
+ * L_b new tokens of each request in qo_indptr order, placed at the request's
+ * last L_b positions; append_options as for paged_kv_append_ex (NULL = a bit
+ * copy into an HND cache; its kv_layout must be the plan's) -- followed by
+ * verify_attn_run_ex over the cache it has just written.  Same arguments,
+ * contract and errors as those two; the append's device check bits go to
+ * the workspace's status word (verify_attn_device_status reads them).
+ *
+ * Ordering: the append waits for the kernel before it in the stream to
+ * complete and then releases the attention kernels at once, so they read q,
+ * the tables and the cache's prefix slots while the append still runs and
+ * wait for it only before reading a draft's slot (verify_attn_run on its own
+ * reads nothing before its predecessor has completed).  k_cache / v_cache
+ * are written, so they are not const here.
+ */
+int verify_attn_append_run(const void* k_new, const void* v_new,
+                           const va_append_options_t* append_options, const void* q, void* k_cache,
+                           void* v_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
+                           const int32_t* last_page_len, const int32_t* qo_indptr,
+                           const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads,
+                           int num_kv_heads, int head_dim, int page_size, float sm_scale,
+                           float k_scale, float v_scale, void* out, float* lse, int num_pages,
+                           const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                           const va_run_options_t* run_options, void* stream);
+
+/*
  * verify_attn_run for callers that cannot allocate device memory.
  *
  * No page describes this entry point; it exists for callers that may not

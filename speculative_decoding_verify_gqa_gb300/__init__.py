@@ -32,7 +32,7 @@ __all__ = [
     "VerifyAttnError", "Plan", "lib", "verify_attn_plan", "verify_attn_run",
     "verify_attn_partial", "verify_attn_merge", "paged_kv_append",
     "verify_attn_device_status", "verify_attn_plan_bounds", "verify_attn_plan_host",
-    "verify_attn_workspace_size", "verify_attn_run_static_scratch",
+    "verify_attn_workspace_size", "verify_attn_run_static_scratch", "verify_attn_append_run",
     "status_string", "num_sms", "KV_BF16", "KV_FP8_E4M3", "library_path",
 ]
 
@@ -116,6 +116,8 @@ def lib():
                                          f32, f32, P, P, i32, P, P, sz, P, P]),
         "paged_kv_append_ex": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
                                      P, P, P]),
+        "verify_attn_append_run": (i32, [P, P, P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32,
+                                         f32, f32, f32, P, P, i32, P, P, sz, P, P]),
         "verify_attn_merge": (i32, [P, i32, i32, i32, P, P, P, P, sz, P]),
         "verify_attn_plan_launches": (i32, [P, Pi]),
         "verify_attn_plan_upload": (i32, [P, P, sz, P]),
@@ -465,6 +467,46 @@ def paged_kv_append(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_pag
     o.rope_scale = float(rope_scale) if positions is not None else 0.0
     rc = lib().paged_kv_append_ex(*common, ctypes.byref(o), _dp(status), _stream(stream))
     _check("paged_kv_append_ex", rc)
+
+
+def verify_attn_append_run(k_new, v_new, q, k_cache, v_cache, kv_indptr, kv_indices,
+                           last_page_len, qo_indptr, mask, mask_indptr, plan: Plan, sm_scale=0.0,
+                           k_scale=1.0, v_scale=1.0, out=None, lse=None, want_lse=True,
+                           num_pages=None, stream=None, q_position=None, rope_theta=10000.0,
+                           rope_scale=1.0, append_k_scale=None, append_v_scale=None,
+                           positions=None, kv_layout="hnd"):
+    """One verification step: append the drafts' K/V (k_new / v_new, one row
+    per query token in qo_indptr order; bf16 into an fp8 cache quantises with
+    append_k_scale / append_v_scale; positions rotates the new keys by RoPE),
+    then verify attention over the cache just written.  Returns (out, lse)."""
+    out, lse = _alloc_out(q, plan, out, lse, want_lse)
+    if num_pages is None:
+        num_pages = k_cache.shape[0]
+    fp8_cache = k_cache.element_size() == 1
+    quantize = fp8_cache and k_new.dtype == torch.bfloat16
+    layout = _LAYOUTS[kv_layout]
+    ao = None
+    if quantize or positions is not None or layout != LAYOUT_HND:
+        ao = AppendOptions()
+        ao.quantize = int(quantize)
+        ao.k_scale = float(append_k_scale) if quantize else 0.0
+        ao.v_scale = float(append_v_scale) if quantize else 0.0
+        ao.kv_layout = layout
+        ao.positions = _dp(positions) if positions is not None else None
+        ao.rope_theta = float(rope_theta) if positions is not None else 0.0
+        ao.rope_scale = float(rope_scale) if positions is not None else 0.0
+    ro = _run_options(q_position, rope_theta, rope_scale)
+    if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise ValueError("q and out must be bfloat16")
+    rc = lib().verify_attn_append_run(
+        _dp(k_new), _dp(v_new), None if ao is None else ctypes.byref(ao), _dp(q), _dp(k_cache),
+        _dp(v_cache), _dp(kv_indptr), _dp(kv_indices), _dp(last_page_len), _dp(qo_indptr),
+        _dp(mask), _dp(mask_indptr), plan.num_qo_heads, plan.num_kv_heads, plan.head_dim,
+        plan.page_size, float(sm_scale), float(k_scale), float(v_scale), _dp(out), _dp(lse),
+        int(num_pages), _hp(plan.host), _dp(plan.workspace), plan.workspace.numel(),
+        None if ro is None else ctypes.byref(ro), _stream(stream))
+    _check("verify_attn_append_run", rc)
+    return out, lse
 
 
 STATIC_SCRATCH_BYTES = 32 << 20

@@ -21,9 +21,11 @@ template <int D>
 __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) {
   constexpr int V = D / 32;
   constexpr int CH = 24;  // splits whose loads are issued together
-  // The merge list (uploaded with the plan) and qo_indptr are read before
-  // the wait for the split kernel: no kernel of the step writes them.
+  // After this library's split kernel in an append-and-run call, the merge
+  // list (uploaded with the plan) and qo_indptr are read before the wait for
+  // it: no kernel of the step writes them.  A call of its own waits first.
   grid_dependents_launch();  // the next kernel may be scheduled; it waits for our completion
+  if (!p.early_inputs) grid_dependency_wait();
   const MergeItem it = p.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * 4 + warp;
@@ -142,11 +144,12 @@ __device__ __forceinline__ void load_f32(const uint8_t* row, int bf16_src, int e
 }
 
 __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams p) {
-  // Launched with programmatic serialization: the attention kernel after this
-  // one may be scheduled at once (it waits for our completion before it reads
-  // a draft's slot).  The index tables are read before the wait for the
-  // kernel before this one; the new rows (which that kernel may produce) are
-  // read, and the cache slots (which it may still be reading) written, after.
+  // Launched with programmatic serialization: nothing is read before the
+  // kernel before this one (which may produce the new rows, q or the tables)
+  // has completed.  The attention kernel after this one is released right
+  // then: it may read q and the prefix pages at once, and waits for our
+  // completion before it reads a draft's slot.
+  grid_dependency_wait();
   grid_dependents_launch();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long per_tok = (long long)p.h_kv * p.row_chunks;
@@ -171,9 +174,6 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
   const bool pos_ok = !(i < a0 || i - a0 >= n || pos < 0 || (npg > 0 && (lpl < 1 || lpl > p.page_size)) ||
                         (pos >> p.log2_page) >= npg);
   const int page = pos_ok ? __ldg(p.kv_indices + pg0 + (int)(pos >> p.log2_page)) : -1;
-  // every thread with a token waits, so that this grid's completion implies
-  // the previous grid's
-  grid_dependency_wait();
   if (!pos_ok) {
     if (p.status) atomicOr(p.status, VA_DEV_BAD_APPEND);
     return;

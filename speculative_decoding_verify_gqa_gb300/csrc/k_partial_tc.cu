@@ -267,9 +267,10 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
   // Every CTA of this persistent grid is resident, so the next kernel (the
   // merge) may be scheduled now: it waits for our completion before reading
   // anything.  The wait for the grid before this one in the stream (which
-  // may still be writing q or the drafts' pages) is the producer's alone: it
-  // is taken before the first load of q or of a key tile holding draft keys,
-  // and every other role consumes what the producer loads after it.
+  // may still be writing the drafts' pages) is the producer's alone: it is
+  // taken before the first load of a key tile holding draft keys, and every
+  // role that writes memory does so after consuming such loads or q, so its
+  // writes follow the previous grid's completion.
   grid_dependents_launch();
 
   // Operand u = 2 j (K_j) or 2 j + 1 (V_j) of the CTA's running tile count j
@@ -294,6 +295,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       };
       int slot = blockIdx.x, steps = 0;
       bool waited = false;  // the dependency on the previous grid has been waited for
+      if (!p.early_inputs) {
+        // a call of its own: nothing is read before the previous grid is done
+        grid_dependency_wait();
+        waited = true;
+      }
       const bool nhd = p.nhd != 0;
       const int ps8 = p.page_size >> 3;
       for (int i = first_item(slot); live && i >= 0; i = next_item(i, slot, steps)) {
@@ -331,25 +337,19 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         };
         load_pages(0, cur);
         load_pages(1, nxt);
-        // The CTA's first item issues its key tiles that hold prefix keys only
-        // (no kernel of this step writes them: an append writes the drafts'
-        // slots) before the dependency wait, as far as the empty ring holds
-        // them, so they stream in while the previous grid (the append)
-        // finishes; q and any tile with draft keys wait for it.
+        // After this library's append (early inputs), the CTA's first item
+        // issues q and its key tiles that hold prefix keys only before the
+        // dependency wait: the append writes none of them (only the drafts'
+        // slots) and releases this kernel only after its own predecessor --
+        // the producer of q -- has completed, so they stream in while the
+        // append finishes.  Tiles with draft keys wait for it.
         bool q_sent = false;
-        if (waited) {
-          if (!issue_q()) break;
-          q_sent = true;
-        }
+        if (!issue_q()) break;
+        q_sent = true;
         for (int j = 0; live && j < g.n_tiles; ++j) {
-          if (!q_sent && (u + 2 > C::NSLOT || min(g.lo + (j + 1) * C::KEYS, g.hi) > g.prefix)) {
+          if (!waited && (u + 2 > C::NSLOT || min(g.lo + (j + 1) * C::KEYS, g.hi) > g.prefix)) {
             grid_dependency_wait();
             waited = true;
-            if (!issue_q()) {
-              live = false;
-              break;
-            }
-            q_sent = true;
           }
           load_pages(j + 2, nx2);
           const int k0 = g.lo + j * C::KEYS;
@@ -394,11 +394,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
           }
         }
         if (!live) break;
-        if (!q_sent) {  // every tile went out before the wait
-          grid_dependency_wait();
-          waited = true;
-          if (!issue_q()) break;
-        }
+        (void)q_sent;
         ++nit;
       }
       // A CTA that met no valid item still waits once, so that this grid's
@@ -664,6 +660,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     const float c = p.scale_log2;
     int ns = 0, no = 0, nit = 0, u0 = 0;            // S tiles seen, items done, items, ring base
     bool live = true;
+    bool dep_waited = false;                        // this thread has waited for the previous grid
     ItemGeo g;
     for (int k = 0; live && take_geo_warp(k, g); ++k) {
       if (!g.ok) continue;
@@ -968,6 +965,14 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       tc_fence_after();
       const float lse = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
       const float inv = l > 0.f ? p.v_scale / l : 0.f;
+      // The first write of this thread waits for the previous grid: an item
+      // whose tiles all went out before the producer's wait could otherwise
+      // finish before it, and that grid may still read the workspace (a
+      // merge of the previous call) or the output
+      if (!dep_waited) {
+        grid_dependency_wait();
+        dep_waited = true;
+      }
       // Output row of block row br (token-major: token br / G, head h G + br % G).
       auto out_row = [&](int brr) -> size_t {
         const int tt = (g.row0 + brr) / G;

@@ -239,6 +239,70 @@ int make_tc_maps(const void* q, int64_t total_qo, const void* k_cache, const voi
 
 }  // namespace
 
+static int verify_attn_merge_impl(const int32_t* qo_indptr, int num_qo_heads, int num_kv_heads,
+                                  int head_dim, void* out, float* lse, const void* plan_h,
+                                  void* workspace_d, size_t workspace_bytes, int early,
+                                  void* stream) {
+  const PlanHeader* hd = plan_header(plan_h);
+  if (!hd) return VA_ERR_INVALID_ARGUMENT;
+  if (hd->h_q != num_qo_heads || hd->h_kv != num_kv_heads || hd->head_dim != head_dim)
+    return VA_ERR_PLAN_MISMATCH;
+  if (hd->n_merge == 0) return VA_OK;
+  if (!workspace_d || workspace_bytes < hd->ws_bytes) return VA_ERR_WORKSPACE_TOO_SMALL;
+  if (!qo_indptr || !out || !aligned16(out) || !aligned16(workspace_d))
+    return VA_ERR_INVALID_ARGUMENT;
+  char* ws = static_cast<char*>(workspace_d);
+  MergeParams m;
+  m.items = reinterpret_cast<const MergeItem*>(ws + hd->off_merge);
+  m.part_out = reinterpret_cast<const float*>(ws + hd->off_part_out);
+  m.part_lse = reinterpret_cast<const float*>(ws + hd->off_part_lse);
+  m.qo_indptr = qo_indptr;
+  m.out = out;
+  m.lse = lse;
+  m.batch = hd->batch;
+  m.part_rows = hd->part_rows;
+  m.h_q = hd->h_q;
+  m.h_kv = hd->h_kv;
+  m.group = hd->group;
+  m.early_inputs = early;
+  cudaError_t e = launch_merge(m, hd->head_dim, hd->n_merge, hd->block_rows,
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
+static int run_partial(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* kv_indptr, const int32_t* kv_indices,
+                           const int32_t* last_page_len, const int32_t* qo_indptr,
+                           const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads,
+                           int num_kv_heads, int head_dim, int page_size, float sm_scale,
+                           float k_scale, float v_scale, void* out, float* lse, int num_pages,
+                           const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                           const va_run_options_t* options, int early, void* stream) {
+  const PlanHeader* hd = nullptr;
+  int rc = check_run(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
+                     mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size, &sm_scale,
+                     k_scale, v_scale, out, lse, num_pages, plan_h, workspace_d, workspace_bytes,
+                     options, &hd);
+  if (rc) return rc;
+  if (hd->n_items == 0) return VA_OK;
+  PartialParams p = make_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len,
+                                 qo_indptr, mask, mask_indptr, sm_scale, k_scale, v_scale, out,
+                                 lse, num_pages, hd, workspace_d, options);
+  p.early_inputs = early;
+  cudaError_t e;
+  if (kernel_is_tc(hd->kernel)) {
+    TcMaps maps;
+    rc = make_tc_maps(q, hd->total_qo, k_cache, v_cache, num_pages, hd, &maps);
+    if (rc) return rc;
+    e = launch_partial_tc(p, maps, hd->kv_dtype == VA_DTYPE_FP8_E4M3, hd->block_rows, hd->n_items,
+                          static_cast<cudaStream_t>(stream));
+  } else {
+    e = launch_partial_mma(p, hd->kernel, hd->head_dim, hd->kv_dtype == VA_DTYPE_FP8_E4M3,
+                           hd->n_items, static_cast<cudaStream_t>(stream));
+  }
+  return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
 extern "C" {
 
 const char* verify_attn_status_string(int status) {
@@ -343,28 +407,10 @@ int verify_attn_partial_ex(const void* q, const void* k_cache, const void* v_cac
                            float k_scale, float v_scale, void* out, float* lse, int num_pages,
                            const void* plan_h, void* workspace_d, size_t workspace_bytes,
                            const va_run_options_t* options, void* stream) {
-  const PlanHeader* hd = nullptr;
-  int rc = check_run(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
-                     mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size, &sm_scale,
+  return run_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
+                     mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale,
                      k_scale, v_scale, out, lse, num_pages, plan_h, workspace_d, workspace_bytes,
-                     options, &hd);
-  if (rc) return rc;
-  if (hd->n_items == 0) return VA_OK;
-  PartialParams p = make_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len,
-                                 qo_indptr, mask, mask_indptr, sm_scale, k_scale, v_scale, out,
-                                 lse, num_pages, hd, workspace_d, options);
-  cudaError_t e;
-  if (kernel_is_tc(hd->kernel)) {
-    TcMaps maps;
-    rc = make_tc_maps(q, hd->total_qo, k_cache, v_cache, num_pages, hd, &maps);
-    if (rc) return rc;
-    e = launch_partial_tc(p, maps, hd->kv_dtype == VA_DTYPE_FP8_E4M3, hd->block_rows, hd->n_items,
-                          static_cast<cudaStream_t>(stream));
-  } else {
-    e = launch_partial_mma(p, hd->kernel, hd->head_dim, hd->kv_dtype == VA_DTYPE_FP8_E4M3,
-                           hd->n_items, static_cast<cudaStream_t>(stream));
-  }
-  return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+                     options, 0, stream);
 }
 
 int verify_attn_partial(const void* q, const void* k_cache, const void* v_cache,
@@ -384,30 +430,8 @@ int verify_attn_partial(const void* q, const void* k_cache, const void* v_cache,
 int verify_attn_merge(const int32_t* qo_indptr, int num_qo_heads, int num_kv_heads, int head_dim,
                       void* out, float* lse, const void* plan_h, void* workspace_d,
                       size_t workspace_bytes, void* stream) {
-  const PlanHeader* hd = plan_header(plan_h);
-  if (!hd) return VA_ERR_INVALID_ARGUMENT;
-  if (hd->h_q != num_qo_heads || hd->h_kv != num_kv_heads || hd->head_dim != head_dim)
-    return VA_ERR_PLAN_MISMATCH;
-  if (hd->n_merge == 0) return VA_OK;
-  if (!workspace_d || workspace_bytes < hd->ws_bytes) return VA_ERR_WORKSPACE_TOO_SMALL;
-  if (!qo_indptr || !out || !aligned16(out) || !aligned16(workspace_d))
-    return VA_ERR_INVALID_ARGUMENT;
-  char* ws = static_cast<char*>(workspace_d);
-  MergeParams m;
-  m.items = reinterpret_cast<const MergeItem*>(ws + hd->off_merge);
-  m.part_out = reinterpret_cast<const float*>(ws + hd->off_part_out);
-  m.part_lse = reinterpret_cast<const float*>(ws + hd->off_part_lse);
-  m.qo_indptr = qo_indptr;
-  m.out = out;
-  m.lse = lse;
-  m.batch = hd->batch;
-  m.part_rows = hd->part_rows;
-  m.h_q = hd->h_q;
-  m.h_kv = hd->h_kv;
-  m.group = hd->group;
-  cudaError_t e = launch_merge(m, hd->head_dim, hd->n_merge, hd->block_rows,
-                               static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+  return verify_attn_merge_impl(qo_indptr, num_qo_heads, num_kv_heads, head_dim, out, lse, plan_h,
+                                workspace_d, workspace_bytes, 0, stream);
 }
 
 int verify_attn_run_ex(const void* q, const void* k_cache, const void* v_cache,
@@ -609,6 +633,41 @@ int paged_kv_append_ex(const void* k_new, const void* v_new, const int32_t* appe
   if (o.positions) rope_frequencies(o.rope_theta, rope_scale, head_dim, &p.rope);
   cudaError_t e = launch_append(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
+int verify_attn_append_run(const void* k_new, const void* v_new,
+                           const va_append_options_t* append_options, const void* q, void* k_cache,
+                           void* v_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
+                           const int32_t* last_page_len, const int32_t* qo_indptr,
+                           const uint8_t* mask, const int32_t* mask_indptr, int num_qo_heads,
+                           int num_kv_heads, int head_dim, int page_size, float sm_scale,
+                           float k_scale, float v_scale, void* out, float* lse, int num_pages,
+                           const void* plan_h, void* workspace_d, size_t workspace_bytes,
+                           const va_run_options_t* run_options, void* stream) {
+  // every check of the run before anything is enqueued
+  const PlanHeader* hd = nullptr;
+  float sc = sm_scale;
+  int rc = check_run(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
+                     mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size, &sc, k_scale,
+                     v_scale, out, lse, num_pages, plan_h, workspace_d, workspace_bytes,
+                     run_options, &hd);
+  if (rc) return rc;
+  const int layout = append_options ? (int)append_options->kv_layout : VA_LAYOUT_HND;
+  if (layout != ((hd->flags & kPlanNhd) ? VA_LAYOUT_NHD : VA_LAYOUT_HND)) return VA_ERR_PLAN_MISMATCH;
+  if (hd->total_qo > 0) {
+    int* status = reinterpret_cast<int*>(static_cast<char*>(workspace_d) + hd->off_status);
+    rc = paged_kv_append_ex(k_new, v_new, qo_indptr, kv_indptr, kv_indices, last_page_len, k_cache,
+                            v_cache, hd->batch, num_kv_heads, head_dim, page_size, num_pages,
+                            (va_dtype)hd->kv_dtype, hd->total_qo, append_options, status, stream);
+    if (rc) return rc;
+  }
+  rc = run_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
+                   mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale, k_scale,
+                   v_scale, out, lse, num_pages, plan_h, workspace_d, workspace_bytes, run_options,
+                   1, stream);
+  if (rc) return rc;
+  return verify_attn_merge_impl(qo_indptr, num_qo_heads, num_kv_heads, head_dim, out, lse, plan_h,
+                                workspace_d, workspace_bytes, 1, stream);
 }
 
 int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_indptr,

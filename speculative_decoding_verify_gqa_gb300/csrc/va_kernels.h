@@ -44,6 +44,9 @@ struct PartialParams {
   int mask_full;              // mask rows hold kv_len bits, prefix included
   int nhd;                    // cache layout [pages, P, h_kv, d]
   const int32_t* q_position;  // nullable: RoPE position of each query token
+  int early_inputs;           // 1: q, the tables and the prefix pages may be read before the
+                              // wait for the previous grid (it is this library's append,
+                              // which releases this kernel only once q's producer is done)
   RopeFreq rope;              // frequencies when q_position is set
 };
 
@@ -56,6 +59,7 @@ struct MergeParams {
   float* lse;                 // nullable
   int64_t part_rows;          // partial rows in the workspace
   int batch, h_q, h_kv, group;
+  int early_inputs;           // 1: the merge list and qo_indptr may be read before the wait
 };
 
 struct AppendParams {

@@ -241,3 +241,119 @@ def test_rope_plan_needs_positions(va):
         va.verify_attn_run(dw.q, dw.k_cache, dw.v_cache, dw.kv_indptr, dw.kv_indices,
                            dw.last_page_len, dw.qo_indptr, None, None, plain,
                            q_position=dw.q_pos)
+
+
+# ------------------------------------------------------------------ fused append + run
+
+def _fused(va, dw, plan, out=None, lse=None, **kw):
+    wl = dw.wl
+    return va.verify_attn_append_run(dw.k_new, dw.v_new, dw.q, dw.k_cache, dw.v_cache,
+                                     dw.kv_indptr, dw.kv_indices, dw.last_page_len, dw.qo_indptr,
+                                     dw.mask, dw.mask_indptr, plan, sm_scale=wl.sm_scale,
+                                     k_scale=wl.k_scale, v_scale=wl.v_scale, out=out, lse=lse,
+                                     q_position=dw.q_pos, rope_theta=wl.rope_theta or 0.0,
+                                     positions=dw.new_pos, kv_layout=wl.kv_layout, **kw)
+
+
+@pytest.mark.parametrize("name", ["tiny_verify", "llama3_8b_tree_verify", "codellama34b_chain_verify"])
+def test_append_run_matches_oracle(va, name):
+    """verify_attn_append_run (the drafts appended and attended in one call,
+    the attention reading q and the prefix while the append runs) on a pool
+    whose draft slots still hold NaN: every row against the oracle, and the
+    pool equal to the oracle's, bit for bit."""
+    wl = synthetic.make_workload(name)
+    dw = DeviceWorkload(wl, append=False)
+    # prefix only: the drafts' slots keep the NaN sentinel until the fused call
+    fp8 = wl.kv_dtype == synthetic.FP8
+    raw = np.uint8 if fp8 else np.int16
+    pre = np.concatenate([np.arange(wl.tok_indptr[b], wl.tok_indptr[b + 1] - wl.qo_lens[b])
+                          for b in range(wl.batch)])
+    pre_indptr = np.concatenate([[0], np.cumsum(wl.prefix_lens)]).astype(np.int32)
+    # appending the prefix alone: a table whose kv_len is the prefix length
+    pages = (wl.prefix_lens + wl.page_size - 1) // wl.page_size
+    kvp = np.zeros(wl.batch + 1, np.int32)
+    idx = []
+    for b in range(wl.batch):
+        kvp[b + 1] = kvp[b] + pages[b]
+        idx.append(wl.kv_indices[wl.kv_indptr[b]:wl.kv_indptr[b] + pages[b]])
+    lpl = np.array([int(n) - (int(p) - 1) * wl.page_size if p > 0 else 0
+                    for n, p in zip(wl.prefix_lens, pages)], np.int32)
+    va.paged_kv_append(to_dev(wl.k_tok[pre].view(raw), "cuda", dw.kvd),
+                       to_dev(wl.v_tok[pre].view(raw), "cuda", dw.kvd), to_dev(pre_indptr, "cuda"),
+                       to_dev(kvp, "cuda"), to_dev(np.concatenate(idx).astype(np.int32), "cuda"),
+                       to_dev(lpl, "cuda"), dw.k_cache, dw.v_cache)
+    plan = dw.plan()
+    out, lse = _fused(va, dw, plan)
+    torch.cuda.synchronize()
+    assert va.verify_attn_device_status(plan) == 0
+    kc, vc = oracle.build_cache(wl)
+    assert np.array_equal(_raw(dw.k_cache, fp8), kc) and np.array_equal(_raw(dw.v_cache, fp8), vc)
+    compare(wl, out, lse, caches=(kc, vc), strict=True)
+
+
+@pytest.mark.parametrize("case", [
+    dict(mask="tree", rope_theta=10000.0),
+    dict(mask="causal", kv_layout="nhd"),
+    dict(mask="tree", kv_dtype=synthetic.FP8),
+], ids=["rope_tree", "nhd_chain", "fp8_tree"])
+def test_append_run_features_match_oracle(va, case):
+    wl = synthetic.make_custom(batch=3, h_q=32, h_kv=8, d=128, prefix=("fixed", [1500, 0, 300]),
+                               qo=("fixed", [17, 40, 6]), seed=101, **case)
+    dw = DeviceWorkload(wl)   # drafts already in place: the fused call rewrites the same bits
+    plan = dw.plan()
+    out, lse = _fused(va, dw, plan)
+    torch.cuda.synchronize()
+    assert va.verify_attn_device_status(plan) == 0
+    compare(wl, out, lse)
+
+
+def test_append_run_quantises_fresh_drafts(va):
+    """The wide fp8 tree in small through the fused call: bf16 drafts are
+    quantised into the fp8 cache and attended in the same call."""
+    base = dict(batch=2, h_q=32, h_kv=8, d=128, prefix=("fixed", [1000, 300]),
+                qo=("fixed", [64, 20]), mask="tree", seed=91)
+    wf = synthetic.make_custom(kv_dtype=synthetic.FP8, **base)
+    wb = synthetic.make_custom(**base)
+    kn, vn = wb.new_tokens()
+    kc, vc = oracle.build_cache(wf)
+    oracle.paged_kv_append_quant(kn, vn, wf.k_scale, wf.v_scale, wf.qo_indptr, wf.kv_indptr,
+                                 wf.kv_indices, wf.last_page_len, wf.page_size, wf.num_pages,
+                                 kc, vc)
+    dw = DeviceWorkload(wf)
+    plan = dw.plan()
+    out, lse = va.verify_attn_append_run(
+        to_dev(kn.view(np.int16), "cuda", torch.bfloat16),
+        to_dev(vn.view(np.int16), "cuda", torch.bfloat16), dw.q, dw.k_cache, dw.v_cache,
+        dw.kv_indptr, dw.kv_indices, dw.last_page_len, dw.qo_indptr, dw.mask, dw.mask_indptr,
+        plan, sm_scale=wf.sm_scale, k_scale=wf.k_scale, v_scale=wf.v_scale,
+        append_k_scale=wf.k_scale, append_v_scale=wf.v_scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(_raw(dw.k_cache, True), kc) and np.array_equal(_raw(dw.v_cache, True), vc)
+    compare(wf, out, lse, caches=(kc, vc))
+
+
+def test_append_run_graph_replays_back_to_back(va):
+    """The fused call captured in a CUDA graph, replayed many times back to
+    back on the same buffers (each replay's append overwrites the drafts the
+    previous replay's attention read), then checked: the early reads of q,
+    the tables and the prefix must never see a half-written step."""
+    wl = synthetic.make_workload("llama3_8b_tree_verify")
+    dw = DeviceWorkload(wl)
+    plan = dw.plan()
+    out = torch.empty_like(dw.q)
+    lse = torch.empty(dw.q.shape[:2], dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _fused(va, dw, plan, out=out, lse=lse)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(8):
+            _fused(va, dw, plan, out=out, lse=lse)
+    out.zero_()
+    for _ in range(20):
+        g.replay()
+    torch.cuda.synchronize()
+    assert va.verify_attn_device_status(plan) == 0
+    compare(wl, out, lse, strict=True)
