@@ -254,7 +254,16 @@ typedef struct {
                                   must be NULL otherwise */
     float rope_theta;          /* RoPE base (> 0, finite) when q_position is given */
     float rope_scale;          /* linear position scaling (> 0, finite); 0 means 1 */
-    int reserved[4];           /* must be zero */
+    int early_reads;           /* 1: q, the index tables, the mask and q_position are complete
+                                  before the kernel preceding this call in the stream starts
+                                  (host copies, or kernels launched before it), and that kernel
+                                  writes none of them nor a prefix slot of the cache; the
+                                  library's kernels may then read them, and the prefix slots,
+                                  while it still runs (programmatic dependent launch).  0: no
+                                  kernel reads anything before its predecessor has completed
+                                  (verify_attn_append_run's attention still overlaps its own
+                                  append). */
+    int reserved[3];           /* must be zero */
 } va_run_options_t;
 
 /*
@@ -397,9 +406,10 @@ int paged_kv_append_ex(const void* k_new, const void* v_new, const int32_t* appe
  * Ordering: the append waits for the kernel before it in the stream to
  * complete and then releases the attention kernels at once, so they read q,
  * the tables and the cache's prefix slots while the append still runs and
- * wait for it only before reading a draft's slot (verify_attn_run on its own
- * reads nothing before its predecessor has completed).  k_cache / v_cache
- * are written, so they are not const here.
+ * wait for it only before reading a draft's slot.  With run_options->
+ * early_reads the append releases them at its start and reads its tables
+ * before its own wait as well (see va_run_options_t for what the caller
+ * then guarantees).  k_cache / v_cache are written, so they are not const.
  */
 int verify_attn_append_run(const void* k_new, const void* v_new,
                            const va_append_options_t* append_options, const void* q, void* k_cache,

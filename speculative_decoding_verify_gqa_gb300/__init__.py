@@ -67,7 +67,8 @@ class PlanOptions(ctypes.Structure):
 
 class RunOptions(ctypes.Structure):
     _fields_ = [("q_position", ctypes.c_void_p), ("rope_theta", ctypes.c_float),
-                ("rope_scale", ctypes.c_float), ("reserved", ctypes.c_int * 4)]
+                ("rope_scale", ctypes.c_float), ("early_reads", ctypes.c_int),
+                ("reserved", ctypes.c_int * 3)]
 
 
 class AppendOptions(ctypes.Structure):
@@ -361,27 +362,33 @@ def _alloc_out(q, plan, out, lse, want_lse):
     return out, lse
 
 
-def _run_options(q_position, rope_theta, rope_scale):
-    if q_position is None:
+def _run_options(q_position, rope_theta, rope_scale, early_reads=False):
+    if q_position is None and not early_reads:
         return None
     o = RunOptions()
-    o.q_position = _dp(q_position)
-    o.rope_theta = float(rope_theta)
-    o.rope_scale = float(rope_scale)
+    if q_position is not None:
+        o.q_position = _dp(q_position)
+        o.rope_theta = float(rope_theta)
+        o.rope_scale = float(rope_scale)
+    o.early_reads = int(bool(early_reads))
     return o
 
 
 def verify_attn_run(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr,
                     mask, mask_indptr, plan: Plan, sm_scale=0.0, k_scale=1.0, v_scale=1.0,
                     out=None, lse=None, want_lse=True, num_pages=None, stream=None,
-                    q_position=None, rope_theta=10000.0, rope_scale=1.0):
+                    q_position=None, rope_theta=10000.0, rope_scale=1.0, early_reads=False):
     """out = softmax(q k^T * sm_scale * k_scale + mask) v * v_scale, and its LSE.
     q_position (int32 device tensor [total_qo]) rotates the queries by RoPE
-    at those positions; the plan must have been made with rope=True."""
+    at those positions; the plan must have been made with rope=True.
+    early_reads: the caller promises that q, the tables, the mask and the
+    positions were complete before the preceding kernel in the stream
+    started, and that it writes none of them nor a prefix slot (see
+    va_run_options_t)."""
     out, lse = _alloc_out(q, plan, out, lse, want_lse)
     args = _run_args(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
                      mask_indptr, plan, sm_scale, k_scale, v_scale, out, lse, num_pages)
-    ro = _run_options(q_position, rope_theta, rope_scale)
+    ro = _run_options(q_position, rope_theta, rope_scale, early_reads)
     if ro is None:
         _check("verify_attn_run", lib().verify_attn_run(*args, _stream(stream)))
     else:
@@ -393,11 +400,11 @@ def verify_attn_run(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, q
 def verify_attn_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr,
                         mask, mask_indptr, plan: Plan, sm_scale=0.0, k_scale=1.0, v_scale=1.0,
                         out=None, lse=None, want_lse=True, num_pages=None, stream=None,
-                        q_position=None, rope_theta=10000.0, rope_scale=1.0):
+                        q_position=None, rope_theta=10000.0, rope_scale=1.0, early_reads=False):
     out, lse = _alloc_out(q, plan, out, lse, want_lse)
     args = _run_args(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
                      mask_indptr, plan, sm_scale, k_scale, v_scale, out, lse, num_pages)
-    ro = _run_options(q_position, rope_theta, rope_scale)
+    ro = _run_options(q_position, rope_theta, rope_scale, early_reads)
     if ro is None:
         _check("verify_attn_partial", lib().verify_attn_partial(*args, _stream(stream)))
     else:
@@ -474,11 +481,12 @@ def verify_attn_append_run(k_new, v_new, q, k_cache, v_cache, kv_indptr, kv_indi
                            k_scale=1.0, v_scale=1.0, out=None, lse=None, want_lse=True,
                            num_pages=None, stream=None, q_position=None, rope_theta=10000.0,
                            rope_scale=1.0, append_k_scale=None, append_v_scale=None,
-                           positions=None, kv_layout="hnd"):
+                           positions=None, kv_layout="hnd", early_reads=False):
     """One verification step: append the drafts' K/V (k_new / v_new, one row
     per query token in qo_indptr order; bf16 into an fp8 cache quantises with
     append_k_scale / append_v_scale; positions rotates the new keys by RoPE),
-    then verify attention over the cache just written.  Returns (out, lse)."""
+    then verify attention over the cache just written.  Returns (out, lse).
+    early_reads as for verify_attn_run."""
     out, lse = _alloc_out(q, plan, out, lse, want_lse)
     if num_pages is None:
         num_pages = k_cache.shape[0]
@@ -495,7 +503,7 @@ def verify_attn_append_run(k_new, v_new, q, k_cache, v_cache, kv_indptr, kv_indi
         ao.positions = _dp(positions) if positions is not None else None
         ao.rope_theta = float(rope_theta) if positions is not None else 0.0
         ao.rope_scale = float(rope_scale) if positions is not None else 0.0
-    ro = _run_options(q_position, rope_theta, rope_scale)
+    ro = _run_options(q_position, rope_theta, rope_scale, early_reads)
     if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
         raise ValueError("q and out must be bfloat16")
     rc = lib().verify_attn_append_run(

@@ -144,12 +144,15 @@ __device__ __forceinline__ void load_f32(const uint8_t* row, int bf16_src, int e
 }
 
 __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams p) {
-  // Launched with programmatic serialization: nothing is read before the
-  // kernel before this one (which may produce the new rows, q or the tables)
-  // has completed.  The attention kernel after this one is released right
+  // Launched with programmatic serialization: nothing the kernel before this
+  // one may produce (the new rows, q, the tables) is read before it has
+  // completed, and the attention kernel after this one is released right
   // then: it may read q and the prefix pages at once, and waits for our
-  // completion before it reads a draft's slot.
-  grid_dependency_wait();
+  // completion before it reads a draft's slot.  When the caller promises
+  // that q and the tables were complete before that kernel started (early),
+  // the next kernel is released at once and the tables are read before the
+  // wait; the new rows are still read, and the slots written, after it.
+  if (!p.early) grid_dependency_wait();
   grid_dependents_launch();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long per_tok = (long long)p.h_kv * p.row_chunks;
@@ -174,6 +177,7 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
   const bool pos_ok = !(i < a0 || i - a0 >= n || pos < 0 || (npg > 0 && (lpl < 1 || lpl > p.page_size)) ||
                         (pos >> p.log2_page) >= npg);
   const int page = pos_ok ? __ldg(p.kv_indices + pg0 + (int)(pos >> p.log2_page)) : -1;
+  if (p.early) grid_dependency_wait();
   if (!pos_ok) {
     if (p.status) atomicOr(p.status, VA_DEV_BAD_APPEND);
     return;

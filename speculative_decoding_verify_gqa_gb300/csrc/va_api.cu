@@ -410,7 +410,7 @@ int verify_attn_partial_ex(const void* q, const void* k_cache, const void* v_cac
   return run_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
                      mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale,
                      k_scale, v_scale, out, lse, num_pages, plan_h, workspace_d, workspace_bytes,
-                     options, 0, stream);
+                     options, options && options->early_reads ? 1 : 0, stream);
 }
 
 int verify_attn_partial(const void* q, const void* k_cache, const void* v_cache,
@@ -448,8 +448,9 @@ int verify_attn_run_ex(const void* q, const void* k_cache, const void* v_cache,
                                   num_pages, plan_h, workspace_d, workspace_bytes, options,
                                   stream);
   if (rc) return rc;
-  return verify_attn_merge(qo_indptr, num_qo_heads, num_kv_heads, head_dim, out, lse, plan_h,
-                           workspace_d, workspace_bytes, stream);
+  return verify_attn_merge_impl(qo_indptr, num_qo_heads, num_kv_heads, head_dim, out, lse, plan_h,
+                                workspace_d, workspace_bytes,
+                                options && options->early_reads ? 1 : 0, stream);
 }
 
 int verify_attn_run(const void* q, const void* k_cache, const void* v_cache,
@@ -574,12 +575,12 @@ int verify_attn_device_status(void* workspace_d, int* bits, void* stream) {
   return v ? VA_ERR_DEVICE_CHECK : VA_OK;
 }
 
-int paged_kv_append_ex(const void* k_new, const void* v_new, const int32_t* append_indptr,
+static int append_impl(const void* k_new, const void* v_new, const int32_t* append_indptr,
                        const int32_t* kv_indptr, const int32_t* kv_indices,
                        const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
                        int num_kv_heads, int head_dim, int page_size, int num_pages,
                        va_dtype kv_dtype, int64_t total_new, const va_append_options_t* options,
-                       int* status_d, void* stream) {
+                       int* status_d, int early, void* stream) {
   va_append_options_t o;
   memset(&o, 0, sizeof(o));
   if (options) o = *options;
@@ -630,9 +631,21 @@ int paged_kv_append_ex(const void* k_new, const void* v_new, const int32_t* appe
   p.k_scale = o.k_scale;
   p.v_scale = o.v_scale;
   p.total_new = total_new;
+  p.early = early;
   if (o.positions) rope_frequencies(o.rope_theta, rope_scale, head_dim, &p.rope);
   cudaError_t e = launch_append(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
+int paged_kv_append_ex(const void* k_new, const void* v_new, const int32_t* append_indptr,
+                       const int32_t* kv_indptr, const int32_t* kv_indices,
+                       const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
+                       int num_kv_heads, int head_dim, int page_size, int num_pages,
+                       va_dtype kv_dtype, int64_t total_new, const va_append_options_t* options,
+                       int* status_d, void* stream) {
+  return append_impl(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_page_len, k_cache,
+                     v_cache, batch, num_kv_heads, head_dim, page_size, num_pages, kv_dtype,
+                     total_new, options, status_d, 0, stream);
 }
 
 int verify_attn_append_run(const void* k_new, const void* v_new,
@@ -652,13 +665,14 @@ int verify_attn_append_run(const void* k_new, const void* v_new,
                      v_scale, out, lse, num_pages, plan_h, workspace_d, workspace_bytes,
                      run_options, &hd);
   if (rc) return rc;
+  const int early = run_options && run_options->early_reads ? 1 : 0;
   const int layout = append_options ? (int)append_options->kv_layout : VA_LAYOUT_HND;
   if (layout != ((hd->flags & kPlanNhd) ? VA_LAYOUT_NHD : VA_LAYOUT_HND)) return VA_ERR_PLAN_MISMATCH;
   if (hd->total_qo > 0) {
     int* status = reinterpret_cast<int*>(static_cast<char*>(workspace_d) + hd->off_status);
-    rc = paged_kv_append_ex(k_new, v_new, qo_indptr, kv_indptr, kv_indices, last_page_len, k_cache,
-                            v_cache, hd->batch, num_kv_heads, head_dim, page_size, num_pages,
-                            (va_dtype)hd->kv_dtype, hd->total_qo, append_options, status, stream);
+    rc = append_impl(k_new, v_new, qo_indptr, kv_indptr, kv_indices, last_page_len, k_cache,
+                     v_cache, hd->batch, num_kv_heads, head_dim, page_size, num_pages,
+                     (va_dtype)hd->kv_dtype, hd->total_qo, append_options, status, early, stream);
     if (rc) return rc;
   }
   rc = run_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
@@ -675,9 +689,9 @@ int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_
                     const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,
                     int num_kv_heads, int head_dim, int page_size, int num_pages,
                     va_dtype kv_dtype, int64_t total_new, int* status_d, void* stream) {
-  return paged_kv_append_ex(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_page_len,
-                            k_cache, v_cache, batch, num_kv_heads, head_dim, page_size,
-                            num_pages, kv_dtype, total_new, nullptr, status_d, stream);
+  return append_impl(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_page_len, k_cache,
+                     v_cache, batch, num_kv_heads, head_dim, page_size, num_pages, kv_dtype,
+                     total_new, nullptr, status_d, 0, stream);
 }
 
 }  // extern "C"

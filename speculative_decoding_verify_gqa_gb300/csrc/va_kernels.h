@@ -45,8 +45,8 @@ struct PartialParams {
   int nhd;                    // cache layout [pages, P, h_kv, d]
   const int32_t* q_position;  // nullable: RoPE position of each query token
   int early_inputs;           // 1: q, the tables and the prefix pages may be read before the
-                              // wait for the previous grid (it is this library's append,
-                              // which releases this kernel only once q's producer is done)
+                              // wait for the previous grid (this library's append, released
+                              // once q's producer is done, or a caller's early-reads promise)
   RopeFreq rope;              // frequencies when q_position is set
 };
 
@@ -78,6 +78,8 @@ struct AppendParams {
   int cache_fp8;              // cache dtype e4m3 (else bf16)
   int quant;                  // bf16 source rows into an e4m3 cache
   int nhd;                    // cache layout [pages, P, h_kv, d] (else [pages, h_kv, P, d])
+  int early;                  // 1: release the next kernel at once and read the tables before
+                              // the wait (they do not depend on the previous kernel)
   float k_scale, v_scale;     // quantising append: stored = e4m3(x / scale)
   int64_t total_new;
   RopeFreq rope;

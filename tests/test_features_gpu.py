@@ -332,7 +332,8 @@ def test_append_run_quantises_fresh_drafts(va):
     compare(wf, out, lse, caches=(kc, vc))
 
 
-def test_append_run_graph_replays_back_to_back(va):
+@pytest.mark.parametrize("early_reads", [False, True])
+def test_append_run_graph_replays_back_to_back(va, early_reads):
     """The fused call captured in a CUDA graph, replayed many times back to
     back on the same buffers (each replay's append overwrites the drafts the
     previous replay's attention read), then checked: the early reads of q,
@@ -345,15 +346,58 @@ def test_append_run_graph_replays_back_to_back(va):
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        _fused(va, dw, plan, out=out, lse=lse)
+        _fused(va, dw, plan, out=out, lse=lse, early_reads=early_reads)
     torch.cuda.current_stream().wait_stream(s)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         for _ in range(8):
-            _fused(va, dw, plan, out=out, lse=lse)
+            _fused(va, dw, plan, out=out, lse=lse, early_reads=early_reads)
     out.zero_()
     for _ in range(20):
         g.replay()
     torch.cuda.synchronize()
     assert va.verify_attn_device_status(plan) == 0
     compare(wl, out, lse, strict=True)
+
+
+@pytest.mark.parametrize("early_reads", [False, True])
+def test_layers_sharing_one_workspace(va, early_reads):
+    """Four "layers" run back to back in one graph, each with its own q and
+    output but one plan and one workspace: a layer's split kernel must not
+    overwrite the split partials before the previous layer's merge has read
+    them, even when it reads its inputs early."""
+    wl = synthetic.make_workload("llama3_8b_tree_verify")
+    dw = DeviceWorkload(wl)
+    plan = dw.plan()
+    assert plan.header()["n_merge"] > 0
+    gen = torch.Generator(device="cpu").manual_seed(7)
+    qs = [(torch.randn(dw.q.shape, generator=gen) * (1 + i)).to(torch.bfloat16).cuda()
+          for i in range(4)]
+    outs = [torch.empty_like(dw.q) for _ in qs]
+    lses = [torch.empty(dw.q.shape[:2], dtype=torch.float32, device="cuda") for _ in qs]
+
+    def layers():
+        for q, o, l in zip(qs, outs, lses):
+            va.verify_attn_run(q, dw.k_cache, dw.v_cache, dw.kv_indptr, dw.kv_indices,
+                               dw.last_page_len, dw.qo_indptr, dw.mask, dw.mask_indptr, plan,
+                               sm_scale=wl.sm_scale, out=o, lse=l, early_reads=early_reads)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layers()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layers()
+    for o in outs:
+        o.zero_()
+    for _ in range(5):
+        g.replay()
+    torch.cuda.synchronize()
+    assert va.verify_attn_device_status(plan) == 0
+    kc, vc = oracle.build_cache(wl)
+    for q, o, l in zip(qs, outs, lses):
+        wq = synthetic.make_workload("llama3_8b_tree_verify")
+        wq.q = q.cpu().view(torch.int16).numpy().view(np.uint16)
+        compare(wq, o, l, caches=(kc, vc), strict=True)
