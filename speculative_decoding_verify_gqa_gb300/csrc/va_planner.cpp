@@ -286,9 +286,25 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   std::vector<Tmp> items;
   std::vector<MergeItem> merges;
   int64_t part_rows = 0;
+  std::vector<int64_t> cuts;
   for (const Unit& u : units) {
     int64_t cu;
-    const int64_t n = split_of(u, chunk, equal, &cu);
+    int64_t n = split_of(u, chunk, equal, &cu);
+    // Chunk boundaries.  The warp-level kernel cuts on its 64-key tile from
+    // the front.  The tcgen05 kernels take chunks on any 16-key boundary:
+    // the range is cut into n near-equal parts whose starts are rounded up
+    // to 16 keys, so the last part ends at the range's end with at most one
+    // short tile and every part holds about kv_end / n keys -- a request's
+    // drafts then share their part with a full tile of prefix keys, which
+    // a CTA can stream before the drafts are appended.
+    cuts.assign(1, 0);
+    for (int64_t s = 1; s < n; ++s) {
+      const int64_t c = kernel_is_tc(kernel) ? (ceil_div(s * (int64_t)u.kv_end, n) + 15) / 16 * 16
+                                             : s * cu;
+      if (c > cuts.back() && c < u.kv_end) cuts.push_back(c);
+    }
+    cuts.push_back(u.kv_end);
+    n = (int64_t)cuts.size() - 1;
     for (int h = 0; h < num_kv_heads; ++h) {
       int64_t base = part_rows;
       if (n > 1) {
@@ -296,7 +312,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
         part_rows += n * u.nrows;
       }
       for (int64_t s = 0; s < n; ++s) {
-        int64_t lo = s * cu, hi = std::min<int64_t>(lo + cu, u.kv_end);
+        int64_t lo = cuts[s], hi = cuts[s + 1];
         WorkItem w{u.b, h, u.row0, u.nrows, (int32_t)lo, (int32_t)hi,
                    n > 1 ? (int32_t)(base + s * u.nrows) : -1, -1};
         items.push_back({w, (hi - lo) * (int64_t)(u.nrows + 16)});
