@@ -321,9 +321,9 @@ class Bench:
     def kernel_times(self, n=64):
         """Average duration (ms) of each kernel of the step: CUDA events
         around a captured graph of n back-to-back launches of that kernel
-        alone (its own calls: verify_attn_partial, verify_attn_merge,
-        paged_kv_append), divided by n, on pool copies rotated as in the
-        step; median of 5 replays."""
+        alone (its own calls: verify_attn_partial with the step's
+        early-reads mode, verify_attn_merge, paged_kv_append), divided by n,
+        on pool copies rotated as in the step; median of 5 replays."""
         torch, va, wl = self.torch, self.va, self.wl
 
         def one(kind, i):
@@ -336,7 +336,7 @@ class Bench:
                                        self.last_page_len, self.qo_indptr, self.mask,
                                        self.mask_indptr, self.plan, sm_scale=wl.sm_scale,
                                        k_scale=wl.k_scale, v_scale=wl.v_scale, out=self.out,
-                                       lse=self.lse)
+                                       lse=self.lse, early_reads=self.early_reads)
             else:
                 va.verify_attn_merge(self.qo_indptr, self.plan, self.out, self.lse)
 

@@ -254,15 +254,17 @@ typedef struct {
                                   must be NULL otherwise */
     float rope_theta;          /* RoPE base (> 0, finite) when q_position is given */
     float rope_scale;          /* linear position scaling (> 0, finite); 0 means 1 */
-    int early_reads;           /* 1: q, the index tables, the mask and q_position are complete
-                                  before the kernel preceding this call in the stream starts
-                                  (host copies, or kernels launched before it), and that kernel
-                                  writes none of them nor a prefix slot of the cache; the
-                                  library's kernels may then read them, and the prefix slots,
-                                  while it still runs (programmatic dependent launch).  0: no
-                                  kernel reads anything before its predecessor has completed
-                                  (verify_attn_append_run's attention still overlaps its own
-                                  append). */
+    int early_reads;           /* 1: the call's inputs -- q, the index tables, the mask,
+                                  q_position, and for verify_attn_append_run k_new / v_new and
+                                  the append positions -- are complete before the kernel
+                                  preceding this call in the stream starts (host copies, or
+                                  kernels launched before it), and that kernel writes none of
+                                  them nor a prefix slot of the cache; the library's kernels may
+                                  then read them, and the prefix slots, while it still runs
+                                  (programmatic dependent launch).  Writes still wait for it.
+                                  0: no kernel reads anything before its predecessor has
+                                  completed (verify_attn_append_run's attention still overlaps
+                                  its own append). */
     int reserved[3];           /* must be zero */
 } va_run_options_t;
 

@@ -149,9 +149,10 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
   // completed, and the attention kernel after this one is released right
   // then: it may read q and the prefix pages at once, and waits for our
   // completion before it reads a draft's slot.  When the caller promises
-  // that q and the tables were complete before that kernel started (early),
-  // the next kernel is released at once and the tables are read before the
-  // wait; the new rows are still read, and the slots written, after it.
+  // that the step's inputs (q, the new rows, the tables) were complete
+  // before that kernel started (early), the next kernel is released at once
+  // and the tables and new rows are read before the wait; the slots are
+  // still written after it.
   if (!p.early) grid_dependency_wait();
   grid_dependents_launch();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -177,13 +178,9 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
   const bool pos_ok = !(i < a0 || i - a0 >= n || pos < 0 || (npg > 0 && (lpl < 1 || lpl > p.page_size)) ||
                         (pos >> p.log2_page) >= npg);
   const int page = pos_ok ? __ldg(p.kv_indices + pg0 + (int)(pos >> p.log2_page)) : -1;
-  if (p.early) grid_dependency_wait();
-  if (!pos_ok) {
-    if (p.status) atomicOr(p.status, VA_DEV_BAD_APPEND);
-    return;
-  }
-  if ((unsigned)page >= (unsigned)p.num_pages) {
-    if (p.status) atomicOr(p.status, VA_DEV_BAD_PAGE);
+  if (!pos_ok || (unsigned)page >= (unsigned)p.num_pages) {
+    if (p.early) grid_dependency_wait();
+    if (p.status) atomicOr(p.status, pos_ok ? VA_DEV_BAD_PAGE : VA_DEV_BAD_APPEND);
     return;
   }
   const size_t row_bytes = (size_t)p.row_chunks * 16;
@@ -199,8 +196,11 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
   const uint8_t* ks = static_cast<const uint8_t*>(p.k_new) + src_row;
   const uint8_t* vs = static_cast<const uint8_t*>(p.v_new) + src_row;
   if (!p.quant && !p.positions) {  // a bit-exact copy
-    *reinterpret_cast<uint4*>(kd) = *reinterpret_cast<const uint4*>(ks + (size_t)ch * 16);
-    *reinterpret_cast<uint4*>(vd) = *reinterpret_cast<const uint4*>(vs + (size_t)ch * 16);
+    const uint4 kq = *reinterpret_cast<const uint4*>(ks + (size_t)ch * 16);
+    const uint4 vq = *reinterpret_cast<const uint4*>(vs + (size_t)ch * 16);
+    if (p.early) grid_dependency_wait();   // the slots may still be read before it
+    *reinterpret_cast<uint4*>(kd) = kq;
+    *reinterpret_cast<uint4*>(vd) = vq;
     return;
   }
   // elements e0 .. e0 + E - 1 of the row: 8 for a bf16 cache, 16 for fp8
@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
       xk[e] = fmaf(xk[e], c, sgn * yk[e] * s);
     }
   }
+  if (p.early) grid_dependency_wait();   // the slots may still be read before it
   if (!p.cache_fp8) {
     uint4 wk, wv;
     wk.x = pack_bf16x2(xk[0], xk[1]); wk.y = pack_bf16x2(xk[2], xk[3]);

@@ -736,6 +736,25 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       const int t = (g.row0 + br) / G;              // draft token of the row
       const int moff = g.moff;
       const int L = g.L, prefix = g.prefix, hi = g.hi;
+      // A draft-block mask row of at most 64 bits is fetched once, here, so
+      // its loads overlap the item's prefix tiles instead of stalling the
+      // tile that holds the drafts.
+      const bool row_bits_pre = p.mask && !p.mask_full && L <= 64 && hi > prefix;
+      uint64_t row_bits = 0;
+      if (row_bits_pre && t < L) {
+        const long long bit0 = (long long)moff + (long long)t * L;
+        const int sh = (int)(bit0 & 7);
+        const int nbytes = (sh + L + 7) >> 3;        // <= 9
+        uint64_t w = 0;
+        uint32_t top = 0;
+        for (int k = 0; k < nbytes; ++k) {
+          const uint32_t byte = __ldg(p.mask + (bit0 >> 3) + k);
+          if (k < 8) w |= (uint64_t)byte << (8 * k);
+          else top = byte;
+        }
+        row_bits = (w >> sh) | (sh ? (uint64_t)top << (64 - sh) : 0ull);
+        if (L < 64) row_bits &= (1ull << L) - 1ull;
+      }
       float m_used = -INFINITY;                     // in units of s * c (log2 domain)
       float l = 0.f;
       for (int j = 0; live && j < g.n_tiles; ++j) {
@@ -821,10 +840,14 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
                 const int nbits = min(32 - below_prefix, L - d0);
                 if (nbits > 0) {
                   uint64_t w = 0;
-                  const int nbytes = (int)((((bit0 & 7) + nbits) + 7) >> 3);
-                  for (int k = 0; k < nbytes; ++k)
-                    w |= (uint64_t)__ldg(p.mask + (bit0 >> 3) + k) << (8 * k);
-                  w >>= (bit0 & 7);
+                  if (row_bits_pre) {
+                    w = row_bits >> d0;
+                  } else {
+                    const int nbytes = (int)((((bit0 & 7) + nbits) + 7) >> 3);
+                    for (int k = 0; k < nbytes; ++k)
+                      w |= (uint64_t)__ldg(p.mask + (bit0 >> 3) + k) << (8 * k);
+                    w >>= (bit0 & 7);
+                  }
                   const uint32_t dbits =
                       (uint32_t)(w & (nbits >= 32 ? 0xffffffffull : ((1ull << nbits) - 1ull)));
                   w32 |= dbits << below_prefix;

@@ -290,19 +290,16 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   for (const Unit& u : units) {
     int64_t cu;
     int64_t n = split_of(u, chunk, equal, &cu);
-    // Chunk boundaries.  The warp-level kernel cuts on its 64-key tile from
-    // the front.  The tcgen05 kernels take chunks on any 16-key boundary:
-    // the range is cut into n near-equal parts whose starts are rounded up
-    // to 16 keys, so the last part ends at the range's end with at most one
-    // short tile and every part holds about kv_end / n keys -- a request's
-    // drafts then share their part with a full tile of prefix keys, which
-    // a CTA can stream before the drafts are appended.
+    // Chunk boundaries: multiples of the chunk size from the front.  For
+    // the tcgen05 kernels a last chunk shorter than one key tile joins the
+    // one before it: the tail of a request (its drafts, appended in the same
+    // step) then shares a CTA with full prefix tiles that stream in before
+    // the append is done, instead of a CTA of its own that would start cold
+    // after it (a 17-key chunk of drafts alone was the tree verify's
+    // critical path).
     cuts.assign(1, 0);
-    for (int64_t s = 1; s < n; ++s) {
-      const int64_t c = kernel_is_tc(kernel) ? (ceil_div(s * (int64_t)u.kv_end, n) + 15) / 16 * 16
-                                             : s * cu;
-      if (c > cuts.back() && c < u.kv_end) cuts.push_back(c);
-    }
+    for (int64_t s = 1; s < n; ++s) cuts.push_back(s * cu);
+    if (kernel_is_tc(kernel) && n > 1 && u.kv_end - cuts.back() < TK) cuts.pop_back();
     cuts.push_back(u.kv_end);
     n = (int64_t)cuts.size() - 1;
     for (int h = 0; h < num_kv_heads; ++h) {

@@ -83,8 +83,7 @@ def _check_cover(va, t, plan):
         b, h, row0, nrows, lo, hi, part_row, _ = (int(x) for x in it)
         assert 0 <= b < len(t["L"]) and 0 <= h < t["h_kv"]
         assert 0 < nrows <= BM and row0 % BM == 0
-        # chunks start on the variant's boundary: 16 keys (tcgen05) or 64
-        assert lo % (16 if hd["kernel"] in (3, 4) else 64) == 0 and lo < hi
+        assert lo % 64 == 0 and lo < hi
         units.setdefault((b, h, row0, nrows), []).append((lo, hi, part_row))
     for b in range(len(t["L"])):
         R = G * int(t["L"][b])
