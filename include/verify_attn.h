@@ -103,7 +103,7 @@ extern "C" {
 
 /* Element types (FlashInfer PR #286: the query dtype and the KV-cache dtype
  * are separate arguments of begin_forward; the cache may be fp8). */
-typedef enum { VA_BF16 = 0, VA_FP8_E4M3 = 1 } va_dtype;
+typedef enum { VA_BF16 = 0, VA_FP8_E4M3 = 1, VA_F32 = 2 } va_dtype;
 #define VA_DTYPE_BF16 VA_BF16
 #define VA_DTYPE_FP8_E4M3 VA_FP8_E4M3
 
@@ -422,6 +422,39 @@ int verify_attn_append_run(const void* k_new, const void* v_new,
                            float k_scale, float v_scale, void* out, float* lse, int num_pages,
                            const void* plan_h, void* workspace_d, size_t workspace_bytes,
                            const va_run_options_t* run_options, void* stream);
+
+/*
+ * Greedy acceptance of draft trees: the step after verification, on the
+ * target model's logits (FlashInfer issue #152: Medusa / EAGLE trees are
+ * verified against the target model's outputs; its logits come from an LM
+ * head outside this library).
+ *
+ * Request b's nodes are rows qo_indptr[b] .. qo_indptr[b+1] of `logits`
+ * ([total_qo, vocab] rows, row_stride elements apart, bf16 or fp32, not
+ * NaN).  Node 0 of a request is its root (the last accepted token,
+ * parents = -1); every other node i has parents[i] in [0, i) (local
+ * indices) and proposes draft_tokens[i].  The root is accepted; node i is
+ * accepted iff its parent is accepted and the argmax of the parent's row --
+ * the first index among equal maxima -- equals draft_tokens[i].  For each
+ * request: accept_len[b] = the number of nodes on the root path of the
+ * deepest accepted node (the smallest node index among equally deep ones),
+ * that path's local node ids at accepted_nodes[qo_indptr[b] ..], and
+ * bonus_token[b] = the argmax of its last node's row (the token the target
+ * model emits next).  An empty request gives accept_len 0 and bonus -1; a
+ * request whose parents break the rule gives the same and raises
+ * VA_DEV_BAD_TABLE in status_d (nullable).  argmax_out (nullable) receives
+ * every row's argmax.  Device pointers; the workspace (caller-owned, at
+ * least verify_accept_workspace_size bytes, 16-byte aligned) holds per-row
+ * scratch.  Errors: VA_ERR_INVALID_ARGUMENT, VA_ERR_UNSUPPORTED (logits
+ * dtype), VA_ERR_WORKSPACE_TOO_SMALL, VA_ERR_CUDA.
+ */
+int verify_accept_workspace_size(int64_t total_qo, int vocab, int num_sms, size_t* bytes);
+int verify_accept_greedy(const void* logits, va_dtype logits_dtype, int64_t total_qo, int vocab,
+                         int64_t row_stride, const int32_t* qo_indptr, int batch,
+                         const int32_t* draft_tokens, const int32_t* parents,
+                         int32_t* accept_len, int32_t* accepted_nodes, int32_t* bonus_token,
+                         int32_t* argmax_out, int* status_d, int num_sms, void* workspace_d,
+                         size_t workspace_bytes, void* stream);
 
 /*
  * verify_attn_run for callers that cannot allocate device memory.

@@ -33,6 +33,7 @@ __all__ = [
     "verify_attn_partial", "verify_attn_merge", "paged_kv_append",
     "verify_attn_device_status", "verify_attn_plan_bounds", "verify_attn_plan_host",
     "verify_attn_workspace_size", "verify_attn_run_static_scratch", "verify_attn_append_run",
+    "verify_accept_greedy",
     "status_string", "num_sms", "KV_BF16", "KV_FP8_E4M3", "library_path",
 ]
 
@@ -119,6 +120,9 @@ def lib():
                                      P, P, P]),
         "verify_attn_append_run": (i32, [P, P, P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32,
                                          f32, f32, f32, P, P, i32, P, P, sz, P, P]),
+        "verify_accept_workspace_size": (i32, [i64, i32, i32, Psz]),
+        "verify_accept_greedy": (i32, [P, i32, i64, i32, i64, P, i32, P, P, P, P, P, P, P, i32,
+                                       P, sz, P]),
         "verify_attn_merge": (i32, [P, i32, i32, i32, P, P, P, P, sz, P]),
         "verify_attn_plan_launches": (i32, [P, Pi]),
         "verify_attn_plan_upload": (i32, [P, P, sz, P]),
@@ -515,6 +519,43 @@ def verify_attn_append_run(k_new, v_new, q, k_cache, v_cache, kv_indptr, kv_indi
         None if ro is None else ctypes.byref(ro), _stream(stream))
     _check("verify_attn_append_run", rc)
     return out, lse
+
+
+def verify_accept_greedy(logits, qo_indptr, draft_tokens, parents, workspace=None,
+                         want_argmax=False, status=None, stream=None):
+    """Greedy acceptance of draft trees (see include/verify_attn.h):
+    logits [total, vocab] bf16 or fp32 (device), qo_indptr [B+1],
+    draft_tokens / parents [total] int32 (device).  Returns (accept_len [B],
+    accepted_nodes [total], bonus_token [B], argmax [total] or None), all
+    int32 device tensors; request b's path is accepted_nodes[qo_indptr[b] :
+    qo_indptr[b] + accept_len[b]]."""
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [total, vocab] with unit column stride")
+    if logits.dtype == torch.bfloat16:
+        code = 0
+    elif logits.dtype == torch.float32:
+        code = 2
+    else:
+        raise ValueError("logits must be bfloat16 or float32")
+    total, vocab = logits.shape
+    batch = qo_indptr.shape[0] - 1
+    dev = logits.device
+    n = ctypes.c_size_t(0)
+    _check("verify_accept_workspace_size",
+           lib().verify_accept_workspace_size(int(total), int(vocab), 0, ctypes.byref(n)))
+    if workspace is None or workspace.numel() < n.value:
+        workspace = torch.empty(max(n.value, 256), dtype=torch.uint8, device=dev)
+    acc = torch.empty(batch, dtype=torch.int32, device=dev)
+    path = torch.full((max(total, 1),), -1, dtype=torch.int32, device=dev)
+    bonus = torch.empty(batch, dtype=torch.int32, device=dev)
+    am = torch.empty(max(total, 1), dtype=torch.int32, device=dev) if want_argmax else None
+    rc = lib().verify_accept_greedy(_dp(logits), code, int(total), int(vocab),
+                                    int(logits.stride(0)), _dp(qo_indptr), int(batch),
+                                    _dp(draft_tokens), _dp(parents), _dp(acc), _dp(path),
+                                    _dp(bonus), _dp(am), _dp(status), 0, _dp(workspace),
+                                    workspace.numel(), _stream(stream))
+    _check("verify_accept_greedy", rc)
+    return acc, path[:total], bonus, None if am is None else am[:total]
 
 
 STATIC_SCRATCH_BYTES = 32 << 20

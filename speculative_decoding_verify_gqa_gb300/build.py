@@ -14,7 +14,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libverify_attn.so")
 
-SOURCES = ["va_api.cu", "va_planner.cpp", "k_partial_mma.cu", "k_partial_tc.cu", "k_merge_append.cu"]
+SOURCES = ["va_api.cu", "va_planner.cpp", "k_partial_mma.cu", "k_partial_tc.cu", "k_merge_append.cu",
+           "k_accept.cu"]
 HEADERS = ["va_internal.h", "va_kernels.h", "va_device.cuh", "va_tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",

@@ -6,6 +6,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/verify_attn.h"
@@ -682,6 +683,81 @@ int verify_attn_append_run(const void* k_new, const void* v_new,
   if (rc) return rc;
   return verify_attn_merge_impl(qo_indptr, num_qo_heads, num_kv_heads, head_dim, out, lse, plan_h,
                                 workspace_d, workspace_bytes, 1, stream);
+}
+
+// Chunks per logits row for the argmax kernel: about two CTAs per SM over
+// all rows, each chunk at least 4096 elements.
+static void accept_chunks(int64_t total_qo, int vocab, int num_sms, int* chunks, int64_t* elems) {
+  int64_t c = total_qo > 0 ? (2LL * num_sms + total_qo - 1) / total_qo : 1;
+  c = std::max<int64_t>(1, std::min<int64_t>(c, (vocab + 4095) / 4096));
+  c = std::min<int64_t>(c, 64);
+  int64_t e = (vocab + c - 1) / c;
+  e = (e + 7) / 8 * 8;
+  *chunks = (int)((vocab + e - 1) / e);
+  *elems = e;
+}
+
+int verify_accept_workspace_size(int64_t total_qo, int vocab, int num_sms, size_t* bytes) {
+  if (!bytes || total_qo < 0 || vocab <= 0) return VA_ERR_INVALID_ARGUMENT;
+  if (num_sms <= 0) {
+    int rc = query_sms(&num_sms);
+    if (rc) return rc;
+  }
+  int chunks;
+  int64_t elems;
+  accept_chunks(total_qo, vocab, num_sms, &chunks, &elems);
+  size_t ws = align_up((size_t)total_qo * chunks * 8, kWsAlign);
+  ws += 2 * align_up((size_t)total_qo * 4, kWsAlign);
+  *bytes = std::max<size_t>(ws, kWsAlign);
+  return VA_OK;
+}
+
+int verify_accept_greedy(const void* logits, va_dtype logits_dtype, int64_t total_qo, int vocab,
+                         int64_t row_stride, const int32_t* qo_indptr, int batch,
+                         const int32_t* draft_tokens, const int32_t* parents,
+                         int32_t* accept_len, int32_t* accepted_nodes, int32_t* bonus_token,
+                         int32_t* argmax_out, int* status_d, int num_sms, void* workspace_d,
+                         size_t workspace_bytes, void* stream) {
+  if (batch < 0 || total_qo < 0 || vocab <= 0 || row_stride < vocab) return VA_ERR_INVALID_ARGUMENT;
+  if (logits_dtype != VA_BF16 && logits_dtype != VA_F32) return VA_ERR_UNSUPPORTED;
+  if (total_qo > 0x7fffffffLL || total_qo * row_stride > (int64_t)1 << 47) return VA_ERR_UNSUPPORTED;
+  if (batch == 0) return VA_OK;
+  if (!qo_indptr || !accept_len || !bonus_token || (total_qo > 0 && (!logits || !draft_tokens ||
+                                                                      !parents || !accepted_nodes)))
+    return VA_ERR_INVALID_ARGUMENT;
+  if (num_sms <= 0) {
+    int rc = query_sms(&num_sms);
+    if (rc) return rc;
+  }
+  size_t need = 0;
+  int rc = verify_accept_workspace_size(total_qo, vocab, num_sms, &need);
+  if (rc) return rc;
+  if (!workspace_d || workspace_bytes < need) return VA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace_d)) return VA_ERR_INVALID_ARGUMENT;
+  AcceptParams p;
+  memset(&p, 0, sizeof(p));
+  accept_chunks(total_qo, vocab, num_sms, &p.chunks, &p.chunk_elems);
+  char* ws = static_cast<char*>(workspace_d);
+  p.keys = reinterpret_cast<uint64_t*>(ws);
+  ws += align_up((size_t)total_qo * p.chunks * 8, kWsAlign);
+  p.node_am = reinterpret_cast<int32_t*>(ws);
+  ws += align_up((size_t)total_qo * 4, kWsAlign);
+  p.node_state = reinterpret_cast<int32_t*>(ws);
+  p.logits = logits;
+  p.qo_indptr = qo_indptr;
+  p.draft_tokens = draft_tokens;
+  p.parents = parents;
+  p.accept_len = accept_len;
+  p.path = accepted_nodes;
+  p.bonus = bonus_token;
+  p.argmax_out = argmax_out;
+  p.status = status_d;
+  p.row_stride = row_stride;
+  p.total = (int)total_qo;
+  p.vocab = vocab;
+  p.batch = batch;
+  cudaError_t e = launch_accept(p, logits_dtype == VA_BF16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
 }
 
 int paged_kv_append(const void* k_new, const void* v_new, const int32_t* append_indptr,

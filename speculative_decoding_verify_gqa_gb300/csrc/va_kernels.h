@@ -85,6 +85,26 @@ struct AppendParams {
   RopeFreq rope;
 };
 
+// Greedy acceptance (see k_accept.cu).
+struct AcceptParams {
+  const void* logits;         // [total, row_stride] bf16 or fp32
+  const int32_t* qo_indptr;   // [batch + 1] rows of each request
+  const int32_t* draft_tokens;  // [total]
+  const int32_t* parents;     // [total] local parent index, -1 for the root
+  int32_t* accept_len;        // [batch]
+  int32_t* path;              // [total]: request b's accepted path at qo_indptr[b] ..
+  int32_t* bonus;             // [batch]
+  int32_t* argmax_out;        // nullable [total]
+  int* status;                // nullable
+  uint64_t* keys;             // workspace [total, chunks]
+  int32_t* node_am;           // workspace [total]
+  int32_t* node_state;        // workspace [total]
+  int64_t row_stride;         // elements between rows
+  int total, vocab, batch, chunks;
+  int64_t chunk_elems;
+};
+cudaError_t launch_accept(const AcceptParams& p, bool bf16, cudaStream_t stream);
+
 // Launch `func` with void** args; pdl = true lets the grid be scheduled
 // before the previous kernel in the stream finishes (programmatic dependent
 // launch); such kernels call grid_dependency_wait() before touching memory.

@@ -395,3 +395,24 @@ def test_append_validation_without_device(va):
     Q = list(P)
     Q[0] = ctypes.c_void_p(4097)  # misaligned
     assert lib.paged_kv_append(*Q, 1, 2, 128, 16, 10, 0, 5, None, None) == -1
+
+
+def test_accept_validation_without_device(va):
+    lib = va.lib()
+    fake = ctypes.c_void_p(4096)
+    n = ctypes.c_size_t(0)
+    assert lib.verify_accept_workspace_size(17, 128256, 152, ctypes.byref(n)) == 0 and n.value > 0
+    assert lib.verify_accept_workspace_size(17, 0, 152, ctypes.byref(n)) == -1
+    P = [fake] * 3
+    # fp8 logits are not served
+    assert lib.verify_accept_greedy(fake, 1, 4, 100, 100, fake, 1, fake, fake, *P, None, None, 152,
+                                    fake, 1 << 20, None) == -2
+    # row stride below the vocabulary
+    assert lib.verify_accept_greedy(fake, 0, 4, 100, 50, fake, 1, fake, fake, *P, None, None, 152,
+                                    fake, 1 << 20, None) == -1
+    # workspace too small
+    assert lib.verify_accept_greedy(fake, 0, 4, 100, 100, fake, 1, fake, fake, *P, None, None, 152,
+                                    fake, 8, None) == -3
+    # nothing to do
+    assert lib.verify_accept_greedy(fake, 0, 0, 100, 100, fake, 0, fake, fake, *P, None, None, 152,
+                                    fake, 8, None) == 0
