@@ -549,7 +549,10 @@ def verify_accept_greedy(logits, qo_indptr, draft_tokens, parents, workspace=Non
     path = torch.full((max(total, 1),), -1, dtype=torch.int32, device=dev)
     bonus = torch.empty(batch, dtype=torch.int32, device=dev)
     am = torch.empty(max(total, 1), dtype=torch.int32, device=dev) if want_argmax else None
-    rc = lib().verify_accept_greedy(_dp(logits), code, int(total), int(vocab),
+    if not logits.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    # rows may be padded (row stride > vocab): the row stride is passed explicitly
+    rc = lib().verify_accept_greedy(ctypes.c_void_p(logits.data_ptr()), code, int(total), int(vocab),
                                     int(logits.stride(0)), _dp(qo_indptr), int(batch),
                                     _dp(draft_tokens), _dp(parents), _dp(acc), _dp(path),
                                     _dp(bonus), _dp(am), _dp(status), 0, _dp(workspace),

@@ -37,6 +37,8 @@ def _case(seed, lens, vocab, kind="tree", plant=0.7, ties=False, dtype=torch.bfl
     indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     parents, toks = [], []
     for b, L in enumerate(lens):
+        if L == 0:
+            continue
         o = int(indptr[b])
         par = [-1] + ([i - 1 for i in range(1, L)] if kind == "chain"
                       else [int(rng.integers(0, i)) for i in range(1, L)])
