@@ -91,8 +91,10 @@ def _load():
                                                   i32, i32, P, P]
         lib.oracle_verify_attn_ex.restype = i32
         lib.oracle_verify_attn_ex.argtypes = [P, P, P, i32, i32, P, P, P, P, P, P, i32, P, dbl,
-                                              dbl, i32, i32, i32, i32, i32, i32, dbl, dbl, dbl,
-                                              P, i64, P, P, i32]
+                                              dbl, i32, i32, i32, i32, i32, i32, i32, dbl, dbl,
+                                              dbl, P, i64, P, P, i32]
+        lib.oracle_quantize_q_e4m3.restype = ctypes.c_float
+        lib.oracle_quantize_q_e4m3.argtypes = [P, i32, P]
         _lib = lib
         return lib
 
@@ -166,7 +168,7 @@ def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_le
 def verify_attn_ex(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_len,
                    qo_indptr, mask, mask_indptr, h_q, h_kv, d, page_size, num_pages, sm_scale,
                    k_scale=1.0, v_scale=1.0, kv_layout=0, mask_layout=0, q_pos=None,
-                   rope_theta=0.0, rope_scale=1.0, rows=None, nthreads=None):
+                   rope_theta=0.0, rope_scale=1.0, q_fp8=False, rows=None, nthreads=None):
     """verify_attn with the cache layout (0 HND, 1 NHD), the mask layout (0:
     L x L draft blocks, 1: L x kv_len rows) and optional query positions for
     the rotary embedding of the queries (the cache holds keys as stored)."""
@@ -186,13 +188,24 @@ def verify_attn_ex(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page
     rc = lib.oracle_verify_attn_ex(_p(q), _p(kc), _p(vc), int(bool(kv_fp8)), int(kv_layout),
                                    _p(kv_indptr), _p(kv_indices), _p(last_page_len),
                                    _p(qo_indptr), _p(mask), _p(mask_indptr), int(mask_layout),
-                                   _p(q_pos), float(rope_theta), float(rope_scale), batch, h_q,
+                                   _p(q_pos), float(rope_theta), float(rope_scale), int(bool(q_fp8)),
+                                   batch, h_q,
                                    h_kv, d, page_size, num_pages, float(sm_scale),
                                    float(k_scale), float(v_scale), _p(sel), int(n), _p(out),
                                    _p(lse), int(nthreads or default_threads()))
     if rc != 0:
         raise ValueError("oracle_verify_attn_ex rejected its inputs (status %d)" % rc)
     return out[:n], lse[:n]
+
+
+def quantize_q_e4m3(row):
+    """The e4m3 codes (uint8) and the binary32 scale of one query row (fp64
+    values), as the e4m3 tensor-core path quantises it."""
+    lib = _load()
+    r = np.ascontiguousarray(row, dtype=np.float64)
+    codes = np.zeros(r.shape[0], np.uint8)
+    qsc = lib.oracle_quantize_q_e4m3(_p(r), r.shape[0], _p(codes))
+    return codes, float(qsc)
 
 
 def encode_bf16(x) -> np.ndarray:
@@ -342,9 +355,9 @@ def build_cache(wl):
     return kc, vc
 
 
-def verify_attn_workload(wl, rows=None, nthreads=None, caches=None):
+def verify_attn_workload(wl, rows=None, nthreads=None, caches=None, q_fp8=False):
     kc, vc = caches if caches is not None else build_cache(wl)
-    if not wl.nhd and wl.mask_layout == "qlen" and wl.q_pos is None:
+    if not wl.nhd and wl.mask_layout == "qlen" and wl.q_pos is None and not q_fp8:
         return verify_attn(wl.q, kc, vc, wl.kv_dtype == "fp8_e4m3", wl.kv_indptr, wl.kv_indices,
                            wl.last_page_len, wl.qo_indptr, wl.mask, wl.mask_indptr, wl.h_q,
                            wl.h_kv, wl.d, wl.page_size, wl.num_pages, wl.sm_scale, wl.k_scale,
@@ -354,4 +367,5 @@ def verify_attn_workload(wl, rows=None, nthreads=None, caches=None):
                           wl.h_kv, wl.d, wl.page_size, wl.num_pages, wl.sm_scale, wl.k_scale,
                           wl.v_scale, kv_layout=1 if wl.nhd else 0,
                           mask_layout=1 if wl.mask_layout == "full" else 0, q_pos=wl.q_pos,
-                          rope_theta=wl.rope_theta or 0.0, rows=rows, nthreads=nthreads)
+                          rope_theta=wl.rope_theta or 0.0, q_fp8=q_fp8, rows=rows,
+                          nthreads=nthreads)

@@ -150,6 +150,27 @@ float oracle_div_f32(float x, float scale) {
     return (float)((double)x / (double)scale);
 }
 
+/* A query row as the e4m3 tensor-core path takes it: with amax = max |q_i|,
+ * inv = 448 / amax and qsc = amax / 448 (binary32 divisions), each element
+ * is stored as the e4m3 code of the binary32 product q_i * inv (round to
+ * nearest even, saturating), and the row stands for codes * qsc.  An all-zero
+ * row keeps scale 1.  Writes the codes and returns qsc. */
+float oracle_quantize_q_e4m3(const double* q, int d, uint8_t* codes) {
+    float amax = 0.0f;
+    for (int e = 0; e < d; ++e) {
+        float a = (float)fabs(q[e]);
+        if (a > amax) amax = a;
+    }
+    float inv = amax > 0.0f ? oracle_div_f32(448.0f, amax) : 1.0f;
+    float qsc = amax > 0.0f ? oracle_div_f32(amax, 448.0f) : 1.0f;
+    for (int e = 0; e < d; ++e) {
+        /* the binary32 product: exact in binary64 (24 + 24 bits), rounded once */
+        float x = (float)((double)(float)q[e] * (double)inv);
+        codes[e] = oracle_encode_e4m3_satfinite(x);
+    }
+    return qsc;
+}
+
 static double decode_kv(const void* base, int64_t idx, int kv_fp8) {
     if (kv_fp8) return oracle_decode_e4m3(((const uint8_t*)base)[idx]);
     return oracle_decode_bf16(((const uint16_t*)base)[idx]);
@@ -290,6 +311,7 @@ typedef struct {
     int h_q, h_kv, d, group;
     double sm_scale;
     const int32_t* q_pos;  /* NULL: no rotary embedding of the queries */
+    int q_fp8;             /* 1: the row is replaced by its e4m3 quantisation */
     double rope_theta, rope_scale;
     const int64_t* rows;   /* flat row ids token*h_q+head of this request */
     const int64_t* dest;   /* where each row's result goes */
@@ -328,6 +350,11 @@ static void* run_rows(void* arg) {
             for (int e = 0; e < jb->d; ++e)
                 qrow[e] = oracle_decode_bf16(oracle_encode_bf16(qrow[e]));
         }
+        if (jb->q_fp8) {
+            uint8_t codes[1024];
+            double qsc = (double)oracle_quantize_q_e4m3(qrow, jb->d, codes);
+            for (int e = 0; e < jb->d; ++e) qrow[e] = oracle_decode_e4m3(codes[e]) * qsc;
+        }
         /* One query row against the request's keys of KV head h: K/V rows are
          * [j][h][:] so the row stride is h_kv * d and the base is offset by h. */
         oracle_dense_attention(1, (int)jb->kv_len, jb->d, qrow, jb->d,
@@ -353,6 +380,9 @@ static void* run_rows(void* arg) {
  *  q_pos    NULL, or [total_qo] positions: each query row is rotated by
  *           oracle_rope_vec at its token's position (rope_theta, rope_scale)
  *           and rounded to bf16 (the query dtype) before the dot products
+ *  q_fp8    1: each query row (after any rotation) is replaced by its e4m3
+ *           quantisation (oracle_quantize_q_e4m3: codes times the row scale),
+ *           the operand of the e4m3 tensor-core path
  *  sel / n_sel: flat row ids token * h_q + head to compute (NULL = all rows,
  *           in flat order); out [n, d] and lse [n] follow the selection order.
  *  nthreads: worker threads (>= 1).
@@ -363,11 +393,13 @@ int oracle_verify_attn_ex(const uint16_t* q, const void* k_cache, const void* v_
                           const int32_t* kv_indices, const int32_t* last_page_len,
                           const int32_t* qo_indptr, const uint8_t* mask,
                           const int32_t* mask_indptr, int mask_layout, const int32_t* q_pos,
-                          double rope_theta, double rope_scale, int batch, int h_q, int h_kv,
+                          double rope_theta, double rope_scale, int q_fp8, int batch, int h_q,
+                          int h_kv,
                           int d, int page_size, int num_pages, double sm_scale, double k_scale,
                           double v_scale, const int32_t* sel, int64_t n_sel, double* out,
                           double* lse, int nthreads) {
     if (h_kv <= 0 || h_q <= 0 || h_q % h_kv != 0 || d <= 0 || nthreads < 1) return OR_EINVAL;
+    if (q_fp8 && d > 1024) return OR_EINVAL;
     if ((kv_layout != 0 && kv_layout != 1) || (mask_layout != 0 && mask_layout != 1))
         return OR_EINVAL;
     if (q_pos && !(rope_theta > 0.0 && rope_scale > 0.0)) return OR_EINVAL;
@@ -437,6 +469,7 @@ int oracle_verify_attn_ex(const uint16_t* q, const void* k_cache, const void* v_
             jb->h_q = h_q; jb->h_kv = h_kv; jb->d = d; jb->group = group;
             jb->sm_scale = sm_scale; jb->rows = rows; jb->dest = dest; jb->n_rows = nr;
             jb->q_pos = q_pos; jb->rope_theta = rope_theta; jb->rope_scale = rope_scale;
+            jb->q_fp8 = q_fp8;
             jb->out = out; jb->lse = lse;
             jb->lo = nr * i / nt; jb->hi = nr * (i + 1) / nt;
             jb->status = OR_OK;
@@ -462,7 +495,7 @@ int oracle_verify_attn(const uint16_t* q, const void* k_cache, const void* v_cac
                        double k_scale, double v_scale, const int32_t* sel, int64_t n_sel,
                        double* out, double* lse, int nthreads) {
     return oracle_verify_attn_ex(q, k_cache, v_cache, kv_fp8, 0, kv_indptr, kv_indices,
-                                 last_page_len, qo_indptr, mask, mask_indptr, 0, NULL, 0.0, 0.0,
+                                 last_page_len, qo_indptr, mask, mask_indptr, 0, NULL, 0.0, 0.0, 0,
                                  batch, h_q, h_kv, d, page_size, num_pages, sm_scale, k_scale,
                                  v_scale, sel, n_sel, out, lse, nthreads);
 }

@@ -366,3 +366,55 @@ def test_extensions_match_scalar_brute_force(oracle_lib, spec):
     assert np.array_equal(np.isfinite(lse), fin)
     np.testing.assert_allclose(out, bo, atol=1e-12, rtol=0)
     np.testing.assert_allclose(lse[fin], bl[fin], atol=1e-12, rtol=0)
+
+
+# ---------------------------------------------------------------- e4m3 queries
+
+def test_query_quantisation_matches_torch(oracle_lib):
+    """oracle_quantize_q_e4m3: amax = max |q|, inv = 448 / amax and qsc = amax
+    / 448 in binary32, codes = the e4m3 cast of the binary32 product q * inv
+    -- restated with torch's float32 arithmetic and its e4m3 cast."""
+    gen = torch.Generator().manual_seed(5)
+    for scale in (1.0, 30.0, 1e-3):
+        q = (torch.randn((16, 128), generator=gen) * scale).to(torch.bfloat16).float()
+        for row in q:
+            amax = row.abs().max()
+            inv = torch.tensor(448.0, dtype=torch.float32) / amax
+            want = (row * inv).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            codes, qsc = oracle.quantize_q_e4m3(row.double().numpy())
+            assert np.array_equal(codes, want)
+            assert qsc == float(amax / torch.tensor(448.0, dtype=torch.float32))
+    codes, qsc = oracle.quantize_q_e4m3(np.zeros(8))
+    assert qsc == 1.0 and not codes.any()
+
+
+def test_e4m3_query_attention_is_attention_over_the_quantised_rows(oracle_lib):
+    """verify attention with e4m3 queries = the plain definition over the
+    dequantised query rows (codes * scale, built here with torch), per row."""
+    wl = synthetic.make_custom(batch=2, h_q=4, h_kv=2, d=16, page_size=4,
+                               prefix=("fixed", [9, 3]), qo=("fixed", [4, 3]), mask="tree",
+                               kv_dtype=synthetic.FP8, seed=111)
+    kc, vc = oracle.build_cache(wl)
+    out, lse = oracle.verify_attn_workload(wl, caches=(kc, vc), q_fp8=True, nthreads=2)
+    qd = torch.from_numpy(wl.q.view(np.int16)).view(torch.bfloat16).float()
+    for b in range(wl.batch):
+        pre, L = int(wl.prefix_lens[b]), int(wl.qo_lens[b])
+        pages = wl.kv_indices[wl.kv_indptr[b]:wl.kv_indptr[b + 1]]
+        pos = np.arange(pre + L)
+        dec = lambda x: torch.from_numpy(np.ascontiguousarray(x)).view(torch.float8_e4m3fn).double().numpy()
+        for t in range(L):
+            tok = int(wl.qo_indptr[b]) + t
+            vis = list(range(pre)) + [pre + u for u in range(L) if wl.mask_dense[b][t, u]]
+            for qh in range(wl.h_q):
+                h = qh // wl.group
+                row = qd[tok, qh]
+                amax = row.abs().max()
+                inv = torch.tensor(448.0, dtype=torch.float32) / amax
+                qsc = float(amax / torch.tensor(448.0, dtype=torch.float32))
+                q8 = (row * inv).to(torch.float8_e4m3fn).double() * qsc
+                K = dec(kc[pages[pos // 4], h, pos % 4]) * wl.k_scale
+                V = dec(vc[pages[pos // 4], h, pos % 4]) * wl.v_scale
+                o, l = oracle.dense_attention(q8.numpy()[None], K[vis], V[vis],
+                                              np.zeros((1, len(vis))), wl.sm_scale)
+                np.testing.assert_allclose(out[tok * wl.h_q + qh], o[0], atol=1e-12, rtol=0)
+                assert abs(lse[tok * wl.h_q + qh] - l[0]) < 1e-12
