@@ -452,32 +452,40 @@ KERNEL_NAMES = {1: "verify_partial_mma_kernel<4 warps>", 2: "verify_partial_mma_
                 3: "verify_partial_tc_kernel<one Q tile>", 4: "verify_partial_tc_kernel<two Q tiles>"}
 
 
-def roofline_for(wl, kt, peaks, peak_kind, kernel=0):
+# dense e4m3 over dense bf16 tensor throughput, from the nominal rates
+# (4.5 vs 2.25 PFLOP/s per GPU)
+E4M3_OVER_BF16 = 2.0
+
+
+def roofline_for(wl, kt, peaks, peak_kind, kernel=0, e4m3=False):
     """Roofline of the split-attention kernel: algorithmic bytes (K + V + Q
     read once, out + LSE written once, tables and mask) or FLOPs per launch
     over its CUDA-event duration, against the measured copy bandwidth or
-    bf16 tensor throughput.  The bound is the one the workload's arithmetic
-    intensity selects."""
+    tensor throughput: measured bf16, or for e4m3 MMAs (plan option q_fp8)
+    measured bf16 times the nominal e4m3 / bf16 ratio.  The bound is the one
+    the workload's arithmetic intensity selects."""
     alg = algorithmic(wl)
     t = kt["partial_ms"] * 1e-3
     hbm = alg["total_bytes"] / t / 1e9
     tfl = alg["flops"] / t / 1e12
     rows_per_kv_head = int((wl.group * wl.qo_lens).max())
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tpeak = peaks["bf16_tflops"] * (E4M3_OVER_BF16 if e4m3 else 1.0)
+    ridge = tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     tensor_bound = alg["flops"] / alg["total_bytes"] > ridge
     if tensor_bound:
-        rf = {"bound": "tensor", "achieved": round(tfl, 2), "peak": peaks["bf16_tflops"],
-              "unit": "TFLOP/s", "frac": round(tfl / peaks["bf16_tflops"], 4)}
+        rf = {"bound": "tensor", "achieved": round(tfl, 2), "peak": round(tpeak, 1),
+              "unit": "TFLOP/s", "frac": round(tfl / tpeak, 4)}
     else:
         rf = {"bound": "hbm", "achieved": round(hbm, 1), "peak": peaks["hbm_gbs"],
               "unit": "GB/s", "frac": round(hbm / peaks["hbm_gbs"], 4)}
-    rf.update({"kernel": KERNEL_NAMES.get(kernel, "verify_partial"),
-               "peak_source": "MEASURED_PEAKS.json (of %s)" % peak_kind,
+    rf.update({"kernel": KERNEL_NAMES.get(kernel, "verify_partial") + ("_e4m3" if e4m3 else ""),
+               "peak_source": ("MEASURED_PEAKS.json (of %s)" % peak_kind
+                               + (", bf16 x %.0f nominal e4m3 ratio" % E4M3_OVER_BF16 if e4m3 else "")),
                "algorithmic_bytes_per_launch": alg["total_bytes"],
                "algorithmic_flops_per_launch": alg["flops"],
                "kernel_ms": round(kt["partial_ms"], 5),
                "hbm_gbs": round(hbm, 1), "hbm_frac": round(hbm / peaks["hbm_gbs"], 4),
-               "tflops": round(tfl, 2), "tensor_frac": round(tfl / peaks["bf16_tflops"], 4),
+               "tflops": round(tfl, 2), "tensor_frac": round(tfl / tpeak, 4),
                "rows_per_kv_head_max": rows_per_kv_head})
     return rf
 
@@ -516,16 +524,16 @@ def barrier_fn(world):
     return dist.barrier
 
 
-def cpu_baseline(wl, seconds=10.0, nthreads=None):
+def cpu_baseline(wl, seconds=10.0, nthreads=None, q_fp8=False):
     """The oracle as it stands, on the host cores, on the workload's full call
-    (every row), repeated for about `seconds`."""
+    (every row), repeated for about `seconds`; q_fp8: with e4m3 queries."""
     import oracle
     nthreads = nthreads or oracle.default_threads()
     caches = oracle.build_cache(wl)
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle.verify_attn_workload(wl, caches=caches, nthreads=nthreads)
+        oracle.verify_attn_workload(wl, caches=caches, nthreads=nthreads, q_fp8=q_fp8)
         n += 1
         el = time.perf_counter() - t0
         if el >= seconds or (n >= 1 and el * (n + 1) / n > 3 * seconds):
@@ -542,6 +550,8 @@ def workload_config(wl, bench=None):
            "kv_dtype": wl.kv_dtype, "mask": wl.mask_kind,
            "prefix_tokens": int(wl.prefix_lens.sum()), "draft_tokens": wl.total_qo,
            "kv_tokens": int(wl.kv_lens.sum())}
+    if bench is not None and bench.plan_opts.get("q_fp8"):
+        cfg["mma"] = "e4m3 queries (per-row amax scale) and e4m3 P: kind::f8f6f4"
     if bench is not None:
         cfg["l2"] = ("inputs rotate over %d KV-pool copies of %.1f MB (%.0f MB total vs 129 MB L2)"
                      % (bench.n_copies, bench.pool_bytes / 1e6,
@@ -559,8 +569,9 @@ def timing_block(bench, peaks, peak_kind, steps, warmup, sampler=None, barrier=N
     ms_v, _ = bench.time_steps(steps, warmup, verify_only=True)
     kt = bench.kernel_times()
     kernel = bench.plan.header()["kernel"]
-    rf = roofline_for(wl, kt, peaks, peak_kind, kernel)
-    rf["traffic"] = profiled_traffic(wl.name, kernel)
+    e4m3 = bool(bench.plan_opts.get("q_fp8"))
+    rf = roofline_for(wl, kt, peaks, peak_kind, kernel, e4m3=e4m3)
+    rf["traffic"] = profiled_traffic(wl.name + ("+q_fp8" if e4m3 else ""), kernel)
     alg = algorithmic(wl)
     return ms, clocks, {
         "verify_only": {"tokens_per_s": round(wl.total_qo / (ms_v * 1e-3), 1),
@@ -572,6 +583,55 @@ def timing_block(bench, peaks, peak_kind, steps, warmup, sampler=None, barrier=N
     }
 
 
+def accept_timing(wl, dev, vocab=128256, n=64):
+    """The step after verification on this workload's drafts: greedy
+    acceptance over [total_qo, vocab] bf16 target logits (N(0, 1), the
+    Llama-3 vocabulary size), trees from the workload's parents (chains when
+    it has none).  Bytes: the logits rows read once, plus the small tables."""
+    import torch
+    import speculative_decoding_verify_gqa_gb300 as va
+    gen = torch.Generator().manual_seed(3)
+    total = wl.total_qo
+    logits = torch.randn((total, vocab), generator=gen).to(torch.bfloat16).to(dev)
+    parents = []
+    for b in range(wl.batch):
+        L = int(wl.qo_lens[b])
+        par = wl.parents[b] if wl.parents is not None and wl.parents[b] is not None else \
+            [i - 1 for i in range(L)]
+        parents += list(par)
+    parents = torch.tensor(parents, dtype=torch.int32, device=dev)
+    toks = torch.randint(0, vocab, (total,), generator=gen, dtype=torch.int32).to(dev)
+    qo = torch.from_numpy(wl.qo_indptr).to(dev)
+    va.verify_accept_greedy(logits, qo, toks, parents)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        va.verify_accept_greedy(logits, qo, toks, parents)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    ws = torch.empty(1 << 22, dtype=torch.uint8, device=dev)
+    with torch.cuda.graph(g):
+        for _ in range(n):
+            va.verify_accept_greedy(logits, qo, toks, parents, workspace=ws)
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / n)
+    ms = statistics.median(ts)
+    nbytes = total * vocab * 2 + 4 * (3 * total + 2 * (wl.batch + 1))
+    return {"us_per_call": round(ms * 1e3, 3), "vocab": vocab, "rows": total,
+            "bytes_per_call": nbytes, "hbm_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "note": "greedy acceptance of the drafts (argmax kernel + tree walk), logits bf16, "
+                    "L2 not flushed between calls"}
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_setup(args.gpus)
@@ -579,7 +639,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     peaks, peak_kind = load_peaks()
     plan_opts = {k: v for k, v in (("kernel", args.kernel), ("target_ctas", args.target_ctas),
-                                   ("min_chunk", args.min_chunk)) if v}
+                                   ("min_chunk", args.min_chunk), ("q_fp8", args.q_fp8)) if v}
     bench = Bench(args.workload, dev, seed=0, plan_opts=plan_opts)
     wl = bench.wl
     sampler = ClockSampler(local)
@@ -605,6 +665,7 @@ def run_ours(args):
                        "tokens_per_s": round(wl.total_qo / (ms_w * 1e-3), 1),
                        "verify_only_us_per_call": round(ms_wv * 1e3, 3),
                        "note": "every step on one KV-pool copy, which stays resident in L2"}
+    line["accept_greedy"] = accept_timing(wl, dev)
     if not args.no_e2e:
         line["e2e"] = bench.e2e(args.e2e_steps)
         line["e2e"]["value"] = round(world * line["e2e"]["value"], 1)
@@ -612,23 +673,30 @@ def run_ours(args):
     torch.cuda.empty_cache()
     if not args.no_configs and world == 1:
         others = {}
+        runs = []
         for name in synthetic.WORKLOAD_ORDER:
-            if name == args.workload:
-                continue
-            b = Bench(name, dev, seed=0)
+            if name != args.workload or plan_opts:
+                runs.append((name, {}))
+            # fp8 caches once more with e4m3 queries: both MMAs on e4m3 operands
+            if synthetic.WORKLOADS[name]["kv_dtype"] == synthetic.FP8:
+                runs.append((name, {"q_fp8": True}))
+        for name, opts in runs:
+            b = Bench(name, dev, seed=0, plan_opts=opts)
             steps = 256 if name != "tiny_verify" else 1024
             ms_o, _, ex = timing_block(b, peaks, peak_kind, steps, 16)
             entry = {"tokens_per_s": round(b.wl.total_qo / (ms_o * 1e-3), 1),
                      "ms_per_step": round(ms_o, 6)}
             entry.update(ex)
             entry["config"] = workload_config(b.wl, b)
-            others[name] = entry
+            others[name + ("+q_fp8" if opts else "")] = entry
             del b
             torch.cuda.empty_cache()
         if rank == 0 and not args.no_cpu_baseline:
-            for name, entry in others.items():
+            for key, entry in others.items():
+                name, _, variant = key.partition("+")
                 entry["cpu_baseline"] = cpu_baseline(synthetic.make_workload(name),
-                                                     seconds=args.cpu_seconds_per_config)
+                                                     seconds=args.cpu_seconds_per_config,
+                                                     q_fp8=variant == "q_fp8")
         line["configs"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
@@ -705,6 +773,8 @@ def main(argv=None):
                          "3: tcgen05); 0 = the planner's choice")
     ap.add_argument("--target-ctas", type=int, default=0, help="planner option (0 = auto)")
     ap.add_argument("--min-chunk", type=int, default=0, help="planner option (0 = auto)")
+    ap.add_argument("--q-fp8", action="store_true",
+                    help="planner option for fp8 caches: e4m3 queries, kind::f8f6f4 MMAs")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

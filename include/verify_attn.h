@@ -139,7 +139,17 @@ typedef struct {
                             (verify_attn_run_ex's q_position) before Q K^T; the cache holds
                             keys already rotated at their own positions (paged_kv_append_ex
                             with positions) */
-    int reserved[1];     /* must be zero */
+    int q_fp8;           /* 1 (fp8-e4m3 caches, tcgen05 variants): run the MMAs on e4m3
+                            operands (kind::f8f6f4): each query row quantised to e4m3 with
+                            its own scale amax|q| / 448, P rounded to e4m3, K / V as
+                            stored -- twice the tensor rate of the default, which widens
+                            K / V to f16, at coarser precision (3 mantissa bits on q and
+                            P).  Against attention over the quantised query rows the LSE
+                            keeps the fp32 error; each output element moves by at most
+                            sum_j e_j |v_j| / sum_j p_j, p_j the key's probability over
+                            the row maximum, e_j = 2^-4 p_j + min(p_j, 2^-9).  Requires
+                            an fp8 cache and a tcgen05 variant (else
+                            VA_ERR_UNSUPPORTED) */
 } va_plan_options_t;
 
 #define VA_KERNEL_AUTO 0

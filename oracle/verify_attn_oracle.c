@@ -31,13 +31,12 @@
  *  - FlashInfer issue #152 "How to implement a tree attention": custom
  *    (tree) masks, -inf (or -5e4) where masked and 0 elsewhere.
  *
- * Readings where the pages leave a step open (each is listed with its
- * reasoning in the design notes): drafts are appended to the pages before
- * attention, so the queries are the last L_b positions of the kv range; the
- * mask is each request's L_b x L_b block, bit-packed LSB-first at bit offset
- * mask_indptr[b], bit 1 = visible, the prefix always visible; with no mask the
- * draft columns are causal (u <= t); a fully masked row has lse = -inf and
- * out = 0.
+ * Readings where the sources leave a step open: drafts are appended to the
+ * pages before attention, so the queries are the last L_b positions of the kv
+ * range; the mask is each request's L_b x L_b block, bit-packed LSB-first at
+ * bit offset mask_indptr[b], bit 1 = visible, the prefix always visible; with
+ * no mask the draft columns are causal (u <= t); a fully masked row has
+ * lse = -inf and out = 0.
  */
 #include <math.h>
 #include <pthread.h>

@@ -63,7 +63,7 @@ class PlanOptions(ctypes.Structure):
     _fields_ = [("max_splits", ctypes.c_int), ("min_chunk", ctypes.c_int),
                 ("target_ctas", ctypes.c_int), ("kernel", ctypes.c_int),
                 ("mask_layout", ctypes.c_int), ("kv_layout", ctypes.c_int),
-                ("rope", ctypes.c_int), ("reserved", ctypes.c_int * 1)]
+                ("rope", ctypes.c_int), ("q_fp8", ctypes.c_int)]
 
 
 class RunOptions(ctypes.Structure):
@@ -190,13 +190,14 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0, mask_layout="qlen",
-             kv_layout="hnd", rope=False):
+             kv_layout="hnd", rope=False, q_fp8=False):
     o = PlanOptions()
     o.max_splits, o.min_chunk, o.target_ctas, o.kernel = (int(max_splits), int(min_chunk),
                                                           int(target_ctas), int(kernel))
     o.mask_layout = _MASK_LAYOUTS[mask_layout]
     o.kv_layout = _LAYOUTS[kv_layout]
     o.rope = int(bool(rope))
+    o.q_fp8 = int(bool(q_fp8))
     return o
 
 

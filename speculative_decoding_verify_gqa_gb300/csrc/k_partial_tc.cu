@@ -48,7 +48,10 @@
 namespace va {
 namespace {
 
-template <bool FP8, int NQ>
+// FP8: the cache is fp8-e4m3.  F8MMA (fp8 caches only): the MMAs run on
+// e4m3 operands (kind::f8f6f4: Q quantised per row, P as e4m3, K / V as
+// stored) instead of widening K / V to f16 (kind::f16).
+template <bool FP8, int NQ, bool F8MMA = false>
 struct TcCfg {
   static constexpr int ROWS = 128, D = 128;              // rows per Q tile = TMEM lanes
   static constexpr int KEYS = 128;                       // keys per tile (MMA N of S, K of PV)
@@ -57,14 +60,15 @@ struct TcCfg {
   // fp8 widening: warps 2, 3 and CONV_WARP0 + 2, + 3 -- all on the SM
   // sub-partitions 2 and 3 (warp % 4), away from the producer's and the MMA
   // issuer's; warps CONV_WARP0 and CONV_WARP0 + 1 stay idle
-  static constexpr int CONV_WARPS = FP8 ? 4 : 0;
+  static constexpr bool WIDEN = FP8 && !F8MMA;           // fp8 widened to f16 by converter warps
+  static constexpr int CONV_WARPS = WIDEN ? 4 : 0;
   static constexpr int THREADS = 32 * (CONV_WARP0 + CONV_WARPS);  // fp8: 4 warps past the softmax
   static constexpr int QT_BYTES = ROWS * D * 2;          // one Q tile: [2 halves][128 rows][128 B]
   static constexpr int Q_BYTES = NQ * QT_BYTES;
   static constexpr int OP_BYTES = KEYS * D * 2;          // 16-bit K (or V) operand tile
   static constexpr int RAW_BYTES = KEYS * D;             // fp8 K (or V) tile [keys][128 B]
   static constexpr int SLOT_BYTES = FP8 ? RAW_BYTES : OP_BYTES;
-  static constexpr int CONV_BYTES = FP8 ? 3 * OP_BYTES : 0;  // widened K (two) and V (one)
+  static constexpr int CONV_BYTES = WIDEN ? 3 * OP_BYTES : 0;  // widened K (two) and V (one)
   static constexpr int BAR_BYTES = 1024;                 // barriers, TMEM address, item queue
   static constexpr int RING_AVAIL = 227 * 1024 - BAR_BYTES - Q_BYTES - CONV_BYTES;
   static constexpr int NSLOT = RING_AVAIL / SLOT_BYTES > 8 ? 8 : RING_AVAIL / SLOT_BYTES;
@@ -164,10 +168,11 @@ __device__ __forceinline__ ItemGeo decode_item(const PartialParams& p, int i) {
 // item k's last S MMA has read Q, and its keys into the same slot ring; the
 // MMA issuer starts item k + 1's S MMAs while the softmax warps still write
 // item k's output, and its first PV once that output has left O.
-template <bool FP8, int NQ>
-__global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
+template <bool FP8, int NQ, bool F8MMA>
+__global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
     verify_partial_tc_kernel(const PartialParams p, const __grid_constant__ TcMaps maps) {
-  using C = TcCfg<FP8, NQ>;
+  using C = TcCfg<FP8, NQ, F8MMA>;
+  constexpr bool WIDEN = C::WIDEN;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the swizzled operand tiles need 1024-byte alignment
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
   const int G = p.group;
   // Q is rewritten in shared memory by the softmax warps before the first S
   // MMA reads it: to f16 for an fp8 cache, rotated at its positions for RoPE
-  const bool q_pass = FP8 || p.q_position != nullptr;
+  const bool q_pass = FP8 || p.q_position != nullptr;   // f16 widening or e4m3 quantisation
   // This CTA's items: chain blockIdx.x (then blockIdx.x + gridDim.x, ... if
   // the grid is smaller than the plan's chain count), linked through next; a
   // malformed link ends its chain.
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     mbar_init(bar(B_Q_FREE), 1);
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(bar(B_FULL + s), 1);
-      mbar_init(bar(B_EMPTY + s), FP8 ? C::CONV_WARPS : 1);
+      mbar_init(bar(B_EMPTY + s), WIDEN ? C::CONV_WARPS : 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_CK_FULL + s), C::CONV_WARPS > 0 ? C::CONV_WARPS : 1);
@@ -413,9 +418,12 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       // K / V operand layouts: widened fp8 in 64-column halves [half][keys][64]
       // (halves KEYS * 128 bytes apart, 8-key groups 1024); bf16 as the TMA
       // boxes land, [8-key group][half][8][64] (groups 2048 apart, halves 1024)
+      // e4m3 operands (F8MMA) as they land: [keys][128 B], 8-key groups 1024
+      // apart, one 128-byte swizzle atom across the whole head dimension
       constexpr uint32_t KV_SBO = FP8 ? 1024 : 2048;            // 8-key group stride
-      constexpr uint32_t KV_HALF = FP8 ? C::KEYS * 128 : 1024;  // 64-column half stride
-      constexpr uint32_t V_LBO = KV_HALF, V_KK = 2 * KV_SBO;    // PV: 16 keys per MMA
+      constexpr uint32_t KV_HALF = WIDEN ? C::KEYS * 128 : (F8MMA ? 0 : 1024);  // 64-column half stride
+      constexpr uint32_t V_LBO = F8MMA ? 8192 : KV_HALF;      // F8MMA: one atom across d (unused)
+      constexpr uint32_t V_KK = (F8MMA ? 4 : 2) * KV_SBO;     // PV: 16 (f16) or 32 (e4m3) keys per MMA
       // tcgen05.mma issue is close to synchronous: whatever this thread runs
       // between two MMAs (an mbarrier poll costs about as much as an N = 128
       // MMA) leaves the tensor core idle, and the thread shares its
@@ -432,15 +440,28 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       for (int qt = 0; qt < NQ; ++qt)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          dq[qt][kk] = smem_desc_sw128(sbase + C::OFF_Q + qt * C::QT_BYTES + (kk >> 2) * (C::ROWS * 128) + (kk & 3) * 32,
-                                       16, 1024);
+          // 16-bit Q: [half][128 rows][128 B], 8 steps of 16 elements; e4m3
+          // Q (F8MMA): [128 rows][128 B] in the first half, 4 steps of 32
+          dq[qt][kk] = F8MMA ? smem_desc_sw128(sbase + C::OFF_Q + qt * C::QT_BYTES + (kk & 3) * 32, 16, 1024)
+                             : smem_desc_sw128(sbase + C::OFF_Q + qt * C::QT_BYTES + (kk >> 2) * (C::ROWS * 128) + (kk & 3) * 32,
+                                               16, 1024);
       // S = Q_qt K^T into TMEM column d (K at shared address kx)
       auto s_batch = [&](uint32_t d, const uint64_t (&aq)[8], uint32_t kx) {
         const uint64_t dk = KD0 + (uint64_t)(kx >> 4);
-        uint64_t bk[8];
+        if constexpr (F8MMA) {
+          uint64_t a4[4], bk[4];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) bk[kk] = dk + (uint64_t)(((kk >> 2) * KV_HALF + (kk & 3) * 32) >> 4);
-        umma_ss_x8(d, aq, bk, id_s);
+          for (int kk = 0; kk < 4; ++kk) {
+            a4[kk] = aq[kk];
+            bk[kk] = dk + (uint64_t)((kk * 32) >> 4);
+          }
+          umma_ss_x4_f8(d, a4, bk, id_s);
+        } else {
+          uint64_t bk[8];
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) bk[kk] = dk + (uint64_t)(((kk >> 2) * KV_HALF + (kk & 3) * 32) >> 4);
+          umma_ss_x8(d, aq, bk, id_s);
+        }
       };
       // O (+)= P V: O at TMEM column d, P at column pc, V at shared address vx
       auto pv_batch = [&](uint32_t d, uint32_t pc, uint32_t vx, uint32_t acc0) {
@@ -448,8 +469,12 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         uint64_t bv[8];
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) bv[kk] = dv + (uint64_t)((kk * V_KK) >> 4);
-        umma_ts_x4(d, pc + p_col(0), bv, id_o, acc0);
-        umma_ts_x4(d, pc + p_col(4), bv + 4, id_o, 1u);
+        if constexpr (F8MMA) {
+          umma_ts_x4_f8(d, pc, bv, id_o, acc0);   // P of keys 32 q at column 32 q
+        } else {
+          umma_ts_x4(d, pc + p_col(0), bv, id_o, acc0);
+          umma_ts_x4(d, pc + p_col(4), bv + 4, id_o, 1u);
+        }
       };
       // Ring cursors of the next K and V operands: bf16 operand u = 2 t (K_t)
       // or 2 t + 1 (V_t) of the running key tile count t sits in slot u % NSLOT,
@@ -469,17 +494,17 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         }
         ++cu.t;
       };
-      auto k_full = [&](const Cur& cu) { return FP8 ? bar(B_CK_FULL + (cu.t & 1)) : bar(B_FULL + cu.slot); };
-      auto k_par = [&](const Cur& cu) -> uint32_t { return FP8 ? (uint32_t)(cu.t >> 1) & 1u : cu.par; };
-      auto k_free = [&](const Cur& cu) { return FP8 ? bar(B_CK_FREE + (cu.t & 1)) : bar(B_EMPTY + cu.slot); };
+      auto k_full = [&](const Cur& cu) { return WIDEN ? bar(B_CK_FULL + (cu.t & 1)) : bar(B_FULL + cu.slot); };
+      auto k_par = [&](const Cur& cu) -> uint32_t { return WIDEN ? (uint32_t)(cu.t >> 1) & 1u : cu.par; };
+      auto k_free = [&](const Cur& cu) { return WIDEN ? bar(B_CK_FREE + (cu.t & 1)) : bar(B_EMPTY + cu.slot); };
       auto k_base = [&](const Cur& cu) -> uint32_t {
-        return FP8 ? sbase + C::OFF_CONV + (cu.t & 1) * C::OP_BYTES : sbase + C::OFF_RING + cu.slot * C::SLOT_BYTES;
+        return WIDEN ? sbase + C::OFF_CONV + (cu.t & 1) * C::OP_BYTES : sbase + C::OFF_RING + cu.slot * C::SLOT_BYTES;
       };
-      auto v_full = [&](const Cur& cu) { return FP8 ? bar(B_CV_FULL) : bar(B_FULL + cu.slot); };
-      auto v_par = [&](const Cur& cu) -> uint32_t { return FP8 ? (uint32_t)cu.t & 1u : cu.par; };
-      auto v_free = [&](const Cur& cu) { return FP8 ? bar(B_CV_FREE) : bar(B_EMPTY + cu.slot); };
+      auto v_full = [&](const Cur& cu) { return WIDEN ? bar(B_CV_FULL) : bar(B_FULL + cu.slot); };
+      auto v_par = [&](const Cur& cu) -> uint32_t { return WIDEN ? (uint32_t)cu.t & 1u : cu.par; };
+      auto v_free = [&](const Cur& cu) { return WIDEN ? bar(B_CV_FREE) : bar(B_EMPTY + cu.slot); };
       auto v_base = [&](const Cur& cu) -> uint32_t {
-        return FP8 ? sbase + C::OFF_CONV + 2 * C::OP_BYTES : sbase + C::OFF_RING + cu.slot * C::SLOT_BYTES;
+        return WIDEN ? sbase + C::OFF_CONV + 2 * C::OP_BYTES : sbase + C::OFF_RING + cu.slot * C::SLOT_BYTES;
       };
       // releases of the last K / V operand (the exit waits for them)
       uint32_t last_k = 0, last_kp = 0, last_v = 0, last_vp = 0;
@@ -590,7 +615,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
         mbar_wait(last_k, last_kp, abort_flag);
       }
     }
-  } else if (FP8 && (warp == 2 || warp == 3 || warp >= C::CONV_WARP0 + 2)) {
+  } else if (WIDEN && (warp == 2 || warp == 3 || warp >= C::CONV_WARP0 + 2)) {
     // ---------------- fp8 -> scaled f16 widening ----------------
     // Step i of an item widens K_i, then V_{i-1}: K runs a tile ahead, since
     // S_i needs only K_i while V's single buffer frees up one PV later.
@@ -657,7 +682,8 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
     const int quad = warp & 3;                      // TMEM lane quarter this warp may access
     const int r = quad * 32 + lane;                 // row of the Q tile = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16) + qt * C::QT_COLS;
-    const float c = p.scale_log2;
+    float c = p.scale_log2;                         // logit scale (log2 units), per row for F8MMA
+    float qsc = 1.f;                                // F8MMA: this row's query scale
     int ns = 0, no = 0, nit = 0, u0 = 0;            // S tiles seen, items done, items, ring base
     bool live = true;
     bool dep_waited = false;                        // this thread has waited for the previous grid
@@ -698,7 +724,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
                 // MMAs take it widened (exactly) to f16
                 wa[k] = pack_bf16x2(ya0, ya1);
                 wb[k] = pack_bf16x2(yb0, yb1);
-                if (FP8) {
+                if (WIDEN) {
                   wa[k] = bf16x2_to_f16x2(wa[k]);
                   wb[k] = bf16x2_to_f16x2(wb[k]);
                 }
@@ -706,7 +732,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
               *reinterpret_cast<uint4*>(h0 + jp * 16) = a;
               *reinterpret_cast<uint4*>(h1 + jp * 16) = b;
             }
-          } else if (FP8) {
+          } else if (WIDEN) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               uint4* q4 = reinterpret_cast<uint4*>(half ? h1 : h0);
@@ -721,12 +747,51 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
               }
             }
           }
+          if constexpr (F8MMA) {
+            // e4m3 row with its own scale: q = q8 * qsc, qsc = amax |q| / 448;
+            // the row (bf16, rotated if RoPE) is read whole before the e4m3
+            // bytes overwrite its first half (the row's first 128 bytes hold
+            // [128 elements] e4m3 in the same 128-byte swizzle)
+            uint4 lo8[8];
+            float amax = 0.f;
+#pragma unroll
+            for (int jp = 0; jp < 8; ++jp) {
+              lo8[jp] = *reinterpret_cast<const uint4*>(h0 + jp * 16);
+              const uint4 hb = *reinterpret_cast<const uint4*>(h1 + jp * 16);
+              const uint32_t wa4[4] = {lo8[jp].x, lo8[jp].y, lo8[jp].z, lo8[jp].w};
+              const uint32_t wb4[4] = {hb.x, hb.y, hb.z, hb.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                amax = fmax3(amax, fabsf(__uint_as_float(wa4[k] << 16)), fabsf(__uint_as_float(wa4[k] & 0xffff0000u)));
+                amax = fmax3(amax, fabsf(__uint_as_float(wb4[k] << 16)), fabsf(__uint_as_float(wb4[k] & 0xffff0000u)));
+              }
+            }
+            const float inv = amax > 0.f ? 448.f / amax : 1.f;
+            qsc = amax > 0.f ? amax / 448.f : 1.f;
+            const int x = r & 7;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+#pragma unroll
+              for (int jp = 0; jp < 8; ++jp) {
+                const uint4 w = half ? *reinterpret_cast<const uint4*>(h1 + jp * 16) : lo8[jp];
+                const int e0 = 64 * half + 8 * (jp ^ x);       // first element of the chunk
+                const uint32_t b0 = e4m3x4_rn_satfinite(
+                    __uint_as_float(w.x << 16) * inv, __uint_as_float(w.x & 0xffff0000u) * inv,
+                    __uint_as_float(w.y << 16) * inv, __uint_as_float(w.y & 0xffff0000u) * inv);
+                const uint32_t b1 = e4m3x4_rn_satfinite(
+                    __uint_as_float(w.z << 16) * inv, __uint_as_float(w.z & 0xffff0000u) * inv,
+                    __uint_as_float(w.w << 16) * inv, __uint_as_float(w.w & 0xffff0000u) * inv);
+                *reinterpret_cast<uint2*>(h0 + (((e0 >> 4) ^ x) << 4) + (e0 & 15)) = make_uint2(b0, b1);
+              }
+            }
+          }
           fence_proxy_async();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_Q_READY));
       }
       ++nit;
+      if constexpr (F8MMA) c = p.scale_log2 * qsc;
       if (!mine) {
         u0 += 2 * g.n_tiles;
         continue;
@@ -759,6 +824,24 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
       float l = 0.f;
       for (int j = 0; live && j < g.n_tiles; ++j) {
         const int k0 = g.lo + j * C::KEYS;
+        if constexpr (F8MMA) {
+          // Rows of V_j past the chunk end inside the last 16-key box may hold
+          // stale (even NaN) slots: zero them, since 0 * NaN would poison O
+          // (e4m3 V as it landed: [keys][128 B])
+          const int tail = hi - k0;
+          if (qt == 0 && tail < C::KEYS && (tail & 15)) {
+            const int u = u0 + 2 * j + 1, s = u % C::NSLOT;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(B_FULL + s), (u / C::NSLOT) & 1, abort_flag))) {
+              live = false;
+              break;
+            }
+            const int zlo = tail, zhi = (tail + 15) & ~15;
+            uint8_t* vt = smem + C::OFF_RING + s * C::SLOT_BYTES;
+            for (int z = r; z < (zhi - zlo) * 8; z += C::ROWS)
+              *reinterpret_cast<uint4*>(vt + (zlo + z / 8) * 128 + ((z & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async();
+          }
+        }
         if constexpr (!FP8) {
           // Rows of V_j past the chunk end inside the last 16-key box may hold
           // stale (even NaN) slots: zero them, since 0 * NaN would poison O.
@@ -921,12 +1004,21 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
               // this tile's P chunks 0 .. q-1, already in tensor memory
               tmem_wait_st();
               for (int q2 = 0; q2 < q; ++q2) {
-                uint32_t pk[16];
-                tmem_ld16(s_addr + 32 * q2, pk);
-                tmem_wait_ld();
+                if constexpr (F8MMA) {
+                  uint32_t pk[8];
+                  tmem_ld8(s_addr + 32 * q2, pk);
+                  tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = FP8 ? scale_f16x2(pk[i], a) : scale_bf16x2(pk[i], a);
-                tmem_st16(s_addr + 32 * q2, pk);
+                  for (int i = 0; i < 8; ++i) pk[i] = scale_e4m3x4(pk[i], a);
+                  tmem_st8(s_addr + 32 * q2, pk);
+                } else {
+                  uint32_t pk[16];
+                  tmem_ld16(s_addr + 32 * q2, pk);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) pk[i] = FP8 ? scale_f16x2(pk[i], a) : scale_bf16x2(pk[i], a);
+                  tmem_st16(s_addr + 32 * q2, pk);
+                }
               }
             }
 #pragma unroll
@@ -952,9 +1044,24 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
               p1 = ex2(f32x2_hi(x));
               sums2[i & 1] = add_f32x2(sums2[i & 1], f32x2(p0, p1));
             }
-            pk[i] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            if constexpr (F8MMA) {
+              raw[2 * i] = __float_as_uint(p0);     // packed four to a column below
+              raw[2 * i + 1] = __float_as_uint(p1);
+            } else {
+              pk[i] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            }
           }
-          tmem_st16(s_addr + 32 * q, pk);
+          if constexpr (F8MMA) {
+            // P of the 32 logits as e4m3, four keys to a column, into columns
+            // 32 q .. 32 q + 7 (P <= 2^8 < 448 by the lazy reference max)
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+              pk[w] = e4m3x4_rn_satfinite(__uint_as_float(raw[4 * w]), __uint_as_float(raw[4 * w + 1]),
+                                          __uint_as_float(raw[4 * w + 2]), __uint_as_float(raw[4 * w + 3]));
+            tmem_st8(s_addr + 32 * q, pk);
+          } else {
+            tmem_st16(s_addr + 32 * q, pk);
+          }
         }
         const float sum = FP8 ? (sums[0] + sums[1]) + (sums[2] + sums[3])
                               : (f32x2_lo(sums2[0]) + f32x2_hi(sums2[0])) + (f32x2_lo(sums2[1]) + f32x2_hi(sums2[1]));
@@ -1071,11 +1178,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ>::THREADS, 1)
   if (tid == 0 && *abort_flag) atomicOr(p.status, VA_DEV_TIMEOUT);
 }
 
-template <bool FP8, int NQ>
+template <bool FP8, int NQ, bool F8MMA = false>
 cudaError_t launch_tc(const PartialParams& p, const TcMaps& maps, int n_items,
                       cudaStream_t stream) {
-  using C = TcCfg<FP8, NQ>;
-  auto kern = verify_partial_tc_kernel<FP8, NQ>;
+  using C = TcCfg<FP8, NQ, F8MMA>;
+  auto kern = verify_partial_tc_kernel<FP8, NQ, F8MMA>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PartialParams*>(&p), const_cast<TcMaps*>(&maps)};
@@ -1089,8 +1196,13 @@ cudaError_t launch_tc(const PartialParams& p, const TcMaps& maps, int n_items,
 }  // namespace
 
 cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, bool kv_fp8,
-                              int block_rows, int n_items, cudaStream_t stream) {
+                              int block_rows, int n_items, bool f8mma, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
+  if (f8mma) {
+    if (!kv_fp8) return cudaErrorInvalidValue;
+    return block_rows == 256 ? launch_tc<true, 2, true>(p, maps, n_items, stream)
+                             : launch_tc<true, 1, true>(p, maps, n_items, stream);
+  }
   if (block_rows == 256)
     return kv_fp8 ? launch_tc<true, 2>(p, maps, n_items, stream)
                   : launch_tc<false, 2>(p, maps, n_items, stream);

@@ -231,7 +231,7 @@ int make_tc_maps(const void* q, int64_t total_qo, const void* k_cache, const voi
     }
     if (enc(dst[i], fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
             const_cast<void*>(src[i]), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+            fp8 && !(hd->flags & kPlanF8Mma) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return VA_ERR_CUDA;
   }
@@ -296,6 +296,7 @@ static int run_partial(const void* q, const void* k_cache, const void* v_cache,
     rc = make_tc_maps(q, hd->total_qo, k_cache, v_cache, num_pages, hd, &maps);
     if (rc) return rc;
     e = launch_partial_tc(p, maps, hd->kv_dtype == VA_DTYPE_FP8_E4M3, hd->block_rows, hd->n_items,
+                          (hd->flags & kPlanF8Mma) != 0,
                           static_cast<cudaStream_t>(stream));
   } else {
     e = launch_partial_mma(p, hd->kernel, hd->head_dim, hd->kv_dtype == VA_DTYPE_FP8_E4M3,

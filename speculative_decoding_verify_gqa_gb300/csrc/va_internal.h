@@ -62,6 +62,7 @@ static_assert(sizeof(MergeItem) == 32, "MergeItem layout");
 constexpr int64_t kPlanMaskFull = 1;  // mask rows of kv_len bits (prefix included)
 constexpr int64_t kPlanNhd = 2;       // cache layout [pages, P, h_kv, d]
 constexpr int64_t kPlanRope = 4;      // queries rotated at their positions
+constexpr int64_t kPlanF8Mma = 8;     // e4m3 MMAs: queries quantised per row, P as e4m3
 
 struct PlanHeader {
   uint32_t magic, version;

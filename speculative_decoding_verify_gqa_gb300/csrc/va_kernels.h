@@ -142,12 +142,13 @@ cudaError_t launch_partial_mma(const PartialParams& p, int kernel, int head_dim,
 // bytes apart and halves 1024 -- a uniform layout that both MMAs read (K
 // K-major, V MN-major), in one 4 KB copy per 16 keys.  An fp8 cache keeps the
 // 4-D view [num_pages, h_kv, P, 128] with 128 x 16 x 1 x 1 boxes (no swizzle).
-// Zero fill out of bounds.
+// Zero fill out of bounds.  With e4m3 MMAs (plan option q_fp8) the fp8
+// boxes land with 128-byte swizzle, as the MMA operands.
 struct TcMaps {
   CUtensorMap q, k, v;
 };
 cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, bool kv_fp8,
-                              int block_rows, int n_items, cudaStream_t stream);
+                              int block_rows, int n_items, bool f8mma, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int head_dim, int n_merge, int block_rows,
                          cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);

@@ -87,13 +87,13 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   va_plan_options_t o;
   std::memset(&o, 0, sizeof(o));
   if (opts) o = *opts;
-  for (int r : o.reserved)
-    if (r) return VA_ERR_INVALID_ARGUMENT;
   if (o.max_splits < 0 || o.min_chunk < 0 || o.target_ctas < 0) return VA_ERR_INVALID_ARGUMENT;
   if ((o.mask_layout != VA_MASK_QLEN && o.mask_layout != VA_MASK_FULL) ||
       (o.kv_layout != VA_LAYOUT_HND && o.kv_layout != VA_LAYOUT_NHD) || (o.rope != 0 && o.rope != 1))
     return VA_ERR_INVALID_ARGUMENT;
   const bool full_mask = o.mask_layout == VA_MASK_FULL;
+  if (o.q_fp8 != 0 && o.q_fp8 != 1) return VA_ERR_INVALID_ARGUMENT;
+  if (o.q_fp8 && kv_dtype != VA_DTYPE_FP8_E4M3) return VA_ERR_UNSUPPORTED;
   if (full_mask && !has_mask) return VA_ERR_INVALID_ARGUMENT;
   if (o.kernel != VA_KERNEL_AUTO && o.kernel != VA_KERNEL_MMA_64 && o.kernel != VA_KERNEL_MMA_128 &&
       o.kernel != VA_KERNEL_TC_128 && o.kernel != VA_KERNEL_TC_256)
@@ -130,6 +130,9 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   const bool tc_ok = head_dim == 128 && page_size % 16 == 0 && 128 % G == 0;
   int kernel = o.kernel;
   if ((kernel == VA_KERNEL_TC_128 || kernel == VA_KERNEL_TC_256) && !tc_ok) return VA_ERR_UNSUPPORTED;
+  // e4m3 MMAs exist in the tcgen05 variants only
+  if (o.q_fp8 && (!tc_ok || kernel == VA_KERNEL_MMA_64 || kernel == VA_KERNEL_MMA_128))
+    return VA_ERR_UNSUPPORTED;
   if (kernel == VA_KERNEL_AUTO) {
     // Measured on GB300: the tcgen05 variants beat the warp-level one on every
     // shape they serve (mma.sync runs at a fraction of the tensor-core rate
@@ -401,7 +404,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   hd.plan_bytes = need;
   hd.n_ctas = n_ctas;
   hd.flags = (full_mask ? kPlanMaskFull : 0) | (o.kv_layout == VA_LAYOUT_NHD ? kPlanNhd : 0) |
-             (o.rope ? kPlanRope : 0);
+             (o.rope ? kPlanRope : 0) | (o.q_fp8 ? kPlanF8Mma : 0);
 
   char* dst = static_cast<char*>(plan_h);
   std::memcpy(dst, &hd, sizeof(hd));

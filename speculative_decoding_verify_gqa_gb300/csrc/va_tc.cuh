@@ -179,6 +179,36 @@ __device__ __forceinline__ void umma_ts_x4(uint32_t d, uint32_t a, const uint64_
       "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc0), "r"(idesc)
       : "memory");
 }
+// Four MMAs D (+)= A_k B_k^T, k = 0..3, of fp8-e4m3 operands (kind::f8f6f4,
+// K = 32 per instruction: one K = 128 contraction), from shared-memory
+// descriptors, back to back; the first overwrites D.
+__device__ __forceinline__ void umma_ss_x4_f8(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4],
+                                              uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %9, %9;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %5, %9, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %6, %9, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %7, %9, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %8, %9, 1;\n}\n" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc)
+      : "memory");
+}
+// Four MMAs D += A_k B_k, k = 0..3, of fp8-e4m3 operands, A from tensor
+// memory: 32 keys each, packed four per column at columns a, a + 32, a + 64,
+// a + 96 (the P of 32 logits over the first quarter of their own S
+// columns); the first accumulates only if acc0 != 0.
+__device__ __forceinline__ void umma_ts_x4_f8(uint32_t d, uint32_t a, const uint64_t* b, uint32_t idesc,
+                                              uint32_t acc0) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b32 a1, a2, a3;\n setp.ne.b32 p, %6, 0;\n"
+      " add.u32 a1, %1, 32;\n add.u32 a2, %1, 64;\n add.u32 a3, %1, 96;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %7, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a1], %3, %7, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a2], %4, %7, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a3], %5, %7, 1;\n}\n" ::"r"(d),
+      "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc0), "r"(idesc)
+      : "memory");
+}
 // Arrive once on the mbarrier when every MMA this thread issued so far is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
@@ -246,6 +276,18 @@ __device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t* r) 
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
+}
+// 8 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");

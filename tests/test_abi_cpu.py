@@ -345,6 +345,12 @@ def test_plan_validation_codes(va):
     assert _plan_rc(va, *ok, kernel=4) == 0
     assert _plan_rc(va, *ok, kernel=4, d=64) == -2         # tcgen05 variants: head_dim 128 only
     assert _plan_rc(va, *ok, kernel=3, P=8) == -2          # page boxes of 16 rows
+    # e4m3 queries: an fp8 cache and a tcgen05 variant (auto picks one)
+    assert _plan_rc(va, *ok, kv_dtype=1, q_fp8=True) == 0
+    assert _plan_rc(va, *ok, kv_dtype=1, q_fp8=True, kernel=4) == 0
+    assert _plan_rc(va, *ok, kv_dtype=0, q_fp8=True) == -2     # bf16 cache
+    assert _plan_rc(va, *ok, kv_dtype=1, q_fp8=True, kernel=2) == -2   # warp-level variant
+    assert _plan_rc(va, *ok, kv_dtype=1, q_fp8=True, d=64) == -2
 
 
 def test_empty_batches_plan_to_nothing(va):
