@@ -150,6 +150,13 @@ typedef struct {
                             the row maximum, e_j = 2^-4 p_j + min(p_j, 2^-9).  Requires
                             an fp8 cache and a tcgen05 variant (else
                             VA_ERR_UNSUPPORTED) */
+    int draft_items;     /* tcgen05 variants: 1 = a split request's drafts (keys prefix ..
+                            kv_len) form a work item of their own, -1 = never, 0 = the
+                            planner's choice (on when the split units are few next to the
+                            CTAs and the drafts fit one key tile).  verify_attn_append_run
+                            with a plain copy append reads such an item's keys and values
+                            from k_new / v_new instead of the pages, so it does not wait
+                            for the append. */
 } va_plan_options_t;
 
 #define VA_KERNEL_AUTO 0
@@ -488,10 +495,9 @@ int verify_accept_greedy(const void* logits, va_dtype logits_dtype, int64_t tota
  *    process exits.
  *  - Set-up: the first call in each CUDA context (normally: on each device,
  *    with that device current) looks up the array's device address with
- *    cudaGetSymbolAddress and keeps it for that context; make that first call
- *    before any stream capture begins.  A context created later (after
- *    cudaDeviceReset, or a driver context the caller makes current) gets its
- *    own look-up.
+ *    cudaGetSymbolAddress and keeps it for that context.  A context created
+ *    later (after cudaDeviceReset, or a driver context the caller makes
+ *    current) gets its own look-up.
  *  - Every call copies the plan's work list from plan_h into the array and
  *    clears its status word on `stream` with asynchronous copies (so plan_h,
  *    if pinned, must stay unchanged until the copy has run), then launches the

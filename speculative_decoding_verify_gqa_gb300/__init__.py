@@ -63,7 +63,7 @@ class PlanOptions(ctypes.Structure):
     _fields_ = [("max_splits", ctypes.c_int), ("min_chunk", ctypes.c_int),
                 ("target_ctas", ctypes.c_int), ("kernel", ctypes.c_int),
                 ("mask_layout", ctypes.c_int), ("kv_layout", ctypes.c_int),
-                ("rope", ctypes.c_int), ("q_fp8", ctypes.c_int)]
+                ("rope", ctypes.c_int), ("q_fp8", ctypes.c_int), ("draft_items", ctypes.c_int)]
 
 
 class RunOptions(ctypes.Structure):
@@ -190,7 +190,7 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0, mask_layout="qlen",
-             kv_layout="hnd", rope=False, q_fp8=False):
+             kv_layout="hnd", rope=False, q_fp8=False, draft_items=0):
     o = PlanOptions()
     o.max_splits, o.min_chunk, o.target_ctas, o.kernel = (int(max_splits), int(min_chunk),
                                                           int(target_ctas), int(kernel))
@@ -198,6 +198,7 @@ def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0, mask_layout="ql
     o.kv_layout = _LAYOUTS[kv_layout]
     o.rope = int(bool(rope))
     o.q_fp8 = int(bool(q_fp8))
+    o.draft_items = int(draft_items)
     return o
 
 
@@ -572,9 +573,8 @@ def verify_attn_run_static_scratch(q, k_cache, v_cache, kv_indptr, kv_indices, l
     """verify_attn_run for callers that cannot allocate device memory: the
     library's own static scratch array (STATIC_SCRATCH_BYTES) stands in for
     the workspace, so `plan` may come from verify_attn_plan_host (no device
-    workspace).  The first call on a device looks up the array's address
-    (make it before any graph capture); calls that overlap on the GPU share
-    the array and race."""
+    workspace).  The first call in each CUDA context looks up the array's
+    address; calls that overlap on the GPU share the array and race."""
     out, lse = _alloc_out(q, plan, out, lse, want_lse)
     if num_pages is None:
         num_pages = k_cache.shape[0]

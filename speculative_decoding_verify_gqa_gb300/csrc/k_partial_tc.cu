@@ -118,8 +118,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 // One work item's geometry, as every role of the CTA decodes it.
+// lov: the item's first key; lo: its tile grid's start, lov rounded down to
+// 16 keys (keys lo .. lov - 1 are loaded and masked: a draft item starts at
+// the prefix length, mid-page).
 struct ItemGeo {
-  int b, h, row0, nrows, lo, hi, part_row, qo0, L, pg0, prefix, n_tiles, nq, moff;
+  int b, h, row0, nrows, lo, lov, hi, part_row, qo0, L, pg0, prefix, n_tiles, nq, moff;
   bool ok;
 };
 // One entry of the item-geometry queue: the producer decodes each item of the
@@ -138,7 +141,8 @@ __device__ __forceinline__ ItemGeo decode_item(const PartialParams& p, int i) {
   g.h = it.h;
   g.row0 = it.row0;
   g.nrows = it.nrows;
-  g.lo = it.kv_lo;
+  g.lov = it.kv_lo;
+  g.lo = it.kv_lo & ~15;
   g.hi = it.kv_hi;
   g.part_row = it.part_row;
   // a work list left in the workspace by another plan may name requests
@@ -154,7 +158,7 @@ __device__ __forceinline__ ItemGeo decode_item(const PartialParams& p, int i) {
   g.ok = g.L >= 0 && npg >= 0 && lpl >= 1 && lpl <= p.page_size && kv_len <= 0x7fffffffLL &&
          g.prefix >= 0 && g.row0 >= 0 && g.nrows > 0 && g.nrows <= BLOCK_ROWS &&
          g.row0 % BLOCK_ROWS == 0 && (long long)g.row0 + g.nrows <= (long long)p.group * g.L &&
-         g.lo >= 0 && g.lo % 16 == 0 && g.lo < g.hi && g.hi <= kv_len &&
+         g.lov >= 0 && g.lov < g.hi && g.hi <= kv_len &&
          (g.part_row < 0 || (long long)g.part_row + g.nrows <= p.part_rows);
   g.n_tiles = g.ok ? (g.hi - g.lo + KEYS - 1) / KEYS : 0;
   g.moff = g.ok && p.mask ? p.mask_indptr[g.b] : 0;
@@ -233,6 +237,10 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
     tma_prefetch_desc(&maps.q);
     tma_prefetch_desc(&maps.k);
     tma_prefetch_desc(&maps.v);
+    if (p.drafts_new) {
+      tma_prefetch_desc(&maps.kn);
+      tma_prefetch_desc(&maps.vn);
+    }
     if ((int)blockIdx.x < p.n_items) prefetch_l1(p.items + blockIdx.x);
   }
   if (tid == 0) {
@@ -342,17 +350,18 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
         };
         load_pages(0, cur);
         load_pages(1, nxt);
-        // After this library's append (early inputs), the CTA's first item
-        // issues q and its key tiles that hold prefix keys only before the
-        // dependency wait: the append writes none of them (only the drafts'
-        // slots) and releases this kernel only after its own predecessor --
-        // the producer of q -- has completed, so they stream in while the
-        // append finishes.  Tiles with draft keys wait for it.
-        bool q_sent = false;
+        // With early inputs (after this library's append, or on the caller's
+        // promise) q and the key tiles that hold prefix keys only are issued
+        // before the dependency wait: the previous grid writes none of them
+        // (the append writes only the drafts' slots, and releases this kernel
+        // only after its own predecessor -- the producer of q -- has
+        // completed), so they stream in while it finishes.  A tile with draft
+        // keys read from the pages waits for it; an item of drafts only,
+        // read from the new rows, does not.
+        const bool from_new = p.drafts_new && g.lov >= g.prefix;
         if (!issue_q()) break;
-        q_sent = true;
         for (int j = 0; live && j < g.n_tiles; ++j) {
-          if (!waited && (u + 2 > C::NSLOT || min(g.lo + (j + 1) * C::KEYS, g.hi) > g.prefix)) {
+          if (!waited && !from_new && min(g.lo + (j + 1) * C::KEYS, g.hi) > g.prefix) {
             grid_dependency_wait();
             waited = true;
           }
@@ -366,6 +375,28 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
             }
             mbar_expect_tx(bar(B_FULL + s), C::SLOT_BYTES);
             const uint32_t dst = sbase + C::OFF_RING + s * C::SLOT_BYTES;
+            if (from_new) {
+              // key k >= prefix is new row qo0 + k - prefix; rows past the item
+              // (a later request's, or past the end: zero fill) are masked, and
+              // V rows past the chunk end are zeroed like a page tile's
+              const void* nmap = v ? static_cast<const void*>(&maps.vn) : static_cast<const void*>(&maps.kn);
+              if constexpr (FP8) {
+#pragma unroll
+                for (int q = 0; q < NG; ++q) {
+                  const int key = k0 + 16 * q;
+                  const int tok = key < g.hi ? g.qo0 + key - g.prefix : p.total_qo;
+                  tma_load_3d(dst + q * 2048, nmap, 0, tok, g.h, bar(B_FULL + s));
+                }
+              } else {
+#pragma unroll
+                for (int q = 0; q < 2 * NG; ++q) {
+                  const int key = k0 + 8 * q;
+                  const int tok = key < g.hi ? g.qo0 + key - g.prefix : p.total_qo;
+                  tma_load_4d(dst + q * 2048, nmap, 0, tok, 0, g.h, bar(B_FULL + s));
+                }
+              }
+              continue;
+            }
             const void* map = v ? static_cast<const void*>(&maps.v) : static_cast<const void*>(&maps.k);
 #pragma unroll
             for (int q = 0; q < NG; ++q) {
@@ -399,7 +430,6 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
           }
         }
         if (!live) break;
-        (void)q_sent;
         ++nit;
       }
       // A CTA that met no valid item still waits once, so that this grid's
@@ -881,6 +911,9 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
         // (prefix 1, drafts from the row's mask bits, nothing at or past hi).
         // A tile every row of the warp sees whole skips the per-key selects.
         const int lim = min(hi, prefix + t + 1) - k0;
+        // keys of the item's first tile below its first key (0 .. 15 of them)
+        const int lowcut = g.lov - k0;
+        const uint32_t lowmask = lowcut > 0 ? ~((1u << lowcut) - 1u) : 0xffffffffu;
         uint32_t vis[C::KEYS / 32];
         bool full;
         if (!p.mask) {
@@ -907,6 +940,8 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
           full = __all_sync(0xffffffffu, all == 0xffffffffu);
         } else if (k0 + C::KEYS <= prefix && k0 + C::KEYS <= hi) {
           full = true;
+#pragma unroll
+          for (int q = 0; q < C::KEYS / 32; ++q) vis[q] = 0xffffffffu;
         } else {
           uint32_t all = 0xffffffffu;
 #pragma unroll
@@ -944,11 +979,16 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
           }
           full = __all_sync(0xffffffffu, all == 0xffffffffu);
         }
+        if (lowcut > 0) {  // uniform over the item
+          full = false;
+          if (p.mask) vis[0] &= lowmask;
+        }
         // Keys 32 q .. 32 q + 31 of the tile this row may see, one bit each.
         auto vis_word = [&](int q) -> uint32_t {
           if (!p.mask) {
             const int n = lim - 32 * q;
-            return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+            const uint32_t w = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+            return q == 0 ? w & lowmask : w;
           }
           return q == 0 ? vis[0] : q == 1 ? vis[1] : q == 2 ? vis[2] : vis[3];
         };

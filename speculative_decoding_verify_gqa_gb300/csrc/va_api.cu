@@ -173,7 +173,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // TMA descriptors of the tensor-core variant (see TcMaps).
 int make_tc_maps(const void* q, int64_t total_qo, const void* k_cache, const void* v_cache,
-                 int num_pages, const PlanHeader* hd, TcMaps* m) {
+                 int num_pages, const PlanHeader* hd, const void* k_new, const void* v_new,
+                 TcMaps* m) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return VA_ERR_CUDA;
   const int G = hd->group, D = hd->head_dim, P = hd->page_size;
@@ -235,6 +236,33 @@ int make_tc_maps(const void* q, int64_t total_qo, const void* k_cache, const voi
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return VA_ERR_CUDA;
   }
+  // the new rows [total_qo, h_kv, D] (see TcMaps)
+  const void* nsrc[2] = {k_new, v_new};
+  CUtensorMap* ndst[2] = {&m->kn, &m->vn};
+  for (int i = 0; i < 2; ++i) {
+    if (!nsrc[i]) {
+      memset(ndst[i], 0, sizeof(CUtensorMap));
+      continue;
+    }
+    CUresult r;
+    if (!fp8) {
+      cuuint64_t nd[4] = {64, (cuuint64_t)total_qo, 2, H};
+      cuuint64_t ns[3] = {H * D * 2, 128, (cuuint64_t)D * 2};
+      cuuint32_t nb[4] = {64, 8, 2, 1};
+      r = enc(ndst[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(nsrc[i]), nd, ns, nb,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+      cuuint64_t nd[3] = {(cuuint64_t)D, (cuuint64_t)total_qo, H};
+      cuuint64_t ns[2] = {H * D, (cuuint64_t)D};
+      cuuint32_t nb[3] = {128, 16, 1};
+      r = enc(ndst[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(nsrc[i]), nd, ns, nb, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE,
+              (hd->flags & kPlanF8Mma) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return VA_ERR_CUDA;
+  }
   return VA_OK;
 }
 
@@ -278,7 +306,8 @@ static int run_partial(const void* q, const void* k_cache, const void* v_cache,
                            int num_kv_heads, int head_dim, int page_size, float sm_scale,
                            float k_scale, float v_scale, void* out, float* lse, int num_pages,
                            const void* plan_h, void* workspace_d, size_t workspace_bytes,
-                           const va_run_options_t* options, int early, void* stream) {
+                           const va_run_options_t* options, int early, void* stream,
+                           const void* k_new = nullptr, const void* v_new = nullptr) {
   const PlanHeader* hd = nullptr;
   int rc = check_run(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
                      mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size, &sm_scale,
@@ -290,10 +319,16 @@ static int run_partial(const void* q, const void* k_cache, const void* v_cache,
                                  qo_indptr, mask, mask_indptr, sm_scale, k_scale, v_scale, out,
                                  lse, num_pages, hd, workspace_d, options);
   p.early_inputs = early;
+  p.total_qo = (int)hd->total_qo;
   cudaError_t e;
   if (kernel_is_tc(hd->kernel)) {
+    // draft items read the new rows only when they are given (a plain copy
+    // append in the same call) and every split holds them apart
+    const bool from_new = k_new && v_new;
+    p.drafts_new = from_new ? 1 : 0;
     TcMaps maps;
-    rc = make_tc_maps(q, hd->total_qo, k_cache, v_cache, num_pages, hd, &maps);
+    rc = make_tc_maps(q, hd->total_qo, k_cache, v_cache, num_pages, hd,
+                      from_new ? k_new : nullptr, from_new ? v_new : nullptr, &maps);
     if (rc) return rc;
     e = launch_partial_tc(p, maps, hd->kv_dtype == VA_DTYPE_FP8_E4M3, hd->block_rows, hd->n_items,
                           (hd->flags & kPlanF8Mma) != 0,
@@ -677,10 +712,13 @@ int verify_attn_append_run(const void* k_new, const void* v_new,
                      (va_dtype)hd->kv_dtype, hd->total_qo, append_options, status, early, stream);
     if (rc) return rc;
   }
+  // A plain copy (no quantisation, no rotation) stores exactly the bytes of
+  // k_new / v_new: the attention may read the drafts from there.
+  const bool plain = !append_options || (!append_options->quantize && !append_options->positions);
   rc = run_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
                    mask_indptr, num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale, k_scale,
                    v_scale, out, lse, num_pages, plan_h, workspace_d, workspace_bytes, run_options,
-                   1, stream);
+                   1, stream, plain ? k_new : nullptr, plain ? v_new : nullptr);
   if (rc) return rc;
   return verify_attn_merge_impl(qo_indptr, num_qo_heads, num_kv_heads, head_dim, out, lse, plan_h,
                                 workspace_d, workspace_bytes, 1, stream);

@@ -48,6 +48,10 @@ struct PartialParams {
                               // wait for the previous grid (this library's append, released
                               // once q's producer is done, or a caller's early-reads promise)
   RopeFreq rope;              // frequencies when q_position is set
+  int drafts_new;             // tcgen05 variants: an item of drafts only (kv_lo >= prefix)
+                              // reads its keys and values from the new rows (TcMaps kn / vn,
+                              // [total_qo, h_kv, D] in the cache dtype) instead of the pages
+  int total_qo;               // rows of q (and of the new K / V)
 };
 
 struct MergeParams {
@@ -144,8 +148,14 @@ cudaError_t launch_partial_mma(const PartialParams& p, int kernel, int head_dim,
 // 4-D view [num_pages, h_kv, P, 128] with 128 x 16 x 1 x 1 boxes (no swizzle).
 // Zero fill out of bounds.  With e4m3 MMAs (plan option q_fp8) the fp8
 // boxes land with 128-byte swizzle, as the MMA operands.
+//
+// kn / vn (drafts_new): the new K / V rows [total_qo, h_kv, D].  bf16: 4-D
+// [total_qo][half][h_kv] x 64 with 64 x 8 x 2 x 1 boxes and 128-byte swizzle,
+// one box per 8 tokens landing as one 8-key group [half][8][128 bytes] of the
+// page tiles' layout; fp8: 3-D [total_qo][h_kv] x 128 with 128 x 16 x 1
+// boxes, one per 16 tokens, swizzled as the fp8 page boxes.
 struct TcMaps {
-  CUtensorMap q, k, v;
+  CUtensorMap q, k, v, kn, vn;
 };
 cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, bool kv_fp8,
                               int block_rows, int n_items, bool f8mma, cudaStream_t stream);

@@ -60,11 +60,13 @@ int plan_bounds(int batch, int64_t total_qo, int num_qo_heads, int num_kv_heads,
   // Units: a request's G * L_b rows in blocks of >= 64 rows, per KV head.
   int64_t units = ceil_div((int64_t)num_qo_heads * total_qo, 64) + (int64_t)num_kv_heads * batch;
   int64_t target = (int64_t)kMaxTargetPerSm * num_sms;
-  // sum_u ceil(kv_end_u / C) <= W / C + units <= target + units.
-  int64_t items = target + units;
+  // sum_u ceil(kv_end_u / C) <= W / C + units <= target + units, plus at most
+  // one draft item per unit.
+  int64_t items = target + 2 * units;
   // Split units hold kv_end > C keys, so their split counts total < 2 W / C
-  // <= 2 target, each with at most the largest block's rows (256).
-  int64_t part_rows = 256 * 2 * target;
+  // <= 2 target (3 target with a draft item each: n + 1 <= 1.5 n for n >= 2),
+  // each with at most the largest block's rows (256).
+  int64_t part_rows = 256 * 3 * target;
   size_t pb = sizeof(PlanHeader) + (size_t)(items + units) * 32;
   size_t ws = kWsAlign + (size_t)(items + units) * 32;
   ws = align_up(ws, kWsAlign) + (size_t)part_rows * 4;
@@ -93,6 +95,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     return VA_ERR_INVALID_ARGUMENT;
   const bool full_mask = o.mask_layout == VA_MASK_FULL;
   if (o.q_fp8 != 0 && o.q_fp8 != 1) return VA_ERR_INVALID_ARGUMENT;
+  if (o.draft_items < -1 || o.draft_items > 1) return VA_ERR_INVALID_ARGUMENT;
   if (o.q_fp8 && kv_dtype != VA_DTYPE_FP8_E4M3) return VA_ERR_UNSUPPORTED;
   if (full_mask && !has_mask) return VA_ERR_INVALID_ARGUMENT;
   if (o.kernel != VA_KERNEL_AUTO && o.kernel != VA_KERNEL_MMA_64 && o.kernel != VA_KERNEL_MMA_128 &&
@@ -290,9 +293,40 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   std::vector<MergeItem> merges;
   int64_t part_rows = 0;
   std::vector<int64_t> cuts;
+  // Draft items: with few units next to the CTAs (the latency-bound verify
+  // shapes, whose units are split many ways), a split unit's drafts -- keys
+  // prefix .. kv_end, at most one key tile -- become an item of their own,
+  // which the fused append + attention call can serve from the new rows
+  // while the append runs.
+  const int64_t all_heads = (int64_t)units.size() * num_kv_heads;
+  const bool draft_items =
+      kernel_is_tc(kernel) && (o.draft_items == 1 || (o.draft_items == 0 && 2 * all_heads <= slots));
   for (const Unit& u : units) {
     int64_t cu;
     int64_t n = split_of(u, chunk, equal, &cu);
+    const int64_t pre = prefix[u.b];
+    if (draft_items && n > 1 && pre > 0 && u.kv_end > pre && u.kv_end - pre <= TK) {
+      // the prefix cut as before (a short last prefix chunk joins the one
+      // before it), then the drafts alone
+      cuts.assign(1, 0);
+      for (int64_t s = 1; s * cu < pre; ++s) cuts.push_back(s * cu);
+      if (cuts.size() > 1 && pre - cuts.back() < TK) cuts.pop_back();
+      cuts.push_back(pre);
+      cuts.push_back(u.kv_end);
+      n = (int64_t)cuts.size() - 1;
+      for (int h = 0; h < num_kv_heads; ++h) {
+        const int64_t base = part_rows;
+        merges.push_back({u.b, h, u.row0, u.nrows, (int32_t)base, (int32_t)n, 0, 0});
+        part_rows += n * u.nrows;
+        for (int64_t s = 0; s < n; ++s) {
+          const int64_t lo = cuts[s], hi = cuts[s + 1];
+          WorkItem w{u.b, h, u.row0, u.nrows, (int32_t)lo, (int32_t)hi,
+                     (int32_t)(base + s * u.nrows), -1};
+          items.push_back({w, (hi - lo) * (int64_t)(u.nrows + 16)});
+        }
+      }
+      continue;
+    }
     // Chunk boundaries: multiples of the chunk size from the front.  For
     // the tcgen05 kernels a last chunk shorter than one key tile joins the
     // one before it: the tail of a request (its drafts, appended in the same

@@ -83,7 +83,11 @@ def _check_cover(va, t, plan):
         b, h, row0, nrows, lo, hi, part_row, _ = (int(x) for x in it)
         assert 0 <= b < len(t["L"]) and 0 <= h < t["h_kv"]
         assert 0 < nrows <= BM and row0 % BM == 0
-        assert lo % 64 == 0 and lo < hi
+        # chunks start on key tiles; a draft item (tcgen05 variants) starts
+        # at the request's prefix length and holds at most one key tile
+        assert lo < hi
+        assert lo % 64 == 0 or (lo == int(t["prefix"][b]) and hd["kernel"] in (3, 4)
+                                and hi - lo <= 128)
         units.setdefault((b, h, row0, nrows), []).append((lo, hi, part_row))
     for b in range(len(t["L"])):
         R = G * int(t["L"][b])
@@ -215,6 +219,41 @@ def test_plans_of_the_named_workloads(va, name):
         assert hd["kernel"] == (4 if rows > 128 else 3)
     else:
         assert hd["kernel"] == (1 if rows <= 64 else 2)
+
+
+@pytest.mark.parametrize("draft_items", [0, 1, -1])
+def test_draft_items(va, draft_items):
+    """Draft items: with few split units (the Llama-3-8B tree: 8 KV heads,
+    each split many ways) every split unit's drafts -- keys prefix .. kv_len
+    -- form one item of their own, merged with the prefix chunks; never for
+    the warp-level variants or when turned off."""
+    wl = synthetic.make_workload("llama3_8b_tree_verify", with_values=False)
+    t = dict(masked=True, prefix=wl.prefix_lens, L=wl.qo_lens, G=wl.group, h_kv=wl.h_kv)
+    pre, kv = int(wl.prefix_lens[0]), int(wl.kv_lens[0])
+    for kernel in (0, 2):
+        plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
+                                        wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                        num_sms=152, kernel=kernel, draft_items=draft_items)
+        _check_cover(va, t, plan)
+        drafts = [it for it in plan.items() if int(it[4]) == pre]
+        if kernel == 0 and draft_items >= 0:
+            assert len(drafts) == wl.h_kv
+            assert all(int(it[5]) == kv and int(it[6]) >= 0 for it in drafts)
+            # the chunk before the drafts ends at the prefix
+            assert sum(1 for it in plan.items() if int(it[5]) == pre) == wl.h_kv
+        elif kernel == 0:
+            assert not drafts   # the 17 drafts join the last prefix chunk
+    # many split units (the batched chain): none unless forced
+    wl = synthetic.make_workload("codellama34b_chain_verify", with_values=False)
+    plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, None, wl.h_q,
+                                    wl.h_kv, wl.d, wl.page_size, num_sms=152,
+                                    draft_items=draft_items)
+    t = dict(masked=False, prefix=wl.prefix_lens, L=wl.qo_lens, G=wl.group, h_kv=wl.h_kv)
+    _check_cover(va, t, plan)
+    n_drafts = sum(1 for it in plan.items() if int(it[4]) == int(wl.prefix_lens[int(it[0])])
+                   and int(it[4]) % 64)
+    assert (n_drafts > 0) == (draft_items == 1)
+    assert _plan_rc(va, [0, 2], [0, 3], [5], None, draft_items=2) == -1
 
 
 @pytest.mark.parametrize("name", ["gqa_varlen_prefill", "wide_tree_fp8_verify",

@@ -10,6 +10,7 @@ import torch
 import oracle
 import synthetic
 from gpu_util import DeviceWorkload, compare, to_dev
+from test_fp8_mma_gpu import check as check_e4m3
 
 pytestmark = pytest.mark.gpu
 
@@ -305,6 +306,64 @@ def test_append_run_features_match_oracle(va, case):
     torch.cuda.synchronize()
     assert va.verify_attn_device_status(plan) == 0
     compare(wl, out, lse)
+
+
+@pytest.mark.parametrize("kernel", [3, 4], ids=["tc128", "tc256"])
+@pytest.mark.parametrize("case", [
+    dict(prefix=("fixed", [37, 700, 0, 2048]), qo=("fixed", [17, 5, 9, 64]), mask="tree"),
+    dict(prefix=("fixed", [130, 16, 1000]), qo=("fixed", [3, 1, 8]), mask="causal"),
+    dict(prefix=("fixed", [301, 77]), qo=("fixed", [20, 33]), mask="tree", kv_dtype=synthetic.FP8),
+    dict(prefix=("fixed", [301, 77]), qo=("fixed", [20, 33]), mask="tree", kv_dtype=synthetic.FP8,
+         q_fp8=True),
+    dict(prefix=("fixed", [500, 63]), qo=("fixed", [12, 40]), mask="tree", kv_layout="nhd"),
+    dict(prefix=("fixed", [500, 63]), qo=("fixed", [12, 40]), mask="random", mask_layout="full",
+         prefix_visible="random"),
+], ids=["tree_unaligned", "chain", "fp8_tree", "fp8_e4m3_mma", "nhd", "full_mask"])
+def test_append_run_draft_items(va, kernel, case):
+    """Draft items (plan option draft_items = 1: each split request's drafts
+    an item of their own, starting at the prefix length, mid-page) through
+    the fused call, which reads them from k_new / v_new and not from the
+    pages: first on a pool whose draft slots still hold NaN, then again on
+    the appended pool; every row against the oracle and the pool equal to the
+    oracle's bit for bit.  Also through verify_attn_run (the drafts read from
+    the pages)."""
+    case = dict(case)
+    q_fp8 = case.pop("q_fp8", False)
+    wl = synthetic.make_custom(batch=len(case["prefix"][1]), h_q=16, h_kv=2, d=128, seed=131,
+                               **case)
+    dw = DeviceWorkload(wl, append=False)
+    fp8 = wl.kv_dtype == synthetic.FP8
+    raw = np.uint8 if fp8 else np.int16
+    # the prefixes only, through a table whose kv_len is the prefix length
+    pre = np.concatenate([np.arange(wl.tok_indptr[b], wl.tok_indptr[b + 1] - wl.qo_lens[b])
+                          for b in range(wl.batch)]).astype(np.int64)
+    pre_indptr = np.concatenate([[0], np.cumsum(wl.prefix_lens)]).astype(np.int32)
+    pages = (wl.prefix_lens + wl.page_size - 1) // wl.page_size
+    kvp = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    idx = np.concatenate([wl.kv_indices[wl.kv_indptr[b]:wl.kv_indptr[b] + pages[b]]
+                          for b in range(wl.batch)]).astype(np.int32)
+    lpl = np.array([int(n) - (int(p) - 1) * wl.page_size if p > 0 else 0
+                    for n, p in zip(wl.prefix_lens, pages)], np.int32)
+    va.paged_kv_append(to_dev(wl.k_tok[pre].view(raw), "cuda", dw.kvd),
+                       to_dev(wl.v_tok[pre].view(raw), "cuda", dw.kvd), to_dev(pre_indptr, "cuda"),
+                       to_dev(kvp, "cuda"), to_dev(idx, "cuda"), to_dev(lpl, "cuda"), dw.k_cache,
+                       dw.v_cache, kv_layout=wl.kv_layout)
+    plan = dw.plan(kernel=kernel, draft_items=1, target_ctas=64, min_chunk=128, q_fp8=q_fp8)
+    items = plan.items()
+    assert any(int(it[4]) == int(wl.prefix_lens[int(it[0])]) and int(it[4]) % 16 for it in items)
+    kc, vc = oracle.build_cache(wl)
+    cmp = (lambda o, l: check_e4m3(wl, o, l, caches=(kc, vc))) if q_fp8 else \
+          (lambda o, l: compare(wl, o, l, caches=(kc, vc)))
+    for call in range(2):
+        out, lse = _fused(va, dw, plan, early_reads=bool(call))
+        torch.cuda.synchronize()
+        assert va.verify_attn_device_status(plan) == 0
+        assert np.array_equal(_raw(dw.k_cache, fp8), kc) and np.array_equal(_raw(dw.v_cache, fp8), vc)
+        cmp(out, lse)
+    out, lse, _ = dw.run(plan=plan)
+    torch.cuda.synchronize()
+    assert va.verify_attn_device_status(plan) == 0
+    cmp(out, lse)
 
 
 def test_append_run_quantises_fresh_drafts(va):
