@@ -95,6 +95,17 @@ def _load():
                                               dbl, P, i64, P, P, i32]
         lib.oracle_quantize_q_e4m3.restype = ctypes.c_float
         lib.oracle_quantize_q_e4m3.argtypes = [P, i32, P]
+        lib.oracle_verify_attn_dv.restype = i32
+        lib.oracle_verify_attn_dv.argtypes = [P, P, P, i32, i32, P, P, P, P, P, P, i32, P, dbl,
+                                              dbl, i32, i32, i32, i32, i32, i32, i32, i32, dbl,
+                                              dbl, dbl, P, i64, P, P, i32]
+        lib.oracle_paged_kv_append_dv.restype = i32
+        lib.oracle_paged_kv_append_dv.argtypes = [P, P, i32, i32, ctypes.c_float, ctypes.c_float,
+                                                  i32, P, dbl, dbl, P, P, P, P, i32, i32, i32,
+                                                  i32, i32, i32, P, P]
+        lib.oracle_dense_attention_dv.restype = None
+        lib.oracle_dense_attention_dv.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, i64, P,
+                                                  dbl, P, P, P]
         _lib = lib
         return lib
 
@@ -125,15 +136,20 @@ def decode_e4m3(bits) -> np.ndarray:
 
 def dense_attention(Q, K, V, M, scale):
     """softmax(scale * Q K^T + M) V and its natural-log LSE, row by row, in fp64.
-    Q [n, d], K/V [m, d], M [n, m] additive."""
+    Q [n, d], K [m, d], V [m, dv], M [n, m] additive; out [n, dv]."""
     lib = _load()
     Q = _c(Q, np.float64); K = _c(K, np.float64); V = _c(V, np.float64); M = _c(M, np.float64)
     n, d = Q.shape
     m = K.shape[0]
-    out = np.zeros((n, d)); lse = np.zeros(n)
+    dv = V.shape[1]
+    out = np.zeros((n, dv)); lse = np.zeros(n)
     s = np.zeros(max(m, 1))
-    lib.oracle_dense_attention(n, m, d, _p(Q), d, _p(K), _p(V), d, _p(M), float(scale),
-                               _p(out), _p(lse), _p(s))
+    if dv == d:
+        lib.oracle_dense_attention(n, m, d, _p(Q), d, _p(K), _p(V), d, _p(M), float(scale),
+                                   _p(out), _p(lse), _p(s))
+    else:
+        lib.oracle_dense_attention_dv(n, m, d, dv, _p(Q), d, _p(K), d, _p(V), dv, _p(M),
+                                      float(scale), _p(out), _p(lse), _p(s))
     return out, lse
 
 
@@ -168,10 +184,13 @@ def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_le
 def verify_attn_ex(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_len,
                    qo_indptr, mask, mask_indptr, h_q, h_kv, d, page_size, num_pages, sm_scale,
                    k_scale=1.0, v_scale=1.0, kv_layout=0, mask_layout=0, q_pos=None,
-                   rope_theta=0.0, rope_scale=1.0, q_fp8=False, rows=None, nthreads=None):
+                   rope_theta=0.0, rope_scale=1.0, q_fp8=False, rows=None, nthreads=None,
+                   dv=None):
     """verify_attn with the cache layout (0 HND, 1 NHD), the mask layout (0:
-    L x L draft blocks, 1: L x kv_len rows) and optional query positions for
-    the rotary embedding of the queries (the cache holds keys as stored)."""
+    L x L draft blocks, 1: L x kv_len rows), optional query positions for
+    the rotary embedding of the queries (the cache holds keys as stored) and
+    value rows of dv elements (default d); out rows hold dv elements."""
+    dv = d if dv is None else int(dv)
     lib = _load()
     q = _c(q, np.uint16)
     kc = _c(k_cache, np.uint8 if kv_fp8 else np.uint16)
@@ -184,17 +203,16 @@ def verify_attn_ex(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page
     total_qo = int(qo_indptr[-1])
     sel = _c(rows, np.int32)
     n = total_qo * h_q if sel is None else len(sel)
-    out = np.zeros((max(n, 1), d)); lse = np.zeros(max(n, 1))
-    rc = lib.oracle_verify_attn_ex(_p(q), _p(kc), _p(vc), int(bool(kv_fp8)), int(kv_layout),
+    out = np.zeros((max(n, 1), dv)); lse = np.zeros(max(n, 1))
+    rc = lib.oracle_verify_attn_dv(_p(q), _p(kc), _p(vc), int(bool(kv_fp8)), int(kv_layout),
                                    _p(kv_indptr), _p(kv_indices), _p(last_page_len),
                                    _p(qo_indptr), _p(mask), _p(mask_indptr), int(mask_layout),
                                    _p(q_pos), float(rope_theta), float(rope_scale), int(bool(q_fp8)),
-                                   batch, h_q,
-                                   h_kv, d, page_size, num_pages, float(sm_scale),
+                                   batch, h_q, h_kv, d, dv, page_size, num_pages, float(sm_scale),
                                    float(k_scale), float(v_scale), _p(sel), int(n), _p(out),
                                    _p(lse), int(nthreads or default_threads()))
     if rc != 0:
-        raise ValueError("oracle_verify_attn_ex rejected its inputs (status %d)" % rc)
+        raise ValueError("oracle_verify_attn_dv rejected its inputs (status %d)" % rc)
     return out[:n], lse[:n]
 
 
@@ -245,16 +263,17 @@ def paged_kv_append_ex(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_
         h_kv, d = k_cache.shape[2], k_cache.shape[3]
     else:
         h_kv, d = k_cache.shape[1], k_cache.shape[3]
+    dv = v_cache.shape[3]   # value rows may be narrower or wider than key rows
     idx = [_c(a, np.int32) for a in (append_indptr, kv_indptr, kv_indices, last_page_len)]
     pos = _c(positions, np.int32)
-    rc = lib.oracle_paged_kv_append_ex(_p(k_new), _p(v_new), int(bool(cache_fp8)),
+    rc = lib.oracle_paged_kv_append_dv(_p(k_new), _p(v_new), int(bool(cache_fp8)),
                                        int(bool(quantize)), float(k_scale), float(v_scale),
                                        int(kv_layout), _p(pos), float(rope_theta),
                                        float(rope_scale), *[_p(a) for a in idx],
-                                       len(idx[0]) - 1, h_kv, d, page_size, num_pages,
+                                       len(idx[0]) - 1, h_kv, d, dv, page_size, num_pages,
                                        _p(k_cache), _p(v_cache))
     if rc != 0:
-        raise ValueError("oracle_paged_kv_append_ex rejected its inputs (status %d)" % rc)
+        raise ValueError("oracle_paged_kv_append_dv rejected its inputs (status %d)" % rc)
 
 
 def attn_range(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_len, qo_indptr,
@@ -343,8 +362,8 @@ def build_cache(wl):
     workload uses rotary positions)."""
     import synthetic
     kc = synthetic.sentinel_pool(wl)
-    vc = synthetic.sentinel_pool(wl)
-    if not wl.nhd and wl.kv_pos is None:
+    vc = synthetic.sentinel_pool(wl, values=True)
+    if not wl.nhd and wl.kv_pos is None and wl.dv == wl.d:
         paged_kv_append(wl.k_tok, wl.v_tok, wl.tok_append_indptr(), wl.kv_indptr, wl.kv_indices,
                         wl.last_page_len, wl.page_size, wl.num_pages, kc, vc)
         return kc, vc
@@ -357,7 +376,7 @@ def build_cache(wl):
 
 def verify_attn_workload(wl, rows=None, nthreads=None, caches=None, q_fp8=False):
     kc, vc = caches if caches is not None else build_cache(wl)
-    if not wl.nhd and wl.mask_layout == "qlen" and wl.q_pos is None and not q_fp8:
+    if not wl.nhd and wl.mask_layout == "qlen" and wl.q_pos is None and not q_fp8 and wl.dv == wl.d:
         return verify_attn(wl.q, kc, vc, wl.kv_dtype == "fp8_e4m3", wl.kv_indptr, wl.kv_indices,
                            wl.last_page_len, wl.qo_indptr, wl.mask, wl.mask_indptr, wl.h_q,
                            wl.h_kv, wl.d, wl.page_size, wl.num_pages, wl.sm_scale, wl.k_scale,
@@ -368,4 +387,4 @@ def verify_attn_workload(wl, rows=None, nthreads=None, caches=None, q_fp8=False)
                           wl.v_scale, kv_layout=1 if wl.nhd else 0,
                           mask_layout=1 if wl.mask_layout == "full" else 0, q_pos=wl.q_pos,
                           rope_theta=wl.rope_theta or 0.0, q_fp8=q_fp8, rows=rows,
-                          nthreads=nthreads)
+                          nthreads=nthreads, dv=wl.dv)

@@ -54,7 +54,8 @@ def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_le
     """kv_layout 1: the cache is [pages, page_size, h_kv, d]; mask_layout 1:
     request b's mask is L rows of kv_len bits (prefix included); q_pos: each
     query row is rotated at its token's position and rounded to bf16 before
-    the dot products."""
+    the dot products.  The value rows' width is v_cache's last axis (it may
+    differ from d); out rows have that width."""
     qd = _decode(q, False)
     kd = _decode(k_cache, kv_fp8)
     vd = _decode(v_cache, kv_fp8)
@@ -62,8 +63,9 @@ def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_le
         kd = kd.transpose(0, 2, 1, 3)
         vd = vd.transpose(0, 2, 1, 3)
     G = h_q // h_kv
+    dv = vd.shape[-1]
     total = int(qo_indptr[-1])
-    out = np.zeros((total * h_q, d))
+    out = np.zeros((total * h_q, dv))
     lse = np.zeros(total * h_q)
     for b in range(len(qo_indptr) - 1):
         npg = int(kv_indptr[b + 1] - kv_indptr[b])
@@ -98,7 +100,7 @@ def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_le
                     dot = math.fsum(qrow[e] * float(kd[page, h, slot, e]) * k_scale
                                     for e in range(d))
                     logits.append(sm_scale * dot)
-                    values.append([float(vd[page, h, slot, e]) * v_scale for e in range(d)])
+                    values.append([float(vd[page, h, slot, e]) * v_scale for e in range(dv)])
                 row = tok * h_q + qh
                 if not logits:
                     lse[row] = -math.inf
@@ -107,6 +109,6 @@ def verify_attn(q, k_cache, v_cache, kv_fp8, kv_indptr, kv_indices, last_page_le
                 l = mx + math.log(math.fsum(math.exp(s - mx) for s in logits))
                 lse[row] = l
                 w = [math.exp(s - l) for s in logits]
-                for e in range(d):
+                for e in range(dv):
                     out[row, e] = math.fsum(w[j] * values[j][e] for j in range(len(w)))
     return out, lse

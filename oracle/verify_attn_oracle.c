@@ -206,25 +206,27 @@ static int check_tables(const int32_t* kv_indptr, const int32_t* kv_indices,
  * out[r][e] = sum_j softmax_j(scale * Q[r].K[j] + M[r][j]) * V[j][e],
  * lse[r] = ln sum_j exp(scale * Q[r].K[j] + M[r][j]).
  * Q row stride q_ld, K / V row stride kv_ld (in doubles).  A row whose every
- * entry is masked gets lse = -inf and out = 0.
+ * entry is masked gets lse = -inf and out = 0.  The _dv form takes values of
+ * dv elements (sglang's value head size, which may differ from the key's d)
+ * and separate K and V row strides; out rows then hold dv elements.
  */
-void oracle_dense_attention(int n_rows, int n_keys, int d, const double* Q, int64_t q_ld,
-                            const double* K, const double* V, int64_t kv_ld,
-                            const double* M, double scale, double* out, double* lse,
-                            double* s_scratch) {
+void oracle_dense_attention_dv(int n_rows, int n_keys, int d, int dv, const double* Q,
+                               int64_t q_ld, const double* K, int64_t k_ld, const double* V,
+                               int64_t v_ld, const double* M, double scale, double* out,
+                               double* lse, double* s_scratch) {
     for (int r = 0; r < n_rows; ++r) {
         const double* qr = Q + (int64_t)r * q_ld;
         double mx = -INFINITY;
         for (int j = 0; j < n_keys; ++j) {
-            const double* kj = K + (int64_t)j * kv_ld;
+            const double* kj = K + (int64_t)j * k_ld;
             double dot = 0.0;
             for (int e = 0; e < d; ++e) dot += qr[e] * kj[e];
             double s = scale * dot + M[(int64_t)r * n_keys + j];
             s_scratch[j] = s;
             if (s > mx) mx = s;
         }
-        double* o = out + (int64_t)r * d;
-        for (int e = 0; e < d; ++e) o[e] = 0.0;
+        double* o = out + (int64_t)r * dv;
+        for (int e = 0; e < dv; ++e) o[e] = 0.0;
         if (mx == -INFINITY) {
             lse[r] = -INFINITY;
             continue;
@@ -236,10 +238,18 @@ void oracle_dense_attention(int n_rows, int n_keys, int d, const double* Q, int6
         for (int j = 0; j < n_keys; ++j) {
             double p = exp(s_scratch[j] - l);
             if (p == 0.0) continue;
-            const double* vj = V + (int64_t)j * kv_ld;
-            for (int e = 0; e < d; ++e) o[e] += p * vj[e];
+            const double* vj = V + (int64_t)j * v_ld;
+            for (int e = 0; e < dv; ++e) o[e] += p * vj[e];
         }
     }
+}
+
+void oracle_dense_attention(int n_rows, int n_keys, int d, const double* Q, int64_t q_ld,
+                            const double* K, const double* V, int64_t kv_ld,
+                            const double* M, double scale, double* out, double* lse,
+                            double* s_scratch) {
+    oracle_dense_attention_dv(n_rows, n_keys, d, d, Q, q_ld, K, kv_ld, V, kv_ld, M, scale, out,
+                              lse, s_scratch);
 }
 
 /* Row index of (page, head, slot) in a cache of the given layout: HND
@@ -250,22 +260,22 @@ static int64_t cache_row(int layout, int64_t page, int h, int64_t slot, int h_kv
     return (page * h_kv + h) * page_size + slot;
 }
 
-/* Gather request b's K and V into [kv_len][h_kv][d] doubles (decoded and
- * scaled), walking its pages in order and stopping at kv_len. */
+/* Gather request b's K into [kv_len][h_kv][d] and V into [kv_len][h_kv][dv]
+ * doubles (decoded and scaled), walking its pages in order and stopping at
+ * kv_len; the V cache's rows hold dv elements. */
 static void gather_request(const void* k_cache, const void* v_cache, int kv_fp8, int layout,
                            const int32_t* kv_indptr, const int32_t* kv_indices, int b,
-                           int64_t kv_len, int h_kv, int d, int page_size, double k_scale,
-                           double v_scale, double* K, double* V) {
+                           int64_t kv_len, int h_kv, int d, int dv, int page_size,
+                           double k_scale, double v_scale, double* K, double* V) {
     for (int64_t j = 0; j < kv_len; ++j) {
         int32_t page = kv_indices[kv_indptr[b] + j / page_size];
         int64_t slot = j % page_size;
         for (int h = 0; h < h_kv; ++h) {
-            int64_t src = cache_row(layout, page, h, slot, h_kv, page_size) * d;
-            int64_t dst = (j * h_kv + h) * d;
-            for (int e = 0; e < d; ++e) {
-                K[dst + e] = decode_kv(k_cache, src + e, kv_fp8) * k_scale;
-                V[dst + e] = decode_kv(v_cache, src + e, kv_fp8) * v_scale;
-            }
+            int64_t row = cache_row(layout, page, h, slot, h_kv, page_size);
+            for (int e = 0; e < d; ++e)
+                K[(j * h_kv + h) * d + e] = decode_kv(k_cache, row * d + e, kv_fp8) * k_scale;
+            for (int e = 0; e < dv; ++e)
+                V[(j * h_kv + h) * dv + e] = decode_kv(v_cache, row * dv + e, kv_fp8) * v_scale;
         }
     }
 }
@@ -307,7 +317,7 @@ typedef struct {
     const double* V;
     const double* M;
     int64_t kv_len, L, qo_start;
-    int h_q, h_kv, d, group;
+    int h_q, h_kv, d, dv, group;
     double sm_scale;
     const int32_t* q_pos;  /* NULL: no rotary embedding of the queries */
     int q_fp8;             /* 1: the row is replaced by its e4m3 quantisation */
@@ -356,11 +366,11 @@ static void* run_rows(void* arg) {
         }
         /* One query row against the request's keys of KV head h: K/V rows are
          * [j][h][:] so the row stride is h_kv * d and the base is offset by h. */
-        oracle_dense_attention(1, (int)jb->kv_len, jb->d, qrow, jb->d,
-                               jb->K + (int64_t)h * jb->d, jb->V + (int64_t)h * jb->d,
-                               (int64_t)jb->h_kv * jb->d, jb->M + t * jb->kv_len,
-                               jb->sm_scale, jb->out + jb->dest[i] * jb->d,
-                               jb->lse + jb->dest[i], s);
+        oracle_dense_attention_dv(1, (int)jb->kv_len, jb->d, jb->dv, qrow, jb->d,
+                                  jb->K + (int64_t)h * jb->d, (int64_t)jb->h_kv * jb->d,
+                                  jb->V + (int64_t)h * jb->dv, (int64_t)jb->h_kv * jb->dv,
+                                  jb->M + t * jb->kv_len, jb->sm_scale,
+                                  jb->out + jb->dest[i] * jb->dv, jb->lse + jb->dest[i], s);
     }
     free(s);
     free(qrow);
@@ -382,22 +392,24 @@ static void* run_rows(void* arg) {
  *  q_fp8    1: each query row (after any rotation) is replaced by its e4m3
  *           quantisation (oracle_quantize_q_e4m3: codes times the row scale),
  *           the operand of the e4m3 tensor-core path
+ *  dv       elements of a value row (v_cache rows and out rows), which may
+ *           differ from the key's d
  *  sel / n_sel: flat row ids token * h_q + head to compute (NULL = all rows,
- *           in flat order); out [n, d] and lse [n] follow the selection order.
+ *           in flat order); out [n, dv] and lse [n] follow the selection order.
  *  nthreads: worker threads (>= 1).
  * Returns 0, or a negative code on an inconsistent page table.
  */
-int oracle_verify_attn_ex(const uint16_t* q, const void* k_cache, const void* v_cache,
+int oracle_verify_attn_dv(const uint16_t* q, const void* k_cache, const void* v_cache,
                           int kv_fp8, int kv_layout, const int32_t* kv_indptr,
                           const int32_t* kv_indices, const int32_t* last_page_len,
                           const int32_t* qo_indptr, const uint8_t* mask,
                           const int32_t* mask_indptr, int mask_layout, const int32_t* q_pos,
                           double rope_theta, double rope_scale, int q_fp8, int batch, int h_q,
-                          int h_kv,
-                          int d, int page_size, int num_pages, double sm_scale, double k_scale,
-                          double v_scale, const int32_t* sel, int64_t n_sel, double* out,
-                          double* lse, int nthreads) {
-    if (h_kv <= 0 || h_q <= 0 || h_q % h_kv != 0 || d <= 0 || nthreads < 1) return OR_EINVAL;
+                          int h_kv, int d, int dv, int page_size, int num_pages, double sm_scale,
+                          double k_scale, double v_scale, const int32_t* sel, int64_t n_sel,
+                          double* out, double* lse, int nthreads) {
+    if (h_kv <= 0 || h_q <= 0 || h_q % h_kv != 0 || d <= 0 || dv <= 0 || nthreads < 1)
+        return OR_EINVAL;
     if (q_fp8 && d > 1024) return OR_EINVAL;
     if ((kv_layout != 0 && kv_layout != 1) || (mask_layout != 0 && mask_layout != 1))
         return OR_EINVAL;
@@ -447,9 +459,9 @@ int oracle_verify_attn_ex(const uint16_t* q, const void* k_cache, const void* v_
         }
         if (nr == 0) continue;
         int64_t kv_len = oracle_kv_len(kv_indptr, last_page_len, b, page_size);
-        size_t kv_elems = (size_t)(kv_len > 0 ? kv_len : 1) * (size_t)h_kv * (size_t)d;
-        double* K = (double*)malloc(sizeof(double) * kv_elems);
-        double* V = (double*)malloc(sizeof(double) * kv_elems);
+        size_t kv_rows = (size_t)(kv_len > 0 ? kv_len : 1) * (size_t)h_kv;
+        double* K = (double*)malloc(sizeof(double) * kv_rows * (size_t)d);
+        double* V = (double*)malloc(sizeof(double) * kv_rows * (size_t)dv);
         double* M = (double*)malloc(sizeof(double) * (size_t)(L * (kv_len > 0 ? kv_len : 1)));
         if (!K || !V || !M) {
             free(K); free(V); free(M);
@@ -457,7 +469,7 @@ int oracle_verify_attn_ex(const uint16_t* q, const void* k_cache, const void* v_
             break;
         }
         gather_request(k_cache, v_cache, kv_fp8, kv_layout, kv_indptr, kv_indices, b, kv_len,
-                       h_kv, d, page_size, k_scale, v_scale, K, V);
+                       h_kv, d, dv, page_size, k_scale, v_scale, K, V);
         build_mask(mask, mask_indptr, mask_layout, b, L, kv_len, M);
         int nt = nthreads;
         if (nt > nr) nt = (int)nr;
@@ -465,7 +477,7 @@ int oracle_verify_attn_ex(const uint16_t* q, const void* k_cache, const void* v_
             job_t* jb = &jobs[i];
             jb->q = q; jb->K = K; jb->V = V; jb->M = M;
             jb->kv_len = kv_len; jb->L = L; jb->qo_start = qo0;
-            jb->h_q = h_q; jb->h_kv = h_kv; jb->d = d; jb->group = group;
+            jb->h_q = h_q; jb->h_kv = h_kv; jb->d = d; jb->dv = dv; jb->group = group;
             jb->sm_scale = sm_scale; jb->rows = rows; jb->dest = dest; jb->n_rows = nr;
             jb->q_pos = q_pos; jb->rope_theta = rope_theta; jb->rope_scale = rope_scale;
             jb->q_fp8 = q_fp8;
@@ -482,6 +494,23 @@ int oracle_verify_attn_ex(const uint16_t* q, const void* k_cache, const void* v_
     }
     free(rows); free(dest); free(th); free(jobs);
     return status;
+}
+
+/* oracle_verify_attn_dv with values of the key's width (dv = d). */
+int oracle_verify_attn_ex(const uint16_t* q, const void* k_cache, const void* v_cache,
+                          int kv_fp8, int kv_layout, const int32_t* kv_indptr,
+                          const int32_t* kv_indices, const int32_t* last_page_len,
+                          const int32_t* qo_indptr, const uint8_t* mask,
+                          const int32_t* mask_indptr, int mask_layout, const int32_t* q_pos,
+                          double rope_theta, double rope_scale, int q_fp8, int batch, int h_q,
+                          int h_kv, int d, int page_size, int num_pages, double sm_scale,
+                          double k_scale, double v_scale, const int32_t* sel, int64_t n_sel,
+                          double* out, double* lse, int nthreads) {
+    return oracle_verify_attn_dv(q, k_cache, v_cache, kv_fp8, kv_layout, kv_indptr, kv_indices,
+                                 last_page_len, qo_indptr, mask, mask_indptr, mask_layout, q_pos,
+                                 rope_theta, rope_scale, q_fp8, batch, h_q, h_kv, d, d, page_size,
+                                 num_pages, sm_scale, k_scale, v_scale, sel, n_sel, out, lse,
+                                 nthreads);
 }
 
 /* oracle_verify_attn_ex for an HND cache, each request's L x L mask block and
@@ -530,7 +559,7 @@ int oracle_attn_range(const uint16_t* q, const void* k_cache, const void* v_cach
         free(K); free(V); free(M); free(s); free(qrow);
         return OR_ENOMEM;
     }
-    gather_request(k_cache, v_cache, kv_fp8, 0, kv_indptr, kv_indices, b, kv_len, h_kv, d,
+    gather_request(k_cache, v_cache, kv_fp8, 0, kv_indptr, kv_indices, b, kv_len, h_kv, d, d,
                    page_size, k_scale, v_scale, K, V);
     build_mask(mask, mask_indptr, 0, b, L, kv_len, M);
     int64_t tok = qo_indptr[b] + t;
@@ -642,14 +671,15 @@ int oracle_paged_kv_append_quant(const uint16_t* k_new, const uint16_t* v_new, f
  *    copied without quantizing is rotated in its stored units).  V rows are
  *    never rotated.
  * Without quantize or positions this is oracle_paged_kv_append's bit copy.
+ * V rows (new and cached) hold dv elements, K rows d.
  */
-int oracle_paged_kv_append_ex(const void* k_new, const void* v_new, int cache_fp8, int quantize,
+int oracle_paged_kv_append_dv(const void* k_new, const void* v_new, int cache_fp8, int quantize,
                               float k_scale, float v_scale, int layout, const int32_t* positions,
                               double theta, double rope_scale, const int32_t* append_indptr,
                               const int32_t* kv_indptr, const int32_t* kv_indices,
-                              const int32_t* last_page_len, int batch, int h_kv, int d,
+                              const int32_t* last_page_len, int batch, int h_kv, int d, int dv,
                               int page_size, int num_pages, void* k_cache, void* v_cache) {
-    if (batch < 0 || h_kv <= 0 || d <= 0 || page_size <= 0) return OR_EINVAL;
+    if (batch < 0 || h_kv <= 0 || d <= 0 || dv <= 0 || page_size <= 0) return OR_EINVAL;
     if (layout != 0 && layout != 1) return OR_EINVAL;
     if (quantize && (!cache_fp8 || !(k_scale > 0.0f) || !(v_scale > 0.0f))) return OR_EINVAL;
     if (positions && !(theta > 0.0 && rope_scale > 0.0)) return OR_EINVAL;
@@ -669,15 +699,17 @@ int oracle_paged_kv_append_ex(const void* k_new, const void* v_new, int cache_fp
             int64_t slot = pos % page_size;
             int64_t tok = (int64_t)append_indptr[b] + i;
             for (int h = 0; h < h_kv; ++h) {
-                size_t dst = (size_t)cache_row(layout, page, h, slot, h_kv, page_size) * (size_t)d;
-                size_t src = ((size_t)tok * h_kv + h) * (size_t)d;
+                size_t crow = (size_t)cache_row(layout, page, h, slot, h_kv, page_size);
                 for (int kv = 0; kv < 2; ++kv) {
+                    const int w = kv ? dv : d;  /* elements of this row */
+                    size_t dst = crow * (size_t)w;
+                    size_t src = ((size_t)tok * h_kv + h) * (size_t)w;
                     const void* in = kv ? v_new : k_new;
                     void* cache = kv ? v_cache : k_cache;
                     const float scale = kv ? v_scale : k_scale;
                     const int rotate = positions && kv == 0;
                     if (!rotate) {
-                        for (int e = 0; e < d; ++e) {
+                        for (int e = 0; e < w; ++e) {
                             if (quantize) {
                                 float x = (float)oracle_decode_bf16(((const uint16_t*)in)[src + e]);
                                 ((uint8_t*)cache)[dst + e] =
@@ -707,6 +739,19 @@ int oracle_paged_kv_append_ex(const void* k_new, const void* v_new, int cache_fp
     }
     free(row);
     return OR_OK;
+}
+
+/* oracle_paged_kv_append_dv with value rows of the key's width (dv = d). */
+int oracle_paged_kv_append_ex(const void* k_new, const void* v_new, int cache_fp8, int quantize,
+                              float k_scale, float v_scale, int layout, const int32_t* positions,
+                              double theta, double rope_scale, const int32_t* append_indptr,
+                              const int32_t* kv_indptr, const int32_t* kv_indices,
+                              const int32_t* last_page_len, int batch, int h_kv, int d,
+                              int page_size, int num_pages, void* k_cache, void* v_cache) {
+    return oracle_paged_kv_append_dv(k_new, v_new, cache_fp8, quantize, k_scale, v_scale, layout,
+                                     positions, theta, rope_scale, append_indptr, kv_indptr,
+                                     kv_indices, last_page_len, batch, h_kv, d, d, page_size,
+                                     num_pages, k_cache, v_cache);
 }
 
 int oracle_paged_kv_append(const void* k_new, const void* v_new, int elem_bytes,

@@ -102,6 +102,11 @@ class Workload:
     rope_theta: Optional[float] = None  # RoPE base when the workload uses rotary positions
     q_pos: Optional[np.ndarray] = None  # [sum L] int32 position of each query token
     kv_pos: Optional[np.ndarray] = None  # [sum kv_len] int32 position of each key, k_tok order
+    dv: int = 0                      # elements of a value row (0: the key's d)
+
+    def __post_init__(self):
+        if not self.dv:
+            self.dv = self.d
 
     @property
     def group(self) -> int:
@@ -213,7 +218,7 @@ def make_custom(name="custom", seed=0, batch=2, h_q=4, h_kv=2, d=64, page_size=1
                 kv_dtype=BF16, prefix=("fixed", [37, 70]), qo=("fixed", [5, 5]),
                 mask="causal", pool_pages=None, pool_factor=1.25, sm_scale=None,
                 shuffle_pages=True, value_std=1.0, with_values=True, kv_layout="hnd",
-                mask_layout="qlen", prefix_visible="all", rope_theta=None) -> Workload:
+                mask_layout="qlen", prefix_visible="all", rope_theta=None, dv=None) -> Workload:
     """A workload from explicit parameters.  with_values=False draws only the
     tables (lengths, trees, pages; q / k / v come last in the draw order, so the
     tables are the same either way) and leaves q / k_tok / v_tok empty.
@@ -224,7 +229,8 @@ def make_custom(name="custom", seed=0, batch=2, h_q=4, h_kv=2, d=64, page_size=1
     draws them (after every other draw).  rope_theta gives the workload rotary
     positions: a prefix key at index j has position j, draft u has position
     prefix + depth(u) (its tree depth; u itself for chains and masks without
-    a tree), and each query token has its draft's position."""
+    a tree), and each query token has its draft's position.  dv gives value
+    rows of their own width (v_tok [sum kv_len, h_kv, dv]); the default is d."""
     gen = torch.Generator().manual_seed(seed)
     prefix_lens = _draw_lengths(prefix, batch, gen)
     qo_lens = _draw_lengths(qo, batch, gen)
@@ -292,7 +298,8 @@ def make_custom(name="custom", seed=0, batch=2, h_q=4, h_kv=2, d=64, page_size=1
         k_scale = 1.0
         k_tok = _bf16_bits(kf)
     del kf
-    vf = torch.randn((total_tok, h_kv, d), generator=gen) * value_std
+    dv = d if dv is None else int(dv)
+    vf = torch.randn((total_tok, h_kv, dv), generator=gen) * value_std
     if kv_dtype == FP8:
         v_scale = float(np.float32(float(vf.abs().max()) / 448.0)) if total_tok else 1.0
         v_tok = _fp8_bits(vf, v_scale)
@@ -347,18 +354,19 @@ def make_custom(name="custom", seed=0, batch=2, h_q=4, h_kv=2, d=64, page_size=1
         q=q, k_tok=k_tok, v_tok=v_tok, sm_scale=sm_scale, k_scale=k_scale,
         v_scale=v_scale, mask_kind=mask, parents=parents, mask_dense=dense,
         mask=packed, mask_indptr=mask_indptr, kv_layout=kv_layout, mask_layout=mask_layout,
-        mask_full=mask_full, rope_theta=rope_theta, q_pos=q_pos, kv_pos=kv_pos)
+        mask_full=mask_full, rope_theta=rope_theta, q_pos=q_pos, kv_pos=kv_pos, dv=dv)
 
 
-def sentinel_pool(wl: Workload) -> np.ndarray:
-    """An empty page pool [num_pages, h_kv, page_size, d] filled with 0xFF
-    bytes: NaN in both bf16 and fp8-e4m3, so any read of an unwritten slot
-    shows up in the result."""
+def sentinel_pool(wl: Workload, values: bool = False) -> np.ndarray:
+    """An empty page pool [num_pages, h_kv, page_size, d] (values=True: rows
+    of the value width dv) filled with 0xFF bytes: NaN in both bf16 and
+    fp8-e4m3, so any read of an unwritten slot shows up in the result."""
     dt = np.uint8 if wl.kv_dtype == FP8 else np.uint16
     fill = 0xFF if wl.kv_dtype == FP8 else 0xFFFF
+    w = wl.dv if values else wl.d
     if wl.nhd:
-        return np.full((wl.num_pages, wl.page_size, wl.h_kv, wl.d), fill, dtype=dt)
-    return np.full((wl.num_pages, wl.h_kv, wl.page_size, wl.d), fill, dtype=dt)
+        return np.full((wl.num_pages, wl.page_size, wl.h_kv, w), fill, dtype=dt)
+    return np.full((wl.num_pages, wl.h_kv, wl.page_size, w), fill, dtype=dt)
 
 
 def sample_rows(wl: Workload, n: int, seed: int = 1):

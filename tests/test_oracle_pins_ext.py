@@ -418,3 +418,102 @@ def test_e4m3_query_attention_is_attention_over_the_quantised_rows(oracle_lib):
                                               np.zeros((1, len(vis))), wl.sm_scale)
                 np.testing.assert_allclose(out[tok * wl.h_q + qh], o[0], atol=1e-12, rtol=0)
                 assert abs(lse[tok * wl.h_q + qh] - l[0]) < 1e-12
+
+
+# ---------------------------------------------------------------- value width dv != d
+
+@pytest.mark.parametrize("spec", [
+    dict(batch=2, h_q=4, h_kv=2, d=16, dv=8, page_size=4, prefix=("fixed", [9, 3]),
+         qo=("fixed", [4, 3]), mask="tree", seed=141),
+    dict(batch=2, h_q=2, h_kv=1, d=8, dv=24, page_size=2, prefix=("fixed", [5, 0]),
+         qo=("fixed", [3, 4]), mask="causal", kv_dtype=synthetic.FP8, seed=142),
+    dict(batch=1, h_q=4, h_kv=2, d=8, dv=16, page_size=4, prefix=("fixed", [6]),
+         qo=("fixed", [3]), mask="random", kv_layout="nhd", mask_layout="full",
+         prefix_visible="random", seed=143),
+], ids=["narrow_values_tree", "wide_values_fp8_chain", "wide_values_nhd_full_mask"])
+def test_value_width_matches_scalar_brute_force(oracle_lib, spec):
+    """sglang's value head size dv != d: the scalar brute force (which takes
+    the value width from the cache it is given) on the cache the oracle's
+    append wrote, with key rows of d and value rows of dv elements."""
+    wl = synthetic.make_custom(**spec)
+    kc, vc = oracle.build_cache(wl)
+    assert kc.shape[-1] == wl.d and vc.shape[-1] == wl.dv
+    out, lse = oracle.verify_attn_workload(wl, caches=(kc, vc), nthreads=2)
+    assert out.shape == (wl.total_qo * wl.h_q, wl.dv)
+    bo, bl = brute.verify_attn(wl.q, kc, vc, wl.kv_dtype == synthetic.FP8, wl.kv_indptr,
+                               wl.kv_indices, wl.last_page_len, wl.qo_indptr, wl.mask,
+                               wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size, wl.sm_scale,
+                               wl.k_scale, wl.v_scale, kv_layout=1 if wl.nhd else 0,
+                               mask_layout=1 if wl.mask_layout == "full" else 0)
+    fin = np.isfinite(bl)
+    assert np.array_equal(np.isfinite(lse), fin)
+    np.testing.assert_allclose(out, bo, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse[fin], bl[fin], atol=1e-12, rtol=0)
+
+
+def test_value_columns_are_independent(oracle_lib):
+    """The weights depend on Q and K alone: with the same keys, values of dv
+    columns give exactly the first dv columns (and the same LSE) of the
+    result for values widened by extra columns -- so no value row is read
+    with the key's width or stride."""
+    base = dict(batch=3, h_q=8, h_kv=2, d=32, page_size=4, prefix=("fixed", [13, 0, 7]),
+                qo=("fixed", [5, 2, 6]), mask="tree", seed=144)
+    narrow = synthetic.make_custom(dv=16, **base)
+    wide = synthetic.make_custom(dv=48, **base)
+    assert np.array_equal(narrow.q, wide.q) and np.array_equal(narrow.k_tok, wide.k_tok)
+    wide.v_tok = wide.v_tok.copy()
+    wide.v_tok[..., :16] = narrow.v_tok
+    on, ln = oracle.verify_attn_workload(narrow, nthreads=2)
+    ow, lw = oracle.verify_attn_workload(wide, nthreads=2)
+    np.testing.assert_array_equal(ln, lw)
+    np.testing.assert_allclose(on, ow[:, :16], atol=1e-13, rtol=0)
+    # and a value width equal to d is the ordinary path
+    same = synthetic.make_custom(dv=32, **base)
+    plain = synthetic.make_custom(**base)
+    o1, l1 = oracle.verify_attn_workload(same, nthreads=2)
+    o2, l2 = oracle.verify_attn_workload(plain, nthreads=2)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_value_width_append_lands_rows_of_their_width(oracle_lib):
+    """The append with dv-wide values: each new V row (dv elements) lands at
+    its token's slot of the dv-wide pool, K rows (d elements) at the same
+    slot of the d-wide pool, bf16 and quantised to e4m3; nothing else moves."""
+    for kvd, quant in ((synthetic.BF16, False), (synthetic.FP8, True)):
+        wl = synthetic.make_custom(batch=2, h_q=4, h_kv=2, d=16, dv=8, page_size=4,
+                                   prefix=("fixed", [5, 2]), qo=("fixed", [3, 4]), kv_dtype=kvd,
+                                   seed=145)
+        wb = synthetic.make_custom(batch=2, h_q=4, h_kv=2, d=16, dv=8, page_size=4,
+                                   prefix=("fixed", [5, 2]), qo=("fixed", [3, 4]), seed=145)
+        src = wb if quant else wl
+        kn, vn = src.new_tokens()
+        kc = synthetic.sentinel_pool(wl)
+        vc = synthetic.sentinel_pool(wl, values=True)
+        oracle.paged_kv_append_ex(kn, vn, wl.qo_indptr, wl.kv_indptr, wl.kv_indices,
+                                  wl.last_page_len, wl.page_size, wl.num_pages, kc, vc,
+                                  cache_fp8=kvd == synthetic.FP8, quantize=quant,
+                                  k_scale=wl.k_scale, v_scale=wl.v_scale)
+        written = np.zeros(kc.shape[:3], bool)
+        for b in range(wl.batch):
+            L, kv = int(wl.qo_lens[b]), int(wl.kv_lens[b])
+            for i in range(L):
+                pos = kv - L + i
+                page = wl.kv_indices[wl.kv_indptr[b] + pos // wl.page_size]
+                slot = pos % wl.page_size
+                tok = int(wl.qo_indptr[b]) + i
+                for h in range(wl.h_kv):
+                    written[page, h, slot] = True
+                    if quant:
+                        want_k = torch.from_numpy(
+                            (torch.from_numpy(kn[tok, h].view(np.int16)).view(torch.bfloat16).float()
+                             / np.float32(wl.k_scale)).numpy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                        want_v = torch.from_numpy(
+                            (torch.from_numpy(vn[tok, h].view(np.int16)).view(torch.bfloat16).float()
+                             / np.float32(wl.v_scale)).numpy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                    else:
+                        want_k, want_v = kn[tok, h], vn[tok, h]
+                    assert np.array_equal(kc[page, h, slot], want_k)
+                    assert np.array_equal(vc[page, h, slot], want_v)
+        fill = 0xFF if kvd == synthetic.FP8 else 0xFFFF
+        assert np.all(kc[~written] == fill) and np.all(vc[~written] == fill)
