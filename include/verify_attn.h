@@ -157,6 +157,12 @@ typedef struct {
                             with a plain copy append reads such an item's keys and values
                             from k_new / v_new instead of the pages, so it does not wait
                             for the append. */
+    int head_dim_v;      /* elements of a value row (sglang's value head size: v_cache rows
+                            and out rows), 64 or 128; 0 means head_dim.  A value width
+                            other than head_dim is served by the warp-level variants
+                            (VA_KERNEL_MMA_64 / _128; a tcgen05 kernel asked for returns
+                            VA_ERR_UNSUPPORTED).  out is then [total_qo, num_qo_heads,
+                            head_dim_v] and the calls take head_dim (the key's) as before. */
 } va_plan_options_t;
 
 #define VA_KERNEL_AUTO 0
@@ -391,7 +397,10 @@ typedef struct {
                                 FlashInfer issue #152 asks).  V rows are not rotated. */
     float rope_theta;        /* RoPE base (> 0, finite; e.g. 1e4, Llama-3: 5e5) */
     float rope_scale;        /* linear position scaling (> 0, finite); 0 means 1 */
-    int reserved[4];         /* must be zero */
+    int head_dim_v;          /* elements of a V row (v_new and v_cache), sglang's value head
+                                size, which may differ from head_dim (64 or 128); 0 means
+                                head_dim */
+    int reserved[3];         /* must be zero */
 } va_append_options_t;
 
 /*

@@ -63,7 +63,8 @@ class PlanOptions(ctypes.Structure):
     _fields_ = [("max_splits", ctypes.c_int), ("min_chunk", ctypes.c_int),
                 ("target_ctas", ctypes.c_int), ("kernel", ctypes.c_int),
                 ("mask_layout", ctypes.c_int), ("kv_layout", ctypes.c_int),
-                ("rope", ctypes.c_int), ("q_fp8", ctypes.c_int), ("draft_items", ctypes.c_int)]
+                ("rope", ctypes.c_int), ("q_fp8", ctypes.c_int), ("draft_items", ctypes.c_int),
+                ("head_dim_v", ctypes.c_int)]
 
 
 class RunOptions(ctypes.Structure):
@@ -76,7 +77,8 @@ class AppendOptions(ctypes.Structure):
     _fields_ = [("quantize", ctypes.c_int), ("k_scale", ctypes.c_float),
                 ("v_scale", ctypes.c_float), ("kv_layout", ctypes.c_int),
                 ("positions", ctypes.c_void_p), ("rope_theta", ctypes.c_float),
-                ("rope_scale", ctypes.c_float), ("reserved", ctypes.c_int * 4)]
+                ("rope_scale", ctypes.c_float), ("head_dim_v", ctypes.c_int),
+                ("reserved", ctypes.c_int * 3)]
 
 
 MASK_QLEN, MASK_FULL = 0, 1
@@ -190,7 +192,7 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0, mask_layout="qlen",
-             kv_layout="hnd", rope=False, q_fp8=False, draft_items=0):
+             kv_layout="hnd", rope=False, q_fp8=False, draft_items=0, head_dim_v=0):
     o = PlanOptions()
     o.max_splits, o.min_chunk, o.target_ctas, o.kernel = (int(max_splits), int(min_chunk),
                                                           int(target_ctas), int(kernel))
@@ -199,6 +201,7 @@ def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0, mask_layout="ql
     o.rope = int(bool(rope))
     o.q_fp8 = int(bool(q_fp8))
     o.draft_items = int(draft_items)
+    o.head_dim_v = int(head_dim_v or 0)
     return o
 
 
@@ -227,7 +230,8 @@ class Plan:
                     n_units=int(ints[16]), num_sms=int(ints[17]), total_qo=int(i64[0]),
                     part_rows=int(i64[1]), chunk=int(i64[2]),
                     ws_bytes=int(np.frombuffer(h[136:144].tobytes(), dtype=np.uint64)[0]),
-                    n_ctas=int(np.frombuffer(h[160:168].tobytes(), dtype=np.int64)[0]))
+                    n_ctas=int(np.frombuffer(h[160:168].tobytes(), dtype=np.int64)[0]),
+                    head_dim_v=int(np.frombuffer(h[168:176].tobytes(), dtype=np.int64)[0]))
 
     def launches(self) -> int:
         n = ctypes.c_int(0)
@@ -362,7 +366,8 @@ def _run_args(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indp
 
 def _alloc_out(q, plan, out, lse, want_lse):
     if out is None:
-        out = torch.empty_like(q)
+        dv = plan.header()["head_dim_v"]
+        out = q.new_empty(q.shape[0], q.shape[1], dv)
     if lse is None and want_lse:
         lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
     return out, lse
@@ -463,10 +468,11 @@ def paged_kv_append(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_pag
         page_size, h_kv, head_dim = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
     else:
         h_kv, page_size, head_dim = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
+    head_dim_v = v_cache.shape[3]
     common = (_dp(k_new), _dp(v_new), _dp(append_indptr), _dp(kv_indptr), _dp(kv_indices),
               _dp(last_page_len), _dp(k_cache), _dp(v_cache), int(batch), int(h_kv),
               int(head_dim), int(page_size), int(num_pages), kv_dtype, int(total_new))
-    if not quantize and positions is None and layout == LAYOUT_HND:
+    if not quantize and positions is None and layout == LAYOUT_HND and head_dim_v == head_dim:
         rc = lib().paged_kv_append(*common, _dp(status), _stream(stream))
         _check("paged_kv_append", rc)
         return
@@ -478,6 +484,7 @@ def paged_kv_append(k_new, v_new, append_indptr, kv_indptr, kv_indices, last_pag
     o.positions = _dp(positions) if positions is not None else None
     o.rope_theta = float(rope_theta) if positions is not None else 0.0
     o.rope_scale = float(rope_scale) if positions is not None else 0.0
+    o.head_dim_v = int(head_dim_v)
     rc = lib().paged_kv_append_ex(*common, ctypes.byref(o), _dp(status), _stream(stream))
     _check("paged_kv_append_ex", rc)
 

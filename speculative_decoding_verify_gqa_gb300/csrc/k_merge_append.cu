@@ -183,33 +183,35 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
     if (p.status) atomicOr(p.status, pos_ok ? VA_DEV_BAD_PAGE : VA_DEV_BAD_APPEND);
     return;
   }
-  const size_t row_bytes = (size_t)p.row_chunks * 16;
+  // K rows hold head_dim elements, V rows head_dim_v: this thread's chunk
+  // ch of each row that has one
+  const bool do_k = ch < p.k_chunks, do_v = ch < p.v_chunks;
   const size_t slot = (size_t)(pos & (p.page_size - 1));
   const size_t row = p.nhd ? ((size_t)page * p.page_size + slot) * p.h_kv + h
                            : ((size_t)page * p.h_kv + h) * p.page_size + slot;
-  const size_t dst = row * row_bytes + (size_t)ch * 16;
-  uint8_t* kd = static_cast<uint8_t*>(p.k_cache) + dst;
-  uint8_t* vd = static_cast<uint8_t*>(p.v_cache) + dst;
+  uint8_t* kd = static_cast<uint8_t*>(p.k_cache) + row * (size_t)p.k_chunks * 16 + (size_t)ch * 16;
+  uint8_t* vd = static_cast<uint8_t*>(p.v_cache) + row * (size_t)p.v_chunks * 16 + (size_t)ch * 16;
   const int D = p.head_dim;
   const bool bf16_src = p.quant || !p.cache_fp8;
-  const size_t src_row = ((size_t)i * p.h_kv + h) * (size_t)D * (bf16_src ? 2 : 1);
-  const uint8_t* ks = static_cast<const uint8_t*>(p.k_new) + src_row;
-  const uint8_t* vs = static_cast<const uint8_t*>(p.v_new) + src_row;
+  const size_t src_es = bf16_src ? 2 : 1;
+  const uint8_t* ks = static_cast<const uint8_t*>(p.k_new) + ((size_t)i * p.h_kv + h) * (size_t)D * src_es;
+  const uint8_t* vs = static_cast<const uint8_t*>(p.v_new) +
+                      ((size_t)i * p.h_kv + h) * (size_t)p.head_dim_v * src_es;
   if (!p.quant && !p.positions) {  // a bit-exact copy
-    const uint4 kq = *reinterpret_cast<const uint4*>(ks + (size_t)ch * 16);
-    const uint4 vq = *reinterpret_cast<const uint4*>(vs + (size_t)ch * 16);
+    const uint4 kq = do_k ? *reinterpret_cast<const uint4*>(ks + (size_t)ch * 16) : make_uint4(0, 0, 0, 0);
+    const uint4 vq = do_v ? *reinterpret_cast<const uint4*>(vs + (size_t)ch * 16) : make_uint4(0, 0, 0, 0);
     if (p.early) grid_dependency_wait();   // the slots may still be read before it
-    *reinterpret_cast<uint4*>(kd) = kq;
-    *reinterpret_cast<uint4*>(vd) = vq;
+    if (do_k) *reinterpret_cast<uint4*>(kd) = kq;
+    if (do_v) *reinterpret_cast<uint4*>(vd) = vq;
     return;
   }
   // elements e0 .. e0 + E - 1 of the row: 8 for a bf16 cache, 16 for fp8
   const int E = p.cache_fp8 ? 16 : 8;
   const int e0 = ch * E;
-  float xk[16], xv[16];
-  load_f32(ks, bf16_src, e0, E, xk);
-  load_f32(vs, bf16_src, e0, E, xv);
-  if (p.positions) {
+  float xk[16] = {}, xv[16] = {};
+  if (do_k) load_f32(ks, bf16_src, e0, E, xk);
+  if (do_v) load_f32(vs, bf16_src, e0, E, xv);
+  if (p.positions && do_k) {
     const int half = D / 2;
     const int partner = e0 < half ? e0 + half : e0 - half;
     float yk[16];
@@ -232,8 +234,8 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
     wk.z = pack_bf16x2(xk[4], xk[5]); wk.w = pack_bf16x2(xk[6], xk[7]);
     wv.x = pack_bf16x2(xv[0], xv[1]); wv.y = pack_bf16x2(xv[2], xv[3]);
     wv.z = pack_bf16x2(xv[4], xv[5]); wv.w = pack_bf16x2(xv[6], xv[7]);
-    *reinterpret_cast<uint4*>(kd) = wk;
-    *reinterpret_cast<uint4*>(vd) = wv;
+    if (do_k) *reinterpret_cast<uint4*>(kd) = wk;
+    if (do_v) *reinterpret_cast<uint4*>(vd) = wv;
     return;
   }
   // e4m3 codes: quantising appends divide by the per-tensor scale first (a
@@ -247,8 +249,8 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
     cv[k] = e4m3x4_rn_satfinite(__fdiv_rn(xv[4 * k], vsc), __fdiv_rn(xv[4 * k + 1], vsc),
                                 __fdiv_rn(xv[4 * k + 2], vsc), __fdiv_rn(xv[4 * k + 3], vsc));
   }
-  *reinterpret_cast<uint4*>(kd) = make_uint4(ck[0], ck[1], ck[2], ck[3]);
-  *reinterpret_cast<uint4*>(vd) = make_uint4(cv[0], cv[1], cv[2], cv[3]);
+  if (do_k) *reinterpret_cast<uint4*>(kd) = make_uint4(ck[0], ck[1], ck[2], ck[3]);
+  if (do_v) *reinterpret_cast<uint4*>(vd) = make_uint4(cv[0], cv[1], cv[2], cv[3]);
 }
 
 }  // namespace

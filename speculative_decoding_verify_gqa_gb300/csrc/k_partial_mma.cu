@@ -29,29 +29,35 @@
 namespace va {
 namespace {
 
-template <int D, bool FP8, int NW, int STAGES>
+// D: elements of a query / key row; DV: of a value / output row (sglang's
+// value head size, which may differ).
+template <int D, int DV, bool FP8, int NW, int STAGES>
 struct MmaCfg {
   static constexpr int BN = kTileKeys;            // keys per tile
   static constexpr int BM = 16 * NW;              // rows per CTA
   static constexpr int NT = 32 * NW;              // threads
-  static constexpr int QROW = D * 2;              // bytes per bf16 row
-  static constexpr int KVROW = FP8 ? D : 2 * D;   // bytes per cache row
-  static constexpr int KV_CH = KVROW / 16;        // 16-byte chunks per cache row
+  static constexpr int QROW = D * 2;              // bytes per bf16 Q / K row
+  static constexpr int VROW = DV * 2;             // bytes per bf16 V row
+  static constexpr int KVROW = FP8 ? D : 2 * D;   // bytes per K cache row
+  static constexpr int VVROW = FP8 ? DV : 2 * DV; // bytes per V cache row
+  static constexpr int KV_CH = KVROW / 16;        // 16-byte chunks per K cache row
+  static constexpr int V_CH = VVROW / 16;         // 16-byte chunks per V cache row
   static constexpr int Q_CH = QROW / 16;
   static constexpr int Q_BYTES = BM * QROW;
-  static constexpr int TILE_BYTES = BN * KVROW;   // one K (or V) tile in cache format
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int CONV_BYTES = FP8 ? 2 * BN * QROW : 0;
+  static constexpr int TILE_BYTES = BN * KVROW;   // one K tile in cache format
+  static constexpr int VTILE_BYTES = BN * VVROW;  // one V tile in cache format
+  static constexpr int STAGE_BYTES = TILE_BYTES + VTILE_BYTES;
+  static constexpr int CONV_BYTES = FP8 ? BN * (QROW + VROW) : 0;
   static constexpr int RING_BYTES = STAGES * BN * 4;  // page id of every key of the tiles in flight
   static constexpr int SMEM = Q_BYTES + STAGES * STAGE_BYTES + CONV_BYTES + RING_BYTES;
   static_assert(BN == 64, "tile loop assumes 64 keys");
   static_assert(NT >= BN, "one thread per key fetches page ids");
 };
 
-template <int D, bool FP8, int NW, int STAGES>
+template <int D, int DV, bool FP8, int NW, int STAGES>
 __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
     verify_partial_mma_kernel(const PartialParams p) {
-  using C = MmaCfg<D, FP8, NW, STAGES>;
+  using C = MmaCfg<D, DV, FP8, NW, STAGES>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* sQ = smem;
   uint8_t* sStage = smem + C::Q_BYTES;
@@ -92,11 +98,12 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
   const int lo = it.kv_lo, hi = it.kv_hi;
   const int n_tiles = (hi - lo + C::BN - 1) / C::BN;
   // HND [page][head][slot][d] or NHD [page][slot][head][d]
-  const size_t slot_stride = p.nhd ? (size_t)p.h_kv * C::KVROW : (size_t)C::KVROW;
-  const size_t head_off = p.nhd ? (size_t)h * C::KVROW : (size_t)h * p.page_size * C::KVROW;
-  const size_t page_stride = (size_t)p.h_kv * p.page_size * C::KVROW;
-  const uint8_t* kbase = static_cast<const uint8_t*>(p.k_cache) + head_off;
-  const uint8_t* vbase = static_cast<const uint8_t*>(p.v_cache) + head_off;
+  // (element strides are the same for K and V; the row widths differ)
+  const size_t slot_rows = p.nhd ? (size_t)p.h_kv : 1;
+  const size_t head_rows = p.nhd ? (size_t)h : (size_t)h * p.page_size;
+  const size_t page_rows = (size_t)p.h_kv * p.page_size;
+  const uint8_t* kbase = static_cast<const uint8_t*>(p.k_cache) + head_rows * C::KVROW;
+  const uint8_t* vbase = static_cast<const uint8_t*>(p.v_cache) + head_rows * C::VVROW;
   const int pmask = p.page_size - 1;
   int bad_page = 0;
 
@@ -126,27 +133,30 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
     const int* pages = sPage + (tile % STAGES) * C::BN;
     uint8_t* sK = sStage + stage * C::STAGE_BYTES;
     uint8_t* sV = sK + C::TILE_BYTES;
+    constexpr int CH = C::KV_CH > C::V_CH ? C::KV_CH : C::V_CH;  // chunks of the wider row
 #pragma unroll 4
-    for (int c = tid; c < C::BN * C::KV_CH; c += C::NT) {
-      const int r = c / C::KV_CH, ch = c % C::KV_CH;
+    for (int c = tid; c < C::BN * CH; c += C::NT) {
+      const int r = c / CH, ch = c % CH;
       const int key = k0 + r;
-      const uint8_t* ks = kbase;
-      const uint8_t* vs = vbase;
+      size_t row = 0;
       int bytes = 0;
       if (key < hi) {
         const int page = pages[r];
         if ((unsigned)page < (unsigned)p.num_pages) {
-          const size_t off = (size_t)page * page_stride + (size_t)(key & pmask) * slot_stride + ch * 16;
-          ks = kbase + off;
-          vs = vbase + off;
+          row = (size_t)page * page_rows + (size_t)(key & pmask) * slot_rows;
           bytes = 16;
         } else {
           bad_page = 1;
         }
       }
-      const uint32_t doff = FP8 ? (uint32_t)(r * C::KVROW + ch * 16) : swz(r, ch, C::QROW);
-      cp_async_16(smem_u32(sK + doff), ks, bytes);
-      cp_async_16(smem_u32(sV + doff), vs, bytes);
+      if (C::KV_CH == CH || ch < C::KV_CH) {
+        const uint32_t doff = FP8 ? (uint32_t)(r * C::KVROW + ch * 16) : swz(r, ch, C::QROW);
+        cp_async_16(smem_u32(sK + doff), bytes ? kbase + row * C::KVROW + ch * 16 : kbase, bytes);
+      }
+      if (C::V_CH == CH || ch < C::V_CH) {
+        const uint32_t doff = FP8 ? (uint32_t)(r * C::VVROW + ch * 16) : swz(r, ch, C::VROW);
+        cp_async_16(smem_u32(sV + doff), bytes ? vbase + row * C::VVROW + ch * 16 : vbase, bytes);
+      }
     }
   };
 
@@ -206,9 +216,9 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
   const float sl2 = p.scale_log2;
 
   uint32_t qa[D / 16][4];
-  float o[D / 8][4];
+  float o[DV / 8][4];
 #pragma unroll
-  for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  for (int j = 0; j < DV / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
 
   for (int tile = 0; tile < n_tiles; ++tile) {
@@ -232,11 +242,14 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
     const uint8_t* sV;
     if constexpr (FP8) {
       const uint8_t* raw = sStage + stage * C::STAGE_BYTES;
-      for (int c = tid; c < 2 * C::BN * C::KV_CH; c += C::NT) {
-        const int which = c / (C::BN * C::KV_CH);
+      // K's 16-byte chunks, then V's (rows of D and DV codes)
+      for (int c = tid; c < C::BN * (C::KV_CH + C::V_CH); c += C::NT) {
+        const int which = c < C::BN * C::KV_CH ? 0 : 1;
+        const int nch = which ? C::V_CH : C::KV_CH;
         const int cc = c - which * (C::BN * C::KV_CH);
-        const int r = cc / C::KV_CH, ch = cc % C::KV_CH;
-        const uint4 w = *reinterpret_cast<const uint4*>(raw + which * C::TILE_BYTES + r * C::KVROW + ch * 16);
+        const int r = cc / nch, ch = cc % nch;
+        const uint4 w = *reinterpret_cast<const uint4*>(raw + which * C::TILE_BYTES +
+                                                        r * (which ? C::VVROW : C::KVROW) + ch * 16);
         uint4 a, bq;
         a.x = e4m3x2_to_bf16x2((uint16_t)(w.x & 0xffff));
         a.y = e4m3x2_to_bf16x2((uint16_t)(w.x >> 16));
@@ -247,8 +260,9 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
         bq.z = e4m3x2_to_bf16x2((uint16_t)(w.w & 0xffff));
         bq.w = e4m3x2_to_bf16x2((uint16_t)(w.w >> 16));
         uint8_t* dst = sConv + which * (C::BN * C::QROW);
-        *reinterpret_cast<uint4*>(dst + swz(r, 2 * ch, C::QROW)) = a;
-        *reinterpret_cast<uint4*>(dst + swz(r, 2 * ch + 1, C::QROW)) = bq;
+        const int rb = which ? C::VROW : C::QROW;
+        *reinterpret_cast<uint4*>(dst + swz(r, 2 * ch, rb)) = a;
+        *reinterpret_cast<uint4*>(dst + swz(r, 2 * ch + 1, rb)) = bq;
       }
       __syncthreads();
       sK = sConv;
@@ -357,7 +371,7 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
       l_lo = l_lo * a_lo + sum_lo;
       l_hi = l_hi * a_hi + sum_hi;
 #pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
+      for (int j = 0; j < DV / 8; ++j) {
         o[j][0] *= a_lo;
         o[j][1] *= a_lo;
         o[j][2] *= a_hi;
@@ -372,11 +386,11 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
         pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
         pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
 #pragma unroll
-        for (int dj = 0; dj < D / 16; ++dj) {
+        for (int dj = 0; dj < DV / 16; ++dj) {
           uint32_t b0, b1, b2, b3;
           const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
           const int ch = 2 * dj + (lane >> 4);
-          ldsm_x4_t(smem_u32(sV + swz(key, ch, C::QROW)), b0, b1, b2, b3);
+          ldsm_x4_t(smem_u32(sV + swz(key, ch, C::VROW)), b0, b1, b2, b3);
           mma_bf16_16816(o[2 * dj], pa, b0, b1);
           mma_bf16_16816(o[2 * dj + 1], pa, b2, b3);
         }
@@ -407,29 +421,29 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1)
       const int rr = row0 + rl;
       const int t = rr / G, g = rr - t * G;
       const size_t orow = (size_t)(qo0 + t) * p.h_q + (size_t)h * G + g;
-      uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + orow * D);
+      uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + orow * DV);
 #pragma unroll
-      for (int j = 0; j < D / 8; ++j)
+      for (int j = 0; j < DV / 8; ++j)
         dst[j * 4 + tq] = pack_bf16x2(o[j][2 * half] * inv, o[j][2 * half + 1] * inv);
       if (p.lse && tq == 0) p.lse[orow] = lse;
     } else {
       const size_t prow = (size_t)it.part_row + rl;
-      float2* dst = reinterpret_cast<float2*>(p.part_out + prow * D);
+      float2* dst = reinterpret_cast<float2*>(p.part_out + prow * DV);
 #pragma unroll
-      for (int j = 0; j < D / 8; ++j)
+      for (int j = 0; j < DV / 8; ++j)
         dst[j * 4 + tq] = make_float2(o[j][2 * half] * inv, o[j][2 * half + 1] * inv);
       if (tq == 0) p.part_lse[prow] = lse;
     }
   }
 }
 
-template <int D, bool FP8, int NW>
+template <int D, int DV, bool FP8, int NW>
 cudaError_t launch_variant(const PartialParams& p, int n_items, cudaStream_t stream) {
   // 8 warps: one CTA per SM, 4 tiles in flight; 4 warps: two CTAs per SM, 3 each.
   constexpr int STAGES = NW == 8 ? 4 : 3;
-  using C = MmaCfg<D, FP8, NW, STAGES>;
+  using C = MmaCfg<D, DV, FP8, NW, STAGES>;
   static_assert(C::SMEM <= (NW == 8 ? 227 * 1024 : 113 * 1024), "shared memory budget");
-  auto kern = verify_partial_mma_kernel<D, FP8, NW, STAGES>;
+  auto kern = verify_partial_mma_kernel<D, DV, FP8, NW, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PartialParams*>(&p)};
@@ -439,22 +453,23 @@ cudaError_t launch_variant(const PartialParams& p, int n_items, cudaStream_t str
 
 }  // namespace
 
-cudaError_t launch_partial_mma(const PartialParams& p, int kernel, int head_dim, bool kv_fp8,
-                               int n_items, cudaStream_t stream) {
+template <int D, int DV>
+static cudaError_t launch_shape(const PartialParams& p, bool w4, bool kv_fp8, int n_items,
+                         cudaStream_t stream) {
+  if (kv_fp8) return w4 ? launch_variant<D, DV, true, 4>(p, n_items, stream)
+                        : launch_variant<D, DV, true, 8>(p, n_items, stream);
+  return w4 ? launch_variant<D, DV, false, 4>(p, n_items, stream)
+            : launch_variant<D, DV, false, 8>(p, n_items, stream);
+}
+
+cudaError_t launch_partial_mma(const PartialParams& p, int kernel, int head_dim, int head_dim_v,
+                               bool kv_fp8, int n_items, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
   const bool w4 = kernel == kKernelMma64;
-  if (head_dim == 128) {
-    if (kv_fp8) return w4 ? launch_variant<128, true, 4>(p, n_items, stream)
-                          : launch_variant<128, true, 8>(p, n_items, stream);
-    return w4 ? launch_variant<128, false, 4>(p, n_items, stream)
-              : launch_variant<128, false, 8>(p, n_items, stream);
-  }
-  if (head_dim == 64) {
-    if (kv_fp8) return w4 ? launch_variant<64, true, 4>(p, n_items, stream)
-                          : launch_variant<64, true, 8>(p, n_items, stream);
-    return w4 ? launch_variant<64, false, 4>(p, n_items, stream)
-              : launch_variant<64, false, 8>(p, n_items, stream);
-  }
+  if (head_dim == 128 && head_dim_v == 128) return launch_shape<128, 128>(p, w4, kv_fp8, n_items, stream);
+  if (head_dim == 64 && head_dim_v == 64) return launch_shape<64, 64>(p, w4, kv_fp8, n_items, stream);
+  if (head_dim == 128 && head_dim_v == 64) return launch_shape<128, 64>(p, w4, kv_fp8, n_items, stream);
+  if (head_dim == 64 && head_dim_v == 128) return launch_shape<64, 128>(p, w4, kv_fp8, n_items, stream);
   return cudaErrorInvalidValue;
 }
 

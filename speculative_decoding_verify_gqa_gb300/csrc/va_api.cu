@@ -294,7 +294,7 @@ static int verify_attn_merge_impl(const int32_t* qo_indptr, int num_qo_heads, in
   m.h_kv = hd->h_kv;
   m.group = hd->group;
   m.early_inputs = early;
-  cudaError_t e = launch_merge(m, hd->head_dim, hd->n_merge, hd->block_rows,
+  cudaError_t e = launch_merge(m, (int)hd->head_dim_v, hd->n_merge, hd->block_rows,
                                static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
 }
@@ -334,7 +334,8 @@ static int run_partial(const void* q, const void* k_cache, const void* v_cache,
                           (hd->flags & kPlanF8Mma) != 0,
                           static_cast<cudaStream_t>(stream));
   } else {
-    e = launch_partial_mma(p, hd->kernel, hd->head_dim, hd->kv_dtype == VA_DTYPE_FP8_E4M3,
+    e = launch_partial_mma(p, hd->kernel, hd->head_dim, (int)hd->head_dim_v,
+                           hd->kv_dtype == VA_DTYPE_FP8_E4M3,
                            hd->n_items, static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
@@ -628,6 +629,9 @@ static int append_impl(const void* k_new, const void* v_new, const int32_t* appe
   if (rc) return rc;
   if (o.kv_layout != VA_LAYOUT_HND && o.kv_layout != VA_LAYOUT_NHD) return VA_ERR_INVALID_ARGUMENT;
   if (o.quantize != 0 && o.quantize != 1) return VA_ERR_INVALID_ARGUMENT;
+  if (o.head_dim_v < 0) return VA_ERR_INVALID_ARGUMENT;
+  const int head_dim_v = o.head_dim_v ? o.head_dim_v : head_dim;
+  if (head_dim_v != 64 && head_dim_v != 128) return VA_ERR_UNSUPPORTED;
   if (o.quantize && (kv_dtype != VA_DTYPE_FP8_E4M3 || !(isfinite(o.k_scale) && o.k_scale > 0.f) ||
                      !(isfinite(o.v_scale) && o.v_scale > 0.f)))
     return VA_ERR_INVALID_ARGUMENT;
@@ -661,8 +665,11 @@ static int append_impl(const void* k_new, const void* v_new, const int32_t* appe
   p.log2_page = log2_int(page_size);
   p.num_pages = num_pages;
   p.cache_fp8 = kv_dtype == VA_DTYPE_FP8_E4M3;
-  p.row_chunks = head_dim * (p.cache_fp8 ? 1 : 2) / 16;
+  p.k_chunks = head_dim * (p.cache_fp8 ? 1 : 2) / 16;
+  p.v_chunks = head_dim_v * (p.cache_fp8 ? 1 : 2) / 16;
+  p.row_chunks = std::max(p.k_chunks, p.v_chunks);
   p.head_dim = head_dim;
+  p.head_dim_v = head_dim_v;
   p.quant = o.quantize;
   p.nhd = o.kv_layout == VA_LAYOUT_NHD;
   p.k_scale = o.k_scale;
@@ -705,11 +712,17 @@ int verify_attn_append_run(const void* k_new, const void* v_new,
   const int early = run_options && run_options->early_reads ? 1 : 0;
   const int layout = append_options ? (int)append_options->kv_layout : VA_LAYOUT_HND;
   if (layout != ((hd->flags & kPlanNhd) ? VA_LAYOUT_NHD : VA_LAYOUT_HND)) return VA_ERR_PLAN_MISMATCH;
+  // the append's value rows are the plan's
+  va_append_options_t ao;
+  memset(&ao, 0, sizeof(ao));
+  if (append_options) ao = *append_options;
+  if (ao.head_dim_v != 0 && ao.head_dim_v != hd->head_dim_v) return VA_ERR_PLAN_MISMATCH;
+  ao.head_dim_v = (int)hd->head_dim_v;
   if (hd->total_qo > 0) {
     int* status = reinterpret_cast<int*>(static_cast<char*>(workspace_d) + hd->off_status);
     rc = append_impl(k_new, v_new, qo_indptr, kv_indptr, kv_indices, last_page_len, k_cache,
                      v_cache, hd->batch, num_kv_heads, head_dim, page_size, num_pages,
-                     (va_dtype)hd->kv_dtype, hd->total_qo, append_options, status, early, stream);
+                     (va_dtype)hd->kv_dtype, hd->total_qo, &ao, status, early, stream);
     if (rc) return rc;
   }
   // A plain copy (no quantisation, no rotation) stores exactly the bytes of

@@ -9,7 +9,7 @@
 namespace va {
 
 constexpr uint32_t kPlanMagic = 0x31504156u;  // "VAP1"
-constexpr uint32_t kPlanVersion = 2;
+constexpr uint32_t kPlanVersion = 3;
 
 // Key tile of the partial kernels (keys per pipeline stage).  Split chunks are
 // cut on multiples of it, so every tile starts on a page boundary whenever
@@ -74,11 +74,13 @@ struct PlanHeader {
   uint64_t plan_bytes;
   int64_t flags;    // feature bits of the call the plan serves (0: none)
   int64_t n_ctas;   // persistent tcgen05 variants: CTAs (item chains); 0 otherwise
-  uint64_t reserved[2];
+  int64_t head_dim_v;  // elements of a value row (v_cache, partials and out)
+  uint64_t reserved[1];
 };
 static_assert(sizeof(PlanHeader) == 184, "PlanHeader layout (read by the Python binding)");
 
 constexpr size_t kWsAlign = 256;
+constexpr int kMaxHeadDimV = 128;  // widest value row a plan may have
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace va

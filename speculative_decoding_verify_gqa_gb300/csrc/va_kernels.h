@@ -77,8 +77,10 @@ struct AppendParams {
   void* v_cache;
   int* status;                // nullable
   const int32_t* positions;   // nullable: RoPE position of each new token's key
-  int batch, h_kv, page_size, log2_page, num_pages, row_chunks;  // row_chunks: 16-byte chunks per cache row
-  int head_dim;
+  int batch, h_kv, page_size, log2_page, num_pages;
+  int row_chunks;             // threads per (token, head): max(k_chunks, v_chunks)
+  int k_chunks, v_chunks;     // 16-byte chunks of a K / V cache row
+  int head_dim, head_dim_v;   // elements of a K / V row
   int cache_fp8;              // cache dtype e4m3 (else bf16)
   int quant;                  // bf16 source rows into an e4m3 cache
   int nhd;                    // cache layout [pages, P, h_kv, d] (else [pages, h_kv, P, d])
@@ -133,8 +135,8 @@ inline cudaError_t launch_kernel(const void* func, dim3 grid, dim3 block, size_t
 
 // Launchers: return the launch's cudaError_t (cudaErrorInvalidValue for a
 // variant that is not compiled).
-cudaError_t launch_partial_mma(const PartialParams& p, int kernel, int head_dim, bool kv_fp8,
-                               int n_items, cudaStream_t stream);
+cudaError_t launch_partial_mma(const PartialParams& p, int kernel, int head_dim, int head_dim_v,
+                               bool kv_fp8, int n_items, cudaStream_t stream);
 
 // TMA descriptors of the tensor-core variant: q as [total_qo, h_q, 128] bf16
 // with 64 x G x (128 / G) boxes, 128-byte swizzle.  A bf16 cache

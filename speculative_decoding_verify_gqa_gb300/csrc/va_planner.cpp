@@ -70,7 +70,8 @@ int plan_bounds(int batch, int64_t total_qo, int num_qo_heads, int num_kv_heads,
   size_t pb = sizeof(PlanHeader) + (size_t)(items + units) * 32;
   size_t ws = kWsAlign + (size_t)(items + units) * 32;
   ws = align_up(ws, kWsAlign) + (size_t)part_rows * 4;
-  ws = align_up(ws, kWsAlign) + (size_t)part_rows * head_dim * 4;
+  // partial rows of the widest value row a plan may have (head_dim_v <= 128)
+  ws = align_up(ws, kWsAlign) + (size_t)part_rows * std::max(head_dim, kMaxHeadDimV) * 4;
   *plan_bytes = pb;
   *workspace_bytes = align_up(ws, kWsAlign);
   return VA_OK;
@@ -96,6 +97,9 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   const bool full_mask = o.mask_layout == VA_MASK_FULL;
   if (o.q_fp8 != 0 && o.q_fp8 != 1) return VA_ERR_INVALID_ARGUMENT;
   if (o.draft_items < -1 || o.draft_items > 1) return VA_ERR_INVALID_ARGUMENT;
+  if (o.head_dim_v < 0) return VA_ERR_INVALID_ARGUMENT;
+  const int dv = o.head_dim_v ? o.head_dim_v : head_dim;
+  if (dv != 64 && dv != 128) return VA_ERR_UNSUPPORTED;
   if (o.q_fp8 && kv_dtype != VA_DTYPE_FP8_E4M3) return VA_ERR_UNSUPPORTED;
   if (full_mask && !has_mask) return VA_ERR_INVALID_ARGUMENT;
   if (o.kernel != VA_KERNEL_AUTO && o.kernel != VA_KERNEL_MMA_64 && o.kernel != VA_KERNEL_MMA_128 &&
@@ -130,7 +134,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
 
   // The tensor-core variant serves head_dim 128, page sizes that are multiples
   // of its 16-row TMA boxes, and groups that tile its 128 rows.
-  const bool tc_ok = head_dim == 128 && page_size % 16 == 0 && 128 % G == 0;
+  const bool tc_ok = head_dim == 128 && dv == head_dim && page_size % 16 == 0 && 128 % G == 0;
   int kernel = o.kernel;
   if ((kernel == VA_KERNEL_TC_128 || kernel == VA_KERNEL_TC_256) && !tc_ok) return VA_ERR_UNSUPPORTED;
   // e4m3 MMAs exist in the tcgen05 variants only
@@ -182,14 +186,14 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
       (int64_t)num_sms * (kernel == kKernelTc128 ? (kv_dtype == VA_DTYPE_BF16 ? 2 : 1)
                                                 : kernel_ctas_per_sm(kernel));
   const int es = kv_dtype == VA_DTYPE_FP8_E4M3 ? 1 : 2;
-  const int64_t key_bytes = 2LL * head_dim * es;
+  const int64_t key_bytes = (int64_t)(head_dim + dv) * es;
   // fixed cost of a work item (prologue, pipeline fill and drain, epilogue)
   // in K/V-byte equivalents: about one key tile for both variants (the
   // persistent tcgen05 CTAs overlap part of it with the previous item); on
   // GB300 the fp8 wide tree measured 407 us with 7 splits per unit against
   // 447 us with 2, which a larger value would have chosen
   const int64_t fixed_bytes = kernel_is_tc(kernel) ? 64 * 1024 : 48 * 1024;
-  const int64_t partial_bytes_per_row = 4LL * head_dim;
+  const int64_t partial_bytes_per_row = 4LL * dv;
   int64_t min_chunk = o.min_chunk > 0 ? o.min_chunk : 2 * TK;
   min_chunk = ceil_div(min_chunk, TK) * TK;
   auto chunk_for = [&](int64_t target) {
@@ -414,6 +418,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   hd.h_q = num_qo_heads;
   hd.h_kv = num_kv_heads;
   hd.head_dim = head_dim;
+  hd.head_dim_v = dv;
   hd.page_size = page_size;
   hd.q_dtype = q_dtype;
   hd.kv_dtype = kv_dtype;
@@ -434,7 +439,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   hd.off_merge = hd.off_items + items.size() * sizeof(WorkItem);
   hd.off_part_lse = align_up(hd.off_merge + merges.size() * sizeof(MergeItem), kWsAlign);
   hd.off_part_out = align_up(hd.off_part_lse + (size_t)part_rows * 4, kWsAlign);
-  hd.ws_bytes = align_up(hd.off_part_out + (size_t)part_rows * head_dim * 4, kWsAlign);
+  hd.ws_bytes = align_up(hd.off_part_out + (size_t)part_rows * dv * 4, kWsAlign);
   hd.plan_bytes = need;
   hd.n_ctas = n_ctas;
   hd.flags = (full_mask ? kPlanMaskFull : 0) | (o.kv_layout == VA_LAYOUT_NHD ? kPlanNhd : 0) |

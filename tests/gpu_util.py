@@ -37,16 +37,17 @@ class DeviceWorkload:
         self.mask_indptr = None if wl.mask_indptr is None else to_dev(wl.mask_indptr, dev)
         shape = ((wl.num_pages, wl.page_size, wl.h_kv, wl.d) if wl.nhd
                  else (wl.num_pages, wl.h_kv, wl.page_size, wl.d))
+        vshape = shape[:3] + (wl.dv,)
         self.q_pos = None if wl.q_pos is None else to_dev(wl.q_pos, dev)
         self.kv_pos = None if wl.kv_pos is None else to_dev(wl.kv_pos, dev)
         self.new_pos = None if wl.kv_pos is None else to_dev(wl.new_positions(), dev)
         # 0xFF bytes: NaN in bf16 and in fp8-e4m3
         if fp8:
             self.k_cache = torch.full(shape, 0xFF, dtype=torch.uint8, device=dev).view(self.kvd)
-            self.v_cache = torch.full(shape, 0xFF, dtype=torch.uint8, device=dev).view(self.kvd)
+            self.v_cache = torch.full(vshape, 0xFF, dtype=torch.uint8, device=dev).view(self.kvd)
         else:
             self.k_cache = torch.full(shape, -1, dtype=torch.int16, device=dev).view(self.kvd)
-            self.v_cache = torch.full(shape, -1, dtype=torch.int16, device=dev).view(self.kvd)
+            self.v_cache = torch.full(vshape, -1, dtype=torch.int16, device=dev).view(self.kvd)
         kn, vn = wl.new_tokens()
         self.k_new = to_dev(kn.view(raw), dev, self.kvd)
         self.v_new = to_dev(vn.view(raw), dev, self.kvd)
@@ -71,8 +72,10 @@ class DeviceWorkload:
 
     def features(self):
         wl = self.wl
-        return dict(kv_layout=wl.kv_layout, mask_layout=wl.mask_layout,
-                    rope=wl.q_pos is not None)
+        f = dict(kv_layout=wl.kv_layout, mask_layout=wl.mask_layout, rope=wl.q_pos is not None)
+        if wl.dv != wl.d:
+            f["head_dim_v"] = wl.dv
+        return f
 
     def plan(self, **opts):
         import speculative_decoding_verify_gqa_gb300 as va
@@ -115,7 +118,7 @@ def compare(wl, out, lse, rows=None, caches=None, nthreads=None, strict=False, o
     |out - oracle| <= out_tol (1e-2 unless given) + half the bf16 spacing at
     the oracle value (the output is bf16: where |out| >= 4 that spacing alone
     exceeds 1e-2); strict=True asserts the plain out_tol on every element."""
-    o, l = host_out(out, lse, wl.d)
+    o, l = host_out(out, lse, wl.dv)
     ref_o, ref_l = oracle.verify_attn_workload(wl, rows=rows, caches=caches, nthreads=nthreads)
     if rows is not None:
         o, l = o[rows], l[rows]

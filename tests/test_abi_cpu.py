@@ -390,6 +390,15 @@ def test_plan_validation_codes(va):
     assert _plan_rc(va, *ok, kv_dtype=0, q_fp8=True) == -2     # bf16 cache
     assert _plan_rc(va, *ok, kv_dtype=1, q_fp8=True, kernel=2) == -2   # warp-level variant
     assert _plan_rc(va, *ok, kv_dtype=1, q_fp8=True, d=64) == -2
+    # a value width of its own: 64 or 128, warp-level variants only
+    assert _plan_rc(va, *ok, head_dim_v=64) == 0
+    assert _plan_rc(va, *ok, d=64, head_dim_v=128) == 0
+    assert _plan_rc(va, *ok, head_dim_v=96) == -2
+    assert _plan_rc(va, *ok, head_dim_v=-1) == -1
+    assert _plan_rc(va, *ok, head_dim_v=64, kernel=3) == -2
+    assert _plan_rc(va, *ok, head_dim_v=64, kernel=4) == -2
+    assert _plan_rc(va, *ok, head_dim_v=64, kv_dtype=1, q_fp8=True) == -2
+    assert _plan_rc(va, *ok, head_dim_v=128) == 0            # = head_dim: the ordinary plan
 
 
 def test_empty_batches_plan_to_nothing(va):

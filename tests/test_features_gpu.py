@@ -459,3 +459,74 @@ def test_layers_sharing_one_workspace(va, early_reads):
         wq = synthetic.make_workload("llama3_8b_tree_verify")
         wq.q = q.cpu().view(torch.int16).numpy().view(np.uint16)
         compare(wq, o, l, caches=(kc, vc), strict=True)
+
+
+# ------------------------------------------------------------------ value width dv != d
+
+DV_CASES = [
+    dict(d=128, dv=64, prefix=("fixed", [700, 0, 90]), qo=("fixed", [17, 40, 3]), mask="tree"),
+    dict(d=64, dv=128, prefix=("fixed", [300, 45]), qo=("fixed", [9, 5]), mask="causal"),
+    dict(d=128, dv=64, prefix=("fixed", [500, 63]), qo=("fixed", [12, 30]), mask="tree",
+         kv_dtype=synthetic.FP8),
+    dict(d=64, dv=128, prefix=("fixed", [200, 1000]), qo=("fixed", [6, 20]), mask="random",
+         kv_layout="nhd", mask_layout="full", prefix_visible="random"),
+]
+
+
+@pytest.mark.parametrize("kernel", [1, 2], ids=["mma64", "mma128"])
+@pytest.mark.parametrize("case", DV_CASES, ids=["d128_dv64_tree", "d64_dv128_chain",
+                                                "fp8_d128_dv64", "nhd_full_d64_dv128"])
+def test_value_width_matches_oracle(va, kernel, case):
+    """sglang's value head size dv != d (plan option head_dim_v): the append
+    writes K rows of d and V rows of dv elements (bit-exact against the
+    oracle's pools), and the warp-level kernels attend with them, unsplit and
+    split (merge over dv-wide partials), against the oracle row by row."""
+    wl = synthetic.make_custom(batch=len(case["prefix"][1]), h_q=8, h_kv=2, seed=151, **case)
+    dw = DeviceWorkload(wl)
+    kc, vc = oracle.build_cache(wl)
+    fp8 = wl.kv_dtype == synthetic.FP8
+    assert np.array_equal(_raw(dw.k_cache, fp8), kc) and np.array_equal(_raw(dw.v_cache, fp8), vc)
+    for splits in (1, 0):
+        out, lse, plan = dw.run(kernel=kernel, max_splits=splits, target_ctas=200, min_chunk=64)
+        torch.cuda.synchronize()
+        hd = plan.header()
+        assert hd["kernel"] == kernel and hd["head_dim_v"] == wl.dv
+        assert tuple(out.shape) == (wl.total_qo, wl.h_q, wl.dv)
+        assert va.verify_attn_device_status(plan) == 0
+        compare(wl, out, lse, caches=(kc, vc))
+
+
+def test_value_width_fused_call_and_quantising_append(va):
+    """The fused append + attention call with dv != d, through a plain copy
+    and through a quantising append into an fp8 cache."""
+    base = dict(batch=2, h_q=8, h_kv=2, d=128, dv=64, prefix=("fixed", [400, 33]),
+                qo=("fixed", [17, 6]), mask="tree", seed=152)
+    wl = synthetic.make_custom(**base)
+    dw = DeviceWorkload(wl)
+    plan = dw.plan()
+    assert plan.header()["head_dim_v"] == 64 and plan.header()["kernel"] in (1, 2)
+    out, lse = _fused(va, dw, plan)
+    torch.cuda.synchronize()
+    assert va.verify_attn_device_status(plan) == 0
+    kc, vc = oracle.build_cache(wl)
+    assert np.array_equal(_raw(dw.k_cache, False), kc) and np.array_equal(_raw(dw.v_cache, False), vc)
+    compare(wl, out, lse, caches=(kc, vc))
+    # quantising: bf16 drafts of the bf16 workload into the fp8 one's cache
+    wf = synthetic.make_custom(kv_dtype=synthetic.FP8, **base)
+    kn, vn = wl.new_tokens()
+    kcf, vcf = oracle.build_cache(wf)
+    oracle.paged_kv_append_ex(kn, vn, wf.qo_indptr, wf.kv_indptr, wf.kv_indices,
+                              wf.last_page_len, wf.page_size, wf.num_pages, kcf, vcf,
+                              cache_fp8=True, quantize=True, k_scale=wf.k_scale,
+                              v_scale=wf.v_scale)
+    dwf = DeviceWorkload(wf)
+    planf = dwf.plan()
+    out, lse = va.verify_attn_append_run(
+        to_dev(kn.view(np.int16), "cuda", torch.bfloat16),
+        to_dev(vn.view(np.int16), "cuda", torch.bfloat16), dwf.q, dwf.k_cache, dwf.v_cache,
+        dwf.kv_indptr, dwf.kv_indices, dwf.last_page_len, dwf.qo_indptr, dwf.mask,
+        dwf.mask_indptr, planf, sm_scale=wf.sm_scale, k_scale=wf.k_scale, v_scale=wf.v_scale,
+        append_k_scale=wf.k_scale, append_v_scale=wf.v_scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(_raw(dwf.k_cache, True), kcf) and np.array_equal(_raw(dwf.v_cache, True), vcf)
+    compare(wf, out, lse, caches=(kcf, vcf))
