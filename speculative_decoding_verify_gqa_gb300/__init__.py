@@ -171,28 +171,92 @@ def _host_i32(a) -> Optional[np.ndarray]:
     return np.ascontiguousarray(a, dtype=np.int32)
 
 
+def _addr(a: np.ndarray) -> int:
+    """Host address of a contiguous numpy array (a plain int).  Through a
+    ctypes view of the array's buffer when it is writable and not empty (a
+    fraction of the cost of numpy's .ctypes), else numpy's own."""
+    try:
+        return ctypes.addressof(ctypes.c_char.from_buffer(a))
+    except (TypeError, ValueError, BufferError):
+        return a.ctypes.data
+
+
 def _hp(a: Optional[np.ndarray]):
-    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    return None if a is None else _addr(a)
+
+
+# The last host buffer whose address was taken, kept referenced so that its
+# address stays valid: a caller that plans into the same buffer every step
+# pays the (slow) address lookup once.
+_LAST_HOST = [None]   # (array, address), replaced as one object
+
+
+def _hp_buf(a: np.ndarray) -> int:
+    cached = _LAST_HOST[0]
+    if cached is None or cached[0] is not a:
+        cached = (a, _addr(a))
+        _LAST_HOST[0] = cached
+    return cached[1]
+
+
+def _tables(*arrays):
+    """Host index arrays (int32) staged in one contiguous buffer: their
+    addresses (None for a missing one) and the buffer, which the caller keeps
+    alive for the call."""
+    parts = [a for a in arrays if a is not None]
+    buf = np.concatenate(parts) if parts else np.zeros(1, np.int32)
+    base = _addr(buf)
+    ptrs, off = [], 0
+    for a in arrays:
+        if a is None:
+            ptrs.append(None)
+        else:
+            ptrs.append(base + 4 * off)
+            off += a.shape[0]
+    return ptrs, buf
 
 
 def _dp(t: Optional[torch.Tensor]):
+    """Device address of a contiguous CUDA tensor (a plain int: ctypes
+    passes it as the void* argument)."""
     if t is None:
         return None
     if not t.is_cuda:
         raise ValueError("expected a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError("expected a contiguous tensor")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
-def _stream(stream) -> ctypes.c_void_p:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream) -> int:
+    """The cudaStream_t of `stream`, or of torch's current stream (read
+    through torch's raw-stream query when it has one: a fraction of the cost
+    of building a Stream object on every call)."""
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
-def _options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0, mask_layout="qlen",
-             kv_layout="hnd", rope=False, q_fp8=False, draft_items=0, head_dim_v=0):
+_OPTIONS_CACHE: dict = {}
+
+
+def _options(**kw):
+    """The PlanOptions struct of these keyword options (built once per
+    distinct set and kept: the library only reads it)."""
+    key = tuple(sorted(kw.items()))
+    o = _OPTIONS_CACHE.get(key)
+    if o is None:
+        o = _OPTIONS_CACHE[key] = _make_options(**kw)
+    return o
+
+
+def _make_options(max_splits=0, min_chunk=0, target_ctas=0, kernel=0, mask_layout="qlen",
+                  kv_layout="hnd", rope=False, q_fp8=False, draft_items=0, head_dim_v=0):
     o = PlanOptions()
     o.max_splits, o.min_chunk, o.target_ctas, o.kernel = (int(max_splits), int(min_chunk),
                                                           int(target_ctas), int(kernel))
@@ -279,7 +343,8 @@ def verify_attn_plan_host(kv_indptr_h, qo_indptr_h, last_page_len_h, mask_indptr
     host = np.zeros(pb, dtype=np.uint8)
     need = ctypes.c_size_t(0)
     opt = _options(**options)
-    rc = lib().verify_attn_plan_host(_hp(kvp), _hp(qop), _hp(lpl), _hp(mip), batch,
+    tp, _keep = _tables(kvp, qop, lpl, mip)
+    rc = lib().verify_attn_plan_host(*tp, batch,
                                      int(num_qo_heads), int(num_kv_heads), int(head_dim),
                                      int(page_size), 0, _kv_code(kv_dtype), int(bool(has_mask)),
                                      int(num_sms), ctypes.byref(opt), _hp(host), host.nbytes,
@@ -328,23 +393,31 @@ def verify_attn_plan(kv_indptr_h, qo_indptr_h, last_page_len_h, mask_indptr_h, n
         plan.workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8,
                                      device=device or "cuda")
         _check("verify_attn_plan_upload",
-               lib().verify_attn_plan_upload(_hp(plan.host), _dp(plan.workspace),
+               lib().verify_attn_plan_upload(_hp_buf(plan.host), _dp(plan.workspace),
                                              plan.workspace.numel(), _stream(stream)))
         return plan
-    pb, _ = verify_attn_plan_bounds(batch, total_qo, num_qo_heads, num_kv_heads, head_dim,
-                                    num_sms)
-    host = plan_buffer if plan_buffer is not None and plan_buffer.nbytes >= pb else \
-        np.zeros(pb, dtype=np.uint8)
-    rc = lib().verify_attn_plan(_hp(kvp), _hp(qop), _hp(lpl), _hp(mip), batch,
-                                int(num_qo_heads), int(num_kv_heads), int(head_dim),
-                                int(page_size), 0, _kv_code(kv_dtype), int(bool(has_mask)),
-                                int(num_sms), ctypes.byref(opt), _hp(host), host.nbytes,
-                                _dp(workspace), workspace.numel(), _stream(stream))
+    # the caller's host buffer first; sized from verify_attn_plan_bounds when
+    # there is none or the library reports it too small
+    host = plan_buffer
+    strm = _stream(stream)
+    tp, _keep = _tables(kvp, qop, lpl, mip)
+    for attempt in range(2):
+        if host is None:
+            pb, _ = verify_attn_plan_bounds(batch, total_qo, num_qo_heads, num_kv_heads,
+                                            head_dim, num_sms)
+            host = np.zeros(pb, dtype=np.uint8)
+        rc = lib().verify_attn_plan(*tp, batch,
+                                    int(num_qo_heads), int(num_kv_heads), int(head_dim),
+                                    int(page_size), 0, _kv_code(kv_dtype), int(bool(has_mask)),
+                                    int(num_sms), ctypes.byref(opt), _hp_buf(host), host.nbytes,
+                                    _dp(workspace), workspace.numel(), strm)
+        if rc != VA_ERR_PLAN_BUFFER_TOO_SMALL or attempt:
+            break
+        host = None
     _check("verify_attn_plan", rc)
-    plan = Plan(host, workspace, 0, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                _kv_code(kv_dtype), bool(has_mask), total_qo)
-    plan.workspace_bytes = plan.header()["ws_bytes"]
-    return plan
+    ws_bytes = int(host[136:144].view(np.uint64)[0])   # the header's workspace size
+    return Plan(host, workspace, ws_bytes, batch, num_qo_heads, num_kv_heads, head_dim,
+                page_size, _kv_code(kv_dtype), bool(has_mask), total_qo)
 
 
 def _run_args(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indptr, mask,
@@ -361,7 +434,7 @@ def _run_args(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len, qo_indp
             _dp(last_page_len), _dp(qo_indptr), _dp(mask), _dp(mask_indptr),
             plan.num_qo_heads, plan.num_kv_heads, plan.head_dim, plan.page_size,
             float(sm_scale), float(k_scale), float(v_scale), _dp(out), _dp(lse),
-            int(num_pages), _hp(plan.host), _dp(plan.workspace), plan.workspace.numel())
+            int(num_pages), _hp_buf(plan.host), _dp(plan.workspace), plan.workspace.numel())
 
 
 def _alloc_out(q, plan, out, lse, want_lse):
@@ -373,9 +446,15 @@ def _alloc_out(q, plan, out, lse, want_lse):
     return out, lse
 
 
+_EARLY_READS = RunOptions()
+_EARLY_READS.early_reads = 1
+
+
 def _run_options(q_position, rope_theta, rope_scale, early_reads=False):
     if q_position is None and not early_reads:
         return None
+    if q_position is None:
+        return _EARLY_READS   # shared: the library only reads it
     o = RunOptions()
     if q_position is not None:
         o.q_position = _dp(q_position)
@@ -427,7 +506,7 @@ def verify_attn_partial(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_le
 def verify_attn_merge(qo_indptr, plan: Plan, out, lse=None, stream=None):
     _check("verify_attn_merge",
            lib().verify_attn_merge(_dp(qo_indptr), plan.num_qo_heads, plan.num_kv_heads,
-                                   plan.head_dim, _dp(out), _dp(lse), _hp(plan.host),
+                                   plan.head_dim, _dp(out), _dp(lse), _hp_buf(plan.host),
                                    _dp(plan.workspace), plan.workspace.numel(), _stream(stream)))
     return out, lse
 
@@ -524,7 +603,7 @@ def verify_attn_append_run(k_new, v_new, q, k_cache, v_cache, kv_indptr, kv_indi
         _dp(v_cache), _dp(kv_indptr), _dp(kv_indices), _dp(last_page_len), _dp(qo_indptr),
         _dp(mask), _dp(mask_indptr), plan.num_qo_heads, plan.num_kv_heads, plan.head_dim,
         plan.page_size, float(sm_scale), float(k_scale), float(v_scale), _dp(out), _dp(lse),
-        int(num_pages), _hp(plan.host), _dp(plan.workspace), plan.workspace.numel(),
+        int(num_pages), _hp_buf(plan.host), _dp(plan.workspace), plan.workspace.numel(),
         None if ro is None else ctypes.byref(ro), _stream(stream))
     _check("verify_attn_append_run", rc)
     return out, lse
@@ -589,6 +668,6 @@ def verify_attn_run_static_scratch(q, k_cache, v_cache, kv_indptr, kv_indices, l
         _dp(q), _dp(k_cache), _dp(v_cache), _dp(kv_indptr), _dp(kv_indices), _dp(last_page_len),
         _dp(qo_indptr), _dp(mask), _dp(mask_indptr), plan.num_qo_heads, plan.num_kv_heads,
         plan.head_dim, plan.page_size, float(sm_scale), float(k_scale), float(v_scale), _dp(out),
-        _dp(lse), int(num_pages), _hp(plan.host), _stream(stream))
+        _dp(lse), int(num_pages), _hp_buf(plan.host), _stream(stream))
     _check("verify_attn_run_static_scratch", rc)
     return out, lse

@@ -18,7 +18,6 @@
 #include <algorithm>
 #include <cstring>
 #include <functional>
-#include <queue>
 #include <vector>
 
 #include "../../include/verify_attn.h"
@@ -265,13 +264,13 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
           for (int h = 0; h < num_kv_heads; ++h) costs.push_back(cost);
         }
       }
-      std::sort(costs.begin(), costs.end(), std::greater<int64_t>());
       // longest-first onto the least-loaded slot: the first `slots` items
       // each get an empty slot, so with no more items than slots the finish
       // is the longest item; otherwise a min-heap of the slot loads takes the
       // rest
-      int64_t finish = costs.empty() ? 0 : costs[0];
+      int64_t finish = costs.empty() ? 0 : *std::max_element(costs.begin(), costs.end());
       if ((int64_t)costs.size() > slots) {
+        std::sort(costs.begin(), costs.end(), std::greater<int64_t>());
         std::vector<int64_t> load(costs.begin(), costs.begin() + slots);
         std::make_heap(load.begin(), load.end(), std::greater<int64_t>());
         for (size_t k = (size_t)slots; k < costs.size(); ++k) {
@@ -360,8 +359,9 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   if (part_rows > INT32_MAX) return VA_ERR_UNSUPPORTED;
   // Longest first; among equals, row blocks that read the same (request, KV
   // head, kv chunk) sit next to each other so they run together and the
-  // later ones find the chunk in L2.
-  std::stable_sort(items.begin(), items.end(), [](const Tmp& a, const Tmp& b) {
+  // later ones find the chunk in L2.  (b, h, kv_lo, row0) identifies an item,
+  // so the order is total.
+  std::sort(items.begin(), items.end(), [](const Tmp& a, const Tmp& b) {
       if (a.cost != b.cost) return a.cost > b.cost;
       if (a.it.b != b.it.b) return a.it.b < b.it.b;
       if (a.it.h != b.it.h) return a.it.h < b.it.h;
@@ -376,32 +376,52 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   int64_t n_ctas = 0;
   if (kernel_is_tc(kernel) && !items.empty()) {
     n_ctas = std::min<int64_t>((int64_t)items.size(), num_sms);
-    std::vector<std::vector<int64_t>> chain(n_ctas);
-    std::priority_queue<std::pair<int64_t, int64_t>, std::vector<std::pair<int64_t, int64_t>>,
-                        std::greater<std::pair<int64_t, int64_t>>> load;
-    for (int64_t c = 0; c < n_ctas; ++c) load.push({0, c});
-    for (size_t i = 0; i < items.size(); ++i) {
-      const auto top = load.top();
-      load.pop();
-      chain[top.second].push_back((int64_t)i);
-      const WorkItem& w = items[i].it;
-      // key tiles plus one of overhead; a tile of two Q tiles costs 5/3 of one
-      const int64_t tiles = ceil_div(w.kv_hi - w.kv_lo, TK) + 1;
-      load.push({top.first + tiles * (w.nrows > kTcRowsPerTile ? 5 : 3), top.second});
-    }
-    std::vector<Tmp> out;
-    out.reserve(items.size());
-    for (int64_t c = 0; c < n_ctas; ++c) out.push_back(items[chain[c][0]]);
-    for (int64_t c = 0; c < n_ctas; ++c) {
-      int32_t prev = (int32_t)c;
-      for (size_t k = 1; k < chain[c].size(); ++k) {
-        out.push_back(items[chain[c][k]]);
-        out[prev].it.next = (int32_t)(out.size() - 1);
-        prev = (int32_t)(out.size() - 1);
+    if ((int64_t)items.size() <= n_ctas) {
+      // one item per CTA: item c is chain c
+      for (auto& t : items) t.it.next = -1;
+    } else {
+      // LPT: each item (longest first) to the least-loaded chain, kept in a
+      // min-heap of (load, chain); then the items are laid out chain by
+      // chain (a counting sort on the owner), chain c's first at index c
+      std::vector<std::pair<int64_t, int64_t>> load((size_t)n_ctas);
+      for (int64_t c = 0; c < n_ctas; ++c) load[(size_t)c] = {0, c};
+      auto later = std::greater<std::pair<int64_t, int64_t>>();
+      std::vector<int32_t> owner(items.size());
+      for (size_t i = 0; i < items.size(); ++i) {
+        std::pop_heap(load.begin(), load.end(), later);
+        auto& top = load.back();
+        owner[i] = (int32_t)top.second;
+        const WorkItem& w = items[i].it;
+        // key tiles plus one of overhead; a tile of two Q tiles costs 5/3 of one
+        const int64_t tiles = ceil_div(w.kv_hi - w.kv_lo, TK) + 1;
+        top.first += tiles * (w.nrows > kTcRowsPerTile ? 5 : 3);
+        std::push_heap(load.begin(), load.end(), later);
       }
-      out[prev].it.next = -1;
+      // chain c: its first item at index c, the rest after all the firsts, in
+      // chain order, each linked to the next
+      std::vector<int32_t> count((size_t)n_ctas, 0), first((size_t)n_ctas, -1);
+      for (size_t i = 0; i < items.size(); ++i) ++count[(size_t)owner[i]];
+      std::vector<int64_t> start((size_t)n_ctas + 1, 0);  // of the chains' tails
+      for (int64_t c = 0; c < n_ctas; ++c) start[(size_t)c + 1] = start[(size_t)c] + count[(size_t)c] - 1;
+      std::vector<Tmp> out(items.size());
+      std::vector<int64_t> fill(start.begin(), start.end() - 1);
+      std::vector<int32_t> last((size_t)n_ctas, -1);
+      for (size_t i = 0; i < items.size(); ++i) {
+        const int32_t c = owner[i];
+        int64_t pos;
+        if (first[(size_t)c] < 0) {
+          pos = c;
+          first[(size_t)c] = c;
+        } else {
+          pos = n_ctas + fill[(size_t)c]++;
+        }
+        out[(size_t)pos] = items[i];
+        out[(size_t)pos].it.next = -1;
+        if (last[(size_t)c] >= 0) out[(size_t)last[(size_t)c]].it.next = (int32_t)pos;
+        last[(size_t)c] = (int32_t)pos;
+      }
+      items.swap(out);
     }
-    items.swap(out);
   }
 
   size_t need = sizeof(PlanHeader) + items.size() * sizeof(WorkItem) +
