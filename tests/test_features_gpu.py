@@ -256,12 +256,16 @@ def _fused(va, dw, plan, out=None, lse=None, **kw):
                                      positions=dw.new_pos, kv_layout=wl.kv_layout, **kw)
 
 
-@pytest.mark.parametrize("name", ["tiny_verify", "llama3_8b_tree_verify", "codellama34b_chain_verify"])
-def test_append_run_matches_oracle(va, name):
+@pytest.mark.parametrize("early_reads", [False, True], ids=["plain", "early_reads"])
+@pytest.mark.parametrize("name", synthetic.WORKLOAD_ORDER)
+def test_append_run_matches_oracle(va, name, early_reads):
     """verify_attn_append_run (the drafts appended and attended in one call,
     the attention reading q and the prefix while the append runs) on a pool
-    whose draft slots still hold NaN: every row against the oracle, and the
-    pool equal to the oracle's, bit for bit."""
+    whose draft slots still hold NaN, for every named workload at full size;
+    with early_reads this is the launch configuration the benchmark times
+    (and the plan's automatic draft items read the drafts from k_new / v_new):
+    every row against the oracle at the strict bound, and the pool equal to
+    the oracle's, bit for bit."""
     wl = synthetic.make_workload(name)
     dw = DeviceWorkload(wl, append=False)
     # prefix only: the drafts' slots keep the NaN sentinel until the fused call
@@ -284,7 +288,7 @@ def test_append_run_matches_oracle(va, name):
                        to_dev(kvp, "cuda"), to_dev(np.concatenate(idx).astype(np.int32), "cuda"),
                        to_dev(lpl, "cuda"), dw.k_cache, dw.v_cache)
     plan = dw.plan()
-    out, lse = _fused(va, dw, plan)
+    out, lse = _fused(va, dw, plan, early_reads=early_reads)
     torch.cuda.synchronize()
     assert va.verify_attn_device_status(plan) == 0
     kc, vc = oracle.build_cache(wl)
