@@ -513,11 +513,21 @@ int verify_accept_greedy(const void* logits, va_dtype logits_dtype, int64_t tota
  *    kernels.  All calls share the one array, which keeps the last call's
  *    contents: calls that can overlap on the GPU (different streams, or
  *    devices sharing the array's context) race and must be serialised by the
- *    caller.  Device-side check bits are not reported by this entry point.
+ *    caller.  Device-side check bits stay in the array's status word until
+ *    the next call clears it: verify_attn_static_scratch_status reads them.
  * Errors: as verify_attn_run, plus VA_ERR_STATIC_SCRATCH_TOO_SMALL, and
  * VA_ERR_CUDA if the address look-up or an enqueue fails.
  */
 #define VA_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+/*
+ * The device-side check bits (VA_DEV_*) of the last
+ * verify_attn_run_static_scratch call in the current context, as
+ * verify_attn_device_status reads a workspace's: copied out on `stream`
+ * (which is synchronised) and cleared; allocates nothing.  Returns VA_OK with
+ * *bits = 0, VA_ERR_DEVICE_CHECK with the bits set, VA_ERR_INVALID_ARGUMENT
+ * (bits NULL) or VA_ERR_CUDA.
+ */
+int verify_attn_static_scratch_status(int* bits, void* stream);
 int verify_attn_run_static_scratch(const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* kv_indptr, const int32_t* kv_indices,
                                    const int32_t* last_page_len, const int32_t* qo_indptr,

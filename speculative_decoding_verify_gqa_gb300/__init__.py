@@ -133,6 +133,7 @@ def lib():
                                   P]),
         "verify_attn_run_static_scratch": (i32, [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32,
                                                  f32, f32, f32, P, P, i32, P, P]),
+        "verify_attn_static_scratch_status": (i32, [Pi, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -650,6 +651,16 @@ def verify_accept_greedy(logits, qo_indptr, draft_tokens, parents, workspace=Non
 
 
 STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def verify_attn_static_scratch_status(stream=None) -> int:
+    """Device check bits (VA_DEV_*) of the last static-scratch call in this
+    context; cleared by the read.  0 when every check passed."""
+    bits = ctypes.c_int(0)
+    rc = lib().verify_attn_static_scratch_status(ctypes.byref(bits), _stream(stream))
+    if rc not in (VA_OK, VA_ERR_DEVICE_CHECK):
+        _check("verify_attn_static_scratch_status", rc)
+    return bits.value
 
 
 def verify_attn_run_static_scratch(q, k_cache, v_cache, kv_indptr, kv_indices, last_page_len,

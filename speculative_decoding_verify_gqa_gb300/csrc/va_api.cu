@@ -613,6 +613,15 @@ int verify_attn_device_status(void* workspace_d, int* bits, void* stream) {
   return v ? VA_ERR_DEVICE_CHECK : VA_OK;
 }
 
+int verify_attn_static_scratch_status(int* bits, void* stream) {
+  if (!bits) return VA_ERR_INVALID_ARGUMENT;
+  void* scratch = nullptr;
+  const int rc = static_scratch_address(&scratch);
+  if (rc) return rc;
+  // the status word is the scratch's first word (every plan's off_status)
+  return verify_attn_device_status(scratch, bits, stream);
+}
+
 static int append_impl(const void* k_new, const void* v_new, const int32_t* append_indptr,
                        const int32_t* kv_indptr, const int32_t* kv_indices,
                        const int32_t* last_page_len, void* k_cache, void* v_cache, int batch,

@@ -107,3 +107,29 @@ def test_static_scratch_refuses_plans_beyond_its_size(va):
         ctypes.c_float(0.0), ctypes.c_float(1.0), ctypes.c_float(1.0), fake, None, 10,
         va._hp(plan.host), None)
     assert rc == -8
+
+
+def test_static_scratch_status_reports_device_checks(va):
+    """The static array's status word: 0 after a clean call; a page id
+    outside the pool (which the kernels skip, zero-fill and flag) raises
+    VA_DEV_BAD_PAGE, read once by verify_attn_static_scratch_status and
+    cleared by the read."""
+    wl = synthetic.make_custom(batch=2, h_q=4, h_kv=2, d=128, prefix=("fixed", [100, 100]),
+                               qo=("fixed", [3, 3]), mask="causal", seed=23)
+    dw = DeviceWorkload(wl)
+    hplan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, None,
+                                     wl.h_q, wl.h_kv, wl.d, wl.page_size)
+    args = (dw.q, dw.k_cache, dw.v_cache, dw.kv_indptr, dw.kv_indices, dw.last_page_len,
+            dw.qo_indptr, None, None, hplan)
+    va.verify_attn_run_static_scratch(*args, sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert va.verify_attn_static_scratch_status() == 0
+    bad = wl.kv_indices.copy()
+    bad[wl.kv_indptr[1] + 1] = 1 << 30          # request 1, second page
+    out, lse = va.verify_attn_run_static_scratch(
+        dw.q, dw.k_cache, dw.v_cache, dw.kv_indptr, torch.from_numpy(bad).cuda(),
+        dw.last_page_len, dw.qo_indptr, None, None, hplan, sm_scale=wl.sm_scale)
+    torch.cuda.synchronize()
+    assert va.verify_attn_static_scratch_status() & 1     # VA_DEV_BAD_PAGE
+    assert va.verify_attn_static_scratch_status() == 0    # cleared by the read
+    assert torch.isfinite(out.float()).all()
