@@ -210,6 +210,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     return ceil_div(u.kv_end, *cu);
   };
   int64_t chunk;
+  double best_lpt = -1.0;  // the chosen split candidate's estimated finish
   bool equal = true;
   if (o.target_ctas > 0) {
     chunk = chunk_for(std::min<int64_t>(o.target_ctas, kMaxTargetPerSm * num_sms));
@@ -286,6 +287,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
         equal = eq;
       }
     }
+    best_lpt = best;
   }
 
   struct Tmp {
@@ -296,6 +298,85 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   std::vector<MergeItem> merges;
   int64_t part_rows = 0;
   std::vector<int64_t> cuts;
+  int64_t n_ctas = 0;
+
+  // Stream cut (two-Q-tile persistent kernel): the key tiles of every unit,
+  // unit after unit, cut into one run of equal length per CTA; a CTA's run is
+  // its chain of items (pieces of the units it crosses), and only the units a
+  // run boundary falls inside are merged -- fewer and larger partials than
+  // cutting every unit, at the same balance.  Scored with the same cost
+  // model as the split candidates and taken when clearly cheaper.
+  bool stream = false;
+  if (kernel == kKernelTc256 && o.target_ctas == 0 && o.max_splits == 0 && o.draft_items != 1 &&
+      best_lpt > 0) {
+    int64_t total = 0;
+    for (const Unit& u : units) total += ceil_div(u.kv_end, TK) * num_kv_heads;
+    const int64_t n = std::min<int64_t>(num_sms, total);
+    // run c covers global tiles [run_lo(c), run_lo(c + 1))
+    auto run_lo = [&](int64_t c) { return c * total / n; };
+    std::vector<int64_t> cost((size_t)n, 0);
+    int64_t g = 0, c = 0;
+    for (const Unit& u : units) {
+      const int64_t T = ceil_div(u.kv_end, TK);
+      for (int h = 0; h < num_kv_heads; ++h, g += T) {
+        while (run_lo(c + 1) <= g) ++c;
+        const bool split = run_lo(c + 1) < g + T;
+        for (int64_t cc = c, t = g; t < g + T; ++cc) {
+          const int64_t t1 = std::min(g + T, run_lo(cc + 1));
+          const int64_t keys = std::min<int64_t>((t1 - g) * TK, u.kv_end) - (t - g) * TK;
+          cost[(size_t)cc] += fixed_bytes + keys * key_bytes +
+                              (split ? (int64_t)u.nrows * partial_bytes_per_row : 0);
+          t = t1;
+        }
+      }
+    }
+    const int64_t finish = *std::max_element(cost.begin(), cost.end());
+    if ((double)finish < best_lpt * 0.97) {
+      stream = true;
+      n_ctas = n;
+      std::vector<std::vector<Tmp>> runs;  // pieces of each run, in order (one plan's worth)
+      runs.resize((size_t)n);
+      g = 0;
+      c = 0;
+      for (const Unit& u : units) {
+        const int64_t T = ceil_div(u.kv_end, TK);
+        for (int h = 0; h < num_kv_heads; ++h, g += T) {
+          while (run_lo(c + 1) <= g) ++c;
+          int64_t pieces = 0;
+          for (int64_t cc = c, t = g; t < g + T; ++cc, ++pieces) t = std::min(g + T, run_lo(cc + 1));
+          int64_t base = -1;
+          if (pieces > 1) {
+            base = part_rows;
+            merges.push_back({u.b, h, u.row0, u.nrows, (int32_t)base, (int32_t)pieces, 0, 0});
+            part_rows += pieces * u.nrows;
+          }
+          int64_t s = 0;
+          for (int64_t cc = c, t = g; t < g + T; ++cc, ++s) {
+            const int64_t t1 = std::min(g + T, run_lo(cc + 1));
+            const int32_t lo = (int32_t)((t - g) * TK);
+            const int32_t hi = (int32_t)std::min<int64_t>((t1 - g) * TK, u.kv_end);
+            WorkItem w{u.b, h, u.row0, u.nrows, lo, hi,
+                       base >= 0 ? (int32_t)(base + s * u.nrows) : -1, -1};
+            runs[(size_t)cc].push_back({w, (int64_t)(hi - lo) * (u.nrows + 16)});
+            t = t1;
+          }
+        }
+      }
+      // chain c's first piece at index c, the rest after all the firsts
+      for (int64_t cc = 0; cc < n; ++cc) items.push_back(runs[(size_t)cc].front());
+      for (int64_t cc = 0; cc < n; ++cc) {
+        int32_t prev = (int32_t)cc;
+        for (size_t k = 1; k < runs[(size_t)cc].size(); ++k) {
+          items.push_back(runs[(size_t)cc][k]);
+          items[(size_t)prev].it.next = (int32_t)(items.size() - 1);
+          prev = (int32_t)(items.size() - 1);
+        }
+        items[(size_t)prev].it.next = -1;
+      }
+    }
+  }
+
+  if (!stream) {
   // Draft items: with few units next to the CTAs (the latency-bound verify
   // shapes, whose units are split many ways), a split unit's drafts -- keys
   // prefix .. kv_end, at most one key tile -- become an item of their own,
@@ -356,12 +437,13 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
       }
     }
   }
+  }  // !stream
   if (part_rows > INT32_MAX) return VA_ERR_UNSUPPORTED;
   // Longest first; among equals, row blocks that read the same (request, KV
   // head, kv chunk) sit next to each other so they run together and the
   // later ones find the chunk in L2.  (b, h, kv_lo, row0) identifies an item,
   // so the order is total.
-  std::sort(items.begin(), items.end(), [](const Tmp& a, const Tmp& b) {
+  if (!stream) std::sort(items.begin(), items.end(), [](const Tmp& a, const Tmp& b) {
       if (a.cost != b.cost) return a.cost > b.cost;
       if (a.it.b != b.it.b) return a.it.b < b.it.b;
       if (a.it.h != b.it.h) return a.it.h < b.it.h;
@@ -373,8 +455,7 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   // longest-first list is dealt onto the CTAs by LPT (each item to the
   // least-loaded CTA, with a per-item overhead of one key tile), chain c's
   // first item is put at index c and the rest follow, linked through next.
-  int64_t n_ctas = 0;
-  if (kernel_is_tc(kernel) && !items.empty()) {
+  if (!stream && kernel_is_tc(kernel) && !items.empty()) {
     n_ctas = std::min<int64_t>((int64_t)items.size(), num_sms);
     if ((int64_t)items.size() <= n_ctas) {
       // one item per CTA: item c is chain c
