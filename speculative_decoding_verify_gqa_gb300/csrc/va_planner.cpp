@@ -209,13 +209,22 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     *cu = equal || n * chunk < u.kv_end ? ceil_div(ceil_div(u.kv_end, n), TK) * TK : chunk;
     return ceil_div(u.kv_end, *cu);
   };
+  // Latency regime (tcgen05, at most four key tiles of K / V per SM: the
+  // verify steps of one or a few requests): spreading the keys over every SM
+  // in the shortest chunks costs more than it gains -- each CTA's set-up and
+  // epilogue, the later start of CTAs on SMs the previous kernel still holds,
+  // a merge over more partials.  On GB300 the Llama-3-8B tree verify step
+  // measured 10.7 us with 96 CTAs against 11.6-12.2 us with 136 and 11.3 us
+  // with 72, so there the candidates aim at two thirds of the SMs.
+  const bool latency = kernel_is_tc(kernel) && W * key_bytes <= 4LL * 64 * 1024 * num_sms;
+  const int64_t cand_slots = latency ? std::max<int64_t>(1, 2 * (int64_t)num_sms / 3) : slots;
   int64_t chunk;
   double best_lpt = -1.0;  // the chosen split candidate's estimated finish
   bool equal = true;
   if (o.target_ctas > 0) {
     chunk = chunk_for(std::min<int64_t>(o.target_ctas, kMaxTargetPerSm * num_sms));
   } else {
-    chunk = chunk_for(slots);
+    chunk = chunk_for(cand_slots);
     double best = -1.0;
     std::vector<int64_t> costs;
     // candidates: 1-4 waves of CTA slots, equal or full-plus-remainder cuts;
@@ -240,13 +249,13 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     };
     for (int cand = 0; cand < 8; ++cand) {
       const int waves = 1 + (cand >> 1);
-      const int64_t target = std::min<int64_t>(waves * slots, kMaxTargetPerSm * num_sms);
+      const int64_t target = std::min<int64_t>(waves * cand_slots, kMaxTargetPerSm * num_sms);
       add(chunk_for(target), (cand & 1) == 0);
     }
     const int64_t unit_heads = std::max<int64_t>(1, (int64_t)units.size() * num_kv_heads);
-    if (kernel_is_tc(kernel) && unit_heads < slots) {
+    if (kernel_is_tc(kernel) && unit_heads < cand_slots) {
       for (int64_t k = 1; k <= 6; ++k) {
-        const int64_t n0 = (k * slots + unit_heads / 2) / unit_heads;
+        const int64_t n0 = (k * cand_slots + unit_heads / 2) / unit_heads;
         for (int64_t n = std::max<int64_t>(1, n0 - 1); n <= std::min<int64_t>(32, n0 + 1); ++n)
           add(std::max<int64_t>(min_chunk, ceil_div(ceil_div(longest, n), TK) * TK), true);
       }
@@ -265,16 +274,16 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
           for (int h = 0; h < num_kv_heads; ++h) costs.push_back(cost);
         }
       }
-      // longest-first onto the least-loaded slot: the first `slots` items
+      // longest-first onto the least-loaded slot: the first `cand_slots` items
       // each get an empty slot, so with no more items than slots the finish
       // is the longest item; otherwise a min-heap of the slot loads takes the
       // rest
       int64_t finish = costs.empty() ? 0 : *std::max_element(costs.begin(), costs.end());
-      if ((int64_t)costs.size() > slots) {
+      if ((int64_t)costs.size() > cand_slots) {
         std::sort(costs.begin(), costs.end(), std::greater<int64_t>());
-        std::vector<int64_t> load(costs.begin(), costs.begin() + slots);
+        std::vector<int64_t> load(costs.begin(), costs.begin() + cand_slots);
         std::make_heap(load.begin(), load.end(), std::greater<int64_t>());
-        for (size_t k = (size_t)slots; k < costs.size(); ++k) {
+        for (size_t k = (size_t)cand_slots; k < costs.size(); ++k) {
           std::pop_heap(load.begin(), load.end(), std::greater<int64_t>());
           load.back() += costs[k];
           finish = std::max(finish, load.back());
