@@ -470,3 +470,47 @@ def test_accept_validation_without_device(va):
     # nothing to do
     assert lib.verify_accept_greedy(fake, 0, 0, 100, 100, fake, 0, fake, fake, *P, None, None, 152,
                                     fake, 8, None) == 0
+
+
+def test_latency_regime_aims_at_two_thirds_of_the_sms(va):
+    """Few key tiles per SM (the Llama-3-8B tree verify: 8 KV heads, 4113
+    keys): the split candidates aim at two thirds of the SMs, so the plan uses
+    at most that many CTAs (plus the drafts' own items) and every chain holds
+    one item; a plan forced to all SMs (target_ctas) uses more."""
+    wl = synthetic.make_workload("llama3_8b_tree_verify", with_values=False)
+    args = (wl.kv_indptr, wl.qo_indptr, wl.last_page_len, wl.mask_indptr, wl.h_q, wl.h_kv, wl.d,
+            wl.page_size)
+    auto = va.verify_attn_plan_host(*args, num_sms=152).header()
+    full = va.verify_attn_plan_host(*args, num_sms=152, target_ctas=152).header()
+    assert auto["n_ctas"] <= 2 * 152 // 3 + wl.h_kv
+    assert full["n_ctas"] > auto["n_ctas"]
+    # a large batch is not in that regime: every SM gets a chain
+    wl = synthetic.make_workload("codellama34b_chain_verify", with_values=False)
+    p = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len, None, wl.h_q,
+                                 wl.h_kv, wl.d, wl.page_size, num_sms=152).header()
+    assert p["n_ctas"] == 152
+
+
+def test_stream_cut_of_the_wide_tree(va):
+    """The two-Q-tile plan of the fp8 wide tree cuts the units' key tiles
+    into one equal run per CTA: 152 chains whose key tiles differ by at most
+    one, items that tile each unit's kv range (checked by the cover test),
+    and far fewer partial rows than cutting every unit seven ways."""
+    wl = synthetic.make_workload("wide_tree_fp8_verify", with_values=False)
+    plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
+                                    wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                    kv_dtype=wl.kv_dtype, num_sms=152)
+    hd = plan.header()
+    assert hd["kernel"] == 4 and hd["n_ctas"] == 152
+    t = dict(masked=True, prefix=wl.prefix_lens, L=wl.qo_lens, G=wl.group, h_kv=wl.h_kv)
+    _check_cover(va, t, plan)
+    items = plan.items()
+    tiles = []
+    for c in range(152):
+        i, n = c, 0
+        while i >= 0:
+            n += (int(items[i][5]) - int(items[i][4]) + 127) // 128
+            i = int(items[i][7])
+        tiles.append(n)
+    assert max(tiles) - min(tiles) <= 1
+    assert hd["part_rows"] < 64 * 256 * 4
