@@ -17,10 +17,13 @@ namespace {
 // splits are read CH at a time, LSE and partial output together, with a
 // running max (sums rescaled when it rises), so a row of up to CH splits costs
 // one round trip to memory.
-template <int D>
+// CH: splits whose loads are issued together, chosen from the plan's largest
+// split count -- enough to merge a row in one round trip, and no more, since
+// the loaded rows live in registers and the registers bound how many rows
+// are in flight.
+template <int D, int CH>
 __global__ void __launch_bounds__(128) verify_merge_kernel(const MergeParams p) {
   constexpr int V = D / 32;
-  constexpr int CH = 24;  // splits whose loads are issued together
   // After this library's split kernel in an append-and-run call, the merge
   // list (uploaded with the plan) and qo_indptr are read before the wait for
   // it: no kernel of the step writes them.  A call of its own waits first.
@@ -255,17 +258,22 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams
 
 }  // namespace
 
-cudaError_t launch_merge(const MergeParams& p, int head_dim, int n_merge, int block_rows,
-                         cudaStream_t stream) {
-  if (n_merge <= 0) return cudaSuccess;
+template <int D>
+static cudaError_t launch_merge_d(const MergeParams& p, int n_merge, int block_rows,
+                                  int max_nsplit, cudaStream_t stream) {
   dim3 grid(n_merge, (block_rows + 3) / 4);
   void* args[] = {const_cast<MergeParams*>(&p)};
-  if (head_dim == 128)
-    return launch_kernel(reinterpret_cast<const void*>(verify_merge_kernel<128>), grid,
-                         dim3(128), 0, stream, args, /*pdl=*/true);
-  if (head_dim == 64)
-    return launch_kernel(reinterpret_cast<const void*>(verify_merge_kernel<64>), grid,
-                         dim3(128), 0, stream, args, /*pdl=*/true);
+  const void* k = max_nsplit <= 4   ? reinterpret_cast<const void*>(verify_merge_kernel<D, 4>)
+                  : max_nsplit <= 8 ? reinterpret_cast<const void*>(verify_merge_kernel<D, 8>)
+                                    : reinterpret_cast<const void*>(verify_merge_kernel<D, 24>);
+  return launch_kernel(k, grid, dim3(128), 0, stream, args, /*pdl=*/true);
+}
+
+cudaError_t launch_merge(const MergeParams& p, int head_dim, int n_merge, int block_rows,
+                         int max_nsplit, cudaStream_t stream) {
+  if (n_merge <= 0) return cudaSuccess;
+  if (head_dim == 128) return launch_merge_d<128>(p, n_merge, block_rows, max_nsplit, stream);
+  if (head_dim == 64) return launch_merge_d<64>(p, n_merge, block_rows, max_nsplit, stream);
   return cudaErrorInvalidValue;
 }
 

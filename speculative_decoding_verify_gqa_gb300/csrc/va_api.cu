@@ -295,6 +295,7 @@ static int verify_attn_merge_impl(const int32_t* qo_indptr, int num_qo_heads, in
   m.group = hd->group;
   m.early_inputs = early;
   cudaError_t e = launch_merge(m, (int)hd->head_dim_v, hd->n_merge, hd->block_rows,
+                               (int)hd->max_nsplit,
                                static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
 }

@@ -9,7 +9,7 @@
 namespace va {
 
 constexpr uint32_t kPlanMagic = 0x31504156u;  // "VAP1"
-constexpr uint32_t kPlanVersion = 3;
+constexpr uint32_t kPlanVersion = 4;
 
 // Key tile of the partial kernels (keys per pipeline stage).  Split chunks are
 // cut on multiples of it, so every tile starts on a page boundary whenever
@@ -75,7 +75,7 @@ struct PlanHeader {
   int64_t flags;    // feature bits of the call the plan serves (0: none)
   int64_t n_ctas;   // persistent tcgen05 variants: CTAs (item chains); 0 otherwise
   int64_t head_dim_v;  // elements of a value row (v_cache, partials and out)
-  uint64_t reserved[1];
+  int64_t max_nsplit;  // largest split count of a merge item (0: no merges)
 };
 static_assert(sizeof(PlanHeader) == 184, "PlanHeader layout (read by the Python binding)");
 

@@ -162,7 +162,7 @@ struct TcMaps {
 cudaError_t launch_partial_tc(const PartialParams& p, const TcMaps& maps, bool kv_fp8,
                               int block_rows, int n_items, bool f8mma, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int head_dim, int n_merge, int block_rows,
-                         cudaStream_t stream);
+                         int max_nsplit, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 
 }  // namespace va

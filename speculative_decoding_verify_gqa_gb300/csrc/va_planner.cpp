@@ -529,6 +529,8 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   hd.h_kv = num_kv_heads;
   hd.head_dim = head_dim;
   hd.head_dim_v = dv;
+  hd.max_nsplit = 0;
+  for (const MergeItem& m : merges) hd.max_nsplit = std::max<int64_t>(hd.max_nsplit, m.nsplit);
   hd.page_size = page_size;
   hd.q_dtype = q_dtype;
   hd.kv_dtype = kv_dtype;
