@@ -370,11 +370,13 @@ class Bench:
         return res
 
     def e2e(self, steps):
-        """End to end through the public API: pinned host inputs copied in,
-        plan on the host, append, attention, out / LSE copied back, every step.
-        The step's inputs sit in one pinned staging buffer and go over in one
-        copy (each at a 256-byte offset, the device side carved the same way);
-        out and LSE share one device buffer and come back in one copy."""
+        """End to end through the public API: one verify_attn_step_host call
+        per step -- the step's inputs (q, the drafts' K/V, the index tables,
+        the mask) copied in from one pinned host buffer, the plan made on the
+        host from those tables, append and attention, out and LSE copied back
+        into one pinned host buffer, the stream synchronised.  Each array sits
+        at a 256-byte offset, the device side carved the same way; out and LSE
+        share one device buffer and come back in one copy."""
         torch, va, wl = self.torch, self.va, self.wl
 
         src = dict(q=self.q, k_new=self.k_new, v_new=self.v_new, kv_indptr=self.kv_indptr,
@@ -388,15 +390,9 @@ class Bench:
             total += (t.numel() * t.element_size() + 255) // 256 * 256
         stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
         stage_d = torch.empty(total, dtype=torch.uint8, device=self.dev)
-
-        def carve(buf, k):
-            t = src[k]
-            n = t.numel() * t.element_size()
-            return buf[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
-
         for k, t in src.items():
-            carve(stage_h, k).copy_(t.cpu())
-        d = {k: carve(stage_d, k) for k in src}
+            n = t.numel() * t.element_size()
+            stage_h[offs[k]:offs[k] + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
         n_out = self.out.numel() * self.out.element_size()
         n_lse = self.lse.numel() * self.lse.element_size()
         lse_off = (n_out + 255) // 256 * 256
@@ -405,29 +401,20 @@ class Bench:
         out_d = res_d[:n_out].view(self.out.dtype).view(self.out.shape)
         lse_d = res_d[lse_off:].view(self.lse.dtype).view(self.lse.shape)
         h2d, d2h = int(total), int(lse_off + n_lse)
-        hv = {k: carve(stage_h, k).numpy() for k in ("kv_indptr", "qo_indptr", "last_page_len")}
-        np_mask_indptr = carve(stage_h, "mask_indptr").numpy() if self.mask is not None else None
         ws = self.plan.workspace
         n_sms = self.plan.header()["num_sms"]
-        plan_buf = np.zeros(self.plan.host.nbytes, dtype=np.uint8)
+        plan_buf = torch.zeros(self.plan.host.nbytes, dtype=torch.uint8).pin_memory()
+        so = va.step_offsets(**offs)
 
         def one(i):
-            stage_d.copy_(stage_h, non_blocking=True)
-            plan = va.verify_attn_plan(hv["kv_indptr"], hv["qo_indptr"], hv["last_page_len"],
-                                       np_mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
-                                       kv_dtype=wl.kv_dtype, workspace=ws, device=self.dev,
-                                       num_sms=n_sms, plan_buffer=plan_buf, **self.plan_opts)
             kc, vc = self.pools[i % self.n_copies]
             # the inputs arrive by a host copy on the stream (not a kernel):
             # the early-reads promise holds
-            va.verify_attn_append_run(d["k_new"], d["v_new"], d["q"], kc, vc, d["kv_indptr"],
-                                      d["kv_indices"], d["last_page_len"], d["qo_indptr"],
-                                      d.get("mask"), d.get("mask_indptr"), plan,
-                                      sm_scale=wl.sm_scale, k_scale=wl.k_scale,
-                                      v_scale=wl.v_scale, out=out_d, lse=lse_d,
-                                      early_reads=True)
-            res_h.copy_(res_d, non_blocking=True)
-            torch.cuda.synchronize()
+            va.verify_attn_step_host(stage_h, stage_d, so, wl.batch, wl.h_q, wl.h_kv, wl.d,
+                                     wl.page_size, kc, vc, out_d, lse_d, res_h, ws, plan_buf,
+                                     kv_dtype=wl.kv_dtype, num_sms=n_sms, sm_scale=wl.sm_scale,
+                                     k_scale=wl.k_scale, v_scale=wl.v_scale, early_reads=True,
+                                     synchronize=True, **self.plan_opts)
 
         for i in range(5):
             one(i)
@@ -436,7 +423,8 @@ class Bench:
             one(i)
         dt_s = (time.perf_counter() - t0) / steps
         return dict(value=wl.total_qo / dt_s, unit="tokens/s", h2d_bytes_per_step=h2d,
-                    d2h_bytes_per_step=d2h, ms_per_step=dt_s * 1e3)
+                    d2h_bytes_per_step=d2h, ms_per_step=dt_s * 1e3,
+                    api="verify_attn_step_host (one call per step, host buffers)")
 
     def plan_us(self, n=50):
         va, wl = self.va, self.wl

@@ -450,6 +450,62 @@ int verify_attn_append_run(const void* k_new, const void* v_new,
                            const va_run_options_t* run_options, void* stream);
 
 /*
+ * One verification step from HOST buffers, in one call: the plan / run split
+ * of FlashInfer PR #286 (begin_forward plans from host copies of the index
+ * arrays) and vLLM PR #1679's step (cache the drafts, then attend), with the
+ * step's inputs and its result crossing between host and device inside the
+ * call.
+ *
+ * staging_h (host, pinned for an asynchronous copy) holds the step's inputs,
+ * each at its byte offset in `offsets`, with the layouts above: q, k_new,
+ * v_new (one row per query token, qo_indptr order), kv_indptr, kv_indices,
+ * last_page_len, qo_indptr, and mask / mask_indptr (offsets -1: no mask,
+ * the causal case).  staging_d (device, staging_bytes long) receives all of
+ * it in one host-to-device copy, and the kernels read the device copies at
+ * the same offsets, so every offset must keep the device pointer 16-byte
+ * aligned (multiples of 256 are simplest).  The plan is made on the host
+ * from the tables in staging_h first (verify_attn_plan_host into plan_h);
+ * then the inputs are copied and the plan's work list is uploaded into
+ * workspace_d (verify_attn_plan_upload).  Then
+ * verify_attn_append_run writes the drafts into k_cache / v_cache and
+ * computes out_d / lse_d (lse_d may be NULL).  Last, out_d (total_qo x
+ * num_qo_heads x value width, bf16) is copied into result_h at byte 0 and,
+ * with lse_d, the LSE (fp32) at byte offset round_up(out bytes, 256): one
+ * copy when lse_d sits at that offset from out_d, else two.  result_bytes
+ * must hold what is copied.  With synchronize != 0 the call returns after
+ * the stream has drained (result_h is then filled); otherwise result_h,
+ * staging_h and plan_h must stay untouched until the stream's work is done.
+ *
+ * q_dtype is bf16; the KV dtype, plan options, append options and run
+ * options are those of verify_attn_plan / verify_attn_append_run (the
+ * options' device pointers -- positions, q_position -- stay device
+ * pointers).  k_new / v_new are bf16 for a quantising append, else the KV
+ * dtype.  The host tables are checked against staging_bytes before they are
+ * read, and every array the tables size must lie inside it.
+ * Errors: those of verify_attn_plan and verify_attn_append_run;
+ * VA_ERR_INVALID_ARGUMENT for an offset or array outside staging_bytes or a
+ * short result_bytes; VA_ERR_CUDA for a failed copy or synchronisation.
+ * The step's own checks and the plan's come before anything is enqueued;
+ * a check of verify_attn_append_run that fails leaves the input copy and
+ * the plan upload enqueued (nothing else).
+ */
+typedef struct {
+  int64_t q, k_new, v_new;                                /* byte offsets into the staging buffers */
+  int64_t kv_indptr, kv_indices, last_page_len, qo_indptr;
+  int64_t mask, mask_indptr;                              /* -1 with no mask */
+} va_step_offsets_t;
+
+int verify_attn_step_host(const void* staging_h, void* staging_d, size_t staging_bytes,
+                          const va_step_offsets_t* offsets, int batch, int num_qo_heads,
+                          int num_kv_heads, int head_dim, int page_size, va_dtype kv_dtype,
+                          int num_sms, const va_plan_options_t* plan_options, void* plan_h,
+                          size_t plan_bytes, void* workspace_d, size_t workspace_bytes,
+                          const va_append_options_t* append_options, void* k_cache, void* v_cache,
+                          int num_pages, float sm_scale, float k_scale, float v_scale, void* out_d,
+                          float* lse_d, void* result_h, size_t result_bytes,
+                          const va_run_options_t* run_options, int synchronize, void* stream);
+
+/*
  * Greedy acceptance of draft trees: the step after verification, on the
  * target model's logits (FlashInfer issue #152: Medusa / EAGLE trees are
  * verified against the target model's outputs; its logits come from an LM

@@ -81,6 +81,20 @@ class AppendOptions(ctypes.Structure):
                 ("reserved", ctypes.c_int * 3)]
 
 
+class StepOffsets(ctypes.Structure):
+    """Byte offsets of a host step's arrays in its staging buffers (-1: absent)."""
+    _fields_ = [(n, ctypes.c_int64) for n in ("q", "k_new", "v_new", "kv_indptr", "kv_indices",
+                                              "last_page_len", "qo_indptr", "mask", "mask_indptr")]
+
+
+def step_offsets(**offsets) -> StepOffsets:
+    """A StepOffsets from keyword byte offsets; the mask fields default to -1."""
+    o = StepOffsets(mask=-1, mask_indptr=-1)
+    for k, v in offsets.items():
+        setattr(o, k, -1 if v is None else int(v))
+    return o
+
+
 MASK_QLEN, MASK_FULL = 0, 1
 LAYOUT_HND, LAYOUT_NHD = 0, 1
 _LAYOUTS = {"hnd": LAYOUT_HND, "nhd": LAYOUT_NHD, LAYOUT_HND: LAYOUT_HND, LAYOUT_NHD: LAYOUT_NHD}
@@ -134,6 +148,9 @@ def lib():
         "verify_attn_run_static_scratch": (i32, [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32,
                                                  f32, f32, f32, P, P, i32, P, P]),
         "verify_attn_static_scratch_status": (i32, [Pi, P]),
+        "verify_attn_step_host": (i32, [P, P, sz, P, i32, i32, i32, i32, i32, i32, i32, P, P, sz,
+                                        P, sz, P, P, P, i32, f32, f32, f32, P, P, P, sz, P, i32,
+                                        P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -608,6 +625,49 @@ def verify_attn_append_run(k_new, v_new, q, k_cache, v_cache, kv_indptr, kv_indi
         None if ro is None else ctypes.byref(ro), _stream(stream))
     _check("verify_attn_append_run", rc)
     return out, lse
+
+
+def _host_ptr(b) -> int:
+    """Host address of a CPU torch tensor or a numpy array."""
+    if isinstance(b, torch.Tensor):
+        if b.is_cuda or not b.is_contiguous():
+            raise ValueError("expected a contiguous host tensor")
+        return b.data_ptr()
+    return _hp_buf(b)
+
+
+def _nbytes(b) -> int:
+    return b.numel() * b.element_size() if isinstance(b, torch.Tensor) else b.nbytes
+
+
+def verify_attn_step_host(staging_h, staging_d, offsets, batch, num_qo_heads, num_kv_heads,
+                          head_dim, page_size, k_cache, v_cache, out, lse, result_h,
+                          workspace, plan_buffer, kv_dtype="bf16", num_sms=0, sm_scale=0.0,
+                          k_scale=1.0, v_scale=1.0, num_pages=None, append_options=None,
+                          early_reads=False, synchronize=True, stream=None, **options):
+    """One verification step from host buffers in one library call
+    (verify_attn_step_host): the pinned staging buffer `staging_h` (uint8,
+    the step's inputs at `offsets`, a StepOffsets or a dict) goes to
+    `staging_d` in one copy, the plan is made from its host tables into
+    `plan_buffer` (host, uint8) and `workspace`, the drafts are appended and
+    attended, and out (then the LSE at round_up(out bytes, 256)) comes back
+    into the pinned `result_h`.  With synchronize the call returns once
+    result_h is filled."""
+    if isinstance(offsets, dict):
+        offsets = step_offsets(**offsets)
+    if num_pages is None:
+        num_pages = k_cache.shape[0]
+    ro = _run_options(None, 0.0, 0.0, early_reads)
+    rc = lib().verify_attn_step_host(
+        _host_ptr(staging_h), _dp(staging_d), _nbytes(staging_h), ctypes.byref(offsets),
+        int(batch), int(num_qo_heads), int(num_kv_heads), int(head_dim), int(page_size),
+        _kv_code(kv_dtype), int(num_sms), ctypes.byref(_options(**options)),
+        _host_ptr(plan_buffer), _nbytes(plan_buffer), _dp(workspace), workspace.numel(),
+        None if append_options is None else ctypes.byref(append_options), _dp(k_cache),
+        _dp(v_cache), int(num_pages), float(sm_scale), float(k_scale), float(v_scale),
+        _dp(out), _dp(lse), _host_ptr(result_h), _nbytes(result_h),
+        None if ro is None else ctypes.byref(ro), int(bool(synchronize)), _stream(stream))
+    _check("verify_attn_step_host", rc)
 
 
 def verify_accept_greedy(logits, qo_indptr, draft_tokens, parents, workspace=None,

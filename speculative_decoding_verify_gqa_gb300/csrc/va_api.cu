@@ -747,6 +747,97 @@ int verify_attn_append_run(const void* k_new, const void* v_new,
                                 workspace_d, workspace_bytes, 1, stream);
 }
 
+// [off, off + bytes) lies inside a buffer of `size` bytes
+static bool in_buffer(int64_t off, int64_t bytes, size_t size) {
+  return off >= 0 && bytes >= 0 && (uint64_t)off <= size && (uint64_t)bytes <= size - (uint64_t)off;
+}
+
+int verify_attn_step_host(const void* staging_h, void* staging_d, size_t staging_bytes,
+                          const va_step_offsets_t* offsets, int batch, int num_qo_heads,
+                          int num_kv_heads, int head_dim, int page_size, va_dtype kv_dtype,
+                          int num_sms, const va_plan_options_t* plan_options, void* plan_h,
+                          size_t plan_bytes, void* workspace_d, size_t workspace_bytes,
+                          const va_append_options_t* append_options, void* k_cache, void* v_cache,
+                          int num_pages, float sm_scale, float k_scale, float v_scale, void* out_d,
+                          float* lse_d, void* result_h, size_t result_bytes,
+                          const va_run_options_t* run_options, int synchronize, void* stream) {
+  if (!staging_h || !staging_d || !offsets || !result_h || !out_d || batch < 0 ||
+      num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return VA_ERR_INVALID_ARGUMENT;
+  const va_step_offsets_t& o = *offsets;
+  const char* h = static_cast<const char*>(staging_h);
+  char* d = static_cast<char*>(staging_d);
+  const int64_t nb = (int64_t)batch;
+  const bool has_mask = o.mask >= 0 || o.mask_indptr >= 0;
+  // the tables the host reads, then the arrays they size
+  if (!in_buffer(o.qo_indptr, 4 * (nb + 1), staging_bytes) ||
+      !in_buffer(o.kv_indptr, 4 * (nb + 1), staging_bytes) ||
+      !in_buffer(o.last_page_len, 4 * nb, staging_bytes) ||
+      (has_mask && !in_buffer(o.mask_indptr, 4 * (nb + 1), staging_bytes)))
+    return VA_ERR_INVALID_ARGUMENT;
+  if ((o.qo_indptr | o.kv_indptr | o.last_page_len | (has_mask ? o.mask_indptr : 0)) & 3)
+    return VA_ERR_INVALID_ARGUMENT;
+  const int32_t* qo_h = reinterpret_cast<const int32_t*>(h + o.qo_indptr);
+  const int32_t* kv_h = reinterpret_cast<const int32_t*>(h + o.kv_indptr);
+  const int32_t* lpl_h = reinterpret_cast<const int32_t*>(h + o.last_page_len);
+  const int32_t* mi_h = has_mask ? reinterpret_cast<const int32_t*>(h + o.mask_indptr) : nullptr;
+  const int64_t total_qo = qo_h[batch], n_idx = kv_h[batch];
+  if (total_qo < 0 || n_idx < 0 || (has_mask && mi_h[batch] < 0)) return VA_ERR_INVALID_ARGUMENT;
+  const int dv = plan_options && plan_options->head_dim_v ? plan_options->head_dim_v : head_dim;
+  const bool quantize = append_options && append_options->quantize;
+  const int64_t es_kv = kv_dtype == VA_FP8_E4M3 ? 1 : 2, es_new = quantize ? 2 : es_kv;
+  const int64_t rows_q = total_qo * num_qo_heads, rows_kv = total_qo * num_kv_heads;
+  if (!in_buffer(o.q, rows_q * head_dim * 2, staging_bytes) ||
+      !in_buffer(o.k_new, rows_kv * head_dim * es_new, staging_bytes) ||
+      !in_buffer(o.v_new, rows_kv * dv * es_new, staging_bytes) ||
+      !in_buffer(o.kv_indices, 4 * n_idx, staging_bytes) ||
+      (has_mask && !in_buffer(o.mask, ((int64_t)mi_h[batch] + 7) / 8, staging_bytes)))
+    return VA_ERR_INVALID_ARGUMENT;
+  const int64_t out_bytes = rows_q * dv * 2, lse_off = (out_bytes + 255) / 256 * 256;
+  const int64_t res_need = lse_d ? lse_off + rows_q * 4 : out_bytes;
+  if ((uint64_t)res_need > result_bytes) return VA_ERR_INVALID_ARGUMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the host plan (no CUDA call) before anything is enqueued
+  size_t ws_need = 0;
+  int rc = verify_attn_plan_host(kv_h, qo_h, lpl_h, mi_h, batch, num_qo_heads, num_kv_heads,
+                                 head_dim, page_size, VA_BF16, kv_dtype, has_mask ? 1 : 0, num_sms,
+                                 plan_options, plan_h, plan_bytes, &ws_need);
+  if (rc) return rc;
+  if (!workspace_d || workspace_bytes < ws_need) return VA_ERR_WORKSPACE_TOO_SMALL;
+  if (staging_bytes > 0 &&
+      cudaMemcpyAsync(staging_d, staging_h, staging_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return VA_ERR_CUDA;
+  rc = verify_attn_plan_upload(plan_h, workspace_d, workspace_bytes, stream);
+  if (rc) return rc;
+  auto dev = [&](int64_t off) -> char* { return off >= 0 ? d + off : nullptr; };
+  rc = verify_attn_append_run(dev(o.k_new), dev(o.v_new), append_options, dev(o.q), k_cache, v_cache,
+                              reinterpret_cast<const int32_t*>(dev(o.kv_indptr)),
+                              reinterpret_cast<const int32_t*>(dev(o.kv_indices)),
+                              reinterpret_cast<const int32_t*>(dev(o.last_page_len)),
+                              reinterpret_cast<const int32_t*>(dev(o.qo_indptr)),
+                              has_mask ? reinterpret_cast<const uint8_t*>(dev(o.mask)) : nullptr,
+                              has_mask ? reinterpret_cast<const int32_t*>(dev(o.mask_indptr)) : nullptr,
+                              num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale, k_scale,
+                              v_scale, out_d, lse_d, num_pages, plan_h, workspace_d,
+                              workspace_bytes, run_options, stream);
+  if (rc) return rc;
+  char* res = static_cast<char*>(result_h);
+  if (lse_d && reinterpret_cast<char*>(lse_d) == static_cast<char*>(out_d) + lse_off) {
+    if (res_need > 0 &&
+        cudaMemcpyAsync(res, out_d, res_need, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return VA_ERR_CUDA;
+  } else {
+    if (out_bytes > 0 &&
+        cudaMemcpyAsync(res, out_d, out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return VA_ERR_CUDA;
+    if (lse_d && rows_q > 0 &&
+        cudaMemcpyAsync(res + lse_off, lse_d, rows_q * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return VA_ERR_CUDA;
+  }
+  if (synchronize && cudaStreamSynchronize(st) != cudaSuccess) return VA_ERR_CUDA;
+  return VA_OK;
+}
+
 // Chunks per logits row for the argmax kernel: about two CTAs per SM over
 // all rows, each chunk at least 4096 elements.
 static void accept_chunks(int64_t total_qo, int vocab, int num_sms, int* chunks, int64_t* elems) {

@@ -514,3 +514,39 @@ def test_stream_cut_of_the_wide_tree(va):
         tiles.append(n)
     assert max(tiles) - min(tiles) <= 1
     assert hd["part_rows"] < 64 * 256 * 4
+
+
+def test_step_host_validation_without_device(va):
+    """verify_attn_step_host checks its staging offsets, the arrays its host
+    tables size, and the result buffer before any CUDA call."""
+    lib = va.lib()
+    stage = np.zeros(8192, np.uint8)
+    i32 = stage.view(np.int32)
+    # batch 1: 5 query tokens, 2 pages, last page 3 slots; 4 q / 2 kv heads, d 64
+    i32[0:2] = [0, 5]          # qo_indptr at byte 0
+    i32[64:66] = [0, 2]        # kv_indptr at byte 256
+    i32[128] = 3               # last_page_len at byte 512
+    i32[192:194] = [0, 1]      # kv_indices at byte 768
+    base = dict(q=1024, k_new=3584, v_new=4864, kv_indptr=256, kv_indices=768,
+                last_page_len=512, qo_indptr=0)
+    fake = 1 << 20
+    res = np.zeros(4096, np.uint8)
+    plan = np.zeros(1 << 16, np.uint8)
+
+    def call(offs, staging_bytes=stage.nbytes, result_bytes=res.nbytes):
+        o = va.step_offsets(**offs)
+        return lib.verify_attn_step_host(stage.ctypes.data, fake, staging_bytes, ctypes.byref(o),
+                                         1, 4, 2, 64, 16, 0, 152, None, plan.ctypes.data,
+                                         plan.nbytes, fake, 1 << 20, None, fake, fake, 8, 0.0,
+                                         1.0, 1.0, fake, fake + 4096, res.ctypes.data,
+                                         result_bytes, None, 1, None)
+
+    assert call(dict(base, kv_indices=8190)) == -1               # indices past the buffer
+    assert call(dict(base, v_new=7000)) == -1                    # v_new needs 1280 bytes
+    assert call(dict(base), staging_bytes=4096) == -1            # arrays past staging_bytes
+    assert call(dict(base, kv_indptr=258)) == -1                 # misaligned table
+    assert call(dict(base, qo_indptr=-256)) == -1                # negative offset
+    assert call(dict(base), result_bytes=2559) == -1             # out + LSE need 2560 + 80
+    assert call(dict(base, mask=6144)) == -1                     # mask without mask_indptr
+    i32[1] = -5
+    assert call(dict(base)) == -1                                # negative total_qo
