@@ -1002,10 +1002,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
         // (once the tile is done) O are multiplied by it.  With bf16 caches
         // the scale-and-shift and the sums run two logits per instruction
         // (fp32x2), which leaves more issue slots to the MMA issuer sharing
-        // this warp's sub-partition; the fp8 variant measured slower that way
-        // and keeps scalar fp32.
-        float sums[4] = {0.f, 0.f, 0.f, 0.f};  // fp8
-        uint64_t sums2[2] = {0ull, 0ull};      // bf16: fp32x2 pairs
+        // this warp's sub-partition; the widened fp8 variant (converter warps
+        // on the same sub-partitions) measured slower that way and keeps
+        // scalar fp32.
+        float sums[4] = {0.f, 0.f, 0.f, 0.f};  // widened fp8
+        uint64_t sums2[2] = {0ull, 0ull};      // bf16, e4m3 MMAs: fp32x2 pairs
         float o_scale = 1.f;                   // product of this tile's rescale factors
 #pragma unroll 1
         for (int q = 0; q < C::KEYS / 32; ++q) {
@@ -1074,7 +1075,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float p0, p1;
-            if constexpr (FP8) {
+            if constexpr (WIDEN) {
               p0 = ex2(fmaf(__uint_as_float(raw[2 * i]), c, -base));
               p1 = ex2(fmaf(__uint_as_float(raw[2 * i + 1]), c, -base));
               sums[i & 3] += p0 + p1;
@@ -1103,7 +1104,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
             tmem_st16(s_addr + 32 * q, pk);
           }
         }
-        const float sum = FP8 ? (sums[0] + sums[1]) + (sums[2] + sums[3])
+        const float sum = WIDEN ? (sums[0] + sums[1]) + (sums[2] + sums[3])
                               : (f32x2_lo(sums2[0]) + f32x2_hi(sums2[0])) + (f32x2_lo(sums2[1]) + f32x2_hi(sums2[1]));
         l = l * o_scale + sum;
         // O holds P_0 V .. P_{j-1} V against the old reference: rescale it once
