@@ -1004,15 +1004,53 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
         // (fp32x2), which leaves more issue slots to the MMA issuer sharing
         // this warp's sub-partition; the widened fp8 variant (converter warps
         // on the same sub-partitions) measured slower that way and keeps
-        // scalar fp32.
+        // scalar fp32.  With e4m3 MMAs the reference max is settled for the
+        // whole tile first, in a pass of its own over S (read from tensor
+        // memory twice): no P chunk is rescaled after it is written.  That
+        // measured faster there (fp8 wide tree 198.0 -> 192.2 us) and slower
+        // for the 16-bit P of the other variants (prefill 222.3 -> 230.5 us).
+        auto mask_chunk = [&](uint32_t* raw, int q) {
+          if (!full) {
+            const uint32_t vw = vis_word(q);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) raw[i] = ((vw >> i) & 1u) ? raw[i] : __float_as_uint(-INFINITY);
+          }
+        };
+        float o_scale = 1.f;                   // product of this tile's rescale factors
+        if constexpr (F8MMA) {
+          float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+          for (int q = 0; q < C::KEYS / 32; ++q) {
+            uint32_t raw[32];
+            tmem_ld32(s_addr + q * 32, raw);
+            tmem_wait_ld();
+            mask_chunk(raw, q);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
+          }
+          const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * c;  // c > 0
+          if (mx > m_used + 8.f) {  // also when m_used = -inf and mx is finite
+            if (m_used == -INFINITY) {
+              o_scale = 0.f;  // nothing seen yet: l and O are 0
+              m_used = mx;
+            } else {
+              const int k = (int)ceilf((mx - m_used - 8.f) * 0.125f);  // >= 1
+              o_scale = k < 15 ? __int_as_float((127 - 8 * k) << 23) : 0.f;   // 2^-8k
+              m_used += 8.f * (float)k;
+            }
+          }
+        }
         float sums[4] = {0.f, 0.f, 0.f, 0.f};  // widened fp8
         uint64_t sums2[2] = {0ull, 0ull};      // bf16, e4m3 MMAs: fp32x2 pairs
-        float o_scale = 1.f;                   // product of this tile's rescale factors
 #pragma unroll 1
         for (int q = 0; q < C::KEYS / 32; ++q) {
           uint32_t raw[32];
           tmem_ld32(s_addr + q * 32, raw);
           tmem_wait_ld();
+          if constexpr (F8MMA) {
+            mask_chunk(raw, q);
+          } else {
           float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
           if (full) {
 #pragma unroll
@@ -1045,21 +1083,12 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
               // this tile's P chunks 0 .. q-1, already in tensor memory
               tmem_wait_st();
               for (int q2 = 0; q2 < q; ++q2) {
-                if constexpr (F8MMA) {
-                  uint32_t pk[8];
-                  tmem_ld8(s_addr + 32 * q2, pk);
-                  tmem_wait_ld();
+                uint32_t pk[16];
+                tmem_ld16(s_addr + 32 * q2, pk);
+                tmem_wait_ld();
 #pragma unroll
-                  for (int i = 0; i < 8; ++i) pk[i] = scale_e4m3x4(pk[i], a);
-                  tmem_st8(s_addr + 32 * q2, pk);
-                } else {
-                  uint32_t pk[16];
-                  tmem_ld16(s_addr + 32 * q2, pk);
-                  tmem_wait_ld();
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) pk[i] = FP8 ? scale_f16x2(pk[i], a) : scale_bf16x2(pk[i], a);
-                  tmem_st16(s_addr + 32 * q2, pk);
-                }
+                for (int i = 0; i < 16; ++i) pk[i] = FP8 ? scale_f16x2(pk[i], a) : scale_bf16x2(pk[i], a);
+                tmem_st16(s_addr + 32 * q2, pk);
               }
             }
 #pragma unroll
@@ -1067,6 +1096,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 2; ++i) sums2[i] = f32x2(f32x2_lo(sums2[i]) * a, f32x2_hi(sums2[i]) * a);
             o_scale *= a;
+          }
           }
           // P of these 32 logits into columns 32 q .. 32 q + 15
           const float base = m_used == -INFINITY ? 0.f : m_used;

@@ -118,16 +118,6 @@ __device__ __forceinline__ uint32_t e4m3x4_rn_satfinite(float a, float b, float 
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-// Four fp8-e4m3 codes (first in the low byte) times a (a power of two),
-// re-encoded (round to nearest even; exact down to e4m3's subnormal range).
-__device__ __forceinline__ uint32_t scale_e4m3x4(uint32_t v, float a) {
-  const uint32_t lo = e4m3x2_to_f16x2((uint16_t)(v & 0xffffu));
-  const uint32_t hi = e4m3x2_to_f16x2((uint16_t)(v >> 16));
-  const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-  const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-  return e4m3x4_rn_satfinite(f0.x * a, f0.y * a, f1.x * a, f1.y * a);
-}
-
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

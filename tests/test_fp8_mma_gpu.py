@@ -13,8 +13,11 @@ lazily raised reference (the row's maximum P lies in [1, 2^8]), so a key whose
 probability relative to the row maximum is p carries a quantisation error of
 at most 2^-4 p (three fraction bits, round to nearest) plus, below e4m3's
 normal range, one subnormal step, 2^-10 in the units where the row maximum
-is 1; a raise rescales P already written by an exact power of two and rounds
-once more.  Per element of the output:
+is 1.  The kernel settles a tile's reference before it writes any of the
+tile's P, so each P is rounded once; the bound below keeps a second
+subnormal step as margin (a variant that raised the reference chunk by
+chunk rescaled P already written and rounded it once more).  Per element of
+the output:
 
     |out - oracle| <= sum_j e_j |v_j| / sum_j p_j,
     e_j = 2^-4 p_j + min(p_j, 2^-9)
