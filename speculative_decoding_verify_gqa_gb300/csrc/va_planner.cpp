@@ -18,6 +18,7 @@
 #include <algorithm>
 #include <cstring>
 #include <functional>
+#include <map>
 #include <vector>
 
 #include "../../include/verify_attn.h"
@@ -226,7 +227,8 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   } else {
     chunk = chunk_for(cand_slots);
     double best = -1.0;
-    std::vector<int64_t> costs;
+    std::vector<std::pair<int64_t, int64_t>> groups;  // (item cost, items)
+    std::map<int64_t, int64_t> loads;                  // slot load -> slots
     // candidates: 1-4 waves of CTA slots, equal or full-plus-remainder cuts;
     // for the persistent tcgen05 variants (items dealt onto one chain per
     // SM), when the units alone would leave SMs idle, also the longest unit
@@ -263,33 +265,37 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
     for (const auto& cand : cands) {
       const int64_t c = cand.first;
       const bool eq = cand.second;
-      costs.clear();
+      // The candidate's items as (cost, count) groups: a unit's chunks are
+      // cu keys long but the last, and each runs on every KV head.
+      groups.clear();
       for (const Unit& u : units) {
         int64_t cu;
         const int64_t n = split_of(u, c, eq, &cu);
-        for (int64_t s = 0; s < n; ++s) {
-          const int64_t keys = std::min<int64_t>(cu, u.kv_end - s * cu);
-          const int64_t cost = fixed_bytes + keys * key_bytes +
-                               (n > 1 ? (int64_t)u.nrows * partial_bytes_per_row : 0);
-          for (int h = 0; h < num_kv_heads; ++h) costs.push_back(cost);
+        const int64_t extra = fixed_bytes + (n > 1 ? (int64_t)u.nrows * partial_bytes_per_row : 0);
+        if (n > 1) groups.push_back({extra + cu * key_bytes, (n - 1) * num_kv_heads});
+        groups.push_back({extra + (u.kv_end - (n - 1) * cu) * key_bytes, (int64_t)num_kv_heads});
+      }
+      std::sort(groups.begin(), groups.end(),
+                [](const std::pair<int64_t, int64_t>& a, const std::pair<int64_t, int64_t>& b) {
+                  return a.first > b.first;
+                });
+      // Longest first onto the least-loaded slot, a group at a time: the slot
+      // loads are kept as (load, number of slots) levels, and the items of a
+      // group fill the lowest level one slot each before the next level is
+      // reached -- the same loads as placing the items one by one.
+      loads.clear();
+      loads[0] = cand_slots;
+      for (const auto& gr : groups) {
+        int64_t cnt = gr.second;
+        while (cnt > 0) {
+          auto lo = loads.begin();
+          const int64_t level = lo->first, take = std::min(cnt, lo->second);
+          if ((lo->second -= take) == 0) loads.erase(lo);
+          loads[level + gr.first] += take;
+          cnt -= take;
         }
       }
-      // longest-first onto the least-loaded slot: the first `cand_slots` items
-      // each get an empty slot, so with no more items than slots the finish
-      // is the longest item; otherwise a min-heap of the slot loads takes the
-      // rest
-      int64_t finish = costs.empty() ? 0 : *std::max_element(costs.begin(), costs.end());
-      if ((int64_t)costs.size() > cand_slots) {
-        std::sort(costs.begin(), costs.end(), std::greater<int64_t>());
-        std::vector<int64_t> load(costs.begin(), costs.begin() + cand_slots);
-        std::make_heap(load.begin(), load.end(), std::greater<int64_t>());
-        for (size_t k = (size_t)cand_slots; k < costs.size(); ++k) {
-          std::pop_heap(load.begin(), load.end(), std::greater<int64_t>());
-          load.back() += costs[k];
-          finish = std::max(finish, load.back());
-          std::push_heap(load.begin(), load.end(), std::greater<int64_t>());
-        }
-      }
+      const int64_t finish = loads.rbegin()->first;
       if (best < 0 || (double)finish < best * 0.97) {
         best = (double)finish;
         chunk = c;
