@@ -114,3 +114,61 @@ def test_step_host_separate_lse_buffer_and_no_lse(va):
                              wl.page_size, dw.k_cache, dw.v_cache, out_d, None, res2, ws,
                              np.zeros(plan.host.nbytes, np.uint8), **kw)
     assert np.array_equal(res2.numpy().view(np.int16), ref_out.view(torch.int16).cpu().numpy().reshape(-1))
+
+
+def test_step_host_quantising_append_and_nhd(va):
+    """The step with append options: bf16 drafts quantised into an fp8 NHD
+    cache (plan option kv_layout=nhd, e4m3 MMAs off and on), against the
+    oracle over its own quantised cache, and the pool bit-equal to it."""
+    base = dict(batch=2, h_q=32, h_kv=8, d=128, prefix=("fixed", [700, 260]),
+                qo=("fixed", [40, 9]), mask="tree", seed=5, kv_layout="nhd")
+    wf = synthetic.make_custom(kv_dtype=synthetic.FP8, **base)
+    wb = synthetic.make_custom(**base)
+    kn, vn = wb.new_tokens()
+    kc, vc = oracle.build_cache(wf)
+    oracle.paged_kv_append_ex(kn, vn, wf.qo_indptr, wf.kv_indptr, wf.kv_indices,
+                              wf.last_page_len, wf.page_size, wf.num_pages, kc, vc,
+                              cache_fp8=True, quantize=True, k_scale=wf.k_scale,
+                              v_scale=wf.v_scale, kv_layout=1)
+    arrays = dict(q=wf.q.view(np.int16), k_new=kn.view(np.int16), v_new=vn.view(np.int16),
+                  kv_indptr=wf.kv_indptr, kv_indices=wf.kv_indices,
+                  last_page_len=wf.last_page_len, qo_indptr=wf.qo_indptr, mask=wf.mask,
+                  mask_indptr=wf.mask_indptr)
+    offs, total = {}, 0
+    for k, a in arrays.items():
+        offs[k] = total
+        total += (np.ascontiguousarray(a).nbytes + 255) // 256 * 256
+    stage_h = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    for k, a in arrays.items():
+        b = np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+        stage_h.numpy()[offs[k]:offs[k] + b.size] = b
+    stage_d = torch.empty_like(stage_h, device="cuda")
+    ao = va.AppendOptions()
+    ao.quantize, ao.k_scale, ao.v_scale, ao.kv_layout = 1, wf.k_scale, wf.v_scale, va.LAYOUT_NHD
+    n_out = wf.total_qo * wf.h_q * wf.dv * 2
+    lse_off = (n_out + 255) // 256 * 256
+    for q_fp8 in (False, True):
+        dw = DeviceWorkload(wf)   # the pool holds every token, the drafts still as fp8 codes
+        res_d = torch.empty(lse_off + wf.total_qo * wf.h_q * 4, dtype=torch.uint8, device="cuda")
+        res_h = torch.zeros_like(res_d, device="cpu").pin_memory()
+        out_d = res_d[:n_out].view(torch.bfloat16).view(wf.total_qo, wf.h_q, wf.dv)
+        lse_d = res_d[lse_off:].view(torch.float32).view(wf.total_qo, wf.h_q)
+        plan = dw.plan(q_fp8=q_fp8)
+        ws = torch.empty_like(plan.workspace)
+        va.verify_attn_step_host(stage_h, stage_d, offs, wf.batch, wf.h_q, wf.h_kv, wf.d,
+                                 wf.page_size, dw.k_cache, dw.v_cache, out_d, lse_d, res_h, ws,
+                                 np.zeros(plan.host.nbytes, np.uint8), kv_dtype=wf.kv_dtype,
+                                 sm_scale=wf.sm_scale, k_scale=wf.k_scale, v_scale=wf.v_scale,
+                                 append_options=ao, kv_layout="nhd", q_fp8=q_fp8)
+        raw = lambda t: t.view(torch.uint8).cpu().numpy()
+        assert np.array_equal(raw(dw.k_cache), kc) and np.array_equal(raw(dw.v_cache), vc)
+        hv = res_h.numpy()
+        out_h = torch.from_numpy(hv[:n_out].view(np.int16).copy()).view(torch.bfloat16)
+        lse_h = torch.from_numpy(hv[lse_off:].view(np.float32).copy())
+        if q_fp8:
+            from test_fp8_mma_gpu import check as check_e4m3
+            check_e4m3(wf, out_h.view(wf.total_qo, wf.h_q, wf.dv), lse_h.view(wf.total_qo, wf.h_q),
+                       caches=(kc, vc))
+        else:
+            compare(wf, out_h.view(wf.total_qo, wf.h_q, wf.dv), lse_h.view(wf.total_qo, wf.h_q),
+                    caches=(kc, vc))
