@@ -400,6 +400,14 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   const int64_t all_heads = (int64_t)units.size() * num_kv_heads;
   const bool draft_items =
       kernel_is_tc(kernel) && (o.draft_items == 1 || (o.draft_items == 0 && 2 * all_heads <= slots));
+  {
+    int64_t n_all = 0;  // an upper bound of the items (a draft item adds one per unit)
+    for (const Unit& u : units) {
+      int64_t cu;
+      n_all += (split_of(u, chunk, equal, &cu) + (draft_items ? 1 : 0)) * num_kv_heads;
+    }
+    items.reserve((size_t)n_all);
+  }
   for (const Unit& u : units) {
     int64_t cu;
     int64_t n = split_of(u, chunk, equal, &cu);
@@ -458,13 +466,28 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
   // head, kv chunk) sit next to each other so they run together and the
   // later ones find the chunk in L2.  (b, h, kv_lo, row0) identifies an item,
   // so the order is total.
-  if (!stream) std::sort(items.begin(), items.end(), [](const Tmp& a, const Tmp& b) {
-      if (a.cost != b.cost) return a.cost > b.cost;
-      if (a.it.b != b.it.b) return a.it.b < b.it.b;
-      if (a.it.h != b.it.h) return a.it.h < b.it.h;
-      if (a.it.kv_lo != b.it.kv_lo) return a.it.kv_lo < b.it.kv_lo;
-      return a.it.row0 < b.it.row0;
+  if (!stream) {
+    // sorted as 24-byte keys (cost descending, then b, h, kv_lo, row0, all
+    // non-negative here) and the items permuted once
+    struct Key {
+      uint64_t k0, k1, k2;
+      uint32_t idx;
+    };
+    std::vector<Key> keys(items.size());
+    for (size_t i = 0; i < items.size(); ++i) {
+      const WorkItem& w = items[i].it;
+      keys[i] = {~(uint64_t)items[i].cost, ((uint64_t)(uint32_t)w.b << 32) | (uint32_t)w.h,
+                 ((uint64_t)(uint32_t)w.kv_lo << 32) | (uint32_t)w.row0, (uint32_t)i};
+    }
+    std::sort(keys.begin(), keys.end(), [](const Key& a, const Key& b) {
+      if (a.k0 != b.k0) return a.k0 < b.k0;
+      if (a.k1 != b.k1) return a.k1 < b.k1;
+      return a.k2 < b.k2;
     });
+    std::vector<Tmp> sorted(items.size());
+    for (size_t i = 0; i < keys.size(); ++i) sorted[i] = items[keys[i].idx];
+    items.swap(sorted);
+  }
 
   // Persistent tcgen05 variants: one CTA per SM walks a chain of items.  The
   // longest-first list is dealt onto the CTAs by LPT (each item to the
@@ -476,22 +499,48 @@ int plan_host(const int32_t* kv_indptr, const int32_t* qo_indptr, const int32_t*
       // one item per CTA: item c is chain c
       for (auto& t : items) t.it.next = -1;
     } else {
-      // LPT: each item (longest first) to the least-loaded chain, kept in a
-      // min-heap of (load, chain); then the items are laid out chain by
-      // chain (a counting sort on the owner), chain c's first at index c
-      std::vector<std::pair<int64_t, int64_t>> load((size_t)n_ctas);
-      for (int64_t c = 0; c < n_ctas; ++c) load[(size_t)c] = {0, c};
-      auto later = std::greater<std::pair<int64_t, int64_t>>();
-      std::vector<int32_t> owner(items.size());
-      for (size_t i = 0; i < items.size(); ++i) {
-        std::pop_heap(load.begin(), load.end(), later);
-        auto& top = load.back();
-        owner[i] = (int32_t)top.second;
-        const WorkItem& w = items[i].it;
-        // key tiles plus one of overhead; a tile of two Q tiles costs 5/3 of one
-        const int64_t tiles = ceil_div(w.kv_hi - w.kv_lo, TK) + 1;
-        top.first += tiles * (w.nrows > kTcRowsPerTile ? 5 : 3);
-        std::push_heap(load.begin(), load.end(), later);
+      // LPT: each item (longest first) to the least-loaded chain, the
+      // lowest chain index among equal loads; then the items are laid out
+      // chain by chain (a counting sort on the owner), chain c's first at
+      // index c.  The chain loads are kept as levels (load -> its chains,
+      // ascending), and a run of items of equal increment is dealt a level
+      // at a time: the lowest level's chains take the next items in index
+      // order and move up together -- the same owners as dealing the items
+      // one by one from a min-heap of (load, chain).
+      // key tiles plus one of overhead; a tile of two Q tiles costs 5/3 of one
+      auto inc = [&](const WorkItem& w) -> int64_t {
+        return (ceil_div(w.kv_hi - w.kv_lo, TK) + 1) * (w.nrows > kTcRowsPerTile ? 5 : 3);
+      };
+      std::map<int64_t, std::vector<int32_t>> levels;
+      {
+        std::vector<int32_t>& all = levels[0];
+        all.resize((size_t)n_ctas);
+        for (int64_t c = 0; c < n_ctas; ++c) all[(size_t)c] = (int32_t)c;
+      }
+      std::vector<int32_t> owner(items.size()), moved, merged;
+      for (size_t i = 0; i < items.size();) {
+        const int64_t x = inc(items[i].it);
+        size_t run = 1;
+        while (i + run < items.size() && inc(items[i + run].it) == x) ++run;
+        while (run > 0) {
+          auto lo = levels.begin();
+          const int64_t level = lo->first;
+          std::vector<int32_t>& ids = lo->second;
+          const size_t take = std::min(run, ids.size());
+          for (size_t t = 0; t < take; ++t) owner[i++] = ids[t];
+          moved.assign(ids.begin(), ids.begin() + (std::ptrdiff_t)take);
+          if (take == ids.size()) levels.erase(lo);
+          else ids.erase(ids.begin(), ids.begin() + (std::ptrdiff_t)take);
+          std::vector<int32_t>& up = levels[level + x];
+          if (up.empty()) {
+            up.swap(moved);
+          } else {
+            merged.resize(up.size() + moved.size());
+            std::merge(up.begin(), up.end(), moved.begin(), moved.end(), merged.begin());
+            up.swap(merged);
+          }
+          run -= take;
+        }
       }
       // chain c: its first item at index c, the rest after all the firsts, in
       // chain order, each linked to the next
