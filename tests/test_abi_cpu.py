@@ -303,6 +303,59 @@ def test_tcgen05_plans_chain_every_item_once(va, name):
     assert max(loads) <= np.mean(loads) + longest + 256
 
 
+@pytest.mark.parametrize("name", ["codellama34b_chain_verify", "gqa_varlen_prefill", "rand"])
+def test_chain_dealing_is_longest_first_onto_the_least_loaded_chain(va, name):
+    """The chains of a persistent tcgen05 plan are the longest-first dealing
+    of its items: items ordered by cost ((hi - lo) (nrows + 16)) descending,
+    then (b, h, kv_lo, row0), each to the chain with the least load (key
+    tiles + 1, times 5 for a two-Q-tile item, 3 for one), the lowest chain
+    index among equal loads -- dealt here one item at a time from a heap."""
+    import heapq
+    if name == "rand":
+        rng = np.random.default_rng(3)
+        batch, G, hkv = 57, 4, 8
+        L = rng.integers(1, 120, batch)
+        kv = rng.integers(0, 5000, batch) + L
+        pages = (kv + 15) // 16
+        tabs = (np.concatenate([[0], np.cumsum(pages)]).astype(np.int32),
+                np.concatenate([[0], np.cumsum(L)]).astype(np.int32),
+                (kv - (pages - 1) * 16).astype(np.int32), None, hkv * G, hkv, 128, 16)
+        kvd = "bf16"
+    else:
+        wl = synthetic.make_workload(name, with_values=False)
+        tabs = (wl.kv_indptr, wl.qo_indptr, wl.last_page_len, wl.mask_indptr, wl.h_q, wl.h_kv,
+                wl.d, wl.page_size)
+        kvd = wl.kv_dtype
+    plan = va.verify_attn_plan_host(*tabs, kv_dtype=kvd, num_sms=152)
+    hd = plan.header()
+    assert hd["kernel"] in (3, 4)
+    it = plan.items()
+    n, nc, tk = len(it), hd["n_ctas"], hd["tile_keys"]
+    assert n > nc
+    chain = np.full(n, -1)
+    for c in range(nc):
+        i = c
+        while i >= 0:
+            chain[i] = c
+            i = int(it[i, 7])
+    order = sorted(range(n), key=lambda i: (-(int(it[i, 5]) - int(it[i, 4])) * (int(it[i, 3]) + 16),
+                                           int(it[i, 0]), int(it[i, 1]), int(it[i, 4]), int(it[i, 2])))
+    heap = [(0, c) for c in range(nc)]
+    for i in order:
+        load, c = heapq.heappop(heap)
+        assert chain[i] == c
+        tiles = -(-(int(it[i, 5]) - int(it[i, 4])) // tk) + 1
+        heapq.heappush(heap, (load + tiles * (5 if it[i, 3] > 128 else 3), c))
+    # and within a chain the items run in the dealing order
+    pos = {i: k for k, i in enumerate(order)}
+    for c in range(nc):
+        i, last = c, -1
+        while i >= 0:
+            assert pos[i] > last
+            last = pos[i]
+            i = int(it[i, 7])
+
+
 def test_warp_level_plans_have_no_chains(va):
     wl = synthetic.make_workload("llama3_8b_tree_verify", with_values=False)
     plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
