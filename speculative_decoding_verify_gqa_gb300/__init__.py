@@ -670,6 +670,56 @@ def verify_attn_step_host(staging_h, staging_d, offsets, batch, num_qo_heads, nu
     _check("verify_attn_step_host", rc)
 
 
+class HostStep:
+    """verify_attn_step_host with its arguments marshalled once: every
+    buffer of a step loop stays put (the staging and result buffers, out /
+    lse, the workspace, the plan buffer), so each call passes the same
+    converted arguments -- only the cache pair may change between calls."""
+
+    def __init__(self, staging_h, staging_d, offsets, batch, num_qo_heads, num_kv_heads,
+                 head_dim, page_size, k_cache, v_cache, out, lse, result_h, workspace,
+                 plan_buffer, kv_dtype="bf16", num_sms=0, sm_scale=0.0, k_scale=1.0,
+                 v_scale=1.0, num_pages=None, append_options=None, early_reads=False,
+                 synchronize=True, stream=None, **options):
+        if isinstance(offsets, dict):
+            offsets = step_offsets(**offsets)
+        if num_pages is None:
+            num_pages = k_cache.shape[0]
+        ro = _run_options(None, 0.0, 0.0, early_reads)
+        # the objects the arguments point into, kept alive with this call
+        self._keep = (staging_h, staging_d, offsets, out, lse, result_h, workspace, plan_buffer,
+                      append_options, ro, k_cache, v_cache)
+        V, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        self._fn = lib().verify_attn_step_host
+        self._args = [
+            V(_host_ptr(staging_h)), V(_dp(staging_d)), S(_nbytes(staging_h)), ctypes.byref(offsets),
+            I(int(batch)), I(int(num_qo_heads)), I(int(num_kv_heads)), I(int(head_dim)),
+            I(int(page_size)), I(_kv_code(kv_dtype)), I(int(num_sms)),
+            ctypes.byref(_options(**options)), V(_host_ptr(plan_buffer)), S(_nbytes(plan_buffer)),
+            V(_dp(workspace)), S(workspace.numel()),
+            None if append_options is None else ctypes.byref(append_options),
+            V(_dp(k_cache)), V(_dp(v_cache)), I(int(num_pages)), F(float(sm_scale)),
+            F(float(k_scale)), F(float(v_scale)), V(_dp(out)), V(_dp(lse)),
+            V(_host_ptr(result_h)), S(_nbytes(result_h)),
+            None if ro is None else ctypes.byref(ro), I(int(bool(synchronize))),
+            V(_stream(stream))]
+        self._caches = {}
+
+    def __call__(self, k_cache=None, v_cache=None):
+        """One step; k_cache / v_cache (both or neither) replace the pair the
+        call was prepared with."""
+        args = self._args
+        if k_cache is not None:
+            key = (k_cache.data_ptr(), v_cache.data_ptr())
+            args = self._caches.get(key)
+            if args is None:
+                args = list(self._args)
+                args[17], args[18] = ctypes.c_void_p(_dp(k_cache)), ctypes.c_void_p(_dp(v_cache))
+                self._caches[key] = args
+                self._keep = self._keep + (k_cache, v_cache)
+        _check("verify_attn_step_host", self._fn(*args))
+
+
 def verify_accept_greedy(logits, qo_indptr, draft_tokens, parents, workspace=None,
                          want_argmax=False, status=None, stream=None):
     """Greedy acceptance of draft trees (see include/verify_attn.h):

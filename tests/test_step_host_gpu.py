@@ -172,3 +172,33 @@ def test_step_host_quantising_append_and_nhd(va):
         else:
             compare(wf, out_h.view(wf.total_qo, wf.h_q, wf.dv), lse_h.view(wf.total_qo, wf.h_q),
                     caches=(kc, vc))
+
+
+def test_prepared_host_step_matches_the_plain_call(va):
+    """HostStep (the binding's call with its arguments marshalled once) gives
+    the bytes of verify_attn_step_host, also with the cache pair swapped."""
+    wl = synthetic.make_workload("llama3_8b_tree_verify")
+    dws = [DeviceWorkload(wl), DeviceWorkload(wl)]
+    stage_h, offs = _stage(wl)
+    stage_d = torch.empty_like(stage_h, device="cuda")
+    n_out = wl.total_qo * wl.h_q * wl.dv * 2
+    lse_off = (n_out + 255) // 256 * 256
+    res_d = torch.empty(lse_off + wl.total_qo * wl.h_q * 4, dtype=torch.uint8, device="cuda")
+    out_d = res_d[:n_out].view(torch.bfloat16).view(wl.total_qo, wl.h_q, wl.dv)
+    lse_d = res_d[lse_off:].view(torch.float32).view(wl.total_qo, wl.h_q)
+    plan = dws[0].plan()
+    ws = torch.empty_like(plan.workspace)
+    kw = dict(kv_dtype=wl.kv_dtype, num_sms=plan.header()["num_sms"], sm_scale=wl.sm_scale,
+              k_scale=wl.k_scale, v_scale=wl.v_scale, early_reads=True)
+    ref = torch.zeros_like(res_d, device="cpu").pin_memory()
+    va.verify_attn_step_host(stage_h, stage_d, offs, wl.batch, wl.h_q, wl.h_kv, wl.d,
+                             wl.page_size, dws[0].k_cache, dws[0].v_cache, out_d, lse_d, ref, ws,
+                             np.zeros(plan.host.nbytes, np.uint8), **kw)
+    res_h = torch.zeros_like(ref).pin_memory()
+    step = va.HostStep(stage_h, stage_d, offs, wl.batch, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                       dws[0].k_cache, dws[0].v_cache, out_d, lse_d, res_h, ws,
+                       np.zeros(plan.host.nbytes, np.uint8), **kw)
+    for dw in (dws[0], dws[1], dws[0]):
+        res_h.zero_()
+        step(dw.k_cache, dw.v_cache)
+        assert np.array_equal(res_h.numpy(), ref.numpy())
