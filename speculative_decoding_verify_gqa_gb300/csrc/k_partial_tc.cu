@@ -1002,12 +1002,10 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
         // that covers the chunk (the row's first visible chunk sets it to the
         // chunk max), so every P stays <= 2^8 and every rescale factor is an
         // exact power of two: the tile's P chunks written so far, the sums and
-        // (once the tile is done) O are multiplied by it.  With bf16 caches
-        // the scale-and-shift and the sums run two logits per instruction
-        // (fp32x2), which leaves more issue slots to the MMA issuer sharing
-        // this warp's sub-partition; the widened fp8 variant (converter warps
-        // on the same sub-partitions) measured slower that way and keeps
-        // scalar fp32.  With e4m3 MMAs the reference max is settled for the
+        // (once the tile is done) O are multiplied by it.  The scale-and-shift
+        // and the sums run two logits per instruction (fp32x2), which leaves
+        // more issue slots to the MMA issuer and the converter warps sharing
+        // the sub-partitions.  With e4m3 MMAs the reference max is settled for the
         // whole tile first, in a pass of its own over S (read from tensor
         // memory twice): no P chunk is rescaled after it is written.  That
         // measured faster there (fp8 wide tree 198.0 -> 192.2 us) and slower
@@ -1044,8 +1042,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
             }
           }
         }
-        float sums[4] = {0.f, 0.f, 0.f, 0.f};  // widened fp8
-        uint64_t sums2[2] = {0ull, 0ull};      // bf16, e4m3 MMAs: fp32x2 pairs
+        uint64_t sums2[2] = {0ull, 0ull};      // fp32x2 pairs
 #pragma unroll 1
         for (int q = 0; q < C::KEYS / 32; ++q) {
           uint32_t raw[32];
@@ -1095,8 +1092,6 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
               }
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) sums[i] *= a;
-#pragma unroll
             for (int i = 0; i < 2; ++i) sums2[i] = f32x2(f32x2_lo(sums2[i]) * a, f32x2_hi(sums2[i]) * a);
             o_scale *= a;
           }
@@ -1107,17 +1102,9 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            float p0, p1;
-            if constexpr (WIDEN) {
-              p0 = ex2(fmaf(__uint_as_float(raw[2 * i]), c, -base));
-              p1 = ex2(fmaf(__uint_as_float(raw[2 * i + 1]), c, -base));
-              sums[i & 3] += p0 + p1;
-            } else {
-              const uint64_t x = fma_f32x2(f32x2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])), cc, nb);
-              p0 = ex2(f32x2_lo(x));
-              p1 = ex2(f32x2_hi(x));
-              sums2[i & 1] = add_f32x2(sums2[i & 1], f32x2(p0, p1));
-            }
+            const uint64_t x = fma_f32x2(f32x2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])), cc, nb);
+            const float p0 = ex2(f32x2_lo(x)), p1 = ex2(f32x2_hi(x));
+            sums2[i & 1] = add_f32x2(sums2[i & 1], f32x2(p0, p1));
             if constexpr (F8MMA) {
               raw[2 * i] = __float_as_uint(p0);     // packed four to a column below
               raw[2 * i + 1] = __float_as_uint(p1);
@@ -1137,8 +1124,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
             tmem_st16(s_addr + 32 * q, pk);
           }
         }
-        const float sum = WIDEN ? (sums[0] + sums[1]) + (sums[2] + sums[3])
-                              : (f32x2_lo(sums2[0]) + f32x2_hi(sums2[0])) + (f32x2_lo(sums2[1]) + f32x2_hi(sums2[1]));
+        const float sum = (f32x2_lo(sums2[0]) + f32x2_hi(sums2[0])) + (f32x2_lo(sums2[1]) + f32x2_hi(sums2[1]));
         l = l * o_scale + sum;
         // O holds P_0 V .. P_{j-1} V against the old reference: rescale it once
         // PV_{j-1} is done with it (with a single S buffer it completed before
