@@ -313,7 +313,8 @@ class Plan:
                     part_rows=int(i64[1]), chunk=int(i64[2]),
                     ws_bytes=int(np.frombuffer(h[136:144].tobytes(), dtype=np.uint64)[0]),
                     n_ctas=int(np.frombuffer(h[160:168].tobytes(), dtype=np.int64)[0]),
-                    head_dim_v=int(np.frombuffer(h[168:176].tobytes(), dtype=np.int64)[0]))
+                    head_dim_v=int(np.frombuffer(h[168:176].tobytes(), dtype=np.int64)[0]),
+                    max_nsplit=int(np.frombuffer(h[176:184].tobytes(), dtype=np.int64)[0]))
 
     def launches(self) -> int:
         n = ctypes.c_int(0)

@@ -356,6 +356,21 @@ def test_chain_dealing_is_longest_first_onto_the_least_loaded_chain(va, name):
             i = int(it[i, 7])
 
 
+@pytest.mark.parametrize("name", synthetic.WORKLOAD_ORDER)
+def test_plan_header_records_the_largest_split(va, name):
+    """The merge kernel sizes its load batch from the plan header's largest
+    split count: it must equal the largest nsplit of the merge list (0 with
+    no merges)."""
+    wl = synthetic.make_workload(name, with_values=False)
+    for opts in ({}, {"kernel": 3}, {"max_splits": 3}):
+        plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
+                                        wl.mask_indptr, wl.h_q, wl.h_kv, wl.d, wl.page_size,
+                                        kv_dtype=wl.kv_dtype, num_sms=152,
+                                        **(opts if wl.d == 128 or "kernel" not in opts else {}))
+        m = plan.merges()
+        assert plan.header()["max_nsplit"] == (int(m[:, 5].max()) if len(m) else 0)
+
+
 def test_warp_level_plans_have_no_chains(va):
     wl = synthetic.make_workload("llama3_8b_tree_verify", with_values=False)
     plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
