@@ -1051,50 +1051,50 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
           if constexpr (F8MMA) {
             mask_chunk(raw, q);
           } else {
-          float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          if (full) {
+            float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (full) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
-          } else {
-            const uint32_t vw = vis_word(q);
+              for (int i = 0; i < 16; ++i)
+                mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
+            } else {
+              const uint32_t vw = vis_word(q);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              raw[2 * i] = ((vw >> (2 * i)) & 1u) ? raw[2 * i] : __float_as_uint(-INFINITY);
-              raw[2 * i + 1] = ((vw >> (2 * i + 1)) & 1u) ? raw[2 * i + 1] : __float_as_uint(-INFINITY);
-              mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
-            }
-          }
-          const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * c;  // c > 0
-          const bool raise = mx > m_used + 8.f;  // also when m_used = -inf and mx is finite
-          if (__any_sync(0xffffffffu, raise)) {
-            float a = 1.f;
-            if (raise) {
-              if (m_used == -INFINITY) {
-                a = 0.f;  // nothing seen yet: every sum so far is 0
-                m_used = mx;
-              } else {
-                const int k = (int)ceilf((mx - m_used - 8.f) * 0.125f);  // >= 1
-                a = k < 15 ? __int_as_float((127 - 8 * k) << 23) : 0.f;   // 2^-8k
-                m_used += 8.f * (float)k;
+              for (int i = 0; i < 16; ++i) {
+                raw[2 * i] = ((vw >> (2 * i)) & 1u) ? raw[2 * i] : __float_as_uint(-INFINITY);
+                raw[2 * i + 1] = ((vw >> (2 * i + 1)) & 1u) ? raw[2 * i + 1] : __float_as_uint(-INFINITY);
+                mxs[i & 3] = fmax3(mxs[i & 3], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
               }
             }
-            if (q > 0) {
-              // this tile's P chunks 0 .. q-1, already in tensor memory
-              tmem_wait_st();
-              for (int q2 = 0; q2 < q; ++q2) {
-                uint32_t pk[16];
-                tmem_ld16(s_addr + 32 * q2, pk);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = FP8 ? scale_f16x2(pk[i], a) : scale_bf16x2(pk[i], a);
-                tmem_st16(s_addr + 32 * q2, pk);
+            const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * c;  // c > 0
+            const bool raise = mx > m_used + 8.f;  // also when m_used = -inf and mx is finite
+            if (__any_sync(0xffffffffu, raise)) {
+              float a = 1.f;
+              if (raise) {
+                if (m_used == -INFINITY) {
+                  a = 0.f;  // nothing seen yet: every sum so far is 0
+                  m_used = mx;
+                } else {
+                  const int k = (int)ceilf((mx - m_used - 8.f) * 0.125f);  // >= 1
+                  a = k < 15 ? __int_as_float((127 - 8 * k) << 23) : 0.f;   // 2^-8k
+                  m_used += 8.f * (float)k;
+                }
               }
-            }
+              if (q > 0) {
+                // this tile's P chunks 0 .. q-1, already in tensor memory
+                tmem_wait_st();
+                for (int q2 = 0; q2 < q; ++q2) {
+                  uint32_t pk[16];
+                  tmem_ld16(s_addr + 32 * q2, pk);
+                  tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 2; ++i) sums2[i] = f32x2(f32x2_lo(sums2[i]) * a, f32x2_hi(sums2[i]) * a);
-            o_scale *= a;
-          }
+                  for (int i = 0; i < 16; ++i) pk[i] = FP8 ? scale_f16x2(pk[i], a) : scale_bf16x2(pk[i], a);
+                  tmem_st16(s_addr + 32 * q2, pk);
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < 2; ++i) sums2[i] = f32x2(f32x2_lo(sums2[i]) * a, f32x2_hi(sums2[i]) * a);
+              o_scale *= a;
+            }
           }
           // P of these 32 logits into columns 32 q .. 32 q + 15
           const float base = m_used == -INFINITY ? 0.f : m_used;
