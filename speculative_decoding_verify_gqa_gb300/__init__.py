@@ -674,8 +674,10 @@ def verify_attn_step_host(staging_h, staging_d, offsets, batch, num_qo_heads, nu
 class HostStep:
     """verify_attn_step_host with its arguments marshalled once: every
     buffer of a step loop stays put (the staging and result buffers, out /
-    lse, the workspace, the plan buffer), so each call passes the same
-    converted arguments -- only the cache pair may change between calls."""
+    lse, the workspace, the plan buffer) and so does the stream (the one
+    given, else torch's current stream when the object is made), so each
+    call passes the same converted arguments -- only the cache pair may
+    change between calls."""
 
     def __init__(self, staging_h, staging_d, offsets, batch, num_qo_heads, num_kv_heads,
                  head_dim, page_size, k_cache, v_cache, out, lse, result_h, workspace,
