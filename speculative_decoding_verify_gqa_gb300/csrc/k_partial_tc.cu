@@ -677,7 +677,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, NQ, F8MMA>::THREADS, 1)
           const int k0 = g.lo + j * C::KEYS;
           const uint8_t* raw = smem + C::OFF_RING + s * C::SLOT_BYTES;
           uint8_t* dst = smem + C::OFF_CONV + (v ? 2 : (tj & 1)) * C::OP_BYTES;
-#pragma unroll 4
+#pragma unroll  // all of a thread's chunks in flight at once (5-6 of them)
           for (int c = ct; c < C::KEYS * 8; c += NCT) {
             const int r = c >> 3, ch = c & 7;         // key row, 16-code group
             uint4 a = make_uint4(0u, 0u, 0u, 0u), bq = a;
