@@ -371,6 +371,102 @@ def test_plan_header_records_the_largest_split(va, name):
         assert plan.header()["max_nsplit"] == (int(m[:, 5].max()) if len(m) else 0)
 
 
+def _model_chunk(kvp, qop, lpl, has_mask, h_q, h_kv, d, page, fp8, num_sms, kernel):
+    """The split size the planner's cost model picks, restated item by item:
+    units of row blocks, candidate chunk sizes (1-4 waves of CTA slots, equal
+    or full-plus-remainder cuts, and for the tcgen05 variants the n-way cuts
+    of the longest unit), each scored by placing every item longest-first on
+    the least-loaded slot (a heap), the first clearly (3 %) better kept."""
+    import heapq
+    cdiv = lambda a, b: -(-a // b)
+    tc = kernel in (3, 4)
+    G = h_q // h_kv
+    bm = 64 if kernel == 1 else (256 if kernel == 4 else 128)
+    tk = 128 if tc else 64
+    units = []
+    for b in range(len(qop) - 1):
+        npg, L = int(kvp[b + 1] - kvp[b]), int(qop[b + 1] - qop[b])
+        kv = (npg - 1) * page + int(lpl[b]) if npg > 0 else 0
+        prefix = kv - L
+        for row0 in range(0, G * L, bm):
+            nrows = min(bm, G * L - row0)
+            units.append((nrows, prefix + L if has_mask else prefix + (row0 + nrows - 1) // G + 1))
+    W = sum(k for _, k in units) * h_kv
+    slots = num_sms * ((1 if fp8 else 2) if kernel == 3 else (2 if kernel == 1 else 1))
+    key_bytes = 2 * d * (1 if fp8 else 2)
+    fixed = 64 * 1024 if tc else 48 * 1024
+    min_chunk = 2 * tk
+    chunk_for = lambda t: max(min_chunk, cdiv(cdiv(W, max(t, 1)), tk) * tk)
+    latency = tc and W * key_bytes <= 4 * 64 * 1024 * num_sms
+    cand_slots = max(1, 2 * num_sms // 3) if latency else slots
+    longest = max(k for _, k in units)
+    whole = max(min_chunk, cdiv(longest, tk) * tk)
+    cands = []
+
+    def add(c, eq):
+        if c >= whole:
+            c, eq = whole, True
+        if (c, eq) not in cands:
+            cands.append((c, eq))
+    for cand in range(8):
+        add(chunk_for(min((1 + (cand >> 1)) * cand_slots, 4 * num_sms)), cand % 2 == 0)
+    unit_heads = max(1, len(units) * h_kv)
+    if tc and unit_heads < cand_slots:
+        for k in range(1, 7):
+            n0 = (k * cand_slots + unit_heads // 2) // unit_heads
+            for n in range(max(1, n0 - 1), min(32, n0 + 1) + 1):
+                add(max(min_chunk, cdiv(cdiv(longest, n), tk) * tk), True)
+    best, chunk = -1.0, chunk_for(cand_slots)
+    for c, eq in cands:
+        costs = []
+        for nrows, kv_end in units:
+            n = max(cdiv(kv_end, c), 1)
+            cu = cdiv(cdiv(kv_end, n), tk) * tk if (eq or n * c < kv_end) else c
+            n = cdiv(kv_end, cu)
+            for s_ in range(n):
+                keys = min(cu, kv_end - s_ * cu)
+                costs += [fixed + keys * key_bytes + (nrows * 4 * d if n > 1 else 0)] * h_kv
+        costs.sort(reverse=True)
+        loads = costs[:cand_slots]
+        finish = max(costs)
+        heapq.heapify(loads)
+        for x in costs[cand_slots:]:
+            lo = heapq.heappop(loads) + x
+            finish = max(finish, lo)
+            heapq.heappush(loads, lo)
+        if best < 0 or finish < best * 0.97:
+            best, chunk = float(finish), c
+    return chunk
+
+
+@pytest.mark.parametrize("name", synthetic.WORKLOAD_ORDER + ["rand0", "rand1", "rand2"])
+def test_split_size_is_the_cost_models_choice(va, name):
+    """The plan's split size equals the cost model's choice restated above
+    (the planner scores candidates on grouped items; the choice must be the
+    same as placing every item one by one)."""
+    if name.startswith("rand"):
+        rng = np.random.default_rng(int(name[-1]) + 20)
+        batch = int(rng.integers(1, 40))
+        G, hkv = int(rng.choice([1, 4, 8])), int(rng.choice([2, 8]))
+        L = rng.integers(1, int(rng.choice([10, 80])), batch)
+        kv = rng.integers(0, int(rng.choice([600, 9000])), batch) + L
+        pages = (kv + 15) // 16
+        kvp = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+        qop = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+        lpl = (kv - (pages - 1) * 16).astype(np.int32)
+        tabs = (kvp, qop, lpl, None, hkv * G, hkv, 128, 16)
+        kvd = "fp8_e4m3" if name == "rand2" else "bf16"
+    else:
+        wl = synthetic.make_workload(name, with_values=False)
+        tabs = (wl.kv_indptr, wl.qo_indptr, wl.last_page_len, wl.mask_indptr, wl.h_q, wl.h_kv,
+                wl.d, wl.page_size)
+        kvd = wl.kv_dtype
+    plan = va.verify_attn_plan_host(*tabs, kv_dtype=kvd, num_sms=152)
+    hd = plan.header()
+    assert hd["chunk"] == _model_chunk(tabs[0], tabs[1], tabs[2], tabs[3] is not None, tabs[4],
+                                       tabs[5], tabs[6], tabs[7], kvd != "bf16", 152, hd["kernel"])
+
+
 def test_warp_level_plans_have_no_chains(va):
     wl = synthetic.make_workload("llama3_8b_tree_verify", with_values=False)
     plan = va.verify_attn_plan_host(wl.kv_indptr, wl.qo_indptr, wl.last_page_len,
